@@ -1,0 +1,34 @@
+"""Shared test set-up: repo root on sys.path, the `gpu` marker, C helper builds."""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _build_host_helpers():
+    import moe_inputs
+    import oracle
+    moe_inputs.build()
+    oracle.build()
+
+
+def read_golden(name):
+    """Rows of whitespace-separated fields from tests/golden/<name>, comments dropped."""
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                rows.append(line.split())
+    return rows
