@@ -1,0 +1,396 @@
+#!/usr/bin/env python3
+"""Benchmark of the sparse MoE FFN layer forward pass on GB300.
+
+One step = one whole moe_ffn_forward call (router -> grouping -> experts ->
+combine) over one batch of seeded synthetic tokens, weights resident in HBM.
+Prints ONE JSON line (rank 0).  Multi-GPU runs are independent replicas (the
+layer has no exchange step on one node): value = all ranks' tokens / the slowest
+rank's time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on this host's cores
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s; decode HBM GB/s and prefill TFLOP/s vs roofline (1×GB300)"
+DEFAULT_WORKLOAD = "qwen35_mini_moe_decode_t64"
+FLUSH_BYTES = 256 << 20          # > 2x the 129 MB L2
+PHASES = ("router_logits", "router_select", "permute", "gate_up", "down", "combine")
+PHASE_KERNEL_FILE = {"router_logits": "router.cu", "router_select": "router.cu",
+                     "permute": "permute.cu", "gate_up": "expert_decode.cu",
+                     "down": "expert_decode.cu", "combine": "combine.cu"}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU oracle baseline budget (0 disables)")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def kernel_hash(fname):
+    path = os.path.join(ROOT, "sparse_moe_ffn_route_gb300", "csrc", fname)
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def ncu_traffic(workload, phase):
+    """Per-launch DRAM bytes of `phase` from the committed ncu summary, if the kernel
+    source is unchanged since the capture (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p)).get(workload, {}).get(phase)
+    if not rec or rec.get("source_sha256_16") != kernel_hash(PHASE_KERNEL_FILE[phase]):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.samples = []
+        self._stop = threading.Event()
+        self._t = None
+
+    def _run(self):
+        try:
+            proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                     "--format=csv,noheader,nounits", "-lms", "50"],
+                                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        try:
+            for line in proc.stdout:
+                self.samples.append((time.perf_counter(), line.strip()))
+                if self._stop.is_set():
+                    break
+        finally:
+            proc.terminate()
+            proc.wait()
+
+    def start(self):
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
+        time.sleep(0.3)
+
+    def stop(self):
+        self._stop.set()
+        if self._t:
+            self._t.join(timeout=5)
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.samples:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                rows.append((ts, float(f[0]), float(f[1]), f))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        note = "samples inside the timed region"
+        if not inside and rows:
+            mid = 0.5 * (t0 + t1)
+            inside = sorted(rows, key=lambda r: abs(r[0] - mid))[:3]
+            note = "timed region shorter than the sampling period: nearest samples"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "nvidia-smi unavailable"}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i in range(4)
+                          if r[3][4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "samples": len(inside), "note": note}
+
+
+# ----------------------------------------------------------------------------- work counting
+def expert_bytes(spec):
+    """(gate+up bytes, down bytes) of one routed expert and of the shared expert."""
+    d, ff, sff = spec.d_model, spec.expert_ff, spec.shared_ff
+    if spec.mxfp4:
+        gu = 2 * ff * (d // 32) * 17 + 2 * ff * 2          # blocks + scales + bias
+        dn = d * (ff // 32) * 17 + d * 2
+    else:
+        gu = 2 * ff * d * 2
+        dn = d * ff * 2
+    return gu, dn, 2 * sff * d * 2, d * sff * 2
+
+
+def work(spec, ids):
+    """Algorithmic bytes and flops per phase for one step with routing `ids` [T, k]."""
+    import numpy as np
+    T, d, ff, sff, E, k = (spec.tokens, spec.d_model, spec.expert_ff, spec.shared_ff,
+                           spec.n_experts, spec.top_k)
+    distinct = int(len(np.unique(ids)))
+    gu, dn, sgu, sdn = expert_bytes(spec)
+    has_sh = sff > 0
+    S = T * (k + has_sh)
+    rows = T * k
+    x_bytes = T * d * 2
+    h_bytes = (rows * ff + T * sff) * 2
+    Y_bytes = S * d * 4
+    by = {
+        "router_logits": (E + has_sh) * d * 2 + x_bytes + T * (E + has_sh) * 4,
+        "router_select": T * (E + has_sh) * 4 + S * 8,
+        "permute": S * 4 * 3,
+        "gate_up": distinct * gu + (sgu if has_sh else 0) + x_bytes + h_bytes,
+        "down": distinct * dn + (sdn if has_sh else 0) + h_bytes + Y_bytes,
+        "combine": Y_bytes + S * 8 + T * d * 2,
+    }
+    fl = {
+        "router_logits": 2 * T * (E + has_sh) * d,
+        "gate_up": 2 * rows * 2 * ff * d + 2 * T * 2 * sff * d,
+        "down": 2 * rows * ff * d + 2 * T * sff * d,
+    }
+    per_unit = {"gate_up": gu, "down": dn}
+    return by, fl, distinct, per_unit
+
+
+# ----------------------------------------------------------------------------- arms
+def cpu_oracle_rate(spec, lay, seconds, tokens=None):
+    """tokens/s of the fp64 oracle over repeated passes on `tokens` (default: all)."""
+    import numpy as np
+    import oracle
+    g = oracle.gating_for(spec)
+    tok = np.arange(spec.tokens, dtype=np.int32) if tokens is None else tokens
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.forward(g, lay, tokens=tok)
+        n += len(tok)
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return n / el, n, el, oracle.num_threads()
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the fp64 CPU oracle timed on this host's cores, rank 0 only."""
+    if rank != 0:
+        return
+    import numpy as np
+    import moe_inputs as mi
+    import oracle
+    spec = mi.WORKLOADS[args.workload]
+    lay = mi.make_layer(spec)
+    g = oracle.gating_for(spec)
+    n_tok = min(spec.tokens, 16)
+    rng = np.random.default_rng(0)
+
+    def step():
+        tok = np.sort(rng.choice(spec.tokens, size=n_tok, replace=False)).astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.forward(g, lay, tokens=tok)
+        return time.perf_counter() - t0
+
+    for _ in range(args.warmup):
+        step()
+    times = [step() for _ in range(args.steps)]
+    ms = 1e3 * statistics.mean(times)
+    value = n_tok / (ms / 1e3)
+    cores = oracle.num_threads()
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(spec),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n_tok} random tokens of the {spec.tokens}-token batch per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def config_of(spec):
+    return {"workload": spec.name, "tokens": spec.tokens, "d_model": spec.d_model,
+            "n_experts": spec.n_experts, "top_k": spec.top_k, "expert_ff": spec.expert_ff,
+            "shared_ff": spec.shared_ff, "weights": "mxfp4" if spec.mxfp4 else "bf16",
+            "router_bias": spec.bias[0] if spec.bias else None,
+            "l2": "flushed between timed steps (256 MiB write, outside the step events)",
+            "parallelism": "replicas"}
+
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import moe_inputs as mi
+    import sparse_moe_ffn_route_gb300 as moe
+    from sparse_moe_ffn_route_gb300 import hostio
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    spec = mi.WORKLOADS[args.workload]
+    lay = mi.make_layer(spec)
+    x, router, experts, shared = hostio.upload(lay, dev)
+    if spec.family == "qwen":
+        cfg = moe.qwen_cfg(spec.d_model, spec.n_experts, spec.top_k, spec.expert_ff, spec.shared_ff)
+    else:
+        cfg = moe.gptoss_cfg(spec.d_model, spec.n_experts, spec.top_k, spec.expert_ff)
+    T = spec.tokens
+    ws = moe.workspace(cfg, T, dev)
+    y = torch.empty_like(x)
+    ids = torch.empty((T, spec.top_k), dtype=torch.int32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    moe.moe_ffn_forward(cfg, x, router, experts, shared, y=y, topk_ids=ids, ws=ws)
+    torch.cuda.synchronize()
+    st, bits = moe.moe_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} bits {bits:#x}")
+    by, fl, distinct, per_unit = work(spec, ids.cpu().numpy())
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        moe.moe_ffn_forward(cfg, x, router, experts, shared, y=y, ws=ws)
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    for e in evs:           # create the event handles outside the timed region
+        for ev in e:
+            ev.record()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank)
+    if rank == 0:
+        sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        moe.moe_set_phase_events(evs[i])
+        moe.moe_ffn_forward(cfg, x, router, experts, shared, y=y, ws=ws)
+    moe.moe_set_phase_events(None)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t1 = time.perf_counter()
+    sampler.stop()
+
+    step_ms = [e[0].elapsed_time(e[6]) for e in evs]
+    phase_ms = {p: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
+                for i, p in enumerate(PHASES)}
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * T / (ms / 1e3)
+
+    # end to end through the host-buffer entry point: pinned x in, pinned y out
+    e2e = None
+    if not args.no_e2e:
+        x_host = x.cpu().pin_memory()
+        y_host = torch.empty_like(x_host).pin_memory()
+        for _ in range(3):
+            moe.moe_ffn_forward_host(cfg, x_host, router, experts, shared, y_host=y_host, ws=ws)
+        n_e2e = max(10, min(args.steps, 200))
+        if world > 1:
+            torch.distributed.barrier()
+        te = []
+        for _ in range(n_e2e):
+            flush.zero_()
+            torch.cuda.synchronize()
+            a = time.perf_counter()
+            moe.moe_ffn_forward_host(cfg, x_host, router, experts, shared, y_host=y_host, ws=ws)
+            te.append(time.perf_counter() - a)
+        e_ms = 1e3 * statistics.mean(te)
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * T / (e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": y_host.numel() * 2,
+               "ms_per_step": e_ms}
+
+    if rank != 0:
+        return
+    hbm, tf, tf_sus, src = peaks()
+    dom = max(("gate_up", "down"), key=lambda p: phase_ms[p])
+    bound = "hbm"
+    achieved = by[dom] / (phase_ms[dom] / 1e3) / 1e9
+    roof = {"bound": bound, "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+            "frac": achieved / hbm, "peak_source": src,
+            "traffic": ncu_traffic(spec.name, dom),
+            "algorithmic_bytes_per_launch": by[dom],
+            "per_unit_bytes": per_unit[dom], "units_per_launch": distinct,
+            "tensor_tflops": fl.get(dom, 0) / (phase_ms[dom] / 1e3) / 1e12}
+    step_bytes = sum(by.values())
+    cpu = None
+    if args.cpu_seconds > 0:
+        rate, n, el, cores = cpu_oracle_rate(spec, lay, args.cpu_seconds,
+                                             tokens=np.arange(min(T, 64), dtype=np.int32))
+        cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{n} token-evaluations (first {min(T, 64)} tokens, repeated) "
+                         f"in {el:.1f} s"}
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_of(spec),
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 6 * args.steps,
+        "clocks": sampler.summary(t0, t1),
+        "phases_ms": phase_ms,
+        "step_hbm_gbs": step_bytes / (ms / 1e3) / 1e9,
+        "step_algorithmic_bytes": step_bytes,
+        "distinct_experts": distinct,
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    run_ours(args, rank, world, local_rank)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

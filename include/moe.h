@@ -1,0 +1,231 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) sparse Mixture-of-Experts FFN forward pass.
+ *
+ * One shared library, libmoe.so, computes the forward pass of a sparse MoE FFN
+ * layer on the GPU in two gating conventions:
+ *
+ *   Qwen3.5-MoE  ("qwen35moe - Forward-Pass Design (Pantheon port)", section
+ *                "Shared-expert MoE FFN (every layer)"; "qwen35moe CPU-reference
+ *                golden vectors", section "Kernel 4 - MoE routing"):
+ *       l = x W_r^T;  p = softmax(l);  ids = top-k(p) by selection sort with
+ *       first-seen tie-break;  w_j = p_ids_j / sum_j p_ids_j * expert_weights_scale;
+ *       moe = sum_j w_j * down_e(silu(gate_e x) * up_e x);
+ *       y = moe + sigmoid(gate_inp_shexp . x) * SwiGLU_shexp(x).
+ *
+ *   gpt-oss      ("Phase 19: MoE - gpt-oss-20b", section 2, Router and Experts;
+ *                section 3, MXFP4 dequantisation):
+ *       l = x W_r^T + b;  ids = top-k(l);  s = softmax(l[ids]);
+ *       gu = x W_gu,e^T + b_gu,e;  gate = gu[0::2], up = gu[1::2];
+ *       gate = min(gate, limit);  up = clamp(up, -limit, limit);
+ *       h = (up + 1) * gate * sigmoid(alpha * gate);
+ *       y = sum_j s_j * (h W_d,e^T + b_d,e),
+ *       with MXFP4 expert weights: per 32 inputs, 16 bytes of E2M1 codes (low
+ *       nibble = even input) and one E8M0 scale byte, value = code * 2^(scale-127).
+ *
+ * Conventions shared by every entry point
+ *   - Pointers named as device pointers must be device memory of the current
+ *     CUDA device; the caller owns every buffer.  The library allocates nothing
+ *     and never synchronises, except where an entry point says otherwise.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Work is enqueued on it in stream order; results are valid once the
+ *     stream has reached the end of the call's work.
+ *   - bf16 tensors are raw IEEE bfloat16 bit patterns (uint16), row-major.
+ *     Weight matrices are stored row = output, column = input (y = x W^T).
+ *   - Every tensor pointer must be 16-byte aligned (MOE_ERR_ALIGNMENT).
+ *   - Return value: MOE_OK (0) or a negative MOE_ERR_* code.  On error nothing
+ *     has been enqueued unless the code is MOE_ERR_CUDA (a launch failed).
+ *   - Scratch memory comes from the caller's workspace `ws` of at least
+ *     moe_workspace_bytes(cfg, T) bytes (16-byte aligned).  Calls that share a
+ *     workspace must be ordered on one stream.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------------ status codes */
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG (-1)   /* null pointer, T < 0, k > E, unknown enum value, ... */
+#define MOE_ERR_UNSUPPORTED (-2)   /* well-formed but outside what the kernels implement */
+#define MOE_ERR_WORKSPACE (-3)     /* ws_bytes < moe_workspace_bytes(cfg, T) */
+#define MOE_ERR_ALIGNMENT (-4)     /* a pointer is not 16-byte aligned */
+#define MOE_ERR_CUDA (-5)          /* a CUDA runtime call or kernel launch failed */
+#define MOE_ERR_DEVICE_CHECK (-6)  /* a kernel's bounds check fired (see moe_device_status) */
+#define MOE_ERR_TIMEOUT (-7)       /* a bounded device-side wait gave up */
+
+/* ------------------------------------------------------------------ configuration */
+enum {
+  MOE_GATING_SOFTMAX_TOPK_RENORM = 0, /* Qwen: softmax over E, top-k, renormalise x scale */
+  MOE_GATING_TOPK_SOFTMAX = 1         /* gpt-oss: top-k on logits, softmax over the k chosen */
+};
+enum {
+  MOE_ACT_SWIGLU = 0,     /* h = silu(gate) * up */
+  MOE_ACT_CLAMPED_GLU = 1 /* h = (clamp(up,+-limit) + 1) * min(gate,limit) * sigmoid(alpha*min(gate,limit)) */
+};
+enum {
+  MOE_WFMT_BF16 = 0,  /* bf16 expert weights */
+  MOE_WFMT_MXFP4 = 1  /* MXFP4 blocks u8 [rows, in/32, 16] + E8M0 scales u8 [rows, in/32] */
+};
+enum {
+  MOE_PATH_AUTO = 0,    /* pick by mean tokens per expert, T*k/E */
+  MOE_PATH_DECODE = 1,  /* weight-streaming grouped matvec (mma.sync) */
+  MOE_PATH_PREFILL = 2  /* grouped GEMM on tcgen05 / TMEM fed by TMA */
+};
+
+typedef struct {
+  int32_t d_model;              /* hidden size d; multiple of 32 */
+  int32_t n_experts;            /* E, 1..1024 */
+  int32_t top_k;                /* k, 1..min(E, 32) */
+  int32_t expert_ff;            /* routed expert FF width; multiple of 32 */
+  int32_t shared_ff;            /* shared expert FF width (multiple of 32); 0 = none */
+  int32_t gating;               /* MOE_GATING_* */
+  int32_t act;                  /* MOE_ACT_* of the routed experts (shared expert: SwiGLU) */
+  int32_t wfmt;                 /* MOE_WFMT_* of the routed experts (shared expert: bf16) */
+  int32_t interleaved_gate_up;  /* 1: one gate_up matrix, gate = even rows, up = odd rows
+                                   (required for MXFP4); 0: separate gate and up matrices */
+  int32_t norm_topk_prob;       /* softmax gating: 1 = divide chosen probabilities by their sum */
+  float expert_weights_scale;   /* multiplies every routing weight (Qwen 1.0; gpt-oss 1.0) */
+  float glu_limit;              /* clamped GLU limit (gpt-oss 7.0) */
+  float glu_alpha;              /* clamped GLU sigmoid slope (gpt-oss 1.702) */
+  int32_t path;                 /* MOE_PATH_* */
+  int32_t reserved[4];          /* must be zero */
+} moe_cfg_t;
+
+/* Router: w bf16 [E, d] (row e = expert e's logit weights); bias bf16 [E] or NULL. */
+typedef struct {
+  const void* w;
+  const void* bias;
+} moe_router_t;
+
+/* Routed experts (device pointers; unused members NULL).
+ *   bf16, separate:     gate bf16 [E, ff, d], up bf16 [E, ff, d]
+ *   bf16, interleaved:  gate_up bf16 [E, 2ff, d] (row 2f = gate f, row 2f+1 = up f)
+ *   MXFP4:              gate_up u8 [E, 2ff, d/32, 16] blocks, gate_up_scales u8 [E, 2ff, d/32]
+ *   gate_up_bias        bf16 [E, 2ff] in gate_up row order (interleaved layouts only) or NULL
+ *   down                bf16 [E, d, ff]  |  MXFP4 u8 [E, d, ff/32, 16], down_scales u8 [E, d, ff/32]
+ *   down_bias           bf16 [E, d] or NULL */
+typedef struct {
+  const void* gate;
+  const void* up;
+  const void* gate_up;
+  const void* gate_up_scales;
+  const void* gate_up_bias;
+  const void* down;
+  const void* down_scales;
+  const void* down_bias;
+} moe_experts_t;
+
+/* Shared expert, always on (bf16): gate/up [sff, d], down [d, sff], gate_inp [d]
+ * ("qwen35moe - Forward-Pass Design", section "Shared-expert MoE FFN": ffn_*_shexp
+ * and ffn_gate_inp_shexp). */
+typedef struct {
+  const void* gate;
+  const void* up;
+  const void* down;
+  const void* gate_inp;
+} moe_shared_t;
+
+/* ------------------------------------------------------------------ entry points */
+
+/* Bytes of workspace that moe_route / moe_ffn_forward / moe_ffn_forward_routed /
+ * moe_ffn_forward_host need for T tokens with this configuration.  Returns 0
+ * if cfg is invalid.  Pure host function, no CUDA calls. */
+size_t moe_workspace_bytes(const moe_cfg_t* cfg, int32_t T);
+
+/* Which expert path MOE_PATH_AUTO takes for T tokens (MOE_PATH_DECODE or
+ * MOE_PATH_PREFILL), or a negative MOE_ERR_* if cfg is invalid. */
+int moe_select_path(const moe_cfg_t* cfg, int32_t T);
+
+/* Router: logits, top-k selection and routing weights, and the shared-expert gate.
+ * Defined by: "qwen35moe CPU-reference golden vectors", Kernel 4 (softmax,
+ * selection sort with first-seen tie-break, norm_topk_prob x expert_weights_scale,
+ * sigmoid(gate_w . x)); "Phase 19: MoE - gpt-oss-20b", section 2 Router
+ * (logits + bias, top-k, softmax over the chosen k).
+ *   x         bf16 [T, d] device
+ *   router    router weights (device)
+ *   shared    NULL, or a shared expert whose gate_inp [d] is used for sgate
+ *   topk_ids  int32 [T, k] device, out: chosen experts in selection order
+ *             (descending logit; equal logits: lower index first)
+ *   topk_w    fp32 [T, k] device, out: routing weights
+ *   sgate     fp32 [T] device or NULL, out: sigmoid(gate_inp . x) (needs shared)
+ *   logits    fp32 [T, E] device or NULL, out: router logits (bias included)
+ * Logits accumulate bf16 x bf16 products in fp32; selection compares the fp32
+ * logits (softmax is strictly increasing, so the order equals the order of the
+ * probabilities).  T == 0 is a no-op. */
+int moe_route(const moe_cfg_t* cfg, const void* x, int32_t T, const moe_router_t* router,
+              const moe_shared_t* shared, int32_t* topk_ids, float* topk_w, float* sgate,
+              float* logits, void* ws, size_t ws_bytes, void* stream);
+
+/* Top-k selection and routing weights from caller-given fp32 logits [T, E]
+ * (device), with the same rule as moe_route.  Needs no workspace. */
+int moe_topk_from_logits(const moe_cfg_t* cfg, const float* logits, int32_t T, int32_t* topk_ids,
+                         float* topk_w, void* stream);
+
+/* The whole layer: route, group tokens by expert, run the selected experts (and
+ * the shared expert), combine.  y bf16 [T, d] device, out.  topk_ids [T, k] /
+ * topk_w [T, k] device or NULL: if given, the routing is also written there.
+ * Defined by the two conventions in the header comment above. */
+int moe_ffn_forward(const moe_cfg_t* cfg, const void* x, int32_t T, const moe_router_t* router,
+                    const moe_experts_t* experts, const moe_shared_t* shared, void* y,
+                    int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes, void* stream);
+
+/* The layer with caller-given routing (no router): topk_ids int32 [T, k] and
+ * topk_w fp32 [T, k] device; sgate fp32 [T] device, required when the layer has
+ * a shared expert.  Out-of-range ids are caught on the device: the call still
+ * returns MOE_OK and moe_device_status() then reports MOE_ERR_DEVICE_CHECK
+ * (rows with a bad id contribute nothing). */
+int moe_ffn_forward_routed(const moe_cfg_t* cfg, const void* x, int32_t T,
+                           const int32_t* topk_ids, const float* topk_w, const float* sgate,
+                           const moe_experts_t* experts, const moe_shared_t* shared, void* y,
+                           void* ws, size_t ws_bytes, void* stream);
+
+/* moe_ffn_forward from and to HOST memory: x_host bf16 [T, d] and y_host bf16
+ * [T, d] are host pointers (pinned memory gives full copy speed); the weights
+ * stay device pointers.  Copies x into the workspace, runs the layer, copies y
+ * back, and synchronises `stream` before returning, so y_host is ready on return. */
+int moe_ffn_forward_host(const moe_cfg_t* cfg, const void* x_host, int32_t T,
+                         const moe_router_t* router, const moe_experts_t* experts,
+                         const moe_shared_t* shared, void* y_host, void* ws, size_t ws_bytes,
+                         void* stream);
+
+/* Decode MXFP4 weights to bf16 with the decoder the expert kernels use on their
+ * weight-load path.  Defined by "Phase 19: MoE - gpt-oss-20b", section 3
+ * (value = fp4_lut[code] * 2^(e8m0 - 127)) and the section 2 tensor layout (16
+ * bytes per 32 inputs, low nibble = even input).
+ *   blocks  u8 [rows, n_in/32, 16] device;  scales u8 [rows, n_in/32] device
+ *   out     bf16 [rows, n_in] device
+ * E2M1 values times a power of two are exact in bf16, so the result is exact
+ * whenever it is a normal or subnormal bf16 (every scale byte 1..254 with
+ * |value| < 2^128); scale byte 255 gives NaN.  n_in must be a positive multiple
+ * of 32; rows >= 0. */
+int moe_mxfp4_to_bf16(const void* blocks, const void* scales, int64_t rows, int32_t n_in,
+                      void* out, void* stream);
+
+/* Phase timing for benchmarks.  While enabled (events != NULL), each later
+ * moe_ffn_forward / moe_ffn_forward_routed call made from this host thread
+ * records events[i] on its stream at the phase boundaries:
+ *   [0] start  [1] router logits done  [2] top-k done  [3] grouping done
+ *   [4] gate_up + activation done  [5] down done  [6] combine done
+ * (the routed entry point records [1] and [2] together after ingesting the
+ * routing).  `events` holds n_events >= 7 cudaEvent_t handles created by the
+ * caller; the array must stay valid while enabled.  events == NULL disables.
+ * No counterpart on the pages: measurement plumbing only. */
+int moe_set_phase_events(void* const* events, int32_t n_events);
+
+/* Synchronises `stream`, then returns MOE_OK, MOE_ERR_DEVICE_CHECK or
+ * MOE_ERR_TIMEOUT according to the device status word kept in `ws`, and clears
+ * it.  *detail (if not NULL) receives the raw status bits. */
+int moe_device_status(void* ws, void* stream, uint32_t* detail);
+
+/* Static text for a status code. */
+const char* moe_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H_ */

@@ -84,6 +84,9 @@ def _get_lib():
                                            ctypes.POINTER(OracleWeights), P, I, P, I, P, P, P, P,
                                            P, P]
             lib.oracle_forward.restype = I
+            lib.oracle_route.argtypes = [ctypes.POINTER(OracleCfg), ctypes.POINTER(OracleWeights),
+                                         P, I, P, I, P, P, P, P]
+            lib.oracle_route.restype = I
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = I
             _lib = lib
@@ -229,6 +232,25 @@ def forward(g: Gating, layer, tokens=None, forced_ids=None, x: Optional[np.ndarr
                                    _p(forced_ids), _p(y), _p(ids), _p(w), _p(sg), _p(lg))
     del keep
     return OracleResult(tokens, y, ids, w, sg, lg, nn)
+
+
+def route(g: Gating, layer, tokens=None, x: Optional[np.ndarray] = None) -> OracleResult:
+    """Routing only (logits, ids, weights, shared gate) for `tokens`; y is left empty."""
+    x = np.ascontiguousarray(layer.x if x is None else x, dtype=np.uint16)
+    T = x.shape[0]
+    tokens = np.arange(T, dtype=np.int32) if tokens is None else np.ascontiguousarray(
+        tokens, dtype=np.int32)
+    n = tokens.shape[0]
+    ids = np.zeros((n, g.top_k), np.int32)
+    w = np.zeros((n, g.top_k), np.float64)
+    sg = np.zeros(n, np.float64)
+    lg = np.zeros((n, g.n_experts), np.float64)
+    W, keep = weights_of(layer)
+    c = g.c()
+    nn = _get_lib().oracle_route(ctypes.byref(c), ctypes.byref(W), _p(x), T, _p(tokens), n,
+                                 _p(ids), _p(w), _p(sg), _p(lg))
+    del keep
+    return OracleResult(tokens, np.zeros((n, 0)), ids, w, sg, lg, nn)
 
 
 def num_threads() -> int:

@@ -210,6 +210,49 @@ static double activation(const oracle_cfg* c, double gate, double up) {
 
 /* ------------------------------------------------------------------ layer forward */
 
+/* Router of one token: logits x . W_r^T (+ b) [QW ffn_gate_inp; OSS Router], then
+   the routing.  Returns 1 if a logit is NaN. */
+static int router_one(const oracle_cfg* c, const oracle_weights* W, const double* xv, double* ll,
+                      const int32_t* forced, int32_t* ids, double* w) {
+  int d = c->d_model, E = c->n_experts, bad = 0;
+  for (int e = 0; e < E; ++e) {
+    double s = 0.0;
+    for (int i = 0; i < d; ++i) s += oracle_bf16(W->router_w[(size_t)e * d + i]) * xv[i];
+    if (W->router_b) s += oracle_bf16(W->router_b[e]);
+    ll[e] = s;
+    if (isnan(s)) bad = 1;
+  }
+  route_one(c, ll, forced, ids, w);
+  return bad;
+}
+
+/* Shared-expert gate sigmoid(gate_inp . x) [QW; GV Kernel 4]. */
+static double shared_gate(const oracle_cfg* c, const oracle_weights* W, const double* xv) {
+  double z = 0.0;
+  for (int i = 0; i < c->d_model; ++i) z += oracle_bf16(W->sh_gate_inp[i]) * xv[i];
+  return sigmoid(z);
+}
+
+/* Routing only, for the n_eval tokens in `tokens`: logits [n, E], ids [n, k],
+   w [n, k], sgate [n] (0 without shared expert).  Returns the NaN-logit count. */
+int oracle_route(const oracle_cfg* c, const oracle_weights* W, const uint16_t* x, int T,
+                 const int32_t* tokens, int n_eval, int32_t* ids, double* w, double* sgate,
+                 double* logits) {
+  int d = c->d_model, E = c->n_experts, k = c->top_k, n_nan = 0;
+  (void)T;
+#pragma omp parallel for schedule(dynamic, 16) reduction(+ : n_nan)
+  for (int n = 0; n < n_eval; ++n) {
+    double* xv = (double*)malloc(sizeof(double) * (size_t)d);
+    for (int i = 0; i < d; ++i) xv[i] = oracle_bf16(x[(size_t)tokens[n] * d + i]);
+    n_nan += router_one(c, W, xv, logits + (size_t)n * E, NULL, ids + (size_t)n * k,
+                        w + (size_t)n * k);
+    sgate[n] = c->shared_ff > 0 ? shared_gate(c, W, xv) : 0.0;
+    free(xv);
+  }
+  return n_nan;
+}
+
+
 /*
  * Forward pass for the n_eval tokens listed in `tokens` (indices into x [T, d]).
  * Outputs, row i for token tokens[i]:
@@ -235,16 +278,8 @@ int oracle_forward(const oracle_cfg* c, const oracle_weights* W, const uint16_t*
     double* ll = logits + (size_t)n * E;
     for (int i = 0; i < d; ++i) xv[i] = oracle_bf16(x[(size_t)t * d + i]);
 
-    /* router logits: x . W_r^T (+ b) [QW ffn_gate_inp; OSS Router] */
-    for (int e = 0; e < E; ++e) {
-      double s = 0.0;
-      for (int i = 0; i < d; ++i) s += oracle_bf16(W->router_w[(size_t)e * d + i]) * xv[i];
-      if (W->router_b) s += oracle_bf16(W->router_b[e]);
-      ll[e] = s;
-      if (isnan(s)) n_nan += 1;
-    }
-    route_one(c, ll, forced_ids ? forced_ids + (size_t)n * k : NULL, ids + (size_t)n * k,
-              w + (size_t)n * k);
+    n_nan += router_one(c, W, xv, ll, forced_ids ? forced_ids + (size_t)n * k : NULL,
+                        ids + (size_t)n * k, w + (size_t)n * k);
 
     /* routed experts: y = sum_j w_j * expert_{id_j}(x) [QW moe_out; OSS out] */
     for (int i = 0; i < d; ++i) yl[i] = 0.0;
@@ -259,9 +294,7 @@ int oracle_forward(const oracle_cfg* c, const oracle_weights* W, const uint16_t*
     /* shared expert: SwiGLU with the shexp weights, gated by sigmoid(gate_inp . x) [QW] */
     double sg = 0.0;
     if (sff > 0) {
-      double z = 0.0;
-      for (int i = 0; i < d; ++i) z += oracle_bf16(W->sh_gate_inp[i]) * xv[i];
-      sg = sigmoid(z);
+      sg = shared_gate(c, W, xv);
       for (int f = 0; f < sff; ++f) {
         double gsum = 0.0, usum = 0.0;
         for (int i = 0; i < d; ++i) {

@@ -1,0 +1,97 @@
+// Internal contract between the C-ABI host code (moe_abi.cu) and the kernel
+// translation units: parameter blocks and launcher declarations.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Bits of the device status word kept at the start of the workspace.
+enum : uint32_t {
+  STATUS_BAD_EXPERT_ID = 1u << 0,   // a routing id outside [0, E) was seen and skipped
+  STATUS_ROW_OVERFLOW = 1u << 1,    // a row index fell outside the permuted-row range
+  STATUS_TILE_OVERFLOW = 1u << 2,   // the prefill tile list would exceed its capacity
+  STATUS_TIMEOUT = 1u << 8,         // a bounded wait on an mbarrier gave up
+};
+
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+
+// Expert weights as the kernels see them.  Virtual expert index v in [0, E) is a
+// routed expert; v == E is the shared expert (bf16, separate gate/up, SwiGLU).
+struct ExpertParams {
+  // routed experts
+  const uint16_t* gate;       // bf16 [E, ff, d]            (separate layout)
+  const uint16_t* up;         // bf16 [E, ff, d]            (separate layout)
+  const uint8_t* gate_up;     // bf16 [E, 2ff, d] or MXFP4 blocks [E, 2ff, d/32, 16]
+  const uint8_t* gu_scales;   // MXFP4 [E, 2ff, d/32]
+  const uint16_t* gu_bias;    // bf16 [E, 2ff] or null
+  const uint8_t* down;        // bf16 [E, d, ff] or MXFP4 blocks [E, d, ff/32, 16]
+  const uint8_t* dn_scales;   // MXFP4 [E, d, ff/32]
+  const uint16_t* dn_bias;    // bf16 [E, d] or null
+  // shared expert
+  const uint16_t* sh_gate;    // bf16 [sff, d]
+  const uint16_t* sh_up;      // bf16 [sff, d]
+  const uint16_t* sh_down;    // bf16 [d, sff]
+  int E, d, ff, sff;
+  int act;                    // MOE_ACT_* of routed experts
+  float limit, alpha;
+};
+
+// Routing state in the workspace.  S = T * K slots, K = k + (shared ? 1 : 0);
+// slot t*K + j is token t's j-th expert (j == k: the shared expert, id E).
+struct RouteState {
+  int32_t* slot_expert;  // [S]
+  float* slot_w;         // [S]
+  int32_t* counts;       // [E1]
+  int32_t* offsets;      // [E1 + 1]  permuted-row ranges per virtual expert
+  int32_t* active;       // [E1]      virtual experts with rows, ascending
+  int32_t* n_active;     // [1]
+  int32_t* row2slot;     // [S]       permuted row -> slot
+  uint32_t* status;      // device status word
+};
+
+// ---------------------------------------------------------------- launchers
+// Each returns cudaSuccess or the launch error.
+
+// logits[t, e] (row stride ldl) = x_t . W_r[e] (+ bias[e]) for e < E, and
+// x_t . wsh for e == E when wsh != null.
+cudaError_t launch_router_logits(const uint16_t* x, int T, int d, const uint16_t* w_r,
+                                 const uint16_t* bias, const uint16_t* wsh, int E, float* logits,
+                                 int ldl, cudaStream_t s);
+
+// Top-k + routing weights from logits [T, ldl] (first E columns; column E is the
+// shared-gate logit when has_shared).  Writes any non-null output.
+cudaError_t launch_router_select(const float* logits, int ldl, int T, int E, int k,
+                                 int norm_topk_prob, float scale, int has_shared,
+                                 int32_t* ids_out, float* w_out, float* sgate_out,
+                                 int32_t* slot_expert, float* slot_w, cudaStream_t s);
+
+// Copy caller routing into the slot arrays (routed entry point).
+cudaError_t launch_ingest_routing(const int32_t* ids, const float* w, const float* sgate, int T,
+                                  int E, int k, int has_shared, int32_t* slot_expert,
+                                  float* slot_w, cudaStream_t s);
+
+// Histogram, offsets, active list and row -> slot map (one CTA).
+cudaError_t launch_permute(const RouteState& rs, int S, int E1, cudaStream_t s);
+
+// Decode path: weight-streaming grouped matvec on mma.sync.
+cudaError_t launch_gateup_decode(const ExpertParams& p, int wfmt, int interleaved,
+                                 const RouteState& rs, const uint16_t* x, int K, uint16_t* h,
+                                 int ldh, int E1, cudaStream_t s);
+cudaError_t launch_down_decode(const ExpertParams& p, int wfmt, const RouteState& rs,
+                               const uint16_t* h, int ldh, float* Y, int E1, cudaStream_t s);
+
+// MXFP4 [rows, n_in/32, 16] + scales -> bf16 [rows, n_in].
+cudaError_t launch_mxfp4_to_bf16(const uint8_t* blocks, const uint8_t* scales, long long rows,
+                                 int n_in, uint16_t* out, cudaStream_t s);
+
+// y[t] = sum_j slot_w[t,j] * Y[t*K + j]  (bf16 out).
+cudaError_t launch_combine(const float* Y, const float* slot_w, const int32_t* slot_expert, int T,
+                           int K, int d, int E1, uint16_t* y, cudaStream_t s);
+
+}  // namespace moe

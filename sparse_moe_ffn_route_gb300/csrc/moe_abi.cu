@@ -1,0 +1,408 @@
+// C-ABI host layer of libmoe.so: argument validation, workspace carving and the
+// stream-ordered launch sequence of each entry point (see include/moe.h).
+#include <cmath>
+#include <cstring>
+
+#include "internal.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kDecodeTokensPerExpert = 16;   // AUTO: decode path below this mean load
+
+size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Layout {
+  int K, E1, S, ldl, ldh;
+  size_t status, counts, offsets, active, n_active, slot_expert, slot_w, row2slot, logits, h, Y,
+      xstage, ystage, total;
+};
+
+int validate_cfg(const moe_cfg_t* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->d_model <= 0 || c->n_experts < 1 || c->n_experts > kMaxExperts || c->top_k < 1 ||
+      c->top_k > c->n_experts || c->top_k > kMaxTopK || c->expert_ff <= 0 || c->shared_ff < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (c->gating < 0 || c->gating > 1 || c->act < 0 || c->act > 1 || c->wfmt < 0 || c->wfmt > 1 ||
+      c->interleaved_gate_up < 0 || c->interleaved_gate_up > 1 || c->norm_topk_prob < 0 ||
+      c->norm_topk_prob > 1 || c->path < 0 || c->path > 2)
+    return MOE_ERR_INVALID_ARG;
+  for (int r : c->reserved)
+    if (r != 0) return MOE_ERR_INVALID_ARG;
+  if (!std::isfinite(c->expert_weights_scale) || !std::isfinite(c->glu_limit) ||
+      !std::isfinite(c->glu_alpha))
+    return MOE_ERR_INVALID_ARG;
+  if (c->d_model % 32 || c->expert_ff % 32 || c->shared_ff % 32) return MOE_ERR_UNSUPPORTED;
+  if (c->wfmt == MOE_WFMT_MXFP4 && (!c->interleaved_gate_up || c->shared_ff > 0))
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+bool make_layout(const moe_cfg_t* c, int T, Layout* L) {
+  const int has_sh = c->shared_ff > 0;
+  L->K = c->top_k + has_sh;
+  L->E1 = c->n_experts + has_sh;
+  const long long S = (long long)T * L->K;
+  if (T < 0 || S > (1LL << 30)) return false;
+  L->S = (int)S;
+  L->ldl = L->E1;
+  L->ldh = c->expert_ff > c->shared_ff ? c->expert_ff : c->shared_ff;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes);
+    return o;
+  };
+  const size_t Tz = (size_t)T, Sz = (size_t)S, d = (size_t)c->d_model;
+  L->status = take(64);
+  L->counts = take(4 * (size_t)L->E1);
+  L->offsets = take(4 * ((size_t)L->E1 + 1));
+  L->active = take(4 * (size_t)L->E1);
+  L->n_active = take(4);
+  L->slot_expert = take(4 * Sz);
+  L->slot_w = take(4 * Sz);
+  L->row2slot = take(4 * Sz);
+  L->logits = take(4 * Tz * (size_t)L->ldl);
+  L->h = take(2 * Sz * (size_t)L->ldh);
+  L->Y = take(4 * Sz * d);
+  L->xstage = take(2 * Tz * d);
+  L->ystage = take(2 * Tz * d);
+  L->total = off;
+  return true;
+}
+
+template <class T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+RouteState route_state(void* ws, const Layout& L) {
+  RouteState rs;
+  rs.slot_expert = at<int32_t>(ws, L.slot_expert);
+  rs.slot_w = at<float>(ws, L.slot_w);
+  rs.counts = at<int32_t>(ws, L.counts);
+  rs.offsets = at<int32_t>(ws, L.offsets);
+  rs.active = at<int32_t>(ws, L.active);
+  rs.n_active = at<int32_t>(ws, L.n_active);
+  rs.row2slot = at<int32_t>(ws, L.row2slot);
+  rs.status = at<uint32_t>(ws, L.status);
+  return rs;
+}
+
+int check_ws(const moe_cfg_t* c, int T, void* ws, size_t ws_bytes, Layout* L) {
+  if (!make_layout(c, T, L)) return MOE_ERR_UNSUPPORTED;
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(ws)) return MOE_ERR_ALIGNMENT;
+  if (ws_bytes < L->total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+// Pointer checks for the expert and shared weights of cfg.
+int check_experts(const moe_cfg_t* c, const moe_experts_t* e, const moe_shared_t* sh) {
+  if (!e) return MOE_ERR_INVALID_ARG;
+  const void* need[4] = {nullptr, nullptr, nullptr, nullptr};
+  if (c->wfmt == MOE_WFMT_MXFP4) {
+    need[0] = e->gate_up; need[1] = e->gate_up_scales; need[2] = e->down; need[3] = e->down_scales;
+    for (const void* p : need)
+      if (!p) return MOE_ERR_INVALID_ARG;
+  } else if (c->interleaved_gate_up) {
+    if (!e->gate_up || !e->down) return MOE_ERR_INVALID_ARG;
+  } else {
+    if (!e->gate || !e->up || !e->down) return MOE_ERR_INVALID_ARG;
+    if (e->gate_up_bias) return MOE_ERR_UNSUPPORTED;   // bias is defined in gate_up row order
+  }
+  const void* all[8] = {e->gate, e->up, e->gate_up, e->gate_up_scales, e->gate_up_bias, e->down,
+                        e->down_scales, e->down_bias};
+  for (const void* p : all)
+    if (p && !aligned16(p)) return MOE_ERR_ALIGNMENT;
+  if (c->shared_ff > 0) {
+    if (!sh || !sh->gate || !sh->up || !sh->down || !sh->gate_inp) return MOE_ERR_INVALID_ARG;
+    const void* s4[4] = {sh->gate, sh->up, sh->down, sh->gate_inp};
+    for (const void* p : s4)
+      if (!aligned16(p)) return MOE_ERR_ALIGNMENT;
+  }
+  return MOE_OK;
+}
+
+int check_router(const moe_router_t* r) {
+  if (!r || !r->w) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(r->w) || (r->bias && !aligned16(r->bias))) return MOE_ERR_ALIGNMENT;
+  return MOE_OK;
+}
+
+ExpertParams expert_params(const moe_cfg_t* c, const moe_experts_t* e, const moe_shared_t* sh) {
+  ExpertParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.gate = static_cast<const uint16_t*>(e->gate);
+  p.up = static_cast<const uint16_t*>(e->up);
+  p.gate_up = static_cast<const uint8_t*>(e->gate_up);
+  p.gu_scales = static_cast<const uint8_t*>(e->gate_up_scales);
+  p.gu_bias = static_cast<const uint16_t*>(e->gate_up_bias);
+  p.down = static_cast<const uint8_t*>(e->down);
+  p.dn_scales = static_cast<const uint8_t*>(e->down_scales);
+  p.dn_bias = static_cast<const uint16_t*>(e->down_bias);
+  if (c->shared_ff > 0) {
+    p.sh_gate = static_cast<const uint16_t*>(sh->gate);
+    p.sh_up = static_cast<const uint16_t*>(sh->up);
+    p.sh_down = static_cast<const uint16_t*>(sh->down);
+  }
+  p.E = c->n_experts;
+  p.d = c->d_model;
+  p.ff = c->expert_ff;
+  p.sff = c->shared_ff;
+  p.act = c->act;
+  p.limit = c->glu_limit;
+  p.alpha = c->glu_alpha;
+  return p;
+}
+
+int path_for(const moe_cfg_t* c, int T) {
+  if (c->path != MOE_PATH_AUTO) return c->path;
+  return (long long)T * c->top_k < (long long)kDecodeTokensPerExpert * c->n_experts
+             ? MOE_PATH_DECODE
+             : MOE_PATH_PREFILL;
+}
+
+// Caller-owned events recorded at phase boundaries (moe_set_phase_events).
+thread_local void* const* g_phase_events = nullptr;
+
+inline cudaError_t mark_phase(int i, cudaStream_t s) {
+  if (!g_phase_events) return cudaSuccess;
+  return cudaEventRecord(static_cast<cudaEvent_t>(g_phase_events[i]), s);
+}
+
+#define MOE_CUDA(call)                          \
+  do {                                          \
+    if ((call) != cudaSuccess) return MOE_ERR_CUDA; \
+  } while (0)
+
+// Router -> slots (the routing state in the workspace), optional caller copies.
+int run_router(const moe_cfg_t* c, const void* x, int T, const moe_router_t* r,
+               const moe_shared_t* sh, const Layout& L, void* ws, int32_t* ids_out, float* w_out,
+               float* sgate_out, float* logits_out, bool fill_slots, cudaStream_t s) {
+  const int has_sh = (c->shared_ff > 0 && sh) ? 1 : 0;
+  const uint16_t* wsh = has_sh ? static_cast<const uint16_t*>(sh->gate_inp) : nullptr;
+  // Logits go straight to the caller's buffer when it has the same row layout.
+  float* lg = at<float>(ws, L.logits);
+  int ldl = c->n_experts + has_sh;
+  if (logits_out && !has_sh) {
+    lg = logits_out;
+    ldl = c->n_experts;
+  }
+  if (fill_slots) MOE_CUDA(mark_phase(0, s));
+  MOE_CUDA(launch_router_logits(static_cast<const uint16_t*>(x), T, c->d_model,
+                                static_cast<const uint16_t*>(r->w),
+                                static_cast<const uint16_t*>(r->bias), wsh, c->n_experts, lg, ldl,
+                                s));
+  if (fill_slots) MOE_CUDA(mark_phase(1, s));
+  const int norm = c->gating == MOE_GATING_TOPK_SOFTMAX ? 1 : c->norm_topk_prob;
+  int32_t* slot_e = fill_slots ? at<int32_t>(ws, L.slot_expert) : nullptr;
+  float* slot_w = fill_slots ? at<float>(ws, L.slot_w) : nullptr;
+  MOE_CUDA(launch_router_select(lg, ldl, T, c->n_experts, c->top_k, norm,
+                                c->expert_weights_scale, has_sh, ids_out, w_out, sgate_out, slot_e,
+                                slot_w, s));
+  if (fill_slots) MOE_CUDA(mark_phase(2, s));
+  if (logits_out && has_sh)
+    MOE_CUDA(cudaMemcpy2DAsync(logits_out, sizeof(float) * c->n_experts, lg, sizeof(float) * ldl,
+                               sizeof(float) * c->n_experts, T, cudaMemcpyDeviceToDevice, s));
+  return MOE_OK;
+}
+
+// Permute, experts, combine.  The slots must already hold the routing.
+int run_experts(const moe_cfg_t* c, const void* x, int T, const moe_experts_t* e,
+                const moe_shared_t* sh, void* y, const Layout& L, void* ws, cudaStream_t s) {
+  const RouteState rs = route_state(ws, L);
+  const ExpertParams p = expert_params(c, e, sh);
+  MOE_CUDA(launch_permute(rs, L.S, L.E1, s));
+  MOE_CUDA(mark_phase(3, s));
+  uint16_t* h = at<uint16_t>(ws, L.h);
+  float* Y = at<float>(ws, L.Y);
+  // Both paths run the weight-streaming kernels for now; the grouped-GEMM
+  // kernels take over the prefill path as they land.
+  (void)path_for(c, T);
+  MOE_CUDA(launch_gateup_decode(p, c->wfmt, c->interleaved_gate_up, rs,
+                                static_cast<const uint16_t*>(x), L.K, h, L.ldh, L.E1, s));
+  MOE_CUDA(mark_phase(4, s));
+  MOE_CUDA(launch_down_decode(p, c->wfmt, rs, h, L.ldh, Y, L.E1, s));
+  MOE_CUDA(mark_phase(5, s));
+  MOE_CUDA(launch_combine(Y, rs.slot_w, rs.slot_expert, T, L.K, c->d_model, L.E1,
+                          static_cast<uint16_t*>(y), s));
+  MOE_CUDA(mark_phase(6, s));
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_workspace_bytes(const moe_cfg_t* cfg, int32_t T) {
+  if (validate_cfg(cfg) != MOE_OK || T < 0) return 0;
+  Layout L;
+  if (!make_layout(cfg, T, &L)) return 0;
+  return L.total;
+}
+
+int moe_select_path(const moe_cfg_t* cfg, int32_t T) {
+  const int st = validate_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  return path_for(cfg, T);
+}
+
+int moe_route(const moe_cfg_t* cfg, const void* x, int32_t T, const moe_router_t* router,
+              const moe_shared_t* shared, int32_t* topk_ids, float* topk_w, float* sgate,
+              float* logits, void* ws, size_t ws_bytes, void* stream) {
+  int st = validate_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (T < 0 || !x || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if ((st = check_router(router)) != MOE_OK) return st;
+  // The shared gate is computed when the layer has a shared expert (shared_ff > 0).
+  const bool has_sh = cfg->shared_ff > 0;
+  if (has_sh && (!shared || !shared->gate_inp)) return MOE_ERR_INVALID_ARG;
+  if (sgate && !has_sh) return MOE_ERR_INVALID_ARG;
+  if (has_sh && !aligned16(shared->gate_inp)) return MOE_ERR_ALIGNMENT;
+  if (!aligned16(x) || !aligned16(topk_ids) || !aligned16(topk_w) || (sgate && !aligned16(sgate)) ||
+      (logits && !aligned16(logits)))
+    return MOE_ERR_ALIGNMENT;
+  Layout L;
+  if ((st = check_ws(cfg, T, ws, ws_bytes, &L)) != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  return run_router(cfg, x, T, router, shared, L, ws, topk_ids, topk_w, sgate, logits, false,
+                    static_cast<cudaStream_t>(stream));
+}
+
+int moe_topk_from_logits(const moe_cfg_t* cfg, const float* logits, int32_t T, int32_t* topk_ids,
+                         float* topk_w, void* stream) {
+  const int st = validate_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (T < 0 || !logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(logits) || !aligned16(topk_ids) || !aligned16(topk_w)) return MOE_ERR_ALIGNMENT;
+  if (T == 0) return MOE_OK;
+  const int norm = cfg->gating == MOE_GATING_TOPK_SOFTMAX ? 1 : cfg->norm_topk_prob;
+  if (launch_router_select(logits, cfg->n_experts, T, cfg->n_experts, cfg->top_k, norm,
+                           cfg->expert_weights_scale, 0, topk_ids, topk_w, nullptr, nullptr,
+                           nullptr, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+int moe_ffn_forward(const moe_cfg_t* cfg, const void* x, int32_t T, const moe_router_t* router,
+                    const moe_experts_t* experts, const moe_shared_t* shared, void* y,
+                    int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes, void* stream) {
+  int st = validate_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (T < 0 || !x || !y) return MOE_ERR_INVALID_ARG;
+  if ((st = check_router(router)) != MOE_OK) return st;
+  if ((st = check_experts(cfg, experts, shared)) != MOE_OK) return st;
+  if (!aligned16(x) || !aligned16(y) || (topk_ids && !aligned16(topk_ids)) ||
+      (topk_w && !aligned16(topk_w)))
+    return MOE_ERR_ALIGNMENT;
+  Layout L;
+  if ((st = check_ws(cfg, T, ws, ws_bytes, &L)) != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((st = run_router(cfg, x, T, router, shared, L, ws, topk_ids, topk_w, nullptr, nullptr, true,
+                       s)) != MOE_OK)
+    return st;
+  return run_experts(cfg, x, T, experts, shared, y, L, ws, s);
+}
+
+int moe_ffn_forward_routed(const moe_cfg_t* cfg, const void* x, int32_t T,
+                           const int32_t* topk_ids, const float* topk_w, const float* sgate,
+                           const moe_experts_t* experts, const moe_shared_t* shared, void* y,
+                           void* ws, size_t ws_bytes, void* stream) {
+  int st = validate_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (T < 0 || !x || !y || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (cfg->shared_ff > 0 && !sgate) return MOE_ERR_INVALID_ARG;
+  if ((st = check_experts(cfg, experts, shared)) != MOE_OK) return st;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(topk_ids) || !aligned16(topk_w) ||
+      (sgate && !aligned16(sgate)))
+    return MOE_ERR_ALIGNMENT;
+  Layout L;
+  if ((st = check_ws(cfg, T, ws, ws_bytes, &L)) != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MOE_CUDA(mark_phase(0, s));
+  MOE_CUDA(launch_ingest_routing(topk_ids, topk_w, sgate, T, cfg->n_experts, cfg->top_k,
+                                 cfg->shared_ff > 0, at<int32_t>(ws, L.slot_expert),
+                                 at<float>(ws, L.slot_w), s));
+  MOE_CUDA(mark_phase(1, s));
+  MOE_CUDA(mark_phase(2, s));
+  return run_experts(cfg, x, T, experts, shared, y, L, ws, s);
+}
+
+int moe_ffn_forward_host(const moe_cfg_t* cfg, const void* x_host, int32_t T,
+                         const moe_router_t* router, const moe_experts_t* experts,
+                         const moe_shared_t* shared, void* y_host, void* ws, size_t ws_bytes,
+                         void* stream) {
+  int st = validate_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (T < 0 || !x_host || !y_host) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if ((st = check_ws(cfg, T, ws, ws_bytes, &L)) != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* xd = at<void>(ws, L.xstage);
+  void* yd = at<void>(ws, L.ystage);
+  const size_t bytes = (size_t)T * cfg->d_model * 2;
+  MOE_CUDA(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s));
+  st = moe_ffn_forward(cfg, xd, T, router, experts, shared, yd, nullptr, nullptr, ws, ws_bytes,
+                       stream);
+  if (st != MOE_OK) return st;
+  MOE_CUDA(cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s));
+  MOE_CUDA(cudaStreamSynchronize(s));
+  return MOE_OK;
+}
+
+int moe_mxfp4_to_bf16(const void* blocks, const void* scales, int64_t rows, int32_t n_in,
+                      void* out, void* stream) {
+  if (!blocks || !scales || !out || rows < 0 || n_in <= 0) return MOE_ERR_INVALID_ARG;
+  if (n_in % 32) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(blocks) || !aligned16(out)) return MOE_ERR_ALIGNMENT;
+  if (rows == 0) return MOE_OK;
+  MOE_CUDA(launch_mxfp4_to_bf16(static_cast<const uint8_t*>(blocks),
+                                static_cast<const uint8_t*>(scales), rows, n_in,
+                                static_cast<uint16_t*>(out), static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+int moe_set_phase_events(void* const* events, int32_t n_events) {
+  if (events && n_events < 7) return MOE_ERR_INVALID_ARG;
+  if (events)
+    for (int i = 0; i < 7; ++i)
+      if (!events[i]) return MOE_ERR_INVALID_ARG;
+  g_phase_events = events;
+  return MOE_OK;
+}
+
+int moe_device_status(void* ws, void* stream, uint32_t* detail) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t bits = 0;
+  MOE_CUDA(cudaStreamSynchronize(s));
+  MOE_CUDA(cudaMemcpy(&bits, ws, sizeof(bits), cudaMemcpyDeviceToHost));
+  MOE_CUDA(cudaMemset(ws, 0, sizeof(bits)));
+  if (detail) *detail = bits;
+  if (bits & STATUS_TIMEOUT) return MOE_ERR_TIMEOUT;
+  return bits ? MOE_ERR_DEVICE_CHECK : MOE_OK;
+}
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case MOE_ERR_CUDA: return "CUDA launch or runtime error";
+    case MOE_ERR_DEVICE_CHECK: return "device-side bounds check fired";
+    case MOE_ERR_TIMEOUT: return "device-side bounded wait timed out";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,127 @@
+// Group token slots by expert: histogram, exclusive scan, active-expert list and
+// the permuted-row -> slot map, in one CTA.
+//
+// This is the "expert-grouped batching" that the qwen35moe forward-pass design
+// ("Batched prefill", remaining levers) names as the way for tokens that share
+// an expert to stream its weights once.
+//
+// Rows of one expert are written in the order the warps reach them (warp-
+// aggregated shared-memory atomics), so the order inside an expert's row range
+// may change from run to run.  Results do not depend on it: every expert row is
+// computed independently and written back to its slot, and the combine sums a
+// token's slots in a fixed order.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kPermuteThreads = 1024;
+
+// Block-wide exclusive scan of two ints per element pair, two elements per thread.
+__device__ __forceinline__ int2 block_exclusive_scan2(int2 val, int2* warp_tot, int2* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int2 inc = val;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int ox = __shfl_up_sync(0xffffffffu, inc.x, off);
+    const int oy = __shfl_up_sync(0xffffffffu, inc.y, off);
+    if (lane >= off) {
+      inc.x += ox;
+      inc.y += oy;
+    }
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    int2 w = warp_tot[lane];
+    int2 wi = w;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int ox = __shfl_up_sync(0xffffffffu, wi.x, off);
+      const int oy = __shfl_up_sync(0xffffffffu, wi.y, off);
+      if (lane >= off) {
+        wi.x += ox;
+        wi.y += oy;
+      }
+    }
+    warp_tot[lane] = make_int2(wi.x - w.x, wi.y - w.y);
+    if (lane == 31) *total = wi;
+  }
+  __syncthreads();
+  const int2 base = warp_tot[warp];
+  return make_int2(base.x + inc.x - val.x, base.y + inc.y - val.y);
+}
+
+__global__ void __launch_bounds__(kPermuteThreads) permute_kernel(RouteState rs, int S, int E1) {
+  __shared__ int cnt[2 * kPermuteThreads];
+  __shared__ int cursor[2 * kPermuteThreads];
+  __shared__ int2 warp_tot[32];
+  __shared__ int2 total;
+  const int tid = threadIdx.x, lane = tid & 31;
+
+  // This is the first kernel of a call that checks anything: start a clean status.
+  if (tid == 0) *rs.status = 0u;
+  for (int v = tid; v < E1; v += kPermuteThreads) cnt[v] = 0;
+  __syncthreads();
+
+  for (int s = tid; s < S; s += kPermuteThreads) {
+    const int v = rs.slot_expert[s];
+    if (v >= 0 && v < E1)
+      atomicAdd(&cnt[v], 1);
+    else
+      flag_status(rs.status, STATUS_BAD_EXPERT_ID);
+  }
+  __syncthreads();
+
+  // Exclusive scan of (count, count > 0) over the virtual experts.
+  const int v0 = 2 * tid, v1 = 2 * tid + 1;
+  const int c0 = v0 < E1 ? cnt[v0] : 0, c1 = v1 < E1 ? cnt[v1] : 0;
+  const int2 ex = block_exclusive_scan2(make_int2(c0 + c1, (c0 > 0) + (c1 > 0)), warp_tot, &total);
+  if (v0 < E1) {
+    cursor[v0] = ex.x;
+    rs.offsets[v0] = ex.x;
+    rs.counts[v0] = c0;
+    if (c0 > 0) rs.active[ex.y] = v0;
+  }
+  if (v1 < E1) {
+    cursor[v1] = ex.x + c0;
+    rs.offsets[v1] = ex.x + c0;
+    rs.counts[v1] = c1;
+    if (c1 > 0) rs.active[ex.y + (c0 > 0)] = v1;
+  }
+  if (tid == 0) {
+    rs.offsets[E1] = total.x;
+    *rs.n_active = total.y;
+  }
+  __syncthreads();
+
+  // Scatter: each warp ranks its 32 slots per expert and reserves a run of rows.
+  for (int s0 = 0; s0 < S; s0 += kPermuteThreads) {
+    const int s = s0 + tid;
+    int v = s < S ? rs.slot_expert[s] : -1;
+    if (v < 0 || v >= E1) v = -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, v);
+    const int leader = __ffs(peers) - 1;
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    int base = 0;
+    if (lane == leader && v >= 0) base = atomicAdd(&cursor[v], __popc(peers));
+    base = __shfl_sync(0xffffffffu, base, leader);
+    if (v >= 0) {
+      const int row = base + rank;
+      if (row < S)
+        rs.row2slot[row] = s;
+      else
+        flag_status(rs.status, STATUS_ROW_OVERFLOW);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_permute(const RouteState& rs, int S, int E1, cudaStream_t s) {
+  permute_kernel<<<1, kPermuteThreads, 0, s>>>(rs, S, E1);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

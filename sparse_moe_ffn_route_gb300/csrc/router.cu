@@ -1,0 +1,215 @@
+// Router: logits on the tensor cores (warp-level bf16 MMA), then a warp per
+// token for the top-k selection and the routing weights.
+//
+// Sources: "qwen35moe CPU-reference golden vectors", Kernel 4 (softmax over the
+// 256 logits, selection sort with first-seen tie-break, norm_topk_prob times
+// expert_weights_scale, sigmoid shared gate); "Phase 19: MoE - gpt-oss-20b",
+// section 2 Router (logits + bias, top-k, softmax over the chosen k).
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kLogitWarps = 4;            // warps per CTA; each owns 8 expert columns
+constexpr int kLogitTokens = 16;          // tokens per CTA (MMA M)
+
+// One CTA: 16 tokens x 32 experts (4 warps x 8).  Operands go straight from
+// global memory into MMA fragments: lane (g, c) loads the 16 bytes at
+// k + 8c of its rows, and the two MMAs of a 32-wide k step consume words {0,1}
+// and {2,3} of those bytes (the same reordering of k on both operands, so the
+// dot products are unchanged).
+__global__ void __launch_bounds__(kLogitWarps * 32)
+router_logits_kernel(const uint16_t* __restrict__ x, int T, int d, const uint16_t* __restrict__ w_r,
+                     const uint16_t* __restrict__ bias, const uint16_t* __restrict__ wsh, int E,
+                     float* __restrict__ logits, int ldl) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, c = lane & 3;
+  const int t0 = blockIdx.x * kLogitTokens;
+  const int e0 = blockIdx.y * (kLogitWarps * 8) + warp * 8;
+  const int E1 = E + (wsh ? 1 : 0);
+  if (e0 >= E1) return;
+
+  const int ta = t0 + g, tb = t0 + g + 8;
+  const uint16_t* xa = ta < T ? x + (size_t)ta * d : nullptr;
+  const uint16_t* xb = tb < T ? x + (size_t)tb * d : nullptr;
+  const int eb = e0 + g;
+  const uint16_t* wrow = eb < E ? w_r + (size_t)eb * d : (eb == E && wsh ? wsh : nullptr);
+
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll 4
+  for (int k = 0; k < d; k += 32) {
+    const int o = k + 8 * c;
+    uint4 a_lo = xa ? ldg_nc_v4(xa + o) : z;
+    uint4 a_hi = xb ? ldg_nc_v4(xb + o) : z;
+    uint4 b = wrow ? ldg_nc_v4(wrow + o) : z;
+    mma_bf16_16816(acc, a_lo.x, a_hi.x, a_lo.y, a_hi.y, b.x, b.y);
+    mma_bf16_16816(acc, a_lo.z, a_hi.z, a_lo.w, a_hi.w, b.z, b.w);
+  }
+  // acc: (token g, expert 2c), (g, 2c+1), (g+8, 2c), (g+8, 2c+1)
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = (i < 2) ? ta : tb;
+    const int e = e0 + 2 * c + (i & 1);
+    if (t < T && e < E1) {
+      float v = acc[i];
+      if (e < E && bias) v += bf16_to_f32(bias[e]);
+      logits[(size_t)t * ldl + e] = v;
+    }
+  }
+}
+
+constexpr int kSelectWarps = 8;
+
+// Warp per token.  Lane l holds logits l, l+32, ... (EPL per lane).  Each of the
+// k rounds takes the largest untaken logit, lowest index on equal values (the
+// selection sort's first-seen rule), via a butterfly argmax whose result lane 0
+// then broadcasts.  Lane j keeps the j-th pick.
+template <int EPL>
+__global__ void __launch_bounds__(kSelectWarps * 32)
+router_select_kernel(const float* __restrict__ logits, int ldl, int T, int E, int k,
+                     int norm_topk_prob, float scale, int has_shared, int32_t* __restrict__ ids_out,
+                     float* __restrict__ w_out, float* __restrict__ sgate_out,
+                     int32_t* __restrict__ slot_expert, float* __restrict__ slot_w) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kSelectWarps + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const float* row = logits + (size_t)t * ldl;
+  float v[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? row[e] : 0.f;
+  }
+  uint32_t taken = 0;
+  int my_id = -1;
+  float my_val = 0.f, top_val = 0.f;
+  for (int j = 0; j < k; ++j) {
+    int bi = -1;
+    float bv = 0.f;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u) && (bi < 0 || v[i] > bv)) {
+        bi = e;
+        bv = v[i];
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (oi >= 0 && (bi < 0 || ov > bv || (ov == bv && oi < bi))) {
+        bi = oi;
+        bv = ov;
+      }
+    }
+    bi = __shfl_sync(0xffffffffu, bi, 0);
+    bv = __shfl_sync(0xffffffffu, bv, 0);
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == j) {
+      my_id = bi;
+      my_val = bv;
+    }
+    if (j == 0) top_val = bv;   // the largest logit overall
+  }
+  // Routing weights.  Renormalised softmax over the chosen k equals
+  // exp(l_j - l_top) / sum_chosen exp(l_i - l_top) (the full softmax's
+  // denominator cancels); this is also the gpt-oss softmax over the chosen k.
+  float ex = (lane < k) ? expf(my_val - top_val) : 0.f;
+  float den = ex;
+  if (!norm_topk_prob) {   // plain softmax probability of each chosen expert
+    den = 0.f;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) den += expf(v[i] - top_val);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+  const float w = ex / den * scale;
+  const int K = k + has_shared;
+  if (lane < k) {
+    if (ids_out) ids_out[(size_t)t * k + lane] = my_id;
+    if (w_out) w_out[(size_t)t * k + lane] = w;
+    if (slot_expert) {
+      slot_expert[(size_t)t * K + lane] = my_id;
+      slot_w[(size_t)t * K + lane] = w;
+    }
+  }
+  if (has_shared && lane == 0) {
+    const float sg = 1.f / (1.f + expf(-row[E]));
+    if (sgate_out) sgate_out[t] = sg;
+    if (slot_expert) {
+      slot_expert[(size_t)t * K + k] = E;
+      slot_w[(size_t)t * K + k] = sg;
+    }
+  }
+}
+
+__global__ void ingest_routing_kernel(const int32_t* __restrict__ ids, const float* __restrict__ w,
+                                      const float* __restrict__ sgate, int T, int E, int k,
+                                      int has_shared, int32_t* __restrict__ slot_expert,
+                                      float* __restrict__ slot_w) {
+  const int K = k + has_shared;
+  const long n = (long)T * K;
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+    const long t = i / K;
+    const int j = (int)(i - t * K);
+    if (j < k) {
+      // A routed id outside [0, E) becomes -1: the permute flags it and every
+      // later kernel skips the slot (E itself would alias the shared expert).
+      const int id = ids[t * k + j];
+      slot_expert[i] = (id >= 0 && id < E) ? id : -1;
+      slot_w[i] = w[t * k + j];
+    } else {
+      slot_expert[i] = E;
+      slot_w[i] = sgate[t];
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_router_logits(const uint16_t* x, int T, int d, const uint16_t* w_r,
+                                 const uint16_t* bias, const uint16_t* wsh, int E, float* logits,
+                                 int ldl, cudaStream_t s) {
+  const int E1 = E + (wsh ? 1 : 0);
+  dim3 grid((T + kLogitTokens - 1) / kLogitTokens, (E1 + kLogitWarps * 8 - 1) / (kLogitWarps * 8));
+  router_logits_kernel<<<grid, kLogitWarps * 32, 0, s>>>(x, T, d, w_r, bias, wsh, E, logits, ldl);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_select(const float* logits, int ldl, int T, int E, int k,
+                                 int norm_topk_prob, float scale, int has_shared,
+                                 int32_t* ids_out, float* w_out, float* sgate_out,
+                                 int32_t* slot_expert, float* slot_w, cudaStream_t s) {
+  dim3 grid((T + kSelectWarps - 1) / kSelectWarps);
+  const int epl = (E + 31) / 32;
+#define MOE_SELECT(N)                                                                     \
+  router_select_kernel<N><<<grid, kSelectWarps * 32, 0, s>>>(                             \
+      logits, ldl, T, E, k, norm_topk_prob, scale, has_shared, ids_out, w_out, sgate_out, \
+      slot_expert, slot_w)
+  if (epl <= 1) MOE_SELECT(1);
+  else if (epl <= 2) MOE_SELECT(2);
+  else if (epl <= 4) MOE_SELECT(4);
+  else if (epl <= 8) MOE_SELECT(8);
+  else if (epl <= 16) MOE_SELECT(16);
+  else MOE_SELECT(32);
+#undef MOE_SELECT
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ingest_routing(const int32_t* ids, const float* w, const float* sgate, int T,
+                                  int E, int k, int has_shared, int32_t* slot_expert,
+                                  float* slot_w, cudaStream_t s) {
+  const long n = (long)T * (k + has_shared);
+  const int blocks = (int)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
+  ingest_routing_kernel<<<blocks, 256, 0, s>>>(ids, w, sgate, T, E, k, has_shared, slot_expert,
+                                                slot_w);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,73 @@
+"""Helpers shared by the GPU parity tests (no test functions here)."""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+import oracle
+
+TOL_RMS = 2e-2      # layer outputs: max |y_gpu - y_ref| <= 2e-2 * rms(y_ref)
+NEAR_TIE = 1e-5     # logit gap under which a selection may legitimately differ
+
+
+def need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def moe_lib():
+    import sparse_moe_ffn_route_gb300 as moe
+    return moe
+
+
+def cfg_for(spec, **kw):
+    moe = moe_lib()
+    if spec.family == "qwen":
+        c = moe.qwen_cfg(spec.d_model, spec.n_experts, spec.top_k, spec.expert_ff, spec.shared_ff,
+                         expert_weights_scale=spec.expert_weights_scale,
+                         norm_topk_prob=spec.norm_topk_prob)
+    else:
+        c = moe.gptoss_cfg(spec.d_model, spec.n_experts, spec.top_k, spec.expert_ff)
+    return c.replace(**kw) if kw else c
+
+
+def upload(layer):
+    from sparse_moe_ffn_route_gb300 import hostio
+    return hostio.upload(layer)
+
+
+def y_numpy(y: torch.Tensor) -> np.ndarray:
+    return y.float().cpu().numpy().astype(np.float64)
+
+
+def check_y(y_gpu: np.ndarray, y_ref: np.ndarray, what=""):
+    rms = float(np.sqrt(np.mean(y_ref ** 2)))
+    err = float(np.max(np.abs(y_gpu - y_ref))) if y_ref.size else 0.0
+    assert np.all(np.isfinite(y_gpu)), what
+    assert err <= TOL_RMS * rms + 1e-30, f"{what}: max err {err:.3e} > {TOL_RMS} * rms {rms:.3e}"
+    return err, rms
+
+
+def check_routing(g, ids_gpu, w_gpu, logits_gpu_f32, ref, what=""):
+    """GPU routing vs the oracle.
+
+    (1) On the GPU's own fp32 logits the oracle's selection must equal the GPU's
+        bit for bit, and the weights agree to 1e-5 relative.
+    (2) Against the oracle's fp64 logits, ids agree except on near-tie tokens,
+        which are returned.
+    """
+    ids_o, w_o = oracle.route_from_logits(g, logits_gpu_f32.astype(np.float64))
+    assert np.array_equal(ids_o, ids_gpu), f"{what}: selection differs on the same fp32 logits"
+    assert np.allclose(w_gpu, w_o, rtol=1e-5, atol=1e-7), what
+    tie = oracle.near_tie_tokens(ref.logits, ref.ids, NEAR_TIE)
+    diff = np.any(ids_gpu != ref.ids, axis=1)
+    assert not np.any(diff & ~tie), f"{what}: ids differ on tokens {np.nonzero(diff & ~tie)[0]}"
+    return tie, diff
+
+
+def sample_tokens(T, n=48, seed=0):
+    if T <= 64:
+        return np.arange(T, dtype=np.int32)
+    rng = np.random.default_rng(seed)
+    mid = rng.choice(np.arange(8, T - 8), size=n - 16, replace=False)
+    return np.sort(np.concatenate([np.arange(8), mid, np.arange(T - 8, T)])).astype(np.int32)

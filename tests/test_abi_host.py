@@ -1,0 +1,109 @@
+"""C-ABI host checks that need no GPU: the library loads, exports every function the
+header declares, and rejects bad arguments before touching the device."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+torch = pytest.importorskip("torch")
+moe = pytest.importorskip("sparse_moe_ffn_route_gb300")
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b(moe_\w+)\s*\(", src, re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_every_declared_function_is_exported():
+    names = declared_functions()
+    assert {"moe_route", "moe_ffn_forward", "moe_workspace_bytes"} <= names
+    lib = ctypes.CDLL(moe.LIB_PATH)
+    for n in sorted(names):
+        assert hasattr(lib, n), n
+    assert names == set(moe.EXPORTED)
+
+
+def test_workspace_and_path_queries():
+    q = moe.qwen_cfg()
+    assert moe.moe_workspace_bytes(q, 0) > 0
+    assert moe.moe_workspace_bytes(q, 64) > moe.moe_workspace_bytes(q, 8)
+    assert moe.moe_select_path(q, 8) == moe.PATH_DECODE
+    assert moe.moe_select_path(q, 4096) == moe.PATH_PREFILL
+    g = moe.gptoss_cfg()
+    assert moe.moe_select_path(g, 32) == moe.PATH_DECODE
+    assert moe.moe_select_path(g, 8192) == moe.PATH_PREFILL
+    assert moe.moe_select_path(g.replace(path=moe.PATH_DECODE), 8192) == moe.PATH_DECODE
+
+
+BAD_CFGS = [
+    dict(top_k=0), dict(top_k=300), dict(n_experts=0), dict(n_experts=2000), dict(d_model=-1),
+    dict(gating=2), dict(act=5), dict(wfmt=3), dict(path=7), dict(expert_weights_scale=float("nan")),
+]
+
+
+@pytest.mark.parametrize("kw", BAD_CFGS)
+def test_invalid_cfg_rejected(kw):
+    c = moe.qwen_cfg().replace(**kw)
+    assert moe.moe_workspace_bytes(c, 8) == 0
+    lib = moe._lib
+    fake = ctypes.c_void_p(1 << 20)
+    st = lib.moe_ffn_forward(ctypes.byref(c), fake, 8, None, None, None, fake, None, None, fake,
+                             1 << 30, None)
+    assert st == -1
+
+
+def test_unsupported_shapes():
+    def path(c):
+        return moe._lib.moe_select_path(ctypes.byref(c), 8)
+    assert path(moe.qwen_cfg(d_model=100)) == -2                    # d % 32
+    assert path(moe.gptoss_cfg().replace(interleaved_gate_up=0)) == -2
+    assert path(moe.gptoss_cfg().replace(shared_ff=32)) == -2
+    assert path(moe.qwen_cfg().replace(reserved=(ctypes.c_int32 * 4)(1, 0, 0, 0))) == -1
+    with pytest.raises(moe.MoeError):
+        moe.moe_select_path(moe.qwen_cfg(d_model=100), 8)
+
+
+def _args(cfg, T, ws_bytes, x=1 << 20, y=2 << 20, ws=3 << 20):
+    lib = moe._lib
+    P = ctypes.c_void_p
+    r = moe._Router(P(4 << 20).value, None)
+    e = moe._Experts(gate=5 << 20, up=6 << 20, down=7 << 20)
+    s = moe._Shared(8 << 20, 9 << 20, 10 << 20, 11 << 20)
+    return lib, (ctypes.byref(cfg), P(x), T, ctypes.byref(r), ctypes.byref(e), ctypes.byref(s),
+                 P(y), None, None, P(ws), ws_bytes, None)
+
+
+def test_argument_errors_before_any_launch():
+    c = moe.qwen_cfg()
+    need = moe.moe_workspace_bytes(c, 64)
+    lib, a = _args(c, 64, need - 1)
+    assert lib.moe_ffn_forward(*a) == -3                   # workspace too small
+    lib, a = _args(c, 64, need, x=(1 << 20) + 8)
+    assert lib.moe_ffn_forward(*a) == -4                   # misaligned x
+    lib, a = _args(c, 64, need, ws=(3 << 20) + 4)
+    assert lib.moe_ffn_forward(*a) == -4                   # misaligned workspace
+    lib, a = _args(c, -1, need)
+    assert lib.moe_ffn_forward(*a) == -1                   # negative T
+    lib, a = _args(c, 0, need)
+    assert lib.moe_ffn_forward(*a) == 0                    # T == 0: no work, no launch
+    a = list(a)
+    a[5] = None                                            # shared expert missing
+    assert lib.moe_ffn_forward(*a) == -1
+    assert lib.moe_topk_from_logits(ctypes.byref(c), None, 4, None, None, None) == -1
+    assert lib.moe_mxfp4_to_bf16(ctypes.c_void_p(1 << 20), ctypes.c_void_p(2 << 20), 4, 48,
+                                 ctypes.c_void_p(3 << 20), None) == -2
+    assert lib.moe_device_status(None, None, None) == -1
+
+
+def test_status_strings():
+    for st in range(-7, 1):
+        assert moe.moe_status_string(st) != "unknown status"
+    assert moe.moe_status_string(-99) == "unknown status"

@@ -1,0 +1,267 @@
+"""CUDA path vs the fp64 oracle, element by element, through the C ABI (GPU only)."""
+import numpy as np
+import pytest
+
+import moe_inputs as mi
+import oracle
+from gpu_util import (check_routing, check_y, cfg_for, moe_lib, need_gpu, sample_tokens, upload,
+                      y_numpy)
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(autouse=True)
+def _gpu():
+    need_gpu()
+
+
+# ----------------------------------------------------------------------------- MXFP4 decode
+@pytest.mark.parametrize("scale", [0, 1, 100, 118, 122, 126, 127, 128, 129, 200, 254, 255])
+def test_mxfp4_decode_bit_exact(scale):
+    moe = moe_lib()
+    rows, n_in = 6, 96
+    blocks = mi.random_bytes(77 + scale, 0, (rows, n_in // 32, 16))
+    blocks[0, 0, :] = np.arange(16, dtype=np.uint8) * 0x11      # every code, both nibbles
+    scales = np.full((rows, n_in // 32), scale, np.uint8)
+    scales[1, :] = [scale, 127, 1]
+    ref = mi.f64_to_bf16(oracle.mxfp4_decode(blocks, scales))
+    out = moe.moe_mxfp4_to_bf16(torch.from_numpy(blocks).cuda(), torch.from_numpy(scales).cuda())
+    from sparse_moe_ffn_route_gb300.hostio import to_numpy_bf16
+    got = to_numpy_bf16(out)
+    nan = np.isnan(mi.bf16_to_f32(ref))
+    assert np.array_equal(np.isnan(mi.bf16_to_f32(got)), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+# ----------------------------------------------------------------------------- top-k
+def _logit_sets():
+    rng = np.random.default_rng(11)
+    yield "normal", rng.standard_normal((300, 256)).astype(np.float32)
+    yield "ties", rng.choice(np.float32([-1, -0.0, 0, 0.5, 1]), size=(300, 256))
+    yield "coarse", (np.round(rng.standard_normal((300, 32)) * 4) / 4).astype(np.float32)
+    yield "wide", rng.standard_normal((64, 1024)).astype(np.float32) * 30
+    yield "narrow", rng.standard_normal((70, 5)).astype(np.float32)
+
+
+@pytest.mark.parametrize("gating,norm,scale", [(0, 1, 1.0), (0, 1, 2.5), (0, 0, 1.0), (1, 1, 1.0)])
+def test_topk_from_logits_exact(gating, norm, scale):
+    moe = moe_lib()
+    for name, L in _logit_sets():
+        T, E = L.shape
+        for k in sorted({1, min(4, E), min(8, E), E if E <= 32 else 32}):
+            c = moe.qwen_cfg(d_model=32, n_experts=E, top_k=k, expert_ff=32, shared_ff=0,
+                             expert_weights_scale=scale, norm_topk_prob=norm).replace(gating=gating)
+            ids, w = moe.moe_topk_from_logits(c, torch.from_numpy(L).cuda())
+            g = oracle.Gating(32, E, k, 32, gating=gating, norm_topk_prob=norm, scale=scale)
+            ids_o, w_o = oracle.route_from_logits(g, L.astype(np.float64))
+            assert np.array_equal(ids.cpu().numpy(), ids_o), (name, k)
+            assert np.allclose(w.cpu().numpy(), w_o, rtol=1e-5, atol=1e-7), (name, k)
+
+
+# ----------------------------------------------------------------------------- router
+ROUTE_SPECS = [
+    mi.small_spec("qwen", 64, 8, 2, 32, 32, 33, bias=None),
+    mi.small_spec("qwen", 128, 40, 6, 32, 64, 17, bias=("normal", 0.5)),
+    mi.small_spec("gptoss", 96, 12, 3, 64, 0, 31, bias=("normal", 0.1)),
+]
+
+
+@pytest.mark.parametrize("spec", ROUTE_SPECS, ids=lambda s: s.name)
+def test_route_matches_oracle(spec):
+    moe = moe_lib()
+    lay = mi.make_layer(spec)
+    g = oracle.gating_for(spec)
+    ref = oracle.route(g, lay)
+    x, router, experts, shared = upload(lay)
+    c = cfg_for(spec)
+    T, E = spec.tokens, spec.n_experts
+    logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    sgate = torch.empty(T, dtype=torch.float32, device="cuda") if spec.shared_ff else None
+    ids, w, sg, lg = moe.moe_route(c, x, router, shared, sgate=sgate, logits=logits)
+    L = lg.cpu().numpy()
+    assert np.allclose(L, ref.logits, rtol=1e-5, atol=2e-5)
+    check_routing(g, ids.cpu().numpy(), w.cpu().numpy(), L, ref, spec.name)
+    if spec.shared_ff:
+        assert np.allclose(sg.cpu().numpy(), ref.sgate, rtol=1e-5, atol=1e-6)
+
+
+# ----------------------------------------------------------------------------- whole layer, small
+def _interleaved_bf16(spec):
+    """A bf16 layer in the interleaved gate_up layout with clamped GLU and biases."""
+    lay = mi.make_layer(spec)
+    E, ff, d = spec.n_experts, spec.expert_ff, spec.d_model
+    gu = np.empty((E, 2 * ff, d), np.uint16)
+    gu[:, 0::2], gu[:, 1::2] = lay.gate, lay.up
+    lay.gate_up = gu
+    lay.gate = lay.up = None
+    rng = np.random.default_rng(5)
+    lay.gu_bias = mi.f64_to_bf16(rng.standard_normal((E, 2 * ff)) * 0.5)
+    lay.dn_bias = mi.f64_to_bf16(rng.standard_normal((E, d)) * 0.1)
+    return lay
+
+
+LAYER_SPECS = [
+    mi.small_spec("qwen", 64, 8, 2, 32, 32, 1),
+    mi.small_spec("qwen", 64, 8, 2, 32, 32, 3),
+    mi.small_spec("qwen", 128, 16, 4, 64, 96, 33, bias=("normal", 0.5)),
+    mi.small_spec("qwen", 96, 6, 6, 32, 0, 31),                                   # E == k
+    mi.small_spec("qwen", 64, 8, 3, 32, 32, 40, expert_weights_scale=2.5),
+    mi.small_spec("qwen", 64, 8, 3, 32, 32, 9, norm_topk_prob=0),
+    mi.small_spec("gptoss", 64, 8, 2, 64, 0, 1, bias=("normal", 0.1)),
+    mi.small_spec("gptoss", 96, 12, 4, 96, 0, 37, bias=("normal", 0.1)),
+    mi.small_spec("gptoss", 160, 8, 2, 224, 0, 70, bias=("zipf", 1.1)),          # > 32 tokens/expert
+    mi.small_spec("gptoss", 64, 4, 4, 32, 0, 19, bias=None, scale_lo=118, scale_hi=120),
+]
+
+
+@pytest.mark.parametrize("spec", LAYER_SPECS, ids=lambda s: s.name)
+def test_layer_matches_oracle(spec):
+    moe = moe_lib()
+    lay = mi.make_layer(spec)
+    g = oracle.gating_for(spec)
+    ref = oracle.forward(g, lay)
+    x, router, experts, shared = upload(lay)
+    c = cfg_for(spec)
+    T, k = spec.tokens, spec.top_k
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    ws = moe.workspace(c, T)
+    y = moe.moe_ffn_forward(c, x, router, experts, shared, topk_ids=ids, topk_w=w, ws=ws)
+    assert moe.moe_device_status(ws)[0] == 0
+    ids_g = ids.cpu().numpy()
+    diff = np.any(ids_g != ref.ids, axis=1)
+    tie = oracle.near_tie_tokens(ref.logits, ref.ids)
+    assert not np.any(diff & ~tie)
+    if np.any(diff):
+        ref = oracle.forward(g, lay, forced_ids=np.where(diff[:, None], ids_g, ref.ids))
+    check_y(y_numpy(y), ref.y, spec.name)
+
+
+def test_interleaved_bf16_clamped_layer():
+    moe = moe_lib()
+    spec = mi.small_spec("qwen", 96, 8, 3, 64, 0, 29, bias=("normal", 0.3))
+    lay = _interleaved_bf16(spec)
+    g = oracle.Gating(96, 8, 3, 64, 0, gating=1, act=1, wfmt=0, interleaved=1)
+    ref = oracle.forward(g, lay)
+    x, router, experts, shared = upload(lay)
+    c = moe.qwen_cfg(96, 8, 3, 64, 0).replace(gating=1, act=1, interleaved_gate_up=1)
+    ids = torch.empty((29, 3), dtype=torch.int32, device="cuda")
+    y = moe.moe_ffn_forward(c, x, router, experts, None, topk_ids=ids)
+    assert np.array_equal(ids.cpu().numpy(), ref.ids)
+    check_y(y_numpy(y), ref.y, "interleaved bf16")
+
+
+@pytest.mark.parametrize("family", ["qwen", "gptoss"])
+def test_forced_routing_hot_expert_and_duplicates(family):
+    """Every token sends all k slots to experts {3, 3, 1, ...}: one expert gets 2T rows."""
+    moe = moe_lib()
+    spec = (mi.small_spec("qwen", 64, 8, 3, 32, 32, 45) if family == "qwen"
+            else mi.small_spec("gptoss", 64, 8, 3, 64, 0, 45, bias=("normal", 0.1)))
+    lay = mi.make_layer(spec)
+    g = oracle.gating_for(spec)
+    T = spec.tokens
+    forced = np.tile(np.array([3, 3, 1], np.int32), (T, 1))
+    forced[::5, 2] = 7
+    ref = oracle.forward(g, lay, forced_ids=forced)
+    x, router, experts, shared = upload(lay)
+    c = cfg_for(spec)
+    sg = torch.from_numpy(ref.sgate.astype(np.float32)).cuda() if spec.shared_ff else None
+    y = moe.moe_ffn_forward_routed(c, x, torch.from_numpy(forced).cuda(),
+                                   torch.from_numpy(ref.w.astype(np.float32)).cuda(), experts,
+                                   shared, sgate=sg)
+    check_y(y_numpy(y), ref.y, family)
+
+
+def test_bad_ids_are_flagged_not_faulting():
+    moe = moe_lib()
+    spec = mi.small_spec("qwen", 64, 8, 2, 32, 32, 6)
+    lay = mi.make_layer(spec)
+    g = oracle.gating_for(spec)
+    ref = oracle.forward(g, lay)
+    x, router, experts, shared = upload(lay)
+    c = cfg_for(spec)
+    ids = ref.ids.copy()
+    ids[2, 1] = 99
+    ids[4, 0] = -3
+    ws = moe.workspace(c, 6)
+    y = moe.moe_ffn_forward_routed(c, x, torch.from_numpy(ids).cuda(),
+                                   torch.from_numpy(ref.w.astype(np.float32)).cuda(), experts,
+                                   shared, sgate=torch.from_numpy(ref.sgate.astype(np.float32)).cuda(),
+                                   ws=ws)
+    st, bits = moe.moe_device_status(ws)
+    assert st == -6 and bits & 1
+    good = [0, 1, 3, 5]
+    check_y(y_numpy(y)[good], ref.y[good], "unaffected tokens")
+    assert moe.moe_device_status(ws)[0] == 0            # cleared by the read
+
+
+def test_deterministic_and_stream_ordered():
+    moe = moe_lib()
+    spec = mi.small_spec("gptoss", 128, 16, 4, 128, 0, 200, bias=("zipf", 1.1))
+    lay = mi.make_layer(spec)
+    x, router, experts, shared = upload(lay)
+    c = cfg_for(spec)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        ws = moe.workspace(c, 200)
+        ys = [moe.moe_ffn_forward(c, x, router, experts, shared, ws=ws).clone() for _ in range(4)]
+    s.synchronize()
+    for yy in ys[1:]:
+        assert torch.equal(yy.view(torch.int16), ys[0].view(torch.int16))
+
+
+def test_zero_tokens():
+    moe = moe_lib()
+    c = moe.qwen_cfg(64, 8, 2, 32, 32)
+    spec = mi.small_spec("qwen", 64, 8, 2, 32, 32, 0)
+    lay = mi.make_layer(spec)
+    x, router, experts, shared = upload(lay)
+    y = moe.moe_ffn_forward(c, x, router, experts, shared)
+    assert y.shape == (0, 64)
+
+
+# ----------------------------------------------------------------------------- full-size workloads
+@pytest.fixture(scope="module")
+def full_layers():
+    cache = {}
+
+    def get(name):
+        if name not in cache:
+            cache.clear()
+            torch.cuda.empty_cache()
+            spec = mi.WORKLOADS[name]
+            lay = mi.make_layer(spec)
+            cache[name] = (spec, lay, upload(lay))
+        return cache[name]
+    return get
+
+
+@pytest.mark.parametrize("name", mi.WORKLOAD_ORDER)
+def test_full_workload(name, full_layers):
+    moe = moe_lib()
+    spec, lay, (x, router, experts, shared) = full_layers(name)
+    g = oracle.gating_for(spec)
+    c = cfg_for(spec)
+    T, k = spec.tokens, spec.top_k
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    ws = moe.workspace(c, T)
+    y = moe.moe_ffn_forward(c, x, router, experts, shared, topk_ids=ids, topk_w=w, ws=ws)
+    assert moe.moe_device_status(ws)[0] == 0
+    # routing of every token
+    logits = torch.empty((T, spec.n_experts), dtype=torch.float32, device="cuda")
+    ids2, w2, _, _ = moe.moe_route(c, x, router, shared, logits=logits)
+    assert torch.equal(ids2, ids) and torch.equal(w2, w)
+    ref_r = oracle.route(g, lay)
+    tie, diff = check_routing(g, ids.cpu().numpy(), w.cpu().numpy(), logits.cpu().numpy(), ref_r,
+                              name)
+    # outputs of sampled tokens (near-tie tokens re-scored with the GPU's selection)
+    tok = sample_tokens(T)
+    ids_g = ids.cpu().numpy()[tok]
+    ref = oracle.forward(g, lay, tokens=tok, forced_ids=ids_g)
+    check_y(y_numpy(y)[tok], ref.y, name)
+    # the host-buffer entry point gives the same bytes
+    xh = x.cpu().pin_memory()
+    yh = moe.moe_ffn_forward_host(c, xh, router, experts, shared, ws=ws)
+    assert torch.equal(yh.view(torch.int16), y.cpu().view(torch.int16))

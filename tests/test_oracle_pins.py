@@ -338,3 +338,12 @@ def test_near_tie_detector():
     lg = np.array([[3.0, 1.0, 1.0 + 5e-6, 0.0], [3.0, 2.0, 1.0, 0.0]])
     ids = np.array([[0, 2], [0, 1]])
     assert list(oracle.near_tie_tokens(lg, ids)) == [True, False]
+
+
+def test_route_only_matches_forward():
+    for spec, lay in (small_qwen(E=16, k=4, bias=("normal", 0.5), T=7), small_oss(E=8, k=2, T=7)):
+        g = oracle.gating_for(spec)
+        f = oracle.forward(g, lay)
+        r = oracle.route(g, lay, tokens=np.arange(7)[::-1].copy())
+        assert np.array_equal(r.ids, f.ids[::-1]) and np.array_equal(r.w, f.w[::-1])
+        assert np.array_equal(r.sgate, f.sgate[::-1]) and np.array_equal(r.logits, f.logits[::-1])
