@@ -30,6 +30,7 @@
  *     Work is enqueued on it in stream order; results are valid once the
  *     stream has reached the end of the call's work.
  *   - bf16 tensors are raw IEEE bfloat16 bit patterns (uint16), row-major.
+ *   - T == 0 is a no-op that returns MOE_OK (data pointers may then be NULL).
  *     Weight matrices are stored row = output, column = input (y = x W^T).
  *   - Every tensor pointer must be 16-byte aligned (MOE_ERR_ALIGNMENT).
  *   - Return value: MOE_OK (0) or a negative MOE_ERR_* code.  On error nothing
@@ -93,7 +94,8 @@ typedef struct {
   float glu_limit;              /* clamped GLU limit (gpt-oss 7.0) */
   float glu_alpha;              /* clamped GLU sigmoid slope (gpt-oss 1.702) */
   int32_t path;                 /* MOE_PATH_* */
-  int32_t reserved[4];          /* must be zero */
+  int32_t y_fp32;               /* 0: y is bf16 [T, d] (RNE of the fp32 result); 1: y is fp32 [T, d] */
+  int32_t reserved[3];          /* must be zero */
 } moe_cfg_t;
 
 /* Router: w bf16 [E, d] (row e = expert e's logit weights); bias bf16 [E] or NULL. */
@@ -169,6 +171,8 @@ int moe_topk_from_logits(const moe_cfg_t* cfg, const float* logits, int32_t T, i
 /* The whole layer: route, group tokens by expert, run the selected experts (and
  * the shared expert), combine.  y bf16 [T, d] device, out.  topk_ids [T, k] /
  * topk_w [T, k] device or NULL: if given, the routing is also written there.
+ * The combine accumulates in fp32; with cfg->y_fp32 = 0, y holds that fp32 result
+ * rounded to bf16 (round to nearest even), with y_fp32 = 1 the fp32 result itself.
  * Defined by the two conventions in the header comment above. */
 int moe_ffn_forward(const moe_cfg_t* cfg, const void* x, int32_t T, const moe_router_t* router,
                     const moe_experts_t* experts, const moe_shared_t* shared, void* y,

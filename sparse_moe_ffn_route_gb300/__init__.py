@@ -51,7 +51,7 @@ class MoeCfg(ctypes.Structure):
                 ("interleaved_gate_up", ctypes.c_int32), ("norm_topk_prob", ctypes.c_int32),
                 ("expert_weights_scale", ctypes.c_float), ("glu_limit", ctypes.c_float),
                 ("glu_alpha", ctypes.c_float), ("path", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 4)]
+                ("y_fp32", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
 
     def replace(self, **kw) -> "MoeCfg":
         c = MoeCfg()
@@ -252,9 +252,11 @@ def moe_topk_from_logits(cfg: MoeCfg, logits: torch.Tensor, topk_ids=None, topk_
 def moe_ffn_forward(cfg: MoeCfg, x: torch.Tensor, router: Router, experts: Experts,
                     shared: Optional[Shared] = None, y=None, topk_ids=None, topk_w=None, ws=None,
                     stream=None) -> torch.Tensor:
-    """The whole layer; returns y bf16 [T, d]."""
+    """The whole layer; returns y [T, d] (bf16, or fp32 when cfg.y_fp32)."""
     T = x.shape[0]
-    y = torch.empty_like(x) if y is None else y
+    if y is None:
+        y = torch.empty(x.shape, dtype=torch.float32 if cfg.y_fp32 else torch.bfloat16,
+                        device=x.device)
     ws = workspace(cfg, T, x.device) if ws is None else ws
     _check(_lib.moe_ffn_forward(ctypes.byref(cfg), _ptr(x, "x"), T, ctypes.byref(_router(router)),
                                 ctypes.byref(_experts(experts)), _shared(shared), _ptr(y, "y"),
@@ -267,7 +269,9 @@ def moe_ffn_forward_routed(cfg: MoeCfg, x: torch.Tensor, topk_ids: torch.Tensor,
                            topk_w: torch.Tensor, experts: Experts, shared: Optional[Shared] = None,
                            sgate=None, y=None, ws=None, stream=None) -> torch.Tensor:
     T = x.shape[0]
-    y = torch.empty_like(x) if y is None else y
+    if y is None:
+        y = torch.empty(x.shape, dtype=torch.float32 if cfg.y_fp32 else torch.bfloat16,
+                        device=x.device)
     ws = workspace(cfg, T, x.device) if ws is None else ws
     _check(_lib.moe_ffn_forward_routed(ctypes.byref(cfg), _ptr(x, "x"), T, _ptr(topk_ids),
                                        _ptr(topk_w), _ptr(sgate), ctypes.byref(_experts(experts)),
@@ -283,7 +287,8 @@ def moe_ffn_forward_host(cfg: MoeCfg, x_host: torch.Tensor, router: Router, expe
     if x_host.is_cuda:
         raise ValueError("x_host must be a CPU tensor")
     T = x_host.shape[0]
-    y_host = torch.empty_like(x_host) if y_host is None else y_host
+    if y_host is None:
+        y_host = torch.empty(x_host.shape, dtype=torch.float32 if cfg.y_fp32 else torch.bfloat16)
     ws = workspace(cfg, T) if ws is None else ws
     _check(_lib.moe_ffn_forward_host(ctypes.byref(cfg), x_host.data_ptr(), T,
                                      ctypes.byref(_router(router)), ctypes.byref(_experts(experts)),

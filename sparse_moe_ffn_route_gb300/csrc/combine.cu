@@ -11,10 +11,11 @@
 namespace moe {
 namespace {
 
+template <bool F32>
 __global__ void __launch_bounds__(256)
 combine_kernel(const float* __restrict__ Y, const float* __restrict__ slot_w,
                const int32_t* __restrict__ slot_expert, int T, int K, int d, int E1,
-               uint16_t* __restrict__ y) {
+               void* __restrict__ y) {
   const int d8 = d / 8;
   const long n = (long)T * d8;
   for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
@@ -31,23 +32,32 @@ combine_kernel(const float* __restrict__ Y, const float* __restrict__ slot_w,
       acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
       acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
     }
-    uint4 out;
-    out.x = pack_bf16x2(acc[0], acc[1]);
-    out.y = pack_bf16x2(acc[2], acc[3]);
-    out.z = pack_bf16x2(acc[4], acc[5]);
-    out.w = pack_bf16x2(acc[6], acc[7]);
-    *reinterpret_cast<uint4*>(y + (size_t)t * d + o) = out;
+    if (F32) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(y) + (size_t)t * d + o);
+      dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    } else {
+      uint4 out;
+      out.x = pack_bf16x2(acc[0], acc[1]);
+      out.y = pack_bf16x2(acc[2], acc[3]);
+      out.z = pack_bf16x2(acc[4], acc[5]);
+      out.w = pack_bf16x2(acc[6], acc[7]);
+      *reinterpret_cast<uint4*>(static_cast<uint16_t*>(y) + (size_t)t * d + o) = out;
+    }
   }
 }
 
 }  // namespace
 
 cudaError_t launch_combine(const float* Y, const float* slot_w, const int32_t* slot_expert, int T,
-                           int K, int d, int E1, uint16_t* y, cudaStream_t s) {
+                           int K, int d, int E1, void* y, bool y_fp32, cudaStream_t s) {
   const long n = (long)T * (d / 8);
   long blocks = (n + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
-  combine_kernel<<<(int)blocks, 256, 0, s>>>(Y, slot_w, slot_expert, T, K, d, E1, y);
+  if (y_fp32)
+    combine_kernel<true><<<(int)blocks, 256, 0, s>>>(Y, slot_w, slot_expert, T, K, d, E1, y);
+  else
+    combine_kernel<false><<<(int)blocks, 256, 0, s>>>(Y, slot_w, slot_expert, T, K, d, E1, y);
   return cudaGetLastError();
 }
 

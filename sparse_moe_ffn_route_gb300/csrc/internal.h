@@ -90,8 +90,8 @@ cudaError_t launch_down_decode(const ExpertParams& p, int wfmt, const RouteState
 cudaError_t launch_mxfp4_to_bf16(const uint8_t* blocks, const uint8_t* scales, long long rows,
                                  int n_in, uint16_t* out, cudaStream_t s);
 
-// y[t] = sum_j slot_w[t,j] * Y[t*K + j]  (bf16 out).
+// y[t] = sum_j slot_w[t,j] * Y[t*K + j]  (fp32 accumulation; bf16 or fp32 out).
 cudaError_t launch_combine(const float* Y, const float* slot_w, const int32_t* slot_expert, int T,
-                           int K, int d, int E1, uint16_t* y, cudaStream_t s);
+                           int K, int d, int E1, void* y, bool y_fp32, cudaStream_t s);
 
 }  // namespace moe

@@ -28,7 +28,7 @@ int validate_cfg(const moe_cfg_t* c) {
     return MOE_ERR_INVALID_ARG;
   if (c->gating < 0 || c->gating > 1 || c->act < 0 || c->act > 1 || c->wfmt < 0 || c->wfmt > 1 ||
       c->interleaved_gate_up < 0 || c->interleaved_gate_up > 1 || c->norm_topk_prob < 0 ||
-      c->norm_topk_prob > 1 || c->path < 0 || c->path > 2)
+      c->norm_topk_prob > 1 || c->path < 0 || c->path > 2 || c->y_fp32 < 0 || c->y_fp32 > 1)
     return MOE_ERR_INVALID_ARG;
   for (int r : c->reserved)
     if (r != 0) return MOE_ERR_INVALID_ARG;
@@ -69,7 +69,7 @@ bool make_layout(const moe_cfg_t* c, int T, Layout* L) {
   L->h = take(2 * Sz * (size_t)L->ldh);
   L->Y = take(4 * Sz * d);
   L->xstage = take(2 * Tz * d);
-  L->ystage = take(2 * Tz * d);
+  L->ystage = take(4 * Tz * d);
   L->total = off;
   return true;
 }
@@ -228,8 +228,8 @@ int run_experts(const moe_cfg_t* c, const void* x, int T, const moe_experts_t* e
   MOE_CUDA(mark_phase(4, s));
   MOE_CUDA(launch_down_decode(p, c->wfmt, rs, h, L.ldh, Y, L.E1, s));
   MOE_CUDA(mark_phase(5, s));
-  MOE_CUDA(launch_combine(Y, rs.slot_w, rs.slot_expert, T, L.K, c->d_model, L.E1,
-                          static_cast<uint16_t*>(y), s));
+  MOE_CUDA(launch_combine(Y, rs.slot_w, rs.slot_expert, T, L.K, c->d_model, L.E1, y,
+                          c->y_fp32 != 0, s));
   MOE_CUDA(mark_phase(6, s));
   return MOE_OK;
 }
@@ -257,7 +257,9 @@ int moe_route(const moe_cfg_t* cfg, const void* x, int32_t T, const moe_router_t
               float* logits, void* ws, size_t ws_bytes, void* stream) {
   int st = validate_cfg(cfg);
   if (st != MOE_OK) return st;
-  if (T < 0 || !x || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
   if ((st = check_router(router)) != MOE_OK) return st;
   // The shared gate is computed when the layer has a shared expert (shared_ff > 0).
   const bool has_sh = cfg->shared_ff > 0;
@@ -269,7 +271,6 @@ int moe_route(const moe_cfg_t* cfg, const void* x, int32_t T, const moe_router_t
     return MOE_ERR_ALIGNMENT;
   Layout L;
   if ((st = check_ws(cfg, T, ws, ws_bytes, &L)) != MOE_OK) return st;
-  if (T == 0) return MOE_OK;
   return run_router(cfg, x, T, router, shared, L, ws, topk_ids, topk_w, sgate, logits, false,
                     static_cast<cudaStream_t>(stream));
 }
@@ -278,9 +279,10 @@ int moe_topk_from_logits(const moe_cfg_t* cfg, const float* logits, int32_t T, i
                          float* topk_w, void* stream) {
   const int st = validate_cfg(cfg);
   if (st != MOE_OK) return st;
-  if (T < 0 || !logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(logits) || !aligned16(topk_ids) || !aligned16(topk_w)) return MOE_ERR_ALIGNMENT;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
+  if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(logits) || !aligned16(topk_ids) || !aligned16(topk_w)) return MOE_ERR_ALIGNMENT;
   const int norm = cfg->gating == MOE_GATING_TOPK_SOFTMAX ? 1 : cfg->norm_topk_prob;
   if (launch_router_select(logits, cfg->n_experts, T, cfg->n_experts, cfg->top_k, norm,
                            cfg->expert_weights_scale, 0, topk_ids, topk_w, nullptr, nullptr,
@@ -294,7 +296,9 @@ int moe_ffn_forward(const moe_cfg_t* cfg, const void* x, int32_t T, const moe_ro
                     int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes, void* stream) {
   int st = validate_cfg(cfg);
   if (st != MOE_OK) return st;
-  if (T < 0 || !x || !y) return MOE_ERR_INVALID_ARG;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !y) return MOE_ERR_INVALID_ARG;
   if ((st = check_router(router)) != MOE_OK) return st;
   if ((st = check_experts(cfg, experts, shared)) != MOE_OK) return st;
   if (!aligned16(x) || !aligned16(y) || (topk_ids && !aligned16(topk_ids)) ||
@@ -302,7 +306,6 @@ int moe_ffn_forward(const moe_cfg_t* cfg, const void* x, int32_t T, const moe_ro
     return MOE_ERR_ALIGNMENT;
   Layout L;
   if ((st = check_ws(cfg, T, ws, ws_bytes, &L)) != MOE_OK) return st;
-  if (T == 0) return MOE_OK;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   if ((st = run_router(cfg, x, T, router, shared, L, ws, topk_ids, topk_w, nullptr, nullptr, true,
                        s)) != MOE_OK)
@@ -316,7 +319,9 @@ int moe_ffn_forward_routed(const moe_cfg_t* cfg, const void* x, int32_t T,
                            void* ws, size_t ws_bytes, void* stream) {
   int st = validate_cfg(cfg);
   if (st != MOE_OK) return st;
-  if (T < 0 || !x || !y || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !y || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
   if (cfg->shared_ff > 0 && !sgate) return MOE_ERR_INVALID_ARG;
   if ((st = check_experts(cfg, experts, shared)) != MOE_OK) return st;
   if (!aligned16(x) || !aligned16(y) || !aligned16(topk_ids) || !aligned16(topk_w) ||
@@ -324,7 +329,6 @@ int moe_ffn_forward_routed(const moe_cfg_t* cfg, const void* x, int32_t T,
     return MOE_ERR_ALIGNMENT;
   Layout L;
   if ((st = check_ws(cfg, T, ws, ws_bytes, &L)) != MOE_OK) return st;
-  if (T == 0) return MOE_OK;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   MOE_CUDA(mark_phase(0, s));
   MOE_CUDA(launch_ingest_routing(topk_ids, topk_w, sgate, T, cfg->n_experts, cfg->top_k,
@@ -341,19 +345,21 @@ int moe_ffn_forward_host(const moe_cfg_t* cfg, const void* x_host, int32_t T,
                          void* stream) {
   int st = validate_cfg(cfg);
   if (st != MOE_OK) return st;
-  if (T < 0 || !x_host || !y_host) return MOE_ERR_INVALID_ARG;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x_host || !y_host) return MOE_ERR_INVALID_ARG;
   Layout L;
   if ((st = check_ws(cfg, T, ws, ws_bytes, &L)) != MOE_OK) return st;
-  if (T == 0) return MOE_OK;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* xd = at<void>(ws, L.xstage);
   void* yd = at<void>(ws, L.ystage);
   const size_t bytes = (size_t)T * cfg->d_model * 2;
+  const size_t ybytes = (size_t)T * cfg->d_model * (cfg->y_fp32 ? 4 : 2);
   MOE_CUDA(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s));
   st = moe_ffn_forward(cfg, xd, T, router, experts, shared, yd, nullptr, nullptr, ws, ws_bytes,
                        stream);
   if (st != MOE_OK) return st;
-  MOE_CUDA(cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s));
+  MOE_CUDA(cudaMemcpyAsync(y_host, yd, ybytes, cudaMemcpyDeviceToHost, s));
   MOE_CUDA(cudaStreamSynchronize(s));
   return MOE_OK;
 }

@@ -40,6 +40,21 @@ def y_numpy(y: torch.Tensor) -> np.ndarray:
     return y.float().cpu().numpy().astype(np.float64)
 
 
+def check_outputs(y32: "torch.Tensor", y16: "torch.Tensor", y_ref: np.ndarray, what=""):
+    """Layer output parity.
+
+    The computation is checked on the fp32 output (cfg.y_fp32 = 1) against the
+    2e-2 * rms(y_ref) bar; the bf16 output must then be exactly that fp32 result
+    rounded to nearest even (bf16 keeps 8 significant bits, so its own rounding
+    alone can reach 2^-8 |y|, above the bar wherever |y| > 5.12 rms).
+    """
+    y32n = y32.cpu().numpy()
+    err = check_y(y32n.astype(np.float64), y_ref, what)
+    bits = y16.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(bits, mi.f64_to_bf16(y32n)), f"{what}: bf16 output is not RNE(fp32 output)"
+    return err
+
+
 def check_y(y_gpu: np.ndarray, y_ref: np.ndarray, what=""):
     rms = float(np.sqrt(np.mean(y_ref ** 2)))
     err = float(np.max(np.abs(y_gpu - y_ref))) if y_ref.size else 0.0

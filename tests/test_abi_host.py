@@ -66,7 +66,7 @@ def test_unsupported_shapes():
     assert path(moe.qwen_cfg(d_model=100)) == -2                    # d % 32
     assert path(moe.gptoss_cfg().replace(interleaved_gate_up=0)) == -2
     assert path(moe.gptoss_cfg().replace(shared_ff=32)) == -2
-    assert path(moe.qwen_cfg().replace(reserved=(ctypes.c_int32 * 4)(1, 0, 0, 0))) == -1
+    assert path(moe.qwen_cfg().replace(reserved=(ctypes.c_int32 * 3)(1, 0, 0))) == -1
     with pytest.raises(moe.MoeError):
         moe.moe_select_path(moe.qwen_cfg(d_model=100), 8)
 
@@ -94,9 +94,13 @@ def test_argument_errors_before_any_launch():
     assert lib.moe_ffn_forward(*a) == -1                   # negative T
     lib, a = _args(c, 0, need)
     assert lib.moe_ffn_forward(*a) == 0                    # T == 0: no work, no launch
+    assert lib.moe_ffn_forward(a[0], None, 0, None, None, None, None, None, None, None, 0,
+                               None) == 0                  # ... even with NULL pointers
+    lib, a = _args(c, 64, need)
     a = list(a)
     a[5] = None                                            # shared expert missing
     assert lib.moe_ffn_forward(*a) == -1
+    assert lib.moe_ffn_forward(*_args(c.replace(y_fp32=2), 64, need)[1]) == -1
     assert lib.moe_topk_from_logits(ctypes.byref(c), None, 4, None, None, None) == -1
     assert lib.moe_mxfp4_to_bf16(ctypes.c_void_p(1 << 20), ctypes.c_void_p(2 << 20), 4, 48,
                                  ctypes.c_void_p(3 << 20), None) == -2

@@ -4,8 +4,8 @@ import pytest
 
 import moe_inputs as mi
 import oracle
-from gpu_util import (check_routing, check_y, cfg_for, moe_lib, need_gpu, sample_tokens, upload,
-                      y_numpy)
+from gpu_util import (check_outputs, check_routing, check_y, cfg_for, moe_lib, need_gpu,
+                      sample_tokens, upload, y_numpy)
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -127,7 +127,8 @@ def test_layer_matches_oracle(spec):
     ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
     w = torch.empty((T, k), dtype=torch.float32, device="cuda")
     ws = moe.workspace(c, T)
-    y = moe.moe_ffn_forward(c, x, router, experts, shared, topk_ids=ids, topk_w=w, ws=ws)
+    y16 = moe.moe_ffn_forward(c, x, router, experts, shared, topk_ids=ids, topk_w=w, ws=ws)
+    y32 = moe.moe_ffn_forward(c.replace(y_fp32=1), x, router, experts, shared, ws=ws)
     assert moe.moe_device_status(ws)[0] == 0
     ids_g = ids.cpu().numpy()
     diff = np.any(ids_g != ref.ids, axis=1)
@@ -135,7 +136,7 @@ def test_layer_matches_oracle(spec):
     assert not np.any(diff & ~tie)
     if np.any(diff):
         ref = oracle.forward(g, lay, forced_ids=np.where(diff[:, None], ids_g, ref.ids))
-    check_y(y_numpy(y), ref.y, spec.name)
+    check_outputs(y32, y16, ref.y, spec.name)
 
 
 def test_interleaved_bf16_clamped_layer():
@@ -147,9 +148,10 @@ def test_interleaved_bf16_clamped_layer():
     x, router, experts, shared = upload(lay)
     c = moe.qwen_cfg(96, 8, 3, 64, 0).replace(gating=1, act=1, interleaved_gate_up=1)
     ids = torch.empty((29, 3), dtype=torch.int32, device="cuda")
-    y = moe.moe_ffn_forward(c, x, router, experts, None, topk_ids=ids)
+    y16 = moe.moe_ffn_forward(c, x, router, experts, None, topk_ids=ids)
+    y32 = moe.moe_ffn_forward(c.replace(y_fp32=1), x, router, experts, None)
     assert np.array_equal(ids.cpu().numpy(), ref.ids)
-    check_y(y_numpy(y), ref.y, "interleaved bf16")
+    check_outputs(y32, y16, ref.y, "interleaved bf16")
 
 
 @pytest.mark.parametrize("family", ["qwen", "gptoss"])
@@ -167,10 +169,11 @@ def test_forced_routing_hot_expert_and_duplicates(family):
     x, router, experts, shared = upload(lay)
     c = cfg_for(spec)
     sg = torch.from_numpy(ref.sgate.astype(np.float32)).cuda() if spec.shared_ff else None
-    y = moe.moe_ffn_forward_routed(c, x, torch.from_numpy(forced).cuda(),
-                                   torch.from_numpy(ref.w.astype(np.float32)).cuda(), experts,
-                                   shared, sgate=sg)
-    check_y(y_numpy(y), ref.y, family)
+    ids_d = torch.from_numpy(forced).cuda()
+    w_d = torch.from_numpy(ref.w.astype(np.float32)).cuda()
+    y16 = moe.moe_ffn_forward_routed(c, x, ids_d, w_d, experts, shared, sgate=sg)
+    y32 = moe.moe_ffn_forward_routed(c.replace(y_fp32=1), x, ids_d, w_d, experts, shared, sgate=sg)
+    check_outputs(y32, y16, ref.y, family)
 
 
 def test_bad_ids_are_flagged_not_faulting():
@@ -185,14 +188,14 @@ def test_bad_ids_are_flagged_not_faulting():
     ids[2, 1] = 99
     ids[4, 0] = -3
     ws = moe.workspace(c, 6)
-    y = moe.moe_ffn_forward_routed(c, x, torch.from_numpy(ids).cuda(),
+    y = moe.moe_ffn_forward_routed(c.replace(y_fp32=1), x, torch.from_numpy(ids).cuda(),
                                    torch.from_numpy(ref.w.astype(np.float32)).cuda(), experts,
                                    shared, sgate=torch.from_numpy(ref.sgate.astype(np.float32)).cuda(),
                                    ws=ws)
     st, bits = moe.moe_device_status(ws)
     assert st == -6 and bits & 1
     good = [0, 1, 3, 5]
-    check_y(y_numpy(y)[good], ref.y[good], "unaffected tokens")
+    check_y(y.cpu().numpy().astype(np.float64)[good], ref.y[good], "unaffected tokens")
     assert moe.moe_device_status(ws)[0] == 0            # cleared by the read
 
 
@@ -248,6 +251,7 @@ def test_full_workload(name, full_layers):
     w = torch.empty((T, k), dtype=torch.float32, device="cuda")
     ws = moe.workspace(c, T)
     y = moe.moe_ffn_forward(c, x, router, experts, shared, topk_ids=ids, topk_w=w, ws=ws)
+    y32 = moe.moe_ffn_forward(c.replace(y_fp32=1), x, router, experts, shared, ws=ws)
     assert moe.moe_device_status(ws)[0] == 0
     # routing of every token
     logits = torch.empty((T, spec.n_experts), dtype=torch.float32, device="cuda")
@@ -260,7 +264,12 @@ def test_full_workload(name, full_layers):
     tok = sample_tokens(T)
     ids_g = ids.cpu().numpy()[tok]
     ref = oracle.forward(g, lay, tokens=tok, forced_ids=ids_g)
-    check_y(y_numpy(y)[tok], ref.y, name)
+    sel = torch.from_numpy(tok).long().cuda()
+    err, rms = check_outputs(y32[sel], y[sel], ref.y, name)
+    # the bf16 output the benchmark times, against the bar as written
+    err16, _ = check_y(y_numpy(y)[tok], ref.y, name + " (bf16 output)")
+    print(f"{name}: max|dy| fp32 {err / rms:.2e} rms, bf16 {err16 / rms:.2e} rms, "
+          f"near-ties {int(tie.sum())}")
     # the host-buffer entry point gives the same bytes
     xh = x.cpu().pin_memory()
     yh = moe.moe_ffn_forward_host(c, xh, router, experts, shared, ws=ws)
