@@ -30,8 +30,8 @@
  *     Work is enqueued on it in stream order; results are valid once the
  *     stream has reached the end of the call's work.
  *   - bf16 tensors are raw IEEE bfloat16 bit patterns (uint16), row-major.
- *   - T == 0 is a no-op that returns MOE_OK (data pointers may then be NULL).
  *     Weight matrices are stored row = output, column = input (y = x W^T).
+ *   - T == 0 is a no-op that returns MOE_OK (data pointers may then be NULL).
  *   - Every tensor pointer must be 16-byte aligned (MOE_ERR_ALIGNMENT).
  *   - Return value: MOE_OK (0) or a negative MOE_ERR_* code.  On error nothing
  *     has been enqueued unless the code is MOE_ERR_CUDA (a launch failed).
