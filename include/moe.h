@@ -197,6 +197,36 @@ int moe_ffn_forward_host(const moe_cfg_t* cfg, const void* x_host, int32_t T,
                          const moe_shared_t* shared, void* y_host, void* ws, size_t ws_bytes,
                          void* stream);
 
+/* Size of the device array that moe_ffn_forward_noalloc uses as its workspace. */
+#define MOE_NOALLOC_WORKSPACE_BYTES ((size_t)8 << 20)
+
+/* moe_ffn_forward for callers that cannot allocate device memory.  (The pages
+ * have no counterpart: this is an interface addition.)
+ *
+ * Some callers are given only their input and output buffers: a plug-in inside
+ * a host program or serving framework that owns all device memory through its
+ * own pool, where a cudaMalloc would fail or take memory the pool has reserved,
+ * or a latency-critical loop that must not make a call which may synchronise
+ * the device.  They cannot provide the workspace moe_ffn_forward needs, so this
+ * entry point takes it from a device array of MOE_NOALLOC_WORKSPACE_BYTES
+ * (8 MiB) held by the library; it calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *   - Arguments and results are those of moe_ffn_forward without ws/ws_bytes.
+ *   - Returns MOE_ERR_WORKSPACE when moe_workspace_bytes(cfg, T) exceeds the
+ *     array (above 86 tokens of the Qwen3.5-mini layer, 96 of gpt-oss-20b).
+ *   - Every GPU that loads the library holds the array until the process exits.
+ *   - The first call on a device, made with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress) and keeps it; make that
+ *     first call before any stream capture begins.
+ *   - All calls on a device share the one array and it keeps the last call's
+ *     contents (the kernels rewrite all scratch they read, so nothing carries
+ *     over): calls that overlap on the GPU -- on different streams or from
+ *     different host threads without ordering -- race and corrupt each other. */
+int moe_ffn_forward_noalloc(const moe_cfg_t* cfg, const void* x, int32_t T,
+                            const moe_router_t* router, const moe_experts_t* experts,
+                            const moe_shared_t* shared, void* y, int32_t* topk_ids, float* topk_w,
+                            void* stream);
+
 /* Decode MXFP4 weights to bf16 with the decoder the expert kernels use on their
  * weight-load path.  Defined by "Phase 19: MoE - gpt-oss-20b", section 3
  * (value = fp4_lut[code] * 2^(e8m0 - 127)) and the section 2 tensor layout (16

@@ -101,6 +101,10 @@ def _load():
                                          ctypes.POINTER(_Experts), ctypes.POINTER(_Shared), P, P,
                                          ctypes.c_size_t, P]
     lib.moe_ffn_forward_host.restype = I
+    lib.moe_ffn_forward_noalloc.argtypes = [C, P, ctypes.c_int32, ctypes.POINTER(_Router),
+                                            ctypes.POINTER(_Experts), ctypes.POINTER(_Shared), P,
+                                            P, P, P]
+    lib.moe_ffn_forward_noalloc.restype = I
     lib.moe_mxfp4_to_bf16.argtypes = [P, P, ctypes.c_int64, ctypes.c_int32, P, P]
     lib.moe_mxfp4_to_bf16.restype = I
     lib.moe_set_phase_events.argtypes = [P, ctypes.c_int32]
@@ -115,6 +119,7 @@ def _load():
 _lib = _load()
 EXPORTED = ("moe_workspace_bytes", "moe_select_path", "moe_route", "moe_topk_from_logits",
             "moe_ffn_forward", "moe_ffn_forward_routed", "moe_ffn_forward_host",
+            "moe_ffn_forward_noalloc",
             "moe_mxfp4_to_bf16", "moe_set_phase_events", "moe_device_status",
             "moe_status_string")
 PHASES = ("router_logits", "router_select", "permute", "gate_up", "down", "combine")
@@ -262,6 +267,27 @@ def moe_ffn_forward(cfg: MoeCfg, x: torch.Tensor, router: Router, experts: Exper
                                 ctypes.byref(_experts(experts)), _shared(shared), _ptr(y, "y"),
                                 _ptr(topk_ids), _ptr(topk_w), _ptr(ws), ws.numel(),
                                 _stream(stream)), "moe_ffn_forward")
+    return y
+
+
+NOALLOC_WORKSPACE_BYTES = 8 << 20
+
+
+def moe_ffn_forward_noalloc(cfg: MoeCfg, x: torch.Tensor, router: Router, experts: Experts,
+                            shared: Optional[Shared] = None, y=None, topk_ids=None, topk_w=None,
+                            stream=None) -> torch.Tensor:
+    """moe_ffn_forward for callers that cannot allocate device memory: the library's own
+    8 MiB device array serves as workspace (see include/moe.h).  Only `y` is allocated
+    here when it is not passed in."""
+    T = x.shape[0]
+    if y is None:
+        y = torch.empty(x.shape, dtype=torch.float32 if cfg.y_fp32 else torch.bfloat16,
+                        device=x.device)
+    _check(_lib.moe_ffn_forward_noalloc(ctypes.byref(cfg), _ptr(x, "x"), T,
+                                        ctypes.byref(_router(router)),
+                                        ctypes.byref(_experts(experts)), _shared(shared),
+                                        _ptr(y, "y"), _ptr(topk_ids), _ptr(topk_w),
+                                        _stream(stream)), "moe_ffn_forward_noalloc")
     return y
 
 
