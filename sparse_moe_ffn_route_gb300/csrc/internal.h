@@ -49,8 +49,9 @@ struct RouteState {
   float* slot_w;         // [S]
   int32_t* counts;       // [E1]
   int32_t* offsets;      // [E1 + 1]  permuted-row ranges per virtual expert
-  int32_t* active;       // [E1]      virtual experts with rows, ascending
-  int32_t* n_active;     // [1]
+  int2* work;            // [E1 + S]  work items (virtual expert, first row within it); each
+                         //           covers up to `tpg` of that expert's rows
+  int32_t* n_work;       // [1]
   int32_t* row2slot;     // [S]       permuted row -> slot
   uint32_t* status;      // device status word
 };
@@ -76,15 +77,18 @@ cudaError_t launch_ingest_routing(const int32_t* ids, const float* w, const floa
                                   int E, int k, int has_shared, int32_t* slot_expert,
                                   float* slot_w, cudaStream_t s);
 
-// Histogram, offsets, active list and row -> slot map (one CTA).
-cudaError_t launch_permute(const RouteState& rs, int S, int E1, cudaStream_t s);
+// Histogram, offsets, work list (items of up to tpg rows) and row -> slot map (one CTA).
+cudaError_t launch_permute(const RouteState& rs, int S, int E1, int tpg, cudaStream_t s);
 
-// Decode path: weight-streaming grouped matvec on mma.sync.
+// Decode path: weight-streaming grouped matvec on mma.sync.  One CTA row per work
+// item; chunks = token chunks of 8 per item (1 or 4, so tpg = 8 * chunks);
+// max_items bounds the work list (grid size).
 cudaError_t launch_gateup_decode(const ExpertParams& p, int wfmt, int interleaved,
                                  const RouteState& rs, const uint16_t* x, int K, uint16_t* h,
-                                 int ldh, int E1, cudaStream_t s);
+                                 int ldh, int max_items, int chunks, cudaStream_t s);
 cudaError_t launch_down_decode(const ExpertParams& p, int wfmt, const RouteState& rs,
-                               const uint16_t* h, int ldh, float* Y, int E1, cudaStream_t s);
+                               const uint16_t* h, int ldh, float* Y, int max_items, int chunks,
+                               cudaStream_t s);
 
 // MXFP4 [rows, n_in/32, 16] + scales -> bf16 [rows, n_in].
 cudaError_t launch_mxfp4_to_bf16(const uint8_t* blocks, const uint8_t* scales, long long rows,

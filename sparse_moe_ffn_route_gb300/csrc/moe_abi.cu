@@ -17,7 +17,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 struct Layout {
   int K, E1, S, ldl, ldh;
-  size_t status, counts, offsets, active, n_active, slot_expert, slot_w, row2slot, logits, h, Y,
+  size_t status, counts, offsets, work, n_work, slot_expert, slot_w, row2slot, logits, h, Y,
       xstage, ystage, total;
 };
 
@@ -60,8 +60,8 @@ bool make_layout(const moe_cfg_t* c, int T, Layout* L) {
   L->status = take(64);
   L->counts = take(4 * (size_t)L->E1);
   L->offsets = take(4 * ((size_t)L->E1 + 1));
-  L->active = take(4 * (size_t)L->E1);
-  L->n_active = take(4);
+  L->work = take(8 * ((size_t)L->E1 + Sz));
+  L->n_work = take(4);
   L->slot_expert = take(4 * Sz);
   L->slot_w = take(4 * Sz);
   L->row2slot = take(4 * Sz);
@@ -85,8 +85,8 @@ RouteState route_state(void* ws, const Layout& L) {
   rs.slot_w = at<float>(ws, L.slot_w);
   rs.counts = at<int32_t>(ws, L.counts);
   rs.offsets = at<int32_t>(ws, L.offsets);
-  rs.active = at<int32_t>(ws, L.active);
-  rs.n_active = at<int32_t>(ws, L.n_active);
+  rs.work = at<int2>(ws, L.work);
+  rs.n_work = at<int32_t>(ws, L.n_work);
   rs.row2slot = at<int32_t>(ws, L.row2slot);
   rs.status = at<uint32_t>(ws, L.status);
   return rs;
@@ -216,7 +216,12 @@ int run_experts(const moe_cfg_t* c, const void* x, int T, const moe_experts_t* e
                 const moe_shared_t* sh, void* y, const Layout& L, void* ws, cudaStream_t s) {
   const RouteState rs = route_state(ws, L);
   const ExpertParams p = expert_params(c, e, sh);
-  MOE_CUDA(launch_permute(rs, L.S, L.E1, s));
+  // Token chunks of 8 per work item: one while experts average at most 4 tokens,
+  // else four.
+  const int chunks = 4LL * T * c->top_k <= 16LL * c->n_experts ? 1 : 4;
+  const int tpg = 8 * chunks;
+  const int max_items = L.E1 + (L.S + tpg - 1) / tpg;
+  MOE_CUDA(launch_permute(rs, L.S, L.E1, tpg, s));
   MOE_CUDA(mark_phase(3, s));
   uint16_t* h = at<uint16_t>(ws, L.h);
   float* Y = at<float>(ws, L.Y);
@@ -224,9 +229,10 @@ int run_experts(const moe_cfg_t* c, const void* x, int T, const moe_experts_t* e
   // kernels take over the prefill path as they land.
   (void)path_for(c, T);
   MOE_CUDA(launch_gateup_decode(p, c->wfmt, c->interleaved_gate_up, rs,
-                                static_cast<const uint16_t*>(x), L.K, h, L.ldh, L.E1, s));
+                                static_cast<const uint16_t*>(x), L.K, h, L.ldh, max_items, chunks,
+                                s));
   MOE_CUDA(mark_phase(4, s));
-  MOE_CUDA(launch_down_decode(p, c->wfmt, rs, h, L.ldh, Y, L.E1, s));
+  MOE_CUDA(launch_down_decode(p, c->wfmt, rs, h, L.ldh, Y, max_items, chunks, s));
   MOE_CUDA(mark_phase(5, s));
   MOE_CUDA(launch_combine(Y, rs.slot_w, rs.slot_expert, T, L.K, c->d_model, L.E1, y,
                           c->y_fp32 != 0, s));

@@ -1,5 +1,9 @@
-// Group token slots by expert: histogram, exclusive scan, active-expert list and
-// the permuted-row -> slot map, in one CTA.
+// Group token slots by expert: histogram, exclusive scan, the work list of the
+// expert kernels and the permuted-row -> slot map, in one CTA.
+//
+// Work items split each expert's rows into groups of at most `tpg` rows, so that
+// an expert chosen by many tokens (the shared expert is chosen by all of them) is
+// spread over many CTAs instead of one CTA making many passes over its weights.
 //
 // This is the "expert-grouped batching" that the qwen35moe forward-pass design
 // ("Batched prefill", remaining levers) names as the way for tokens that share
@@ -53,7 +57,8 @@ __device__ __forceinline__ int2 block_exclusive_scan2(int2 val, int2* warp_tot, 
   return make_int2(base.x + inc.x - val.x, base.y + inc.y - val.y);
 }
 
-__global__ void __launch_bounds__(kPermuteThreads) permute_kernel(RouteState rs, int S, int E1) {
+__global__ void __launch_bounds__(kPermuteThreads)
+permute_kernel(RouteState rs, int S, int E1, int tpg) {
   __shared__ int cnt[2 * kPermuteThreads];
   __shared__ int cursor[2 * kPermuteThreads];
   __shared__ int2 warp_tot[32];
@@ -74,25 +79,26 @@ __global__ void __launch_bounds__(kPermuteThreads) permute_kernel(RouteState rs,
   }
   __syncthreads();
 
-  // Exclusive scan of (count, count > 0) over the virtual experts.
+  // Exclusive scan of (rows, work items) over the virtual experts.
   const int v0 = 2 * tid, v1 = 2 * tid + 1;
   const int c0 = v0 < E1 ? cnt[v0] : 0, c1 = v1 < E1 ? cnt[v1] : 0;
-  const int2 ex = block_exclusive_scan2(make_int2(c0 + c1, (c0 > 0) + (c1 > 0)), warp_tot, &total);
+  const int i0 = (c0 + tpg - 1) / tpg, i1 = (c1 + tpg - 1) / tpg;
+  const int2 ex = block_exclusive_scan2(make_int2(c0 + c1, i0 + i1), warp_tot, &total);
   if (v0 < E1) {
     cursor[v0] = ex.x;
     rs.offsets[v0] = ex.x;
     rs.counts[v0] = c0;
-    if (c0 > 0) rs.active[ex.y] = v0;
+    for (int j = 0; j < i0; ++j) rs.work[ex.y + j] = make_int2(v0, j * tpg);
   }
   if (v1 < E1) {
     cursor[v1] = ex.x + c0;
     rs.offsets[v1] = ex.x + c0;
     rs.counts[v1] = c1;
-    if (c1 > 0) rs.active[ex.y + (c0 > 0)] = v1;
+    for (int j = 0; j < i1; ++j) rs.work[ex.y + i0 + j] = make_int2(v1, j * tpg);
   }
   if (tid == 0) {
     rs.offsets[E1] = total.x;
-    *rs.n_active = total.y;
+    *rs.n_work = total.y;
   }
   __syncthreads();
 
@@ -119,8 +125,8 @@ __global__ void __launch_bounds__(kPermuteThreads) permute_kernel(RouteState rs,
 
 }  // namespace
 
-cudaError_t launch_permute(const RouteState& rs, int S, int E1, cudaStream_t s) {
-  permute_kernel<<<1, kPermuteThreads, 0, s>>>(rs, S, E1);
+cudaError_t launch_permute(const RouteState& rs, int S, int E1, int tpg, cudaStream_t s) {
+  permute_kernel<<<1, kPermuteThreads, 0, s>>>(rs, S, E1, tpg);
   return cudaGetLastError();
 }
 

@@ -11,49 +11,71 @@
 namespace moe {
 namespace {
 
-constexpr int kLogitWarps = 4;            // warps per CTA; each owns 8 expert columns
+constexpr int kLogitWarps = 8;            // warps per CTA; they split the k steps
 constexpr int kLogitTokens = 16;          // tokens per CTA (MMA M)
+constexpr int kLogitExperts = 32;         // experts per CTA (4 MMA N tiles of 8)
 
-// One CTA: 16 tokens x 32 experts (4 warps x 8).  Operands go straight from
-// global memory into MMA fragments: lane (g, c) loads the 16 bytes at
-// k + 8c of its rows, and the two MMAs of a 32-wide k step consume words {0,1}
-// and {2,3} of those bytes (the same reordering of k on both operands, so the
-// dot products are unchanged).
+// One CTA: 16 tokens x 32 experts.  Warp w takes the 32-wide k steps w, w+8, ...
+// and accumulates all four 8-expert tiles, reusing its token fragment; the eight
+// partial sums are then added in shared memory.  Operands go straight from global
+// memory into MMA fragments: lane (g, c) loads the 16 bytes at k + 8c of its rows,
+// and the two MMAs of a k step consume words {0,1} and {2,3} of those bytes (the
+// same reordering of k on both operands, so the dot products are unchanged).
 __global__ void __launch_bounds__(kLogitWarps * 32)
 router_logits_kernel(const uint16_t* __restrict__ x, int T, int d, const uint16_t* __restrict__ w_r,
                      const uint16_t* __restrict__ bias, const uint16_t* __restrict__ wsh, int E,
                      float* __restrict__ logits, int ldl) {
+  __shared__ float part[kLogitWarps][kLogitTokens][kLogitExperts + 1];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, c = lane & 3;
   const int t0 = blockIdx.x * kLogitTokens;
-  const int e0 = blockIdx.y * (kLogitWarps * 8) + warp * 8;
+  const int e0 = blockIdx.y * kLogitExperts;
   const int E1 = E + (wsh ? 1 : 0);
-  if (e0 >= E1) return;
 
   const int ta = t0 + g, tb = t0 + g + 8;
   const uint16_t* xa = ta < T ? x + (size_t)ta * d : nullptr;
   const uint16_t* xb = tb < T ? x + (size_t)tb * d : nullptr;
-  const int eb = e0 + g;
-  const uint16_t* wrow = eb < E ? w_r + (size_t)eb * d : (eb == E && wsh ? wsh : nullptr);
-
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll 4
-  for (int k = 0; k < d; k += 32) {
-    const int o = k + 8 * c;
-    uint4 a_lo = xa ? ldg_nc_v4(xa + o) : z;
-    uint4 a_hi = xb ? ldg_nc_v4(xb + o) : z;
-    uint4 b = wrow ? ldg_nc_v4(wrow + o) : z;
-    mma_bf16_16816(acc, a_lo.x, a_hi.x, a_lo.y, a_hi.y, b.x, b.y);
-    mma_bf16_16816(acc, a_lo.z, a_hi.z, a_lo.w, a_hi.w, b.z, b.w);
-  }
-  // acc: (token g, expert 2c), (g, 2c+1), (g+8, 2c), (g+8, 2c+1)
+  const uint16_t* wrow[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int t = (i < 2) ? ta : tb;
-    const int e = e0 + 2 * c + (i & 1);
+  for (int n = 0; n < 4; ++n) {
+    const int e = e0 + 8 * n + g;
+    wrow[n] = e < E ? w_r + (size_t)e * d : (e == E && wsh ? wsh : nullptr);
+  }
+
+  float acc[4][4];
+#pragma unroll
+  for (int n = 0; n < 4; ++n)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[n][q] = 0.f;
+  const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll 2
+  for (int k = warp * 32; k < d; k += kLogitWarps * 32) {
+    const int o = k + 8 * c;
+    const uint4 a_lo = xa ? ldg_nc_v4(xa + o) : z;
+    const uint4 a_hi = xb ? ldg_nc_v4(xb + o) : z;
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+      const uint4 b = wrow[n] ? ldg_nc_v4(wrow[n] + o) : z;
+      mma_bf16_16816(acc[n], a_lo.x, a_hi.x, a_lo.y, a_hi.y, b.x, b.y);
+      mma_bf16_16816(acc[n], a_lo.z, a_hi.z, a_lo.w, a_hi.w, b.z, b.w);
+    }
+  }
+  // acc[n]: (token g, expert 8n+2c), (g, 8n+2c+1), (g+8, 8n+2c), (g+8, 8n+2c+1)
+#pragma unroll
+  for (int n = 0; n < 4; ++n) {
+    part[warp][g][8 * n + 2 * c] = acc[n][0];
+    part[warp][g][8 * n + 2 * c + 1] = acc[n][1];
+    part[warp][g + 8][8 * n + 2 * c] = acc[n][2];
+    part[warp][g + 8][8 * n + 2 * c + 1] = acc[n][3];
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < kLogitTokens * kLogitExperts; i += kLogitWarps * 32) {
+    const int tt = i / kLogitExperts, ee = i % kLogitExperts;
+    const int t = t0 + tt, e = e0 + ee;
     if (t < T && e < E1) {
-      float v = acc[i];
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < kLogitWarps; ++w) v += part[w][tt][ee];
       if (e < E && bias) v += bf16_to_f32(bias[e]);
       logits[(size_t)t * ldl + e] = v;
     }
@@ -177,7 +199,7 @@ cudaError_t launch_router_logits(const uint16_t* x, int T, int d, const uint16_t
                                  const uint16_t* bias, const uint16_t* wsh, int E, float* logits,
                                  int ldl, cudaStream_t s) {
   const int E1 = E + (wsh ? 1 : 0);
-  dim3 grid((T + kLogitTokens - 1) / kLogitTokens, (E1 + kLogitWarps * 8 - 1) / (kLogitWarps * 8));
+  dim3 grid((T + kLogitTokens - 1) / kLogitTokens, (E1 + kLogitExperts - 1) / kLogitExperts);
   router_logits_kernel<<<grid, kLogitWarps * 32, 0, s>>>(x, T, d, w_r, bias, wsh, E, logits, ldl);
   return cudaGetLastError();
 }
