@@ -66,10 +66,11 @@ __device__ __forceinline__ uint32_t fp4_frag(const uint4& w, const Fp4Scale& sc)
 // Eight MMAs of one MXFP4 k group for both tiles and all token chunks.
 // W[0..3] are the lane's blocks of rows (tile0 row g, tile0 row g+8, tile1 row g,
 // tile1 row g+8); xo is the byte offset of the block's 32 inputs in a token row.
-template <bool TWO, int CH>
+template <bool TWO, int CH, bool LO>
 __device__ __forceinline__ void fp4_group_mma(const uint4 (&W)[4], const Fp4Scale (&S)[4],
                                               const uint8_t* const (&br)[CH], int nch,
-                                              bool ok, size_t xo, float (&acc)[2][CH][4]) {
+                                              bool ok, size_t xo, float (&acc)[2][CH][4],
+                                              size_t lo_off) {
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     uint32_t a[2][4];
@@ -90,6 +91,12 @@ __device__ __forceinline__ void fp4_group_mma(const uint4 (&W)[4], const Fp4Scal
         if (ok && br[ch]) b = *reinterpret_cast<const uint2*>(br[ch] + xo + 8 * j);
         mma_bf16_16816(acc[0][ch], a[0][0], a[0][1], a[0][2], a[0][3], b.x, b.y);
         mma_bf16_16816(acc[1][ch], a[1][0], a[1][1], a[1][2], a[1][3], b.x, b.y);
+        if (LO) {
+          uint2 l = make_uint2(0, 0);
+          if (ok && br[ch]) l = *reinterpret_cast<const uint2*>(br[ch] + lo_off + xo + 8 * j);
+          mma_bf16_16816(acc[0][ch], a[0][0], a[0][1], a[0][2], a[0][3], l.x, l.y);
+          mma_bf16_16816(acc[1][ch], a[1][0], a[1][1], a[1][2], a[1][3], l.x, l.y);
+        }
       }
     }
   }
@@ -99,11 +106,13 @@ __device__ __forceinline__ void fp4_group_mma(const uint4 (&W)[4], const Fp4Scal
 // R[2i+1] as MMA rows g / g+8) times token chunk ch, over Kin inputs.
 // R: byte pointers to the lane's 4 weight rows; Sc: their MXFP4 scale rows;
 // br: byte pointers to the token rows (bf16) of the lane's B column per chunk.
-template <int WFMT, int CH>
+// LO: the token operand is an (hi, lo) bf16 pair whose lo half sits lo_off bytes
+// after the hi half in each row; both halves are multiplied by the same weights.
+template <int WFMT, int CH, bool LO>
 __device__ __forceinline__ void stream_rows(const uint8_t* const (&R)[4],
                                             const uint8_t* const (&Sc)[4], int Kin, int c,
                                             const uint8_t* const (&br)[CH], int nch,
-                                            float (&acc)[2][CH][4]) {
+                                            float (&acc)[2][CH][4], size_t lo_off) {
   const uint4 z = make_uint4(0, 0, 0, 0);
   if (WFMT == MOE_WFMT_BF16) {
     constexpr int P = kDepthBf16;
@@ -134,6 +143,13 @@ __device__ __forceinline__ void stream_rows(const uint8_t* const (&R)[4],
               mma_bf16_16816(acc[0][ch], w0.z, w1.z, w0.w, w1.w, b.z, b.w);
               mma_bf16_16816(acc[1][ch], w2.x, w3.x, w2.y, w3.y, b.x, b.y);
               mma_bf16_16816(acc[1][ch], w2.z, w3.z, w2.w, w3.w, b.z, b.w);
+              if (LO) {
+                const uint4 l = br[ch] ? ldg_nc_v4(br[ch] + lo_off + o) : z;
+                mma_bf16_16816(acc[0][ch], w0.x, w1.x, w0.y, w1.y, l.x, l.y);
+                mma_bf16_16816(acc[0][ch], w0.z, w1.z, w0.w, w1.w, l.z, l.w);
+                mma_bf16_16816(acc[1][ch], w2.x, w3.x, w2.y, w3.y, l.x, l.y);
+                mma_bf16_16816(acc[1][ch], w2.z, w3.z, w2.w, w3.w, l.z, l.w);
+              }
             }
           }
         }
@@ -179,9 +195,9 @@ __device__ __forceinline__ void stream_rows(const uint8_t* const (&R)[4],
           for (int r = 0; r < 4; ++r) sc[r] = fp4_scale(cs[r]);
           const bool big = (cs[0] | cs[1] | cs[2] | cs[3]) > 128u;   // any scale > 128
           if (__any_sync(0xffffffffu, big))
-            fp4_group_mma<true, CH>(cw, sc, br, nch, ok, (size_t)blk * 64, acc);
+            fp4_group_mma<true, CH, LO>(cw, sc, br, nch, ok, (size_t)blk * 64, acc, lo_off);
           else
-            fp4_group_mma<false, CH>(cw, sc, br, nch, ok, (size_t)blk * 64, acc);
+            fp4_group_mma<false, CH, LO>(cw, sc, br, nch, ok, (size_t)blk * 64, acc, lo_off);
         }
       }
     }
@@ -269,7 +285,7 @@ gateup_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__
     }
     float acc[2][CH][4];
     zero_acc(acc);
-    stream_rows<WFMT, CH>(R, Sc, d, c, br, nch, acc);
+    stream_rows<WFMT, CH, false>(R, Sc, d, c, br, nch, acc, 0);
 
     // Epilogue: bias, activation, bf16 h rows (permuted order).
 #pragma unroll
@@ -284,7 +300,11 @@ gateup_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__
             const float uv = acc[i][ch][2 + q] + bias_u[i];
             const float hv = act == MOE_ACT_SWIGLU ? act_swiglu(gv, uv)
                                                    : act_clamped(gv, uv, p.limit, p.alpha);
-            h[(size_t)(r0 + ti) * ldh + fs[i]] = f32_to_bf16(hv);
+            // h as a pair of bf16 (hi, lo = bf16(h - hi)): ~16 significant bits
+            const uint16_t hi = f32_to_bf16(hv);
+            uint16_t* hr = h + (size_t)(r0 + ti) * 2 * ldh + fs[i];
+            hr[0] = hi;
+            hr[ldh] = f32_to_bf16(hv - bf16_to_f32(hi));
           }
         }
       }
@@ -341,12 +361,12 @@ down_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__ h
 #pragma unroll
     for (int ch = 0; ch < CH; ++ch) {
       const int i = p0 + 8 * ch + g;
-      br[ch] = (ch < nch && i < cnt) ? reinterpret_cast<const uint8_t*>(h + (size_t)(r0 + i) * ldh)
+      br[ch] = (ch < nch && i < cnt) ? reinterpret_cast<const uint8_t*>(h + (size_t)(r0 + i) * 2 * ldh)
                                      : nullptr;
     }
     float acc[2][CH][4];
     zero_acc(acc);
-    stream_rows<WFMT, CH>(R, Sc, Kin, c, br, nch, acc);
+    stream_rows<WFMT, CH, true>(R, Sc, Kin, c, br, nch, acc, (size_t)ldh * 2);
 
 #pragma unroll
     for (int ch = 0; ch < CH; ++ch) {

@@ -1,0 +1,556 @@
+// Prefill path: grouped GEMMs on the 5th-generation tensor cores (tcgen05, TMEM
+// accumulators) fed by TMA through an mbarrier pipeline.
+//
+// Per expert e with rows (tokens, in the grouped order of the permute kernel):
+//   gate_up:  h[r, f] = act(X_r . G_e[f], X_r . U_e[f])       A = X rows, B = weights
+//   down   :  Y[slot(r), o] = h_r . D_e[o] (+ b_e[o])
+// Both are D[128 x N] = A[128 x K] . B[N x K]^T with both operands K-major, the
+// natural layouts of activations and of row = output weights.
+//
+// One persistent CTA per SM walks the tiles (m tile of 128 rows of one expert,
+// n tile of N output columns), n-tile-major so that concurrently running CTAs
+// share the same weight tiles through L2.  Warp roles:
+//   warp 0      TMA producer: A and B tiles of 64 k (128-byte rows, 128-byte
+//               swizzle) into a 4-stage shared-memory ring;
+//   warp 1      owns TMEM (two accumulators of up to 256 fp32 columns) and issues
+//               tcgen05.mma (M 128, N <= 256, K 16) from one thread, committing
+//               each stage back to the producer and each finished tile to the
+//               epilogue;
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator row that their TMEM lane
+//               quarter holds, bias + activation (gate_up) or bias (down), stores.
+// Every mbarrier wait is bounded; a wait that gives up sets the device status
+// and an abort flag, the CTA drains its copies and MMAs in flight, frees TMEM and
+// returns.
+//
+// Sources: "qwen35moe - Forward-Pass Design", sections "Shared-expert MoE FFN" and
+// "Batched prefill" (expert-grouped batching: tokens that share an expert stream
+// its weights once); "Phase 19: MoE - gpt-oss-20b", section 2 Experts.
+#include <cuda.h>
+
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kBM = 128;                         // rows per tile (MMA M)
+constexpr int kBK = 64;                          // k per stage: 128 bytes of bf16
+constexpr int kMaxN = 256;
+constexpr int kTileA = kBM * kBK * 2;            // 16 KiB
+constexpr int kTileB = kMaxN * kBK * 2;          // 32 KiB
+constexpr int kStageBytes = kTileA + kTileB;
+constexpr int kSmemBytes = kStages * kStageBytes + 1024;   // + alignment slack
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;              // two accumulators of 256 columns
+
+enum : int { kModeGateUpSplit = 0, kModeGateUpInterleaved = 1, kModeDown = 2 };
+
+struct GemmArgs {
+  RouteState rs;          // offsets, work = m tiles (expert, first row), n_work, row2slot
+  int E;                  // routed experts; v == E is the shared expert
+  int mode;               // kMode*
+  int N;                  // MMA N (B rows per tile)
+  int nt_routed, nt_shared, nt_max;   // n tiles per routed / shared expert
+  int k_routed, k_shared;             // reduction length (elements)
+  int b_rows_routed;      // rows of one routed expert in the B tensor (gate/up: ff or 2ff; down: d)
+  int nf;                 // gate_up: features per n tile (N / 2)
+  int act;
+  float limit, alpha;
+  const uint16_t* gu_bias;    // [E, 2ff] gate_up row order, or null
+  const uint16_t* dn_bias;    // [E, d] or null
+  int d, ff;
+  uint16_t* h;            // gate_up output [S, 2*ldh]: bf16 (hi, lo) halves, grouped row order
+  int ldh;                // width of each half
+  int split_k;            // down: K runs over [h_hi | h_lo] against [D | D]
+  float* Y;               // down output [S, d] (slot order)
+};
+
+struct Tile {
+  int v, row0, n, cnt, kk;    // expert, first row within it, n tile, rows in this tile, k
+  int nkc;                    // k chunks of 64 the MMA runs (2 kk/64 when split_k)
+  bool skip;
+};
+
+__device__ __forceinline__ Tile tile_at(const GemmArgs& g, int t, int n_m) {
+  Tile tl;
+  tl.n = t / n_m;
+  const int2 w = g.rs.work[t - tl.n * n_m];
+  tl.v = w.x;
+  tl.row0 = w.y;
+  const bool sh = (tl.v == g.E);
+  const int rows = g.rs.offsets[tl.v + 1] - g.rs.offsets[tl.v];
+  tl.cnt = min(kBM, rows - tl.row0);
+  tl.kk = sh ? g.k_shared : g.k_routed;
+  tl.nkc = (tl.kk / kBK) * (g.split_k ? 2 : 1);
+  tl.skip = tl.n >= (sh ? g.nt_shared : g.nt_routed);
+  return tl;
+}
+
+__device__ __forceinline__ float act_swiglu(float gt, float up) { return gt / (1.f + __expf(-gt)) * up; }
+
+__device__ __forceinline__ float act_clamped(float gt, float up, float limit, float alpha) {
+  gt = fminf(gt, limit);
+  up = fminf(fmaxf(up, -limit), limit);
+  return (up + 1.f) * gt / (1.f + __expf(-alpha * gt));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                    const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmS0,
+                    const __grid_constant__ CUtensorMap tmS1, const GemmArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], tfull_bar[2], tempty_bar[2],
+      drain_bar;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_s;
+  __shared__ int consumed_s;     // stage loads the MMA thread has waited for
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t* status = g.rs.status;
+  volatile int* abort = &abort_s;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(tc::smem_u32(&full_bar[s]), 1);
+      tc::mbar_init(tc::smem_u32(&empty_bar[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(tc::smem_u32(&tfull_bar[b]), 1);
+      tc::mbar_init(tc::smem_u32(&tempty_bar[b]), 4);
+    }
+    tc::mbar_init(tc::smem_u32(&drain_bar), 1);
+    abort_s = 0;
+    consumed_s = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::tma_prefetch_desc(&tmA);
+    tc::tma_prefetch_desc(&tmB0);
+    tc::tma_prefetch_desc(&tmS0);
+    if (g.mode == kModeGateUpSplit) {
+      tc::tma_prefetch_desc(&tmB1);
+      tc::tma_prefetch_desc(&tmS1);
+    }
+  }
+  if (warp == 1) tc::tmem_alloc(tc::smem_u32(&tmem_base_s), kTmemCols);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+  const int n_m = *g.rs.n_work;
+  const int total = n_m > 0 ? n_m * g.nt_max : 0;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (tc::elect_one()) {
+      int s = 0, issued = 0;
+      uint32_t ph = 0;
+      const uint32_t b_bytes = (uint32_t)g.N * kBK * 2;
+      for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
+        const Tile tl = tile_at(g, t, n_m);
+        if (tl.skip) continue;
+        const bool sh = (tl.v == g.E);
+        const int a_row = g.rs.offsets[tl.v] + tl.row0;
+        const int nb = (g.mode == kModeGateUpSplit) ? g.nf : g.N;
+        const int b_row = (sh ? 0 : tl.v * g.b_rows_routed) + tl.n * nb;
+        const CUtensorMap* m0 = sh ? &tmS0 : &tmB0;
+        const CUtensorMap* m1 = sh ? &tmS1 : &tmB1;
+        const int nk = tl.kk / kBK;
+        for (int kc = 0; kc < tl.nkc; ++kc) {
+          if (!tc::mbar_wait(tc::smem_u32(&empty_bar[s]), ph ^ 1, abort, status)) break;
+          const uint32_t fb = tc::smem_u32(&full_bar[s]);
+          const uint32_t sa = tc::smem_u32(smem + s * kStageBytes);
+          const uint32_t sb = sa + kTileA;
+          // split_k: chunks [nk, 2nk) read the lo half of h against the same weights
+          const int kb = kc < nk ? kc : kc - nk;
+          const int ka = kc < nk ? kc * kBK : g.ldh + (kc - nk) * kBK;
+          tc::mbar_arrive_expect_tx(fb, kTileA + b_bytes);
+          tc::tma_load_2d(sa, &tmA, ka, a_row, fb);
+          if (g.mode == kModeGateUpSplit) {
+            tc::tma_load_2d(sb, m0, kb * kBK, b_row, fb);
+            tc::tma_load_2d(sb + (uint32_t)g.nf * 128u, m1, kb * kBK, b_row, fb);
+          } else {
+            tc::tma_load_2d(sb, m0, kb * kBK, b_row, fb);
+          }
+          ++issued;
+          if (++s == kStages) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      if (*abort) {
+        // Drain: wait (bounded, regardless of the abort flag) for the loads still in flight.
+        int zero = 0;
+        volatile int* never = &zero;
+        for (int i = consumed_s; i < issued; ++i)
+          tc::mbar_wait(tc::smem_u32(&full_bar[i % kStages]), (i / kStages) & 1, never, status);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (tc::elect_one()) {
+      int s = 0, b = 0;
+      uint32_t ph = 0, aph = 0;
+      const uint32_t idesc = tc::idesc_bf16_f32(kBM, g.N);
+      bool any = false;
+      for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
+        const Tile tl = tile_at(g, t, n_m);
+        if (tl.skip) continue;
+        if (!tc::mbar_wait(tc::smem_u32(&tempty_bar[b]), aph ^ 1, abort, status)) break;
+        tc::tc_fence_after();
+        const uint32_t dt = tmem + (uint32_t)b * 256u;
+        bool ok = true;
+        for (int kc = 0; kc < tl.nkc; ++kc) {
+          if (!tc::mbar_wait(tc::smem_u32(&full_bar[s]), ph, abort, status)) {
+            ok = false;
+            break;
+          }
+          consumed_s = consumed_s + 1;
+          tc::tc_fence_after();
+          const uint32_t sa = tc::smem_u32(smem + s * kStageBytes);
+          const uint64_t ad = tc::sdesc_sw128(sa), bd = tc::sdesc_sw128(sa + kTileA);
+#pragma unroll
+          for (int j = 0; j < kBK / 16; ++j)
+            tc::umma_bf16(dt, ad + 2 * j, bd + 2 * j, idesc, (kc | j) != 0);
+          tc::umma_commit(tc::smem_u32(&empty_bar[s]));
+          any = true;
+          if (++s == kStages) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc::umma_commit(tc::smem_u32(&tfull_bar[b]));
+        if (++b == 2) {
+          b = 0;
+          aph ^= 1;
+        }
+      }
+      if (*abort && any) {
+        // Let every MMA issued so far finish before TMEM is released.
+        tc::umma_commit(tc::smem_u32(&drain_bar));
+        int zero = 0;
+        volatile int* never = &zero;
+        tc::mbar_wait(tc::smem_u32(&drain_bar), 0, never, status);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp & 3;                 // TMEM lane quarter this warp may read
+    const int row = 32 * q + lane;
+    int b = 0;
+    uint32_t aph = 0;
+    for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
+      const Tile tl = tile_at(g, t, n_m);
+      if (tl.skip) continue;
+      if (!tc::mbar_wait(tc::smem_u32(&tfull_bar[b]), aph, abort, status)) break;
+      tc::tc_fence_after();
+      const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)b * 256u;
+      const bool valid = row < tl.cnt;
+      const int grow = g.rs.offsets[tl.v] + tl.row0 + row;     // grouped row index
+      const bool sh = (tl.v == g.E);
+      if (g.mode == kModeDown) {
+        float* yrow = valid ? g.Y + (size_t)g.rs.row2slot[grow] * g.d : nullptr;
+        const int o0 = tl.n * g.N;
+        for (int c0 = 0; c0 < g.N; c0 += 32) {
+          float v[32];
+          tc::tmem_ld32(taddr + (uint32_t)c0, v);
+          if (valid) {
+            const int ncol = min(32, g.N - c0);
+            if (!sh && g.dn_bias) {
+              const uint16_t* bp = g.dn_bias + (size_t)tl.v * g.d + o0 + c0;
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i < ncol) v[i] += bf16_to_f32(bp[i]);
+            }
+            float4* dst = reinterpret_cast<float4*>(yrow + o0 + c0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (4 * i < ncol) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          }
+        }
+      } else {
+        const int f0 = tl.n * g.nf;
+        const int act = sh ? MOE_ACT_SWIGLU : g.act;
+        uint16_t* hrow = g.h + (size_t)grow * 2 * g.ldh;
+        const uint16_t* bias = (!sh && g.gu_bias) ? g.gu_bias + (size_t)tl.v * 2 * g.ff : nullptr;
+        if (g.mode == kModeGateUpSplit) {
+          // columns [0, nf) gate, [nf, 2nf) up: 32 features per step
+          for (int j0 = 0; j0 < g.nf; j0 += 32) {
+            float gv[32], uv[32];
+            tc::tmem_ld32(taddr + (uint32_t)j0, gv);
+            tc::tmem_ld32(taddr + (uint32_t)(g.nf + j0), uv);
+            if (valid) {
+              uint32_t packed[16], plo[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                float h0, h1;
+                const int f = f0 + j0 + 2 * i;
+                float ga = gv[2 * i], ua = uv[2 * i], gb = gv[2 * i + 1], ub = uv[2 * i + 1];
+                if (bias) {
+                  ga += bf16_to_f32(bias[2 * f]); ua += bf16_to_f32(bias[2 * f + 1]);
+                  gb += bf16_to_f32(bias[2 * f + 2]); ub += bf16_to_f32(bias[2 * f + 3]);
+                }
+                h0 = act == MOE_ACT_SWIGLU ? act_swiglu(ga, ua) : act_clamped(ga, ua, g.limit, g.alpha);
+                h1 = act == MOE_ACT_SWIGLU ? act_swiglu(gb, ub) : act_clamped(gb, ub, g.limit, g.alpha);
+                packed[i] = pack_bf16x2(h0, h1);
+                plo[i] = pack_bf16x2(h0 - bf16_lo(packed[i]), h1 - bf16_hi(packed[i]));
+              }
+              uint4* dst = reinterpret_cast<uint4*>(hrow + f0 + j0);
+              uint4* dlo = reinterpret_cast<uint4*>(hrow + g.ldh + f0 + j0);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+                dlo[i] = make_uint4(plo[4 * i], plo[4 * i + 1], plo[4 * i + 2], plo[4 * i + 3]);
+              }
+            }
+          }
+        } else {
+          // interleaved: column 2j gate, 2j+1 up: 16 features per step
+          for (int c0 = 0; c0 < g.N; c0 += 32) {
+            float v[32];
+            tc::tmem_ld32(taddr + (uint32_t)c0, v);
+            if (valid) {
+              uint32_t packed[8], plo[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const int f = f0 + c0 / 2 + 2 * i;
+                float ga = v[4 * i], ua = v[4 * i + 1], gb = v[4 * i + 2], ub = v[4 * i + 3];
+                if (bias) {
+                  ga += bf16_to_f32(bias[2 * f]); ua += bf16_to_f32(bias[2 * f + 1]);
+                  gb += bf16_to_f32(bias[2 * f + 2]); ub += bf16_to_f32(bias[2 * f + 3]);
+                }
+                const float h0 = act == MOE_ACT_SWIGLU ? act_swiglu(ga, ua) : act_clamped(ga, ua, g.limit, g.alpha);
+                const float h1 = act == MOE_ACT_SWIGLU ? act_swiglu(gb, ub) : act_clamped(gb, ub, g.limit, g.alpha);
+                packed[i] = pack_bf16x2(h0, h1);
+                plo[i] = pack_bf16x2(h0 - bf16_lo(packed[i]), h1 - bf16_hi(packed[i]));
+              }
+              uint4* dst = reinterpret_cast<uint4*>(hrow + f0 + c0 / 2);
+              dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+              dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+              uint4* dlo = reinterpret_cast<uint4*>(hrow + g.ldh + f0 + c0 / 2);
+              dlo[0] = make_uint4(plo[0], plo[1], plo[2], plo[3]);
+              dlo[1] = make_uint4(plo[4], plo[5], plo[6], plo[7]);
+            }
+          }
+        }
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&tempty_bar[b]));
+      if (++b == 2) {
+        b = 0;
+        aph ^= 1;
+      }
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+// Copy the x row of every grouped row into Xp (the A operand of gate_up).
+__global__ void __launch_bounds__(256)
+gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ row2slot, int S,
+                   int K, int d, uint16_t* __restrict__ xp) {
+  const int lane = threadIdx.x & 31;
+  const int nvec = d / 8;
+  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < S; r += (gridDim.x * blockDim.x) >> 5) {
+    const int t = row2slot[r] / K;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+    uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)r * d);
+    for (int i = lane; i < nvec; i += 32) dst[i] = ldg_nc_v4(src + i);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2D map over a row-major bf16 matrix [rows, cols] (row stride in bytes), box of
+// box_rows x 64 columns, 128-byte swizzle.
+bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t stride,
+                   uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || !base) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {stride};
+  const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 148;
+}
+
+// gate_up features per n tile: N = 2 nf <= 256 with nf a multiple of 16 (of 32 for
+// separate gate/up, whose epilogue reads 32 gate and 32 up columns at a time),
+// dividing ff and, with a shared expert, sff.  0 if none.
+int gateup_nf(const ExpertParams& p, int interleaved) {
+  const int step = interleaved ? 16 : 32;
+  for (int f = kMaxN / 2; f >= step; f -= step)
+    if (p.ff % f == 0 && (p.sff == 0 || p.sff % f == 0)) return f;
+  return 0;
+}
+
+void set_smem_attr() {
+  static bool done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || done[dev]) return;
+  cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  done[dev] = true;
+}
+
+}  // namespace
+
+// Largest N (multiple of 16, at most 256) that divides `rows`; 0 if none.
+int prefill_tile_n(int rows) {
+  for (int n = kMaxN; n >= 16; n -= 16)
+    if (rows % n == 0) return n;
+  return 0;
+}
+
+bool prefill_supported(int d, int ff, int sff, int wfmt, int interleaved) {
+  if (wfmt != MOE_WFMT_BF16) return false;
+  if (d % kBK || ff % kBK || (sff && sff % kBK)) return false;
+  ExpertParams p{};
+  p.d = d;
+  p.ff = ff;
+  p.sff = sff;
+  if (!gateup_nf(p, interleaved)) return false;
+  if (!prefill_tile_n(d)) return false;
+  if (sff && interleaved) return false;   // the shared expert has separate gate/up maps
+  return true;
+}
+
+cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* row2slot, int S, int K, int d,
+                               uint16_t* xp, cudaStream_t s) {
+  int blocks = (S + 7) / 8;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  if (blocks < 1) blocks = 1;
+  gather_rows_kernel<<<blocks, 256, 0, s>>>(x, row2slot, S, K, d, xp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gateup_prefill(const ExpertParams& p, int interleaved, const RouteState& rs,
+                                  const uint16_t* xp, int S, uint16_t* h, int ldh, int max_mtiles,
+                                  cudaStream_t s) {
+  const int nf = gateup_nf(p, interleaved);
+  GemmArgs g{};
+  g.rs = rs;
+  g.E = p.E;
+  g.mode = interleaved ? kModeGateUpInterleaved : kModeGateUpSplit;
+  g.N = 2 * nf;
+  g.nf = nf;
+  g.nt_routed = p.ff / nf;
+  g.nt_shared = p.sff ? p.sff / nf : 0;
+  g.nt_max = g.nt_routed > g.nt_shared ? g.nt_routed : g.nt_shared;
+  g.k_routed = p.d;
+  g.k_shared = p.d;
+  g.b_rows_routed = interleaved ? 2 * p.ff : p.ff;
+  g.act = p.act;
+  g.limit = p.limit;
+  g.alpha = p.alpha;
+  g.gu_bias = p.gu_bias;
+  g.d = p.d;
+  g.ff = p.ff;
+  g.h = h;
+  g.ldh = ldh;
+  CUtensorMap tA, tB0, tB1, tS0, tS1;
+  std::memset(&tB1, 0, sizeof(tB1));
+  std::memset(&tS0, 0, sizeof(tS0));
+  std::memset(&tS1, 0, sizeof(tS1));
+  const uint64_t rowb = (uint64_t)p.d * 2;
+  if (!make_map_bf16(&tA, xp, (uint64_t)S, p.d, rowb, kBM)) return cudaErrorInvalidValue;
+  if (interleaved) {
+    if (!make_map_bf16(&tB0, p.gate_up, (uint64_t)p.E * 2 * p.ff, p.d, rowb, g.N)) return cudaErrorInvalidValue;
+  } else {
+    if (!make_map_bf16(&tB0, p.gate, (uint64_t)p.E * p.ff, p.d, rowb, nf)) return cudaErrorInvalidValue;
+    if (!make_map_bf16(&tB1, p.up, (uint64_t)p.E * p.ff, p.d, rowb, nf)) return cudaErrorInvalidValue;
+  }
+  if (p.sff) {
+    if (!make_map_bf16(&tS0, p.sh_gate, p.sff, p.d, rowb, nf)) return cudaErrorInvalidValue;
+    if (!make_map_bf16(&tS1, p.sh_up, p.sff, p.d, rowb, nf)) return cudaErrorInvalidValue;
+  } else {
+    tS0 = tB0;
+    tS1 = interleaved ? tB0 : tB1;
+  }
+  if (interleaved) tB1 = tB0;
+  set_smem_attr();
+  long long tiles = (long long)max_mtiles * g.nt_max;
+  int grid = sm_count();
+  if (tiles < grid) grid = (int)(tiles > 0 ? tiles : 1);
+  grouped_gemm_kernel<<<grid, kThreads, kSmemBytes, s>>>(tA, tB0, tB1, tS0, tS1, g);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_down_prefill(const ExpertParams& p, const RouteState& rs, const uint16_t* h,
+                                int ldh, int S, float* Y, int max_mtiles, cudaStream_t s) {
+  GemmArgs g{};
+  g.rs = rs;
+  g.E = p.E;
+  g.mode = kModeDown;
+  g.N = prefill_tile_n(p.d);
+  g.nt_routed = p.d / g.N;
+  g.nt_shared = p.sff ? p.d / g.N : 0;
+  g.nt_max = g.nt_routed;
+  g.k_routed = p.ff;
+  g.k_shared = p.sff;
+  g.b_rows_routed = p.d;
+  g.dn_bias = p.dn_bias;
+  g.d = p.d;
+  g.Y = Y;
+  g.ldh = ldh;
+  g.split_k = 1;
+  CUtensorMap tA, tB0, tS0;
+  std::memset(&tS0, 0, sizeof(tS0));
+  if (!make_map_bf16(&tA, h, (uint64_t)S, 2 * (uint64_t)ldh, (uint64_t)ldh * 4, kBM))
+    return cudaErrorInvalidValue;
+  if (!make_map_bf16(&tB0, p.down, (uint64_t)p.E * p.d, p.ff, (uint64_t)p.ff * 2, g.N))
+    return cudaErrorInvalidValue;
+  if (p.sff) {
+    if (!make_map_bf16(&tS0, p.sh_down, p.d, p.sff, (uint64_t)p.sff * 2, g.N)) return cudaErrorInvalidValue;
+  } else {
+    tS0 = tB0;
+  }
+  set_smem_attr();
+  long long tiles = (long long)max_mtiles * g.nt_max;
+  int grid = sm_count();
+  if (tiles < grid) grid = (int)(tiles > 0 ? tiles : 1);
+  grouped_gemm_kernel<<<grid, kThreads, kSmemBytes, s>>>(tA, tB0, tB0, tS0, tS0, g);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

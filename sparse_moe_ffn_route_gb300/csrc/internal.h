@@ -90,6 +90,17 @@ cudaError_t launch_down_decode(const ExpertParams& p, int wfmt, const RouteState
                                const uint16_t* h, int ldh, float* Y, int max_items, int chunks,
                                cudaStream_t s);
 
+// Prefill path: grouped GEMMs on tcgen05 (see expert_prefill.cu).  The work list
+// must hold 128-row m tiles (permute with tpg = 128).
+bool prefill_supported(int d, int ff, int sff, int wfmt, int interleaved);
+cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* row2slot, int S, int K, int d,
+                               uint16_t* xp, cudaStream_t s);
+cudaError_t launch_gateup_prefill(const ExpertParams& p, int interleaved, const RouteState& rs,
+                                  const uint16_t* xp, int S, uint16_t* h, int ldh, int max_mtiles,
+                                  cudaStream_t s);
+cudaError_t launch_down_prefill(const ExpertParams& p, const RouteState& rs, const uint16_t* h,
+                                int ldh, int S, float* Y, int max_mtiles, cudaStream_t s);
+
 // MXFP4 [rows, n_in/32, 16] + scales -> bf16 [rows, n_in].
 cudaError_t launch_mxfp4_to_bf16(const uint8_t* blocks, const uint8_t* scales, long long rows,
                                  int n_in, uint16_t* out, cudaStream_t s);

@@ -17,9 +17,12 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 struct Layout {
   int K, E1, S, ldl, ldh;
+  bool prefill;             // the expert phase runs the tcgen05 grouped GEMMs
   size_t status, counts, offsets, work, n_work, slot_expert, slot_w, row2slot, logits, h, Y,
-      xstage, ystage, total;
+      xp, xstage, ystage, total;
 };
+
+int path_for(const moe_cfg_t* c, int T);
 
 int validate_cfg(const moe_cfg_t* c) {
   if (!c) return MOE_ERR_INVALID_ARG;
@@ -66,8 +69,12 @@ bool make_layout(const moe_cfg_t* c, int T, Layout* L) {
   L->slot_w = take(4 * Sz);
   L->row2slot = take(4 * Sz);
   L->logits = take(4 * Tz * (size_t)L->ldl);
-  L->h = take(2 * Sz * (size_t)L->ldh);
+  L->h = take(4 * Sz * (size_t)L->ldh);   // (hi, lo) bf16 halves
   L->Y = take(4 * Sz * d);
+  L->prefill = path_for(c, T) == MOE_PATH_PREFILL &&
+               prefill_supported(c->d_model, c->expert_ff, c->shared_ff, c->wfmt,
+                                 c->interleaved_gate_up);
+  L->xp = take(L->prefill ? 2 * Sz * d : 0);
   L->xstage = take(2 * Tz * d);
   L->ystage = take(4 * Tz * d);
   L->total = off;
@@ -216,6 +223,26 @@ int run_experts(const moe_cfg_t* c, const void* x, int T, const moe_experts_t* e
                 const moe_shared_t* sh, void* y, const Layout& L, void* ws, cudaStream_t s) {
   const RouteState rs = route_state(ws, L);
   const ExpertParams p = expert_params(c, e, sh);
+  uint16_t* h = at<uint16_t>(ws, L.h);
+  float* Y = at<float>(ws, L.Y);
+  if (L.prefill) {
+    // Grouped GEMMs on tcgen05: m tiles of 128 rows; A rows of gate_up gathered first.
+    constexpr int kTileRows = 128;
+    const int max_mtiles = L.E1 + (L.S + kTileRows - 1) / kTileRows;
+    uint16_t* xp = at<uint16_t>(ws, L.xp);
+    MOE_CUDA(launch_permute(rs, L.S, L.E1, kTileRows, s));
+    MOE_CUDA(launch_gather_rows(static_cast<const uint16_t*>(x), rs.row2slot, L.S, L.K,
+                                c->d_model, xp, s));
+    MOE_CUDA(mark_phase(3, s));
+    MOE_CUDA(launch_gateup_prefill(p, c->interleaved_gate_up, rs, xp, L.S, h, L.ldh, max_mtiles, s));
+    MOE_CUDA(mark_phase(4, s));
+    MOE_CUDA(launch_down_prefill(p, rs, h, L.ldh, L.S, Y, max_mtiles, s));
+    MOE_CUDA(mark_phase(5, s));
+    MOE_CUDA(launch_combine(Y, rs.slot_w, rs.slot_expert, T, L.K, c->d_model, L.E1, y,
+                            c->y_fp32 != 0, s));
+    MOE_CUDA(mark_phase(6, s));
+    return MOE_OK;
+  }
   // Token chunks of 8 per work item: one while experts average at most 4 tokens,
   // else four.
   const int chunks = 4LL * T * c->top_k <= 16LL * c->n_experts ? 1 : 4;
@@ -223,11 +250,6 @@ int run_experts(const moe_cfg_t* c, const void* x, int T, const moe_experts_t* e
   const int max_items = L.E1 + (L.S + tpg - 1) / tpg;
   MOE_CUDA(launch_permute(rs, L.S, L.E1, tpg, s));
   MOE_CUDA(mark_phase(3, s));
-  uint16_t* h = at<uint16_t>(ws, L.h);
-  float* Y = at<float>(ws, L.Y);
-  // Both paths run the weight-streaming kernels for now; the grouped-GEMM
-  // kernels take over the prefill path as they land.
-  (void)path_for(c, T);
   MOE_CUDA(launch_gateup_decode(p, c->wfmt, c->interleaved_gate_up, rs,
                                 static_cast<const uint16_t*>(x), L.K, h, L.ldh, max_items, chunks,
                                 s));

@@ -11,71 +11,96 @@
 namespace moe {
 namespace {
 
-constexpr int kLogitWarps = 8;            // warps per CTA; they split the k steps
-constexpr int kLogitTokens = 16;          // tokens per CTA (MMA M)
-constexpr int kLogitExperts = 32;         // experts per CTA (4 MMA N tiles of 8)
-
-// One CTA: 16 tokens x 32 experts.  Warp w takes the 32-wide k steps w, w+8, ...
-// and accumulates all four 8-expert tiles, reusing its token fragment; the eight
-// partial sums are then added in shared memory.  Operands go straight from global
-// memory into MMA fragments: lane (g, c) loads the 16 bytes at k + 8c of its rows,
-// and the two MMAs of a k step consume words {0,1} and {2,3} of those bytes (the
-// same reordering of k on both operands, so the dot products are unchanged).
-__global__ void __launch_bounds__(kLogitWarps * 32)
+// Router logits kernel, one CTA per (16*MT tokens) x (8*NT experts) tile.  Its
+// WARPS warps split the 32-wide k steps (warp w takes steps w, w+WARPS, ...) and
+// each accumulates the whole tile, reusing every loaded fragment MT or NT times;
+// the partial sums are then added in shared memory in a fixed order, so logits
+// are bit-reproducible.  A warp issues the loads of up to STEPS of its k steps
+// before its first MMA, which at decode sizes covers all of them.
+//
+// Operands go straight from global memory into MMA fragments: lane (g, c) loads
+// the 16 bytes at k + 8c of its rows, and the two MMAs of a k step consume words
+// {0,1} and {2,3} of those bytes (the same reordering of k on both operands, so
+// the dot products are unchanged).
+template <int MT, int NT, int WARPS, int STEPS>
+__global__ void __launch_bounds__(WARPS * 32)
 router_logits_kernel(const uint16_t* __restrict__ x, int T, int d, const uint16_t* __restrict__ w_r,
                      const uint16_t* __restrict__ bias, const uint16_t* __restrict__ wsh, int E,
                      float* __restrict__ logits, int ldl) {
-  __shared__ float part[kLogitWarps][kLogitTokens][kLogitExperts + 1];
+  constexpr int TM = 16 * MT, TN = 8 * NT;
+  __shared__ float part[WARPS][TM][TN + 1];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, c = lane & 3;
-  const int t0 = blockIdx.x * kLogitTokens;
-  const int e0 = blockIdx.y * kLogitExperts;
+  const int t0 = blockIdx.x * TM;
+  const int e0 = blockIdx.y * TN;
   const int E1 = E + (wsh ? 1 : 0);
 
-  const int ta = t0 + g, tb = t0 + g + 8;
-  const uint16_t* xa = ta < T ? x + (size_t)ta * d : nullptr;
-  const uint16_t* xb = tb < T ? x + (size_t)tb * d : nullptr;
-  const uint16_t* wrow[4];
+  const uint16_t* xr[MT][2];
 #pragma unroll
-  for (int n = 0; n < 4; ++n) {
+  for (int m = 0; m < MT; ++m)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int t = t0 + 16 * m + 8 * hh + g;
+      xr[m][hh] = t < T ? x + (size_t)t * d : nullptr;
+    }
+  const uint16_t* wrow[NT];
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
     const int e = e0 + 8 * n + g;
     wrow[n] = e < E ? w_r + (size_t)e * d : (e == E && wsh ? wsh : nullptr);
   }
 
-  float acc[4][4];
+  float acc[MT][NT][4];
 #pragma unroll
-  for (int n = 0; n < 4; ++n)
+  for (int m = 0; m < MT; ++m)
 #pragma unroll
-    for (int q = 0; q < 4; ++q) acc[n][q] = 0.f;
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[m][n][q] = 0.f;
   const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll 2
-  for (int k = warp * 32; k < d; k += kLogitWarps * 32) {
-    const int o = k + 8 * c;
-    const uint4 a_lo = xa ? ldg_nc_v4(xa + o) : z;
-    const uint4 a_hi = xb ? ldg_nc_v4(xb + o) : z;
+  const int nk = d >> 5;
+  for (int s0 = warp; s0 < nk; s0 += WARPS * STEPS) {
+    uint4 A[STEPS][MT][2], B[STEPS][NT];
 #pragma unroll
-    for (int n = 0; n < 4; ++n) {
-      const uint4 b = wrow[n] ? ldg_nc_v4(wrow[n] + o) : z;
-      mma_bf16_16816(acc[n], a_lo.x, a_hi.x, a_lo.y, a_hi.y, b.x, b.y);
-      mma_bf16_16816(acc[n], a_lo.z, a_hi.z, a_lo.w, a_hi.w, b.z, b.w);
+    for (int s = 0; s < STEPS; ++s) {
+      const int ks = s0 + s * WARPS;
+      const int o = ks * 32 + 8 * c;
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) A[s][m][hh] = (ks < nk && xr[m][hh]) ? ldg_nc_v4(xr[m][hh] + o) : z;
+#pragma unroll
+      for (int n = 0; n < NT; ++n) B[s][n] = (ks < nk && wrow[n]) ? ldg_nc_v4(wrow[n] + o) : z;
     }
-  }
-  // acc[n]: (token g, expert 8n+2c), (g, 8n+2c+1), (g+8, 8n+2c), (g+8, 8n+2c+1)
 #pragma unroll
-  for (int n = 0; n < 4; ++n) {
-    part[warp][g][8 * n + 2 * c] = acc[n][0];
-    part[warp][g][8 * n + 2 * c + 1] = acc[n][1];
-    part[warp][g + 8][8 * n + 2 * c] = acc[n][2];
-    part[warp][g + 8][8 * n + 2 * c + 1] = acc[n][3];
+    for (int s = 0; s < STEPS; ++s)
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          const uint4 &a0 = A[s][m][0], &a1 = A[s][m][1], &b = B[s][n];
+          mma_bf16_16816(acc[m][n], a0.x, a1.x, a0.y, a1.y, b.x, b.y);
+          mma_bf16_16816(acc[m][n], a0.z, a1.z, a0.w, a1.w, b.z, b.w);
+        }
   }
+  // acc[m][n]: (token 16m+g, expert 8n+2c), (.., 8n+2c+1), (16m+g+8, 8n+2c), (.., 8n+2c+1)
+#pragma unroll
+  for (int m = 0; m < MT; ++m)
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      part[warp][16 * m + g][8 * n + 2 * c] = acc[m][n][0];
+      part[warp][16 * m + g][8 * n + 2 * c + 1] = acc[m][n][1];
+      part[warp][16 * m + g + 8][8 * n + 2 * c] = acc[m][n][2];
+      part[warp][16 * m + g + 8][8 * n + 2 * c + 1] = acc[m][n][3];
+    }
   __syncthreads();
-  for (int i = threadIdx.x; i < kLogitTokens * kLogitExperts; i += kLogitWarps * 32) {
-    const int tt = i / kLogitExperts, ee = i % kLogitExperts;
+  for (int i = threadIdx.x; i < TM * TN; i += WARPS * 32) {
+    const int tt = i / TN, ee = i % TN;
     const int t = t0 + tt, e = e0 + ee;
     if (t < T && e < E1) {
       float v = 0.f;
 #pragma unroll
-      for (int w = 0; w < kLogitWarps; ++w) v += part[w][tt][ee];
+      for (int w = 0; w < WARPS; ++w) v += part[w][tt][ee];
       if (e < E && bias) v += bf16_to_f32(bias[e]);
       logits[(size_t)t * ldl + e] = v;
     }
@@ -199,8 +224,13 @@ cudaError_t launch_router_logits(const uint16_t* x, int T, int d, const uint16_t
                                  const uint16_t* bias, const uint16_t* wsh, int E, float* logits,
                                  int ldl, cudaStream_t s) {
   const int E1 = E + (wsh ? 1 : 0);
-  dim3 grid((T + kLogitTokens - 1) / kLogitTokens, (E1 + kLogitExperts - 1) / kLogitExperts);
-  router_logits_kernel<<<grid, kLogitWarps * 32, 0, s>>>(x, T, d, w_r, bias, wsh, E, logits, ldl);
+  if (T <= 256) {   // latency-bound: many small CTAs, all loads of a warp in flight at once
+    dim3 grid((T + 15) / 16, (E1 + 15) / 16);
+    router_logits_kernel<1, 2, 16, 6><<<grid, 16 * 32, 0, s>>>(x, T, d, w_r, bias, wsh, E, logits, ldl);
+  } else {          // throughput-bound: larger tiles, fewer re-reads of x and W_r from L2
+    dim3 grid((T + 63) / 64, (E1 + 31) / 32);
+    router_logits_kernel<4, 4, 4, 2><<<grid, 4 * 32, 0, s>>>(x, T, d, w_r, bias, wsh, E, logits, ldl);
+  }
   return cudaGetLastError();
 }
 

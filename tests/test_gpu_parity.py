@@ -274,3 +274,75 @@ def test_full_workload(name, full_layers):
     xh = x.cpu().pin_memory()
     yh = moe.moe_ffn_forward_host(c, xh, router, experts, shared, ws=ws)
     assert torch.equal(yh.view(torch.int16), y.cpu().view(torch.int16))
+
+
+# ----------------------------------------------------------------------------- prefill (tcgen05) path
+PREFILL_SPECS = [
+    mi.small_spec("qwen", 128, 8, 2, 64, 64, 200),
+    mi.small_spec("qwen", 256, 16, 4, 128, 128, 300, bias=("normal", 0.5)),
+    mi.small_spec("qwen", 512, 8, 3, 256, 0, 333, expert_weights_scale=1.5),
+    mi.small_spec("qwen", 192, 4, 4, 320, 64, 129),                            # E == k, N 192
+]
+
+
+@pytest.mark.parametrize("spec", PREFILL_SPECS, ids=lambda s: s.name)
+@pytest.mark.parametrize("path", [1, 2], ids=["decode", "prefill"])
+def test_layer_paths_match_oracle(spec, path):
+    moe = moe_lib()
+    lay = mi.make_layer(spec)
+    g = oracle.gating_for(spec)
+    ref = oracle.forward(g, lay)
+    x, router, experts, shared = upload(lay)
+    c = cfg_for(spec, path=path)
+    T, k = spec.tokens, spec.top_k
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    ws = moe.workspace(c, T)
+    y16 = moe.moe_ffn_forward(c, x, router, experts, shared, topk_ids=ids, ws=ws)
+    y32 = moe.moe_ffn_forward(c.replace(y_fp32=1), x, router, experts, shared, ws=ws)
+    st, bits = moe.moe_device_status(ws)
+    assert st == 0, bits
+    ids_g = ids.cpu().numpy()
+    diff = np.any(ids_g != ref.ids, axis=1)
+    assert not np.any(diff & ~oracle.near_tie_tokens(ref.logits, ref.ids))
+    if np.any(diff):
+        ref = oracle.forward(g, lay, forced_ids=np.where(diff[:, None], ids_g, ref.ids))
+    check_outputs(y32, y16, ref.y, f"{spec.name} path {path}")
+
+
+def test_prefill_interleaved_bf16_clamped():
+    moe = moe_lib()
+    spec = mi.small_spec("qwen", 128, 8, 2, 192, 0, 150, bias=("normal", 0.3))
+    lay = _interleaved_bf16(spec)
+    g = oracle.Gating(128, 8, 2, 192, 0, gating=1, act=1, wfmt=0, interleaved=1)
+    ref = oracle.forward(g, lay)
+    x, router, experts, shared = upload(lay)
+    c = moe.qwen_cfg(128, 8, 2, 192, 0).replace(gating=1, act=1, interleaved_gate_up=1,
+                                                 path=moe.PATH_PREFILL)
+    ids = torch.empty((150, 2), dtype=torch.int32, device="cuda")
+    y16 = moe.moe_ffn_forward(c, x, router, experts, None, topk_ids=ids)
+    y32 = moe.moe_ffn_forward(c.replace(y_fp32=1), x, router, experts, None)
+    ids_g = ids.cpu().numpy()
+    diff = np.any(ids_g != ref.ids, axis=1)
+    assert not np.any(diff & ~oracle.near_tie_tokens(ref.logits, ref.ids))
+    if np.any(diff):
+        ref = oracle.forward(g, lay, forced_ids=np.where(diff[:, None], ids_g, ref.ids))
+    check_outputs(y32, y16, ref.y, "prefill interleaved bf16")
+
+
+def test_prefill_hot_expert_many_tiles():
+    """Forced routing: every token's two slots go to experts 5 and 2 (> 2 m tiles each)."""
+    moe = moe_lib()
+    spec = mi.small_spec("qwen", 128, 8, 2, 64, 64, 300)
+    lay = mi.make_layer(spec)
+    g = oracle.gating_for(spec)
+    forced = np.tile(np.array([5, 2], np.int32), (300, 1))
+    forced[::7] = [2, 7]
+    ref = oracle.forward(g, lay, forced_ids=forced)
+    x, router, experts, shared = upload(lay)
+    c = cfg_for(spec, path=moe.PATH_PREFILL)
+    ids_d = torch.from_numpy(forced).cuda()
+    w_d = torch.from_numpy(ref.w.astype(np.float32)).cuda()
+    sg = torch.from_numpy(ref.sgate.astype(np.float32)).cuda()
+    y16 = moe.moe_ffn_forward_routed(c, x, ids_d, w_d, experts, shared, sgate=sg)
+    y32 = moe.moe_ffn_forward_routed(c.replace(y_fp32=1), x, ids_d, w_d, experts, shared, sgate=sg)
+    check_outputs(y32, y16, ref.y, "hot expert")
