@@ -39,13 +39,23 @@ namespace {
 constexpr int kStages = 4;
 constexpr int kBM = 128;                         // rows per tile (MMA M)
 constexpr int kBK = 64;                          // k per stage: 128 bytes of bf16
-constexpr int kMaxN = 256;
 constexpr int kTileA = kBM * kBK * 2;            // 16 KiB
-constexpr int kTileB = kMaxN * kBK * 2;          // 32 KiB
-constexpr int kStageBytes = kTileA + kTileB;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024;   // + alignment slack
-constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;              // two accumulators of 256 columns
+
+// Shared-memory stage of each variant.  bf16 weights: A | B.  MXFP4 weights: A |
+// B (bf16, written by the dequant warps) | packed codes (N x 32 bytes per 64 k) |
+// scales (2 x N bytes: the two 32-input blocks of the chunk).  Stages are
+// multiples of 1024 bytes so every swizzled tile starts 1024-aligned.
+template <bool FP4>
+struct Lay {
+  static constexpr int kMaxN = FP4 ? 240 : 256;
+  static constexpr int kTileB = kMaxN * kBK * 2;
+  static constexpr int kPacked = FP4 ? kMaxN * (kBK / 2) : 0;
+  static constexpr int kScales = FP4 ? 512 : 0;
+  static constexpr int kStageBytes = ((kTileA + kTileB + kPacked + kScales + 1023) / 1024) * 1024;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024;   // + alignment slack
+  static constexpr int kThreads = FP4 ? 320 : 192;                 // + 4 dequant warps
+};
 
 enum : int { kModeGateUpSplit = 0, kModeGateUpInterleaved = 1, kModeDown = 2 };
 
@@ -67,6 +77,8 @@ struct GemmArgs {
   int ldh;                // width of each half
   int split_k;            // down: K runs over [h_hi | h_lo] against [D | D]
   float* Y;               // down output [S, d] (slot order)
+  int scale_rows;         // MXFP4: rows of one expert in the transposed scales
+  int scale_nblk;         // MXFP4: 32-input blocks per weight row
 };
 
 struct Tile {
@@ -98,14 +110,40 @@ __device__ __forceinline__ float act_clamped(float gt, float up, float limit, fl
   return (up + 1.f) * gt / (1.f + __expf(-alpha * gt));
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// MXFP4 dequant of one stage: N rows x 64 inputs from packed codes (smem, [N][32])
+// and scales (smem, [2][N]) into the bf16 B tile with the 128-byte swizzle.
+// Work unit = one 16-byte output chunk (8 inputs, 4 code bytes, one scale).
+__device__ __forceinline__ void dequant_stage(const uint8_t* packed, const uint8_t* scales, uint8_t* btile,
+                                              int N, int tid, int nthreads) {
+  for (int c = tid; c < N * 8; c += nthreads) {
+    const int r = c >> 3, j = c & 7;
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(packed + r * 32 + j * 4);
+    const Fp4Scale sc = fp4_scale(scales[(j >> 2) * N + r]);
+    const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
+    uint4 o;
+    o.x = fp4_pair<0>(lo, hi, sc);
+    o.y = fp4_pair<1>(lo, hi, sc);
+    o.z = fp4_pair<2>(lo, hi, sc);
+    o.w = fp4_pair<3>(lo, hi, sc);
+    *reinterpret_cast<uint4*>(btile + r * 128 + ((j ^ (r & 7)) << 4)) = o;
+  }
+}
+
+// FP4: B comes from MXFP4 weights (tmB0: packed codes [rows, nblk*16] bytes, tmB1:
+// transposed scales [E*nblk, rows] bytes); else tmB0/tmB1 (and tmS0/tmS1 for the
+// shared expert) are bf16 weight maps.
+template <bool FP4>
+__global__ void __launch_bounds__(Lay<FP4>::kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmS0,
                     const __grid_constant__ CUtensorMap tmS1, const GemmArgs g) {
+  using L = Lay<FP4>;
+  constexpr int kStageBytes = L::kStageBytes;
+  constexpr int kTileB = L::kTileB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], tfull_bar[2], tempty_bar[2],
-      drain_bar;
+  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], bready_bar[kStages],
+      tfull_bar[2], tempty_bar[2], drain_bar;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
   __shared__ int consumed_s;     // stage loads the MMA thread has waited for
@@ -118,6 +156,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(tc::smem_u32(&full_bar[s]), 1);
       tc::mbar_init(tc::smem_u32(&empty_bar[s]), 1);
+      tc::mbar_init(tc::smem_u32(&bready_bar[s]), 4);   // one arrive per dequant warp
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(tc::smem_u32(&tfull_bar[b]), 1);
@@ -132,7 +171,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     tc::tma_prefetch_desc(&tmA);
     tc::tma_prefetch_desc(&tmB0);
     tc::tma_prefetch_desc(&tmS0);
-    if (g.mode == kModeGateUpSplit) {
+    if (FP4 || g.mode == kModeGateUpSplit) {
       tc::tma_prefetch_desc(&tmB1);
       tc::tma_prefetch_desc(&tmS1);
     }
@@ -169,6 +208,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           // split_k: chunks [nk, 2nk) read the lo half of h against the same weights
           const int kb = kc < nk ? kc : kc - nk;
           const int ka = kc < nk ? kc * kBK : g.ldh + (kc - nk) * kBK;
+          if (FP4) {
+            // A, packed codes of rows b_row.. (32 bytes = 64 inputs), the chunk's two scale rows
+            const uint32_t sp = sb + (uint32_t)kTileB, ss = sp + (uint32_t)L::kPacked;
+            tc::mbar_arrive_expect_tx(fb, kTileA + (uint32_t)g.N * 32u + 2u * (uint32_t)g.N);
+            tc::tma_load_2d(sa, &tmA, ka, a_row, fb);
+            tc::tma_load_2d(sp, &tmB0, kb * 32, b_row, fb);
+            tc::tma_load_2d(ss, &tmB1, tl.n * g.N, tl.v * g.scale_nblk + 2 * kb, fb);
+          } else {
           tc::mbar_arrive_expect_tx(fb, kTileA + b_bytes);
           tc::tma_load_2d(sa, &tmA, ka, a_row, fb);
           if (g.mode == kModeGateUpSplit) {
@@ -176,6 +223,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             tc::tma_load_2d(sb + (uint32_t)g.nf * 128u, m1, kb * kBK, b_row, fb);
           } else {
             tc::tma_load_2d(sb, m0, kb * kBK, b_row, fb);
+          }
           }
           ++issued;
           if (++s == kStages) {
@@ -207,7 +255,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const uint32_t dt = tmem + (uint32_t)b * 256u;
         bool ok = true;
         for (int kc = 0; kc < tl.nkc; ++kc) {
-          if (!tc::mbar_wait(tc::smem_u32(&full_bar[s]), ph, abort, status)) {
+          if (!tc::mbar_wait(tc::smem_u32(&full_bar[s]), ph, abort, status) ||
+              (FP4 && !tc::mbar_wait(tc::smem_u32(&bready_bar[s]), ph, abort, status))) {
             ok = false;
             break;
           }
@@ -239,6 +288,32 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         volatile int* never = &zero;
         tc::mbar_wait(tc::smem_u32(&drain_bar), 0, never, status);
       }
+    }
+  } else if (FP4 && warp >= 6) {
+    // ---------------------------------------------------------------- MXFP4 dequant
+    const int dt = threadIdx.x - 192;
+    int s = 0;
+    uint32_t ph = 0;
+    for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
+      const Tile tl = tile_at(g, t, n_m);
+      if (tl.skip) continue;
+      bool ok = true;
+      for (int kc = 0; kc < tl.nkc; ++kc) {
+        if (!tc::mbar_wait(tc::smem_u32(&full_bar[s]), ph, abort, status)) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = smem + s * kStageBytes;
+        dequant_stage(st + kTileA + kTileB, st + kTileA + kTileB + L::kPacked, st + kTileA, g.N, dt, 128);
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bready_bar[s]));
+        if (++s == kStages) {
+          s = 0;
+          ph ^= 1;
+        }
+      }
+      if (!ok) break;
     }
   } else {
     // ---------------------------------------------------------------- epilogue
@@ -371,6 +446,21 @@ gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ r
   }
 }
 
+// MXFP4 scales [E, rows, nblk] -> [E, nblk, rows], so that the scales of one
+// 64-input chunk for a tile's consecutive rows are contiguous (a TMA box).
+__global__ void __launch_bounds__(256)
+transpose_scales_kernel(const uint8_t* __restrict__ src, int E, int rows, int nblk,
+                        uint8_t* __restrict__ dst) {
+  const long long n = (long long)E * rows * nblk;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long r = i % rows;
+    const long long vb = i / rows;            // v * nblk + blk
+    const long long v = vb / nblk, blk = vb - v * nblk;
+    dst[i] = src[(v * rows + r) * nblk + blk];
+  }
+}
+
 // ---------------------------------------------------------------- host side
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -392,19 +482,34 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2D map over a row-major bf16 matrix [rows, cols] (row stride in bytes), box of
-// box_rows x 64 columns, 128-byte swizzle.
-bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t stride,
-                   uint32_t box_rows) {
+// 2D map over a row-major matrix [rows, cols] (row stride in bytes) with a box of
+// box_rows x box_cols elements.
+bool make_map(CUtensorMap* m, CUtensorMapDataType type, const void* base, uint64_t rows,
+              uint64_t cols, uint64_t stride, uint32_t box_rows, uint32_t box_cols,
+              CUtensorMapSwizzle swz) {
   EncodeTiledFn fn = encode_fn();
   if (!fn || !base) return false;
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {stride};
-  const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+  const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(m, type, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// bf16 matrix, box of box_rows x 64 columns, 128-byte swizzle (operand tiles).
+bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t stride,
+                   uint32_t box_rows) {
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rows, cols, stride, box_rows, kBK,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// byte matrix, box of box_rows x box_cols bytes, no swizzle (MXFP4 codes, scales).
+bool make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                 uint32_t box_cols) {
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, rows, cols, cols, box_rows, box_cols,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 int sm_count() {
@@ -414,45 +519,63 @@ int sm_count() {
   return n > 0 ? n : 148;
 }
 
-// gate_up features per n tile: N = 2 nf <= 256 with nf a multiple of 16 (of 32 for
-// separate gate/up, whose epilogue reads 32 gate and 32 up columns at a time),
-// dividing ff and, with a shared expert, sff.  0 if none.
-int gateup_nf(const ExpertParams& p, int interleaved) {
-  const int step = interleaved ? 16 : 32;
-  for (int f = kMaxN / 2; f >= step; f -= step)
-    if (p.ff % f == 0 && (p.sff == 0 || p.sff % f == 0)) return f;
+// Largest N (multiple of 16, at most max_n) that divides `rows`; 0 if none.
+int tile_n(int rows, int max_n) {
+  for (int n = max_n; n >= 16; n -= 16)
+    if (rows % n == 0) return n;
   return 0;
 }
 
+// gate_up features per n tile: N = 2 nf <= max_n with nf a multiple of 16 (of 32 for
+// separate gate/up, whose epilogue reads 32 gate and 32 up columns at a time),
+// dividing ff and, with a shared expert, sff.  0 if none.
+int gateup_nf(int ff, int sff, int interleaved, int max_n) {
+  const int step = interleaved ? 16 : 32;
+  for (int f = (max_n / 2) / step * step; f >= step; f -= step)
+    if (ff % f == 0 && (sff == 0 || sff % f == 0)) return f;
+  return 0;
+}
+
+template <bool FP4>
 void set_smem_attr() {
   static bool done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || done[dev]) return;
-  cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaFuncSetAttribute(grouped_gemm_kernel<FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       Lay<FP4>::kSmemBytes);
   done[dev] = true;
+}
+
+template <bool FP4>
+cudaError_t launch_gemm(const CUtensorMap& tA, const CUtensorMap& tB0, const CUtensorMap& tB1,
+                        const CUtensorMap& tS0, const CUtensorMap& tS1, const GemmArgs& g,
+                        int max_mtiles, cudaStream_t s) {
+  set_smem_attr<FP4>();
+  const long long tiles = (long long)max_mtiles * g.nt_max;
+  int grid = sm_count();
+  if (tiles < grid) grid = (int)(tiles > 0 ? tiles : 1);
+  grouped_gemm_kernel<FP4><<<grid, Lay<FP4>::kThreads, Lay<FP4>::kSmemBytes, s>>>(tA, tB0, tB1, tS0,
+                                                                                  tS1, g);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
-// Largest N (multiple of 16, at most 256) that divides `rows`; 0 if none.
-int prefill_tile_n(int rows) {
-  for (int n = kMaxN; n >= 16; n -= 16)
-    if (rows % n == 0) return n;
-  return 0;
-}
-
 bool prefill_supported(int d, int ff, int sff, int wfmt, int interleaved) {
-  if (wfmt != MOE_WFMT_BF16) return false;
+  const bool fp4 = wfmt == MOE_WFMT_MXFP4;
+  const int max_n = fp4 ? Lay<true>::kMaxN : Lay<false>::kMaxN;
   if (d % kBK || ff % kBK || (sff && sff % kBK)) return false;
-  ExpertParams p{};
-  p.d = d;
-  p.ff = ff;
-  p.sff = sff;
-  if (!gateup_nf(p, interleaved)) return false;
-  if (!prefill_tile_n(d)) return false;
+  if (fp4 && (!interleaved || sff)) return false;
+  if (!gateup_nf(ff, sff, interleaved, max_n)) return false;
+  if (!tile_n(d, max_n)) return false;
   if (sff && interleaved) return false;   // the shared expert has separate gate/up maps
   return true;
+}
+
+size_t prefill_scales_bytes(const ExpertParams& p, int wfmt) {
+  if (wfmt != MOE_WFMT_MXFP4) return 0;
+  return (size_t)p.E * 2 * p.ff * (p.d / 32) + (size_t)p.E * p.d * (p.ff / 32);
 }
 
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* row2slot, int S, int K, int d,
@@ -464,10 +587,20 @@ cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* row2slot, int S
   return cudaGetLastError();
 }
 
-cudaError_t launch_gateup_prefill(const ExpertParams& p, int interleaved, const RouteState& rs,
-                                  const uint16_t* xp, int S, uint16_t* h, int ldh, int max_mtiles,
-                                  cudaStream_t s) {
-  const int nf = gateup_nf(p, interleaved);
+cudaError_t launch_transpose_scales(const ExpertParams& p, uint8_t* scratch, cudaStream_t s) {
+  const long long n1 = (long long)p.E * 2 * p.ff * (p.d / 32);
+  const long long n2 = (long long)p.E * p.d * (p.ff / 32);
+  transpose_scales_kernel<<<152 * 4, 256, 0, s>>>(p.gu_scales, p.E, 2 * p.ff, p.d / 32, scratch);
+  transpose_scales_kernel<<<152 * 4, 256, 0, s>>>(p.dn_scales, p.E, p.d, p.ff / 32, scratch + n1);
+  (void)n2;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gateup_prefill(const ExpertParams& p, int wfmt, int interleaved,
+                                  const RouteState& rs, const uint16_t* xp, int S, uint16_t* h,
+                                  int ldh, const uint8_t* scalesT, int max_mtiles, cudaStream_t s) {
+  const bool fp4 = wfmt == MOE_WFMT_MXFP4;
+  const int nf = gateup_nf(p.ff, p.sff, interleaved, fp4 ? Lay<true>::kMaxN : Lay<false>::kMaxN);
   GemmArgs g{};
   g.rs = rs;
   g.E = p.E;
@@ -488,14 +621,23 @@ cudaError_t launch_gateup_prefill(const ExpertParams& p, int interleaved, const 
   g.ff = p.ff;
   g.h = h;
   g.ldh = ldh;
+  g.scale_rows = 2 * p.ff;
+  g.scale_nblk = p.d / 32;
   CUtensorMap tA, tB0, tB1, tS0, tS1;
   std::memset(&tB1, 0, sizeof(tB1));
-  std::memset(&tS0, 0, sizeof(tS0));
-  std::memset(&tS1, 0, sizeof(tS1));
   const uint64_t rowb = (uint64_t)p.d * 2;
   if (!make_map_bf16(&tA, xp, (uint64_t)S, p.d, rowb, kBM)) return cudaErrorInvalidValue;
+  if (fp4) {
+    const uint64_t rows = (uint64_t)p.E * 2 * p.ff;
+    if (!make_map_u8(&tB0, p.gate_up, rows, (uint64_t)(p.d / 32) * 16, g.N, kBK / 2))
+      return cudaErrorInvalidValue;
+    if (!make_map_u8(&tB1, scalesT, (uint64_t)p.E * (p.d / 32), 2 * (uint64_t)p.ff, 2, g.N))
+      return cudaErrorInvalidValue;
+    return launch_gemm<true>(tA, tB0, tB1, tB0, tB1, g, max_mtiles, s);
+  }
   if (interleaved) {
     if (!make_map_bf16(&tB0, p.gate_up, (uint64_t)p.E * 2 * p.ff, p.d, rowb, g.N)) return cudaErrorInvalidValue;
+    tB1 = tB0;
   } else {
     if (!make_map_bf16(&tB0, p.gate, (uint64_t)p.E * p.ff, p.d, rowb, nf)) return cudaErrorInvalidValue;
     if (!make_map_bf16(&tB1, p.up, (uint64_t)p.E * p.ff, p.d, rowb, nf)) return cudaErrorInvalidValue;
@@ -505,24 +647,20 @@ cudaError_t launch_gateup_prefill(const ExpertParams& p, int interleaved, const 
     if (!make_map_bf16(&tS1, p.sh_up, p.sff, p.d, rowb, nf)) return cudaErrorInvalidValue;
   } else {
     tS0 = tB0;
-    tS1 = interleaved ? tB0 : tB1;
+    tS1 = tB1;
   }
-  if (interleaved) tB1 = tB0;
-  set_smem_attr();
-  long long tiles = (long long)max_mtiles * g.nt_max;
-  int grid = sm_count();
-  if (tiles < grid) grid = (int)(tiles > 0 ? tiles : 1);
-  grouped_gemm_kernel<<<grid, kThreads, kSmemBytes, s>>>(tA, tB0, tB1, tS0, tS1, g);
-  return cudaGetLastError();
+  return launch_gemm<false>(tA, tB0, tB1, tS0, tS1, g, max_mtiles, s);
 }
 
-cudaError_t launch_down_prefill(const ExpertParams& p, const RouteState& rs, const uint16_t* h,
-                                int ldh, int S, float* Y, int max_mtiles, cudaStream_t s) {
+cudaError_t launch_down_prefill(const ExpertParams& p, int wfmt, const RouteState& rs,
+                                const uint16_t* h, int ldh, int S, float* Y,
+                                const uint8_t* scalesT, int max_mtiles, cudaStream_t s) {
+  const bool fp4 = wfmt == MOE_WFMT_MXFP4;
   GemmArgs g{};
   g.rs = rs;
   g.E = p.E;
   g.mode = kModeDown;
-  g.N = prefill_tile_n(p.d);
+  g.N = tile_n(p.d, fp4 ? Lay<true>::kMaxN : Lay<false>::kMaxN);
   g.nt_routed = p.d / g.N;
   g.nt_shared = p.sff ? p.d / g.N : 0;
   g.nt_max = g.nt_routed;
@@ -534,10 +672,19 @@ cudaError_t launch_down_prefill(const ExpertParams& p, const RouteState& rs, con
   g.Y = Y;
   g.ldh = ldh;
   g.split_k = 1;
-  CUtensorMap tA, tB0, tS0;
-  std::memset(&tS0, 0, sizeof(tS0));
+  g.scale_rows = p.d;
+  g.scale_nblk = p.ff / 32;
+  CUtensorMap tA, tB0, tB1, tS0;
   if (!make_map_bf16(&tA, h, (uint64_t)S, 2 * (uint64_t)ldh, (uint64_t)ldh * 4, kBM))
     return cudaErrorInvalidValue;
+  if (fp4) {
+    const uint8_t* sT = scalesT + (size_t)p.E * 2 * p.ff * (p.d / 32);
+    if (!make_map_u8(&tB0, p.down, (uint64_t)p.E * p.d, (uint64_t)(p.ff / 32) * 16, g.N, kBK / 2))
+      return cudaErrorInvalidValue;
+    if (!make_map_u8(&tB1, sT, (uint64_t)p.E * (p.ff / 32), (uint64_t)p.d, 2, g.N))
+      return cudaErrorInvalidValue;
+    return launch_gemm<true>(tA, tB0, tB1, tB0, tB1, g, max_mtiles, s);
+  }
   if (!make_map_bf16(&tB0, p.down, (uint64_t)p.E * p.d, p.ff, (uint64_t)p.ff * 2, g.N))
     return cudaErrorInvalidValue;
   if (p.sff) {
@@ -545,12 +692,7 @@ cudaError_t launch_down_prefill(const ExpertParams& p, const RouteState& rs, con
   } else {
     tS0 = tB0;
   }
-  set_smem_attr();
-  long long tiles = (long long)max_mtiles * g.nt_max;
-  int grid = sm_count();
-  if (tiles < grid) grid = (int)(tiles > 0 ? tiles : 1);
-  grouped_gemm_kernel<<<grid, kThreads, kSmemBytes, s>>>(tA, tB0, tB0, tS0, tS0, g);
-  return cudaGetLastError();
+  return launch_gemm<false>(tA, tB0, tB0, tS0, tS0, g, max_mtiles, s);
 }
 
 }  // namespace moe

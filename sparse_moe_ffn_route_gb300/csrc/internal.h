@@ -95,11 +95,15 @@ cudaError_t launch_down_decode(const ExpertParams& p, int wfmt, const RouteState
 bool prefill_supported(int d, int ff, int sff, int wfmt, int interleaved);
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* row2slot, int S, int K, int d,
                                uint16_t* xp, cudaStream_t s);
-cudaError_t launch_gateup_prefill(const ExpertParams& p, int interleaved, const RouteState& rs,
-                                  const uint16_t* xp, int S, uint16_t* h, int ldh, int max_mtiles,
-                                  cudaStream_t s);
-cudaError_t launch_down_prefill(const ExpertParams& p, const RouteState& rs, const uint16_t* h,
-                                int ldh, int S, float* Y, int max_mtiles, cudaStream_t s);
+// MXFP4: bytes of the transposed-scale scratch, and the kernel that fills it.
+size_t prefill_scales_bytes(const ExpertParams& p, int wfmt);
+cudaError_t launch_transpose_scales(const ExpertParams& p, uint8_t* scratch, cudaStream_t s);
+cudaError_t launch_gateup_prefill(const ExpertParams& p, int wfmt, int interleaved,
+                                  const RouteState& rs, const uint16_t* xp, int S, uint16_t* h,
+                                  int ldh, const uint8_t* scalesT, int max_mtiles, cudaStream_t s);
+cudaError_t launch_down_prefill(const ExpertParams& p, int wfmt, const RouteState& rs,
+                                const uint16_t* h, int ldh, int S, float* Y,
+                                const uint8_t* scalesT, int max_mtiles, cudaStream_t s);
 
 // MXFP4 [rows, n_in/32, 16] + scales -> bf16 [rows, n_in].
 cudaError_t launch_mxfp4_to_bf16(const uint8_t* blocks, const uint8_t* scales, long long rows,

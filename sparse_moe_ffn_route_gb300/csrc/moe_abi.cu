@@ -19,7 +19,7 @@ struct Layout {
   int K, E1, S, ldl, ldh;
   bool prefill;             // the expert phase runs the tcgen05 grouped GEMMs
   size_t status, counts, offsets, work, n_work, slot_expert, slot_w, row2slot, logits, h, Y,
-      xp, xstage, ystage, total;
+      xp, scalesT, xstage, ystage, total;
 };
 
 int path_for(const moe_cfg_t* c, int T);
@@ -75,6 +75,13 @@ bool make_layout(const moe_cfg_t* c, int T, Layout* L) {
                prefill_supported(c->d_model, c->expert_ff, c->shared_ff, c->wfmt,
                                  c->interleaved_gate_up);
   L->xp = take(L->prefill ? 2 * Sz * d : 0);
+  {
+    ExpertParams sp{};
+    sp.E = c->n_experts;
+    sp.d = c->d_model;
+    sp.ff = c->expert_ff;
+    L->scalesT = take(L->prefill ? prefill_scales_bytes(sp, c->wfmt) : 0);
+  }
   L->xstage = take(2 * Tz * d);
   L->ystage = take(4 * Tz * d);
   L->total = off;
@@ -230,13 +237,16 @@ int run_experts(const moe_cfg_t* c, const void* x, int T, const moe_experts_t* e
     constexpr int kTileRows = 128;
     const int max_mtiles = L.E1 + (L.S + kTileRows - 1) / kTileRows;
     uint16_t* xp = at<uint16_t>(ws, L.xp);
+    uint8_t* scalesT = at<uint8_t>(ws, L.scalesT);
+    if (c->wfmt == MOE_WFMT_MXFP4) MOE_CUDA(launch_transpose_scales(p, scalesT, s));
     MOE_CUDA(launch_permute(rs, L.S, L.E1, kTileRows, s));
     MOE_CUDA(launch_gather_rows(static_cast<const uint16_t*>(x), rs.row2slot, L.S, L.K,
                                 c->d_model, xp, s));
     MOE_CUDA(mark_phase(3, s));
-    MOE_CUDA(launch_gateup_prefill(p, c->interleaved_gate_up, rs, xp, L.S, h, L.ldh, max_mtiles, s));
+    MOE_CUDA(launch_gateup_prefill(p, c->wfmt, c->interleaved_gate_up, rs, xp, L.S, h, L.ldh,
+                                   scalesT, max_mtiles, s));
     MOE_CUDA(mark_phase(4, s));
-    MOE_CUDA(launch_down_prefill(p, rs, h, L.ldh, L.S, Y, max_mtiles, s));
+    MOE_CUDA(launch_down_prefill(p, c->wfmt, rs, h, L.ldh, L.S, Y, scalesT, max_mtiles, s));
     MOE_CUDA(mark_phase(5, s));
     MOE_CUDA(launch_combine(Y, rs.slot_w, rs.slot_expert, T, L.K, c->d_model, L.E1, y,
                             c->y_fp32 != 0, s));

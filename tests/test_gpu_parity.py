@@ -282,6 +282,10 @@ PREFILL_SPECS = [
     mi.small_spec("qwen", 256, 16, 4, 128, 128, 300, bias=("normal", 0.5)),
     mi.small_spec("qwen", 512, 8, 3, 256, 0, 333, expert_weights_scale=1.5),
     mi.small_spec("qwen", 192, 4, 4, 320, 64, 129),                            # E == k, N 192
+    mi.small_spec("gptoss", 128, 8, 2, 128, 0, 200, bias=("zipf", 1.1)),
+    mi.small_spec("gptoss", 320, 4, 2, 192, 0, 150, bias=("normal", 0.1)),      # N 192 / 160
+    mi.small_spec("gptoss", 256, 16, 4, 256, 0, 300, bias=("normal", 0.1), scale_lo=118,
+                  scale_hi=120),
 ]
 
 
