@@ -8,8 +8,8 @@
 // natural layouts of activations and of row = output weights.
 //
 // One persistent CTA per SM walks the tiles (m tile of 128 rows of one expert,
-// n tile of N output columns), n-tile-major so that concurrently running CTAs
-// share the same weight tiles through L2.  Warp roles:
+// n tile of N output columns), m-tile-major so that concurrently running CTAs
+// share A tiles and weight tiles through L2.  Warp roles:
 //   warp 0      TMA producer: A and B tiles of 64 k (128-byte rows, 128-byte
 //               swizzle) into a 4-stage shared-memory ring;
 //   warp 1      owns TMEM (two accumulators of up to 256 fp32 columns) and issues
@@ -36,26 +36,31 @@
 namespace moe {
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kBM = 128;                         // rows per tile (MMA M)
 constexpr int kBK = 64;                          // k per stage: 128 bytes of bf16
 constexpr int kTileA = kBM * kBK * 2;            // 16 KiB
 constexpr uint32_t kTmemCols = 512;              // two accumulators of 256 columns
 
-// Shared-memory stage of each variant.  bf16 weights: A | B.  MXFP4 weights: A |
-// B (bf16, written by the dequant warps) | packed codes (N x 32 bytes per 64 k) |
-// scales (2 x N bytes: the two 32-input blocks of the chunk).  Stages are
-// multiples of 1024 bytes so every swizzled tile starts 1024-aligned.
-template <bool FP4>
+// Shared-memory stage of each variant: A tile(s) | B (bf16) | MXFP4 only: packed
+// codes (N x 32 bytes per 64 k) | scales (2 x N bytes: the two 32-input blocks of
+// the chunk).  DUAL (the down projection): two A tiles, h_hi and h_lo, multiply the
+// same B tile.  Stages are multiples of 1024 bytes so every swizzled tile starts
+// 1024-aligned.  MXFP4 variants add 12 dequant warps (warps 6..17).
+template <bool FP4, bool DUAL>
 struct Lay {
   static constexpr int kMaxN = FP4 ? 240 : 256;
+  static constexpr int kATiles = DUAL ? 2 : 1;
   static constexpr int kTileB = kMaxN * kBK * 2;
   static constexpr int kPacked = FP4 ? kMaxN * (kBK / 2) : 0;
   static constexpr int kScales = FP4 ? 512 : 0;
-  static constexpr int kStageBytes = ((kTileA + kTileB + kPacked + kScales + 1023) / 1024) * 1024;
+  static constexpr int kStageBytes =
+      ((kATiles * kTileA + kTileB + kPacked + kScales + 1023) / 1024) * 1024;
+  static constexpr int kStages = DUAL ? 3 : 4;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024;   // + alignment slack
-  static constexpr int kThreads = FP4 ? 320 : 192;                 // + 4 dequant warps
+  static constexpr int kDequantWarps = FP4 ? 12 : 0;
+  static constexpr int kThreads = 192 + 32 * kDequantWarps;
 };
+constexpr int kMaxStages = 4;
 
 enum : int { kModeGateUpSplit = 0, kModeGateUpInterleaved = 1, kModeDown = 2 };
 
@@ -75,7 +80,7 @@ struct GemmArgs {
   int d, ff;
   uint16_t* h;            // gate_up output [S, 2*ldh]: bf16 (hi, lo) halves, grouped row order
   int ldh;                // width of each half
-  int split_k;            // down: K runs over [h_hi | h_lo] against [D | D]
+  int dual;               // down: A = h_hi and h_lo tiles against the same B tile
   float* Y;               // down output [S, d] (slot order)
   int scale_rows;         // MXFP4: rows of one expert in the transposed scales
   int scale_nblk;         // MXFP4: 32-input blocks per weight row
@@ -83,21 +88,25 @@ struct GemmArgs {
 
 struct Tile {
   int v, row0, n, cnt, kk;    // expert, first row within it, n tile, rows in this tile, k
-  int nkc;                    // k chunks of 64 the MMA runs (2 kk/64 when split_k)
+  int nkc;                    // k chunks of 64
   bool skip;
 };
 
+// Tiles run m-tile-major: the CTAs working at the same time take the n tiles of a
+// few consecutive m tiles, so each A tile and each expert's weight tiles are read
+// from HBM about once and then served to the other CTAs from L2.
 __device__ __forceinline__ Tile tile_at(const GemmArgs& g, int t, int n_m) {
   Tile tl;
-  tl.n = t / n_m;
-  const int2 w = g.rs.work[t - tl.n * n_m];
+  const int m = t / g.nt_max;
+  tl.n = t - m * g.nt_max;
+  const int2 w = g.rs.work[m];
   tl.v = w.x;
   tl.row0 = w.y;
   const bool sh = (tl.v == g.E);
   const int rows = g.rs.offsets[tl.v + 1] - g.rs.offsets[tl.v];
   tl.cnt = min(kBM, rows - tl.row0);
   tl.kk = sh ? g.k_shared : g.k_routed;
-  tl.nkc = (tl.kk / kBK) * (g.split_k ? 2 : 1);
+  tl.nkc = tl.kk / kBK;
   tl.skip = tl.n >= (sh ? g.nt_shared : g.nt_routed);
   return tl;
 }
@@ -113,37 +122,63 @@ __device__ __forceinline__ float act_clamped(float gt, float up, float limit, fl
 // MXFP4 dequant of one stage: N rows x 64 inputs from packed codes (smem, [N][32])
 // and scales (smem, [2][N]) into the bf16 B tile with the 128-byte swizzle.
 // Work unit = one 16-byte output chunk (8 inputs, 4 code bytes, one scale).
-__device__ __forceinline__ void dequant_stage(const uint8_t* packed, const uint8_t* scales, uint8_t* btile,
-                                              int N, int tid, int nthreads) {
-  for (int c = tid; c < N * 8; c += nthreads) {
-    const int r = c >> 3, j = c & 7;
-    const uint32_t w = *reinterpret_cast<const uint32_t*>(packed + r * 32 + j * 4);
-    const Fp4Scale sc = fp4_scale(scales[(j >> 2) * N + r]);
-    const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
-    uint4 o;
+// Thread `tid` always takes chunk column j = tid % 8 of rows tid / 8 + step * i
+// (step = nthreads / 8, a multiple of 8), so its swizzle XOR (j ^ row % 8), its
+// scale row and all its addresses advance by constants.
+__device__ __forceinline__ uint4 dq_chunk(uint32_t w, const Fp4Scale& sc, bool two) {
+  const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
+  uint4 o;
+  if (!two) {
+    const Fp4Scale one{sc.first, 0u, false};
+    o.x = fp4_pair<0>(lo, hi, one);
+    o.y = fp4_pair<1>(lo, hi, one);
+    o.z = fp4_pair<2>(lo, hi, one);
+    o.w = fp4_pair<3>(lo, hi, one);
+  } else {
     o.x = fp4_pair<0>(lo, hi, sc);
     o.y = fp4_pair<1>(lo, hi, sc);
     o.z = fp4_pair<2>(lo, hi, sc);
     o.w = fp4_pair<3>(lo, hi, sc);
-    *reinterpret_cast<uint4*>(btile + r * 128 + ((j ^ (r & 7)) << 4)) = o;
+  }
+  return o;
+}
+
+__device__ __forceinline__ void dequant_stage(const uint8_t* packed, const uint8_t* scales, uint8_t* btile,
+                                              int N, int tid, int nthreads) {
+  const int j = tid & 7, r0 = tid >> 3, step = nthreads >> 3;
+  const uint8_t* pk = packed + r0 * 32 + j * 4;
+  const uint8_t* sp = scales + (j >> 2) * N + r0;
+  uint8_t* bt = btile + r0 * 128 + ((j ^ (r0 & 7)) << 4);
+#pragma unroll 5
+  for (int r = r0; r < N; r += step) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(pk);
+    const uint32_t sv = *sp;
+    const Fp4Scale sc = fp4_scale(sv);
+    const bool two = __any_sync(0xffffffffu, sv > 128u);   // warp-uniform: 2nd multiply needed
+    *reinterpret_cast<uint4*>(bt) = dq_chunk(w, sc, two);
+    pk += step * 32;
+    sp += step;
+    bt += step * 128;
   }
 }
 
 // FP4: B comes from MXFP4 weights (tmB0: packed codes [rows, nblk*16] bytes, tmB1:
 // transposed scales [E*nblk, rows] bytes); else tmB0/tmB1 (and tmS0/tmS1 for the
 // shared expert) are bf16 weight maps.
-template <bool FP4>
-__global__ void __launch_bounds__(Lay<FP4>::kThreads, 1)
+template <bool FP4, bool DUAL>
+__global__ void __launch_bounds__(Lay<FP4, DUAL>::kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmS0,
                     const __grid_constant__ CUtensorMap tmS1, const GemmArgs g) {
-  using L = Lay<FP4>;
+  using L = Lay<FP4, DUAL>;
+  constexpr int kStages = L::kStages;
   constexpr int kStageBytes = L::kStageBytes;
   constexpr int kTileB = L::kTileB;
+  constexpr int kAB = L::kATiles * kTileA;     // offset of B in a stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], bready_bar[kStages],
-      tfull_bar[2], tempty_bar[2], drain_bar;
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages], empty_bar[kMaxStages],
+      bready_bar[kMaxStages], tfull_bar[2], tempty_bar[2], drain_bar;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
   __shared__ int consumed_s;     // stage loads the MMA thread has waited for
@@ -156,7 +191,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(tc::smem_u32(&full_bar[s]), 1);
       tc::mbar_init(tc::smem_u32(&empty_bar[s]), 1);
-      tc::mbar_init(tc::smem_u32(&bready_bar[s]), 4);   // one arrive per dequant warp
+      tc::mbar_init(tc::smem_u32(&bready_bar[s]), L::kDequantWarps ? L::kDequantWarps : 1);
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(tc::smem_u32(&tfull_bar[b]), 1);
@@ -189,7 +224,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (tc::elect_one()) {
       int s = 0, issued = 0;
       uint32_t ph = 0;
-      const uint32_t b_bytes = (uint32_t)g.N * kBK * 2;
       for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
         const Tile tl = tile_at(g, t, n_m);
         if (tl.skip) continue;
@@ -199,31 +233,27 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const int b_row = (sh ? 0 : tl.v * g.b_rows_routed) + tl.n * nb;
         const CUtensorMap* m0 = sh ? &tmS0 : &tmB0;
         const CUtensorMap* m1 = sh ? &tmS1 : &tmB1;
-        const int nk = tl.kk / kBK;
         for (int kc = 0; kc < tl.nkc; ++kc) {
           if (!tc::mbar_wait(tc::smem_u32(&empty_bar[s]), ph ^ 1, abort, status)) break;
           const uint32_t fb = tc::smem_u32(&full_bar[s]);
           const uint32_t sa = tc::smem_u32(smem + s * kStageBytes);
-          const uint32_t sb = sa + kTileA;
-          // split_k: chunks [nk, 2nk) read the lo half of h against the same weights
-          const int kb = kc < nk ? kc : kc - nk;
-          const int ka = kc < nk ? kc * kBK : g.ldh + (kc - nk) * kBK;
+          const uint32_t sb = sa + kAB;
+          const int k0 = kc * kBK;
+          uint32_t bytes = (uint32_t)kAB;
+          if (FP4) bytes += (uint32_t)g.N * 34u;          // codes (32 B) + 2 scales per row
+          else bytes += (uint32_t)g.N * kBK * 2;
+          tc::mbar_arrive_expect_tx(fb, bytes);
+          tc::tma_load_2d(sa, &tmA, k0, a_row, fb);
+          if (DUAL) tc::tma_load_2d(sa + kTileA, &tmA, g.ldh + k0, a_row, fb);
           if (FP4) {
-            // A, packed codes of rows b_row.. (32 bytes = 64 inputs), the chunk's two scale rows
             const uint32_t sp = sb + (uint32_t)kTileB, ss = sp + (uint32_t)L::kPacked;
-            tc::mbar_arrive_expect_tx(fb, kTileA + (uint32_t)g.N * 32u + 2u * (uint32_t)g.N);
-            tc::tma_load_2d(sa, &tmA, ka, a_row, fb);
-            tc::tma_load_2d(sp, &tmB0, kb * 32, b_row, fb);
-            tc::tma_load_2d(ss, &tmB1, tl.n * g.N, tl.v * g.scale_nblk + 2 * kb, fb);
+            tc::tma_load_2d(sp, &tmB0, kc * 32, b_row, fb);
+            tc::tma_load_2d(ss, &tmB1, tl.n * g.N, tl.v * g.scale_nblk + 2 * kc, fb);
+          } else if (g.mode == kModeGateUpSplit) {
+            tc::tma_load_2d(sb, m0, k0, b_row, fb);
+            tc::tma_load_2d(sb + (uint32_t)g.nf * 128u, m1, k0, b_row, fb);
           } else {
-          tc::mbar_arrive_expect_tx(fb, kTileA + b_bytes);
-          tc::tma_load_2d(sa, &tmA, ka, a_row, fb);
-          if (g.mode == kModeGateUpSplit) {
-            tc::tma_load_2d(sb, m0, kb * kBK, b_row, fb);
-            tc::tma_load_2d(sb + (uint32_t)g.nf * 128u, m1, kb * kBK, b_row, fb);
-          } else {
-            tc::tma_load_2d(sb, m0, kb * kBK, b_row, fb);
-          }
+            tc::tma_load_2d(sb, m0, k0, b_row, fb);
           }
           ++issued;
           if (++s == kStages) {
@@ -263,10 +293,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           consumed_s = consumed_s + 1;
           tc::tc_fence_after();
           const uint32_t sa = tc::smem_u32(smem + s * kStageBytes);
-          const uint64_t ad = tc::sdesc_sw128(sa), bd = tc::sdesc_sw128(sa + kTileA);
+          const uint64_t ad = tc::sdesc_sw128(sa), bd = tc::sdesc_sw128(sa + kAB);
 #pragma unroll
-          for (int j = 0; j < kBK / 16; ++j)
+          for (int j = 0; j < kBK / 16; ++j) {
             tc::umma_bf16(dt, ad + 2 * j, bd + 2 * j, idesc, (kc | j) != 0);
+            if (DUAL) tc::umma_bf16(dt, ad + (kTileA >> 4) + 2 * j, bd + 2 * j, idesc, 1);
+          }
           tc::umma_commit(tc::smem_u32(&empty_bar[s]));
           any = true;
           if (++s == kStages) {
@@ -292,6 +324,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   } else if (FP4 && warp >= 6) {
     // ---------------------------------------------------------------- MXFP4 dequant
     const int dt = threadIdx.x - 192;
+    constexpr int kDq = 32 * L::kDequantWarps;
     int s = 0;
     uint32_t ph = 0;
     for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
@@ -304,7 +337,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           break;
         }
         uint8_t* st = smem + s * kStageBytes;
-        dequant_stage(st + kTileA + kTileB, st + kTileA + kTileB + L::kPacked, st + kTileA, g.N, dt, 128);
+        dequant_stage(st + kAB + kTileB, st + kAB + kTileB + L::kPacked, st + kAB, g.N, dt, kDq);
         tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(tc::smem_u32(&bready_bar[s]));
@@ -536,27 +569,27 @@ int gateup_nf(int ff, int sff, int interleaved, int max_n) {
   return 0;
 }
 
-template <bool FP4>
+template <bool FP4, bool DUAL>
 void set_smem_attr() {
   static bool done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || done[dev]) return;
-  cudaFuncSetAttribute(grouped_gemm_kernel<FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       Lay<FP4>::kSmemBytes);
+  cudaFuncSetAttribute(grouped_gemm_kernel<FP4, DUAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       Lay<FP4, DUAL>::kSmemBytes);
   done[dev] = true;
 }
 
-template <bool FP4>
+template <bool FP4, bool DUAL>
 cudaError_t launch_gemm(const CUtensorMap& tA, const CUtensorMap& tB0, const CUtensorMap& tB1,
                         const CUtensorMap& tS0, const CUtensorMap& tS1, const GemmArgs& g,
                         int max_mtiles, cudaStream_t s) {
-  set_smem_attr<FP4>();
+  set_smem_attr<FP4, DUAL>();
   const long long tiles = (long long)max_mtiles * g.nt_max;
   int grid = sm_count();
   if (tiles < grid) grid = (int)(tiles > 0 ? tiles : 1);
-  grouped_gemm_kernel<FP4><<<grid, Lay<FP4>::kThreads, Lay<FP4>::kSmemBytes, s>>>(tA, tB0, tB1, tS0,
-                                                                                  tS1, g);
+  grouped_gemm_kernel<FP4, DUAL><<<grid, Lay<FP4, DUAL>::kThreads, Lay<FP4, DUAL>::kSmemBytes, s>>>(
+      tA, tB0, tB1, tS0, tS1, g);
   return cudaGetLastError();
 }
 
@@ -564,7 +597,7 @@ cudaError_t launch_gemm(const CUtensorMap& tA, const CUtensorMap& tB0, const CUt
 
 bool prefill_supported(int d, int ff, int sff, int wfmt, int interleaved) {
   const bool fp4 = wfmt == MOE_WFMT_MXFP4;
-  const int max_n = fp4 ? Lay<true>::kMaxN : Lay<false>::kMaxN;
+  const int max_n = fp4 ? Lay<true, false>::kMaxN : Lay<false, false>::kMaxN;
   if (d % kBK || ff % kBK || (sff && sff % kBK)) return false;
   if (fp4 && (!interleaved || sff)) return false;
   if (!gateup_nf(ff, sff, interleaved, max_n)) return false;
@@ -600,7 +633,7 @@ cudaError_t launch_gateup_prefill(const ExpertParams& p, int wfmt, int interleav
                                   const RouteState& rs, const uint16_t* xp, int S, uint16_t* h,
                                   int ldh, const uint8_t* scalesT, int max_mtiles, cudaStream_t s) {
   const bool fp4 = wfmt == MOE_WFMT_MXFP4;
-  const int nf = gateup_nf(p.ff, p.sff, interleaved, fp4 ? Lay<true>::kMaxN : Lay<false>::kMaxN);
+  const int nf = gateup_nf(p.ff, p.sff, interleaved, fp4 ? Lay<true, false>::kMaxN : Lay<false, false>::kMaxN);
   GemmArgs g{};
   g.rs = rs;
   g.E = p.E;
@@ -633,7 +666,7 @@ cudaError_t launch_gateup_prefill(const ExpertParams& p, int wfmt, int interleav
       return cudaErrorInvalidValue;
     if (!make_map_u8(&tB1, scalesT, (uint64_t)p.E * (p.d / 32), 2 * (uint64_t)p.ff, 2, g.N))
       return cudaErrorInvalidValue;
-    return launch_gemm<true>(tA, tB0, tB1, tB0, tB1, g, max_mtiles, s);
+    return launch_gemm<true, false>(tA, tB0, tB1, tB0, tB1, g, max_mtiles, s);
   }
   if (interleaved) {
     if (!make_map_bf16(&tB0, p.gate_up, (uint64_t)p.E * 2 * p.ff, p.d, rowb, g.N)) return cudaErrorInvalidValue;
@@ -649,7 +682,7 @@ cudaError_t launch_gateup_prefill(const ExpertParams& p, int wfmt, int interleav
     tS0 = tB0;
     tS1 = tB1;
   }
-  return launch_gemm<false>(tA, tB0, tB1, tS0, tS1, g, max_mtiles, s);
+  return launch_gemm<false, false>(tA, tB0, tB1, tS0, tS1, g, max_mtiles, s);
 }
 
 cudaError_t launch_down_prefill(const ExpertParams& p, int wfmt, const RouteState& rs,
@@ -660,7 +693,7 @@ cudaError_t launch_down_prefill(const ExpertParams& p, int wfmt, const RouteStat
   g.rs = rs;
   g.E = p.E;
   g.mode = kModeDown;
-  g.N = tile_n(p.d, fp4 ? Lay<true>::kMaxN : Lay<false>::kMaxN);
+  g.N = tile_n(p.d, fp4 ? Lay<true, false>::kMaxN : Lay<false, false>::kMaxN);
   g.nt_routed = p.d / g.N;
   g.nt_shared = p.sff ? p.d / g.N : 0;
   g.nt_max = g.nt_routed;
@@ -671,7 +704,7 @@ cudaError_t launch_down_prefill(const ExpertParams& p, int wfmt, const RouteStat
   g.d = p.d;
   g.Y = Y;
   g.ldh = ldh;
-  g.split_k = 1;
+  g.dual = 1;
   g.scale_rows = p.d;
   g.scale_nblk = p.ff / 32;
   CUtensorMap tA, tB0, tB1, tS0;
@@ -683,7 +716,7 @@ cudaError_t launch_down_prefill(const ExpertParams& p, int wfmt, const RouteStat
       return cudaErrorInvalidValue;
     if (!make_map_u8(&tB1, sT, (uint64_t)p.E * (p.ff / 32), (uint64_t)p.d, 2, g.N))
       return cudaErrorInvalidValue;
-    return launch_gemm<true>(tA, tB0, tB1, tB0, tB1, g, max_mtiles, s);
+    return launch_gemm<true, true>(tA, tB0, tB1, tB0, tB1, g, max_mtiles, s);
   }
   if (!make_map_bf16(&tB0, p.down, (uint64_t)p.E * p.d, p.ff, (uint64_t)p.ff * 2, g.N))
     return cudaErrorInvalidValue;
@@ -692,7 +725,7 @@ cudaError_t launch_down_prefill(const ExpertParams& p, int wfmt, const RouteStat
   } else {
     tS0 = tB0;
   }
-  return launch_gemm<false>(tA, tB0, tB0, tS0, tS0, g, max_mtiles, s);
+  return launch_gemm<false, true>(tA, tB0, tB0, tS0, tS0, g, max_mtiles, s);
 }
 
 }  // namespace moe
