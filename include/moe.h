@@ -247,7 +247,9 @@ int moe_mxfp4_to_bf16(const void* blocks, const void* scales, int64_t rows, int3
  *   [4] gate_up + activation done  [5] down done  [6] combine done
  * (the routed entry point records [1] and [2] together after ingesting the
  * routing).  `events` holds n_events >= 7 cudaEvent_t handles created by the
- * caller; the array must stay valid while enabled.  events == NULL disables.
+ * caller, or exactly 2: then only the start (events[0]) and the end
+ * (events[1]) are recorded, which keeps the kernels free to overlap their
+ * launches.  The array must stay valid while enabled.  events == NULL disables.
  * No counterpart on the pages: measurement plumbing only. */
 int moe_set_phase_events(void* const* events, int32_t n_events);
 

@@ -339,9 +339,9 @@ _phase_keepalive = None
 
 
 def moe_set_phase_events(events) -> None:
-    """Record torch.cuda.Event objects (>= 7, timing enabled) at the phase boundaries of
-    later forward calls from this thread; None disables.  Each event is recorded once
-    here first so that its CUDA handle exists."""
+    """Record torch.cuda.Event objects (7 for every phase boundary, or 2 for start and
+    end only; timing enabled) during later forward calls from this thread; None
+    disables.  Each event is recorded once here first so that its CUDA handle exists."""
     global _phase_keepalive
     if events is None:
         _check(_lib.moe_set_phase_events(None, 0), "moe_set_phase_events")

@@ -16,6 +16,7 @@ __global__ void __launch_bounds__(256)
 combine_kernel(const float* __restrict__ Y, const float* __restrict__ slot_w,
                const int32_t* __restrict__ slot_expert, int T, int K, int d, int E1,
                void* __restrict__ y) {
+  pdl_wait();
   const int d8 = d / 8;
   const long n = (long)T * d8;
   for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
@@ -45,6 +46,7 @@ combine_kernel(const float* __restrict__ Y, const float* __restrict__ slot_w,
       *reinterpret_cast<uint4*>(static_cast<uint16_t*>(y) + (size_t)t * d + o) = out;
     }
   }
+  pdl_trigger();
 }
 
 }  // namespace
@@ -55,10 +57,10 @@ cudaError_t launch_combine(const float* Y, const float* slot_w, const int32_t* s
   long blocks = (n + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
   if (y_fp32)
-    combine_kernel<true><<<(int)blocks, 256, 0, s>>>(Y, slot_w, slot_expert, T, K, d, E1, y);
-  else
-    combine_kernel<false><<<(int)blocks, 256, 0, s>>>(Y, slot_w, slot_expert, T, K, d, E1, y);
-  return cudaGetLastError();
+    return launch_pdl(combine_kernel<true>, dim3((int)blocks), dim3(256), 0, s, Y, slot_w, slot_expert,
+                      T, K, d, E1, y);
+  return launch_pdl(combine_kernel<false>, dim3((int)blocks), dim3(256), 0, s, Y, slot_w, slot_expert,
+                    T, K, d, E1, y);
 }
 
 }  // namespace moe

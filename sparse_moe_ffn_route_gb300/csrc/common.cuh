@@ -10,6 +10,14 @@
 
 namespace moe {
 
+// Programmatic dependent launch: wait until the preceding kernel of the stream has
+// completed and its writes are visible (a no-op when launched without the
+// attribute); let the next kernel start launching once every CTA got here.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void flag_status(uint32_t* status, uint32_t bits) {
   if (status) atomicOr(status, bits);
 }

@@ -36,6 +36,7 @@ constexpr int kGateUpFeatures = kWarps * 16;     // features per CTA (2 tiles of
 constexpr int kDownRows = kWarps * 32;           // output rows per CTA (2 tiles of 16 per warp)
 constexpr int kDepthBf16 = 4;                    // k steps of weight loads in flight (bf16)
 constexpr int kDepthFp4 = 2;                     // k groups of weight loads in flight (MXFP4)
+constexpr size_t kMaxStage = 48 * 1024;          // largest staged token-row block per CTA
 
 __device__ __forceinline__ float act_swiglu(float g, float u) {
   return g / (1.f + __expf(-g)) * u;
@@ -45,6 +46,25 @@ __device__ __forceinline__ float act_clamped(float g, float u, float limit, floa
   g = fminf(g, limit);
   u = fminf(fmaxf(u, -limit), limit);
   return (u + 1.f) * g / (1.f + __expf(-alpha * g));
+}
+
+// 16 bytes of a token row: from shared memory (staged rows, generic pointer) or
+// through the read-only path from global memory.
+template <bool SB>
+__device__ __forceinline__ uint4 ld_b16(const uint8_t* p) {
+  if (SB) return *reinterpret_cast<const uint4*>(p);
+  return ldg_nc_v4(p);
+}
+
+// Copy `n` token rows of `rb` bytes (rows[i], global) into shared memory `dst`
+// (row i at i * rb), all threads of the CTA, then synchronise.
+__device__ __forceinline__ void stage_rows(uint8_t* dst, const uint8_t* const* rows, int n, int rb) {
+  const int per = rb >> 4;
+  for (int i = threadIdx.x; i < n * per; i += blockDim.x) {
+    const int r = i / per, c = i - r * per;
+    reinterpret_cast<uint4*>(dst + r * rb)[c] = ldg_nc_v4(rows[r] + 16 * c);
+  }
+  __syncthreads();
 }
 
 // bf16 pair of the block's inputs (4j, 4j+1) [B = 0] or (4j+2, 4j+3) [B = 1].
@@ -66,7 +86,7 @@ __device__ __forceinline__ uint32_t fp4_frag(const uint4& w, const Fp4Scale& sc)
 // Eight MMAs of one MXFP4 k group for both tiles and all token chunks.
 // W[0..3] are the lane's blocks of rows (tile0 row g, tile0 row g+8, tile1 row g,
 // tile1 row g+8); xo is the byte offset of the block's 32 inputs in a token row.
-template <bool TWO, int CH, bool LO>
+template <bool TWO, int CH, bool LO, bool SB>
 __device__ __forceinline__ void fp4_group_mma(const uint4 (&W)[4], const Fp4Scale (&S)[4],
                                               const uint8_t* const (&br)[CH], int nch,
                                               bool ok, size_t xo, float (&acc)[2][CH][4],
@@ -108,7 +128,8 @@ __device__ __forceinline__ void fp4_group_mma(const uint4 (&W)[4], const Fp4Scal
 // br: byte pointers to the token rows (bf16) of the lane's B column per chunk.
 // LO: the token operand is an (hi, lo) bf16 pair whose lo half sits lo_off bytes
 // after the hi half in each row; both halves are multiplied by the same weights.
-template <int WFMT, int CH, bool LO>
+// SB: the token rows were staged in shared memory (br are generic pointers to it).
+template <int WFMT, int CH, bool LO, bool SB>
 __device__ __forceinline__ void stream_rows(const uint8_t* const (&R)[4],
                                             const uint8_t* const (&Sc)[4], int Kin, int c,
                                             const uint8_t* const (&br)[CH], int nch,
@@ -138,13 +159,13 @@ __device__ __forceinline__ void stream_rows(const uint8_t* const (&R)[4],
 #pragma unroll
           for (int ch = 0; ch < CH; ++ch) {
             if (ch < nch) {
-              const uint4 b = br[ch] ? ldg_nc_v4(br[ch] + o) : z;
+              const uint4 b = br[ch] ? ld_b16<SB>(br[ch] + o) : z;
               mma_bf16_16816(acc[0][ch], w0.x, w1.x, w0.y, w1.y, b.x, b.y);
               mma_bf16_16816(acc[0][ch], w0.z, w1.z, w0.w, w1.w, b.z, b.w);
               mma_bf16_16816(acc[1][ch], w2.x, w3.x, w2.y, w3.y, b.x, b.y);
               mma_bf16_16816(acc[1][ch], w2.z, w3.z, w2.w, w3.w, b.z, b.w);
               if (LO) {
-                const uint4 l = br[ch] ? ldg_nc_v4(br[ch] + lo_off + o) : z;
+                const uint4 l = br[ch] ? ld_b16<SB>(br[ch] + lo_off + o) : z;
                 mma_bf16_16816(acc[0][ch], w0.x, w1.x, w0.y, w1.y, l.x, l.y);
                 mma_bf16_16816(acc[0][ch], w0.z, w1.z, w0.w, w1.w, l.z, l.w);
                 mma_bf16_16816(acc[1][ch], w2.x, w3.x, w2.y, w3.y, l.x, l.y);
@@ -195,9 +216,9 @@ __device__ __forceinline__ void stream_rows(const uint8_t* const (&R)[4],
           for (int r = 0; r < 4; ++r) sc[r] = fp4_scale(cs[r]);
           const bool big = (cs[0] | cs[1] | cs[2] | cs[3]) > 128u;   // any scale > 128
           if (__any_sync(0xffffffffu, big))
-            fp4_group_mma<true, CH, LO>(cw, sc, br, nch, ok, (size_t)blk * 64, acc, lo_off);
+            fp4_group_mma<true, CH, LO, SB>(cw, sc, br, nch, ok, (size_t)blk * 64, acc, lo_off);
           else
-            fp4_group_mma<false, CH, LO>(cw, sc, br, nch, ok, (size_t)blk * 64, acc, lo_off);
+            fp4_group_mma<false, CH, LO, SB>(cw, sc, br, nch, ok, (size_t)blk * 64, acc, lo_off);
         }
       }
     }
@@ -219,10 +240,12 @@ __device__ __forceinline__ void zero_acc(float (&acc)[2][CH][4]) {
 // Tile i of a warp covers features f = f0 + 8i + g: its A rows 0..7 are their gate
 // rows and rows 8..15 their up rows, so the accumulator of lane (g, c) holds gate
 // (d0, d1) and up (d2, d3) of feature f for tokens 2c and 2c+1.
-template <int WFMT, int CH>
+// STAGE: a one-chunk item (CH == 1) copies its token rows to shared memory first.
+template <int WFMT, int CH, bool STAGE>
 __global__ void __launch_bounds__(kWarps * 32, 3)
 gateup_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__ x, int K,
                      uint16_t* __restrict__ h, int ldh, int interleaved) {
+  pdl_wait();
   const int a = blockIdx.y;
   if (a >= *rs.n_work) return;
   const int2 item = rs.work[a];                    // (virtual expert, first row within it)
@@ -233,10 +256,13 @@ gateup_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, c = lane & 3;
   const int f0 = blockIdx.x * kGateUpFeatures + warp * 16;
-  if (f0 >= ffv) return;                           // ff % 32 == 0: all 16 features valid
+  // ff % 32 == 0: a warp's 16 features are all valid or all past the end; a warp
+  // past the end still takes part in the row staging and its barriers.
+  const bool warp_on = f0 < ffv;
+  const int fclamp = warp_on ? f0 : 0;
   const int d = p.d;
   const int r0 = rs.offsets[v], cnt = min(rs.offsets[v + 1] - r0, item.y + 8 * CH);
-  const int fs[2] = {f0 + g, f0 + 8 + g};          // lane's feature in tile 0 / tile 1
+  const int fs[2] = {fclamp + g, fclamp + 8 + g};  // lane's feature in tile 0 / tile 1
 
   // Byte pointers of the lane's rows: R = {gate f0+g, up f0+g, gate f0+8+g, up f0+8+g}.
   const uint8_t* R[4];
@@ -273,19 +299,33 @@ gateup_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__
   }
   const int act = shared ? MOE_ACT_SWIGLU : p.act;
 
+  extern __shared__ __align__(16) uint8_t stage[];
   for (int p0 = item.y; p0 < cnt; p0 += 8 * CH) {
     const int nch = min(CH, (cnt - p0 + 7) / 8);
     const uint8_t* br[CH];
+    if (STAGE) {
+      // one chunk: stage its (up to 8) x rows in shared memory for all warps
+      __shared__ const uint8_t* rows[8];
+      const int n = min(8, cnt - p0);
+      if (threadIdx.x < n)
+        rows[threadIdx.x] = reinterpret_cast<const uint8_t*>(x + (size_t)(rs.row2slot[r0 + p0 + threadIdx.x] / K) * d);
+      __syncthreads();
+      stage_rows(stage, rows, n, d * 2);
+      br[0] = g < n ? stage + g * d * 2 : nullptr;
+    } else {
 #pragma unroll
-    for (int ch = 0; ch < CH; ++ch) {
-      const int i = p0 + 8 * ch + g;
-      br[ch] = (ch < nch && i < cnt)
-                   ? reinterpret_cast<const uint8_t*>(x + (size_t)(rs.row2slot[r0 + i] / K) * d)
-                   : nullptr;
+      for (int ch = 0; ch < CH; ++ch) {
+        const int i = p0 + 8 * ch + g;
+        br[ch] = (ch < nch && i < cnt)
+                     ? reinterpret_cast<const uint8_t*>(x + (size_t)(rs.row2slot[r0 + i] / K) * d)
+                     : nullptr;
+      }
     }
     float acc[2][CH][4];
     zero_acc(acc);
-    stream_rows<WFMT, CH, false>(R, Sc, d, c, br, nch, acc, 0);
+    if (!warp_on) continue;
+    stream_rows<WFMT, CH, false, STAGE>(R, Sc, d, c, br, nch, acc, 0);
+    pdl_trigger();
 
     // Epilogue: bias, activation, bf16 h rows (permuted order).
 #pragma unroll
@@ -317,10 +357,11 @@ gateup_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__
 // Tile i of a warp covers output rows o0 + 16i + {g, g+8}; the accumulator of
 // lane (g, c) holds rows (o, o+8) for tokens 2c, 2c+1.  Results (plus the down
 // bias) go to the token's slot row of Y.
-template <int WFMT, int CH>
+template <int WFMT, int CH, bool STAGE>
 __global__ void __launch_bounds__(kWarps * 32, 3)
 down_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__ h, int ldh,
                    float* __restrict__ Y) {
+  pdl_wait();
   const int a = blockIdx.y;
   if (a >= *rs.n_work) return;
   const int2 item = rs.work[a];                    // (virtual expert, first row within it)
@@ -331,8 +372,11 @@ down_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__ h
   const int d = p.d;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, c = lane & 3;
-  const int o0 = blockIdx.x * kDownRows + warp * 32;
-  if (o0 >= d) return;                             // d % 32 == 0: both 16-row tiles valid
+  const int o0raw = blockIdx.x * kDownRows + warp * 32;
+  // d % 32 == 0: both 16-row tiles of a warp are valid or both past the end; a warp
+  // past the end still takes part in the row staging and its barriers.
+  const bool warp_on = o0raw < d;
+  const int o0 = warp_on ? o0raw : 0;
   const int r0 = rs.offsets[v], cnt = min(rs.offsets[v + 1] - r0, item.y + 8 * CH);
 
   // R = {o0+g, o0+8+g, o0+16+g, o0+24+g}: tile i uses rows (2i, 2i+1) as MMA rows g, g+8.
@@ -355,18 +399,37 @@ down_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__ h
     if (!shared && p.dn_bias) bias[r] = bf16_to_f32(p.dn_bias[(size_t)v * d + o]);
   }
 
+  extern __shared__ __align__(16) uint8_t stage[];
   for (int p0 = item.y; p0 < cnt; p0 += 8 * CH) {
     const int nch = min(CH, (cnt - p0 + 7) / 8);
     const uint8_t* br[CH];
+    size_t lo_off = (size_t)ldh * 2;
+    if (STAGE) {
+      // one chunk: stage its (up to 8) h rows, hi then lo halves of Kin each
+      __shared__ const uint8_t* rows[16];
+      const int n = min(8, cnt - p0);
+      if (threadIdx.x < 2 * n) {
+        const int i = threadIdx.x >> 1;
+        rows[threadIdx.x] = reinterpret_cast<const uint8_t*>(h + (size_t)(r0 + p0 + i) * 2 * ldh) +
+                            (threadIdx.x & 1) * lo_off;
+      }
+      __syncthreads();
+      stage_rows(stage, rows, 2 * n, Kin * 2);
+      br[0] = g < n ? stage + 2 * g * Kin * 2 : nullptr;
+      lo_off = (size_t)Kin * 2;
+    } else {
 #pragma unroll
-    for (int ch = 0; ch < CH; ++ch) {
-      const int i = p0 + 8 * ch + g;
-      br[ch] = (ch < nch && i < cnt) ? reinterpret_cast<const uint8_t*>(h + (size_t)(r0 + i) * 2 * ldh)
-                                     : nullptr;
+      for (int ch = 0; ch < CH; ++ch) {
+        const int i = p0 + 8 * ch + g;
+        br[ch] = (ch < nch && i < cnt) ? reinterpret_cast<const uint8_t*>(h + (size_t)(r0 + i) * 2 * ldh)
+                                       : nullptr;
+      }
     }
     float acc[2][CH][4];
     zero_acc(acc);
-    stream_rows<WFMT, CH, true>(R, Sc, Kin, c, br, nch, acc, (size_t)ldh * 2);
+    if (!warp_on) continue;
+    stream_rows<WFMT, CH, true, STAGE>(R, Sc, Kin, c, br, nch, acc, lo_off);
+    pdl_trigger();
 
 #pragma unroll
     for (int ch = 0; ch < CH; ++ch) {
@@ -389,17 +452,37 @@ down_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__ h
 
 }  // namespace
 
+// Dynamic shared memory of a one-chunk item: its token rows (gate_up: x rows of
+// d inputs; down: h rows, hi and lo halves of the widest K).
+template <class Kern>
+static cudaError_t set_smem(Kern k, size_t bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
 cudaError_t launch_gateup_decode(const ExpertParams& p, int wfmt, int interleaved,
                                  const RouteState& rs, const uint16_t* x, int K, uint16_t* h,
                                  int ldh, int max_items, int chunks, cudaStream_t s) {
   const int ffmax = p.ff > p.sff ? p.ff : p.sff;
   dim3 grid((ffmax + kGateUpFeatures - 1) / kGateUpFeatures, max_items);
-  const bool one = chunks == 1;
-#define MOE_GU(F, C) gateup_decode_kernel<F, C><<<grid, kWarps * 32, 0, s>>>(p, rs, x, K, h, ldh, interleaved)
+  const size_t sm1 = (size_t)8 * p.d * 2;
+#define MOE_GU(F, C, ST, SM)                                                                  \
+  do {                                                                                        \
+    cudaError_t e = set_smem(gateup_decode_kernel<F, C, ST>, SM);                            \
+    if (e != cudaSuccess) return e;                                                           \
+    e = launch_pdl(gateup_decode_kernel<F, C, ST>, grid, dim3(kWarps * 32), SM, s, p, rs, x, K, h, \
+                   ldh, interleaved);                                                           \
+    if (e != cudaSuccess) return e;                                                             \
+  } while (0)
+  const bool st = chunks == 1 && sm1 <= kMaxStage;
   if (wfmt == MOE_WFMT_BF16) {
-    if (one) MOE_GU(MOE_WFMT_BF16, 1); else MOE_GU(MOE_WFMT_BF16, kMaxChunks);
+    if (st) MOE_GU(MOE_WFMT_BF16, 1, true, sm1);
+    else if (chunks == 1) MOE_GU(MOE_WFMT_BF16, 1, false, 0);
+    else MOE_GU(MOE_WFMT_BF16, kMaxChunks, false, 0);
   } else {
-    if (one) MOE_GU(MOE_WFMT_MXFP4, 1); else MOE_GU(MOE_WFMT_MXFP4, kMaxChunks);
+    if (st) MOE_GU(MOE_WFMT_MXFP4, 1, true, sm1);
+    else if (chunks == 1) MOE_GU(MOE_WFMT_MXFP4, 1, false, 0);
+    else MOE_GU(MOE_WFMT_MXFP4, kMaxChunks, false, 0);
   }
 #undef MOE_GU
   return cudaGetLastError();
@@ -409,12 +492,24 @@ cudaError_t launch_down_decode(const ExpertParams& p, int wfmt, const RouteState
                                const uint16_t* h, int ldh, float* Y, int max_items, int chunks,
                                cudaStream_t s) {
   dim3 grid((p.d + kDownRows - 1) / kDownRows, max_items);
-  const bool one = chunks == 1;
-#define MOE_DN(F, C) down_decode_kernel<F, C><<<grid, kWarps * 32, 0, s>>>(p, rs, h, ldh, Y)
+  const int kmax = p.ff > p.sff ? p.ff : p.sff;
+  const size_t sm1 = (size_t)16 * kmax * 2;
+#define MOE_DN(F, C, ST, SM)                                                          \
+  do {                                                                                \
+    cudaError_t e = set_smem(down_decode_kernel<F, C, ST>, SM);                      \
+    if (e != cudaSuccess) return e;                                                   \
+    e = launch_pdl(down_decode_kernel<F, C, ST>, grid, dim3(kWarps * 32), SM, s, p, rs, h, ldh, Y); \
+    if (e != cudaSuccess) return e;                                                   \
+  } while (0)
+  const bool st = chunks == 1 && sm1 <= kMaxStage;
   if (wfmt == MOE_WFMT_BF16) {
-    if (one) MOE_DN(MOE_WFMT_BF16, 1); else MOE_DN(MOE_WFMT_BF16, kMaxChunks);
+    if (st) MOE_DN(MOE_WFMT_BF16, 1, true, sm1);
+    else if (chunks == 1) MOE_DN(MOE_WFMT_BF16, 1, false, 0);
+    else MOE_DN(MOE_WFMT_BF16, kMaxChunks, false, 0);
   } else {
-    if (one) MOE_DN(MOE_WFMT_MXFP4, 1); else MOE_DN(MOE_WFMT_MXFP4, kMaxChunks);
+    if (st) MOE_DN(MOE_WFMT_MXFP4, 1, true, sm1);
+    else if (chunks == 1) MOE_DN(MOE_WFMT_MXFP4, 1, false, 0);
+    else MOE_DN(MOE_WFMT_MXFP4, kMaxChunks, false, 0);
   }
 #undef MOE_DN
   return cudaGetLastError();

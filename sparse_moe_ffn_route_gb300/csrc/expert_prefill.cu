@@ -186,6 +186,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint32_t* status = g.rs.status;
   volatile int* abort = &abort_s;
+  pdl_wait();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -459,6 +460,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     }
   }
 
+  pdl_trigger();
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
@@ -469,6 +471,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 __global__ void __launch_bounds__(256)
 gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ row2slot, int S,
                    int K, int d, uint16_t* __restrict__ xp) {
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int nvec = d / 8;
   for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < S; r += (gridDim.x * blockDim.x) >> 5) {
@@ -477,6 +480,7 @@ gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ r
     uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)r * d);
     for (int i = lane; i < nvec; i += 32) dst[i] = ldg_nc_v4(src + i);
   }
+  pdl_trigger();
 }
 
 // MXFP4 scales [E, rows, nblk] -> [E, nblk, rows], so that the scales of one
@@ -484,6 +488,8 @@ gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ r
 __global__ void __launch_bounds__(256)
 transpose_scales_kernel(const uint8_t* __restrict__ src, int E, int rows, int nblk,
                         uint8_t* __restrict__ dst) {
+  pdl_wait();
+  pdl_trigger();
   const long long n = (long long)E * rows * nblk;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
@@ -588,9 +594,8 @@ cudaError_t launch_gemm(const CUtensorMap& tA, const CUtensorMap& tB0, const CUt
   const long long tiles = (long long)max_mtiles * g.nt_max;
   int grid = sm_count();
   if (tiles < grid) grid = (int)(tiles > 0 ? tiles : 1);
-  grouped_gemm_kernel<FP4, DUAL><<<grid, Lay<FP4, DUAL>::kThreads, Lay<FP4, DUAL>::kSmemBytes, s>>>(
-      tA, tB0, tB1, tS0, tS1, g);
-  return cudaGetLastError();
+  return launch_pdl(grouped_gemm_kernel<FP4, DUAL>, dim3(grid), dim3(Lay<FP4, DUAL>::kThreads),
+                    Lay<FP4, DUAL>::kSmemBytes, s, tA, tB0, tB1, tS0, tS1, g);
 }
 
 }  // namespace
@@ -616,17 +621,18 @@ cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* row2slot, int S
   int blocks = (S + 7) / 8;
   if (blocks > 152 * 8) blocks = 152 * 8;
   if (blocks < 1) blocks = 1;
-  gather_rows_kernel<<<blocks, 256, 0, s>>>(x, row2slot, S, K, d, xp);
-  return cudaGetLastError();
+  return launch_pdl(gather_rows_kernel, dim3(blocks), dim3(256), 0, s, x, row2slot, S, K, d, xp);
 }
 
 cudaError_t launch_transpose_scales(const ExpertParams& p, uint8_t* scratch, cudaStream_t s) {
   const long long n1 = (long long)p.E * 2 * p.ff * (p.d / 32);
   const long long n2 = (long long)p.E * p.d * (p.ff / 32);
-  transpose_scales_kernel<<<152 * 4, 256, 0, s>>>(p.gu_scales, p.E, 2 * p.ff, p.d / 32, scratch);
-  transpose_scales_kernel<<<152 * 4, 256, 0, s>>>(p.dn_scales, p.E, p.d, p.ff / 32, scratch + n1);
   (void)n2;
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(transpose_scales_kernel, dim3(152 * 4), dim3(256), 0, s, p.gu_scales, p.E,
+                             2 * p.ff, p.d / 32, scratch);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(transpose_scales_kernel, dim3(152 * 4), dim3(256), 0, s, p.dn_scales, p.E, p.d,
+                    p.ff / 32, scratch + n1);
 }
 
 cudaError_t launch_gateup_prefill(const ExpertParams& p, int wfmt, int interleaved,

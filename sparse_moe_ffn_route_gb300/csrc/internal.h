@@ -10,6 +10,25 @@
 
 namespace moe {
 
+// Launch with programmatic stream serialization: the kernel may begin launching
+// while its predecessor on the stream finishes; it calls pdl_wait() before reading
+// anything the predecessor wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Bits of the device status word kept at the start of the workspace.
 enum : uint32_t {
   STATUS_BAD_EXPERT_ID = 1u << 0,   // a routing id outside [0, E) was seen and skipped

@@ -181,10 +181,17 @@ int path_for(const moe_cfg_t* c, int T) {
 }
 
 // Caller-owned events recorded at phase boundaries (moe_set_phase_events).
+// With two events only the start ([0]) and the end ([6]) of the call are recorded,
+// which leaves consecutive kernels free to overlap their launches.
 thread_local void* const* g_phase_events = nullptr;
+thread_local int g_phase_n = 0;
 
 inline cudaError_t mark_phase(int i, cudaStream_t s) {
   if (!g_phase_events) return cudaSuccess;
+  if (g_phase_n == 2) {
+    if (i != 0 && i != 6) return cudaSuccess;
+    return cudaEventRecord(static_cast<cudaEvent_t>(g_phase_events[i == 0 ? 0 : 1]), s);
+  }
   return cudaEventRecord(static_cast<cudaEvent_t>(g_phase_events[i]), s);
 }
 
@@ -415,11 +422,13 @@ int moe_mxfp4_to_bf16(const void* blocks, const void* scales, int64_t rows, int3
 }
 
 int moe_set_phase_events(void* const* events, int32_t n_events) {
-  if (events && n_events < 7) return MOE_ERR_INVALID_ARG;
+  if (events && n_events != 2 && n_events < 7) return MOE_ERR_INVALID_ARG;
+  const int need = n_events == 2 ? 2 : 7;
   if (events)
-    for (int i = 0; i < 7; ++i)
+    for (int i = 0; i < need; ++i)
       if (!events[i]) return MOE_ERR_INVALID_ARG;
   g_phase_events = events;
+  g_phase_n = events ? need : 0;
   return MOE_OK;
 }
 

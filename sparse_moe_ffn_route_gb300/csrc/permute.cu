@@ -64,6 +64,7 @@ permute_kernel(RouteState rs, int S, int E1, int tpg) {
   __shared__ int2 warp_tot[32];
   __shared__ int2 total;
   const int tid = threadIdx.x, lane = tid & 31;
+  pdl_wait();
 
   // This is the first kernel of a call that checks anything: start a clean status.
   if (tid == 0) *rs.status = 0u;
@@ -121,13 +122,13 @@ permute_kernel(RouteState rs, int S, int E1, int tpg) {
         flag_status(rs.status, STATUS_ROW_OVERFLOW);
     }
   }
+  pdl_trigger();
 }
 
 }  // namespace
 
 cudaError_t launch_permute(const RouteState& rs, int S, int E1, int tpg, cudaStream_t s) {
-  permute_kernel<<<1, kPermuteThreads, 0, s>>>(rs, S, E1, tpg);
-  return cudaGetLastError();
+  return launch_pdl(permute_kernel, dim3(1), dim3(kPermuteThreads), 0, s, rs, S, E1, tpg);
 }
 
 }  // namespace moe

@@ -29,6 +29,8 @@ router_logits_kernel(const uint16_t* __restrict__ x, int T, int d, const uint16_
                      float* __restrict__ logits, int ldl) {
   constexpr int TM = 16 * MT, TN = 8 * NT;
   __shared__ float part[WARPS][TM][TN + 1];
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, c = lane & 3;
   const int t0 = blockIdx.x * TM;
@@ -119,6 +121,8 @@ router_select_kernel(const float* __restrict__ logits, int ldl, int T, int E, in
                      int norm_topk_prob, float scale, int has_shared, int32_t* __restrict__ ids_out,
                      float* __restrict__ w_out, float* __restrict__ sgate_out,
                      int32_t* __restrict__ slot_expert, float* __restrict__ slot_w) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kSelectWarps + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -200,6 +204,8 @@ __global__ void ingest_routing_kernel(const int32_t* __restrict__ ids, const flo
                                       const float* __restrict__ sgate, int T, int E, int k,
                                       int has_shared, int32_t* __restrict__ slot_expert,
                                       float* __restrict__ slot_w) {
+  pdl_wait();
+  pdl_trigger();
   const int K = k + has_shared;
   const long n = (long)T * K;
   for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
@@ -226,10 +232,12 @@ cudaError_t launch_router_logits(const uint16_t* x, int T, int d, const uint16_t
   const int E1 = E + (wsh ? 1 : 0);
   if (T <= 256) {   // latency-bound: many small CTAs, all loads of a warp in flight at once
     dim3 grid((T + 15) / 16, (E1 + 15) / 16);
-    router_logits_kernel<1, 2, 16, 6><<<grid, 16 * 32, 0, s>>>(x, T, d, w_r, bias, wsh, E, logits, ldl);
+    return launch_pdl(router_logits_kernel<1, 2, 16, 6>, grid, dim3(16 * 32), 0, s, x, T, d, w_r,
+                      bias, wsh, E, logits, ldl);
   } else {          // throughput-bound: larger tiles, fewer re-reads of x and W_r from L2
     dim3 grid((T + 63) / 64, (E1 + 31) / 32);
-    router_logits_kernel<4, 4, 4, 2><<<grid, 4 * 32, 0, s>>>(x, T, d, w_r, bias, wsh, E, logits, ldl);
+    return launch_pdl(router_logits_kernel<4, 4, 4, 2>, grid, dim3(4 * 32), 0, s, x, T, d, w_r, bias,
+                      wsh, E, logits, ldl);
   }
   return cudaGetLastError();
 }
@@ -241,9 +249,9 @@ cudaError_t launch_router_select(const float* logits, int ldl, int T, int E, int
   dim3 grid((T + kSelectWarps - 1) / kSelectWarps);
   const int epl = (E + 31) / 32;
 #define MOE_SELECT(N)                                                                     \
-  router_select_kernel<N><<<grid, kSelectWarps * 32, 0, s>>>(                             \
-      logits, ldl, T, E, k, norm_topk_prob, scale, has_shared, ids_out, w_out, sgate_out, \
-      slot_expert, slot_w)
+  return launch_pdl(router_select_kernel<N>, grid, dim3(kSelectWarps * 32), 0, s, logits, ldl, T, \
+                    E, k, norm_topk_prob, scale, has_shared, ids_out, w_out, sgate_out,       \
+                    slot_expert, slot_w)
   if (epl <= 1) MOE_SELECT(1);
   else if (epl <= 2) MOE_SELECT(2);
   else if (epl <= 4) MOE_SELECT(4);
@@ -259,9 +267,8 @@ cudaError_t launch_ingest_routing(const int32_t* ids, const float* w, const floa
                                   float* slot_w, cudaStream_t s) {
   const long n = (long)T * (k + has_shared);
   const int blocks = (int)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
-  ingest_routing_kernel<<<blocks, 256, 0, s>>>(ids, w, sgate, T, E, k, has_shared, slot_expert,
-                                                slot_w);
-  return cudaGetLastError();
+  return launch_pdl(ingest_routing_kernel, dim3(blocks), dim3(256), 0, s, ids, w, sgate, T, E, k,
+                    has_shared, slot_expert, slot_w);
 }
 
 }  // namespace moe
