@@ -77,6 +77,51 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
   return r;
 }
 
+// ---------------------------------------------------------------- f16 operands
+
+// Two fp32 -> f16x2 (round to nearest even); `lo` lands in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ void unpack_f16x2(uint32_t v, float& lo, float& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi) : "r"(v));
+}
+
+__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// D(16x8, fp32) += A(16x16, f16) * B(16x8, f16); same fragment layout as the bf16 form.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 2^e as fp32 for -126 <= e <= 127.
+__device__ __forceinline__ float exp2i(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
+
+// The four code bytes of `w` (eight E2M1 values, low nibble first) as exact f16
+// pairs, byte t -> o[t] with its low nibble in the low half.
+__device__ __forceinline__ void e2m1x8_to_f16(uint32_t w, uint32_t (&o)[4]) {
+  asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
+      "mov.b32 {q0, q1, q2, q3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, q0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, q1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, q2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, q3;\n\t}"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+      : "r"(w));
+}
+
 // ---------------------------------------------------------------- MXFP4 decoding
 //
 // An E2M1 code c = s e1 e0 m (bit 3 sign, bits 2..1 exponent with bias 1, bit 0
@@ -88,7 +133,8 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
 // scale byte whose result is a normal or subnormal bf16.
 
 // Scale factor(s) for one E8M0 byte: the value multiplies a decoded pair by
-// `first` and then, when `two` is set, by `second`.
+// `first` and then, when `two` is set, by `second` (1.0 otherwise, so that a warp
+// that takes the two-multiply form for all of its rows stays exact).
 struct Fp4Scale {
   uint32_t first, second;
   bool two;
@@ -99,7 +145,7 @@ __device__ __forceinline__ Fp4Scale fp4_scale(uint32_t s) {
   if (s <= 128u) {                       // 2^(s-1): exponent field s+126 <= 254
     uint32_t b = (s + 126u) << 7;
     r.first = b | (b << 16);
-    r.second = 0;
+    r.second = 0x3F803F80u;              // 1.0: a caller that multiplies twice
     r.two = false;
   } else if (s < 255u) {                 // 2^126 then 2^(s-127)
     r.first = 0x7E807E80u;
@@ -108,7 +154,7 @@ __device__ __forceinline__ Fp4Scale fp4_scale(uint32_t s) {
     r.two = true;
   } else {                               // 0xFF is NaN in E8M0
     r.first = 0x7FC07FC0u;
-    r.second = 0;
+    r.second = 0x3F803F80u;
     r.two = false;
   }
   return r;

@@ -225,6 +225,222 @@ __device__ __forceinline__ void stream_rows(const uint8_t* const (&R)[4],
   }
 }
 
+// ---------------------------------------------------------------- MXFP4 x f16 tokens
+//
+// One-chunk MXFP4 items stage their token rows as f16, each row scaled by a power
+// of two 2^e (e per token) that puts its largest magnitude in [2^14, 2^15): bf16
+// rows convert exactly, and an (hi, lo) h row keeps 11 significant bits.  A weight
+// code then decodes with one conversion instruction per byte (E2M1 values are
+// exact in f16) and one f16 multiply by 2^(s - 127), which is exact while the
+// scale byte s lies in [113, 140] (products stay normal-or-exact and below 65504).
+// A k group in which some lane sees a scale outside that range takes the bf16
+// decode instead and splits each f16 token value into an exact bf16 (hi, lo)
+// pair.  The accumulators carry the token's 2^e; the epilogues remove it.
+constexpr uint32_t kF16ScaleLo = 113, kF16ScaleSpan = 27;   // fast scale bytes: [113, 140]
+
+// 16-byte units per staged f16 row: a multiple of 8 plus one, so that rows g of
+// the 8 token columns start in different bank groups.
+__host__ __device__ __forceinline__ int f16_row_units(int kin) { return (((kin >> 3) + 7) & ~7) + 1; }
+
+// Unit u of a staged row sits at u ^ ((u >> 2) & 2): the lanes c and c + 2 of a
+// quad, whose blocks are 128 bytes apart, then read different bank groups.
+__device__ __forceinline__ int f16_unit(int u) { return u ^ ((u >> 2) & 2); }
+
+// Exponent e of a token row from the bf16 bits of its largest magnitude.
+__device__ __forceinline__ int token_exp(uint32_t m16) {
+  const int E = (int)(m16 >> 7);
+  if (m16 == 0 || E == 255) return 0;
+  return min(141 - E, 126);
+}
+
+// Stage n (<= 8) token rows of kin values, one warp per row, as scaled f16 (layout
+// above, row i at unit i * ru); esc[i] receives the row's exponent.  rows[i] is a
+// bf16 row in global memory; PAIR: it is the hi half of an (hi, lo) pair whose lo
+// half sits lo_off bytes further, and the staged value is hi + lo.
+template <bool PAIR>
+__device__ __forceinline__ void stage_rows_f16(uint8_t* dst, const uint8_t* const* rows, int n,
+                                               int kin, int ru, size_t lo_off, int* esc) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per = kin >> 3;
+  for (int r = warp; r < n; r += kWarps) {
+    uint4* drow = reinterpret_cast<uint4*>(dst) + (size_t)r * ru;
+    uint32_t m2 = 0;
+    for (int u = lane; u < per; u += 32) {
+      const uint4 v = ldg_nc_v4(rows[r] + 16 * u);
+      drow[f16_unit(u)] = v;
+      const uint32_t mask = 0x7FFF7FFFu;
+      m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(v.x & mask, v.y & mask), __vmaxu2(v.z & mask, v.w & mask)));
+    }
+    // the magnitude of lo is below half an ulp of hi: the max of hi sets e
+    const int e = token_exp(__reduce_max_sync(0xffffffffu, max(m2 & 0xffffu, m2 >> 16)));
+    const float s = exp2i(e);
+    for (int u = lane; u < per; u += 32) {
+      uint4* q = drow + f16_unit(u);
+      const uint4 v = *q;                      // written by this lane above
+      uint4 l = make_uint4(0, 0, 0, 0);
+      if (PAIR) l = ldg_nc_v4(rows[r] + lo_off + 16 * u);
+      uint4 o;
+      o.x = pack_f16x2(s * (bf16_lo(v.x) + bf16_lo(l.x)), s * (bf16_hi(v.x) + bf16_hi(l.x)));
+      o.y = pack_f16x2(s * (bf16_lo(v.y) + bf16_lo(l.y)), s * (bf16_hi(v.y) + bf16_hi(l.y)));
+      o.z = pack_f16x2(s * (bf16_lo(v.z) + bf16_lo(l.z)), s * (bf16_hi(v.z) + bf16_hi(l.z)));
+      o.w = pack_f16x2(s * (bf16_lo(v.w) + bf16_lo(l.w)), s * (bf16_hi(v.w) + bf16_hi(l.w)));
+      *q = o;
+    }
+    if (lane == 0) esc[r] = e;
+  }
+  __syncthreads();
+}
+
+// Word q of a 16-byte block of codes.
+__device__ __forceinline__ uint32_t word_of(const uint4& w, int q) {
+  return q == 0 ? w.x : q == 1 ? w.y : q == 2 ? w.z : w.w;
+}
+
+// One MXFP4 k group (the lane's block of each of its 4 rows) against the staged
+// f16 token column b0 (null: empty column), fast decode: all scales in range.
+// Word q of a block holds inputs 8q..8q+7 and feeds MMA j = 2q (bytes 4q, 4q+1)
+// and j = 2q + 1 (bytes 4q+2, 4q+3); the token operand is the matching 16 bytes.
+__device__ __forceinline__ void fp4h_group_fast(const uint4 (&W)[4], const uint32_t (&S)[4],
+                                                const uint8_t* b0, const int (&qo)[4],
+                                                float (&acc)[2][1][4]) {
+  uint32_t sh[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const uint32_t e = S[r] - 112u;           // f16 exponent field of 2^(s - 127)
+    sh[r] = (e << 10) | (e << 26);
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t f[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      e2m1x8_to_f16(word_of(W[r], q), f[r]);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) f[r][t] = f16x2_mul(f[r][t], sh[r]);
+    }
+    const uint4 b = b0 ? *reinterpret_cast<const uint4*>(b0 + qo[q]) : make_uint4(0, 0, 0, 0);
+    mma_f16_16816(acc[0][0], f[0][0], f[1][0], f[0][1], f[1][1], b.x, b.y);
+    mma_f16_16816(acc[1][0], f[2][0], f[3][0], f[2][1], f[3][1], b.x, b.y);
+    mma_f16_16816(acc[0][0], f[0][2], f[1][2], f[0][3], f[1][3], b.z, b.w);
+    mma_f16_16816(acc[1][0], f[2][2], f[3][2], f[2][3], f[3][3], b.z, b.w);
+  }
+}
+
+// bf16 pair of byte t of `word` (low nibble low), scaled (fp4_frag with a byte
+// index known after unrolling).
+__device__ __forceinline__ uint32_t fp4_byte_bf16(uint32_t word, int t, const Fp4Scale& sc, bool two) {
+  const uint32_t lo = word & 0x0F0F0F0Fu, hi = (word >> 4) & 0x0F0F0F0Fu;
+  const uint32_t sel = (uint32_t)t | (0x8u << 4) | ((uint32_t)(4 + t) << 8) | (0x8u << 12);
+  uint32_t p;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(p) : "r"(lo), "r"(hi), "r"(sel));
+  uint32_t v = bf16x2_mul((p * 0x1040u) & 0x81C081C0u, sc.first);
+  if (two) v = bf16x2_mul(v, sc.second);
+  return v;
+}
+
+// The same k group when some scale is out of the fast range: bf16 weights, and
+// each f16 token value split into bf16 hi + lo (exact: 11 = 8 + 3 bits).
+template <bool TWO>
+__device__ __forceinline__ void fp4h_group_split(const uint4 (&W)[4], const Fp4Scale (&S)[4],
+                                                 const uint8_t* b0, const int (&qo)[4],
+                                                 float (&acc)[2][1][4]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 b = b0 ? *reinterpret_cast<const uint4*>(b0 + qo[q]) : make_uint4(0, 0, 0, 0);
+    const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+    uint32_t bh[4], bl[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      float v0, v1;
+      unpack_f16x2(bw[t], v0, v1);
+      bh[t] = pack_bf16x2(v0, v1);
+      bl[t] = pack_bf16x2(v0 - bf16_lo(bh[t]), v1 - bf16_hi(bh[t]));
+    }
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      uint32_t a[4][2];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const uint32_t w = word_of(W[r], q);
+        a[r][0] = fp4_byte_bf16(w, 2 * jj, S[r], TWO);
+        a[r][1] = fp4_byte_bf16(w, 2 * jj + 1, S[r], TWO);
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        mma_bf16_16816(acc[i][0], a[2 * i][0], a[2 * i + 1][0], a[2 * i][1], a[2 * i + 1][1],
+                       bh[2 * jj], bh[2 * jj + 1]);
+        mma_bf16_16816(acc[i][0], a[2 * i][0], a[2 * i + 1][0], a[2 * i][1], a[2 * i + 1][1],
+                       bl[2 * jj], bl[2 * jj + 1]);
+      }
+    }
+  }
+}
+
+// stream_rows for MXFP4 weights against one staged f16 token chunk (column b0 of
+// this lane, null when empty): the same register ring of k groups.
+__device__ __forceinline__ void stream_rows_fp4h(const uint8_t* const (&R)[4],
+                                                 const uint8_t* const (&Sc)[4], int Kin, int c,
+                                                 const uint8_t* b0, float (&acc)[2][1][4]) {
+  constexpr int P = kDepthFp4;
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  const int nb = Kin >> 5;
+  const int ng = (nb + 3) >> 2;
+  const int xq = c & 2;                        // the unit swizzle of this lane's blocks
+  uint4 W[P][4];
+  uint32_t S[P][4];
+#pragma unroll
+  for (int s = 0; s < P; ++s) {
+    const int blk = 4 * s + c;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const bool ok = s < ng && blk < nb;
+      W[s][r] = ok ? ldg_stream_v4(R[r] + (size_t)blk * 16) : z;
+      S[s][r] = ok ? Sc[r][blk] : 127u;
+    }
+  }
+  for (int g0 = 0; g0 < ng; g0 += P) {
+#pragma unroll
+    for (int s = 0; s < P; ++s) {
+      const int gg = g0 + s;
+      if (gg < ng) {
+        const uint4 cw[4] = {W[s][0], W[s][1], W[s][2], W[s][3]};
+        const uint32_t cs[4] = {S[s][0], S[s][1], S[s][2], S[s][3]};
+        const int gn = gg + P;
+        if (gn < ng) {
+          const int blk = 4 * gn + c;
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const bool ok = blk < nb;
+            W[s][r] = ok ? ldg_stream_v4(R[r] + (size_t)blk * 16) : z;
+            S[s][r] = ok ? Sc[r][blk] : 127u;
+          }
+        }
+        const int blk = 4 * gg + c;
+        // past the last block the codes are zero and the token operand must be too
+        const uint8_t* bb = blk < nb ? b0 : nullptr;
+        int qo[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) qo[q] = 64 * blk + 16 * (q ^ xq);
+        bool fast = true;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) fast = fast && (cs[r] - kF16ScaleLo <= kF16ScaleSpan);
+        if (__all_sync(0xffffffffu, fast)) {
+          fp4h_group_fast(cw, cs, bb, qo, acc);
+        } else {
+          Fp4Scale sc[4];
+#pragma unroll
+          for (int r = 0; r < 4; ++r) sc[r] = fp4_scale(cs[r]);
+          const bool big = (cs[0] | cs[1] | cs[2] | cs[3]) > 128u;
+          if (__any_sync(0xffffffffu, big))
+            fp4h_group_split<true>(cw, sc, bb, qo, acc);
+          else
+            fp4h_group_split<false>(cw, sc, bb, qo, acc);
+        }
+      }
+    }
+  }
+}
+
 template <int CH>
 __device__ __forceinline__ void zero_acc(float (&acc)[2][CH][4]) {
 #pragma unroll
@@ -299,7 +515,10 @@ gateup_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__
   }
   const int act = shared ? MOE_ACT_SWIGLU : p.act;
 
+  // MXFP4 with staged rows: f16 token operand (see "MXFP4 x f16 tokens")
+  constexpr bool H16 = WFMT == MOE_WFMT_MXFP4 && STAGE;
   extern __shared__ __align__(16) uint8_t stage[];
+  __shared__ int esc[8];                           // H16: token exponents
   for (int p0 = item.y; p0 < cnt; p0 += 8 * CH) {
     const int nch = min(CH, (cnt - p0 + 7) / 8);
     const uint8_t* br[CH];
@@ -310,8 +529,14 @@ gateup_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__
       if (threadIdx.x < n)
         rows[threadIdx.x] = reinterpret_cast<const uint8_t*>(x + (size_t)(rs.row2slot[r0 + p0 + threadIdx.x] / K) * d);
       __syncthreads();
-      stage_rows(stage, rows, n, d * 2);
-      br[0] = g < n ? stage + g * d * 2 : nullptr;
+      if (H16) {
+        const int ru = f16_row_units(d);
+        stage_rows_f16<false>(stage, rows, n, d, ru, 0, esc);
+        br[0] = g < n ? stage + (size_t)g * ru * 16 : nullptr;
+      } else {
+        stage_rows(stage, rows, n, d * 2);
+        br[0] = g < n ? stage + g * d * 2 : nullptr;
+      }
     } else {
 #pragma unroll
       for (int ch = 0; ch < CH; ++ch) {
@@ -324,7 +549,10 @@ gateup_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__
     float acc[2][CH][4];
     zero_acc(acc);
     if (!warp_on) continue;
-    stream_rows<WFMT, CH, false, STAGE>(R, Sc, d, c, br, nch, acc, 0);
+    if constexpr (H16)
+      stream_rows_fp4h(R, Sc, d, c, br[0], acc);
+    else
+      stream_rows<WFMT, CH, false, STAGE>(R, Sc, d, c, br, nch, acc, 0);
     pdl_trigger();
 
     // Epilogue: bias, activation, bf16 h rows (permuted order).
@@ -336,8 +564,9 @@ gateup_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__
         for (int q = 0; q < 2; ++q) {
           const int ti = p0 + 8 * ch + 2 * c + q;
           if (ch < nch && ti < cnt) {
-            const float gv = acc[i][ch][q] + bias_g[i];
-            const float uv = acc[i][ch][2 + q] + bias_u[i];
+            const float un = H16 ? exp2i(-esc[2 * c + q]) : 1.f;   // undo the token scale
+            const float gv = acc[i][ch][q] * un + bias_g[i];
+            const float uv = acc[i][ch][2 + q] * un + bias_u[i];
             const float hv = act == MOE_ACT_SWIGLU ? act_swiglu(gv, uv)
                                                    : act_clamped(gv, uv, p.limit, p.alpha);
             // h as a pair of bf16 (hi, lo = bf16(h - hi)): ~16 significant bits
@@ -399,12 +628,24 @@ down_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__ h
     if (!shared && p.dn_bias) bias[r] = bf16_to_f32(p.dn_bias[(size_t)v * d + o]);
   }
 
+  constexpr bool H16 = WFMT == MOE_WFMT_MXFP4 && STAGE;
   extern __shared__ __align__(16) uint8_t stage[];
+  __shared__ int esc[8];                           // H16: token exponents
   for (int p0 = item.y; p0 < cnt; p0 += 8 * CH) {
     const int nch = min(CH, (cnt - p0 + 7) / 8);
     const uint8_t* br[CH];
     size_t lo_off = (size_t)ldh * 2;
-    if (STAGE) {
+    if (H16) {
+      // one chunk: stage its (up to 8) h rows as single scaled f16 rows
+      __shared__ const uint8_t* rows[8];
+      const int n = min(8, cnt - p0);
+      if (threadIdx.x < n)
+        rows[threadIdx.x] = reinterpret_cast<const uint8_t*>(h + (size_t)(r0 + p0 + threadIdx.x) * 2 * ldh);
+      __syncthreads();
+      const int ru = f16_row_units(Kin);
+      stage_rows_f16<true>(stage, rows, n, Kin, ru, lo_off, esc);
+      br[0] = g < n ? stage + (size_t)g * ru * 16 : nullptr;
+    } else if (STAGE) {
       // one chunk: stage its (up to 8) h rows, hi then lo halves of Kin each
       __shared__ const uint8_t* rows[16];
       const int n = min(8, cnt - p0);
@@ -428,7 +669,10 @@ down_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__ h
     float acc[2][CH][4];
     zero_acc(acc);
     if (!warp_on) continue;
-    stream_rows<WFMT, CH, true, STAGE>(R, Sc, Kin, c, br, nch, acc, lo_off);
+    if constexpr (H16)
+      stream_rows_fp4h(R, Sc, Kin, c, br[0], acc);
+    else
+      stream_rows<WFMT, CH, true, STAGE>(R, Sc, Kin, c, br, nch, acc, lo_off);
     pdl_trigger();
 
 #pragma unroll
@@ -438,11 +682,12 @@ down_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__ h
         const int ti = p0 + 8 * ch + 2 * c + q;
         if (ch < nch && ti < cnt) {
           float* yrow = Y + (size_t)rs.row2slot[r0 + ti] * d;
+          const float un = H16 ? exp2i(-esc[2 * c + q]) : 1.f;     // undo the token scale
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
             const int o = o0 + 16 * i + g;
-            yrow[o] = acc[i][ch][q] + bias[2 * i];
-            yrow[o + 8] = acc[i][ch][2 + q] + bias[2 * i + 1];
+            yrow[o] = acc[i][ch][q] * un + bias[2 * i];
+            yrow[o + 8] = acc[i][ch][2 + q] * un + bias[2 * i + 1];
           }
         }
       }
@@ -453,7 +698,7 @@ down_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__ h
 }  // namespace
 
 // Dynamic shared memory of a one-chunk item: its token rows (gate_up: x rows of
-// d inputs; down: h rows, hi and lo halves of the widest K).
+// d inputs; down: h rows of the widest K).
 template <class Kern>
 static cudaError_t set_smem(Kern k, size_t bytes) {
   if (bytes <= 48 * 1024) return cudaSuccess;
@@ -465,7 +710,8 @@ cudaError_t launch_gateup_decode(const ExpertParams& p, int wfmt, int interleave
                                  int ldh, int max_items, int chunks, cudaStream_t s) {
   const int ffmax = p.ff > p.sff ? p.ff : p.sff;
   dim3 grid((ffmax + kGateUpFeatures - 1) / kGateUpFeatures, max_items);
-  const size_t sm1 = (size_t)8 * p.d * 2;
+  // staged x rows of a one-chunk item: bf16, or scaled f16 in padded rows (MXFP4)
+  const size_t sm1 = wfmt == MOE_WFMT_BF16 ? (size_t)8 * p.d * 2 : (size_t)8 * f16_row_units(p.d) * 16;
 #define MOE_GU(F, C, ST, SM)                                                                  \
   do {                                                                                        \
     cudaError_t e = set_smem(gateup_decode_kernel<F, C, ST>, SM);                            \
@@ -493,7 +739,8 @@ cudaError_t launch_down_decode(const ExpertParams& p, int wfmt, const RouteState
                                cudaStream_t s) {
   dim3 grid((p.d + kDownRows - 1) / kDownRows, max_items);
   const int kmax = p.ff > p.sff ? p.ff : p.sff;
-  const size_t sm1 = (size_t)16 * kmax * 2;
+  // staged h rows of a one-chunk item: bf16 (hi, lo) pairs, or one scaled f16 row (MXFP4)
+  const size_t sm1 = wfmt == MOE_WFMT_BF16 ? (size_t)16 * kmax * 2 : (size_t)8 * f16_row_units(kmax) * 16;
 #define MOE_DN(F, C, ST, SM)                                                          \
   do {                                                                                \
     cudaError_t e = set_smem(down_decode_kernel<F, C, ST>, SM);                      \
