@@ -74,8 +74,13 @@ enum {
 };
 enum {
   MOE_PATH_AUTO = 0,    /* pick by mean tokens per expert, T*k/E */
-  MOE_PATH_DECODE = 1,  /* weight-streaming grouped matvec (mma.sync) */
-  MOE_PATH_PREFILL = 2  /* grouped GEMM on tcgen05 / TMEM fed by TMA */
+  MOE_PATH_DECODE = 1,  /* weight-streaming grouped matvec (mma.sync); MXFP4 weights of
+                           experts with at most 4 tokens on average stream through a
+                           TMA-fed shared-memory ring */
+  MOE_PATH_PREFILL = 2, /* grouped GEMM on tcgen05 / TMEM fed by TMA */
+  MOE_PATH_DECODE_REGISTERS = 3  /* MOE_PATH_DECODE with every weight load going straight
+                                    to registers (no shared-memory ring); same results to
+                                    within rounding, kept for comparison and tests */
 };
 
 typedef struct {

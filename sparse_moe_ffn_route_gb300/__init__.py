@@ -32,7 +32,7 @@ STATUS_NAMES = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED
 GATING_SOFTMAX_TOPK_RENORM, GATING_TOPK_SOFTMAX = 0, 1
 ACT_SWIGLU, ACT_CLAMPED_GLU = 0, 1
 WFMT_BF16, WFMT_MXFP4 = 0, 1
-PATH_AUTO, PATH_DECODE, PATH_PREFILL = 0, 1, 2
+PATH_AUTO, PATH_DECODE, PATH_PREFILL, PATH_DECODE_REGISTERS = 0, 1, 2, 3
 
 
 class MoeError(RuntimeError):

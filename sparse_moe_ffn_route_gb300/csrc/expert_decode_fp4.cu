@@ -1,0 +1,594 @@
+// Decode path for MXFP4 experts with few tokens per expert: an asynchronous weight
+// stream through shared memory.
+//
+// One persistent CTA per SM takes a contiguous share of the units (work item of up
+// to 8 token rows of one expert) x (128 weight rows), so every CTA gets the same
+// number of units and re-stages its token rows only when the item changes.  Warp 16
+// is the producer: one elected lane streams each unit's codes into a ring of
+// shared-memory stages with TMA (128 rows x 128 bytes = 256 inputs per stage,
+// 128-byte swizzle) and the unit's E8M0 scale bytes with one bulk copy.  About
+// 128 KB of weights are in flight per SM at any time, without holding registers.
+//
+// Warps 0..15 consume: the pair of warps w and w + 8 owns rows 16w..16w+15 of the
+// unit (one MMA tile), each taking every other block of a stage.  An
+// ldmatrix of the swizzled stage hands lane (g, c) the four code bytes 4c..4c+3 of
+// one 32-input block of rows g and g+8, so both k16 MMAs of that block see inputs of
+// that block only: the block's two MMAs accumulate into a fresh fp32 fragment that
+// is then scaled once by 2^(s - 127) (exact in fp32 for every scale byte, through a
+// 256-entry table that also maps 0 to 2^-127 and 255 to NaN).  Codes become exact
+// f16 pairs with cvt.rn.f16x2.e2m1x2.  The token operand is the item's rows staged
+// in shared memory as f16 scaled by 2^e per token (largest magnitude in
+// [2^14, 2^15)), so bf16 x is exact and h = hi + lo keeps 11 bits; the epilogue
+// removes 2^e.
+//
+// Sources: "Phase 19: MoE - gpt-oss-20b", section 2 Experts (interleaved gate_up
+// with bias, clamped GLU, down with bias) and section 3 (MXFP4: E2M1 codes, low
+// nibble first, one E8M0 scale per 32 inputs).
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kTiles = 8;                         // 16-row MMA tiles per unit
+constexpr int kCW = 2 * kTiles;                   // consumer warps: two per tile (even / odd blocks)
+constexpr int kThreads = (kCW + 1) * 32;          // + the producer warp
+constexpr int kRows = 16 * kTiles;                // weight rows per unit
+constexpr int kStageBytes = kRows * 128;          // 128 rows x 128 bytes of codes
+constexpr int kBlocksPerStage = 8;                // 32-input blocks per stage row
+constexpr int kMaxRingStages = 12;
+constexpr int kTokens = 8;                        // token rows per work item
+
+// Shared memory, from a 1024-aligned base: ring stages | scale buffers (2) |
+// scale table | partial sums | token rows.
+struct F4Smem {
+  int stages, nb;            // ring depth; 32-input blocks per weight row
+  int scale_bytes;           // one scale buffer (kRows * nb, rounded to 16)
+  int pitch;                 // bytes per staged token row
+  int ring, scales, lut, part, tok, total;
+};
+
+__host__ __device__ inline int round_up(int v, int a) { return (v + a - 1) / a * a; }
+
+// Token row pitch: >= 2 * kin bytes and an odd multiple of 64, so that the rows of
+// the 8 token columns read by one 8-lane phase fall in different bank groups.
+__host__ __device__ inline int token_pitch(int kin) { return round_up(2 * kin, 128) + 64; }
+
+__host__ __device__ inline F4Smem f4_smem(int kin, int stages) {
+  F4Smem m;
+  m.stages = stages;
+  m.nb = kin / 32;
+  m.scale_bytes = round_up(kRows * m.nb, 16);
+  m.pitch = token_pitch(kin);
+  m.ring = 0;
+  m.scales = stages * kStageBytes;
+  m.lut = m.scales + 2 * m.scale_bytes;
+  m.part = m.lut + 256 * 4;                        // odd-block partial sums [kTiles][32][4]
+  m.tok = m.part + kTiles * 32 * 16;
+  m.total = m.tok + kTokens * m.pitch;
+  return m;
+}
+
+__device__ __forceinline__ float act_swiglu(float g, float u) { return g / (1.f + __expf(-g)) * u; }
+
+__device__ __forceinline__ float act_clamped(float g, float u, float limit, float alpha) {
+  g = fminf(g, limit);
+  u = fminf(fmaxf(u, -limit), limit);
+  return (u + 1.f) * g / (1.f + __expf(-alpha * g));
+}
+
+// Barrier among the consumer warps only (the producer keeps streaming).
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kCW * 32) : "memory");
+}
+
+// Barrier between the two warps of one tile (named barriers 2 .. 2 + kTiles - 1).
+__device__ __forceinline__ void pair_sync(int tile) {
+  asm volatile("bar.sync %0, 64;" ::"r"(2 + tile) : "memory");
+}
+
+// volatile: it reads shared memory that an mbarrier wait (volatile asm) made valid,
+// so it must stay after that wait.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// Contiguous global -> shared copy completing `bytes` of transaction count on
+// `bar` (both addresses 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Exponent e of a token row from the bf16 bits of its largest magnitude, so that
+// the row times 2^e has its largest magnitude in [2^14, 2^15).
+__device__ __forceinline__ int row_exp(uint32_t m16) {
+  const int E = (int)(m16 >> 7);
+  if (m16 == 0 || E == 255) return 0;
+  return min(141 - E, 126);
+}
+
+// 16-byte units per lane kept in registers while staging (a half row of up to 192 * 8
+// = 1536 inputs in one round trip; longer rows load twice).  17 warps leave 96
+// registers per thread (5 warps share one scheduler's 16K registers).
+constexpr int kStageUnits = 6;
+
+__device__ __forceinline__ uint32_t max_abs_bf16x8(const uint4& v) {
+  const uint32_t m = 0x7FFF7FFFu;
+  return __vmaxu2(__vmaxu2(v.x & m, v.y & m), __vmaxu2(v.z & m, v.w & m));
+}
+
+__device__ __forceinline__ uint4 scaled_f16x8(const uint4& v, const uint4& l, float s) {
+  uint4 o;
+  o.x = pack_f16x2(s * (bf16_lo(v.x) + bf16_lo(l.x)), s * (bf16_hi(v.x) + bf16_hi(l.x)));
+  o.y = pack_f16x2(s * (bf16_lo(v.y) + bf16_lo(l.y)), s * (bf16_hi(v.y) + bf16_hi(l.y)));
+  o.z = pack_f16x2(s * (bf16_lo(v.z) + bf16_lo(l.z)), s * (bf16_hi(v.z) + bf16_hi(l.z)));
+  o.w = pack_f16x2(s * (bf16_lo(v.w) + bf16_lo(l.w)), s * (bf16_hi(v.w) + bf16_hi(l.w)));
+  return o;
+}
+
+// Stage the item's token rows (n <= 8; rows n..7 become zeros) as scaled f16: the
+// two warps w and w + 8 take the halves of row w % 8.  Every lane issues all of its
+// loads of a half row at once (up to kStageUnits 16-byte units), so that staging
+// costs one round trip to memory for x rows and two for (hi, lo) h rows while the
+// weight stream keeps the memory system busy.  rows[i] is a bf16 row of kin values in global memory; PAIR:
+// the hi half of an (hi, lo) pair whose lo half is lo_off bytes further, and the
+// staged value is hi + lo.  rmax[8] must be zero on entry; esc[i] receives row i's
+// exponent.  Contains the consumer barriers that separate its two phases.
+template <bool PAIR>
+__device__ void stage_tokens(uint8_t* tok, int pitch, const uint8_t* const* rows, int n, int kin,
+                             size_t lo_off, int* esc, uint32_t* rmax, int warp, int lane) {
+  const int r = warp % kTokens, hf = warp / kTokens;
+  const int per = kin >> 3;                       // 16-byte units of bf16 input per row
+  const int hu = (per + 1) >> 1;                  // units per half row
+  const int ub = hf * hu, ue = min(per, ub + hu);
+  const bool one = hu <= 32 * kStageUnits;        // the half row fits in registers
+  uint4* drow = reinterpret_cast<uint4*>(tok + (size_t)r * pitch);
+  const uint8_t* src = r < n ? rows[r] : nullptr;
+  uint4 hv[kStageUnits], lv[kStageUnits];
+  uint32_t m2 = 0;
+  if (src) {
+    for (int u0 = ub; u0 < ue; u0 += 32 * kStageUnits) {
+#pragma unroll
+      for (int i = 0; i < kStageUnits; ++i) {
+        const int u = u0 + lane + 32 * i;
+        hv[i] = make_uint4(0, 0, 0, 0);
+        if (u < ue) hv[i] = ldg_nc_v4(src + 16 * u);
+      }
+#pragma unroll
+      for (int i = 0; i < kStageUnits; ++i) m2 = __vmaxu2(m2, max_abs_bf16x8(hv[i]));
+    }
+    // |lo| is below half an ulp of hi: the largest hi sets e
+    const uint32_t m = __reduce_max_sync(0xffffffffu, max(m2 & 0xffffu, m2 >> 16));
+    if (lane == 0) atomicMax(&rmax[r], m);
+  }
+  consumers_sync();
+  const int e = src ? row_exp(rmax[r]) : 0;
+  const float s = exp2i(e);
+  for (int u0 = ub; u0 < ue; u0 += 32 * kStageUnits) {
+    // hi again when the row is longer than the registers; lo (PAIR) now
+#pragma unroll
+    for (int i = 0; i < kStageUnits; ++i) {
+      const int u = u0 + lane + 32 * i;
+      lv[i] = make_uint4(0, 0, 0, 0);
+      if (src && u < ue) {
+        if (!one) hv[i] = ldg_nc_v4(src + 16 * u);
+        if (PAIR) lv[i] = ldg_nc_v4(src + lo_off + 16 * u);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kStageUnits; ++i) {
+      const int u = u0 + lane + 32 * i;
+      if (u < ue) drow[u] = src ? scaled_f16x8(hv[i], lv[i], s) : make_uint4(0, 0, 0, 0);
+    }
+  }
+  if (lane == 0 && hf == 0) esc[r] = e;
+}
+
+// D = A * B with a zero accumulator (f16 operands, fp32 result).
+__device__ __forceinline__ void mma_f16_zero(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                             uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+// The blocks b = half, half + 2, half + 4, half + 6 (< nblk) of one stage for one
+// tile: acc += 2^(s - 127) * (block's codes x token rows), per block.  rbase: the
+// lane's ldmatrix row in the stage; gb0: global block index of block `half`.
+// Block k of the four is b = half + 2k; matrix pair p = k / 2 of the ldmatrix loads
+// holds rows g / g+8 of blocks half + 4p and half + 4p + 2.
+__device__ __forceinline__ void block_mma(const uint32_t wa, const uint32_t wb, const uint4& B, float s0,
+                                          float s1, float (&acc)[4]) {
+  uint32_t fa[4], fb[4];
+  e2m1x8_to_f16(wa, fa);
+  e2m1x8_to_f16(wb, fb);
+  float tt[4];
+  mma_f16_zero(tt, fa[0], fb[0], fa[1], fb[1], B.x, B.y);
+  mma_f16_16816(tt, fa[2], fb[2], fa[3], fb[3], B.z, B.w);
+  acc[0] = fmaf(s0, tt[0], acc[0]);
+  acc[1] = fmaf(s0, tt[1], acc[1]);
+  acc[2] = fmaf(s1, tt[2], acc[2]);
+  acc[3] = fmaf(s1, tt[3], acc[3]);
+}
+
+template <bool FULL>
+__device__ __forceinline__ void stage_blocks(uint32_t rbase, int mi, int ri, int half, const uint8_t* tg,
+                                             const uint8_t* sc0, const uint8_t* sc1, const float* lut,
+                                             int gb0, int nblk, float (&acc)[4]) {
+  if (FULL) {
+    // every operand of the four blocks first, so that their latencies overlap
+    uint32_t r[2][4];
+#pragma unroll
+    for (int p = 0; p < 2; ++p)
+      ldmatrix_x4(rbase + ((uint32_t)((half + 4 * p + 2 * (mi >> 1)) ^ ri) << 4), r[p]);
+    uint4 B[4];
+    uint32_t c0[4], c1[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      B[k] = *reinterpret_cast<const uint4*>(tg + 64 * (gb0 + 2 * k));
+      c0[k] = sc0[gb0 + 2 * k];
+      c1[k] = sc1[gb0 + 2 * k];
+    }
+    float s0[4], s1[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      s0[k] = lut[c0[k]];
+      s1[k] = lut[c1[k]];
+    }
+    float part[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      block_mma(r[k >> 1][2 * (k & 1)], r[k >> 1][2 * (k & 1) + 1], B[k], s0[k], s1[k], part[k & 1]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[j] += part[0][j] + part[1][j];
+  } else {
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    if (half + 4 * p < nblk) {
+      uint32_t r[4];
+      ldmatrix_x4(rbase + ((uint32_t)((half + 4 * p + 2 * (mi >> 1)) ^ ri) << 4), r);
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        if (half + 4 * p + 2 * q < nblk) {
+          const int gb = gb0 + 4 * p + 2 * q;
+          const uint4 B = *reinterpret_cast<const uint4*>(tg + 64 * gb);
+          block_mma(r[2 * q], r[2 * q + 1], B, lut[sc0[gb]], lut[sc1[gb]], acc);
+        }
+      }
+    }
+  }
+  }
+}
+
+struct F4Args {
+  RouteState rs;
+  int R;                      // weight rows per expert: gate_up 2ff (gate, up interleaved), down d
+  int kin;                    // inputs per weight row: gate_up d, down ff
+  int tiles;                  // units per work item: ceil(R / kRows)
+  int stages;                 // ring depth
+  const uint8_t* scales;      // E8M0 [E, R, kin/32]
+  const uint16_t* bias;       // bf16 [E, R] or null
+  // gate_up: x rows in, h (hi, lo) rows out
+  const uint16_t* x;
+  int K;                      // slots per token (row2slot / K = token)
+  uint16_t* h;
+  int ldh;
+  int act;
+  float limit, alpha;
+  // down: Y rows (slot order) out
+  float* Y;
+};
+
+// GATEUP: codes are gate_up [E, 2ff, d/2] bytes, tokens are x rows, output h.
+// Otherwise: codes are down [E, d, ff/2], tokens are h rows, output Y.
+template <bool GATEUP>
+__global__ void __launch_bounds__(kThreads, 1)
+fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t full_bar[kMaxRingStages], empty_bar[kMaxRingStages], sfull_bar[2],
+      sempty_bar[2];
+  __shared__ int abort_s;
+  __shared__ int esc[kTokens];
+  __shared__ const uint8_t* trows[kTokens];
+  __shared__ uint32_t rmax[kTokens];
+
+  const F4Smem L = f4_smem(a.kin, a.stages);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t* status = a.rs.status;
+  volatile int* abort = &abort_s;
+  float* lut = reinterpret_cast<float*>(smem + L.lut);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < a.stages; ++i) {
+      tc::mbar_init(tc::smem_u32(&full_bar[i]), 1);
+      tc::mbar_init(tc::smem_u32(&empty_bar[i]), kCW);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(tc::smem_u32(&sfull_bar[i]), 1);
+      tc::mbar_init(tc::smem_u32(&sempty_bar[i]), kCW);
+    }
+    abort_s = 0;
+    tc::fence_barrier_init();
+  }
+  // E8M0 byte -> 2^(s - 127) as fp32: 0 is 2^-127 (subnormal), 255 is NaN
+  for (int i = threadIdx.x; i < 256; i += blockDim.x)
+    lut[i] = i == 0 ? __uint_as_float(0x00400000u) : i == 255 ? __uint_as_float(0x7FC00000u) : exp2i(i - 127);
+  if (warp == kCW && lane == 0) tc::tma_prefetch_desc(&tmW);
+  __syncthreads();
+  pdl_wait();
+
+  const int n_items = *a.rs.n_work;
+  const long long U = (long long)(n_items > 0 ? n_items : 0) * a.tiles;
+  const int u0 = (int)(U * blockIdx.x / gridDim.x), u1 = (int)(U * (blockIdx.x + 1) / gridDim.x);
+  const int nst = (L.nb + kBlocksPerStage - 1) / kBlocksPerStage;   // stages per unit
+
+  if (warp == kCW) {
+    // ------------------------------------------------------------ producer
+    if (tc::elect_one()) {
+      int it = 0, its = 0;                      // ring loads, scale loads issued
+      int st = 0;                               // ring slot of load `it`
+      uint32_t ph = 0;                          // its phase parity
+      for (int u = u0; u < u1 && !*abort; ++u) {
+        const int ai = u / a.tiles, t = u - ai * a.tiles;
+        const int v = a.rs.work[ai].x;
+        const int row0 = t * kRows, nrows = min(kRows, a.R - row0);
+        const long long grow = (long long)v * a.R + row0;
+        const int sb = its & 1;
+        if (!tc::mbar_wait(tc::smem_u32(&sempty_bar[sb]), ((its >> 1) & 1) ^ 1, abort, status)) break;
+        const uint32_t sbytes = (uint32_t)(nrows * L.nb);
+        tc::mbar_arrive_expect_tx(tc::smem_u32(&sfull_bar[sb]), sbytes);
+        bulk_load(tc::smem_u32(smem + L.scales + sb * L.scale_bytes), a.scales + grow * L.nb, sbytes,
+                  tc::smem_u32(&sfull_bar[sb]));
+        ++its;
+        for (int s = 0; s < nst; ++s) {
+          if (!tc::mbar_wait(tc::smem_u32(&empty_bar[st]), ph ^ 1, abort, status)) break;
+          tc::mbar_arrive_expect_tx(tc::smem_u32(&full_bar[st]), kStageBytes);
+          tc::tma_load_2d(tc::smem_u32(smem + st * kStageBytes), &tmW, s * 128, (int)grow,
+                          tc::smem_u32(&full_bar[st]));
+          ++it;
+          if (++st == a.stages) {
+            st = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      if (*abort) {
+        // Drain: wait (bounded, regardless of the abort flag) for the most recent load
+        // into every buffer, so that no copy lands after the CTA has exited.
+        int zero = 0;
+        volatile int* never = &zero;
+        for (int i = it - a.stages > 0 ? it - a.stages : 0; i < it; ++i)
+          tc::mbar_wait(tc::smem_u32(&full_bar[i % a.stages]), (i / a.stages) & 1, never, status);
+        for (int i = its - 2 > 0 ? its - 2 : 0; i < its; ++i)
+          tc::mbar_wait(tc::smem_u32(&sfull_bar[i & 1]), (i >> 1) & 1, never, status);
+      }
+    }
+    pdl_trigger();
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  // Warp w owns tile w % kTiles (rows 16 tile .. 16 tile + 15 of the unit) and the
+  // blocks of parity w / kTiles of every stage: the pair of warps of one tile runs two
+  // independent chains, and the odd-block warp hands its sums over at the unit's end.
+  const int tile = warp % kTiles, half = warp / kTiles;
+  const int g = lane >> 2, c = lane & 3;
+  const int mi = lane >> 3, ri = lane & 7;        // this lane's ldmatrix address: matrix, row
+  uint8_t* tok = smem + L.tok;
+  const uint8_t* tg = tok + g * L.pitch + 16 * c; // token column g, inputs 8c.. of each block
+  float4* part = reinterpret_cast<float4*>(smem + L.part) + tile * 32 + lane;
+  int st = 0, its = 0, cur = -1;               // ring slot, scale loads consumed, staged item
+  uint32_t ph = 0;                               // phase parity of ring slot st
+  for (int u = u0; u < u1; ++u) {
+    // On abort every wait returns at once; the loop still runs to its end so that
+    // all consumer warps take the same barriers.
+    const int ai = u / a.tiles, t = u - ai * a.tiles;
+    const int2 item = a.rs.work[ai];
+    const int v = item.x;
+    const int r0 = a.rs.offsets[v] + item.y;     // first permuted row of the item
+    const int n = min(kTokens, a.rs.offsets[v + 1] - r0);
+    if (ai != cur) {
+      consumers_sync();                          // every warp is done with the old rows
+      if (threadIdx.x < kTokens) {
+        const int i = threadIdx.x;
+        rmax[i] = 0;
+        const uint8_t* p = nullptr;
+        if (i < n) {
+          if (GATEUP)
+            p = reinterpret_cast<const uint8_t*>(a.x + (size_t)(a.rs.row2slot[r0 + i] / a.K) * a.kin);
+          else
+            p = reinterpret_cast<const uint8_t*>(a.h + (size_t)(r0 + i) * 2 * a.ldh);
+        }
+        trows[i] = p;
+      }
+      consumers_sync();
+      stage_tokens<!GATEUP>(tok, L.pitch, trows, n, a.kin, (size_t)a.ldh * 2, esc, rmax, warp, lane);
+      consumers_sync();
+      cur = ai;
+    }
+    const int row0 = t * kRows, nrows = min(kRows, a.R - row0);
+    const bool on = 16 * tile < nrows;           // nrows is a multiple of 32
+    const int sb = its & 1;
+    bool ok = tc::mbar_wait(tc::smem_u32(&sfull_bar[sb]), (its >> 1) & 1, abort, status);
+    const uint8_t* sc0 = smem + L.scales + sb * L.scale_bytes + (16 * tile + g) * L.nb;
+    const uint8_t* sc1 = sc0 + 8 * L.nb;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int s = 0; s < nst; ++s) {
+      ok = ok && tc::mbar_wait(tc::smem_u32(&full_bar[st]), ph, abort, status);
+      if (ok && on) {
+        const uint32_t rbase = tc::smem_u32(smem + st * kStageBytes) + (16 * tile + 8 * (mi & 1) + ri) * 128;
+        const int nblk = min(kBlocksPerStage, L.nb - s * kBlocksPerStage);
+        const int gb0 = s * kBlocksPerStage + half;
+        if (nblk == kBlocksPerStage)
+          stage_blocks<true>(rbase, mi, ri, half, tg, sc0, sc1, lut, gb0, kBlocksPerStage, acc);
+        else
+          stage_blocks<false>(rbase, mi, ri, half, tg, sc0, sc1, lut, gb0, nblk, acc);
+      }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&empty_bar[st]));
+      if (++st == a.stages) {
+        st = 0;
+        ph ^= 1;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sempty_bar[sb]));
+    ++its;
+    if (!on) continue;
+    // the odd-block warp of the tile hands its sums to the even-block warp
+    if (half) *part = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    pair_sync(tile);
+    if (!half) {
+      const float4 o = *part;
+      acc[0] += o.x;
+      acc[1] += o.y;
+      acc[2] += o.z;
+      acc[3] += o.w;
+    }
+    pair_sync(tile);                             // read before the next unit writes
+    if (half || !ok) continue;
+
+    // ------------------------------------------------------------ epilogue
+    // acc: rows g (tokens 2c, 2c+1) and g+8 of the tile, times 2^e of the token.
+    const float un[2] = {exp2i(-esc[2 * c]), exp2i(-esc[2 * c + 1])};
+    if (GATEUP) {
+      // MMA row i is memory row row0 + 16 tile + i: feature (row0 + 16 tile + i) / 2, its gate
+      // when i is even.  Lanes g and g^1 (lane ^ 4) trade accumulators: even g finishes
+      // the feature of its row g, odd g the feature of its row g + 8.
+      float pr[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) pr[k] = __shfl_xor_sync(0xffffffffu, acc[k], 4);
+      const bool odd = g & 1;
+      const int f = row0 / 2 + 8 * tile + (odd ? 4 : 0) + (g >> 1);
+      const float gt[2] = {odd ? pr[2] : acc[0], odd ? pr[3] : acc[1]};
+      const float upv[2] = {odd ? acc[2] : pr[0], odd ? acc[3] : pr[1]};
+      float bg = 0.f, bu = 0.f;
+      if (a.bias) {
+        bg = bf16_to_f32(a.bias[(size_t)v * a.R + 2 * f]);
+        bu = bf16_to_f32(a.bias[(size_t)v * a.R + 2 * f + 1]);
+      }
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int ti = 2 * c + q;
+        if (ti < n) {
+          const float gv = gt[q] * un[q] + bg, uv = upv[q] * un[q] + bu;
+          const float hv =
+              a.act == MOE_ACT_SWIGLU ? act_swiglu(gv, uv) : act_clamped(gv, uv, a.limit, a.alpha);
+          // h as a pair of bf16 (hi, lo = bf16(h - hi)), the layout both down paths read
+          const uint16_t hi = f32_to_bf16(hv);
+          uint16_t* hr = a.h + (size_t)(r0 + ti) * 2 * a.ldh + f;
+          hr[0] = hi;
+          hr[a.ldh] = f32_to_bf16(hv - bf16_to_f32(hi));
+        }
+      }
+    } else {
+      const int o = row0 + 16 * tile + g;
+      float b0 = 0.f, b1 = 0.f;
+      if (a.bias) {
+        b0 = bf16_to_f32(a.bias[(size_t)v * a.R + o]);
+        b1 = bf16_to_f32(a.bias[(size_t)v * a.R + o + 8]);
+      }
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int ti = 2 * c + q;
+        if (ti < n) {
+          float* yrow = a.Y + (size_t)a.rs.row2slot[r0 + ti] * a.R;
+          yrow[o] = acc[q] * un[q] + b0;
+          yrow[o + 8] = acc[2 + q] * un[q] + b1;
+        }
+      }
+    }
+  }
+  pdl_trigger();
+}
+
+template <bool GATEUP>
+void set_fp4_smem(int bytes) {
+  static int done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || done[dev] >= bytes) return;
+  if (cudaFuncSetAttribute(fp4_stream_kernel<GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) ==
+      cudaSuccess)
+    done[dev] = bytes;
+}
+
+// Ring depth that fits next to the fixed parts for `kin` inputs (0: it does not fit).
+int fp4_stream_stages(int kin) {
+  int dev = 0, optin = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  const int fixed = f4_smem(kin, 0).total + 1024 + 1024;   // + base alignment + static smem
+  int st = (optin - fixed) / kStageBytes;
+  if (st > kMaxRingStages) st = kMaxRingStages;
+  return st >= 3 ? st : 0;
+}
+
+template <bool GATEUP>
+cudaError_t launch_fp4_stream(const uint8_t* codes, const F4Args& a0, int n_experts, int max_items,
+                              cudaStream_t s, bool* launched) {
+  *launched = false;
+  F4Args a = a0;
+  a.stages = fp4_stream_stages(a.kin);
+  if (!a.stages) return cudaSuccess;
+  if ((reinterpret_cast<uintptr_t>(a.scales) & 15) || (reinterpret_cast<uintptr_t>(codes) & 15))
+    return cudaSuccess;
+  CUtensorMap m;
+  if (!make_map(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, (uint64_t)n_experts * a.R, (uint64_t)a.kin / 2,
+                (uint64_t)a.kin / 2, kRows, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaSuccess;
+  a.tiles = (a.R + kRows - 1) / kRows;
+  const int bytes = f4_smem(a.kin, a.stages).total + 1024;
+  set_fp4_smem<GATEUP>(bytes);
+  const long long units = (long long)max_items * a.tiles;
+  int grid = sm_count();
+  if (units < grid) grid = (int)(units > 0 ? units : 1);
+  *launched = true;
+  return launch_pdl(fp4_stream_kernel<GATEUP>, dim3(grid), dim3(kThreads), (size_t)bytes, s, m, a);
+}
+
+}  // namespace
+
+cudaError_t launch_gateup_decode_fp4(const ExpertParams& p, const RouteState& rs, const uint16_t* x, int K,
+                                     uint16_t* h, int ldh, int max_items, cudaStream_t s, bool* launched) {
+  F4Args a{};
+  a.rs = rs;
+  a.R = 2 * p.ff;
+  a.kin = p.d;
+  a.scales = p.gu_scales;
+  a.bias = p.gu_bias;
+  a.x = x;
+  a.K = K;
+  a.h = h;
+  a.ldh = ldh;
+  a.act = p.act;
+  a.limit = p.limit;
+  a.alpha = p.alpha;
+  return launch_fp4_stream<true>(p.gate_up, a, p.E, max_items, s, launched);
+}
+
+cudaError_t launch_down_decode_fp4(const ExpertParams& p, const RouteState& rs, const uint16_t* h, int ldh,
+                                   float* Y, int max_items, cudaStream_t s, bool* launched) {
+  F4Args a{};
+  a.rs = rs;
+  a.R = p.d;
+  a.kin = p.ff;
+  a.scales = p.dn_scales;
+  a.bias = p.dn_bias;
+  a.h = const_cast<uint16_t*>(h);
+  a.ldh = ldh;
+  a.Y = Y;
+  return launch_fp4_stream<false>(p.down, a, p.E, max_items, s, launched);
+}
+
+}  // namespace moe

@@ -500,12 +500,15 @@ transpose_scales_kernel(const uint8_t* __restrict__ src, int E, int rows, int nb
   }
 }
 
+}  // namespace
+
 // ---------------------------------------------------------------- host side
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+namespace {
 EncodeTiledFn encode_fn() {
   static EncodeTiledFn fn = nullptr;
   static bool tried = false;
@@ -519,6 +522,14 @@ EncodeTiledFn encode_fn() {
       fn = reinterpret_cast<EncodeTiledFn>(p);
   }
   return fn;
+}
+}  // namespace
+
+int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 148;
 }
 
 // 2D map over a row-major matrix [rows, cols] (row stride in bytes) with a box of
@@ -537,6 +548,8 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType type, const void* base, uint64
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+namespace {
+
 // bf16 matrix, box of box_rows x 64 columns, 128-byte swizzle (operand tiles).
 bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t stride,
                    uint32_t box_rows) {
@@ -551,12 +564,6 @@ bool make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
                   CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-int sm_count() {
-  int dev = 0, n = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 148;
-}
 
 // Largest N (multiple of 16, at most max_n) that divides `rows`; 0 if none.
 int tile_n(int rows, int max_n) {

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/moe.h"
@@ -75,8 +76,25 @@ struct RouteState {
   uint32_t* status;      // device status word
 };
 
+// ---------------------------------------------------------------- host helpers
+// 2D TMA map over a row-major matrix [rows, cols] of `type` (row stride in bytes)
+// with a box of box_rows x box_cols elements; false if the driver rejects it.
+bool make_map(CUtensorMap* m, CUtensorMapDataType type, const void* base, uint64_t rows,
+              uint64_t cols, uint64_t stride, uint32_t box_rows, uint32_t box_cols,
+              CUtensorMapSwizzle swz);
+int sm_count();   // SMs of the current device
+
 // ---------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error.
+
+// MXFP4 decode with one-chunk work items (at most 8 rows each): the asynchronous
+// weight-stream kernels.  *launched is false (and nothing is enqueued) when the
+// shapes or alignments do not suit them; the caller then uses the register-stream
+// kernels below.
+cudaError_t launch_gateup_decode_fp4(const ExpertParams& p, const RouteState& rs, const uint16_t* x, int K,
+                                     uint16_t* h, int ldh, int max_items, cudaStream_t s, bool* launched);
+cudaError_t launch_down_decode_fp4(const ExpertParams& p, const RouteState& rs, const uint16_t* h, int ldh,
+                                   float* Y, int max_items, cudaStream_t s, bool* launched);
 
 // logits[t, e] (row stride ldl) = x_t . W_r[e] (+ bias[e]) for e < E, and
 // x_t . wsh for e == E when wsh != null.

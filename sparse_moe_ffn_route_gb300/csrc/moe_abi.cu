@@ -31,7 +31,7 @@ int validate_cfg(const moe_cfg_t* c) {
     return MOE_ERR_INVALID_ARG;
   if (c->gating < 0 || c->gating > 1 || c->act < 0 || c->act > 1 || c->wfmt < 0 || c->wfmt > 1 ||
       c->interleaved_gate_up < 0 || c->interleaved_gate_up > 1 || c->norm_topk_prob < 0 ||
-      c->norm_topk_prob > 1 || c->path < 0 || c->path > 2 || c->y_fp32 < 0 || c->y_fp32 > 1)
+      c->norm_topk_prob > 1 || c->path < 0 || c->path > MOE_PATH_DECODE_REGISTERS || c->y_fp32 < 0 || c->y_fp32 > 1)
     return MOE_ERR_INVALID_ARG;
   for (int r : c->reserved)
     if (r != 0) return MOE_ERR_INVALID_ARG;
@@ -267,11 +267,20 @@ int run_experts(const moe_cfg_t* c, const void* x, int T, const moe_experts_t* e
   const int max_items = L.E1 + (L.S + tpg - 1) / tpg;
   MOE_CUDA(launch_permute(rs, L.S, L.E1, tpg, s));
   MOE_CUDA(mark_phase(3, s));
-  MOE_CUDA(launch_gateup_decode(p, c->wfmt, c->interleaved_gate_up, rs,
-                                static_cast<const uint16_t*>(x), L.K, h, L.ldh, max_items, chunks,
-                                s));
+  // MXFP4 one-chunk items: the TMA-fed shared-memory weight stream when it applies.
+  const bool ring = c->wfmt == MOE_WFMT_MXFP4 && chunks == 1 && c->path != MOE_PATH_DECODE_REGISTERS;
+  bool done = false;
+  if (ring)
+    MOE_CUDA(launch_gateup_decode_fp4(p, rs, static_cast<const uint16_t*>(x), L.K, h, L.ldh, max_items,
+                                      s, &done));
+  if (!done)
+    MOE_CUDA(launch_gateup_decode(p, c->wfmt, c->interleaved_gate_up, rs,
+                                  static_cast<const uint16_t*>(x), L.K, h, L.ldh, max_items, chunks,
+                                  s));
   MOE_CUDA(mark_phase(4, s));
-  MOE_CUDA(launch_down_decode(p, c->wfmt, rs, h, L.ldh, Y, max_items, chunks, s));
+  done = false;
+  if (ring) MOE_CUDA(launch_down_decode_fp4(p, rs, h, L.ldh, Y, max_items, s, &done));
+  if (!done) MOE_CUDA(launch_down_decode(p, c->wfmt, rs, h, L.ldh, Y, max_items, chunks, s));
   MOE_CUDA(mark_phase(5, s));
   MOE_CUDA(launch_combine(Y, rs.slot_w, rs.slot_expert, T, L.K, c->d_model, L.E1, y,
                           c->y_fp32 != 0, s));

@@ -1,8 +1,10 @@
 """MXFP4 decode kernels vs the fp64 oracle: scale ranges and token magnitudes (GPU only).
 
 One-chunk MXFP4 decode items run with an f16 token operand: each staged token row
-is scaled by a power of two, and a k group whose E8M0 scales all lie in [113, 140]
-decodes its weights with f16 arithmetic, while any other group takes the exact bf16
+is scaled by a power of two.  The default kernels stream the weights through a
+TMA-fed shared-memory ring and apply each block's E8M0 scale in fp32; the
+register-stream kernels (MOE_PATH_DECODE_REGISTERS) decode a k group whose scales
+all lie in [113, 140] with f16 arithmetic and any other group with the exact bf16
 decode against a bf16 (hi, lo) split of the f16 tokens.  These cases put both kinds
 of group in one layer, drive the per-token scaling to both ends, and run the
 many-token (unstaged) kernels on the same scale ranges.
@@ -60,14 +62,21 @@ STAGED_SPECS = [
 ]
 
 
+# path 1: one-chunk MXFP4 items stream their weights through the TMA-fed shared-memory
+# ring; path 3 keeps every weight load in registers (the kernels above)
+KERNELS = pytest.mark.parametrize("path", [1, 3], ids=["ring", "registers"])
+
+
+@KERNELS
 @pytest.mark.parametrize("spec,note", STAGED_SPECS, ids=lambda v: v.name if hasattr(v, "name") else "")
-def test_staged_scale_ranges(spec, note):
+def test_staged_scale_ranges(spec, note, path):
     assert 4 * spec.tokens * spec.top_k <= 16 * spec.n_experts     # one-chunk items
-    _run(spec, mi.make_layer(spec))
+    _run(spec, mi.make_layer(spec), path)
 
 
+@KERNELS
 @pytest.mark.parametrize("shift", [-40, -14, 0, 17, 40])
-def test_staged_token_magnitudes(shift):
+def test_staged_token_magnitudes(shift, path):
     """x scaled by 2^shift (exact in bf16): the per-token f16 scaling must absorb it.
 
     The expert biases are zero, so that h (and y) follow x's magnitude down to
@@ -81,7 +90,7 @@ def test_staged_token_magnitudes(shift):
     x[1] = 0.0                                   # an all-zero token row
     x[2, 5] *= 2.0 ** 20                         # one large value among ordinary ones
     lay.x = mi.f64_to_bf16(x)
-    _run(spec, lay)
+    _run(spec, lay, path)
 
 
 @pytest.mark.parametrize("scale_lo,scale_hi", [(100, 150), (127, 140), (105, 128)])
