@@ -1,0 +1,649 @@
+// Prefill path for MXFP4 experts with the clamped GLU: grouped GEMMs on tcgen05
+// with f16 operands, each weight tile decoded once for two m tiles.
+//
+// Per expert e with rows (tokens, in the grouped order of the permute kernel):
+//   gate_up:  gu[r, n] = X_r . W_gu,e[n] + b[n];  h = (clamp(up) + 1) * min(gate, L) * sigmoid(a * min(gate, L))
+//   down   :  Y[slot(r), o] = h_r . W_d,e[o] + b_d[o]
+//
+// Operands.  Both MMA operands are f16 (kind::f16, fp32 accumulation in TMEM):
+//   - x rows are staged as f16 times 2^e per row (largest magnitude in
+//     [2^14, 2^15)), which holds every bf16 value of the row exactly except those
+//     more than 2^38 below its largest; rowmul[r] = 2^-e undoes it in the epilogue.
+//   - h is bounded by the clamps (|h| <= (L + 1) * max(L, 1/a)), so it is stored
+//     as plain f16 (11 significant bits) and the down projection takes one MMA per
+//     k step.
+//   - weights: an E2M1 code converts exactly to f16 with cvt.rn.f16x2.e2m1x2; the
+//     block scale 2^(s - 127) is split into 2^(s - 127 - c_n) * 2^c_n, with c_n per
+//     weight row n chosen (fp4_prep_kernel) so that the largest finite block scale
+//     of the row maps to 2^13.  Every block whose scale byte is within 36 of the row's
+//     largest then decodes exactly in f16 (6 * 2^13 <= 65504, 0.5 * 2^-23 = 2^-24);
+//     a block more than 2^36 below the row's largest decodes to zero (its products
+//     are below fp32 rounding of the row's dot product).  colmul[n] = 2^c_n is
+//     applied in the epilogue.  Scale byte 255 (NaN) stays NaN.
+//
+// Tiling.  A work item is up to 256 rows of one expert (two m tiles of 128); a
+// unit is (work item, n tile of N <= 240 weight rows).  The dequantised B tile of
+// a k step feeds the MMAs of both m tiles, which accumulate into two TMEM
+// accumulators (columns 0 and 256).  One persistent CTA per SM walks the units
+// m-major.  Warp roles:
+//   warp 0        TMA producer: per 64-input k step, the A tile of each m tile
+//                 (128 x 64 f16, 128-byte swizzle) and the codes (N x 32 bytes)
+//                 into a 4-stage ring;
+//   warp 1        TMEM owner and MMA issuer (M 128, N, K 16, one elected thread);
+//   warps 2..9    epilogue: two warps per TMEM lane quarter, each half of the columns;
+//   warps 10..17  dequant: codes -> f16 B tile (128-byte swizzle) in a 2-deep ring;
+//                 each thread reads the scale bytes of its rows for the next k step
+//                 from global memory (the E8M0 layout as given) while it converts
+//                 the current one.
+// Every mbarrier wait is bounded; a wait that gives up sets the device status and
+// an abort flag, the CTA drains its copies and MMAs in flight, frees TMEM, returns.
+//
+// Sources: "Phase 19: MoE - gpt-oss-20b", section 2 (Experts: interleaved gate_up
+// with bias, clamped GLU, down with bias) and section 3 (MXFP4: E2M1 codes, low
+// nibble first, one E8M0 scale per 32 inputs); "qwen35moe - Forward-Pass Design",
+// "Batched prefill" (expert-grouped batching).
+#include <cuda.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBM = 128;                          // rows per m tile (MMA M)
+constexpr int kBK = 64;                           // inputs per k step: 128 bytes of f16
+constexpr int kG = 2;                             // m tiles per unit (share one B tile)
+constexpr int kMaxN = 240;                        // weight rows per unit (MMA N)
+constexpr int kTileA = kBM * kBK * 2;             // 16 KiB
+constexpr int kTileB = kMaxN * kBK * 2;           // 30 KiB
+constexpr int kCodes = kMaxN * (kBK / 2);         // 7680 B
+constexpr int kLoadStage = ((kG * kTileA + kCodes + 1023) / 1024) * 1024;
+constexpr int kLoadStages = 4;
+constexpr int kBStages = 2;
+constexpr int kSmemBytes = kLoadStages * kLoadStage + kBStages * kTileB + 1024;
+constexpr int kEpiWarps = 8;
+constexpr int kDqWarps = 8;
+constexpr int kThreads = 32 * (2 + kEpiWarps + kDqWarps);
+constexpr uint32_t kTmemCols = 512;               // accumulators at columns 0 and 256
+
+static_assert(kTileB % 1024 == 0, "B tiles must stay 1024-aligned");
+
+struct F4Gemm {
+  RouteState rs;              // work items of up to kG * kBM rows
+  int E, R, nb;               // experts; weight rows per expert; 32-input blocks per row
+  int N, nt, nkc;             // n tile width, n tiles per expert, k steps
+  const float* colmul;        // [E * R] 2^c_n
+  const int32_t* cshift;      // [E * R] c_n
+  const uint8_t* scales;      // E8M0 [E, R, nb]
+  const float* rowmul;        // [S] 2^-e_r of the staged x rows (gate_up) or null
+  const uint16_t* bias;       // bf16 [E, R] or null
+  int gateup;                 // 1: gate_up (h16 out), 0: down (Y out)
+  uint16_t* h16;              // f16 [S, ldh16]
+  int ldh16;
+  float limit, alpha;
+  float* Y;                   // fp32 [S, d] in slot order
+  int d;
+};
+
+struct Unit {
+  int v, row0, cnt, n;        // expert, first row within it, rows (<= 256), n tile
+};
+
+__device__ __forceinline__ Unit unit_at(const F4Gemm& g, int t) {
+  Unit u;
+  const int m = t / g.nt;
+  u.n = t - m * g.nt;
+  const int2 w = g.rs.work[m];
+  u.v = w.x;
+  u.row0 = w.y;
+  const int rows = g.rs.offsets[u.v + 1] - g.rs.offsets[u.v];
+  u.cnt = min(kG * kBM, rows - u.row0);
+  return u;
+}
+
+// h for one (gate, up) pair; sigmoid(z) = (1 + tanh(z / 2)) / 2 with the hardware tanh.
+__device__ __forceinline__ float tanh_fast(float z) {
+  float r;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(r) : "f"(z));
+  return r;
+}
+
+__device__ __forceinline__ float clamped_glu(float gt, float up, float limit, float alpha) {
+  gt = fminf(gt, limit);
+  up = fminf(fmaxf(up, -limit), limit);
+  const float sg = fmaf(0.5f, tanh_fast(0.5f * alpha * gt), 0.5f);
+  return (up + 1.f) * gt * sg;
+}
+
+// f16 bits of the block multiplier 2^(s - 127 - c): exact for -23 <= s - 127 - c <= 15
+// (subnormal below -14), 0 below -23 (the block is flushed), NaN for s = 255.
+__device__ __forceinline__ uint32_t block_mult_f16(uint32_t s, int c) {
+  const int qe = (int)s - 127 - c;
+  uint32_t m = qe >= -14 ? (uint32_t)(qe + 15) << 10 : (qe >= -23 ? 1u << (qe + 24) : 0u);
+  if (s == 255u) m = 0x7E00u;
+  return m | (m << 16);
+}
+
+// Rows of one k step a dequant thread converts: r = tid / 8 + 32 i (i < kRowsPerThread),
+// chunk j = tid % 8 (inputs 8j..8j+7 of the step, block j / 4).
+constexpr int kRowStep = 32 * kDqWarps / 8;
+constexpr int kRowsPerThread = (kMaxN + kRowStep - 1) / kRowStep;
+
+// One k step of B: N rows x 64 inputs from codes (smem [N][32] bytes) into the f16
+// B tile with the 128-byte swizzle.  sb[i]: the scale byte of row r_i's block of
+// this step; c[i]: the row's shift.  Unit of work = one 16-byte output chunk.
+__device__ __forceinline__ void dequant_f16(const uint8_t* codes, uint8_t* btile, int N, int tid,
+                                            const uint32_t (&sb)[kRowsPerThread],
+                                            const int (&c)[kRowsPerThread]) {
+  const int j = tid & 7;
+#pragma unroll
+  for (int i = 0; i < kRowsPerThread; ++i) {
+    const int r = (tid >> 3) + kRowStep * i;
+    if (r < N) {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(codes + r * 32 + j * 4);
+      const uint32_t m2 = block_mult_f16(sb[i], c[i]);
+      uint32_t o[4];
+      e2m1x8_to_f16(w, o);
+      uint4 q;
+      q.x = f16x2_mul(o[0], m2);
+      q.y = f16x2_mul(o[1], m2);
+      q.z = f16x2_mul(o[2], m2);
+      q.w = f16x2_mul(o[3], m2);
+      *reinterpret_cast<uint4*>(btile + r * 128 + ((j ^ (r & 7)) << 4)) = q;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmC,
+                const F4Gemm g) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* bring = smem + kLoadStages * kLoadStage;
+  __shared__ __align__(8) uint64_t full_bar[kLoadStages], empty_bar[kLoadStages], bfull_bar[kBStages],
+      bempty_bar[kBStages], tfull_bar, tempty_bar, drain_bar;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_s;
+  __shared__ int consumed_s;     // loads the MMA thread has waited for
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t* status = g.rs.status;
+  volatile int* abort = &abort_s;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kLoadStages; ++s) {
+      tc::mbar_init(tc::smem_u32(&full_bar[s]), 1);
+      tc::mbar_init(tc::smem_u32(&empty_bar[s]), 1 + kDqWarps);   // MMA commit + dequant warps
+    }
+    for (int b = 0; b < kBStages; ++b) {
+      tc::mbar_init(tc::smem_u32(&bfull_bar[b]), kDqWarps);
+      tc::mbar_init(tc::smem_u32(&bempty_bar[b]), 1);
+    }
+    tc::mbar_init(tc::smem_u32(&tfull_bar), 1);
+    tc::mbar_init(tc::smem_u32(&tempty_bar), kEpiWarps);
+    tc::mbar_init(tc::smem_u32(&drain_bar), 1);
+    abort_s = 0;
+    consumed_s = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::tma_prefetch_desc(&tmA);
+    tc::tma_prefetch_desc(&tmC);
+  }
+  if (warp == 1) tc::tmem_alloc(tc::smem_u32(&tmem_base_s), kTmemCols);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+  pdl_wait();
+  const int n_m = *g.rs.n_work;
+  const int total = n_m > 0 ? n_m * g.nt : 0;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (tc::elect_one()) {
+      int s = 0, issued = 0;
+      uint32_t ph = 0;
+      for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
+        const Unit u = unit_at(g, t);
+        const int a_row = g.rs.offsets[u.v] + u.row0;
+        const int b_row = u.v * g.R + u.n * g.N;
+        const int gm = u.cnt > kBM ? 2 : 1;
+        const uint32_t bytes = (uint32_t)(gm * kTileA + g.N * 32);
+        for (int kc = 0; kc < g.nkc; ++kc) {
+          if (!tc::mbar_wait(tc::smem_u32(&empty_bar[s]), ph ^ 1, abort, status)) break;
+          const uint32_t fb = tc::smem_u32(&full_bar[s]);
+          const uint32_t sa = tc::smem_u32(smem + s * kLoadStage);
+          tc::mbar_arrive_expect_tx(fb, bytes);
+          tc::tma_load_2d(sa, &tmA, kc * kBK, a_row, fb);
+          if (gm == 2) tc::tma_load_2d(sa + kTileA, &tmA, kc * kBK, a_row + kBM, fb);
+          tc::tma_load_2d(sa + kG * kTileA, &tmC, kc * 32, b_row, fb);
+          ++issued;
+          if (++s == kLoadStages) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      if (*abort) {
+        // Drain: wait (bounded, regardless of the abort flag) for the loads still in flight.
+        int zero = 0;
+        volatile int* never = &zero;
+        for (int i = consumed_s; i < issued; ++i)
+          tc::mbar_wait(tc::smem_u32(&full_bar[i % kLoadStages]), (i / kLoadStages) & 1, never, status);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (tc::elect_one()) {
+      int s = 0, bs = 0;
+      uint32_t ph = 0, bph = 0, aph = 0;
+      const uint32_t idesc = tc::idesc_f16_f32(kBM, g.N);
+      bool any = false;
+      for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
+        const Unit u = unit_at(g, t);
+        const int gm = u.cnt > kBM ? 2 : 1;
+        if (!tc::mbar_wait(tc::smem_u32(&tempty_bar), aph ^ 1, abort, status)) break;
+        tc::tc_fence_after();
+        bool ok = true;
+        for (int kc = 0; kc < g.nkc; ++kc) {
+          if (!tc::mbar_wait(tc::smem_u32(&full_bar[s]), ph, abort, status) ||
+              !tc::mbar_wait(tc::smem_u32(&bfull_bar[bs]), bph, abort, status)) {
+            ok = false;
+            break;
+          }
+          consumed_s = consumed_s + 1;
+          tc::tc_fence_after();
+          const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(smem + s * kLoadStage));
+          const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(bring + bs * kTileB));
+#pragma unroll
+          for (int j = 0; j < kBK / 16; ++j) {
+            tc::umma_bf16(tmem, ad + 2 * j, bd + 2 * j, idesc, (kc | j) != 0);
+            if (gm == 2) tc::umma_bf16(tmem + 256u, ad + (kTileA >> 4) + 2 * j, bd + 2 * j, idesc, (kc | j) != 0);
+          }
+          tc::umma_commit(tc::smem_u32(&empty_bar[s]));
+          tc::umma_commit(tc::smem_u32(&bempty_bar[bs]));
+          any = true;
+          if (++s == kLoadStages) {
+            s = 0;
+            ph ^= 1;
+          }
+          if (++bs == kBStages) {
+            bs = 0;
+            bph ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc::umma_commit(tc::smem_u32(&tfull_bar));
+        aph ^= 1;
+      }
+      if (*abort && any) {
+        // Let every MMA issued so far finish before TMEM is released.
+        tc::umma_commit(tc::smem_u32(&drain_bar));
+        int zero = 0;
+        volatile int* never = &zero;
+        tc::mbar_wait(tc::smem_u32(&drain_bar), 0, never, status);
+      }
+    }
+  } else if (warp >= 2 + kEpiWarps) {
+    // ---------------------------------------------------------------- MXFP4 dequant
+    const int tid = threadIdx.x - 32 * (2 + kEpiWarps);
+    const int j = tid & 7;
+    int s = 0, bs = 0;
+    uint32_t ph = 0, bph = 0;
+    for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
+      const Unit u = unit_at(g, t);
+      const size_t row0 = (size_t)u.v * g.R + (size_t)u.n * g.N;
+      int c[kRowsPerThread];
+      const uint8_t* sp[kRowsPerThread];
+      uint32_t sb[kRowsPerThread];
+#pragma unroll
+      for (int i = 0; i < kRowsPerThread; ++i) {
+        const int r = min((tid >> 3) + kRowStep * i, g.N - 1);
+        c[i] = g.cshift[row0 + r];
+        sp[i] = g.scales + (row0 + r) * g.nb + (j >> 2);
+        sb[i] = sp[i][0];
+      }
+      bool ok = true;
+      for (int kc = 0; kc < g.nkc; ++kc) {
+        // the next step's scale bytes, read while this one converts
+        uint32_t nx[kRowsPerThread];
+        const int kn = min(kc + 1, g.nkc - 1);
+#pragma unroll
+        for (int i = 0; i < kRowsPerThread; ++i) nx[i] = __ldg(sp[i] + 2 * kn);
+        if (!tc::mbar_wait(tc::smem_u32(&full_bar[s]), ph, abort, status) ||
+            !tc::mbar_wait(tc::smem_u32(&bempty_bar[bs]), bph ^ 1, abort, status)) {
+          ok = false;
+          break;
+        }
+        dequant_f16(smem + s * kLoadStage + kG * kTileA, bring + bs * kTileB, g.N, tid, sb, c);
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tc::mbar_arrive(tc::smem_u32(&bfull_bar[bs]));
+          tc::mbar_arrive(tc::smem_u32(&empty_bar[s]));
+        }
+#pragma unroll
+        for (int i = 0; i < kRowsPerThread; ++i) sb[i] = nx[i];
+        if (++s == kLoadStages) {
+          s = 0;
+          ph ^= 1;
+        }
+        if (++bs == kBStages) {
+          bs = 0;
+          bph ^= 1;
+        }
+      }
+      if (!ok) break;
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp & 3;                      // TMEM lane quarter this warp may read
+    const int half = (warp - 2) >> 2;            // which half of the 16-column chunks
+    const int nch = g.N / 16;
+    const int c_begin = half ? (nch + 1) / 2 : 0, c_end = half ? nch : (nch + 1) / 2;
+    uint32_t aph = 0;
+    for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
+      const Unit u = unit_at(g, t);
+      const int gm = u.cnt > kBM ? 2 : 1;
+      if (!tc::mbar_wait(tc::smem_u32(&tfull_bar), aph, abort, status)) break;
+      tc::tc_fence_after();
+      const int col0 = u.n * g.N;                          // first weight row of the unit
+      const float* cm = g.colmul + (size_t)u.v * g.R + col0;
+      const uint16_t* bias = g.bias ? g.bias + (size_t)u.v * g.R + col0 : nullptr;
+      for (int gi = 0; gi < gm; ++gi) {
+        const int row = gi * kBM + 32 * q + lane;          // row within the work item
+        const bool valid = row < u.cnt;
+        const int grow = g.rs.offsets[u.v] + u.row0 + row;  // grouped row index
+        const float rm = (valid && g.rowmul) ? g.rowmul[grow] : 1.f;
+        const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(256 * gi);
+        float* yrow = (!g.gateup && valid) ? g.Y + (size_t)g.rs.row2slot[grow] * g.d + col0 : nullptr;
+        uint16_t* hrow = (g.gateup && valid) ? g.h16 + (size_t)grow * g.ldh16 + col0 / 2 : nullptr;
+        for (int c = c_begin; c < c_end; ++c) {
+          float v[16];
+          tc::tmem_ld16(taddr + (uint32_t)(16 * c), v);
+          if (!valid) continue;
+          float sc[16], bi[16];
+          const float4* cm4 = reinterpret_cast<const float4*>(cm + 16 * c);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float4 f = __ldg(cm4 + i);
+            sc[4 * i] = f.x * rm;
+            sc[4 * i + 1] = f.y * rm;
+            sc[4 * i + 2] = f.z * rm;
+            sc[4 * i + 3] = f.w * rm;
+          }
+          if (bias) {
+            const uint4* b4 = reinterpret_cast<const uint4*>(bias + 16 * c);
+            const uint4 b0 = __ldg(b4), b1 = __ldg(b4 + 1);
+            const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              bi[2 * i] = bf16_lo(bw[i]);
+              bi[2 * i + 1] = bf16_hi(bw[i]);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) bi[i] = 0.f;
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = fmaf(v[i], sc[i], bi[i]);
+          if (g.gateup) {
+            // columns 2i (gate) and 2i + 1 (up) of feature 8c + i
+            uint32_t hp[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              hp[i] = pack_f16x2(clamped_glu(v[4 * i], v[4 * i + 1], g.limit, g.alpha),
+                                 clamped_glu(v[4 * i + 2], v[4 * i + 3], g.limit, g.alpha));
+            *reinterpret_cast<uint4*>(hrow + 8 * c) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
+          } else {
+            float4* dst = reinterpret_cast<float4*>(yrow + 16 * c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          }
+        }
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&tempty_bar));
+      aph ^= 1;
+    }
+  }
+
+  pdl_trigger();
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+// Per weight row n of one matrix [E * R rows, nb blocks]: c_n from the row's largest
+// finite scale byte (that block's multiplier becomes 2^13), cshift[n] = c_n and
+// colmul[n] = 2^c_n.  One warp per weight row.
+__global__ void __launch_bounds__(256)
+fp4_prep_kernel(const uint8_t* __restrict__ scales, long long rows, int nb, float* __restrict__ colmul,
+                int32_t* __restrict__ cshift) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  for (long long n = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; n < rows;
+       n += ((long long)gridDim.x * blockDim.x) >> 5) {
+    const uint8_t* sr = scales + n * nb;
+    int smax = -1;
+    for (int b = lane; b < nb; b += 32) {
+      const int s = sr[b];
+      if (s != 255) smax = max(smax, s);
+    }
+    smax = __reduce_max_sync(0xffffffffu, smax);
+    const int c = smax < 0 ? 0 : smax - 140;
+    if (lane == 0) {
+      cshift[n] = c;
+      colmul[n] = ldexpf(1.f, c);
+    }
+  }
+}
+
+// Copy the x row of every grouped row into xp as f16 times 2^e (largest magnitude
+// of the row in [2^14, 2^15)), and rowmul[r] = 2^-e.  One warp per row.
+__global__ void __launch_bounds__(256)
+gather_rows_f16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ row2slot, int S, int K,
+                       int d, uint16_t* __restrict__ xp, float* __restrict__ rowmul) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int nvec = d / 8;
+  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < S; r += (gridDim.x * blockDim.x) >> 5) {
+    const int t = row2slot[r] / K;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+    uint32_t m2 = 0;
+    for (int i = lane; i < nvec; i += 32) {
+      const uint4 v = ldg_nc_v4(src + i);
+      const uint32_t mk = 0x7FFF7FFFu;
+      m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(v.x & mk, v.y & mk), __vmaxu2(v.z & mk, v.w & mk)));
+    }
+    const uint32_t m = __reduce_max_sync(0xffffffffu, max(m2 & 0xffffu, m2 >> 16));
+    const int ex = (int)(m >> 7);
+    const int e = (m == 0 || ex == 255) ? 0 : min(141 - ex, 126);   // m * 2^e in [2^14, 2^15)
+    const float sc = exp2i(e);
+    uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)r * d);
+    for (int i = lane; i < nvec; i += 32) {
+      const uint4 v = ldg_nc_v4(src + i);
+      uint4 o;
+      o.x = pack_f16x2(bf16_lo(v.x) * sc, bf16_hi(v.x) * sc);
+      o.y = pack_f16x2(bf16_lo(v.y) * sc, bf16_hi(v.y) * sc);
+      o.z = pack_f16x2(bf16_lo(v.z) * sc, bf16_hi(v.z) * sc);
+      o.w = pack_f16x2(bf16_lo(v.w) * sc, bf16_hi(v.w) * sc);
+      dst[i] = o;
+    }
+    if (lane == 0) rowmul[r] = exp2i(-e);
+  }
+  pdl_trigger();
+}
+
+// Largest N (multiple of 16, at most max_n) that divides `rows`; 0 if none.
+int tile_n16(int rows, int max_n) {
+  for (int n = max_n; n >= 16; n -= 16)
+    if (rows % n == 0) return n;
+  return 0;
+}
+
+void set_fp4_gemm_smem() {
+  static bool done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || done[dev]) return;
+  cudaFuncSetAttribute(fp4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  done[dev] = true;
+}
+
+struct Fp4Scratch {
+  float* colmul_gu;     // [E * 2ff]
+  float* colmul_dn;     // [E * d]
+  int32_t* cshift_gu;   // [E * 2ff]
+  int32_t* cshift_dn;   // [E * d]
+  float* rowmul;        // [S]
+};
+
+size_t carve_off(const ExpertParams& p, int S, Fp4Scratch* sc, uint8_t* base) {
+  auto a256 = [](size_t v) { return (v + 255) & ~size_t(255); };
+  const size_t Rg = 2 * (size_t)p.ff * p.E, Rd = (size_t)p.d * p.E;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    uint8_t* q = base ? base + off : nullptr;
+    off = a256(off + bytes);
+    return q;
+  };
+  uint8_t* a = take(4 * Rg);
+  uint8_t* b = take(4 * Rd);
+  uint8_t* c = take(4 * Rg);
+  uint8_t* d = take(4 * Rd);
+  uint8_t* e = take(4 * (size_t)S);
+  if (sc) {
+    sc->colmul_gu = reinterpret_cast<float*>(a);
+    sc->colmul_dn = reinterpret_cast<float*>(b);
+    sc->cshift_gu = reinterpret_cast<int32_t*>(c);
+    sc->cshift_dn = reinterpret_cast<int32_t*>(d);
+    sc->rowmul = reinterpret_cast<float*>(e);
+  }
+  return off;
+}
+
+Fp4Scratch carve(const ExpertParams& p, uint8_t* base, int S) {
+  Fp4Scratch sc;
+  carve_off(p, S, &sc, base);
+  return sc;
+}
+
+cudaError_t launch_fp4_gemm(const CUtensorMap& tA, const CUtensorMap& tC, const F4Gemm& g, int max_items,
+                            cudaStream_t s) {
+  set_fp4_gemm_smem();
+  const long long units = (long long)max_items * g.nt;
+  int grid = sm_count();
+  if (units < grid) grid = (int)(units > 0 ? units : 1);
+  return launch_pdl(fp4_gemm_kernel, dim3(grid), dim3(kThreads), kSmemBytes, s, tA, tC, g);
+}
+
+}  // namespace
+
+bool prefill_fp4_supported(const ExpertParams& p, int wfmt, int interleaved) {
+  if (wfmt != MOE_WFMT_MXFP4 || !interleaved || p.sff || p.act != MOE_ACT_CLAMPED_GLU) return false;
+  if (p.d % kBK || p.ff % kBK) return false;
+  // h must stay well inside the f16 range: |h| <= (L + 1) * max(L, 1 / alpha).
+  if (!(p.limit >= 0.f) || !(p.alpha > 0.f)) return false;
+  const double bound = ((double)p.limit + 1.0) * fmax((double)p.limit, 1.0 / (double)p.alpha);
+  if (!(bound <= 16384.0)) return false;
+  // gate_up N: a multiple of 16 (so gate, up pairs never straddle a tile) dividing 2ff.
+  return tile_n16(2 * p.ff, kMaxN) != 0 && tile_n16(p.d, kMaxN) != 0;
+}
+
+size_t prefill_fp4_scratch_bytes(const ExpertParams& p, int S) { return carve_off(p, S, nullptr, nullptr); }
+
+cudaError_t launch_prefill_fp4_prep(const ExpertParams& p, uint8_t* scratch, int S, cudaStream_t s) {
+  const Fp4Scratch sc = carve(p, scratch, S);
+  const long long rg = (long long)p.E * 2 * p.ff, rd = (long long)p.E * p.d;
+  int blocks = (int)std::min<long long>((rg * 32 + 255) / 256, 152 * 8);
+  cudaError_t e = launch_pdl(fp4_prep_kernel, dim3(blocks), dim3(256), 0, s, p.gu_scales, rg, p.d / 32,
+                             sc.colmul_gu, sc.cshift_gu);
+  if (e != cudaSuccess) return e;
+  blocks = (int)std::min<long long>((rd * 32 + 255) / 256, 152 * 8);
+  return launch_pdl(fp4_prep_kernel, dim3(blocks), dim3(256), 0, s, p.dn_scales, rd, p.ff / 32, sc.colmul_dn,
+                    sc.cshift_dn);
+}
+
+cudaError_t launch_gather_rows_f16(const ExpertParams& p, const uint16_t* x, const int32_t* row2slot, int S,
+                                   int K, uint16_t* xp16, uint8_t* scratch, cudaStream_t s) {
+  const Fp4Scratch sc = carve(p, scratch, S);
+  int blocks = (S + 7) / 8;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  if (blocks < 1) blocks = 1;
+  return launch_pdl(gather_rows_f16_kernel, dim3(blocks), dim3(256), 0, s, x, row2slot, S, K, p.d, xp16,
+                    sc.rowmul);
+}
+
+cudaError_t launch_gateup_prefill_fp4(const ExpertParams& p, const RouteState& rs, const uint16_t* xp16, int S,
+                                      uint16_t* h16, int ldh16, uint8_t* scratch, int max_items,
+                                      cudaStream_t s) {
+  const Fp4Scratch sc = carve(p, scratch, S);
+  F4Gemm g{};
+  g.rs = rs;
+  g.E = p.E;
+  g.R = 2 * p.ff;
+  g.nb = p.d / 32;
+  g.N = tile_n16(g.R, kMaxN);
+  g.nt = g.R / g.N;
+  g.nkc = p.d / kBK;
+  g.colmul = sc.colmul_gu;
+  g.cshift = sc.cshift_gu;
+  g.scales = p.gu_scales;
+  g.rowmul = sc.rowmul;
+  g.bias = p.gu_bias;
+  g.gateup = 1;
+  g.h16 = h16;
+  g.ldh16 = ldh16;
+  g.limit = p.limit;
+  g.alpha = p.alpha;
+  g.d = p.d;
+  CUtensorMap tA, tC;
+  if (!make_map(&tA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xp16, (uint64_t)(S > 0 ? S : 1), (uint64_t)p.d,
+                (uint64_t)p.d * 2, kBM, kBK, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if (!make_map(&tC, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.gate_up, (uint64_t)p.E * g.R, (uint64_t)p.d / 2,
+                (uint64_t)p.d / 2, (uint32_t)g.N, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  return launch_fp4_gemm(tA, tC, g, max_items, s);
+}
+
+cudaError_t launch_down_prefill_fp4(const ExpertParams& p, const RouteState& rs, const uint16_t* h16, int ldh16,
+                                    int S, float* Y, uint8_t* scratch, int max_items, cudaStream_t s) {
+  const Fp4Scratch sc = carve(p, scratch, S);
+  F4Gemm g{};
+  g.rs = rs;
+  g.E = p.E;
+  g.R = p.d;
+  g.nb = p.ff / 32;
+  g.N = tile_n16(g.R, kMaxN);
+  g.nt = g.R / g.N;
+  g.nkc = p.ff / kBK;
+  g.colmul = sc.colmul_dn;
+  g.cshift = sc.cshift_dn;
+  g.scales = p.dn_scales;
+  g.rowmul = nullptr;
+  g.bias = p.dn_bias;
+  g.gateup = 0;
+  g.Y = Y;
+  g.d = p.d;
+  CUtensorMap tA, tC;
+  if (!make_map(&tA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, h16, (uint64_t)(S > 0 ? S : 1), (uint64_t)p.ff,
+                (uint64_t)ldh16 * 2, kBM, kBK, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if (!make_map(&tC, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.down, (uint64_t)p.E * g.R, (uint64_t)p.ff / 2,
+                (uint64_t)p.ff / 2, (uint32_t)g.N, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  return launch_fp4_gemm(tA, tC, g, max_items, s);
+}
+
+}  // namespace moe

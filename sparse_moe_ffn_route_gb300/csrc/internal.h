@@ -142,6 +142,21 @@ cudaError_t launch_down_prefill(const ExpertParams& p, int wfmt, const RouteStat
                                 const uint16_t* h, int ldh, int S, float* Y,
                                 const uint8_t* scalesT, int max_mtiles, cudaStream_t s);
 
+// Prefill path for MXFP4 experts with the clamped GLU (expert_prefill_fp4.cu): f16
+// operands, weights decoded once per two m tiles.  The work list must hold items of
+// up to 256 rows (permute with tpg = 256).  Scratch (prefill_fp4_scratch_bytes):
+// per weight row shifts and multipliers, per grouped row x multipliers.
+bool prefill_fp4_supported(const ExpertParams& p, int wfmt, int interleaved);
+size_t prefill_fp4_scratch_bytes(const ExpertParams& p, int S);
+cudaError_t launch_prefill_fp4_prep(const ExpertParams& p, uint8_t* scratch, int S, cudaStream_t s);
+cudaError_t launch_gather_rows_f16(const ExpertParams& p, const uint16_t* x, const int32_t* row2slot, int S,
+                                   int K, uint16_t* xp16, uint8_t* scratch, cudaStream_t s);
+cudaError_t launch_gateup_prefill_fp4(const ExpertParams& p, const RouteState& rs, const uint16_t* xp16, int S,
+                                      uint16_t* h16, int ldh16, uint8_t* scratch, int max_items,
+                                      cudaStream_t s);
+cudaError_t launch_down_prefill_fp4(const ExpertParams& p, const RouteState& rs, const uint16_t* h16, int ldh16,
+                                    int S, float* Y, uint8_t* scratch, int max_items, cudaStream_t s);
+
 // MXFP4 [rows, n_in/32, 16] + scales -> bf16 [rows, n_in].
 cudaError_t launch_mxfp4_to_bf16(const uint8_t* blocks, const uint8_t* scales, long long rows,
                                  int n_in, uint16_t* out, cudaStream_t s);

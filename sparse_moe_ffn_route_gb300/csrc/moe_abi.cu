@@ -18,6 +18,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct Layout {
   int K, E1, S, ldl, ldh;
   bool prefill;             // the expert phase runs the tcgen05 grouped GEMMs
+  bool prefill_fp4;         // ... in their f16-operand MXFP4 form (expert_prefill_fp4.cu)
   size_t status, counts, offsets, work, n_work, slot_expert, slot_w, row2slot, logits, h, Y,
       xp, scalesT, xstage, ystage, total;
 };
@@ -80,7 +81,14 @@ bool make_layout(const moe_cfg_t* c, int T, Layout* L) {
     sp.E = c->n_experts;
     sp.d = c->d_model;
     sp.ff = c->expert_ff;
-    L->scalesT = take(L->prefill ? prefill_scales_bytes(sp, c->wfmt) : 0);
+    sp.sff = c->shared_ff;
+    sp.act = c->act;
+    sp.limit = c->glu_limit;
+    sp.alpha = c->glu_alpha;
+    L->prefill_fp4 = L->prefill && prefill_fp4_supported(sp, c->wfmt, c->interleaved_gate_up);
+    L->scalesT = take(!L->prefill        ? 0
+                      : L->prefill_fp4 ? prefill_fp4_scratch_bytes(sp, L->S)
+                                       : prefill_scales_bytes(sp, c->wfmt));
   }
   L->xstage = take(2 * Tz * d);
   L->ystage = take(4 * Tz * d);
@@ -239,6 +247,27 @@ int run_experts(const moe_cfg_t* c, const void* x, int T, const moe_experts_t* e
   const ExpertParams p = expert_params(c, e, sh);
   uint16_t* h = at<uint16_t>(ws, L.h);
   float* Y = at<float>(ws, L.Y);
+  if (L.prefill_fp4) {
+    // MXFP4 with the clamped GLU: f16-operand grouped GEMMs over work items of 256 rows
+    // (two m tiles per dequantised weight tile).
+    constexpr int kItemRows = 256;
+    const int max_items = L.E1 + (L.S + kItemRows - 1) / kItemRows;
+    uint16_t* xp16 = at<uint16_t>(ws, L.xp);
+    uint8_t* scratch = at<uint8_t>(ws, L.scalesT);
+    MOE_CUDA(launch_prefill_fp4_prep(p, scratch, L.S, s));
+    MOE_CUDA(launch_permute(rs, L.S, L.E1, kItemRows, s));
+    MOE_CUDA(launch_gather_rows_f16(p, static_cast<const uint16_t*>(x), rs.row2slot, L.S, L.K, xp16, scratch,
+                                    s));
+    MOE_CUDA(mark_phase(3, s));
+    MOE_CUDA(launch_gateup_prefill_fp4(p, rs, xp16, L.S, h, L.ldh, scratch, max_items, s));
+    MOE_CUDA(mark_phase(4, s));
+    MOE_CUDA(launch_down_prefill_fp4(p, rs, h, L.ldh, L.S, Y, scratch, max_items, s));
+    MOE_CUDA(mark_phase(5, s));
+    MOE_CUDA(launch_combine(Y, rs.slot_w, rs.slot_expert, T, L.K, c->d_model, L.E1, y,
+                            c->y_fp32 != 0, s));
+    MOE_CUDA(mark_phase(6, s));
+    return MOE_OK;
+  }
   if (L.prefill) {
     // Grouped GEMMs on tcgen05: m tiles of 128 rows; A rows of gate_up gathered first.
     constexpr int kTileRows = 128;

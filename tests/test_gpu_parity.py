@@ -1,4 +1,6 @@
 """CUDA path vs the fp64 oracle, element by element, through the C ABI (GPU only)."""
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -350,3 +352,62 @@ def test_prefill_hot_expert_many_tiles():
     y16 = moe.moe_ffn_forward_routed(c, x, ids_d, w_d, experts, shared, sgate=sg)
     y32 = moe.moe_ffn_forward_routed(c.replace(y_fp32=1), x, ids_d, w_d, experts, shared, sgate=sg)
     check_outputs(y32, y16, ref.y, "hot expert")
+
+
+# ----------------------------------------------------------------------------- MXFP4 prefill forms
+FP4_PREFILL_SPECS = [
+    # about 300 rows per expert: work items of 256 rows (two m tiles) and a ragged one
+    mi.small_spec("gptoss", 128, 4, 2, 128, 0, 600, bias=("normal", 0.1)),
+    # E == k: every expert takes all 333 tokens; gate_up N 128, down N 192
+    mi.small_spec("gptoss", 192, 3, 3, 64, 0, 333),
+    # scale bytes spread over 70..130: blocks far below their row's largest scale
+    mi.small_spec("gptoss", 256, 8, 2, 192, 0, 700, bias=("zipf", 1.1), scale_lo=70, scale_hi=130),
+]
+
+
+@pytest.mark.parametrize("spec", FP4_PREFILL_SPECS, ids=lambda s: s.name)
+def test_mxfp4_prefill_f16_operands(spec):
+    """The f16-operand MXFP4 grouped GEMMs (two m tiles per decoded weight tile)."""
+    moe = moe_lib()
+    lay = mi.make_layer(spec)
+    g = oracle.gating_for(spec)
+    ref = oracle.forward(g, lay)
+    x, router, experts, shared = upload(lay)
+    c = cfg_for(spec, path=moe.PATH_PREFILL)
+    T, k = spec.tokens, spec.top_k
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    ws = moe.workspace(c, T)
+    y16 = moe.moe_ffn_forward(c, x, router, experts, shared, topk_ids=ids, ws=ws)
+    y32 = moe.moe_ffn_forward(c.replace(y_fp32=1), x, router, experts, shared, ws=ws)
+    st, bits = moe.moe_device_status(ws)
+    assert st == 0, bits
+    ids_g = ids.cpu().numpy()
+    diff = np.any(ids_g != ref.ids, axis=1)
+    assert not np.any(diff & ~oracle.near_tie_tokens(ref.logits, ref.ids))
+    if np.any(diff):
+        ref = oracle.forward(g, lay, forced_ids=np.where(diff[:, None], ids_g, ref.ids))
+    check_outputs(y32, y16, ref.y, spec.name)
+
+
+@pytest.mark.parametrize("path", [1, 2], ids=["decode", "prefill"])
+def test_mxfp4_unbounded_glu_limit(path):
+    """A clamp limit too wide for an f16 h takes the bf16-dequant grouped GEMMs."""
+    moe = moe_lib()
+    spec = mi.small_spec("gptoss", 128, 8, 2, 128, 0, 300, bias=("normal", 0.1), scale_lo=112,
+                         scale_hi=118)
+    lay = mi.make_layer(spec)
+    g = dataclasses.replace(oracle.gating_for(spec), limit=300.0)
+    ref = oracle.forward(g, lay)
+    x, router, experts, shared = upload(lay)
+    c = cfg_for(spec, path=path).replace(glu_limit=300.0)
+    ids = torch.empty((300, 2), dtype=torch.int32, device="cuda")
+    ws = moe.workspace(c, 300)
+    y16 = moe.moe_ffn_forward(c, x, router, experts, shared, topk_ids=ids, ws=ws)
+    y32 = moe.moe_ffn_forward(c.replace(y_fp32=1), x, router, experts, shared, ws=ws)
+    assert moe.moe_device_status(ws)[0] == 0
+    ids_g = ids.cpu().numpy()
+    diff = np.any(ids_g != ref.ids, axis=1)
+    assert not np.any(diff & ~oracle.near_tie_tokens(ref.logits, ref.ids))
+    if np.any(diff):
+        ref = oracle.forward(g, lay, forced_ids=np.where(diff[:, None], ids_g, ref.ids))
+    check_outputs(y32, y16, ref.y, "limit 300")
