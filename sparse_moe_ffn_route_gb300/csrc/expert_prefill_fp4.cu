@@ -65,7 +65,8 @@ constexpr int kCodes = kMaxN * (kBK / 2);         // 7680 B
 constexpr int kLoadStage = ((kG * kTileA + kCodes + 1023) / 1024) * 1024;
 constexpr int kLoadStages = 4;
 constexpr int kBStages = 2;
-constexpr int kSmemBytes = kLoadStages * kLoadStage + kBStages * kTileB + 1024;
+constexpr int kEpiConst = 2 * kMaxN * 4;         // per-unit column multipliers and biases (fp32)
+constexpr int kSmemBytes = kLoadStages * kLoadStage + kBStages * kTileB + kEpiConst + 1024;
 constexpr int kEpiWarps = 8;
 constexpr int kDqWarps = 8;
 constexpr int kThreads = 32 * (2 + kEpiWarps + kDqWarps);
@@ -78,7 +79,8 @@ struct F4Gemm {
   int E, R, nb;               // experts; weight rows per expert; 32-input blocks per row
   int N, nt, nkc;             // n tile width, n tiles per expert, k steps
   const float* colmul;        // [E * R] 2^c_n
-  const int32_t* cshift;      // [E * R] c_n
+  const int32_t* cinfo;       // [E * R] c_n in the low 16 bits (signed); bit 16: a block of the
+                              // row needs the general multiplier (subnormal, flushed or NaN)
   const uint8_t* scales;      // E8M0 [E, R, nb]
   const float* rowmul;        // [S] 2^-e_r of the staged x rows (gate_up) or null
   const uint16_t* bias;       // bf16 [E, R] or null
@@ -120,7 +122,7 @@ __device__ __forceinline__ float clamped_glu(float gt, float up, float limit, fl
   return (up + 1.f) * gt * sg;
 }
 
-// f16 bits of the block multiplier 2^(s - 127 - c): exact for -23 <= s - 127 - c <= 15
+// f16x2 of the block multiplier 2^(s - 127 - c): exact for -23 <= s - 127 - c <= 15
 // (subnormal below -14), 0 below -23 (the block is flushed), NaN for s = 255.
 __device__ __forceinline__ uint32_t block_mult_f16(uint32_t s, int c) {
   const int qe = (int)s - 127 - c;
@@ -129,34 +131,44 @@ __device__ __forceinline__ uint32_t block_mult_f16(uint32_t s, int c) {
   return m | (m << 16);
 }
 
-// Rows of one k step a dequant thread converts: r = tid / 8 + 32 i (i < kRowsPerThread),
-// chunk j = tid % 8 (inputs 8j..8j+7 of the step, block j / 4).
-constexpr int kRowStep = 32 * kDqWarps / 8;
-constexpr int kRowsPerThread = (kMaxN + kRowStep - 1) / kRowStep;
+// A dequant thread converts whole 32-input blocks: segment sg = tid + 256 i is block
+// sg % 2 of the k step for weight row sg / 2.
+constexpr int kDqThreads = 32 * kDqWarps;
+constexpr int kSegs = (2 * kMaxN + kDqThreads - 1) / kDqThreads;
 
-// One k step of B: N rows x 64 inputs from codes (smem [N][32] bytes) into the f16
-// B tile with the 128-byte swizzle.  sb[i]: the scale byte of row r_i's block of
-// this step; c[i]: the row's shift.  Unit of work = one 16-byte output chunk.
-__device__ __forceinline__ void dequant_f16(const uint8_t* codes, uint8_t* btile, int N, int tid,
-                                            const uint32_t (&sb)[kRowsPerThread],
-                                            const int (&c)[kRowsPerThread]) {
-  const int j = tid & 7;
+// One block (16 code bytes at codes[r][16 b]) -> 32 f16 of row r of the swizzled B tile.
+__device__ __forceinline__ void dequant_block(const uint8_t* codes, uint8_t* btile, int r, int b, uint32_t m2) {
+  const uint4 w = *reinterpret_cast<const uint4*>(codes + r * 32 + b * 16);
+  const uint32_t wk[4] = {w.x, w.y, w.z, w.w};
+  uint8_t* row = btile + r * 128;
 #pragma unroll
-  for (int i = 0; i < kRowsPerThread; ++i) {
-    const int r = (tid >> 3) + kRowStep * i;
-    if (r < N) {
-      const uint32_t w = *reinterpret_cast<const uint32_t*>(codes + r * 32 + j * 4);
-      const uint32_t m2 = block_mult_f16(sb[i], c[i]);
-      uint32_t o[4];
-      e2m1x8_to_f16(w, o);
-      uint4 q;
-      q.x = f16x2_mul(o[0], m2);
-      q.y = f16x2_mul(o[1], m2);
-      q.z = f16x2_mul(o[2], m2);
-      q.w = f16x2_mul(o[3], m2);
-      *reinterpret_cast<uint4*>(btile + r * 128 + ((j ^ (r & 7)) << 4)) = q;
-    }
+  for (int k = 0; k < 4; ++k) {
+    uint32_t o[4];
+    e2m1x8_to_f16(wk[k], o);
+    uint4 q;
+    q.x = f16x2_mul(o[0], m2);
+    q.y = f16x2_mul(o[1], m2);
+    q.z = f16x2_mul(o[2], m2);
+    q.w = f16x2_mul(o[3], m2);
+    *reinterpret_cast<uint4*>(row + (((4 * b + k) ^ (r & 7)) << 4)) = q;
   }
+}
+
+// Barrier among the epilogue warps only (named barrier 1).
+__device__ __forceinline__ void epi_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+}
+
+// The same barrier, returning whether `p` holds for any epilogue thread: a decision
+// that every epilogue warp takes alike (so none is left waiting at a barrier).
+__device__ __forceinline__ bool epi_any(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{ .reg .pred pi, po; setp.ne.u32 pi, %1, 0; bar.red.or.pred po, 1, %2, pi; selp.u32 %0, 1, 0, po; }"
+      : "=r"(r)
+      : "r"((uint32_t)p), "n"(32 * kEpiWarps)
+      : "memory");
+  return r != 0;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -293,35 +305,52 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   } else if (warp >= 2 + kEpiWarps) {
     // ---------------------------------------------------------------- MXFP4 dequant
     const int tid = threadIdx.x - 32 * (2 + kEpiWarps);
-    const int j = tid & 7;
     int s = 0, bs = 0;
     uint32_t ph = 0, bph = 0;
     for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
       const Unit u = unit_at(g, t);
       const size_t row0 = (size_t)u.v * g.R + (size_t)u.n * g.N;
-      int c[kRowsPerThread];
-      const uint8_t* sp[kRowsPerThread];
-      uint32_t sb[kRowsPerThread];
+      int c[kSegs], kr[kSegs];
+      bool general = false;
+      const uint8_t* sp[kSegs];
+      uint32_t sb[kSegs];
 #pragma unroll
-      for (int i = 0; i < kRowsPerThread; ++i) {
-        const int r = min((tid >> 3) + kRowStep * i, g.N - 1);
-        c[i] = g.cshift[row0 + r];
-        sp[i] = g.scales + (row0 + r) * g.nb + (j >> 2);
+      for (int i = 0; i < kSegs; ++i) {
+        const int sg = min(tid + kDqThreads * i, 2 * g.N - 1);
+        const int r = sg >> 1;
+        const int ci = g.cinfo[row0 + r];
+        c[i] = (int)(int16_t)(ci & 0xFFFF);
+        kr[i] = 15 - 127 - c[i];
+        general |= (ci >> 16) & 1;
+        sp[i] = g.scales + (row0 + r) * g.nb + (sg & 1);
         sb[i] = sp[i][0];
       }
+      // every row of the warp's segments in the plain range: multiplier = (s + kr) << 10
+      general = __any_sync(0xffffffffu, general);
       bool ok = true;
       for (int kc = 0; kc < g.nkc; ++kc) {
         // the next step's scale bytes, read while this one converts
-        uint32_t nx[kRowsPerThread];
+        uint32_t nx[kSegs];
         const int kn = min(kc + 1, g.nkc - 1);
 #pragma unroll
-        for (int i = 0; i < kRowsPerThread; ++i) nx[i] = __ldg(sp[i] + 2 * kn);
+        for (int i = 0; i < kSegs; ++i) nx[i] = __ldg(sp[i] + 2 * kn);
         if (!tc::mbar_wait(tc::smem_u32(&full_bar[s]), ph, abort, status) ||
             !tc::mbar_wait(tc::smem_u32(&bempty_bar[bs]), bph ^ 1, abort, status)) {
           ok = false;
           break;
         }
-        dequant_f16(smem + s * kLoadStage + kG * kTileA, bring + bs * kTileB, g.N, tid, sb, c);
+        const uint8_t* codes = smem + s * kLoadStage + kG * kTileA;
+        uint8_t* bt = bring + bs * kTileB;
+#pragma unroll
+        for (int i = 0; i < kSegs; ++i) {
+          const int sg = tid + kDqThreads * i;
+          if (sg < 2 * g.N) {
+            uint32_t m2;
+            if (!general) m2 = ((sb[i] + (uint32_t)kr[i]) << 10) * 0x10001u;
+            else m2 = block_mult_f16(sb[i], c[i]);
+            dequant_block(codes, bt, sg >> 1, sg & 1, m2);
+          }
+        }
         tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -329,7 +358,7 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           tc::mbar_arrive(tc::smem_u32(&empty_bar[s]));
         }
 #pragma unroll
-        for (int i = 0; i < kRowsPerThread; ++i) sb[i] = nx[i];
+        for (int i = 0; i < kSegs; ++i) sb[i] = nx[i];
         if (++s == kLoadStages) {
           s = 0;
           ph ^= 1;
@@ -345,54 +374,57 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;                      // TMEM lane quarter this warp may read
     const int half = (warp - 2) >> 2;            // which half of the 16-column chunks
+    const int etid = threadIdx.x - 64;           // 0 .. 255 over the epilogue warps
     const int nch = g.N / 16;
     const int c_begin = half ? (nch + 1) / 2 : 0, c_end = half ? nch : (nch + 1) / 2;
+    float* ecm = reinterpret_cast<float*>(bring + kBStages * kTileB);   // [N] 2^c_n
+    float* ebi = ecm + kMaxN;                                            // [N] bias
     uint32_t aph = 0;
-    for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      // A uniform exit (the barrier also ends every use of the previous unit's constants).
+      if (epi_any(*abort != 0)) break;
       const Unit u = unit_at(g, t);
       const int gm = u.cnt > kBM ? 2 : 1;
-      if (!tc::mbar_wait(tc::smem_u32(&tfull_bar), aph, abort, status)) break;
-      tc::tc_fence_after();
       const int col0 = u.n * g.N;                          // first weight row of the unit
-      const float* cm = g.colmul + (size_t)u.v * g.R + col0;
-      const uint16_t* bias = g.bias ? g.bias + (size_t)u.v * g.R + col0 : nullptr;
+      // The unit's column constants into shared memory and the rows' factors into
+      // registers while the MMAs run.
+      for (int i = etid; i < g.N; i += 32 * kEpiWarps) {
+        ecm[i] = g.colmul[(size_t)u.v * g.R + col0 + i];
+        ebi[i] = g.bias ? bf16_to_f32(g.bias[(size_t)u.v * g.R + col0 + i]) : 0.f;
+      }
+      float rm[kG];
+      size_t dst[kG];
+#pragma unroll
+      for (int gi = 0; gi < kG; ++gi) {
+        const int row = gi * kBM + 32 * q + lane;
+        const int grow = g.rs.offsets[u.v] + u.row0 + row;
+        const bool valid = gi < gm && row < u.cnt;
+        rm[gi] = (valid && g.rowmul) ? g.rowmul[grow] : 1.f;
+        dst[gi] = !valid ? ~size_t(0)
+                  : g.gateup ? (size_t)grow * g.ldh16 + col0 / 2
+                             : (size_t)g.rs.row2slot[grow] * g.d + col0;
+      }
+      epi_sync();
+      // On give-up the abort flag is set, and the next epi_any leaves the loop.
+      if (!tc::mbar_wait(tc::smem_u32(&tfull_bar), aph, abort, status)) continue;
+      tc::tc_fence_after();
       for (int gi = 0; gi < gm; ++gi) {
-        const int row = gi * kBM + 32 * q + lane;          // row within the work item
-        const bool valid = row < u.cnt;
-        const int grow = g.rs.offsets[u.v] + u.row0 + row;  // grouped row index
-        const float rm = (valid && g.rowmul) ? g.rowmul[grow] : 1.f;
+        const bool valid = dst[gi] != ~size_t(0);
         const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(256 * gi);
-        float* yrow = (!g.gateup && valid) ? g.Y + (size_t)g.rs.row2slot[grow] * g.d + col0 : nullptr;
-        uint16_t* hrow = (g.gateup && valid) ? g.h16 + (size_t)grow * g.ldh16 + col0 / 2 : nullptr;
         for (int c = c_begin; c < c_end; ++c) {
           float v[16];
           tc::tmem_ld16(taddr + (uint32_t)(16 * c), v);
           if (!valid) continue;
-          float sc[16], bi[16];
-          const float4* cm4 = reinterpret_cast<const float4*>(cm + 16 * c);
+          const float4* cm4 = reinterpret_cast<const float4*>(ecm + 16 * c);
+          const float4* bi4 = reinterpret_cast<const float4*>(ebi + 16 * c);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const float4 f = __ldg(cm4 + i);
-            sc[4 * i] = f.x * rm;
-            sc[4 * i + 1] = f.y * rm;
-            sc[4 * i + 2] = f.z * rm;
-            sc[4 * i + 3] = f.w * rm;
+            const float4 f = cm4[i], b = bi4[i];
+            v[4 * i] = fmaf(v[4 * i], f.x * rm[gi], b.x);
+            v[4 * i + 1] = fmaf(v[4 * i + 1], f.y * rm[gi], b.y);
+            v[4 * i + 2] = fmaf(v[4 * i + 2], f.z * rm[gi], b.z);
+            v[4 * i + 3] = fmaf(v[4 * i + 3], f.w * rm[gi], b.w);
           }
-          if (bias) {
-            const uint4* b4 = reinterpret_cast<const uint4*>(bias + 16 * c);
-            const uint4 b0 = __ldg(b4), b1 = __ldg(b4 + 1);
-            const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              bi[2 * i] = bf16_lo(bw[i]);
-              bi[2 * i + 1] = bf16_hi(bw[i]);
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) bi[i] = 0.f;
-          }
-#pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = fmaf(v[i], sc[i], bi[i]);
           if (g.gateup) {
             // columns 2i (gate) and 2i + 1 (up) of feature 8c + i
             uint32_t hp[4];
@@ -400,11 +432,11 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             for (int i = 0; i < 4; ++i)
               hp[i] = pack_f16x2(clamped_glu(v[4 * i], v[4 * i + 1], g.limit, g.alpha),
                                  clamped_glu(v[4 * i + 2], v[4 * i + 3], g.limit, g.alpha));
-            *reinterpret_cast<uint4*>(hrow + 8 * c) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
+            *reinterpret_cast<uint4*>(g.h16 + dst[gi] + 8 * c) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
           } else {
-            float4* dst = reinterpret_cast<float4*>(yrow + 16 * c);
+            float4* yp = reinterpret_cast<float4*>(g.Y + dst[gi] + 16 * c);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            for (int i = 0; i < 4; ++i) yp[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
           }
         }
       }
@@ -423,26 +455,31 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 }
 
 // Per weight row n of one matrix [E * R rows, nb blocks]: c_n from the row's largest
-// finite scale byte (that block's multiplier becomes 2^13), cshift[n] = c_n and
-// colmul[n] = 2^c_n.  One warp per weight row.
+// finite scale byte (that block's multiplier becomes 2^13), colmul[n] = 2^c_n, and
+// cinfo[n] = c_n | general << 16, where `general` marks a row with a block whose
+// multiplier is not a normal f16 (scale byte more than 27 below the largest, or 255).
+// One warp per weight row.
 __global__ void __launch_bounds__(256)
 fp4_prep_kernel(const uint8_t* __restrict__ scales, long long rows, int nb, float* __restrict__ colmul,
-                int32_t* __restrict__ cshift) {
+                int32_t* __restrict__ cinfo) {
   pdl_wait();
   pdl_trigger();
   const int lane = threadIdx.x & 31;
   for (long long n = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; n < rows;
        n += ((long long)gridDim.x * blockDim.x) >> 5) {
     const uint8_t* sr = scales + n * nb;
-    int smax = -1;
+    int smax = -1, smin = 256;
     for (int b = lane; b < nb; b += 32) {
       const int s = sr[b];
       if (s != 255) smax = max(smax, s);
+      smin = min(smin, s == 255 ? -1000 : s);
     }
     smax = __reduce_max_sync(0xffffffffu, smax);
+    smin = __reduce_min_sync(0xffffffffu, smin);
     const int c = smax < 0 ? 0 : smax - 140;
+    const int general = (smax < 0 || smin < smax - 27) ? 1 : 0;
     if (lane == 0) {
-      cshift[n] = c;
+      cinfo[n] = (c & 0xFFFF) | (general << 16);
       colmul[n] = ldexpf(1.f, c);
     }
   }
@@ -503,8 +540,8 @@ void set_fp4_gemm_smem() {
 struct Fp4Scratch {
   float* colmul_gu;     // [E * 2ff]
   float* colmul_dn;     // [E * d]
-  int32_t* cshift_gu;   // [E * 2ff]
-  int32_t* cshift_dn;   // [E * d]
+  int32_t* cinfo_gu;    // [E * 2ff]
+  int32_t* cinfo_dn;    // [E * d]
   float* rowmul;        // [S]
 };
 
@@ -525,8 +562,8 @@ size_t carve_off(const ExpertParams& p, int S, Fp4Scratch* sc, uint8_t* base) {
   if (sc) {
     sc->colmul_gu = reinterpret_cast<float*>(a);
     sc->colmul_dn = reinterpret_cast<float*>(b);
-    sc->cshift_gu = reinterpret_cast<int32_t*>(c);
-    sc->cshift_dn = reinterpret_cast<int32_t*>(d);
+    sc->cinfo_gu = reinterpret_cast<int32_t*>(c);
+    sc->cinfo_dn = reinterpret_cast<int32_t*>(d);
     sc->rowmul = reinterpret_cast<float*>(e);
   }
   return off;
@@ -567,11 +604,11 @@ cudaError_t launch_prefill_fp4_prep(const ExpertParams& p, uint8_t* scratch, int
   const long long rg = (long long)p.E * 2 * p.ff, rd = (long long)p.E * p.d;
   int blocks = (int)std::min<long long>((rg * 32 + 255) / 256, 152 * 8);
   cudaError_t e = launch_pdl(fp4_prep_kernel, dim3(blocks), dim3(256), 0, s, p.gu_scales, rg, p.d / 32,
-                             sc.colmul_gu, sc.cshift_gu);
+                             sc.colmul_gu, sc.cinfo_gu);
   if (e != cudaSuccess) return e;
   blocks = (int)std::min<long long>((rd * 32 + 255) / 256, 152 * 8);
   return launch_pdl(fp4_prep_kernel, dim3(blocks), dim3(256), 0, s, p.dn_scales, rd, p.ff / 32, sc.colmul_dn,
-                    sc.cshift_dn);
+                    sc.cinfo_dn);
 }
 
 cudaError_t launch_gather_rows_f16(const ExpertParams& p, const uint16_t* x, const int32_t* row2slot, int S,
@@ -597,7 +634,7 @@ cudaError_t launch_gateup_prefill_fp4(const ExpertParams& p, const RouteState& r
   g.nt = g.R / g.N;
   g.nkc = p.d / kBK;
   g.colmul = sc.colmul_gu;
-  g.cshift = sc.cshift_gu;
+  g.cinfo = sc.cinfo_gu;
   g.scales = p.gu_scales;
   g.rowmul = sc.rowmul;
   g.bias = p.gu_bias;
@@ -629,7 +666,7 @@ cudaError_t launch_down_prefill_fp4(const ExpertParams& p, const RouteState& rs,
   g.nt = g.R / g.N;
   g.nkc = p.ff / kBK;
   g.colmul = sc.colmul_dn;
-  g.cshift = sc.cshift_dn;
+  g.cinfo = sc.cinfo_dn;
   g.scales = p.dn_scales;
   g.rowmul = nullptr;
   g.bias = p.dn_bias;
