@@ -9,9 +9,14 @@
 //   - x rows are staged as f16 times 2^e per row (largest magnitude in
 //     [2^14, 2^15)), which holds every bf16 value of the row exactly except those
 //     more than 2^38 below its largest; rowmul[r] = 2^-e undoes it in the epilogue.
-//   - h is bounded by the clamps (|h| <= (L + 1) * max(L, 1/a)), so it is stored
-//     as plain f16 (11 significant bits) and the down projection takes one MMA per
-//     k step.
+//   - h is bounded by the clamps, |h| <= (L + 1) * max(L, 1 / alpha), so the gate_up
+//     epilogue stores it as f16 times a fixed 2^kh (the bound lands below 2^15) and
+//     records each row's largest |h|.  A row whose largest |h| is below 2^(-2 - kh)
+//     would lose bits to f16 subnormals: for such rows (all of whose 8-feature
+//     chunks are then small too) the epilogue also writes each small chunk in fp32,
+//     and h_fix_f16_kernel (stage_f16.cu) re-stages the row with its own power of
+//     two.  The down projection thus takes one f16 MMA per k step and h keeps 11
+//     significant bits at any magnitude.
 //   - weights: an E2M1 code converts exactly to f16 with cvt.rn.f16x2.e2m1x2; the
 //     block scale 2^(s - 127) is split into 2^(s - 127 - c_n) * 2^c_n, with c_n per
 //     weight row n chosen (fp4_prep_kernel) so that the largest finite block scale
@@ -49,6 +54,7 @@
 #include <cstring>
 
 #include "common.cuh"
+#include "fp4_f16.cuh"
 #include "internal.h"
 #include "tc.cuh"
 
@@ -84,9 +90,12 @@ struct F4Gemm {
   const uint8_t* scales;      // E8M0 [E, R, nb]
   const float* rowmul;        // [S] 2^-e_r of the staged x rows (gate_up) or null
   const uint16_t* bias;       // bf16 [E, R] or null
-  int gateup;                 // 1: gate_up (h16 out), 0: down (Y out)
-  uint16_t* h16;              // f16 [S, ldh16]
-  int ldh16;
+  int gateup;                 // 1: gate_up (h out), 0: down (Y out)
+  uint16_t* h16;              // f16 [S, ldh]: h * 2^kh
+  float* hside;               // fp32 [S, ldh]: chunks of 8 features whose largest |h| < hsmall
+  int ldh;
+  float hboost, hsmall;       // 2^kh, 2^(-2 - kh)
+  uint32_t* hmax;             // [S] largest |h| of each row (fp32 bits), accumulated
   float limit, alpha;
   float* Y;                   // fp32 [S, d] in slot order
   int d;
@@ -108,51 +117,10 @@ __device__ __forceinline__ Unit unit_at(const F4Gemm& g, int t) {
   return u;
 }
 
-// h for one (gate, up) pair; sigmoid(z) = (1 + tanh(z / 2)) / 2 with the hardware tanh.
-__device__ __forceinline__ float tanh_fast(float z) {
-  float r;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(r) : "f"(z));
-  return r;
-}
-
-__device__ __forceinline__ float clamped_glu(float gt, float up, float limit, float alpha) {
-  gt = fminf(gt, limit);
-  up = fminf(fmaxf(up, -limit), limit);
-  const float sg = fmaf(0.5f, tanh_fast(0.5f * alpha * gt), 0.5f);
-  return (up + 1.f) * gt * sg;
-}
-
-// f16x2 of the block multiplier 2^(s - 127 - c): exact for -23 <= s - 127 - c <= 15
-// (subnormal below -14), 0 below -23 (the block is flushed), NaN for s = 255.
-__device__ __forceinline__ uint32_t block_mult_f16(uint32_t s, int c) {
-  const int qe = (int)s - 127 - c;
-  uint32_t m = qe >= -14 ? (uint32_t)(qe + 15) << 10 : (qe >= -23 ? 1u << (qe + 24) : 0u);
-  if (s == 255u) m = 0x7E00u;
-  return m | (m << 16);
-}
-
 // A dequant thread converts whole 32-input blocks: segment sg = tid + 256 i is block
 // sg % 2 of the k step for weight row sg / 2.
 constexpr int kDqThreads = 32 * kDqWarps;
 constexpr int kSegs = (2 * kMaxN + kDqThreads - 1) / kDqThreads;
-
-// One block (16 code bytes at codes[r][16 b]) -> 32 f16 of row r of the swizzled B tile.
-__device__ __forceinline__ void dequant_block(const uint8_t* codes, uint8_t* btile, int r, int b, uint32_t m2) {
-  const uint4 w = *reinterpret_cast<const uint4*>(codes + r * 32 + b * 16);
-  const uint32_t wk[4] = {w.x, w.y, w.z, w.w};
-  uint8_t* row = btile + r * 128;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    uint32_t o[4];
-    e2m1x8_to_f16(wk[k], o);
-    uint4 q;
-    q.x = f16x2_mul(o[0], m2);
-    q.y = f16x2_mul(o[1], m2);
-    q.z = f16x2_mul(o[2], m2);
-    q.w = f16x2_mul(o[3], m2);
-    *reinterpret_cast<uint4*>(row + (((4 * b + k) ^ (r & 7)) << 4)) = q;
-  }
-}
 
 // Barrier among the epilogue warps only (named barrier 1).
 __device__ __forceinline__ void epi_sync() {
@@ -346,9 +314,9 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           const int sg = tid + kDqThreads * i;
           if (sg < 2 * g.N) {
             uint32_t m2;
-            if (!general) m2 = ((sb[i] + (uint32_t)kr[i]) << 10) * 0x10001u;
-            else m2 = block_mult_f16(sb[i], c[i]);
-            dequant_block(codes, bt, sg >> 1, sg & 1, m2);
+            if (!general) m2 = f16op::block_mult_f16_plain(sb[i], (uint32_t)kr[i]);
+            else m2 = f16op::block_mult_f16(sb[i], c[i]);
+            f16op::dequant_block(codes, bt, sg >> 1, sg & 1, m2);
           }
         }
         tc::fence_proxy_async_smem();
@@ -401,7 +369,7 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         const bool valid = gi < gm && row < u.cnt;
         rm[gi] = (valid && g.rowmul) ? g.rowmul[grow] : 1.f;
         dst[gi] = !valid ? ~size_t(0)
-                  : g.gateup ? (size_t)grow * g.ldh16 + col0 / 2
+                  : g.gateup ? (size_t)grow * g.ldh + col0 / 2
                              : (size_t)g.rs.row2slot[grow] * g.d + col0;
       }
       epi_sync();
@@ -411,6 +379,7 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       for (int gi = 0; gi < gm; ++gi) {
         const bool valid = dst[gi] != ~size_t(0);
         const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(256 * gi);
+        uint32_t hm = 0;                                   // largest |h| of this row here
         for (int c = c_begin; c < c_end; ++c) {
           float v[16];
           tc::tmem_ld16(taddr + (uint32_t)(16 * c), v);
@@ -427,18 +396,30 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           }
           if (g.gateup) {
             // columns 2i (gate) and 2i + 1 (up) of feature 8c + i
+            float hv[8];
+            uint32_t cmax = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              hv[i] = f16op::clamped_glu(v[2 * i], v[2 * i + 1], g.limit, g.alpha);
+              cmax = max(cmax, f16op::abs_bits(hv[i]));
+            }
+            hm = max(hm, cmax);
             uint32_t hp[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              hp[i] = pack_f16x2(clamped_glu(v[4 * i], v[4 * i + 1], g.limit, g.alpha),
-                                 clamped_glu(v[4 * i + 2], v[4 * i + 3], g.limit, g.alpha));
+            for (int i = 0; i < 4; ++i) hp[i] = pack_f16x2(hv[2 * i] * g.hboost, hv[2 * i + 1] * g.hboost);
             *reinterpret_cast<uint4*>(g.h16 + dst[gi] + 8 * c) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
+            if (__uint_as_float(cmax) < g.hsmall) {
+              float4* sp = reinterpret_cast<float4*>(g.hside + dst[gi] + 8 * c);
+              sp[0] = make_float4(hv[0], hv[1], hv[2], hv[3]);
+              sp[1] = make_float4(hv[4], hv[5], hv[6], hv[7]);
+            }
           } else {
             float4* yp = reinterpret_cast<float4*>(g.Y + dst[gi] + 16 * c);
 #pragma unroll
             for (int i = 0; i < 4; ++i) yp[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
           }
         }
+        if (g.gateup && valid) atomicMax(g.hmax + (dst[gi] - col0 / 2) / g.ldh, hm);
       }
       tc::tc_fence_before();
       __syncwarp();
@@ -485,42 +466,6 @@ fp4_prep_kernel(const uint8_t* __restrict__ scales, long long rows, int nb, floa
   }
 }
 
-// Copy the x row of every grouped row into xp as f16 times 2^e (largest magnitude
-// of the row in [2^14, 2^15)), and rowmul[r] = 2^-e.  One warp per row.
-__global__ void __launch_bounds__(256)
-gather_rows_f16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ row2slot, int S, int K,
-                       int d, uint16_t* __restrict__ xp, float* __restrict__ rowmul) {
-  pdl_wait();
-  const int lane = threadIdx.x & 31;
-  const int nvec = d / 8;
-  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < S; r += (gridDim.x * blockDim.x) >> 5) {
-    const int t = row2slot[r] / K;
-    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
-    uint32_t m2 = 0;
-    for (int i = lane; i < nvec; i += 32) {
-      const uint4 v = ldg_nc_v4(src + i);
-      const uint32_t mk = 0x7FFF7FFFu;
-      m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(v.x & mk, v.y & mk), __vmaxu2(v.z & mk, v.w & mk)));
-    }
-    const uint32_t m = __reduce_max_sync(0xffffffffu, max(m2 & 0xffffu, m2 >> 16));
-    const int ex = (int)(m >> 7);
-    const int e = (m == 0 || ex == 255) ? 0 : min(141 - ex, 126);   // m * 2^e in [2^14, 2^15)
-    const float sc = exp2i(e);
-    uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)r * d);
-    for (int i = lane; i < nvec; i += 32) {
-      const uint4 v = ldg_nc_v4(src + i);
-      uint4 o;
-      o.x = pack_f16x2(bf16_lo(v.x) * sc, bf16_hi(v.x) * sc);
-      o.y = pack_f16x2(bf16_lo(v.y) * sc, bf16_hi(v.y) * sc);
-      o.z = pack_f16x2(bf16_lo(v.z) * sc, bf16_hi(v.z) * sc);
-      o.w = pack_f16x2(bf16_lo(v.w) * sc, bf16_hi(v.w) * sc);
-      dst[i] = o;
-    }
-    if (lane == 0) rowmul[r] = exp2i(-e);
-  }
-  pdl_trigger();
-}
-
 // Largest N (multiple of 16, at most max_n) that divides `rows`; 0 if none.
 int tile_n16(int rows, int max_n) {
   for (int n = max_n; n >= 16; n -= 16)
@@ -542,7 +487,9 @@ struct Fp4Scratch {
   float* colmul_dn;     // [E * d]
   int32_t* cinfo_gu;    // [E * 2ff]
   int32_t* cinfo_dn;    // [E * d]
-  float* rowmul;        // [S]
+  float* rowmul;        // [S] 2^-e of the staged x rows
+  uint32_t* hmax;       // [S] largest |h| per row
+  float* hmul;          // [S] 2^-e of the staged h rows
 };
 
 size_t carve_off(const ExpertParams& p, int S, Fp4Scratch* sc, uint8_t* base) {
@@ -559,12 +506,16 @@ size_t carve_off(const ExpertParams& p, int S, Fp4Scratch* sc, uint8_t* base) {
   uint8_t* c = take(4 * Rg);
   uint8_t* d = take(4 * Rd);
   uint8_t* e = take(4 * (size_t)S);
+  uint8_t* f = take(4 * (size_t)S);
+  uint8_t* h = take(4 * (size_t)S);
   if (sc) {
     sc->colmul_gu = reinterpret_cast<float*>(a);
     sc->colmul_dn = reinterpret_cast<float*>(b);
     sc->cinfo_gu = reinterpret_cast<int32_t*>(c);
     sc->cinfo_dn = reinterpret_cast<int32_t*>(d);
     sc->rowmul = reinterpret_cast<float*>(e);
+    sc->hmax = reinterpret_cast<uint32_t*>(f);
+    sc->hmul = reinterpret_cast<float*>(h);
   }
   return off;
 }
@@ -599,6 +550,13 @@ bool prefill_fp4_supported(const ExpertParams& p, int wfmt, int interleaved) {
 
 size_t prefill_fp4_scratch_bytes(const ExpertParams& p, int S) { return carve_off(p, S, nullptr, nullptr); }
 
+int h_stage_exp(float limit, float alpha) {
+  const double bound = ((double)limit + 1.0) * fmax((double)limit, 1.0 / (double)alpha);
+  int kh = 0;
+  while (kh < 24 && bound * std::ldexp(1.0, kh + 1) < 32768.0) ++kh;
+  return kh;
+}
+
 cudaError_t launch_prefill_fp4_prep(const ExpertParams& p, uint8_t* scratch, int S, cudaStream_t s) {
   const Fp4Scratch sc = carve(p, scratch, S);
   const long long rg = (long long)p.E * 2 * p.ff, rd = (long long)p.E * p.d;
@@ -611,19 +569,14 @@ cudaError_t launch_prefill_fp4_prep(const ExpertParams& p, uint8_t* scratch, int
                     sc.cinfo_dn);
 }
 
-cudaError_t launch_gather_rows_f16(const ExpertParams& p, const uint16_t* x, const int32_t* row2slot, int S,
-                                   int K, uint16_t* xp16, uint8_t* scratch, cudaStream_t s) {
+Fp4Rows prefill_fp4_rows(const ExpertParams& p, uint8_t* scratch, int S) {
   const Fp4Scratch sc = carve(p, scratch, S);
-  int blocks = (S + 7) / 8;
-  if (blocks > 152 * 8) blocks = 152 * 8;
-  if (blocks < 1) blocks = 1;
-  return launch_pdl(gather_rows_f16_kernel, dim3(blocks), dim3(256), 0, s, x, row2slot, S, K, p.d, xp16,
-                    sc.rowmul);
+  return Fp4Rows{sc.rowmul, sc.hmax, sc.hmul};
 }
 
 cudaError_t launch_gateup_prefill_fp4(const ExpertParams& p, const RouteState& rs, const uint16_t* xp16, int S,
-                                      uint16_t* h16, int ldh16, uint8_t* scratch, int max_items,
-                                      cudaStream_t s) {
+                                      uint16_t* h16, float* hside, int ldh, int kh, uint8_t* scratch,
+                                      int max_items, cudaStream_t s) {
   const Fp4Scratch sc = carve(p, scratch, S);
   F4Gemm g{};
   g.rs = rs;
@@ -640,7 +593,11 @@ cudaError_t launch_gateup_prefill_fp4(const ExpertParams& p, const RouteState& r
   g.bias = p.gu_bias;
   g.gateup = 1;
   g.h16 = h16;
-  g.ldh16 = ldh16;
+  g.hside = hside;
+  g.ldh = ldh;
+  g.hboost = ldexpf(1.f, kh);
+  g.hsmall = ldexpf(1.f, -2 - kh);
+  g.hmax = sc.hmax;
   g.limit = p.limit;
   g.alpha = p.alpha;
   g.d = p.d;
@@ -668,7 +625,7 @@ cudaError_t launch_down_prefill_fp4(const ExpertParams& p, const RouteState& rs,
   g.colmul = sc.colmul_dn;
   g.cinfo = sc.cinfo_dn;
   g.scales = p.dn_scales;
-  g.rowmul = nullptr;
+  g.rowmul = sc.hmul;
   g.bias = p.dn_bias;
   g.gateup = 0;
   g.Y = Y;

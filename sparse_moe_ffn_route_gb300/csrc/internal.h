@@ -142,18 +142,37 @@ cudaError_t launch_down_prefill(const ExpertParams& p, int wfmt, const RouteStat
                                 const uint16_t* h, int ldh, int S, float* Y,
                                 const uint8_t* scalesT, int max_mtiles, cudaStream_t s);
 
+// f16 token operands (stage_f16.cu).  Per grouped row: rowmul = 2^-e of the staged
+// x row, hmax = largest |h| (fp32 bits, accumulated by the gate_up epilogue), hmul =
+// 2^-e of the staged h row.
+struct Fp4Rows {
+  float* rowmul;
+  uint32_t* hmax;
+  float* hmul;
+};
+// x rows of the grouped order as f16 times 2^e per row (largest magnitude in
+// [2^14, 2^15)), rowmul[r] = 2^-e; clears hmax[r] when hmax is non-null.
+cudaError_t launch_gather_rows_f16(const uint16_t* x, const int32_t* row2slot, int S, int K, int d, uint16_t* xp16,
+                                   float* rowmul, uint32_t* hmax, cudaStream_t s);
+// h rows staged by the gate_up epilogue as f16 times 2^kh: hmul[r] = 2^-kh, except
+// rows whose largest |h| (hmax) is below 2^(-2 - kh), which are re-staged from their
+// fp32 copy (hside [S, ldh]) with their own power of two.
+cudaError_t launch_h_fix_f16(const float* hside, const uint32_t* hmax, int S, int ff, int kh, uint16_t* h16,
+                             int ldh, float* hmul, cudaStream_t s);
+// kh of the f16 h staging: the clamped GLU's bound on |h| times 2^kh stays below 2^15.
+int h_stage_exp(float limit, float alpha);
+
 // Prefill path for MXFP4 experts with the clamped GLU (expert_prefill_fp4.cu): f16
 // operands, weights decoded once per two m tiles.  The work list must hold items of
 // up to 256 rows (permute with tpg = 256).  Scratch (prefill_fp4_scratch_bytes):
-// per weight row shifts and multipliers, per grouped row x multipliers.
+// per weight row shifts and multipliers, and the per grouped row arrays.
 bool prefill_fp4_supported(const ExpertParams& p, int wfmt, int interleaved);
 size_t prefill_fp4_scratch_bytes(const ExpertParams& p, int S);
+Fp4Rows prefill_fp4_rows(const ExpertParams& p, uint8_t* scratch, int S);
 cudaError_t launch_prefill_fp4_prep(const ExpertParams& p, uint8_t* scratch, int S, cudaStream_t s);
-cudaError_t launch_gather_rows_f16(const ExpertParams& p, const uint16_t* x, const int32_t* row2slot, int S,
-                                   int K, uint16_t* xp16, uint8_t* scratch, cudaStream_t s);
 cudaError_t launch_gateup_prefill_fp4(const ExpertParams& p, const RouteState& rs, const uint16_t* xp16, int S,
-                                      uint16_t* h16, int ldh16, uint8_t* scratch, int max_items,
-                                      cudaStream_t s);
+                                      uint16_t* h16, float* hside, int ldh, int kh, uint8_t* scratch,
+                                      int max_items, cudaStream_t s);
 cudaError_t launch_down_prefill_fp4(const ExpertParams& p, const RouteState& rs, const uint16_t* h16, int ldh16,
                                     int S, float* Y, uint8_t* scratch, int max_items, cudaStream_t s);
 

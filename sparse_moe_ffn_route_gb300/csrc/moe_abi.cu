@@ -71,7 +71,7 @@ bool make_layout(const moe_cfg_t* c, int T, Layout* L) {
   L->row2slot = take(4 * Sz);
   L->logits = take(4 * Tz * (size_t)L->ldl);
   L->h = take(4 * Sz * (size_t)L->ldh);   // (hi, lo) bf16 halves
-  L->Y = take(4 * Sz * d);
+  L->Y = take(4 * Sz * (d > (size_t)L->ldh ? d : (size_t)L->ldh));   // also h's fp32 side copies
   L->prefill = path_for(c, T) == MOE_PATH_PREFILL &&
                prefill_supported(c->d_model, c->expert_ff, c->shared_ff, c->wfmt,
                                  c->interleaved_gate_up);
@@ -86,7 +86,7 @@ bool make_layout(const moe_cfg_t* c, int T, Layout* L) {
     sp.limit = c->glu_limit;
     sp.alpha = c->glu_alpha;
     L->prefill_fp4 = L->prefill && prefill_fp4_supported(sp, c->wfmt, c->interleaved_gate_up);
-    L->scalesT = take(!L->prefill        ? 0
+    L->scalesT = take(!L->prefill      ? 0
                       : L->prefill_fp4 ? prefill_fp4_scratch_bytes(sp, L->S)
                                        : prefill_scales_bytes(sp, c->wfmt));
   }
@@ -252,37 +252,21 @@ int run_experts(const moe_cfg_t* c, const void* x, int T, const moe_experts_t* e
     // (two m tiles per dequantised weight tile).
     constexpr int kItemRows = 256;
     const int max_items = L.E1 + (L.S + kItemRows - 1) / kItemRows;
-    uint16_t* xp16 = at<uint16_t>(ws, L.xp);
+    uint16_t* xp16 = at<uint16_t>(ws, L.xp);          // x rows as f16
     uint8_t* scratch = at<uint8_t>(ws, L.scalesT);
+    const Fp4Rows rows = prefill_fp4_rows(p, scratch, L.S);
+    uint16_t* h16 = at<uint16_t>(ws, L.h);            // h rows as f16 [S, ldh]
+    float* hside = Y;                                 // fp32 copies of small h chunks (Y is free until down)
+    const int kh = h_stage_exp(c->glu_limit, c->glu_alpha);
     MOE_CUDA(launch_prefill_fp4_prep(p, scratch, L.S, s));
     MOE_CUDA(launch_permute(rs, L.S, L.E1, kItemRows, s));
-    MOE_CUDA(launch_gather_rows_f16(p, static_cast<const uint16_t*>(x), rs.row2slot, L.S, L.K, xp16, scratch,
-                                    s));
+    MOE_CUDA(launch_gather_rows_f16(static_cast<const uint16_t*>(x), rs.row2slot, L.S, L.K, c->d_model, xp16,
+                                    rows.rowmul, rows.hmax, s));
     MOE_CUDA(mark_phase(3, s));
-    MOE_CUDA(launch_gateup_prefill_fp4(p, rs, xp16, L.S, h, L.ldh, scratch, max_items, s));
+    MOE_CUDA(launch_gateup_prefill_fp4(p, rs, xp16, L.S, h16, hside, L.ldh, kh, scratch, max_items, s));
     MOE_CUDA(mark_phase(4, s));
-    MOE_CUDA(launch_down_prefill_fp4(p, rs, h, L.ldh, L.S, Y, scratch, max_items, s));
-    MOE_CUDA(mark_phase(5, s));
-    MOE_CUDA(launch_combine(Y, rs.slot_w, rs.slot_expert, T, L.K, c->d_model, L.E1, y,
-                            c->y_fp32 != 0, s));
-    MOE_CUDA(mark_phase(6, s));
-    return MOE_OK;
-  }
-  if (L.prefill) {
-    // Grouped GEMMs on tcgen05: m tiles of 128 rows; A rows of gate_up gathered first.
-    constexpr int kTileRows = 128;
-    const int max_mtiles = L.E1 + (L.S + kTileRows - 1) / kTileRows;
-    uint16_t* xp = at<uint16_t>(ws, L.xp);
-    uint8_t* scalesT = at<uint8_t>(ws, L.scalesT);
-    if (c->wfmt == MOE_WFMT_MXFP4) MOE_CUDA(launch_transpose_scales(p, scalesT, s));
-    MOE_CUDA(launch_permute(rs, L.S, L.E1, kTileRows, s));
-    MOE_CUDA(launch_gather_rows(static_cast<const uint16_t*>(x), rs.row2slot, L.S, L.K,
-                                c->d_model, xp, s));
-    MOE_CUDA(mark_phase(3, s));
-    MOE_CUDA(launch_gateup_prefill(p, c->wfmt, c->interleaved_gate_up, rs, xp, L.S, h, L.ldh,
-                                   scalesT, max_mtiles, s));
-    MOE_CUDA(mark_phase(4, s));
-    MOE_CUDA(launch_down_prefill(p, c->wfmt, rs, h, L.ldh, L.S, Y, scalesT, max_mtiles, s));
+    MOE_CUDA(launch_h_fix_f16(hside, rows.hmax, L.S, c->expert_ff, kh, h16, L.ldh, rows.hmul, s));
+    MOE_CUDA(launch_down_prefill_fp4(p, rs, h16, L.ldh, L.S, Y, scratch, max_items, s));
     MOE_CUDA(mark_phase(5, s));
     MOE_CUDA(launch_combine(Y, rs.slot_w, rs.slot_expert, T, L.K, c->d_model, L.E1, y,
                             c->y_fp32 != 0, s));

@@ -1,0 +1,113 @@
+// Staging of the f16 token operands of the f16-operand MXFP4 kernels.
+//
+// An f16 operand keeps 11 significant bits but only 5 exponent bits, so every row
+// (a token's x, or its h) is scaled by a power of two 2^e chosen from the row's
+// largest magnitude, which then lands in [2^14, 2^15): all values of the row within
+// 2^38 of its largest keep every bit they have in bf16 (x) or 11 bits (h).  The
+// matching 2^-e is applied in the consumer's epilogue.
+//
+//   gather_rows_f16_kernel: x rows of the grouped order -> f16, rowmul[r] = 2^-e;
+//                           also clears the per-row maxima that the gate_up
+//                           epilogue accumulates for h.
+//   h_fix_f16_kernel:       h rows, written by the gate_up epilogue as f16 times a
+//                           fixed 2^kh with each row's largest |h|: rows whose
+//                           largest |h| fits that scale keep it (hmul = 2^-kh); a row
+//                           below 2^(-2 - kh) is re-staged from its fp32 copy with
+//                           its own 2^e (hmul = 2^-e).
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+// e with m * 2^e in [2^14, 2^15) for the largest magnitude m of a row, given the
+// biased exponent field of m (0 for a zero row, which then keeps e = 0; the field
+// of inf / NaN also gives e = 0 so that they propagate).
+__device__ __forceinline__ int row_exp_from_field(int ex, bool zero) {
+  if (zero || ex == 255) return 0;
+  return min(141 - ex, 126);
+}
+
+__global__ void __launch_bounds__(256)
+gather_rows_f16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ row2slot, int S, int K,
+                       int d, uint16_t* __restrict__ xp, float* __restrict__ rowmul,
+                       uint32_t* __restrict__ hmax) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int nvec = d / 8;
+  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < S; r += (gridDim.x * blockDim.x) >> 5) {
+    const int t = row2slot[r] / K;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+    uint32_t m2 = 0;
+    for (int i = lane; i < nvec; i += 32) {
+      const uint4 v = ldg_nc_v4(src + i);
+      const uint32_t mk = 0x7FFF7FFFu;
+      m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(v.x & mk, v.y & mk), __vmaxu2(v.z & mk, v.w & mk)));
+    }
+    const uint32_t m = __reduce_max_sync(0xffffffffu, max(m2 & 0xffffu, m2 >> 16));
+    const int e = row_exp_from_field((int)(m >> 7), m == 0);       // bf16 exponent field
+    const float sc = exp2i(e);
+    uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)r * d);
+    for (int i = lane; i < nvec; i += 32) {
+      const uint4 v = ldg_nc_v4(src + i);
+      uint4 o;
+      o.x = pack_f16x2(bf16_lo(v.x) * sc, bf16_hi(v.x) * sc);
+      o.y = pack_f16x2(bf16_lo(v.y) * sc, bf16_hi(v.y) * sc);
+      o.z = pack_f16x2(bf16_lo(v.z) * sc, bf16_hi(v.z) * sc);
+      o.w = pack_f16x2(bf16_lo(v.w) * sc, bf16_hi(v.w) * sc);
+      dst[i] = o;
+    }
+    if (lane == 0) {
+      rowmul[r] = exp2i(-e);
+      if (hmax) hmax[r] = 0u;
+    }
+  }
+  pdl_trigger();
+}
+
+__global__ void __launch_bounds__(256)
+h_fix_f16_kernel(const float* __restrict__ hside, const uint32_t* __restrict__ hmax, int S, int ff, int kh,
+                 uint16_t* __restrict__ h16, int ldh, float* __restrict__ hmul) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const float small = exp2i(-2 - kh);
+  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < S; r += (gridDim.x * blockDim.x) >> 5) {
+    const uint32_t m = hmax[r];
+    // NaN / inf compare false here and keep the fixed scale, so that they propagate
+    if (!(__uint_as_float(m) < small)) {
+      if (lane == 0) hmul[r] = exp2i(-kh);
+      continue;
+    }
+    const int e = row_exp_from_field((int)(m >> 23), m == 0);       // fp32 exponent field
+    const float sc = exp2i(e);
+    const float4* src = reinterpret_cast<const float4*>(hside + (size_t)r * ldh);
+    uint2* dst = reinterpret_cast<uint2*>(h16 + (size_t)r * ldh);
+    for (int i = lane; i < ff / 4; i += 32) {
+      const float4 v = src[i];
+      dst[i] = make_uint2(pack_f16x2(v.x * sc, v.y * sc), pack_f16x2(v.z * sc, v.w * sc));
+    }
+    if (lane == 0) hmul[r] = exp2i(-e);
+  }
+  pdl_trigger();
+}
+
+int grid_rows(int S) {
+  int blocks = (S + 7) / 8;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  return blocks < 1 ? 1 : blocks;
+}
+
+}  // namespace
+
+cudaError_t launch_gather_rows_f16(const uint16_t* x, const int32_t* row2slot, int S, int K, int d, uint16_t* xp16,
+                                   float* rowmul, uint32_t* hmax, cudaStream_t s) {
+  return launch_pdl(gather_rows_f16_kernel, dim3(grid_rows(S)), dim3(256), 0, s, x, row2slot, S, K, d, xp16,
+                    rowmul, hmax);
+}
+
+cudaError_t launch_h_fix_f16(const float* hside, const uint32_t* hmax, int S, int ff, int kh, uint16_t* h16,
+                             int ldh, float* hmul, cudaStream_t s) {
+  return launch_pdl(h_fix_f16_kernel, dim3(grid_rows(S)), dim3(256), 0, s, hside, hmax, S, ff, kh, h16, ldh, hmul);
+}
+
+}  // namespace moe

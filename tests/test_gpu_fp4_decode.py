@@ -93,10 +93,17 @@ def test_staged_token_magnitudes(shift, path):
     _run(spec, lay, path)
 
 
-@pytest.mark.parametrize("scale_lo,scale_hi", [(100, 150), (127, 140), (105, 128)])
+@pytest.mark.parametrize("scale_lo,scale_hi", [(100, 150), (127, 140), (105, 128), (60, 130)])
 def test_unstaged_scale_ranges(scale_lo, scale_hi):
     """Many tokens per expert (4 chunks of 8, token rows read from global memory)."""
     spec = mi.small_spec("gptoss", 128, 4, 2, 128, 0, 40, bias=("normal", 0.1),
                          scale_lo=scale_lo, scale_hi=scale_hi)
     assert 4 * spec.tokens * spec.top_k > 16 * spec.n_experts       # four-chunk items
     _run(spec, mi.make_layer(spec))
+
+
+def test_decode_many_items_and_ragged_row_tiles():
+    """Several items per expert and a ragged last 128-row tile of the down projection
+    (d = 320)."""
+    spec = mi.small_spec("gptoss", 320, 4, 2, 192, 0, 90, bias=("normal", 0.1))
+    _run(spec, mi.make_layer(spec), 1)

@@ -411,3 +411,33 @@ def test_mxfp4_unbounded_glu_limit(path):
     if np.any(diff):
         ref = oracle.forward(g, lay, forced_ids=np.where(diff[:, None], ids_g, ref.ids))
     check_outputs(y32, y16, ref.y, "limit 300")
+
+
+@pytest.mark.parametrize("shift", [-40, -14, 0, 30])
+def test_mxfp4_prefill_token_magnitudes(shift):
+    """x scaled by 2^shift (exact in bf16) with zero expert biases, so that h and y
+    follow x's magnitude: the per-row f16 staging of x and of h must absorb it."""
+    moe = moe_lib()
+    spec = mi.small_spec("gptoss", 128, 4, 2, 128, 0, 300, scale_lo=116, scale_hi=126)
+    lay = mi.make_layer(spec)
+    lay.gu_bias = np.zeros_like(lay.gu_bias)
+    lay.dn_bias = np.zeros_like(lay.dn_bias)
+    x = mi.bf16_to_f32(lay.x).astype(np.float64) * 2.0 ** shift
+    x[1] = 0.0                                   # an all-zero token row
+    x[2, 5] *= 2.0 ** 20                         # one large value among ordinary ones
+    lay.x = mi.f64_to_bf16(x)
+    g = oracle.gating_for(spec)
+    ref = oracle.forward(g, lay)
+    xd, router, experts, shared = upload(lay)
+    c = cfg_for(spec, path=moe.PATH_PREFILL)
+    ids = torch.empty((300, 2), dtype=torch.int32, device="cuda")
+    ws = moe.workspace(c, 300)
+    y16 = moe.moe_ffn_forward(c, xd, router, experts, shared, topk_ids=ids, ws=ws)
+    y32 = moe.moe_ffn_forward(c.replace(y_fp32=1), xd, router, experts, shared, ws=ws)
+    assert moe.moe_device_status(ws)[0] == 0
+    ids_g = ids.cpu().numpy()
+    diff = np.any(ids_g != ref.ids, axis=1)
+    assert not np.any(diff & ~oracle.near_tie_tokens(ref.logits, ref.ids))
+    if np.any(diff):
+        ref = oracle.forward(g, lay, forced_ids=np.where(diff[:, None], ids_g, ref.ids))
+    check_outputs(y32, y16, ref.y, f"shift {shift}")
