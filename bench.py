@@ -156,6 +156,16 @@ def expert_bytes(spec):
     return gu, dn, 2 * sff * d * 2, d * sff * 2
 
 
+def launches_per_step(plan, mxfp4):
+    """Kernels of this library one moe_ffn_forward enqueues, by kernel plan."""
+    router = 2                                            # logits, select
+    if plan in (1, 2):                                    # decode: permute, gate_up, down, combine
+        return router + 4
+    if plan == 3:                                         # (+ 2 scale transposes) permute, gather, 2 GEMMs, combine
+        return router + 5 + (2 if mxfp4 else 0)
+    return router + 8    # 2 scale preps, permute, gather, gate_up, h fix-up, down, combine
+
+
 def work(spec, ids):
     """Algorithmic bytes and flops per phase for one step with routing `ids` [T, k]."""
     import numpy as np
@@ -274,6 +284,7 @@ def run_ours(args, rank, world, local_rank):
     sink = torch.zeros((), dtype=torch.int64, device=dev)
     stream = torch.cuda.current_stream()
 
+    plan = moe.moe_kernel_plan(cfg, T)
     moe.moe_ffn_forward(cfg, x, router, experts, shared, y=y, topk_ids=ids, ws=ws)
     torch.cuda.synchronize()
     st, bits = moe.moe_device_status(ws)
@@ -378,8 +389,7 @@ def run_ours(args, rank, world, local_rank):
             "per_unit_bytes": per_unit[dom], "units_per_launch": distinct,
             "hbm_gbs": gbs, "hbm_frac": gbs / hbm,
             "tensor_tflops": tfs, "tensor_frac": tfs / tpeak,
-            "path": "prefill (tcgen05 grouped GEMM)" if moe.moe_select_path(cfg, T) == moe.PATH_PREFILL
-            else "decode (weight-streaming grouped matvec)"}
+            "path": moe.PLAN_NAMES[plan]}
     step_bytes = sum(by.values())
     cpu = None
     if args.cpu_seconds > 0:
@@ -396,7 +406,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 6 * args.steps,
+        "gpu_launches": launches_per_step(plan, spec.mxfp4) * args.steps,
         "clocks": sampler.summary(t0, t1),
         "phases_ms": phase_ms,
         "step_hbm_gbs": step_bytes / (ms / 1e3) / 1e9,

@@ -148,6 +148,22 @@ size_t moe_workspace_bytes(const moe_cfg_t* cfg, int32_t T);
  * MOE_PATH_PREFILL), or a negative MOE_ERR_* if cfg is invalid. */
 int moe_select_path(const moe_cfg_t* cfg, int32_t T);
 
+/* The kernel family the expert phase of moe_ffn_forward runs for T tokens: */
+enum {
+  MOE_PLAN_DECODE_WARP = 1,     /* weight-streaming grouped matvec on warp MMAs, weights
+                                   loaded straight into registers */
+  MOE_PLAN_DECODE_RING = 2,     /* the same, MXFP4 weights streaming through a TMA-fed
+                                   shared-memory ring (items of at most 8 tokens) */
+  MOE_PLAN_PREFILL_BF16 = 3,    /* tcgen05 grouped GEMMs with bf16 operands (bf16 weights,
+                                   or MXFP4 decoded to bf16 in shared memory) */
+  MOE_PLAN_PREFILL_F16 = 4      /* tcgen05 grouped GEMMs with f16 operands: MXFP4 with the
+                                   clamped GLU, each decoded weight tile shared by two
+                                   128-row tiles */
+};
+/* Returns one of MOE_PLAN_* (a host-side decision from cfg and T alone; no device
+ * work), or a negative MOE_ERR_* if cfg is invalid or T < 0. */
+int moe_kernel_plan(const moe_cfg_t* cfg, int32_t T);
+
 /* Router: logits, top-k selection and routing weights, and the shared-expert gate.
  * Defined by: "qwen35moe CPU-reference golden vectors", Kernel 4 (softmax,
  * selection sort with first-seen tie-break, norm_topk_prob x expert_weights_scale,

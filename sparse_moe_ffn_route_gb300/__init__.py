@@ -83,6 +83,8 @@ def _load():
     lib.moe_workspace_bytes.argtypes = [C, ctypes.c_int32]
     lib.moe_workspace_bytes.restype = ctypes.c_size_t
     lib.moe_select_path.argtypes = [C, ctypes.c_int32]
+    lib.moe_kernel_plan.restype = I
+    lib.moe_kernel_plan.argtypes = [C, ctypes.c_int32]
     lib.moe_select_path.restype = I
     lib.moe_route.argtypes = [C, P, ctypes.c_int32, ctypes.POINTER(_Router),
                               ctypes.POINTER(_Shared), P, P, P, P, P, ctypes.c_size_t, P]
@@ -117,7 +119,7 @@ def _load():
 
 
 _lib = _load()
-EXPORTED = ("moe_workspace_bytes", "moe_select_path", "moe_route", "moe_topk_from_logits",
+EXPORTED = ("moe_workspace_bytes", "moe_select_path", "moe_kernel_plan", "moe_route", "moe_topk_from_logits",
             "moe_ffn_forward", "moe_ffn_forward_routed", "moe_ffn_forward_host",
             "moe_ffn_forward_noalloc",
             "moe_mxfp4_to_bf16", "moe_set_phase_events", "moe_device_status",
@@ -218,6 +220,20 @@ def moe_select_path(cfg: MoeCfg, T: int) -> int:
     st = _lib.moe_select_path(ctypes.byref(cfg), T)
     if st < 0:
         raise MoeError(st, "moe_select_path")
+    return st
+
+
+PLAN_DECODE_WARP, PLAN_DECODE_RING, PLAN_PREFILL_BF16, PLAN_PREFILL_F16 = 1, 2, 3, 4
+PLAN_NAMES = {1: "decode: warp MMAs, register-held weight loads",
+              2: "decode: warp MMAs, TMA-fed MXFP4 weight ring",
+              3: "prefill: tcgen05 grouped GEMMs, bf16 operands",
+              4: "prefill: tcgen05 grouped GEMMs, f16 operands (MXFP4, two m tiles per weight tile)"}
+
+
+def moe_kernel_plan(cfg: MoeCfg, T: int) -> int:
+    st = _lib.moe_kernel_plan(ctypes.byref(cfg), T)
+    if st < 0:
+        raise MoeError(st, "moe_kernel_plan")
     return st
 
 

@@ -188,6 +188,18 @@ int path_for(const moe_cfg_t* c, int T) {
              : MOE_PATH_PREFILL;
 }
 
+// Decode path: token chunks of 8 per work item, one while experts average at most 4
+// tokens, else four.
+int decode_chunks(const moe_cfg_t* c, int T) {
+  return 4LL * T * c->top_k <= 16LL * c->n_experts ? 1 : 4;
+}
+
+// Decode path: one-chunk MXFP4 items take the TMA-fed ring kernels (which fall back to
+// the register-stream ones only if the device lacks the shared memory they need).
+bool decode_ring(const moe_cfg_t* c) {
+  return c->wfmt == MOE_WFMT_MXFP4 && c->path != MOE_PATH_DECODE_REGISTERS;
+}
+
 // Caller-owned events recorded at phase boundaries (moe_set_phase_events).
 // With two events only the start ([0]) and the end ([6]) of the call are recorded,
 // which leaves consecutive kernels free to overlap their launches.
@@ -273,15 +285,34 @@ int run_experts(const moe_cfg_t* c, const void* x, int T, const moe_experts_t* e
     MOE_CUDA(mark_phase(6, s));
     return MOE_OK;
   }
-  // Token chunks of 8 per work item: one while experts average at most 4 tokens,
-  // else four.
-  const int chunks = 4LL * T * c->top_k <= 16LL * c->n_experts ? 1 : 4;
+  if (L.prefill) {
+    // Grouped GEMMs on tcgen05: m tiles of 128 rows; A rows of gate_up gathered first.
+    constexpr int kTileRows = 128;
+    const int max_mtiles = L.E1 + (L.S + kTileRows - 1) / kTileRows;
+    uint16_t* xp = at<uint16_t>(ws, L.xp);
+    uint8_t* scalesT = at<uint8_t>(ws, L.scalesT);
+    if (c->wfmt == MOE_WFMT_MXFP4) MOE_CUDA(launch_transpose_scales(p, scalesT, s));
+    MOE_CUDA(launch_permute(rs, L.S, L.E1, kTileRows, s));
+    MOE_CUDA(launch_gather_rows(static_cast<const uint16_t*>(x), rs.row2slot, L.S, L.K,
+                                c->d_model, xp, s));
+    MOE_CUDA(mark_phase(3, s));
+    MOE_CUDA(launch_gateup_prefill(p, c->wfmt, c->interleaved_gate_up, rs, xp, L.S, h, L.ldh,
+                                   scalesT, max_mtiles, s));
+    MOE_CUDA(mark_phase(4, s));
+    MOE_CUDA(launch_down_prefill(p, c->wfmt, rs, h, L.ldh, L.S, Y, scalesT, max_mtiles, s));
+    MOE_CUDA(mark_phase(5, s));
+    MOE_CUDA(launch_combine(Y, rs.slot_w, rs.slot_expert, T, L.K, c->d_model, L.E1, y,
+                            c->y_fp32 != 0, s));
+    MOE_CUDA(mark_phase(6, s));
+    return MOE_OK;
+  }
+  const int chunks = decode_chunks(c, T);
   const int tpg = 8 * chunks;
   const int max_items = L.E1 + (L.S + tpg - 1) / tpg;
   MOE_CUDA(launch_permute(rs, L.S, L.E1, tpg, s));
   MOE_CUDA(mark_phase(3, s));
   // MXFP4 one-chunk items: the TMA-fed shared-memory weight stream when it applies.
-  const bool ring = c->wfmt == MOE_WFMT_MXFP4 && chunks == 1 && c->path != MOE_PATH_DECODE_REGISTERS;
+  const bool ring = chunks == 1 && decode_ring(c);
   bool done = false;
   if (ring)
     MOE_CUDA(launch_gateup_decode_fp4(p, rs, static_cast<const uint16_t*>(x), L.K, h, L.ldh, max_items,
@@ -317,6 +348,17 @@ int moe_select_path(const moe_cfg_t* cfg, int32_t T) {
   if (st != MOE_OK) return st;
   if (T < 0) return MOE_ERR_INVALID_ARG;
   return path_for(cfg, T);
+}
+
+int moe_kernel_plan(const moe_cfg_t* cfg, int32_t T) {
+  const int st = validate_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (!make_layout(cfg, T, &L)) return MOE_ERR_UNSUPPORTED;
+  if (L.prefill_fp4) return MOE_PLAN_PREFILL_F16;
+  if (L.prefill) return MOE_PLAN_PREFILL_BF16;
+  return decode_chunks(cfg, T) == 1 && decode_ring(cfg) ? MOE_PLAN_DECODE_RING : MOE_PLAN_DECODE_WARP;
 }
 
 int moe_route(const moe_cfg_t* cfg, const void* x, int32_t T, const moe_router_t* router,

@@ -43,6 +43,41 @@ def test_workspace_and_path_queries():
     assert moe.moe_select_path(g.replace(path=moe.PATH_DECODE), 8192) == moe.PATH_DECODE
 
 
+def test_kernel_plan_per_workload():
+    """The kernel family each workload runs (a silent fallback to another family keeps
+    results correct, so only this check would notice it)."""
+    import moe_inputs as mi
+    want = {
+        "qwen35_mini_moe_decode_t8": moe.PLAN_DECODE_WARP,
+        "qwen35_mini_moe_decode_t64": moe.PLAN_DECODE_WARP,
+        "qwen35_mini_moe_prefill_t4096": moe.PLAN_PREFILL_BF16,
+        "gptoss_20b_moe_decode_t32": moe.PLAN_DECODE_RING,
+        "gptoss_20b_moe_prefill_t8192": moe.PLAN_PREFILL_F16,
+    }
+    assert set(want) == set(mi.WORKLOADS)
+    for name, plan in want.items():
+        spec = mi.WORKLOADS[name]
+        if spec.family == "qwen":
+            c = moe.qwen_cfg(spec.d_model, spec.n_experts, spec.top_k, spec.expert_ff, spec.shared_ff)
+        else:
+            c = moe.gptoss_cfg(spec.d_model, spec.n_experts, spec.top_k, spec.expert_ff)
+        assert moe.moe_kernel_plan(c, spec.tokens) == plan, name
+
+
+def test_kernel_plan_forms():
+    g = moe.gptoss_cfg()
+    # forced paths
+    assert moe.moe_kernel_plan(g.replace(path=moe.PATH_PREFILL), 32) == moe.PLAN_PREFILL_F16
+    assert moe.moe_kernel_plan(g.replace(path=moe.PATH_DECODE_REGISTERS), 32) == moe.PLAN_DECODE_WARP
+    assert moe.moe_kernel_plan(g.replace(path=moe.PATH_DECODE), 8192) == moe.PLAN_DECODE_WARP  # 4-chunk items
+    # a clamp limit too wide for an f16 h keeps the bf16-dequant GEMMs
+    assert moe.moe_kernel_plan(g.replace(glu_limit=300.0), 8192) == moe.PLAN_PREFILL_BF16
+    # shapes the tcgen05 tiles do not take fall back to the decode kernels
+    q = moe.qwen_cfg(d_model=96, n_experts=8, top_k=2, expert_ff=32, shared_ff=0)
+    assert moe.moe_kernel_plan(q, 4096) == moe.PLAN_DECODE_WARP
+    assert moe._lib.moe_kernel_plan(ctypes.byref(moe.qwen_cfg()), -1) == -1
+
+
 BAD_CFGS = [
     dict(top_k=0), dict(top_k=300), dict(n_experts=0), dict(n_experts=2000), dict(d_model=-1),
     dict(gating=2), dict(act=5), dict(wfmt=3), dict(path=7), dict(expert_weights_scale=float("nan")),
