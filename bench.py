@@ -156,14 +156,15 @@ def expert_bytes(spec):
     return gu, dn, 2 * sff * d * 2, d * sff * 2
 
 
-def launches_per_step(plan, mxfp4):
+def launches_per_step(plan, mxfp4, spec_slots):
     """Kernels of this library one moe_ffn_forward enqueues, by kernel plan."""
     router = 2                                            # logits, select
-    if plan in (1, 2):                                    # decode: permute, gate_up, down, combine
-        return router + 4
-    if plan == 3:                                         # (+ 2 scale transposes) permute, gather, 2 GEMMs, combine
-        return router + 5 + (2 if mxfp4 else 0)
-    return router + 8    # 2 scale preps, permute, gather, gate_up, h fix-up, down, combine
+    permute = 3 if spec_slots > 2048 else 1               # count, scan, scatter (or one CTA)
+    if plan in (1, 2):                                    # decode: gate_up, down, combine
+        return router + permute + 3
+    if plan == 3:                                         # (2 scale transposes) gather, 2 GEMMs, combine
+        return router + permute + 4 + (2 if mxfp4 else 0)
+    return router + permute + 7   # 2 scale preps, gather, gate_up, h fix-up, down, combine
 
 
 def work(spec, ids):
@@ -406,7 +407,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": launches_per_step(plan, spec.mxfp4) * args.steps,
+        "gpu_launches": launches_per_step(plan, spec.mxfp4, T * (spec.top_k + (spec.shared_ff > 0))) * args.steps,
         "clocks": sampler.summary(t0, t1),
         "phases_ms": phase_ms,
         "step_hbm_gbs": step_bytes / (ms / 1e3) / 1e9,

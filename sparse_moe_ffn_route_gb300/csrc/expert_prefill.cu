@@ -62,7 +62,7 @@ struct Lay {
 };
 constexpr int kMaxStages = 4;
 
-enum : int { kModeGateUpSplit = 0, kModeGateUpInterleaved = 1, kModeDown = 2 };
+enum : int { kModeGateUpSplit = 0, kModeGateUpInterleaved = 1, kModeDown = 2, kModeDense = 3 };
 
 struct GemmArgs {
   RouteState rs;          // offsets, work = m tiles (expert, first row), n_work, row2slot
@@ -84,6 +84,11 @@ struct GemmArgs {
   float* Y;               // down output [S, d] (slot order)
   int scale_rows;         // MXFP4: rows of one expert in the transposed scales
   int scale_nblk;         // MXFP4: 32-input blocks per weight row
+  // kModeDense (router logits): A = x [rows, d], B = W_r [E, d]; no routing state
+  int dense_rows;         // T
+  float* logits;          // [T, ldl] fp32
+  int ldl;
+  const uint16_t* rbias;  // bf16 [E] or null
 };
 
 struct Tile {
@@ -99,6 +104,15 @@ __device__ __forceinline__ Tile tile_at(const GemmArgs& g, int t, int n_m) {
   Tile tl;
   const int m = t / g.nt_max;
   tl.n = t - m * g.nt_max;
+  if (g.mode == kModeDense) {
+    tl.v = 0;
+    tl.row0 = m * kBM;
+    tl.cnt = min(kBM, g.dense_rows - tl.row0);
+    tl.kk = g.k_routed;
+    tl.nkc = tl.kk / kBK;
+    tl.skip = false;
+    return tl;
+  }
   const int2 w = g.rs.work[m];
   tl.v = w.x;
   tl.row0 = w.y;
@@ -217,7 +231,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = tmem_base_s;
-  const int n_m = *g.rs.n_work;
+  // dense mode is the first kernel of a call: start a clean device status (after the
+  // wait above, so that no flag of the previous call can land later)
+  if (g.mode == kModeDense && status && blockIdx.x == 0 && threadIdx.x == 0) *status = 0u;
+  const int n_m = g.mode == kModeDense ? (g.dense_rows + kBM - 1) / kBM : *g.rs.n_work;
   const int total = n_m > 0 ? n_m * g.nt_max : 0;
 
   if (warp == 0) {
@@ -229,7 +246,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const Tile tl = tile_at(g, t, n_m);
         if (tl.skip) continue;
         const bool sh = (tl.v == g.E);
-        const int a_row = g.rs.offsets[tl.v] + tl.row0;
+        const int a_row = (g.mode == kModeDense ? 0 : g.rs.offsets[tl.v]) + tl.row0;
         const int nb = (g.mode == kModeGateUpSplit) ? g.nf : g.N;
         const int b_row = (sh ? 0 : tl.v * g.b_rows_routed) + tl.n * nb;
         const CUtensorMap* m0 = sh ? &tmS0 : &tmB0;
@@ -362,9 +379,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       tc::tc_fence_after();
       const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)b * 256u;
       const bool valid = row < tl.cnt;
-      const int grow = g.rs.offsets[tl.v] + tl.row0 + row;     // grouped row index
+      const int grow = (g.mode == kModeDense ? 0 : g.rs.offsets[tl.v]) + tl.row0 + row;   // grouped row
       const bool sh = (tl.v == g.E);
-      if (g.mode == kModeDown) {
+      if (g.mode == kModeDense) {
+        // router logits of token grow, experts n*N .. n*N + N - 1 (+ bias)
+        float* lrow = valid ? g.logits + (size_t)grow * g.ldl : nullptr;
+        const int e0 = tl.n * g.N;
+        for (int c0 = 0; c0 < g.N; c0 += 32) {
+          float v[32];
+          tc::tmem_ld32(taddr + (uint32_t)c0, v);
+          if (valid) {
+            const int ncol = min(32, g.N - c0);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < ncol) lrow[e0 + c0 + i] = v[i] + (g.rbias ? bf16_to_f32(g.rbias[e0 + c0 + i]) : 0.f);
+          }
+        }
+      } else if (g.mode == kModeDown) {
         float* yrow = valid ? g.Y + (size_t)g.rs.row2slot[grow] * g.d : nullptr;
         const int o0 = tl.n * g.N;
         for (int c0 = 0; c0 < g.N; c0 += 32) {
@@ -696,6 +727,40 @@ cudaError_t launch_gateup_prefill(const ExpertParams& p, int wfmt, int interleav
     tS1 = tB1;
   }
   return launch_gemm<false, false>(tA, tB0, tB1, tS0, tS1, g, max_mtiles, s);
+}
+
+bool router_gemm_supported(int T, int d, int E) {
+  return T >= kBM && d % kBK == 0 && E % 16 == 0 && tile_n(E, Lay<false, false>::kMaxN) != 0;
+}
+
+// N of the router GEMM: the largest divisor of E (a multiple of 16, at most 256) that
+// still gives every SM a tile, else 16 (the router GEMM is small; keeping all SMs
+// busy matters more than the MMA shape).
+int router_n(int T, int E) {
+  const int m_tiles = (T + kBM - 1) / kBM, sms = sm_count();
+  int best = 16;
+  for (int n = 16; n <= Lay<false, false>::kMaxN && n <= E; n += 16)
+    if (E % n == 0 && (long long)m_tiles * (E / n) >= sms) best = n;
+  return best;
+}
+
+cudaError_t launch_router_gemm(const uint16_t* x, int T, int d, const uint16_t* w_r, const uint16_t* bias,
+                               int E, float* logits, int ldl, uint32_t* status, cudaStream_t s) {
+  GemmArgs g{};
+  g.rs.status = status;
+  g.E = 1;
+  g.mode = kModeDense;
+  g.N = router_n(T, E);
+  g.nt_routed = g.nt_max = E / g.N;
+  g.k_routed = d;
+  g.dense_rows = T;
+  g.logits = logits;
+  g.ldl = ldl;
+  g.rbias = bias;
+  CUtensorMap tA, tB;
+  if (!make_map_bf16(&tA, x, (uint64_t)T, d, (uint64_t)d * 2, kBM)) return cudaErrorInvalidValue;
+  if (!make_map_bf16(&tB, w_r, (uint64_t)E, d, (uint64_t)d * 2, g.N)) return cudaErrorInvalidValue;
+  return launch_gemm<false, false>(tA, tB, tB, tB, tB, g, (T + kBM - 1) / kBM, s);
 }
 
 cudaError_t launch_down_prefill(const ExpertParams& p, int wfmt, const RouteState& rs,

@@ -96,26 +96,35 @@ cudaError_t launch_gateup_decode_fp4(const ExpertParams& p, const RouteState& rs
 cudaError_t launch_down_decode_fp4(const ExpertParams& p, const RouteState& rs, const uint16_t* h, int ldh,
                                    float* Y, int max_items, cudaStream_t s, bool* launched);
 
-// logits[t, e] (row stride ldl) = x_t . W_r[e] (+ bias[e]) for e < E, and
-// x_t . wsh for e == E when wsh != null.
+// logits[t, e] (row stride ldl) = x_t . W_r[e] (+ bias[e]) for e < E, and, when
+// *gate_in_logits comes back true, x_t . wsh for e == E (else the select kernel
+// computes that dot itself).  The first kernel of a call: it clears *status.
 cudaError_t launch_router_logits(const uint16_t* x, int T, int d, const uint16_t* w_r,
                                  const uint16_t* bias, const uint16_t* wsh, int E, float* logits,
-                                 int ldl, cudaStream_t s);
+                                 int ldl, uint32_t* status, bool* gate_in_logits, cudaStream_t s);
+// Router logits of many tokens as a dense tcgen05 GEMM (expert_prefill.cu).
+bool router_gemm_supported(int T, int d, int E);
+cudaError_t launch_router_gemm(const uint16_t* x, int T, int d, const uint16_t* w_r, const uint16_t* bias,
+                               int E, float* logits, int ldl, uint32_t* status, cudaStream_t s);
 
-// Top-k + routing weights from logits [T, ldl] (first E columns; column E is the
-// shared-gate logit when has_shared).  Writes any non-null output.
+// Top-k + routing weights from logits [T, ldl] (first E columns).  With has_shared,
+// the shared-gate logit is column E, or, when wsh is non-null, x_t . wsh computed
+// here (x bf16 [T, d]).  Writes any non-null output.
 cudaError_t launch_router_select(const float* logits, int ldl, int T, int E, int k,
                                  int norm_topk_prob, float scale, int has_shared,
                                  int32_t* ids_out, float* w_out, float* sgate_out,
-                                 int32_t* slot_expert, float* slot_w, cudaStream_t s);
+                                 int32_t* slot_expert, float* slot_w, const uint16_t* x, int d,
+                                 const uint16_t* wsh, cudaStream_t s);
 
 // Copy caller routing into the slot arrays (routed entry point).
 cudaError_t launch_ingest_routing(const int32_t* ids, const float* w, const float* sgate, int T,
                                   int E, int k, int has_shared, int32_t* slot_expert,
-                                  float* slot_w, cudaStream_t s);
+                                  float* slot_w, uint32_t* status, cudaStream_t s);
 
-// Histogram, offsets, work list (items of up to tpg rows) and row -> slot map (one CTA).
-cudaError_t launch_permute(const RouteState& rs, int S, int E1, int tpg, cudaStream_t s);
+// Histogram, offsets, work list (items of up to tpg rows) and row -> slot map; hist is
+// scratch of permute_scratch_bytes(S, E1).
+size_t permute_scratch_bytes(int S, int E1);
+cudaError_t launch_permute(const RouteState& rs, int S, int E1, int tpg, int* hist, cudaStream_t s);
 
 // Decode path: weight-streaming grouped matvec on mma.sync.  One CTA row per work
 // item; chunks = token chunks of 8 per item (1 or 4, so tpg = 8 * chunks);

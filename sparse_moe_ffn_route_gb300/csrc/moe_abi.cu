@@ -19,7 +19,7 @@ struct Layout {
   int K, E1, S, ldl, ldh;
   bool prefill;             // the expert phase runs the tcgen05 grouped GEMMs
   bool prefill_fp4;         // ... in their f16-operand MXFP4 form (expert_prefill_fp4.cu)
-  size_t status, counts, offsets, work, n_work, slot_expert, slot_w, row2slot, logits, h, Y,
+  size_t status, counts, offsets, work, n_work, slot_expert, slot_w, row2slot, hist, logits, h, Y,
       xp, scalesT, xstage, ystage, total;
 };
 
@@ -69,6 +69,7 @@ bool make_layout(const moe_cfg_t* c, int T, Layout* L) {
   L->slot_expert = take(4 * Sz);
   L->slot_w = take(4 * Sz);
   L->row2slot = take(4 * Sz);
+  L->hist = take(permute_scratch_bytes(L->S, L->E1));
   L->logits = take(4 * Tz * (size_t)L->ldl);
   L->h = take(4 * Sz * (size_t)L->ldh);   // (hi, lo) bf16 halves
   L->Y = take(4 * Sz * (d > (size_t)L->ldh ? d : (size_t)L->ldh));   // also h's fp32 side copies
@@ -234,17 +235,19 @@ int run_router(const moe_cfg_t* c, const void* x, int T, const moe_router_t* r,
     ldl = c->n_experts;
   }
   if (fill_slots) MOE_CUDA(mark_phase(0, s));
+  bool gate_in_logits = false;
   MOE_CUDA(launch_router_logits(static_cast<const uint16_t*>(x), T, c->d_model,
                                 static_cast<const uint16_t*>(r->w),
                                 static_cast<const uint16_t*>(r->bias), wsh, c->n_experts, lg, ldl,
-                                s));
+                                at<uint32_t>(ws, L.status), &gate_in_logits, s));
   if (fill_slots) MOE_CUDA(mark_phase(1, s));
   const int norm = c->gating == MOE_GATING_TOPK_SOFTMAX ? 1 : c->norm_topk_prob;
   int32_t* slot_e = fill_slots ? at<int32_t>(ws, L.slot_expert) : nullptr;
   float* slot_w = fill_slots ? at<float>(ws, L.slot_w) : nullptr;
   MOE_CUDA(launch_router_select(lg, ldl, T, c->n_experts, c->top_k, norm,
                                 c->expert_weights_scale, has_sh, ids_out, w_out, sgate_out, slot_e,
-                                slot_w, s));
+                                slot_w, static_cast<const uint16_t*>(x), c->d_model,
+                                gate_in_logits ? nullptr : wsh, s));
   if (fill_slots) MOE_CUDA(mark_phase(2, s));
   if (logits_out && has_sh)
     MOE_CUDA(cudaMemcpy2DAsync(logits_out, sizeof(float) * c->n_experts, lg, sizeof(float) * ldl,
@@ -271,7 +274,7 @@ int run_experts(const moe_cfg_t* c, const void* x, int T, const moe_experts_t* e
     float* hside = Y;                                 // fp32 copies of small h chunks (Y is free until down)
     const int kh = h_stage_exp(c->glu_limit, c->glu_alpha);
     MOE_CUDA(launch_prefill_fp4_prep(p, scratch, L.S, s));
-    MOE_CUDA(launch_permute(rs, L.S, L.E1, kItemRows, s));
+    MOE_CUDA(launch_permute(rs, L.S, L.E1, kItemRows, at<int>(ws, L.hist), s));
     MOE_CUDA(launch_gather_rows_f16(static_cast<const uint16_t*>(x), rs.row2slot, L.S, L.K, c->d_model, xp16,
                                     rows.rowmul, rows.hmax, s));
     MOE_CUDA(mark_phase(3, s));
@@ -292,7 +295,7 @@ int run_experts(const moe_cfg_t* c, const void* x, int T, const moe_experts_t* e
     uint16_t* xp = at<uint16_t>(ws, L.xp);
     uint8_t* scalesT = at<uint8_t>(ws, L.scalesT);
     if (c->wfmt == MOE_WFMT_MXFP4) MOE_CUDA(launch_transpose_scales(p, scalesT, s));
-    MOE_CUDA(launch_permute(rs, L.S, L.E1, kTileRows, s));
+    MOE_CUDA(launch_permute(rs, L.S, L.E1, kTileRows, at<int>(ws, L.hist), s));
     MOE_CUDA(launch_gather_rows(static_cast<const uint16_t*>(x), rs.row2slot, L.S, L.K,
                                 c->d_model, xp, s));
     MOE_CUDA(mark_phase(3, s));
@@ -309,7 +312,7 @@ int run_experts(const moe_cfg_t* c, const void* x, int T, const moe_experts_t* e
   const int chunks = decode_chunks(c, T);
   const int tpg = 8 * chunks;
   const int max_items = L.E1 + (L.S + tpg - 1) / tpg;
-  MOE_CUDA(launch_permute(rs, L.S, L.E1, tpg, s));
+  MOE_CUDA(launch_permute(rs, L.S, L.E1, tpg, at<int>(ws, L.hist), s));
   MOE_CUDA(mark_phase(3, s));
   // MXFP4 one-chunk items: the TMA-fed shared-memory weight stream when it applies.
   const bool ring = chunks == 1 && decode_ring(c);
@@ -395,7 +398,7 @@ int moe_topk_from_logits(const moe_cfg_t* cfg, const float* logits, int32_t T, i
   const int norm = cfg->gating == MOE_GATING_TOPK_SOFTMAX ? 1 : cfg->norm_topk_prob;
   if (launch_router_select(logits, cfg->n_experts, T, cfg->n_experts, cfg->top_k, norm,
                            cfg->expert_weights_scale, 0, topk_ids, topk_w, nullptr, nullptr,
-                           nullptr, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+                           nullptr, nullptr, 0, nullptr, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -442,7 +445,7 @@ int moe_ffn_forward_routed(const moe_cfg_t* cfg, const void* x, int32_t T,
   MOE_CUDA(mark_phase(0, s));
   MOE_CUDA(launch_ingest_routing(topk_ids, topk_w, sgate, T, cfg->n_experts, cfg->top_k,
                                  cfg->shared_ff > 0, at<int32_t>(ws, L.slot_expert),
-                                 at<float>(ws, L.slot_w), s));
+                                 at<float>(ws, L.slot_w), at<uint32_t>(ws, L.status), s));
   MOE_CUDA(mark_phase(1, s));
   MOE_CUDA(mark_phase(2, s));
   return run_experts(cfg, x, T, experts, shared, y, L, ws, s);

@@ -26,11 +26,13 @@ template <int MT, int NT, int WARPS, int STEPS>
 __global__ void __launch_bounds__(WARPS * 32)
 router_logits_kernel(const uint16_t* __restrict__ x, int T, int d, const uint16_t* __restrict__ w_r,
                      const uint16_t* __restrict__ bias, const uint16_t* __restrict__ wsh, int E,
-                     float* __restrict__ logits, int ldl) {
+                     float* __restrict__ logits, int ldl, uint32_t* __restrict__ status) {
   constexpr int TM = 16 * MT, TN = 8 * NT;
   __shared__ float part[WARPS][TM][TN + 1];
   pdl_wait();
   pdl_trigger();
+  // the first kernel of a call: start a clean device status
+  if (status && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *status = 0u;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, c = lane & 3;
   const int t0 = blockIdx.x * TM;
@@ -120,7 +122,8 @@ __global__ void __launch_bounds__(kSelectWarps * 32)
 router_select_kernel(const float* __restrict__ logits, int ldl, int T, int E, int k,
                      int norm_topk_prob, float scale, int has_shared, int32_t* __restrict__ ids_out,
                      float* __restrict__ w_out, float* __restrict__ sgate_out,
-                     int32_t* __restrict__ slot_expert, float* __restrict__ slot_w) {
+                     int32_t* __restrict__ slot_expert, float* __restrict__ slot_w,
+                     const uint16_t* __restrict__ x, int d, const uint16_t* __restrict__ wsh) {
   pdl_wait();
   pdl_trigger();
   const int lane = threadIdx.x & 31;
@@ -190,8 +193,24 @@ router_select_kernel(const float* __restrict__ logits, int ldl, int T, int E, in
       slot_w[(size_t)t * K + lane] = w;
     }
   }
+  float sl = 0.f;   // the shared-gate logit: column E of the logits, or w_sh . x here
+  if (has_shared && wsh) {
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+    const uint4* wr = reinterpret_cast<const uint4*>(wsh);
+    for (int i = lane; i < d / 8; i += 32) {
+      const uint4 a = ldg_nc_v4(xr + i), b = ldg_nc_v4(wr + i);
+      sl = fmaf(bf16_lo(a.x), bf16_lo(b.x), sl); sl = fmaf(bf16_hi(a.x), bf16_hi(b.x), sl);
+      sl = fmaf(bf16_lo(a.y), bf16_lo(b.y), sl); sl = fmaf(bf16_hi(a.y), bf16_hi(b.y), sl);
+      sl = fmaf(bf16_lo(a.z), bf16_lo(b.z), sl); sl = fmaf(bf16_hi(a.z), bf16_hi(b.z), sl);
+      sl = fmaf(bf16_lo(a.w), bf16_lo(b.w), sl); sl = fmaf(bf16_hi(a.w), bf16_hi(b.w), sl);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sl += __shfl_xor_sync(0xffffffffu, sl, off);
+  } else if (has_shared) {
+    sl = row[E];
+  }
   if (has_shared && lane == 0) {
-    const float sg = 1.f / (1.f + expf(-row[E]));
+    const float sg = 1.f / (1.f + expf(-sl));
     if (sgate_out) sgate_out[t] = sg;
     if (slot_expert) {
       slot_expert[(size_t)t * K + k] = E;
@@ -203,9 +222,11 @@ router_select_kernel(const float* __restrict__ logits, int ldl, int T, int E, in
 __global__ void ingest_routing_kernel(const int32_t* __restrict__ ids, const float* __restrict__ w,
                                       const float* __restrict__ sgate, int T, int E, int k,
                                       int has_shared, int32_t* __restrict__ slot_expert,
-                                      float* __restrict__ slot_w) {
+                                      float* __restrict__ slot_w, uint32_t* __restrict__ status) {
   pdl_wait();
   pdl_trigger();
+  // the first kernel of a call: start a clean device status
+  if (status && blockIdx.x == 0 && threadIdx.x == 0) *status = 0u;
   const int K = k + has_shared;
   const long n = (long)T * K;
   for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
@@ -228,30 +249,37 @@ __global__ void ingest_routing_kernel(const int32_t* __restrict__ ids, const flo
 
 cudaError_t launch_router_logits(const uint16_t* x, int T, int d, const uint16_t* w_r,
                                  const uint16_t* bias, const uint16_t* wsh, int E, float* logits,
-                                 int ldl, cudaStream_t s) {
+                                 int ldl, uint32_t* status, bool* gate_in_logits, cudaStream_t s) {
+  *gate_in_logits = wsh != nullptr;
   const int E1 = E + (wsh ? 1 : 0);
+  if (T > 256 && router_gemm_supported(T, d, E)) {
+    // a dense GEMM on tcgen05 over the routed experts; the shared-gate dot is left to
+    // the select kernel
+    *gate_in_logits = false;
+    return launch_router_gemm(x, T, d, w_r, bias, E, logits, ldl, status, s);
+  }
   if (T <= 256) {   // latency-bound: many small CTAs, all loads of a warp in flight at once
     dim3 grid((T + 15) / 16, (E1 + 15) / 16);
     return launch_pdl(router_logits_kernel<1, 2, 16, 6>, grid, dim3(16 * 32), 0, s, x, T, d, w_r,
-                      bias, wsh, E, logits, ldl);
+                      bias, wsh, E, logits, ldl, status);
   } else {          // throughput-bound: larger tiles, fewer re-reads of x and W_r from L2
     dim3 grid((T + 63) / 64, (E1 + 31) / 32);
     return launch_pdl(router_logits_kernel<4, 4, 4, 2>, grid, dim3(4 * 32), 0, s, x, T, d, w_r, bias,
-                      wsh, E, logits, ldl);
+                      wsh, E, logits, ldl, status);
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_router_select(const float* logits, int ldl, int T, int E, int k,
                                  int norm_topk_prob, float scale, int has_shared,
                                  int32_t* ids_out, float* w_out, float* sgate_out,
-                                 int32_t* slot_expert, float* slot_w, cudaStream_t s) {
+                                 int32_t* slot_expert, float* slot_w, const uint16_t* x, int d,
+                                 const uint16_t* wsh, cudaStream_t s) {
   dim3 grid((T + kSelectWarps - 1) / kSelectWarps);
   const int epl = (E + 31) / 32;
 #define MOE_SELECT(N)                                                                     \
   return launch_pdl(router_select_kernel<N>, grid, dim3(kSelectWarps * 32), 0, s, logits, ldl, T, \
                     E, k, norm_topk_prob, scale, has_shared, ids_out, w_out, sgate_out,       \
-                    slot_expert, slot_w)
+                    slot_expert, slot_w, x, d, wsh)
   if (epl <= 1) MOE_SELECT(1);
   else if (epl <= 2) MOE_SELECT(2);
   else if (epl <= 4) MOE_SELECT(4);
@@ -264,11 +292,11 @@ cudaError_t launch_router_select(const float* logits, int ldl, int T, int E, int
 
 cudaError_t launch_ingest_routing(const int32_t* ids, const float* w, const float* sgate, int T,
                                   int E, int k, int has_shared, int32_t* slot_expert,
-                                  float* slot_w, cudaStream_t s) {
+                                  float* slot_w, uint32_t* status, cudaStream_t s) {
   const long n = (long)T * (k + has_shared);
   const int blocks = (int)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
   return launch_pdl(ingest_routing_kernel, dim3(blocks), dim3(256), 0, s, ids, w, sgate, T, E, k,
-                    has_shared, slot_expert, slot_w);
+                    has_shared, slot_expert, slot_w, status);
 }
 
 }  // namespace moe
