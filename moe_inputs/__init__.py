@@ -35,6 +35,7 @@ LAYER_STREAM = 1_000_000   # stream offset for layer-level tensors (router, x, s
 # tensor slots inside the layer-level stream
 SLOT_ROUTER_W, SLOT_SHARED_GATE_INP, SLOT_ROUTER_BIAS, SLOT_X = 0, 1, 2, 3
 SLOT_SH_GATE, SLOT_SH_UP, SLOT_SH_DOWN = 4, 5, 6
+SLOT_NORM_W = 7
 # tensor slots inside an expert's stream (bf16 experts)
 SLOT_E_GATE, SLOT_E_UP, SLOT_E_DOWN = 0, 1, 2
 # tensor slots inside an expert's stream (MXFP4 experts)
@@ -205,6 +206,8 @@ class Layer:
     sh_up: Optional[np.ndarray] = None       # [sff, d]
     sh_down: Optional[np.ndarray] = None     # [d, sff]
     sh_gate_inp: Optional[np.ndarray] = None  # [d]
+    # RMSNorm weight before the MoE (layers run with the norm / residual steps)
+    norm_w: Optional[np.ndarray] = None      # [d] bf16
 
     @property
     def T(self) -> int:
@@ -282,6 +285,13 @@ def make_layer(spec: LayerSpec, T: Optional[int] = None, experts: Optional[list]
         lay.sh_up = normal_bf16(key, SLOT_SH_UP, (sff, d), 1.0 / math.sqrt(d))
         lay.sh_down = normal_bf16(key, SLOT_SH_DOWN, (d, sff), 1.0 / math.sqrt(sff))
     return lay
+
+
+def make_norm_w(spec: LayerSpec) -> np.ndarray:
+    """RMSNorm weight bf16 [d] ~ 1 + N(0, 0.1): a norm weight near 1, as the pages
+    describe the model's (QK-norm weights of about 1 +- 0.1)."""
+    z = normal_f64(spec.seed + LAYER_STREAM, SLOT_NORM_W, spec.d_model)
+    return f64_to_bf16(1.0 + 0.1 * z)
 
 
 def small_spec(family: str, d: int, E: int, k: int, ff: int, sff: int, T: int,

@@ -13,6 +13,11 @@ Functions and the passages they follow (page title, section):
   * ``route_from_logits`` / ``forward``: Kernel 4 above for the softmax/renorm
     gating, "qwen35moe - Forward-Pass Design", section "Shared-expert MoE FFN", and
     "Phase 19", section 2 (Router, Experts) for the gpt-oss gating and experts.
+  * ``Gating.rms_norm`` / ``Gating.residual`` (the steps either side of the MoE):
+    "qwen35moe - Forward-Pass Design", "Block scaffold" (post_attention_norm, the
+    residual adds the un-normalised input); "qwen35moe CPU-reference golden vectors",
+    Kernel 3 (RMS = 1 / sqrt(mean(x^2) + eps), times the weight); "Phase 19",
+    section 2 (RMSNorm, Decoder layer: out = h + moe(post_norm(h))).
 """
 from __future__ import annotations
 
@@ -39,14 +44,15 @@ class OracleCfg(ctypes.Structure):
                 ("act", ctypes.c_int32), ("wfmt", ctypes.c_int32),
                 ("norm_topk_prob", ctypes.c_int32), ("interleaved", ctypes.c_int32),
                 ("scale", ctypes.c_double), ("limit", ctypes.c_double),
-                ("alpha", ctypes.c_double)]
+                ("alpha", ctypes.c_double), ("rms_norm", ctypes.c_int32),
+                ("residual", ctypes.c_int32), ("rms_eps", ctypes.c_double)]
 
 
 class OracleWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "router_w", "router_b", "gate", "up", "gate_up", "down", "gu_blocks", "gu_scales",
         "dn_blocks", "dn_scales", "gu_bias", "dn_bias", "sh_gate", "sh_up", "sh_down",
-        "sh_gate_inp")]
+        "sh_gate_inp", "norm_w")]
 
 
 def build(force: bool = False) -> str:
@@ -149,6 +155,9 @@ class Gating:
     scale: float = 1.0
     limit: float = 7.0
     alpha: float = 1.702
+    rms_norm: int = 0        # 1: the MoE runs on RMSNorm(x) (needs layer.norm_w)
+    residual: int = 0        # 1: y = x + MoE(...)
+    rms_eps: float = 1e-6
 
     def c(self) -> OracleCfg:
         return OracleCfg(**dataclasses.asdict(self))
@@ -205,7 +214,7 @@ def weights_of(layer) -> tuple:
                       dn_blocks=p(layer.dn_blocks), dn_scales=p(layer.dn_scales),
                       gu_bias=p(layer.gu_bias), dn_bias=p(layer.dn_bias), sh_gate=p(layer.sh_gate),
                       sh_up=p(layer.sh_up), sh_down=p(layer.sh_down),
-                      sh_gate_inp=p(layer.sh_gate_inp))
+                      sh_gate_inp=p(layer.sh_gate_inp), norm_w=p(getattr(layer, "norm_w", None)))
     return W, keep
 
 

@@ -17,6 +17,13 @@
  *   [OSS] "Phase 19: MoE - gpt-oss-20b", section 2 "Router (GptOssTopKRouter)"
  *         and "Experts (GptOssExperts)", the measured tensor-layout listing, and
  *         section 3 "MXFP4 dequantisation".
+ *   Optional steps either side of the MoE (cfg rms_norm, residual):
+ *   [QW]  "Block scaffold": x -> post_attention_norm -> shared-MoE FFN -> + the
+ *         un-normalised input; all norms RMS.
+ *   [GV]  "Kernel 3 - QK-RMSNorm": RMS uses 1 / sqrt(mean(x^2) + eps), times the
+ *         norm weight.
+ *   [OSS] section 2, "RMSNorm" (standard) and "Decoder layer":
+ *         out = h + moe(post_norm(h)).
  *
  * Readings taken where the pages leave a step open:
  *   - SwiGLU(x) = down(silu(gate x) * (up x)), silu(z) = z / (1 + e^-z).
@@ -45,6 +52,9 @@ typedef struct {
   int32_t interleaved;     /* 1: one gate_up matrix, gate = even rows, up = odd rows [OSS] */
   double scale;            /* expert_weights_scale [GV] */
   double limit, alpha;     /* 7.0, 1.702 [OSS] */
+  int32_t rms_norm;        /* 1: the MoE runs on RMSNorm(x) [QW Block scaffold; OSS Decoder layer] */
+  int32_t residual;        /* 1: y = x + MoE(...) (x un-normalised) [QW; OSS] */
+  double rms_eps;          /* 1e-6 [QW config], 1e-5 [OSS] */
 } oracle_cfg;
 
 typedef struct {
@@ -59,6 +69,7 @@ typedef struct {
   const uint16_t *dn_bias;    /* bf16 [E, d] or NULL */
   /* shared expert (NULL when shared_ff == 0): gate/up [sff, d], down [d, sff], gate_inp [d] */
   const uint16_t *sh_gate, *sh_up, *sh_down, *sh_gate_inp;
+  const uint16_t *norm_w;     /* bf16 [d]: RMSNorm weight (cfg rms_norm), else NULL */
 } oracle_weights;
 
 /* ------------------------------------------------------------------ number formats */
@@ -210,6 +221,20 @@ static double activation(const oracle_cfg* c, double gate, double up) {
 
 /* ------------------------------------------------------------------ layer forward */
 
+/* The MoE's input from the layer input x (d values): RMSNorm(x) when cfg rms_norm,
+   x / sqrt(mean(x^2) + eps) * w [GV Kernel 3; OSS RMSNorm], else x itself. */
+static void moe_input(const oracle_cfg* c, const oracle_weights* W, const double* x, double* out) {
+  int d = c->d_model;
+  if (!c->rms_norm) {
+    for (int i = 0; i < d; ++i) out[i] = x[i];
+    return;
+  }
+  double ss = 0.0;
+  for (int i = 0; i < d; ++i) ss += x[i] * x[i];
+  double inv = 1.0 / sqrt(ss / d + c->rms_eps);
+  for (int i = 0; i < d; ++i) out[i] = x[i] * inv * oracle_bf16(W->norm_w[i]);
+}
+
 /* Router of one token: logits x . W_r^T (+ b) [QW ffn_gate_inp; OSS Router], then
    the routing.  Returns 1 if a logit is NaN. */
 static int router_one(const oracle_cfg* c, const oracle_weights* W, const double* xv, double* ll,
@@ -242,11 +267,14 @@ int oracle_route(const oracle_cfg* c, const oracle_weights* W, const uint16_t* x
   (void)T;
 #pragma omp parallel for schedule(dynamic, 16) reduction(+ : n_nan)
   for (int n = 0; n < n_eval; ++n) {
+    double* xin = (double*)malloc(sizeof(double) * (size_t)d);
     double* xv = (double*)malloc(sizeof(double) * (size_t)d);
-    for (int i = 0; i < d; ++i) xv[i] = oracle_bf16(x[(size_t)tokens[n] * d + i]);
+    for (int i = 0; i < d; ++i) xin[i] = oracle_bf16(x[(size_t)tokens[n] * d + i]);
+    moe_input(c, W, xin, xv);
     n_nan += router_one(c, W, xv, logits + (size_t)n * E, NULL, ids + (size_t)n * k,
                         w + (size_t)n * k);
     sgate[n] = c->shared_ff > 0 ? shared_gate(c, W, xv) : 0.0;
+    free(xin);
     free(xv);
   }
   return n_nan;
@@ -272,11 +300,13 @@ int oracle_forward(const oracle_cfg* c, const oracle_weights* W, const uint16_t*
   for (int n = 0; n < n_eval; ++n) {
     int t = tokens[n];
     int hmax = ff > sff ? ff : sff;
+    double* xin = (double*)malloc(sizeof(double) * (size_t)d);
     double* xv = (double*)malloc(sizeof(double) * (size_t)d);
     double* h = (double*)malloc(sizeof(double) * (size_t)hmax);
     double* yl = y + (size_t)n * d;
     double* ll = logits + (size_t)n * E;
-    for (int i = 0; i < d; ++i) xv[i] = oracle_bf16(x[(size_t)t * d + i]);
+    for (int i = 0; i < d; ++i) xin[i] = oracle_bf16(x[(size_t)t * d + i]);
+    moe_input(c, W, xin, xv);   /* the MoE runs on RMSNorm(x) or on x */
 
     n_nan += router_one(c, W, xv, ll, forced_ids ? forced_ids + (size_t)n * k : NULL,
                         ids + (size_t)n * k, w + (size_t)n * k);
@@ -310,6 +340,10 @@ int oracle_forward(const oracle_cfg* c, const oracle_weights* W, const uint16_t*
       }
     }
     sgate[n] = sg;
+    /* + the un-normalised layer input [QW Block scaffold; OSS Decoder layer] */
+    if (c->residual)
+      for (int o = 0; o < d; ++o) yl[o] += xin[o];
+    free(xin);
     free(xv);
     free(h);
   }

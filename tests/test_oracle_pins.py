@@ -347,3 +347,93 @@ def test_route_only_matches_forward():
         r = oracle.route(g, lay, tokens=np.arange(7)[::-1].copy())
         assert np.array_equal(r.ids, f.ids[::-1]) and np.array_equal(r.w, f.w[::-1])
         assert np.array_equal(r.sgate, f.sgate[::-1]) and np.array_equal(r.logits, f.logits[::-1])
+
+
+# ----------------------------------------------------------------------------- RMSNorm and residual
+def _with_norm(spec, lay):
+    lay.norm_w = mi.make_norm_w(spec)
+    return lay
+
+
+def test_rmsnorm_one_hot_closed_form():
+    """x = c e_i: mean(x^2) = c^2 / d, so with eps = 0 the MoE input is sqrt(d) sign(c) w_i e_i
+    and the logits are sqrt(d) sign(c) w_i W_r[:, i] + b."""
+    spec, lay = small_qwen(bias=("normal", 0.5))
+    _with_norm(spec, lay)
+    g = oracle.gating_for(spec)
+    g.rms_norm, g.rms_eps = 1, 0.0
+    d = spec.d_model
+    x = np.zeros((d, d), np.uint16)
+    for i in range(d):
+        x[i, i] = BF(-1.5 if i % 2 else 2.25)[()]
+    r = oracle.forward(g, lay, x=x)
+    Wr = mi.bf16_to_f32(lay.router_w).astype(np.float64)
+    b = mi.bf16_to_f32(lay.router_b).astype(np.float64)
+    w = mi.bf16_to_f32(lay.norm_w).astype(np.float64)
+    sgn = np.where(np.arange(d) % 2, -1.0, 1.0)
+    want = math.sqrt(d) * (sgn * w)[:, None] * Wr.T + b[None, :]
+    assert np.allclose(r.logits, want, rtol=1e-13, atol=1e-13)
+
+
+def test_rmsnorm_per_token_scale_invariance():
+    """With eps = 0 the normalised input does not depend on each token's scale: tokens
+    scaled by different powers of two (exact in bf16) give the same outputs."""
+    for spec, lay in (small_qwen(), small_oss()):
+        _with_norm(spec, lay)
+        g = oracle.gating_for(spec)
+        g.rms_norm, g.rms_eps = 1, 0.0
+        x = mi.bf16_to_f32(lay.x).astype(np.float64)
+        f = 2.0 ** (np.arange(x.shape[0]) % 5 * 3 - 6)
+        r0 = oracle.forward(g, lay)
+        r1 = oracle.forward(g, lay, x=BF(x * f[:, None]))
+        assert np.array_equal(r0.ids, r1.ids)
+        assert np.allclose(r0.y, r1.y, rtol=1e-12, atol=1e-12 * np.abs(r0.y).max())
+
+
+def test_rmsnorm_eps_keeps_zero_rows_finite():
+    """A zero token normalises to zero (0 / sqrt(eps)), giving the zero-input closed form."""
+    spec, lay = small_qwen(E=16, k=8)
+    _with_norm(spec, lay)
+    g = oracle.gating_for(spec)
+    g.rms_norm = 1
+    r = oracle.forward(g, lay, x=np.zeros((2, spec.d_model), np.uint16))
+    assert np.array_equal(r.ids, np.tile(np.arange(8), (2, 1)))
+    assert np.all(r.y == 0.0) and np.all(r.sgate == 0.5)
+
+
+@pytest.mark.parametrize("family", ["qwen", "gptoss"])
+def test_residual_adds_the_unnormalised_input(family):
+    """y(residual) - y(no residual) = x exactly, and with every down projection zero y = x."""
+    spec, lay = small_qwen() if family == "qwen" else small_oss()
+    _with_norm(spec, lay)
+    g = oracle.gating_for(spec)
+    g.rms_norm = 1
+    x = mi.bf16_to_f32(lay.x).astype(np.float64)
+    g.residual = 0
+    y0 = oracle.forward(g, lay).y
+    g.residual = 1
+    y1 = oracle.forward(g, lay).y
+    assert np.allclose(y1 - y0, x, rtol=0, atol=1e-12 * max(1.0, np.abs(y0).max()))
+    if family == "qwen":
+        lay.down[:] = 0
+        lay.sh_down[:] = 0
+    else:
+        lay.dn_blocks[:] = 0
+        lay.dn_bias[:] = 0
+    assert np.array_equal(oracle.forward(g, lay).y, x)
+
+
+def test_rmsnorm_eps_inside_the_root():
+    """A constant row x = 0.125 with eps = 0.046875: mean(x^2) + eps = 0.0625 whose root is
+    0.25, so the MoE input is exactly 0.5 w, and the logits are 0.5 w . W_r^T + b."""
+    spec, lay = small_qwen(bias=("normal", 0.5))
+    _with_norm(spec, lay)
+    g = oracle.gating_for(spec)
+    g.rms_norm, g.rms_eps = 1, 0.046875
+    x = np.full((2, spec.d_model), BF(0.125)[()], np.uint16)
+    r = oracle.forward(g, lay, x=x)
+    Wr = mi.bf16_to_f32(lay.router_w).astype(np.float64)
+    b = mi.bf16_to_f32(lay.router_b).astype(np.float64)
+    w = mi.bf16_to_f32(lay.norm_w).astype(np.float64)
+    want = (0.5 * w) @ Wr.T + b
+    assert np.allclose(r.logits, np.tile(want, (2, 1)), rtol=1e-13, atol=1e-13)
