@@ -221,8 +221,21 @@ static double activation(const oracle_cfg* c, double gate, double up) {
 
 /* ------------------------------------------------------------------ layer forward */
 
+/* fp64 -> the nearest bf16 value (ties to even), returned as fp64: 8 significant
+   bits, 8 exponent bits (finite, normal-range values; zero, inf and NaN pass). */
+static double round_bf16(double v) {
+  if (v == 0.0 || !isfinite(v)) return v;
+  int e;
+  double m = frexp(v, &e);          /* v = m * 2^e, 0.5 <= |m| < 1 */
+  if (e < -125) e = -125;           /* below the normal range: bf16 subnormal spacing 2^-133 */
+  return ldexp(nearbyint(ldexp(v, 8 - e)), e - 8);
+}
+
 /* The MoE's input from the layer input x (d values): RMSNorm(x) when cfg rms_norm,
-   x / sqrt(mean(x^2) + eps) * w [GV Kernel 3; OSS RMSNorm], else x itself. */
+   x / sqrt(mean(x^2) + eps) * w [GV Kernel 3; OSS RMSNorm], else x itself.  The
+   normalised value is an activation in the layer's type, bf16, as x is: the
+   "standard" RMSNorm of [OSS section 2] keeps its statistics in higher precision
+   and returns the input's type; rounded to nearest, ties to even. */
 static void moe_input(const oracle_cfg* c, const oracle_weights* W, const double* x, double* out) {
   int d = c->d_model;
   if (!c->rms_norm) {
@@ -232,7 +245,7 @@ static void moe_input(const oracle_cfg* c, const oracle_weights* W, const double
   double ss = 0.0;
   for (int i = 0; i < d; ++i) ss += x[i] * x[i];
   double inv = 1.0 / sqrt(ss / d + c->rms_eps);
-  for (int i = 0; i < d; ++i) out[i] = x[i] * inv * oracle_bf16(W->norm_w[i]);
+  for (int i = 0; i < d; ++i) out[i] = round_bf16(x[i] * inv * oracle_bf16(W->norm_w[i]));
 }
 
 /* Router of one token: logits x . W_r^T (+ b) [QW ffn_gate_inp; OSS Router], then

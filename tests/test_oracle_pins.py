@@ -437,3 +437,29 @@ def test_rmsnorm_eps_inside_the_root():
     w = mi.bf16_to_f32(lay.norm_w).astype(np.float64)
     want = (0.5 * w) @ Wr.T + b
     assert np.allclose(r.logits, np.tile(want, (2, 1)), rtol=1e-13, atol=1e-13)
+
+
+def test_rmsnorm_output_is_bf16_rounded():
+    """The normalised input is a bf16 activation: x = 3 e_0 + (1 + 2^-7) e_2, w = 1,
+    eps = 0.  Router rows that pick inputs 0 and 2 expose the two normalised values,
+    which must equal the exact quotients rounded to the nearest bf16 (the input
+    generator's independent conversion)."""
+    spec, lay = small_qwen(E=8, k=1, bias=None)
+    _with_norm(spec, lay)
+    lay.norm_w[:] = BF(1.0)[()]
+    lay.router_w[:] = 0
+    lay.router_w[0, 0] = BF(1.0)[()]            # logit 0 = xn[0]
+    lay.router_w[1, 2] = BF(1.0)[()]            # logit 1 = xn[2]
+    g = oracle.gating_for(spec)
+    g.rms_norm, g.rms_eps = 1, 0.0
+    d = spec.d_model
+    x = np.zeros((1, d), np.float64)
+    x[0, 0] = 3.0
+    x[0, 2] = 1.0 + 2.0 ** -7                   # exact in bf16 (8 significant bits)
+    r = oracle.forward(g, lay, x=BF(x))
+    inv = 1.0 / math.sqrt((9.0 + (1.0 + 2.0 ** -7) ** 2) / d)
+    exact0, exact2 = 3.0 * inv, (1.0 + 2.0 ** -7) * inv
+    b0 = float(mi.bf16_to_f32(BF(exact0))[()])
+    b2 = float(mi.bf16_to_f32(BF(exact2))[()])
+    assert r.logits[0, 0] == b0 and r.logits[0, 1] == b2
+    assert b0 != exact0                          # the case does exercise the rounding
