@@ -100,13 +100,22 @@ typedef struct {
   float glu_alpha;              /* clamped GLU sigmoid slope (gpt-oss 1.702) */
   int32_t path;                 /* MOE_PATH_* */
   int32_t y_fp32;               /* 0: y is bf16 [T, d] (RNE of the fp32 result); 1: y is fp32 [T, d] */
+  /* Steps either side of the MoE ("qwen35moe - Forward-Pass Design", "Block
+   * scaffold": post_attention_norm, then the residual adds the un-normalised input;
+   * "Phase 19: MoE - gpt-oss-20b", section 2, "Decoder layer": out = h + moe(post_norm(h))). */
+  int32_t rms_norm;             /* 1: route and run the experts on RMSNorm(x) = x / sqrt(mean(x^2) +
+                                   rms_eps) * router.norm_w (fp32 statistics, rounded to bf16) */
+  float rms_eps;                /* Qwen 1e-6, gpt-oss 1e-5; finite and >= 0 */
+  int32_t residual;             /* 1: y = x + MoE(...) (x un-normalised), summed in fp32 */
   int32_t reserved[3];          /* must be zero */
 } moe_cfg_t;
 
-/* Router: w bf16 [E, d] (row e = expert e's logit weights); bias bf16 [E] or NULL. */
+/* Router: w bf16 [E, d] (row e = expert e's logit weights); bias bf16 [E] or NULL;
+ * norm_w bf16 [d], the RMSNorm weight (required when cfg.rms_norm, else ignored). */
 typedef struct {
   const void* w;
   const void* bias;
+  const void* norm_w;
 } moe_router_t;
 
 /* Routed experts (device pointers; unused members NULL).
@@ -194,6 +203,8 @@ int moe_topk_from_logits(const moe_cfg_t* cfg, const float* logits, int32_t T, i
  * topk_w [T, k] device or NULL: if given, the routing is also written there.
  * The combine accumulates in fp32; with cfg->y_fp32 = 0, y holds that fp32 result
  * rounded to bf16 (round to nearest even), with y_fp32 = 1 the fp32 result itself.
+ * With cfg->rms_norm the router and the experts see RMSNorm(x) (router->norm_w);
+ * with cfg->residual, y = x + MoE(...).  moe_route applies the same norm.
  * Defined by the two conventions in the header comment above. */
 int moe_ffn_forward(const moe_cfg_t* cfg, const void* x, int32_t T, const moe_router_t* router,
                     const moe_experts_t* experts, const moe_shared_t* shared, void* y,
@@ -203,7 +214,9 @@ int moe_ffn_forward(const moe_cfg_t* cfg, const void* x, int32_t T, const moe_ro
  * topk_w fp32 [T, k] device; sgate fp32 [T] device, required when the layer has
  * a shared expert.  Out-of-range ids are caught on the device: the call still
  * returns MOE_OK and moe_device_status() then reports MOE_ERR_DEVICE_CHECK
- * (rows with a bad id contribute nothing). */
+ * (rows with a bad id contribute nothing).  cfg->residual applies; cfg->rms_norm
+ * returns MOE_ERR_UNSUPPORTED (the norm weight belongs to the router, which this
+ * entry point does not take: pass the normalised input instead). */
 int moe_ffn_forward_routed(const moe_cfg_t* cfg, const void* x, int32_t T,
                            const int32_t* topk_ids, const float* topk_w, const float* sgate,
                            const moe_experts_t* experts, const moe_shared_t* shared, void* y,

@@ -51,7 +51,9 @@ class MoeCfg(ctypes.Structure):
                 ("interleaved_gate_up", ctypes.c_int32), ("norm_topk_prob", ctypes.c_int32),
                 ("expert_weights_scale", ctypes.c_float), ("glu_limit", ctypes.c_float),
                 ("glu_alpha", ctypes.c_float), ("path", ctypes.c_int32),
-                ("y_fp32", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+                ("y_fp32", ctypes.c_int32), ("rms_norm", ctypes.c_int32),
+                ("rms_eps", ctypes.c_float), ("residual", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 3)]
 
     def replace(self, **kw) -> "MoeCfg":
         c = MoeCfg()
@@ -62,7 +64,7 @@ class MoeCfg(ctypes.Structure):
 
 
 class _Router(ctypes.Structure):
-    _fields_ = [("w", ctypes.c_void_p), ("bias", ctypes.c_void_p)]
+    _fields_ = [("w", ctypes.c_void_p), ("bias", ctypes.c_void_p), ("norm_w", ctypes.c_void_p)]
 
 
 class _Experts(ctypes.Structure):
@@ -152,6 +154,7 @@ def gptoss_cfg(d_model=2880, n_experts=32, top_k=4, expert_ff=2880, glu_limit=7.
 class Router:
     w: torch.Tensor                       # bf16 [E, d]
     bias: Optional[torch.Tensor] = None   # bf16 [E]
+    norm_w: Optional[torch.Tensor] = None  # bf16 [d]: RMSNorm weight (cfg.rms_norm)
 
 
 @dataclasses.dataclass
@@ -185,7 +188,8 @@ def _ptr(t: Optional[torch.Tensor], name: str = "tensor") -> Optional[int]:
 
 
 def _router(r: Router) -> _Router:
-    return _Router(_ptr(r.w, "router.w"), _ptr(r.bias, "router.bias"))
+    return _Router(_ptr(r.w, "router.w"), _ptr(r.bias, "router.bias"),
+                   _ptr(r.norm_w, "router.norm_w"))
 
 
 def _experts(e: Experts) -> _Experts:

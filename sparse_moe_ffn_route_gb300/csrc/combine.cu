@@ -1,10 +1,14 @@
-// Combine: y[t] = sum_j w[t, j] * Y[t*K + j] over a token's routed slots and,
-// last, its shared-expert slot (weight = sigmoid gate), accumulated in fp32 in
-// that fixed order and rounded once to bf16.
+// Combine: y[t] = (x[t] +) sum_j w[t, j] * Y[t*K + j] over a token's routed slots
+// and, last, its shared-expert slot (weight = sigmoid gate), accumulated in fp32 in
+// that fixed order (the residual first) and rounded once to bf16.
+// RMSNorm: the MoE's input RMSNorm(x) = x / sqrt(mean(x^2) + eps) * w, in bf16.
 //
 // Sources: "qwen35moe - Forward-Pass Design", section "Shared-expert MoE FFN"
-// (out = moe_out + sgate * shexp); "Phase 19: MoE - gpt-oss-20b", section 2
-// Experts (out = sum over the top-4 of scores * y_e).
+// (out = moe_out + sgate * shexp) and "Block scaffold" (post_attention_norm; the
+// residual adds the un-normalised input); "qwen35moe CPU-reference golden vectors",
+// Kernel 3 (RMS = 1 / sqrt(mean(x^2) + eps)); "Phase 19: MoE - gpt-oss-20b",
+// section 2 Experts (out = sum over the top-4 of scores * y_e), RMSNorm (fp32
+// variance) and Decoder layer (out = h + moe(post_norm(h))).
 #include "common.cuh"
 #include "internal.h"
 
@@ -15,7 +19,7 @@ template <bool F32>
 __global__ void __launch_bounds__(256)
 combine_kernel(const float* __restrict__ Y, const float* __restrict__ slot_w,
                const int32_t* __restrict__ slot_expert, int T, int K, int d, int E1,
-               void* __restrict__ y) {
+               const uint16_t* __restrict__ resid, void* __restrict__ y) {
   pdl_wait();
   const int d8 = d / 8;
   const long n = (long)T * d8;
@@ -23,6 +27,11 @@ combine_kernel(const float* __restrict__ Y, const float* __restrict__ slot_w,
     const long t = i / d8;
     const int o = (int)(i - t * d8) * 8;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (resid) {
+      const uint4 r = ldg_nc_v4(resid + (size_t)t * d + o);
+      acc[0] = bf16_lo(r.x); acc[1] = bf16_hi(r.x); acc[2] = bf16_lo(r.y); acc[3] = bf16_hi(r.y);
+      acc[4] = bf16_lo(r.z); acc[5] = bf16_hi(r.z); acc[6] = bf16_lo(r.w); acc[7] = bf16_hi(r.w);
+    }
     for (int j = 0; j < K; ++j) {
       const long s = t * K + j;
       const int v = slot_expert[s];
@@ -49,18 +58,65 @@ combine_kernel(const float* __restrict__ Y, const float* __restrict__ slot_w,
   pdl_trigger();
 }
 
+// One warp per token row: sum of squares in fp32, r = 1 / sqrt(mean + eps), and
+// xn = bf16(x * r * w).  Also the first kernel of a call that uses it: it clears the
+// device status word.
+__global__ void __launch_bounds__(256)
+rmsnorm_kernel(const uint16_t* __restrict__ x, int T, int d, const uint16_t* __restrict__ w, float eps,
+               uint16_t* __restrict__ xn, uint32_t* __restrict__ status) {
+  pdl_wait();
+  if (status && blockIdx.x == 0 && threadIdx.x == 0) *status = 0u;
+  const int lane = threadIdx.x & 31;
+  const int d8 = d / 8;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += (gridDim.x * blockDim.x) >> 5) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+    float ss = 0.f;
+    for (int i = lane; i < d8; i += 32) {
+      const uint4 v = ldg_nc_v4(src + i);
+      const float a[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                          bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ss = fmaf(a[j], a[j], ss);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float r = 1.f / sqrtf(ss / (float)d + eps);
+    uint4* dst = reinterpret_cast<uint4*>(xn + (size_t)t * d);
+    const uint4* wv = reinterpret_cast<const uint4*>(w);
+    for (int i = lane; i < d8; i += 32) {
+      const uint4 v = ldg_nc_v4(src + i), g = ldg_nc_v4(wv + i);
+      uint4 o;
+      o.x = pack_bf16x2(bf16_lo(v.x) * r * bf16_lo(g.x), bf16_hi(v.x) * r * bf16_hi(g.x));
+      o.y = pack_bf16x2(bf16_lo(v.y) * r * bf16_lo(g.y), bf16_hi(v.y) * r * bf16_hi(g.y));
+      o.z = pack_bf16x2(bf16_lo(v.z) * r * bf16_lo(g.z), bf16_hi(v.z) * r * bf16_hi(g.z));
+      o.w = pack_bf16x2(bf16_lo(v.w) * r * bf16_lo(g.w), bf16_hi(v.w) * r * bf16_hi(g.w));
+      dst[i] = o;
+    }
+  }
+  pdl_trigger();
+}
+
 }  // namespace
 
 cudaError_t launch_combine(const float* Y, const float* slot_w, const int32_t* slot_expert, int T,
-                           int K, int d, int E1, void* y, bool y_fp32, cudaStream_t s) {
+                           int K, int d, int E1, const uint16_t* resid, void* y, bool y_fp32,
+                           cudaStream_t s) {
   const long n = (long)T * (d / 8);
   long blocks = (n + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
   if (y_fp32)
     return launch_pdl(combine_kernel<true>, dim3((int)blocks), dim3(256), 0, s, Y, slot_w, slot_expert,
-                      T, K, d, E1, y);
+                      T, K, d, E1, resid, y);
   return launch_pdl(combine_kernel<false>, dim3((int)blocks), dim3(256), 0, s, Y, slot_w, slot_expert,
-                    T, K, d, E1, y);
+                    T, K, d, E1, resid, y);
+}
+
+cudaError_t launch_rmsnorm(const uint16_t* x, int T, int d, const uint16_t* w, float eps, uint16_t* xn,
+                           uint32_t* status, cudaStream_t s) {
+  int blocks = (T + 7) / 8;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  if (blocks < 1) blocks = 1;
+  return launch_pdl(rmsnorm_kernel, dim3(blocks), dim3(256), 0, s, x, T, d, w, eps, xn, status);
 }
 
 }  // namespace moe

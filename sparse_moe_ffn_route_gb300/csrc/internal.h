@@ -189,8 +189,13 @@ cudaError_t launch_down_prefill_fp4(const ExpertParams& p, const RouteState& rs,
 cudaError_t launch_mxfp4_to_bf16(const uint8_t* blocks, const uint8_t* scales, long long rows,
                                  int n_in, uint16_t* out, cudaStream_t s);
 
-// y[t] = sum_j slot_w[t,j] * Y[t*K + j]  (fp32 accumulation; bf16 or fp32 out).
+// y[t] = (resid[t] +) sum_j slot_w[t,j] * Y[t*K + j]  (fp32 accumulation; bf16 or fp32 out).
 cudaError_t launch_combine(const float* Y, const float* slot_w, const int32_t* slot_expert, int T,
-                           int K, int d, int E1, void* y, bool y_fp32, cudaStream_t s);
+                           int K, int d, int E1, const uint16_t* resid, void* y, bool y_fp32,
+                           cudaStream_t s);
+// xn = bf16(x * w / sqrt(mean(x^2) + eps)) per token row; clears *status (the first
+// kernel of a call that normalises).
+cudaError_t launch_rmsnorm(const uint16_t* x, int T, int d, const uint16_t* w, float eps, uint16_t* xn,
+                           uint32_t* status, cudaStream_t s);
 
 }  // namespace moe

@@ -19,7 +19,7 @@ struct Layout {
   int K, E1, S, ldl, ldh;
   bool prefill;             // the expert phase runs the tcgen05 grouped GEMMs
   bool prefill_fp4;         // ... in their f16-operand MXFP4 form (expert_prefill_fp4.cu)
-  size_t status, counts, offsets, work, n_work, slot_expert, slot_w, row2slot, hist, logits, h, Y,
+  size_t status, counts, offsets, work, n_work, slot_expert, slot_w, row2slot, hist, logits, h, Y, xn,
       xp, scalesT, xstage, ystage, total;
 };
 
@@ -36,6 +36,9 @@ int validate_cfg(const moe_cfg_t* c) {
     return MOE_ERR_INVALID_ARG;
   for (int r : c->reserved)
     if (r != 0) return MOE_ERR_INVALID_ARG;
+  if (c->rms_norm < 0 || c->rms_norm > 1 || c->residual < 0 || c->residual > 1 ||
+      !std::isfinite(c->rms_eps) || c->rms_eps < 0.f)
+    return MOE_ERR_INVALID_ARG;
   if (!std::isfinite(c->expert_weights_scale) || !std::isfinite(c->glu_limit) ||
       !std::isfinite(c->glu_alpha))
     return MOE_ERR_INVALID_ARG;
@@ -91,6 +94,7 @@ bool make_layout(const moe_cfg_t* c, int T, Layout* L) {
                       : L->prefill_fp4 ? prefill_fp4_scratch_bytes(sp, L->S)
                                        : prefill_scales_bytes(sp, c->wfmt));
   }
+  L->xn = take(c->rms_norm ? 2 * Tz * d : 0);   // RMSNorm(x), the MoE's input
   L->xstage = take(2 * Tz * d);
   L->ystage = take(4 * Tz * d);
   L->total = off;
@@ -150,9 +154,13 @@ int check_experts(const moe_cfg_t* c, const moe_experts_t* e, const moe_shared_t
   return MOE_OK;
 }
 
-int check_router(const moe_router_t* r) {
+int check_router(const moe_cfg_t* c, const moe_router_t* r) {
   if (!r || !r->w) return MOE_ERR_INVALID_ARG;
   if (!aligned16(r->w) || (r->bias && !aligned16(r->bias))) return MOE_ERR_ALIGNMENT;
+  if (c->rms_norm) {
+    if (!r->norm_w) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(r->norm_w)) return MOE_ERR_ALIGNMENT;
+  }
   return MOE_OK;
 }
 
@@ -235,19 +243,27 @@ int run_router(const moe_cfg_t* c, const void* x, int T, const moe_router_t* r,
     ldl = c->n_experts;
   }
   if (fill_slots) MOE_CUDA(mark_phase(0, s));
+  // The MoE's input: RMSNorm(x) when cfg.rms_norm (that kernel then clears the status).
+  const uint16_t* xr = static_cast<const uint16_t*>(x);
+  uint32_t* status = at<uint32_t>(ws, L.status);
+  if (c->rms_norm) {
+    uint16_t* xn = at<uint16_t>(ws, L.xn);
+    MOE_CUDA(launch_rmsnorm(xr, T, c->d_model, static_cast<const uint16_t*>(r->norm_w), c->rms_eps, xn,
+                            status, s));
+    xr = xn;
+    status = nullptr;
+  }
   bool gate_in_logits = false;
-  MOE_CUDA(launch_router_logits(static_cast<const uint16_t*>(x), T, c->d_model,
-                                static_cast<const uint16_t*>(r->w),
+  MOE_CUDA(launch_router_logits(xr, T, c->d_model, static_cast<const uint16_t*>(r->w),
                                 static_cast<const uint16_t*>(r->bias), wsh, c->n_experts, lg, ldl,
-                                at<uint32_t>(ws, L.status), &gate_in_logits, s));
+                                status, &gate_in_logits, s));
   if (fill_slots) MOE_CUDA(mark_phase(1, s));
   const int norm = c->gating == MOE_GATING_TOPK_SOFTMAX ? 1 : c->norm_topk_prob;
   int32_t* slot_e = fill_slots ? at<int32_t>(ws, L.slot_expert) : nullptr;
   float* slot_w = fill_slots ? at<float>(ws, L.slot_w) : nullptr;
   MOE_CUDA(launch_router_select(lg, ldl, T, c->n_experts, c->top_k, norm,
                                 c->expert_weights_scale, has_sh, ids_out, w_out, sgate_out, slot_e,
-                                slot_w, static_cast<const uint16_t*>(x), c->d_model,
-                                gate_in_logits ? nullptr : wsh, s));
+                                slot_w, xr, c->d_model, gate_in_logits ? nullptr : wsh, s));
   if (fill_slots) MOE_CUDA(mark_phase(2, s));
   if (logits_out && has_sh)
     MOE_CUDA(cudaMemcpy2DAsync(logits_out, sizeof(float) * c->n_experts, lg, sizeof(float) * ldl,
@@ -256,9 +272,13 @@ int run_router(const moe_cfg_t* c, const void* x, int T, const moe_router_t* r,
 }
 
 // Permute, experts, combine.  The slots must already hold the routing.
-int run_experts(const moe_cfg_t* c, const void* x, int T, const moe_experts_t* e,
+int run_experts(const moe_cfg_t* c, const void* x_layer, int T, const moe_experts_t* e,
                 const moe_shared_t* sh, void* y, const Layout& L, void* ws, cudaStream_t s) {
   const RouteState rs = route_state(ws, L);
+  // The experts run on the MoE's input (RMSNorm(x) when cfg.rms_norm, written by the
+  // router step); the residual adds the un-normalised layer input.
+  const void* x = c->rms_norm ? static_cast<const void*>(at<uint16_t>(ws, L.xn)) : x_layer;
+  const uint16_t* resid = c->residual ? static_cast<const uint16_t*>(x_layer) : nullptr;
   const ExpertParams p = expert_params(c, e, sh);
   uint16_t* h = at<uint16_t>(ws, L.h);
   float* Y = at<float>(ws, L.Y);
@@ -283,7 +303,7 @@ int run_experts(const moe_cfg_t* c, const void* x, int T, const moe_experts_t* e
     MOE_CUDA(launch_h_fix_f16(hside, rows.hmax, L.S, c->expert_ff, kh, h16, L.ldh, rows.hmul, s));
     MOE_CUDA(launch_down_prefill_fp4(p, rs, h16, L.ldh, L.S, Y, scratch, max_items, s));
     MOE_CUDA(mark_phase(5, s));
-    MOE_CUDA(launch_combine(Y, rs.slot_w, rs.slot_expert, T, L.K, c->d_model, L.E1, y,
+    MOE_CUDA(launch_combine(Y, rs.slot_w, rs.slot_expert, T, L.K, c->d_model, L.E1, resid, y,
                             c->y_fp32 != 0, s));
     MOE_CUDA(mark_phase(6, s));
     return MOE_OK;
@@ -304,7 +324,7 @@ int run_experts(const moe_cfg_t* c, const void* x, int T, const moe_experts_t* e
     MOE_CUDA(mark_phase(4, s));
     MOE_CUDA(launch_down_prefill(p, c->wfmt, rs, h, L.ldh, L.S, Y, scalesT, max_mtiles, s));
     MOE_CUDA(mark_phase(5, s));
-    MOE_CUDA(launch_combine(Y, rs.slot_w, rs.slot_expert, T, L.K, c->d_model, L.E1, y,
+    MOE_CUDA(launch_combine(Y, rs.slot_w, rs.slot_expert, T, L.K, c->d_model, L.E1, resid, y,
                             c->y_fp32 != 0, s));
     MOE_CUDA(mark_phase(6, s));
     return MOE_OK;
@@ -329,7 +349,7 @@ int run_experts(const moe_cfg_t* c, const void* x, int T, const moe_experts_t* e
   if (ring) MOE_CUDA(launch_down_decode_fp4(p, rs, h, L.ldh, Y, max_items, s, &done));
   if (!done) MOE_CUDA(launch_down_decode(p, c->wfmt, rs, h, L.ldh, Y, max_items, chunks, s));
   MOE_CUDA(mark_phase(5, s));
-  MOE_CUDA(launch_combine(Y, rs.slot_w, rs.slot_expert, T, L.K, c->d_model, L.E1, y,
+  MOE_CUDA(launch_combine(Y, rs.slot_w, rs.slot_expert, T, L.K, c->d_model, L.E1, resid, y,
                           c->y_fp32 != 0, s));
   MOE_CUDA(mark_phase(6, s));
   return MOE_OK;
@@ -372,7 +392,7 @@ int moe_route(const moe_cfg_t* cfg, const void* x, int32_t T, const moe_router_t
   if (T < 0) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!x || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
-  if ((st = check_router(router)) != MOE_OK) return st;
+  if ((st = check_router(cfg, router)) != MOE_OK) return st;
   // The shared gate is computed when the layer has a shared expert (shared_ff > 0).
   const bool has_sh = cfg->shared_ff > 0;
   if (has_sh && (!shared || !shared->gate_inp)) return MOE_ERR_INVALID_ARG;
@@ -411,7 +431,7 @@ int moe_ffn_forward(const moe_cfg_t* cfg, const void* x, int32_t T, const moe_ro
   if (T < 0) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!x || !y) return MOE_ERR_INVALID_ARG;
-  if ((st = check_router(router)) != MOE_OK) return st;
+  if ((st = check_router(cfg, router)) != MOE_OK) return st;
   if ((st = check_experts(cfg, experts, shared)) != MOE_OK) return st;
   if (!aligned16(x) || !aligned16(y) || (topk_ids && !aligned16(topk_ids)) ||
       (topk_w && !aligned16(topk_w)))
@@ -435,6 +455,9 @@ int moe_ffn_forward_routed(const moe_cfg_t* cfg, const void* x, int32_t T,
   if (T == 0) return MOE_OK;
   if (!x || !y || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
   if (cfg->shared_ff > 0 && !sgate) return MOE_ERR_INVALID_ARG;
+  // The norm weight lives in the router description, which this entry point does not
+  // take: callers that route themselves pass the MoE's input (already normalised).
+  if (cfg->rms_norm) return MOE_ERR_UNSUPPORTED;
   if ((st = check_experts(cfg, experts, shared)) != MOE_OK) return st;
   if (!aligned16(x) || !aligned16(y) || !aligned16(topk_ids) || !aligned16(topk_w) ||
       (sgate && !aligned16(sgate)))

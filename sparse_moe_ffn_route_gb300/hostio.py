@@ -37,7 +37,8 @@ def to_numpy_bf16(t: torch.Tensor) -> np.ndarray:
 def upload(layer, device="cuda"):
     """(x, Router, Experts, Shared | None) for an object with the layer's host arrays."""
     x = bf16_tensor(layer.x, device)
-    router = Router(bf16_tensor(layer.router_w, device), bf16_tensor(layer.router_b, device))
+    router = Router(bf16_tensor(layer.router_w, device), bf16_tensor(layer.router_b, device),
+                    bf16_tensor(getattr(layer, "norm_w", None), device))
     if getattr(layer, "gu_blocks", None) is not None:
         experts = Experts(gate_up=u8_tensor(layer.gu_blocks, device),
                           gate_up_scales=u8_tensor(layer.gu_scales, device),

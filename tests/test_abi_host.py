@@ -81,6 +81,7 @@ def test_kernel_plan_forms():
 BAD_CFGS = [
     dict(top_k=0), dict(top_k=300), dict(n_experts=0), dict(n_experts=2000), dict(d_model=-1),
     dict(gating=2), dict(act=5), dict(wfmt=3), dict(path=7), dict(expert_weights_scale=float("nan")),
+    dict(rms_norm=2), dict(residual=-1), dict(rms_eps=float("nan")), dict(rms_eps=-1e-6),
 ]
 
 
@@ -146,3 +147,21 @@ def test_status_strings():
     for st in range(-7, 1):
         assert moe.moe_status_string(st) != "unknown status"
     assert moe.moe_status_string(-99) == "unknown status"
+
+
+def test_rms_norm_needs_the_norm_weight_and_a_router():
+    """cfg.rms_norm without router.norm_w is an invalid argument; the routed entry point,
+    which takes no router, does not support it (both checked before any launch)."""
+    c = moe.qwen_cfg(64, 8, 2, 32, 32).replace(rms_norm=1, rms_eps=1e-6)
+    fake = ctypes.c_void_p(1 << 20)
+    r = moe._Router(fake, None, None)
+    sh = moe._Shared(fake, fake, fake, fake)
+    ex = moe._Experts(gate=fake, up=fake, down=fake)
+    st = moe._lib.moe_ffn_forward(ctypes.byref(c), fake, 8, ctypes.byref(r), ctypes.byref(ex),
+                                  ctypes.byref(sh), fake, None, None, fake, 1 << 30, None)
+    assert st == -1
+    st = moe._lib.moe_ffn_forward_routed(ctypes.byref(c), fake, 8, fake, fake, fake,
+                                         ctypes.byref(ex), ctypes.byref(sh), fake, fake, 1 << 30, None)
+    assert st == -2
+    # the norm's input copy makes the workspace larger
+    assert moe.moe_workspace_bytes(c, 64) > moe.moe_workspace_bytes(c.replace(rms_norm=0), 64)

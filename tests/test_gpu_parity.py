@@ -441,3 +441,66 @@ def test_mxfp4_prefill_token_magnitudes(shift):
     if np.any(diff):
         ref = oracle.forward(g, lay, forced_ids=np.where(diff[:, None], ids_g, ref.ids))
     check_outputs(y32, y16, ref.y, f"shift {shift}")
+
+
+# ----------------------------------------------------------------------------- RMSNorm + residual
+NORM_CASES = [
+    (mi.small_spec("qwen", 128, 16, 4, 64, 96, 33, bias=("normal", 0.5)), 1),       # decode, warp
+    (mi.small_spec("qwen", 256, 16, 4, 128, 128, 300, bias=("normal", 0.5)), 2),    # prefill bf16
+    (mi.small_spec("gptoss", 96, 12, 4, 96, 0, 7, bias=("normal", 0.1)), 1),        # decode ring
+    (mi.small_spec("gptoss", 128, 4, 2, 128, 0, 600, bias=("normal", 0.1)), 2),     # prefill f16
+]
+
+
+def _eps(spec):
+    return 1e-6 if spec.family == "qwen" else 1e-5
+
+
+@pytest.mark.parametrize("spec,path", NORM_CASES, ids=lambda v: v.name if hasattr(v, "name") else str(v))
+def test_rmsnorm_and_residual_match_oracle(spec, path):
+    """y = x + MoE(RMSNorm(x)) through every kernel plan, against the oracle."""
+    moe = moe_lib()
+    lay = mi.make_layer(spec)
+    lay.norm_w = mi.make_norm_w(spec)
+    g = dataclasses.replace(oracle.gating_for(spec), rms_norm=1, residual=1, rms_eps=_eps(spec))
+    ref = oracle.forward(g, lay)
+    x, router, experts, shared = upload(lay)
+    c = cfg_for(spec, path=path).replace(rms_norm=1, residual=1, rms_eps=_eps(spec))
+    T, k = spec.tokens, spec.top_k
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    ws = moe.workspace(c, T)
+    y16 = moe.moe_ffn_forward(c, x, router, experts, shared, topk_ids=ids, ws=ws)
+    y32 = moe.moe_ffn_forward(c.replace(y_fp32=1), x, router, experts, shared, ws=ws)
+    assert moe.moe_device_status(ws)[0] == 0
+    ids_g = ids.cpu().numpy()
+    diff = np.any(ids_g != ref.ids, axis=1)
+    assert not np.any(diff & ~oracle.near_tie_tokens(ref.logits, ref.ids))
+    if np.any(diff):
+        ref = oracle.forward(g, lay, forced_ids=np.where(diff[:, None], ids_g, ref.ids))
+    check_outputs(y32, y16, ref.y, f"{spec.name} path {path}")
+    # the router alone applies the same norm: its ids and logits agree with the layer's
+    logits = torch.empty((T, spec.n_experts), dtype=torch.float32, device="cuda")
+    ids2, _, _, _ = moe.moe_route(c, x, router, shared, logits=logits, ws=ws)
+    assert torch.equal(ids2, ids)
+    # (a normalised element may round to the other neighbouring bf16 value in fp32)
+    assert np.allclose(logits.cpu().numpy(), ref.logits, rtol=1e-3, atol=2e-3)
+
+
+def test_residual_with_caller_routing():
+    """The routed entry point adds the residual; with rms_norm it refuses (no router)."""
+    moe = moe_lib()
+    spec = mi.small_spec("qwen", 64, 8, 3, 32, 32, 45)
+    lay = mi.make_layer(spec)
+    g = dataclasses.replace(oracle.gating_for(spec), residual=1)
+    ref = oracle.forward(g, lay)
+    x, router, experts, shared = upload(lay)
+    c = cfg_for(spec).replace(residual=1)
+    ids_d = torch.from_numpy(ref.ids).cuda()
+    w_d = torch.from_numpy(ref.w.astype(np.float32)).cuda()
+    sg = torch.from_numpy(ref.sgate.astype(np.float32)).cuda()
+    y16 = moe.moe_ffn_forward_routed(c, x, ids_d, w_d, experts, shared, sgate=sg)
+    y32 = moe.moe_ffn_forward_routed(c.replace(y_fp32=1), x, ids_d, w_d, experts, shared, sgate=sg)
+    check_outputs(y32, y16, ref.y, "routed residual")
+    with pytest.raises(moe.MoeError):
+        moe.moe_ffn_forward_routed(c.replace(rms_norm=1, rms_eps=1e-6), x, ids_d, w_d, experts, shared,
+                                   sgate=sg)
