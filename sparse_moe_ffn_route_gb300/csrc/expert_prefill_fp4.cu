@@ -435,34 +435,43 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
+constexpr int kPrepRows = 128;                     // weight rows per prep CTA (one per thread)
+
 // Per weight row n of one matrix [E * R rows, nb blocks]: c_n from the row's largest
 // finite scale byte (that block's multiplier becomes 2^13), colmul[n] = 2^c_n, and
 // cinfo[n] = c_n | general << 16, where `general` marks a row with a block whose
 // multiplier is not a normal f16 (scale byte more than 27 below the largest, or 255).
-// One warp per weight row.
+// One CTA per 128 weight rows, one thread per row, the rows staged in shared memory.
 __global__ void __launch_bounds__(256)
 fp4_prep_kernel(const uint8_t* __restrict__ scales, long long rows, int nb, float* __restrict__ colmul,
                 int32_t* __restrict__ cinfo) {
+  extern __shared__ uint8_t tile[];               // kPrepRows rows of nb scale bytes
   pdl_wait();
   pdl_trigger();
-  const int lane = threadIdx.x & 31;
-  for (long long n = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; n < rows;
-       n += ((long long)gridDim.x * blockDim.x) >> 5) {
-    const uint8_t* sr = scales + n * nb;
+  const long long r0 = (long long)blockIdx.x * kPrepRows;
+  const int nrows = (int)min((long long)kPrepRows, rows - r0);
+  const int bytes = nrows * nb;
+  // The tile's rows are contiguous: copy them with 16-byte loads (r0 * nb is a
+  // multiple of 16), the ragged end byte by byte.
+  const uint8_t* src = scales + r0 * nb;
+  const int nvec = bytes / 16;
+  for (int i = threadIdx.x; i < nvec; i += blockDim.x)
+    reinterpret_cast<uint4*>(tile)[i] = ldg_nc_v4(src + 16 * i);
+  for (int i = 16 * nvec + threadIdx.x; i < bytes; i += blockDim.x) tile[i] = src[i];
+  __syncthreads();
+  const int t = threadIdx.x;
+  if (t < nrows) {
+    const uint8_t* sr = tile + t * nb;
     int smax = -1, smin = 256;
-    for (int b = lane; b < nb; b += 32) {
-      const int s = sr[b];
-      if (s != 255) smax = max(smax, s);
-      smin = min(smin, s == 255 ? -1000 : s);
+    for (int b = 0; b < nb; ++b) {
+      const int sv = sr[b];
+      if (sv != 255) smax = max(smax, sv);
+      smin = min(smin, sv == 255 ? -1000 : sv);
     }
-    smax = __reduce_max_sync(0xffffffffu, smax);
-    smin = __reduce_min_sync(0xffffffffu, smin);
     const int c = smax < 0 ? 0 : smax - 140;
     const int general = (smax < 0 || smin < smax - 27) ? 1 : 0;
-    if (lane == 0) {
-      cinfo[n] = (c & 0xFFFF) | (general << 16);
-      colmul[n] = ldexpf(1.f, c);
-    }
+    cinfo[r0 + t] = (c & 0xFFFF) | (general << 16);
+    colmul[r0 + t] = ldexpf(1.f, c);
   }
 }
 
@@ -560,13 +569,17 @@ int h_stage_exp(float limit, float alpha) {
 cudaError_t launch_prefill_fp4_prep(const ExpertParams& p, uint8_t* scratch, int S, cudaStream_t s) {
   const Fp4Scratch sc = carve(p, scratch, S);
   const long long rg = (long long)p.E * 2 * p.ff, rd = (long long)p.E * p.d;
-  int blocks = (int)std::min<long long>((rg * 32 + 255) / 256, 152 * 8);
-  cudaError_t e = launch_pdl(fp4_prep_kernel, dim3(blocks), dim3(256), 0, s, p.gu_scales, rg, p.d / 32,
-                             sc.colmul_gu, sc.cinfo_gu);
+  const int nbg = p.d / 32, nbd = p.ff / 32;
+  const int smem = kPrepRows * (nbg > nbd ? nbg : nbd);
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(fp4_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return cudaErrorInvalidValue;
+  cudaError_t e = launch_pdl(fp4_prep_kernel, dim3((unsigned)((rg + kPrepRows - 1) / kPrepRows)),
+                             dim3(kPrepRows), (size_t)kPrepRows * nbg, s, p.gu_scales, rg, nbg, sc.colmul_gu,
+                             sc.cinfo_gu);
   if (e != cudaSuccess) return e;
-  blocks = (int)std::min<long long>((rd * 32 + 255) / 256, 152 * 8);
-  return launch_pdl(fp4_prep_kernel, dim3(blocks), dim3(256), 0, s, p.dn_scales, rd, p.ff / 32, sc.colmul_dn,
-                    sc.cinfo_dn);
+  return launch_pdl(fp4_prep_kernel, dim3((unsigned)((rd + kPrepRows - 1) / kPrepRows)), dim3(kPrepRows),
+                    (size_t)kPrepRows * nbd, s, p.dn_scales, rd, nbd, sc.colmul_dn, sc.cinfo_dn);
 }
 
 Fp4Rows prefill_fp4_rows(const ExpertParams& p, uint8_t* scratch, int S) {

@@ -162,12 +162,17 @@ perm_scan_kernel(RouteState rs, int E1, int tpg, int* __restrict__ hist, int nch
   const int tid = threadIdx.x;
   pdl_wait();
   for (int v = tid; v < E1; v += kPermuteThreads) {
+    // chunks in groups of 8 whose loads are all in flight before the running sum
     int run = 0;
-    for (int c = 0; c < nchunk; ++c) {
-      int* p = hist + (size_t)c * E1 + v;
-      const int n = *p;
-      *p = run;
-      run += n;
+    for (int c0 = 0; c0 < nchunk; c0 += 8) {
+      int n[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) n[j] = c0 + j < nchunk ? hist[(size_t)(c0 + j) * E1 + v] : 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (c0 + j < nchunk) hist[(size_t)(c0 + j) * E1 + v] = run;
+        run += n[j];
+      }
     }
     tot[v] = run;
   }
