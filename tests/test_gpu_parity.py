@@ -504,3 +504,41 @@ def test_residual_with_caller_routing():
     with pytest.raises(moe.MoeError):
         moe.moe_ffn_forward_routed(c.replace(rms_norm=1, rms_eps=1e-6), x, ids_d, w_d, experts, shared,
                                    sgate=sg)
+
+
+# ----------------------------------------------------------------------------- CUDA graphs
+GRAPH_CASES = [
+    mi.small_spec("qwen", 128, 16, 4, 64, 96, 33, bias=("normal", 0.5)),          # decode
+    mi.small_spec("gptoss", 96, 12, 4, 96, 0, 7, bias=("normal", 0.1)),           # decode ring
+    mi.small_spec("gptoss", 128, 4, 2, 128, 0, 600, bias=("normal", 0.1)),        # prefill f16
+    mi.small_spec("qwen", 256, 16, 4, 128, 128, 300, bias=("normal", 0.5)),       # prefill bf16
+]
+
+
+@pytest.mark.parametrize("spec", GRAPH_CASES, ids=lambda s: s.name)
+def test_forward_captured_in_a_cuda_graph(spec):
+    """moe_ffn_forward captured once and replayed on new inputs gives, bit for bit, what
+    eager calls give (no host synchronisation, no allocation, no state kept between
+    calls).  The first, eager call sets the kernels' launch attributes."""
+    moe = moe_lib()
+    lay = mi.make_layer(spec)
+    x, router, experts, shared = upload(lay)
+    c = cfg_for(spec)
+    T = spec.tokens
+    ws = moe.workspace(c, T)
+    y = torch.empty_like(x)
+    moe.moe_ffn_forward(c, x, router, experts, shared, y=y, ws=ws)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            moe.moe_ffn_forward(c, x, router, experts, shared, y=y, ws=ws, stream=s)
+    for rep in range(3):
+        xs = mi.make_x(dataclasses.replace(spec, seed=spec.seed + 17 * rep), T)
+        x.copy_(torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16).cuda())
+        graph.replay()
+        torch.cuda.synchronize()
+        want = moe.moe_ffn_forward(c, x, router, experts, shared, ws=moe.workspace(c, T))
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), want.view(torch.int16)), rep
