@@ -223,9 +223,12 @@ int moe_ffn_forward_routed(const moe_cfg_t* cfg, const void* x, int32_t T,
                            void* ws, size_t ws_bytes, void* stream);
 
 /* moe_ffn_forward from and to HOST memory: x_host bf16 [T, d] and y_host bf16
- * [T, d] are host pointers (pinned memory gives full copy speed); the weights
- * stay device pointers.  Copies x into the workspace, runs the layer, copies y
- * back, and synchronises `stream` before returning, so y_host is ready on return. */
+ * [T, d] (fp32 with cfg->y_fp32) are host pointers (pinned memory gives full copy
+ * speed); the weights stay device pointers.  Copies x into the workspace, runs the
+ * layer and synchronises `stream` before returning, so y_host is ready on return.
+ * A page-locked y_host that has a device address (cudaHostAlloc, or cudaHostRegister
+ * with mapping) and is 16-byte aligned is written by the last kernel directly;
+ * other memory receives y through a workspace buffer and a device-to-host copy. */
 int moe_ffn_forward_host(const moe_cfg_t* cfg, const void* x_host, int32_t T,
                          const moe_router_t* router, const moe_experts_t* experts,
                          const moe_shared_t* shared, void* y_host, void* ws, size_t ws_bytes,

@@ -32,15 +32,31 @@ combine_kernel(const float* __restrict__ Y, const float* __restrict__ slot_w,
       acc[0] = bf16_lo(r.x); acc[1] = bf16_hi(r.x); acc[2] = bf16_lo(r.y); acc[3] = bf16_hi(r.y);
       acc[4] = bf16_lo(r.z); acc[5] = bf16_hi(r.z); acc[6] = bf16_lo(r.w); acc[7] = bf16_hi(r.w);
     }
-    for (int j = 0; j < K; ++j) {
-      const long s = t * K + j;
-      const int v = slot_expert[s];
-      if (v < 0 || v >= E1) continue;          // flagged by the permute, contributes nothing
-      const float w = slot_w[s];
-      const float4* src = reinterpret_cast<const float4*>(Y + (size_t)s * d + o);
-      const float4 a = src[0], b = src[1];
-      acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
-      acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
+    // Slots in groups of four: the loads of a group are all in flight together, and
+    // the sums still take the slots in order.  A slot flagged by the permute (expert
+    // out of range) contributes nothing and its Y row is not read.
+    for (int j0 = 0; j0 < K; j0 += 4) {
+      uint32_t okm = 0;
+      float w[4];
+      float4 a[4], b[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const long s = t * K + j0 + q;
+        const int v = j0 + q < K ? slot_expert[s] : -1;
+        const bool ok = v >= 0 && v < E1;
+        okm |= ok ? 1u << q : 0u;
+        w[q] = ok ? slot_w[s] : 0.f;
+        const float4* src = reinterpret_cast<const float4*>(Y + (size_t)s * d + o);
+        a[q] = ok ? src[0] : make_float4(0.f, 0.f, 0.f, 0.f);
+        b[q] = ok ? src[1] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (okm & (1u << q)) {
+          acc[0] += w[q] * a[q].x; acc[1] += w[q] * a[q].y; acc[2] += w[q] * a[q].z; acc[3] += w[q] * a[q].w;
+          acc[4] += w[q] * b[q].x; acc[5] += w[q] * b[q].y; acc[6] += w[q] * b[q].z; acc[7] += w[q] * b[q].w;
+        }
+      }
     }
     if (F32) {
       float4* dst = reinterpret_cast<float4*>(static_cast<float*>(y) + (size_t)t * d + o);

@@ -56,7 +56,12 @@ struct Lay {
   static constexpr int kStageBytes =
       ((kATiles * kTileA + kTileB + kPacked + kScales + 1023) / 1024) * 1024;
   static constexpr int kStages = DUAL ? 3 : 4;
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024;   // + alignment slack
+  // bf16 down: each epilogue warp turns its 32 rows x 32 fp32 columns around in
+  // shared memory ([32][kEpiPitch] floats) so that its Y stores are whole lines
+  static constexpr bool kEpiStage = DUAL && !FP4;
+  static constexpr int kEpiPitch = 36;
+  static constexpr int kEpiBytes = kEpiStage ? 4 * 32 * kEpiPitch * 4 : 0;
+  static constexpr int kSmemBytes = kStages * kStageBytes + kEpiBytes + 1024;   // + alignment slack
   static constexpr int kDequantWarps = FP4 ? 12 : 0;
   static constexpr int kThreads = 192 + 32 * kDequantWarps;
 };
@@ -394,6 +399,47 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             for (int i = 0; i < 32; ++i)
               if (i < ncol) lrow[e0 + c0 + i] = v[i] + (g.rbias ? bf16_to_f32(g.rbias[e0 + c0 + i]) : 0.f);
           }
+        }
+      } else if (L::kEpiStage && g.mode == kModeDown) {
+        // Lane l first holds row l of the warp's 32 rows; after the turn in shared
+        // memory, lanes 8j..8j+7 store 128 contiguous bytes of one row, so each store
+        // instruction writes four whole lines of Y instead of 32 partial ones.
+        float* stg = reinterpret_cast<float*>(smem + kStages * kStageBytes) + q * 32 * L::kEpiPitch;
+        const int slot = valid ? g.rs.row2slot[grow] : -1;
+        const int rr = lane >> 3, cc = (lane & 7) * 4;
+        int rs_[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rs_[i] = __shfl_sync(0xffffffffu, slot, 4 * i + rr);
+        const int o0 = tl.n * g.N;
+        const uint16_t* bp = (!sh && g.dn_bias) ? g.dn_bias + (size_t)tl.v * g.d + o0 : nullptr;
+        for (int c0 = 0; c0 < g.N; c0 += 32) {
+          float v[32];
+          tc::tmem_ld32(taddr + (uint32_t)c0, v);
+          float4* wr = reinterpret_cast<float4*>(stg + lane * L::kEpiPitch);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) wr[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          __syncwarp();
+          if (c0 + cc < g.N) {
+            float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (bp) {
+              const uint16_t* bq = bp + c0 + cc;
+              b4 = make_float4(bf16_to_f32(bq[0]), bf16_to_f32(bq[1]), bf16_to_f32(bq[2]), bf16_to_f32(bq[3]));
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              if (rs_[i] >= 0) {
+                float4 val = *reinterpret_cast<const float4*>(stg + (4 * i + rr) * L::kEpiPitch + cc);
+                if (bp) {
+                  val.x += b4.x;
+                  val.y += b4.y;
+                  val.z += b4.z;
+                  val.w += b4.w;
+                }
+                *reinterpret_cast<float4*>(g.Y + (size_t)rs_[i] * g.d + o0 + c0 + cc) = val;
+              }
+            }
+          }
+          __syncwarp();
         }
       } else if (g.mode == kModeDown) {
         float* yrow = valid ? g.Y + (size_t)g.rs.row2slot[grow] * g.d : nullptr;

@@ -490,11 +490,23 @@ int moe_ffn_forward_host(const moe_cfg_t* cfg, const void* x_host, int32_t T,
   void* yd = at<void>(ws, L.ystage);
   const size_t bytes = (size_t)T * cfg->d_model * 2;
   const size_t ybytes = (size_t)T * cfg->d_model * (cfg->y_fp32 ? 4 : 2);
+  // Page-locked y_host with a device address (cudaHostAlloc, or cudaHostRegister
+  // with mapping) takes the layer's output directly: the combine kernel writes it
+  // across the host link, in place of a device staging buffer and a second copy.
+  // Pageable memory reports cudaMemoryTypeUnregistered and takes the staged copy.
+  void* ydirect = nullptr;
+  cudaPointerAttributes pa;
+  if (cudaPointerGetAttributes(&pa, y_host) == cudaSuccess) {
+    if (pa.type == cudaMemoryTypeHost && pa.devicePointer && aligned16(pa.devicePointer))
+      ydirect = pa.devicePointer;
+  } else {
+    (void)cudaGetLastError();
+  }
   MOE_CUDA(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s));
-  st = moe_ffn_forward(cfg, xd, T, router, experts, shared, yd, nullptr, nullptr, ws, ws_bytes,
-                       stream);
+  st = moe_ffn_forward(cfg, xd, T, router, experts, shared, ydirect ? ydirect : yd, nullptr, nullptr,
+                       ws, ws_bytes, stream);
   if (st != MOE_OK) return st;
-  MOE_CUDA(cudaMemcpyAsync(y_host, yd, ybytes, cudaMemcpyDeviceToHost, s));
+  if (!ydirect) MOE_CUDA(cudaMemcpyAsync(y_host, yd, ybytes, cudaMemcpyDeviceToHost, s));
   MOE_CUDA(cudaStreamSynchronize(s));
   return MOE_OK;
 }

@@ -272,10 +272,17 @@ def test_full_workload(name, full_layers):
     err16, _ = check_y(y_numpy(y)[tok], ref.y, name + " (bf16 output)")
     print(f"{name}: max|dy| fp32 {err / rms:.2e} rms, bf16 {err16 / rms:.2e} rms, "
           f"near-ties {int(tie.sum())}")
-    # the host-buffer entry point gives the same bytes
+    # the host-buffer entry point gives the same bytes: pageable y (device buffer and
+    # a copy) and page-locked y (written by the combine kernel across the host link)
     xh = x.cpu().pin_memory()
     yh = moe.moe_ffn_forward_host(c, xh, router, experts, shared, ws=ws)
     assert torch.equal(yh.view(torch.int16), y.cpu().view(torch.int16))
+    yp = torch.full_like(yh, float("nan")).pin_memory()
+    moe.moe_ffn_forward_host(c, xh, router, experts, shared, y_host=yp, ws=ws)
+    assert torch.equal(yp.view(torch.int16), y.cpu().view(torch.int16))
+    yp32 = torch.full((T, spec.d_model), float("nan"), dtype=torch.float32).pin_memory()
+    moe.moe_ffn_forward_host(c.replace(y_fp32=1), xh, router, experts, shared, y_host=yp32, ws=ws)
+    assert torch.equal(yp32, y32.cpu())
 
 
 # ----------------------------------------------------------------------------- prefill (tcgen05) path
