@@ -61,6 +61,14 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   return r;
 }
 
+// One 32-byte store of eight fp32 values (p 32-byte aligned): a whole sector per
+// thread, half the store instructions of 16-byte vectors.
+__device__ __forceinline__ void stg_v8(float* p, const float* v) {
+  asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(v[0]), "f"(v[1]), "f"(v[2]),
+               "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+               : "memory");
+}
+
 // Streaming load for weights read once: skip L1, and let L2 fetch 256-byte
 // granules (the following k steps of the same row are requested right after).
 __device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {

@@ -455,10 +455,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
               for (int i = 0; i < 32; ++i)
                 if (i < ncol) v[i] += bf16_to_f32(bp[i]);
             }
-            float4* dst = reinterpret_cast<float4*>(yrow + o0 + c0);
+            // 32-byte stores: d is a multiple of 32 and o0 + c0 of 16
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              if (4 * i < ncol) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            for (int i = 0; i < 4; ++i)
+              if (8 * i < ncol) stg_v8(yrow + o0 + c0 + 8 * i, v + 8 * i);
           }
         }
       } else {

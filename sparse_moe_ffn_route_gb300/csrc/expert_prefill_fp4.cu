@@ -414,9 +414,10 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
               sp[1] = make_float4(hv[4], hv[5], hv[6], hv[7]);
             }
           } else {
-            float4* yp = reinterpret_cast<float4*>(g.Y + dst[gi] + 16 * c);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) yp[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            // Y rows are d fp32 apart with d a multiple of 32, and 16 c + col0 is a
+            // multiple of 16: both halves of the chunk start on 32 bytes.
+            stg_v8(g.Y + dst[gi] + 16 * c, v);
+            stg_v8(g.Y + dst[gi] + 16 * c + 8, v + 8);
           }
         }
         if (g.gateup && valid) atomicMax(g.hmax + (dst[gi] - col0 / 2) / g.ldh, hm);
