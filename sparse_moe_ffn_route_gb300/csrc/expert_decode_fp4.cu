@@ -5,9 +5,10 @@
 // to 8 token rows of one expert) x (128 weight rows), so every CTA gets the same
 // number of units and re-stages its token rows only when the item changes.  Warp 16
 // is the producer: one elected lane streams each unit's codes into a ring of
-// shared-memory stages with TMA (128 rows x 128 bytes = 256 inputs per stage,
-// 128-byte swizzle) and the unit's E8M0 scale bytes with one bulk copy.  About
-// 128 KB of weights are in flight per SM at any time, without holding registers.
+// shared-memory stages with TMA (two boxes of 128 rows x 128 bytes, 128-byte
+// swizzle: 512 inputs of each row per stage) and the unit's E8M0 scale bytes with
+// one bulk copy.  About 128 KB of weights are in flight per SM at any time, without
+// holding registers.
 //
 // Warps 0..15 consume: the pair of warps w and w + 8 owns rows 16w..16w+15 of the
 // unit (one MMA tile), each taking every other block of a stage.  An
@@ -37,9 +38,12 @@ constexpr int kTiles = 8;                         // 16-row MMA tiles per unit
 constexpr int kCW = 2 * kTiles;                   // consumer warps: two per tile (even / odd blocks)
 constexpr int kThreads = (kCW + 1) * 32;          // + the producer warp
 constexpr int kRows = 16 * kTiles;                // weight rows per unit
-constexpr int kStageBytes = kRows * 128;          // 128 rows x 128 bytes of codes
-constexpr int kBlocksPerStage = 8;                // 32-input blocks per stage row
-constexpr int kMaxRingStages = 12;
+constexpr int kBoxBytes = kRows * 128;            // one TMA box: 128 rows x 128 bytes of codes
+constexpr int kBlocksPerBox = 8;                  // 32-input blocks per box row
+constexpr int kBoxes = 2;                         // boxes per ring stage
+constexpr int kStageBytes = kBoxes * kBoxBytes;
+constexpr int kBlocksPerStage = kBoxes * kBlocksPerBox;
+constexpr int kMaxRingStages = 8;
 constexpr int kTokens = 8;                        // token rows per work item
 
 // Shared memory, from a 1024-aligned base: ring stages | scale buffers (2) |
@@ -244,12 +248,9 @@ __device__ __forceinline__ void stage_blocks(uint32_t rbase, int mi, int ri, int
       s0[k] = lut[c0[k]];
       s1[k] = lut[c1[k]];
     }
-    float part[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
     for (int k = 0; k < 4; ++k)
-      block_mma(r[k >> 1][2 * (k & 1)], r[k >> 1][2 * (k & 1) + 1], B[k], s0[k], s1[k], part[k & 1]);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[j] += part[0][j] + part[1][j];
+      block_mma(r[k >> 1][2 * (k & 1)], r[k >> 1][2 * (k & 1) + 1], B[k], s0[k], s1[k], acc);
   } else {
 #pragma unroll
   for (int p = 0; p < 2; ++p) {
@@ -294,7 +295,7 @@ template <bool GATEUP>
 __global__ void __launch_bounds__(kThreads, 1)
 fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = tc::smem_align1024(smem_raw);
   __shared__ __align__(8) uint64_t full_bar[kMaxRingStages], empty_bar[kMaxRingStages], sfull_bar[2],
       sempty_bar[2];
   __shared__ int abort_s;
@@ -311,7 +312,7 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.stages; ++i) {
       tc::mbar_init(tc::smem_u32(&full_bar[i]), 1);
-      tc::mbar_init(tc::smem_u32(&empty_bar[i]), kCW);
+      tc::mbar_init(tc::smem_u32(&empty_bar[i]), kCW * 32);   // every consumer lane arrives
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(tc::smem_u32(&sfull_bar[i]), 1);
@@ -352,9 +353,13 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
         ++its;
         for (int s = 0; s < nst; ++s) {
           if (!tc::mbar_wait(tc::smem_u32(&empty_bar[st]), ph ^ 1, abort, status)) break;
-          tc::mbar_arrive_expect_tx(tc::smem_u32(&full_bar[st]), kStageBytes);
-          tc::tma_load_2d(tc::smem_u32(smem + st * kStageBytes), &tmW, s * 128, (int)grow,
-                          tc::smem_u32(&full_bar[st]));
+          // only the boxes that start inside the row (kin / 2 bytes)
+          const int k0 = s * kBoxes * 128;
+          const int nbox = min(kBoxes, (a.kin / 2 - k0 + 127) / 128);
+          tc::mbar_arrive_expect_tx(tc::smem_u32(&full_bar[st]), (uint32_t)(nbox * kBoxBytes));
+          for (int j = 0; j < nbox; ++j)
+            tc::tma_load_2d(tc::smem_u32(smem + st * kStageBytes + j * kBoxBytes), &tmW, k0 + 128 * j,
+                            (int)grow, tc::smem_u32(&full_bar[st]));
           ++it;
           if (++st == a.stages) {
             st = 0;
@@ -428,14 +433,19 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
       if (ok && on) {
         const uint32_t rbase = tc::smem_u32(smem + st * kStageBytes) + (16 * tile + 8 * (mi & 1) + ri) * 128;
         const int nblk = min(kBlocksPerStage, L.nb - s * kBlocksPerStage);
-        const int gb0 = s * kBlocksPerStage + half;
-        if (nblk == kBlocksPerStage)
-          stage_blocks<true>(rbase, mi, ri, half, tg, sc0, sc1, lut, gb0, kBlocksPerStage, acc);
-        else
-          stage_blocks<false>(rbase, mi, ri, half, tg, sc0, sc1, lut, gb0, nblk, acc);
+#pragma unroll
+        for (int j = 0; j < kBoxes; ++j) {
+          const int nbj = min(kBlocksPerBox, nblk - j * kBlocksPerBox);
+          const int gb0 = s * kBlocksPerStage + j * kBlocksPerBox + half;
+          if (nbj == kBlocksPerBox)
+            stage_blocks<true>(rbase + j * kBoxBytes, mi, ri, half, tg, sc0, sc1, lut, gb0, kBlocksPerBox, acc);
+          else if (nbj > 0)
+            stage_blocks<false>(rbase + j * kBoxBytes, mi, ri, half, tg, sc0, sc1, lut, gb0, nbj, acc);
+        }
       }
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&empty_bar[st]));
+      // Each lane arrives once its own reads of the stage are done (its ldmatrix
+      // results have been consumed), so the stage needs no warp barrier first.
+      tc::mbar_arrive(tc::smem_u32(&empty_bar[st]));
       if (++st == a.stages) {
         st = 0;
         ph ^= 1;
@@ -531,7 +541,7 @@ int fp4_stream_stages(int kin) {
   const int fixed = f4_smem(kin, 0).total + 1024 + 1024;   // + base alignment + static smem
   int st = (optin - fixed) / kStageBytes;
   if (st > kMaxRingStages) st = kMaxRingStages;
-  return st >= 3 ? st : 0;
+  return st >= 2 ? st : 0;
 }
 
 template <bool GATEUP>

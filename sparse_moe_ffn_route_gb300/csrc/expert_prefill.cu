@@ -195,7 +195,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   constexpr int kTileB = L::kTileB;
   constexpr int kAB = L::kATiles * kTileA;     // offset of B in a stage
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = tc::smem_align1024(smem_raw);
   __shared__ __align__(8) uint64_t full_bar[kMaxStages], empty_bar[kMaxStages],
       bready_bar[kMaxStages], tfull_bar[2], tempty_bar[2], drain_bar;
   __shared__ uint32_t tmem_base_s;

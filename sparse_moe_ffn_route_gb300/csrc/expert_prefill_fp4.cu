@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmC,
                 const F4Gemm g) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = tc::smem_align1024(smem_raw);
   uint8_t* bring = smem + kLoadStages * kLoadStage;
   __shared__ __align__(8) uint64_t full_bar[kLoadStages], empty_bar[kLoadStages], bfull_bar[kBStages],
       bempty_bar[kBStages], tfull_bar, tempty_bar, drain_bar;
