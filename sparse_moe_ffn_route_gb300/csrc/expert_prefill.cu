@@ -56,9 +56,10 @@ struct Lay {
   static constexpr int kStageBytes =
       ((kATiles * kTileA + kTileB + kPacked + kScales + 1023) / 1024) * 1024;
   static constexpr int kStages = DUAL ? 3 : 4;
-  // bf16 down: each epilogue warp turns its 32 rows x 32 fp32 columns around in
-  // shared memory ([32][kEpiPitch] floats) so that its Y stores are whole lines
-  static constexpr bool kEpiStage = DUAL && !FP4;
+  // bf16 down and dense logits: each epilogue warp turns its 32 rows x 32 fp32
+  // columns around in shared memory ([32][kEpiPitch] floats) so that its stores are
+  // whole lines
+  static constexpr bool kEpiStage = !FP4;
   static constexpr int kEpiPitch = 36;
   static constexpr int kEpiBytes = kEpiStage ? 4 * 32 * kEpiPitch * 4 : 0;
   static constexpr int kSmemBytes = kStages * kStageBytes + kEpiBytes + 1024;   // + alignment slack
@@ -91,7 +92,10 @@ struct GemmArgs {
   int scale_nblk;         // MXFP4: 32-input blocks per weight row
   // kModeDense (router logits): A = x [rows, d], B = W_r [E, d]; no routing state
   int dense_rows;         // T
-  float* logits;          // [T, ldl] fp32
+  int nsplit;             // dense: the k range is cut into nsplit parts (split-K)
+  int dense_vec;          // dense: logits, ldl allow 16-byte stores (the staged epilogue)
+  size_t split_stride;    // dense: floats between the partial logits of two parts
+  float* logits;          // [T, ldl] fp32 (part s at logits + s * split_stride)
   int ldl;
   const uint16_t* rbias;  // bf16 [E] or null
 };
@@ -99,6 +103,7 @@ struct GemmArgs {
 struct Tile {
   int v, row0, n, cnt, kk;    // expert, first row within it, n tile, rows in this tile, k
   int nkc;                    // k chunks of 64
+  int kbeg, split;            // first k of the tile's range and its part (dense split-K)
   bool skip;
 };
 
@@ -109,12 +114,21 @@ __device__ __forceinline__ Tile tile_at(const GemmArgs& g, int t, int n_m) {
   Tile tl;
   const int m = t / g.nt_max;
   tl.n = t - m * g.nt_max;
+  tl.kbeg = 0;
+  tl.split = 0;
   if (g.mode == kModeDense) {
+    // nt_max counts (k part, n tile) pairs
+    const int nt = g.nt_max / g.nsplit;
+    tl.split = tl.n / nt;
+    tl.n -= tl.split * nt;
+    const int ks = g.k_routed / kBK;
+    const int kb0 = ks * tl.split / g.nsplit, kb1 = ks * (tl.split + 1) / g.nsplit;
     tl.v = 0;
     tl.row0 = m * kBM;
     tl.cnt = min(kBM, g.dense_rows - tl.row0);
-    tl.kk = g.k_routed;
-    tl.nkc = tl.kk / kBK;
+    tl.kbeg = kb0 * kBK;
+    tl.nkc = kb1 - kb0;
+    tl.kk = tl.nkc * kBK;
     tl.skip = false;
     return tl;
   }
@@ -179,6 +193,49 @@ __device__ __forceinline__ void dequant_stage(const uint8_t* packed, const uint8
     sp += step;
     bt += step * 128;
   }
+}
+
+// The staged epilogue: row index (or -1) of each of the 8 rows 4i + lane / 8 that
+// this lane stores, from `r`, the row index lane l holds for row l of its warp.
+__device__ __forceinline__ void turned_rows(int r, int lane, int (&ridx)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) ridx[i] = __shfl_sync(0xffffffffu, r, 4 * i + (lane >> 3));
+}
+
+// One 32 x 32 fp32 block of a warp's rows (lane l holds row l's 32 values in v) to
+// rows ridx[i] (negative: skipped) of `base`, `pitch` floats apart, columns col ..
+// col + min(32, ncol) - 1, plus a bf16 bias per column when `bias` is non-null.
+// The block turns around in stg ([32][PITCH] floats, conflict-free both ways) so
+// that lanes 8j..8j+7 store 128 contiguous bytes of one row: each store instruction
+// writes four whole lines instead of 32 partial ones.  base, pitch and col keep
+// every 16-byte store aligned (pitch and col multiples of 4).
+template <int PITCH>
+__device__ __forceinline__ void store_turned(float* stg, const float (&v)[32], const int (&ridx)[8], float* base,
+                                             size_t pitch, int col, int ncol, const uint16_t* bias, int lane) {
+  float4* wr = reinterpret_cast<float4*>(stg + lane * PITCH);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) wr[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  __syncwarp();
+  const int rr = lane >> 3, cc = (lane & 7) * 4;
+  if (cc < ncol) {
+    float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (bias) b4 = make_float4(bf16_to_f32(bias[cc]), bf16_to_f32(bias[cc + 1]), bf16_to_f32(bias[cc + 2]),
+                               bf16_to_f32(bias[cc + 3]));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (ridx[i] >= 0) {
+        float4 val = *reinterpret_cast<const float4*>(stg + (4 * i + rr) * PITCH + cc);
+        if (bias) {
+          val.x += b4.x;
+          val.y += b4.y;
+          val.z += b4.z;
+          val.w += b4.w;
+        }
+        *reinterpret_cast<float4*>(base + (size_t)ridx[i] * pitch + col + cc) = val;
+      }
+    }
+  }
+  __syncwarp();
 }
 
 // FP4: B comes from MXFP4 weights (tmB0: packed codes [rows, nblk*16] bytes, tmB1:
@@ -261,7 +318,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           const uint32_t fb = tc::smem_u32(&full_bar[s]);
           const uint32_t sa = tc::smem_u32(smem + s * kStageBytes);
           const uint32_t sb = sa + kAB;
-          const int k0 = kc * kBK;
+          const int k0 = tl.kbeg + kc * kBK;
           uint32_t bytes = (uint32_t)kAB;
           if (FP4) bytes += (uint32_t)g.N * 34u;          // codes (32 B) + 2 scales per row
           else bytes += (uint32_t)g.N * kBK * 2;
@@ -386,9 +443,24 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       const bool valid = row < tl.cnt;
       const int grow = (g.mode == kModeDense ? 0 : g.rs.offsets[tl.v]) + tl.row0 + row;   // grouped row
       const bool sh = (tl.v == g.E);
-      if (g.mode == kModeDense) {
-        // router logits of token grow, experts n*N .. n*N + N - 1 (+ bias)
-        float* lrow = valid ? g.logits + (size_t)grow * g.ldl : nullptr;
+      if (L::kEpiStage && g.mode == kModeDense && g.dense_vec) {
+        // router logits of token grow, experts n*N .. n*N + N - 1 (+ bias, in part 0)
+        int ridx[8];
+        turned_rows(valid ? grow : -1, lane, ridx);
+        const int e0 = tl.n * g.N;
+        const uint16_t* rbias = tl.split == 0 && g.rbias ? g.rbias + e0 : nullptr;
+        float* base = g.logits + tl.split * g.split_stride;
+        float* stg = reinterpret_cast<float*>(smem + kStages * kStageBytes) + q * 32 * L::kEpiPitch;
+        for (int c0 = 0; c0 < g.N; c0 += 32) {
+          float v[32];
+          tc::tmem_ld32(taddr + (uint32_t)c0, v);
+          store_turned<L::kEpiPitch>(stg, v, ridx, base, (size_t)g.ldl, e0 + c0, g.N - c0,
+                                     rbias ? rbias + c0 : nullptr, lane);
+        }
+      } else if (g.mode == kModeDense) {
+        // router logits of token grow, experts n*N .. n*N + N - 1 (+ bias, in part 0)
+        float* lrow = valid ? g.logits + tl.split * g.split_stride + (size_t)grow * g.ldl : nullptr;
+        const uint16_t* rbias = tl.split == 0 ? g.rbias : nullptr;
         const int e0 = tl.n * g.N;
         for (int c0 = 0; c0 < g.N; c0 += 32) {
           float v[32];
@@ -397,49 +469,21 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const int ncol = min(32, g.N - c0);
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              if (i < ncol) lrow[e0 + c0 + i] = v[i] + (g.rbias ? bf16_to_f32(g.rbias[e0 + c0 + i]) : 0.f);
+              if (i < ncol) lrow[e0 + c0 + i] = v[i] + (rbias ? bf16_to_f32(rbias[e0 + c0 + i]) : 0.f);
           }
         }
       } else if (L::kEpiStage && g.mode == kModeDown) {
-        // Lane l first holds row l of the warp's 32 rows; after the turn in shared
-        // memory, lanes 8j..8j+7 store 128 contiguous bytes of one row, so each store
-        // instruction writes four whole lines of Y instead of 32 partial ones.
-        float* stg = reinterpret_cast<float*>(smem + kStages * kStageBytes) + q * 32 * L::kEpiPitch;
         const int slot = valid ? g.rs.row2slot[grow] : -1;
-        const int rr = lane >> 3, cc = (lane & 7) * 4;
-        int rs_[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) rs_[i] = __shfl_sync(0xffffffffu, slot, 4 * i + rr);
+        int ridx[8];
+        turned_rows(slot, lane, ridx);
         const int o0 = tl.n * g.N;
         const uint16_t* bp = (!sh && g.dn_bias) ? g.dn_bias + (size_t)tl.v * g.d + o0 : nullptr;
+        float* stg = reinterpret_cast<float*>(smem + kStages * kStageBytes) + q * 32 * L::kEpiPitch;
         for (int c0 = 0; c0 < g.N; c0 += 32) {
           float v[32];
           tc::tmem_ld32(taddr + (uint32_t)c0, v);
-          float4* wr = reinterpret_cast<float4*>(stg + lane * L::kEpiPitch);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) wr[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-          __syncwarp();
-          if (c0 + cc < g.N) {
-            float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (bp) {
-              const uint16_t* bq = bp + c0 + cc;
-              b4 = make_float4(bf16_to_f32(bq[0]), bf16_to_f32(bq[1]), bf16_to_f32(bq[2]), bf16_to_f32(bq[3]));
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              if (rs_[i] >= 0) {
-                float4 val = *reinterpret_cast<const float4*>(stg + (4 * i + rr) * L::kEpiPitch + cc);
-                if (bp) {
-                  val.x += b4.x;
-                  val.y += b4.y;
-                  val.z += b4.z;
-                  val.w += b4.w;
-                }
-                *reinterpret_cast<float4*>(g.Y + (size_t)rs_[i] * g.d + o0 + c0 + cc) = val;
-              }
-            }
-          }
-          __syncwarp();
+          store_turned<L::kEpiPitch>(stg, v, ridx, g.Y, (size_t)g.d, o0 + c0, g.N - c0, bp ? bp + c0 : nullptr,
+                                     lane);
         }
       } else if (g.mode == kModeDown) {
         float* yrow = valid ? g.Y + (size_t)g.rs.row2slot[grow] * g.d : nullptr;
@@ -791,17 +835,43 @@ int router_n(int T, int E) {
 }
 
 cudaError_t launch_router_gemm(const uint16_t* x, int T, int d, const uint16_t* w_r, const uint16_t* bias,
-                               int E, float* logits, int ldl, uint32_t* status, cudaStream_t s) {
+                               int E, float* logits, int ldl, float* parts, size_t part_floats, int* nsplit,
+                               int* ppitch, uint32_t* status, cudaStream_t s) {
   GemmArgs g{};
   g.rs.status = status;
   g.E = 1;
   g.mode = kModeDense;
+  // Where there is room, the logits go to `parts` with a row pitch of E rounded up to
+  // 4 (whole-line stores from the staged epilogue).  Few m tiles: then one n tile as
+  // wide as possible (x is read once per k part) and the k range cut into parts until
+  // every SM has a tile; the select kernel adds the parts in order.  Otherwise the n
+  // tiles give the parallelism.
+  const int m_tiles = (T + kBM - 1) / kBM, sms = sm_count(), ks = d / kBK;
+  const int nwide = tile_n(E, Lay<false, false>::kMaxN);
+  const int ldp = (E + 3) / 4 * 4;
+  const bool use_parts = parts && (reinterpret_cast<uintptr_t>(parts) & 15) == 0 &&
+                         (size_t)T * ldp <= part_floats;
+  int ns = 1;
   g.N = router_n(T, E);
-  g.nt_routed = g.nt_max = E / g.N;
+  if (use_parts && nwide && (long long)m_tiles * (E / nwide) < sms) {
+    int want = min(sms / (m_tiles * (E / nwide)), min(8, ks));
+    while (want > 1 && (size_t)want * T * ldp > part_floats) --want;
+    if (want > 1) {
+      ns = want;
+      g.N = nwide;
+    }
+  }
+  *nsplit = ns;
+  *ppitch = use_parts ? ldp : 0;
+  g.nsplit = ns;
+  g.nt_routed = E / g.N;
+  g.nt_max = g.nt_routed * ns;
   g.k_routed = d;
   g.dense_rows = T;
-  g.logits = logits;
-  g.ldl = ldl;
+  g.logits = use_parts ? parts : logits;
+  g.ldl = use_parts ? ldp : ldl;
+  g.split_stride = (size_t)T * g.ldl;
+  g.dense_vec = use_parts ? 1 : 0;
   g.rbias = bias;
   CUtensorMap tA, tB;
   if (!make_map_bf16(&tA, x, (uint64_t)T, d, (uint64_t)d * 2, kBM)) return cudaErrorInvalidValue;

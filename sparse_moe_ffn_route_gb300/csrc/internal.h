@@ -99,19 +99,27 @@ cudaError_t launch_down_decode_fp4(const ExpertParams& p, const RouteState& rs, 
 // logits[t, e] (row stride ldl) = x_t . W_r[e] (+ bias[e]) for e < E, and, when
 // *gate_in_logits comes back true, x_t . wsh for e == E (else the select kernel
 // computes that dot itself).  The first kernel of a call: it clears *status.
+// With many tokens the logits may come back in `parts` (part_floats floats of
+// scratch): when *ppitch > 0, as *nsplit partial sums at parts + i * T * *ppitch
+// (row pitch *ppitch), which the select kernel adds in order; else in logits.
 cudaError_t launch_router_logits(const uint16_t* x, int T, int d, const uint16_t* w_r,
                                  const uint16_t* bias, const uint16_t* wsh, int E, float* logits,
-                                 int ldl, uint32_t* status, bool* gate_in_logits, cudaStream_t s);
+                                 int ldl, float* parts, size_t part_floats, int* nsplit, int* ppitch,
+                                 uint32_t* status, bool* gate_in_logits, cudaStream_t s);
 // Router logits of many tokens as a dense tcgen05 GEMM (expert_prefill.cu).
 bool router_gemm_supported(int T, int d, int E);
 cudaError_t launch_router_gemm(const uint16_t* x, int T, int d, const uint16_t* w_r, const uint16_t* bias,
-                               int E, float* logits, int ldl, uint32_t* status, cudaStream_t s);
+                               int E, float* logits, int ldl, float* parts, size_t part_floats, int* nsplit,
+                               int* ppitch, uint32_t* status, cudaStream_t s);
 
-// Top-k + routing weights from logits [T, ldl] (first E columns).  With has_shared,
-// the shared-gate logit is column E, or, when wsh is non-null, x_t . wsh computed
-// here (x bf16 [T, d]).  Writes any non-null output.
-cudaError_t launch_router_select(const float* logits, int ldl, int T, int E, int k,
-                                 int norm_topk_prob, float scale, int has_shared,
+// Top-k + routing weights from logits [T, ldl] (first E columns), given as nsplit
+// partial sums nstride floats apart that are added in order (lsum [T, ldsum], when
+// non-null, receives the sums).  With has_shared, the shared-gate logit is column
+// E, or, when wsh is non-null, x_t . wsh computed here (x bf16 [T, d]).  Writes any
+// non-null output.
+cudaError_t launch_router_select(const float* logits, int ldl, int nsplit, size_t nstride, float* lsum,
+                                 int ldsum, int T, int E, int k, int norm_topk_prob, float scale,
+                                 int has_shared,
                                  int32_t* ids_out, float* w_out, float* sgate_out,
                                  int32_t* slot_expert, float* slot_w, const uint16_t* x, int d,
                                  const uint16_t* wsh, cudaStream_t s);

@@ -254,14 +254,24 @@ int run_router(const moe_cfg_t* c, const void* x, int T, const moe_router_t* r,
     status = nullptr;
   }
   bool gate_in_logits = false;
+  // The expert outputs' region is free while routing runs: it may hold the router
+  // GEMM's partial logits (split-K over d).
+  const size_t part_floats = (size_t)L.S * (size_t)(c->d_model > L.ldh ? c->d_model : L.ldh);
+  int nsplit = 1, ppitch = 0;
   MOE_CUDA(launch_router_logits(xr, T, c->d_model, static_cast<const uint16_t*>(r->w),
                                 static_cast<const uint16_t*>(r->bias), wsh, c->n_experts, lg, ldl,
-                                status, &gate_in_logits, s));
+                                at<float>(ws, L.Y), part_floats, &nsplit, &ppitch, status, &gate_in_logits,
+                                s));
   if (fill_slots) MOE_CUDA(mark_phase(1, s));
   const int norm = c->gating == MOE_GATING_TOPK_SOFTMAX ? 1 : c->norm_topk_prob;
   int32_t* slot_e = fill_slots ? at<int32_t>(ws, L.slot_expert) : nullptr;
   float* slot_w = fill_slots ? at<float>(ws, L.slot_w) : nullptr;
-  MOE_CUDA(launch_router_select(lg, ldl, T, c->n_experts, c->top_k, norm,
+  // Logits in the scratch (possibly as partial sums): the select kernel adds them and
+  // writes the logits where the caller asked for them.
+  const bool scratch = ppitch > 0;
+  MOE_CUDA(launch_router_select(scratch ? at<float>(ws, L.Y) : lg, scratch ? ppitch : ldl, nsplit,
+                                (size_t)T * ppitch, scratch && logits_out ? lg : nullptr, ldl, T,
+                                c->n_experts, c->top_k, norm,
                                 c->expert_weights_scale, has_sh, ids_out, w_out, sgate_out, slot_e,
                                 slot_w, xr, c->d_model, gate_in_logits ? nullptr : wsh, s));
   if (fill_slots) MOE_CUDA(mark_phase(2, s));
@@ -416,7 +426,7 @@ int moe_topk_from_logits(const moe_cfg_t* cfg, const float* logits, int32_t T, i
   if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
   if (!aligned16(logits) || !aligned16(topk_ids) || !aligned16(topk_w)) return MOE_ERR_ALIGNMENT;
   const int norm = cfg->gating == MOE_GATING_TOPK_SOFTMAX ? 1 : cfg->norm_topk_prob;
-  if (launch_router_select(logits, cfg->n_experts, T, cfg->n_experts, cfg->top_k, norm,
+  if (launch_router_select(logits, cfg->n_experts, 1, 0, nullptr, 0, T, cfg->n_experts, cfg->top_k, norm,
                            cfg->expert_weights_scale, 0, topk_ids, topk_w, nullptr, nullptr,
                            nullptr, nullptr, 0, nullptr, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MOE_ERR_CUDA;

@@ -113,13 +113,29 @@ router_logits_kernel(const uint16_t* __restrict__ x, int T, int d, const uint16_
 
 constexpr int kSelectWarps = 8;
 
-// Warp per token.  Lane l holds logits l, l+32, ... (EPL per lane).  Each of the
-// k rounds takes the largest untaken logit, lowest index on equal values (the
-// selection sort's first-seen rule), via a butterfly argmax whose result lane 0
-// then broadcasts.  Lane j keeps the j-th pick.
+// Order-preserving unsigned key of a non-NaN logit: a > b exactly when key(a) >
+// key(b), and -0 takes +0's key (they compare equal).  Key 0 (a NaN's) is below
+// every logit and marks an absent or taken entry.
+__device__ __forceinline__ uint32_t logit_key(float f) {
+  uint32_t b = __float_as_uint(f);
+  if (b == 0x80000000u) b = 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_logit(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Warp per token.  Lane l holds logits l, l+32, ... (EPL per lane) and keeps the
+// best untaken one among them.  Each of the k rounds takes the largest untaken
+// logit, lowest index on equal values (the selection sort's first-seen rule): one
+// warp max over the lanes' best keys, one warp min over the indices that reach it;
+// the lane that gave up its entry then finds its next best.  Lane j keeps the j-th
+// pick.  (NaN logits are outside the routing's contract.)
 template <int EPL>
 __global__ void __launch_bounds__(kSelectWarps * 32)
-router_select_kernel(const float* __restrict__ logits, int ldl, int T, int E, int k,
+router_select_kernel(const float* __restrict__ logits, int ldl, int nsplit, size_t nstride,
+                     float* __restrict__ lsum, int ldsum, int T, int E, int k,
                      int norm_topk_prob, float scale, int has_shared, int32_t* __restrict__ ids_out,
                      float* __restrict__ w_out, float* __restrict__ sgate_out,
                      int32_t* __restrict__ slot_expert, float* __restrict__ slot_w,
@@ -136,37 +152,71 @@ router_select_kernel(const float* __restrict__ logits, int ldl, int T, int E, in
     const int e = lane + 32 * i;
     v[i] = e < E ? row[e] : 0.f;
   }
-  uint32_t taken = 0;
-  int my_id = -1;
-  float my_val = 0.f, top_val = 0.f;
-  for (int j = 0; j < k; ++j) {
-    int bi = -1;
-    float bv = 0.f;
+  if (nsplit > 1) {
+    // partial logits of the k parts, added in part order (three parts' loads at once)
+    for (int p0 = 1; p0 < nsplit; p0 += 3) {
+      float pv[3][EPL];
+#pragma unroll
+      for (int q = 0; q < 3; ++q) {
+        const float* rp = row + (size_t)(p0 + q) * nstride;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+          const int e = lane + 32 * i;
+          pv[q][i] = (p0 + q < nsplit && e < E) ? rp[e] : 0.f;
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 3; ++q) {
+        if (p0 + q >= nsplit) break;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) v[i] += pv[q][i];
+      }
+    }
+  }
+  if (lsum) {   // the logits themselves, when they were read from scratch
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
       const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u) && (bi < 0 || v[i] > bv)) {
-        bi = e;
-        bv = v[i];
-      }
+      if (e < E) lsum[(size_t)t * ldsum + e] = v[i];
     }
+  }
+  uint32_t key[EPL];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      if (oi >= 0 && (bi < 0 || ov > bv || (ov == bv && oi < bi))) {
-        bi = oi;
-        bv = ov;
-      }
+  for (int i = 0; i < EPL; ++i) key[i] = lane + 32 * i < E ? logit_key(v[i]) : 0u;
+  // this lane's best: the largest key, the lowest slot i on equal keys
+  uint32_t bk = 0u;
+  int bi = 0;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i)
+    if (key[i] > bk) {
+      bk = key[i];
+      bi = i;
     }
-    bi = __shfl_sync(0xffffffffu, bi, 0);
-    bv = __shfl_sync(0xffffffffu, bv, 0);
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+  int my_id = -1;
+  float my_val = 0.f, top_val = 0.f;
+  for (int j = 0; j < k; ++j) {
+    const uint32_t gk = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t gi = __reduce_min_sync(0xffffffffu, bk == gk ? (uint32_t)(lane + 32 * bi) : 0xffffffffu);
+    const float gv = key_logit(gk);
     if (lane == j) {
-      my_id = bi;
-      my_val = bv;
+      my_id = (int)gi;
+      my_val = gv;
     }
-    if (j == 0) top_val = bv;   // the largest logit overall
+    if (j == 0) top_val = gv;   // the largest logit overall
+    if ((int)(gi & 31u) == lane) {
+      // this lane's entry gi >> 5 is taken: its next best
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        if (i == (int)(gi >> 5)) key[i] = 0u;
+      bk = 0u;
+      bi = 0;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        if (key[i] > bk) {
+          bk = key[i];
+          bi = i;
+        }
+    }
   }
   // Routing weights.  Renormalised softmax over the chosen k equals
   // exp(l_j - l_top) / sum_chosen exp(l_i - l_top) (the full softmax's
@@ -195,14 +245,30 @@ router_select_kernel(const float* __restrict__ logits, int ldl, int T, int E, in
   }
   float sl = 0.f;   // the shared-gate logit: column E of the logits, or w_sh . x here
   if (has_shared && wsh) {
+    // pieces i = lane, lane + 32, ... in order, eight pieces' loads in flight at once
+    constexpr int kDotBatch = 8;
     const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * d);
     const uint4* wr = reinterpret_cast<const uint4*>(wsh);
-    for (int i = lane; i < d / 8; i += 32) {
-      const uint4 a = ldg_nc_v4(xr + i), b = ldg_nc_v4(wr + i);
-      sl = fmaf(bf16_lo(a.x), bf16_lo(b.x), sl); sl = fmaf(bf16_hi(a.x), bf16_hi(b.x), sl);
-      sl = fmaf(bf16_lo(a.y), bf16_lo(b.y), sl); sl = fmaf(bf16_hi(a.y), bf16_hi(b.y), sl);
-      sl = fmaf(bf16_lo(a.z), bf16_lo(b.z), sl); sl = fmaf(bf16_hi(a.z), bf16_hi(b.z), sl);
-      sl = fmaf(bf16_lo(a.w), bf16_lo(b.w), sl); sl = fmaf(bf16_hi(a.w), bf16_hi(b.w), sl);
+    for (int i0 = 0; 32 * i0 < d / 8; i0 += kDotBatch) {
+      uint4 xa[kDotBatch], wb[kDotBatch];
+#pragma unroll
+      for (int q = 0; q < kDotBatch; ++q) {
+        const int i = lane + 32 * (i0 + q);
+        xa[q] = wb[q] = make_uint4(0u, 0u, 0u, 0u);
+        if (i < d / 8) {
+          xa[q] = ldg_nc_v4(xr + i);
+          wb[q] = ldg_nc_v4(wr + i);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < kDotBatch; ++q) {
+        if (lane + 32 * (i0 + q) >= d / 8) break;
+        const uint4 a = xa[q], b = wb[q];
+        sl = fmaf(bf16_lo(a.x), bf16_lo(b.x), sl); sl = fmaf(bf16_hi(a.x), bf16_hi(b.x), sl);
+        sl = fmaf(bf16_lo(a.y), bf16_lo(b.y), sl); sl = fmaf(bf16_hi(a.y), bf16_hi(b.y), sl);
+        sl = fmaf(bf16_lo(a.z), bf16_lo(b.z), sl); sl = fmaf(bf16_hi(a.z), bf16_hi(b.z), sl);
+        sl = fmaf(bf16_lo(a.w), bf16_lo(b.w), sl); sl = fmaf(bf16_hi(a.w), bf16_hi(b.w), sl);
+      }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) sl += __shfl_xor_sync(0xffffffffu, sl, off);
@@ -249,14 +315,18 @@ __global__ void ingest_routing_kernel(const int32_t* __restrict__ ids, const flo
 
 cudaError_t launch_router_logits(const uint16_t* x, int T, int d, const uint16_t* w_r,
                                  const uint16_t* bias, const uint16_t* wsh, int E, float* logits,
-                                 int ldl, uint32_t* status, bool* gate_in_logits, cudaStream_t s) {
+                                 int ldl, float* parts, size_t part_floats, int* nsplit, int* ppitch,
+                                 uint32_t* status, bool* gate_in_logits, cudaStream_t s) {
   *gate_in_logits = wsh != nullptr;
+  *nsplit = 1;
+  *ppitch = 0;
   const int E1 = E + (wsh ? 1 : 0);
   if (T > 256 && router_gemm_supported(T, d, E)) {
     // a dense GEMM on tcgen05 over the routed experts; the shared-gate dot is left to
     // the select kernel
     *gate_in_logits = false;
-    return launch_router_gemm(x, T, d, w_r, bias, E, logits, ldl, status, s);
+    return launch_router_gemm(x, T, d, w_r, bias, E, logits, ldl, parts, part_floats, nsplit, ppitch, status,
+                              s);
   }
   if (T <= 256) {   // latency-bound: many small CTAs, all loads of a warp in flight at once
     dim3 grid((T + 15) / 16, (E1 + 15) / 16);
@@ -269,15 +339,17 @@ cudaError_t launch_router_logits(const uint16_t* x, int T, int d, const uint16_t
   }
 }
 
-cudaError_t launch_router_select(const float* logits, int ldl, int T, int E, int k,
-                                 int norm_topk_prob, float scale, int has_shared,
+cudaError_t launch_router_select(const float* logits, int ldl, int nsplit, size_t nstride, float* lsum,
+                                 int ldsum, int T, int E, int k, int norm_topk_prob, float scale,
+                                 int has_shared,
                                  int32_t* ids_out, float* w_out, float* sgate_out,
                                  int32_t* slot_expert, float* slot_w, const uint16_t* x, int d,
                                  const uint16_t* wsh, cudaStream_t s) {
   dim3 grid((T + kSelectWarps - 1) / kSelectWarps);
   const int epl = (E + 31) / 32;
 #define MOE_SELECT(N)                                                                     \
-  return launch_pdl(router_select_kernel<N>, grid, dim3(kSelectWarps * 32), 0, s, logits, ldl, T, \
+  return launch_pdl(router_select_kernel<N>, grid, dim3(kSelectWarps * 32), 0, s, logits, ldl, nsplit, \
+                    nstride, lsum, ldsum, T,                                                          \
                     E, k, norm_topk_prob, scale, has_shared, ids_out, w_out, sgate_out,       \
                     slot_expert, slot_w, x, d, wsh)
   if (epl <= 1) MOE_SELECT(1);

@@ -59,6 +59,8 @@ STAGED_SPECS = [
                    scale_hi=160), "all split groups, all two-multiply scales"),
     (mi.small_spec("gptoss", 320, 8, 4, 160, 0, 6, bias=("normal", 0.1), scale_lo=113,
                    scale_hi=140), "the fast range's two ends"),
+    (mi.small_spec("gptoss", 640, 8, 4, 576, 0, 6, bias=("normal", 0.1), scale_lo=110,
+                   scale_hi=140), "rows over 256 bytes: a last ring stage of one box"),
 ]
 
 
