@@ -163,8 +163,8 @@ def launches_per_step(plan, mxfp4, spec_slots):
     permute = 3 if spec_slots > 2048 else 1               # count, scan, scatter (or one CTA)
     if plan in (1, 2):                                    # decode: gate_up, down, combine
         return router + permute + 3
-    if plan == 3:                                         # (2 scale transposes) gather, 2 GEMMs, combine
-        return router + permute + 4 + (2 if mxfp4 else 0)
+    if plan == 3:                                         # 2 GEMMs, combine (MXFP4: 2 scale transposes, gather)
+        return router + permute + 3 + (3 if mxfp4 else 0)
     return router + permute + 7   # 2 scale preps, gather, gate_up, h fix-up, down, combine
 
 

@@ -64,7 +64,9 @@ struct Lay {
   static constexpr int kEpiBytes = kEpiStage ? 4 * 32 * kEpiPitch * 4 : 0;
   static constexpr int kSmemBytes = kStages * kStageBytes + kEpiBytes + 1024;   // + alignment slack
   static constexpr int kDequantWarps = FP4 ? 12 : 0;
-  static constexpr int kThreads = 192 + 32 * kDequantWarps;
+  // bf16 gate_up: 8 warps copy the A rows straight from x by row index (cp.async)
+  static constexpr int kLoadWarps = (!FP4 && !DUAL) ? 8 : 0;
+  static constexpr int kThreads = 192 + 32 * (kDequantWarps + kLoadWarps);
 };
 constexpr int kMaxStages = 4;
 
@@ -85,6 +87,9 @@ struct GemmArgs {
   const uint16_t* dn_bias;    // [E, d] or null
   int d, ff;
   uint16_t* h;            // gate_up output [S, 2*ldh]: bf16 (hi, lo) halves, grouped row order
+  int a_gather;           // gate_up (bf16): A rows copied from ax by row index, not by TMA
+  const uint16_t* ax;     // x [T, d] bf16; grouped row r is token row2slot[r] / aK
+  int aK;                 // slots per token
   int ldh;                // width of each half
   int dual;               // down: A = h_hi and h_lo tiles against the same B tile
   float* Y;               // down output [S, d] (slot order)
@@ -266,7 +271,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      tc::mbar_init(tc::smem_u32(&full_bar[s]), 1);
+      tc::mbar_init(tc::smem_u32(&full_bar[s]), 1 + (g.a_gather ? 128 : 0));   // TMA + one loader half
       tc::mbar_init(tc::smem_u32(&empty_bar[s]), 1);
       tc::mbar_init(tc::smem_u32(&bready_bar[s]), L::kDequantWarps ? L::kDequantWarps : 1);
     }
@@ -319,11 +324,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           const uint32_t sa = tc::smem_u32(smem + s * kStageBytes);
           const uint32_t sb = sa + kAB;
           const int k0 = tl.kbeg + kc * kBK;
-          uint32_t bytes = (uint32_t)kAB;
+          uint32_t bytes = g.a_gather ? 0u : (uint32_t)kAB;
           if (FP4) bytes += (uint32_t)g.N * 34u;          // codes (32 B) + 2 scales per row
           else bytes += (uint32_t)g.N * kBK * 2;
           tc::mbar_arrive_expect_tx(fb, bytes);
-          tc::tma_load_2d(sa, &tmA, k0, a_row, fb);
+          if (!g.a_gather) tc::tma_load_2d(sa, &tmA, k0, a_row, fb);
           if (DUAL) tc::tma_load_2d(sa + kTileA, &tmA, g.ldh + k0, a_row, fb);
           if (FP4) {
             const uint32_t sp = sb + (uint32_t)kTileB, ss = sp + (uint32_t)L::kPacked;
@@ -400,6 +405,64 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         volatile int* never = &zero;
         tc::mbar_wait(tc::smem_u32(&drain_bar), 0, never, status);
       }
+    }
+  } else if (L::kLoadWarps && warp >= 6) {
+    // ---------------------------------------------------------------- A rows by index
+    // Two halves of 128 threads take alternate k steps (half h the steps of parity h,
+    // counted over all of the CTA's tiles).  Thread lt of a half copies 16-byte chunk
+    // c = lt % 8 of rows lt / 8 + 16 j (j < 8) of the step's A tile: tile row r is x's
+    // row of the token of grouped row offsets[v] + row0 + r, stored where the 128-byte
+    // swizzle puts it (rows past the tile's count are zero-filled).  A step's copies
+    // are waited for when the half has issued its next step (so each half keeps two
+    // steps in flight, four in all; waiting further back would tie a step's
+    // announcement to the MMAs freeing the slot of a later step), then made visible to
+    // the tensor core's proxy and announced on the stage's full barrier (with the TMA's
+    // bytes of the weight tile).
+    if (g.a_gather) {
+      const int lt = (threadIdx.x - 192) & 127, half = (threadIdx.x - 192) >> 7;
+      const int c = lt & 7, rq = lt >> 3;
+      int step = 0, pending = -1;              // global k step; the half's unannounced step
+      for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
+        const Tile tl = tile_at(g, t, n_m);
+        if (tl.skip) continue;
+        const int base = g.rs.offsets[tl.v] + tl.row0;
+        const uint16_t* src[8];
+        uint32_t nb[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int r = rq + 16 * j;
+          const bool in = r < tl.cnt;
+          const int tok = in ? g.rs.row2slot[base + r] / g.aK : 0;
+          src[j] = g.ax + (size_t)tok * g.d + 8 * c;
+          nb[j] = in ? 16u : 0u;
+        }
+        bool ok = true;
+        for (int kc = 0; kc < tl.nkc; ++kc, ++step) {
+          if ((step & 1) != half) continue;
+          const int s = step % kStages;
+          if (!tc::mbar_wait(tc::smem_u32(&empty_bar[s]), ((step / kStages) & 1) ^ 1, abort, status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = tc::smem_u32(smem + s * kStageBytes);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int r = rq + 16 * j;
+            tc::cp_async16(sa + (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)), src[j] + kc * kBK, nb[j]);
+          }
+          tc::cp_async_commit();
+          if (pending >= 0) {
+            tc::cp_async_wait<1>();             // the half's previous step has landed
+            tc::fence_proxy_async_smem();
+            tc::mbar_arrive(tc::smem_u32(&full_bar[pending % kStages]));
+          }
+          pending = step;
+        }
+        if (!ok) break;
+      }
+      tc::cp_async_wait_all();
+      tc::fence_proxy_async_smem();
+      if (pending >= 0) tc::mbar_arrive(tc::smem_u32(&full_bar[pending % kStages]));
     }
   } else if (FP4 && warp >= 6) {
     // ---------------------------------------------------------------- MXFP4 dequant
@@ -764,8 +827,9 @@ cudaError_t launch_transpose_scales(const ExpertParams& p, uint8_t* scratch, cud
 }
 
 cudaError_t launch_gateup_prefill(const ExpertParams& p, int wfmt, int interleaved,
-                                  const RouteState& rs, const uint16_t* xp, int S, uint16_t* h,
-                                  int ldh, const uint8_t* scalesT, int max_mtiles, cudaStream_t s) {
+                                  const RouteState& rs, const uint16_t* xp, int S, const uint16_t* x, int T,
+                                  int K, uint16_t* h, int ldh, const uint8_t* scalesT, int max_mtiles,
+                                  cudaStream_t s) {
   const bool fp4 = wfmt == MOE_WFMT_MXFP4;
   const int nf = gateup_nf(p.ff, p.sff, interleaved, fp4 ? Lay<true, false>::kMaxN : Lay<false, false>::kMaxN);
   GemmArgs g{};
@@ -793,7 +857,14 @@ cudaError_t launch_gateup_prefill(const ExpertParams& p, int wfmt, int interleav
   CUtensorMap tA, tB0, tB1, tS0, tS1;
   std::memset(&tB1, 0, sizeof(tB1));
   const uint64_t rowb = (uint64_t)p.d * 2;
-  if (!make_map_bf16(&tA, xp, (uint64_t)S, p.d, rowb, kBM)) return cudaErrorInvalidValue;
+  // bf16 weights: the A rows come straight from x by row index (no gathered copy);
+  // MXFP4: from the gathered rows xp by TMA
+  g.a_gather = fp4 ? 0 : 1;
+  g.ax = x;
+  g.aK = K;
+  if (fp4 ? !make_map_bf16(&tA, xp, (uint64_t)S, p.d, rowb, kBM)
+          : !make_map_bf16(&tA, x, (uint64_t)T, p.d, rowb, kBM))
+    return cudaErrorInvalidValue;
   if (fp4) {
     const uint64_t rows = (uint64_t)p.E * 2 * p.ff;
     if (!make_map_u8(&tB0, p.gate_up, rows, (uint64_t)(p.d / 32) * 16, g.N, kBK / 2))

@@ -152,9 +152,13 @@ cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* row2slot, int S
 // MXFP4: bytes of the transposed-scale scratch, and the kernel that fills it.
 size_t prefill_scales_bytes(const ExpertParams& p, int wfmt);
 cudaError_t launch_transpose_scales(const ExpertParams& p, uint8_t* scratch, cudaStream_t s);
+// gate_up over the grouped rows: A rows come from xp (the gathered x rows, MXFP4
+// weights) or, with bf16 weights, straight from x [T, d] by row index (grouped row r
+// is token row2slot[r] / K), so that no gathered copy is needed.
 cudaError_t launch_gateup_prefill(const ExpertParams& p, int wfmt, int interleaved,
-                                  const RouteState& rs, const uint16_t* xp, int S, uint16_t* h,
-                                  int ldh, const uint8_t* scalesT, int max_mtiles, cudaStream_t s);
+                                  const RouteState& rs, const uint16_t* xp, int S, const uint16_t* x, int T,
+                                  int K, uint16_t* h, int ldh, const uint8_t* scalesT, int max_mtiles,
+                                  cudaStream_t s);
 cudaError_t launch_down_prefill(const ExpertParams& p, int wfmt, const RouteState& rs,
                                 const uint16_t* h, int ldh, int S, float* Y,
                                 const uint8_t* scalesT, int max_mtiles, cudaStream_t s);

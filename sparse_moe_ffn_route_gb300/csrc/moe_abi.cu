@@ -79,7 +79,7 @@ bool make_layout(const moe_cfg_t* c, int T, Layout* L) {
   L->prefill = path_for(c, T) == MOE_PATH_PREFILL &&
                prefill_supported(c->d_model, c->expert_ff, c->shared_ff, c->wfmt,
                                  c->interleaved_gate_up);
-  L->xp = take(L->prefill ? 2 * Sz * d : 0);
+  L->xp = take(L->prefill && c->wfmt == MOE_WFMT_MXFP4 ? 2 * Sz * d : 0);   // gathered x rows (MXFP4)
   {
     ExpertParams sp{};
     sp.E = c->n_experts;
@@ -319,18 +319,22 @@ int run_experts(const moe_cfg_t* c, const void* x_layer, int T, const moe_expert
     return MOE_OK;
   }
   if (L.prefill) {
-    // Grouped GEMMs on tcgen05: m tiles of 128 rows; A rows of gate_up gathered first.
+    // Grouped GEMMs on tcgen05: m tiles of 128 rows.  With MXFP4 weights the A rows of
+    // gate_up are gathered first; bf16 gate_up reads them from x by row index.
     constexpr int kTileRows = 128;
     const int max_mtiles = L.E1 + (L.S + kTileRows - 1) / kTileRows;
+    const bool fp4 = c->wfmt == MOE_WFMT_MXFP4;
     uint16_t* xp = at<uint16_t>(ws, L.xp);
     uint8_t* scalesT = at<uint8_t>(ws, L.scalesT);
-    if (c->wfmt == MOE_WFMT_MXFP4) MOE_CUDA(launch_transpose_scales(p, scalesT, s));
+    if (fp4) MOE_CUDA(launch_transpose_scales(p, scalesT, s));
     MOE_CUDA(launch_permute(rs, L.S, L.E1, kTileRows, at<int>(ws, L.hist), s));
-    MOE_CUDA(launch_gather_rows(static_cast<const uint16_t*>(x), rs.row2slot, L.S, L.K,
-                                c->d_model, xp, s));
+    if (fp4)
+      MOE_CUDA(launch_gather_rows(static_cast<const uint16_t*>(x), rs.row2slot, L.S, L.K,
+                                  c->d_model, xp, s));
     MOE_CUDA(mark_phase(3, s));
-    MOE_CUDA(launch_gateup_prefill(p, c->wfmt, c->interleaved_gate_up, rs, xp, L.S, h, L.ldh,
-                                   scalesT, max_mtiles, s));
+    MOE_CUDA(launch_gateup_prefill(p, c->wfmt, c->interleaved_gate_up, rs, xp, L.S,
+                                   static_cast<const uint16_t*>(x), T, L.K, h, L.ldh, scalesT,
+                                   max_mtiles, s));
     MOE_CUDA(mark_phase(4, s));
     MOE_CUDA(launch_down_prefill(p, c->wfmt, rs, h, L.ldh, L.S, Y, scalesT, max_mtiles, s));
     MOE_CUDA(mark_phase(5, s));
