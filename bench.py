@@ -252,6 +252,21 @@ def run_reference(args, rank, world):
     }), flush=True)
 
 
+def max_over_ranks(x, world, dev):
+    """The largest x over the ranks (the slowest replica's time); x itself alone."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(tokens, ms, world):
+    """Whole-job tokens/s: every replica's T tokens over the slowest replica's step time."""
+    return world * tokens / (ms / 1e3)
+
+
 def config_of(spec):
     return {"workload": spec.name, "tokens": spec.tokens, "d_model": spec.d_model,
             "n_experts": spec.n_experts, "top_k": spec.top_k, "expert_ff": spec.expert_ff,
@@ -336,12 +351,8 @@ def run_ours(args, rank, world, local_rank):
     sampler.stop()
 
     step_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    ms = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * T / (ms / 1e3)
+    ms = max_over_ranks(statistics.mean(step_ms), world, dev)
+    value = job_rate(T, ms, world)
 
     # The same step captured once in a CUDA graph and replayed (how a serving loop
     # would drive it): launch work leaves the critical path.
@@ -362,12 +373,8 @@ def run_ours(args, rank, world, local_rank):
             graph.replay()
             g_evs[i][1].record()
         torch.cuda.synchronize()
-        g_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in g_evs)
-        if world > 1:
-            t = torch.tensor([g_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            g_ms = float(t.item())
-        graph_rec = {"ms_per_step": g_ms, "value": world * T / (g_ms / 1e3), "unit": "tokens/s",
+        g_ms = max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in g_evs), world, dev)
+        graph_rec = {"ms_per_step": g_ms, "value": job_rate(T, g_ms, world), "unit": "tokens/s",
                      "note": "one captured moe_ffn_forward replayed per step, L2 flushed between"}
 
     # end to end through the host-buffer entry point: pinned x in, pinned y out
@@ -387,12 +394,8 @@ def run_ours(args, rank, world, local_rank):
             a = time.perf_counter()
             moe.moe_ffn_forward_host(cfg, x_host, router, experts, shared, y_host=y_host, ws=ws)
             te.append(time.perf_counter() - a)
-        e_ms = 1e3 * statistics.mean(te)
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * T / (e_ms / 1e3), "unit": "tokens/s",
+        e_ms = max_over_ranks(1e3 * statistics.mean(te), world, dev)
+        e2e = {"value": job_rate(T, e_ms, world), "unit": "tokens/s",
                "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": y_host.numel() * 2,
                "ms_per_step": e_ms}
 
