@@ -6,7 +6,8 @@
 // 2^38 of its largest keep every bit they have in bf16 (x) or 11 bits (h).  The
 // matching 2^-e is applied in the consumer's epilogue.
 //
-//   gather_rows_f16_kernel: x rows of the grouped order -> f16, rowmul[r] = 2^-e;
+//   gather_rows_f16_kernel: x rows of the grouped order -> f16 (one pass, the row held
+//                           in registers), rowmul[r] = 2^-e;
 //                           also clears the per-row maxima that the gate_up
 //                           epilogue accumulates for h.
 //   h_fix_f16_kernel:       h rows, written by the gate_up epilogue as f16 times a
@@ -28,6 +29,25 @@ __device__ __forceinline__ int row_exp_from_field(int ex, bool zero) {
   return min(141 - ex, 126);
 }
 
+// The f16 row of bf16 values v (8 per 16-byte unit) times sc.
+__device__ __forceinline__ uint4 scaled_f16x8(const uint4& v, float sc) {
+  uint4 o;
+  o.x = pack_f16x2(bf16_lo(v.x) * sc, bf16_hi(v.x) * sc);
+  o.y = pack_f16x2(bf16_lo(v.y) * sc, bf16_hi(v.y) * sc);
+  o.z = pack_f16x2(bf16_lo(v.z) * sc, bf16_hi(v.z) * sc);
+  o.w = pack_f16x2(bf16_lo(v.w) * sc, bf16_hi(v.w) * sc);
+  return o;
+}
+
+__device__ __forceinline__ uint32_t max_abs_bf16x8(const uint4& v) {
+  const uint32_t mk = 0x7FFF7FFFu;
+  return __vmaxu2(__vmaxu2(v.x & mk, v.y & mk), __vmaxu2(v.z & mk, v.w & mk));
+}
+
+// Warp per grouped row.  UNITS > 0: the row (at most 32 * UNITS 16-byte units) is
+// loaded into registers at once (one round trip), its largest magnitude found and the
+// row converted from the registers; UNITS == 0: any width, two passes over the row.
+template <int UNITS>
 __global__ void __launch_bounds__(256)
 gather_rows_f16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ row2slot, int S, int K,
                        int d, uint16_t* __restrict__ xp, float* __restrict__ rowmul,
@@ -38,24 +58,32 @@ gather_rows_f16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict
   for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < S; r += (gridDim.x * blockDim.x) >> 5) {
     const int t = row2slot[r] / K;
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d);
-    uint32_t m2 = 0;
-    for (int i = lane; i < nvec; i += 32) {
-      const uint4 v = ldg_nc_v4(src + i);
-      const uint32_t mk = 0x7FFF7FFFu;
-      m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(v.x & mk, v.y & mk), __vmaxu2(v.z & mk, v.w & mk)));
-    }
-    const uint32_t m = __reduce_max_sync(0xffffffffu, max(m2 & 0xffffu, m2 >> 16));
-    const int e = row_exp_from_field((int)(m >> 7), m == 0);       // bf16 exponent field
-    const float sc = exp2i(e);
     uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)r * d);
-    for (int i = lane; i < nvec; i += 32) {
-      const uint4 v = ldg_nc_v4(src + i);
-      uint4 o;
-      o.x = pack_f16x2(bf16_lo(v.x) * sc, bf16_hi(v.x) * sc);
-      o.y = pack_f16x2(bf16_lo(v.y) * sc, bf16_hi(v.y) * sc);
-      o.z = pack_f16x2(bf16_lo(v.z) * sc, bf16_hi(v.z) * sc);
-      o.w = pack_f16x2(bf16_lo(v.w) * sc, bf16_hi(v.w) * sc);
-      dst[i] = o;
+    uint32_t m2 = 0;
+    int e;
+    if (UNITS > 0) {
+      uint4 v[UNITS > 0 ? UNITS : 1];
+#pragma unroll
+      for (int j = 0; j < UNITS; ++j) {
+        const int i = lane + 32 * j;
+        v[j] = i < nvec ? ldg_nc_v4(src + i) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int j = 0; j < UNITS; ++j) m2 = __vmaxu2(m2, max_abs_bf16x8(v[j]));
+      const uint32_t m = __reduce_max_sync(0xffffffffu, max(m2 & 0xffffu, m2 >> 16));
+      e = row_exp_from_field((int)(m >> 7), m == 0);                // bf16 exponent field
+      const float sc = exp2i(e);
+#pragma unroll
+      for (int j = 0; j < UNITS; ++j) {
+        const int i = lane + 32 * j;
+        if (i < nvec) dst[i] = scaled_f16x8(v[j], sc);
+      }
+    } else {
+      for (int i = lane; i < nvec; i += 32) m2 = __vmaxu2(m2, max_abs_bf16x8(ldg_nc_v4(src + i)));
+      const uint32_t m = __reduce_max_sync(0xffffffffu, max(m2 & 0xffffu, m2 >> 16));
+      e = row_exp_from_field((int)(m >> 7), m == 0);
+      const float sc = exp2i(e);
+      for (int i = lane; i < nvec; i += 32) dst[i] = scaled_f16x8(ldg_nc_v4(src + i), sc);
     }
     if (lane == 0) {
       rowmul[r] = exp2i(-e);
@@ -101,7 +129,17 @@ int grid_rows(int S) {
 
 cudaError_t launch_gather_rows_f16(const uint16_t* x, const int32_t* row2slot, int S, int K, int d, uint16_t* xp16,
                                    float* rowmul, uint32_t* hmax, cudaStream_t s) {
-  return launch_pdl(gather_rows_f16_kernel, dim3(grid_rows(S)), dim3(256), 0, s, x, row2slot, S, K, d, xp16,
+  const int units = (d / 8 + 31) / 32;   // 16-byte units per lane
+  if (units <= 8)
+    return launch_pdl(gather_rows_f16_kernel<8>, dim3(grid_rows(S)), dim3(256), 0, s, x, row2slot, S, K, d,
+                      xp16, rowmul, hmax);
+  if (units <= 12)
+    return launch_pdl(gather_rows_f16_kernel<12>, dim3(grid_rows(S)), dim3(256), 0, s, x, row2slot, S, K, d,
+                      xp16, rowmul, hmax);
+  if (units <= 16)
+    return launch_pdl(gather_rows_f16_kernel<16>, dim3(grid_rows(S)), dim3(256), 0, s, x, row2slot, S, K, d,
+                      xp16, rowmul, hmax);
+  return launch_pdl(gather_rows_f16_kernel<0>, dim3(grid_rows(S)), dim3(256), 0, s, x, row2slot, S, K, d, xp16,
                     rowmul, hmax);
 }
 
