@@ -35,7 +35,8 @@ namespace moe {
 namespace {
 
 constexpr int kTiles = 8;                         // 16-row MMA tiles per unit
-constexpr int kCW = 2 * kTiles;                   // consumer warps: two per tile (even / odd blocks)
+constexpr int kClasses = 4;                       // block classes (block index mod 4)
+constexpr int kCW = kTiles / 2 * kClasses;        // consumer warps: one per (tile pair, block class)
 constexpr int kThreads = (kCW + 1) * 32;          // + the producer warp
 constexpr int kRows = 16 * kTiles;                // weight rows per unit
 constexpr int kBoxBytes = kRows * 128;            // one TMA box: 128 rows x 128 bytes of codes
@@ -70,8 +71,8 @@ __host__ __device__ inline F4Smem f4_smem(int kin, int stages) {
   m.ring = 0;
   m.scales = stages * kStageBytes;
   m.lut = m.scales + 2 * m.scale_bytes;
-  m.part = m.lut + 256 * 4;                        // odd-block partial sums [kTiles][32][4]
-  m.tok = m.part + kTiles * 32 * 16;
+  m.part = m.lut + 256 * 4;                        // partial sums [pair][class][tile][32][4]
+  m.tok = m.part + kCW * 2 * 32 * 16;
   m.total = m.tok + kTokens * m.pitch;
   return m;
 }
@@ -89,9 +90,9 @@ __device__ __forceinline__ void consumers_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kCW * 32) : "memory");
 }
 
-// Barrier between the two warps of one tile (named barriers 2 .. 2 + kTiles - 1).
-__device__ __forceinline__ void pair_sync(int tile) {
-  asm volatile("bar.sync %0, 64;" ::"r"(2 + tile) : "memory");
+// Barrier among the four warps of one tile pair (named barriers 2 .. 2 + kTiles / 2 - 1).
+__device__ __forceinline__ void quad_sync(int tp) {
+  asm volatile("bar.sync %0, %1;" ::"r"(2 + tp), "n"(kClasses * 32) : "memory");
 }
 
 // volatile: it reads shared memory that an mbarrier wait (volatile asm) made valid,
@@ -205,11 +206,9 @@ __device__ __forceinline__ void mma_f16_zero(float (&d)[4], uint32_t a0, uint32_
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
 }
 
-// The blocks b = half, half + 2, half + 4, half + 6 (< nblk) of one stage for one
-// tile: acc += 2^(s - 127) * (block's codes x token rows), per block.  rbase: the
-// lane's ldmatrix row in the stage; gb0: global block index of block `half`.
-// Block k of the four is b = half + 2k; matrix pair p = k / 2 of the ldmatrix loads
-// holds rows g / g+8 of blocks half + 4p and half + 4p + 2.
+// One 32-input block of one 16-row tile: wa / wb are this lane's code bytes of rows
+// g and g + 8, B its token fragment, s0 / s1 the rows' block scales 2^(s - 127):
+// the block's two k16 MMAs give a fresh product, which is scaled into acc.
 __device__ __forceinline__ void block_mma(const uint32_t wa, const uint32_t wb, const uint4& B, float s0,
                                           float s1, float (&acc)[4]) {
   uint32_t fa[4], fb[4];
@@ -224,49 +223,58 @@ __device__ __forceinline__ void block_mma(const uint32_t wa, const uint32_t wb, 
   acc[3] = fmaf(s1, tt[3], acc[3]);
 }
 
+// Blocks q and q + 4 (those below nblk) of one box for the two tiles of a pair:
+// acc[t] += 2^(s - 127) * (block's codes x token rows), per block.  rbase: the lane's
+// ldmatrix row in the box for the pair's first tile (the second's is 16 rows on);
+// sc: the scale bytes of row g of the first tile; gb0: global block index of block q.
+// One x4 ldmatrix per tile hands lane (g, c) the code bytes 4c..4c+3 of rows g and
+// g + 8 of both blocks; the token fragments of a block serve both tiles.
 template <bool FULL>
-__device__ __forceinline__ void stage_blocks(uint32_t rbase, int mi, int ri, int half, const uint8_t* tg,
-                                             const uint8_t* sc0, const uint8_t* sc1, const float* lut,
-                                             int gb0, int nblk, float (&acc)[4]) {
+__device__ __forceinline__ void box_pair(uint32_t rbase, int mi, int ri, int q, const uint8_t* tg, const uint8_t* sc,
+                                         int nb, const float* lut, int gb0, int nblk, float (&acc)[2][4]) {
   if (FULL) {
-    // every operand of the four blocks first, so that their latencies overlap
+    // every operand first, so that their latencies overlap
     uint32_t r[2][4];
 #pragma unroll
-    for (int p = 0; p < 2; ++p)
-      ldmatrix_x4(rbase + ((uint32_t)((half + 4 * p + 2 * (mi >> 1)) ^ ri) << 4), r[p]);
-    uint4 B[4];
-    uint32_t c0[4], c1[4];
+    for (int t = 0; t < 2; ++t) ldmatrix_x4(rbase + t * 16 * 128 + ((uint32_t)((q + 4 * (mi >> 1)) ^ ri) << 4), r[t]);
+    uint4 B[2];
+    uint32_t cb[2][2][2];                         // [tile][block][row g / g + 8]
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      B[k] = *reinterpret_cast<const uint4*>(tg + 64 * (gb0 + 2 * k));
-      c0[k] = sc0[gb0 + 2 * k];
-      c1[k] = sc1[gb0 + 2 * k];
+    for (int k = 0; k < 2; ++k) {
+      B[k] = *reinterpret_cast<const uint4*>(tg + 64 * (gb0 + 4 * k));
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        cb[t][k][0] = sc[16 * t * nb + gb0 + 4 * k];
+        cb[t][k][1] = sc[(16 * t + 8) * nb + gb0 + 4 * k];
+      }
     }
-    float s0[4], s1[4];
+    float sv[2][2][2];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      s0[k] = lut[c0[k]];
-      s1[k] = lut[c1[k]];
-    }
+    for (int t = 0; t < 2; ++t)
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-      block_mma(r[k >> 1][2 * (k & 1)], r[k >> 1][2 * (k & 1) + 1], B[k], s0[k], s1[k], acc);
+      for (int k = 0; k < 2; ++k) {
+        sv[t][k][0] = lut[cb[t][k][0]];
+        sv[t][k][1] = lut[cb[t][k][1]];
+      }
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+#pragma unroll
+      for (int t = 0; t < 2; ++t) block_mma(r[t][2 * k], r[t][2 * k + 1], B[k], sv[t][k][0], sv[t][k][1], acc[t]);
   } else {
 #pragma unroll
-  for (int p = 0; p < 2; ++p) {
-    if (half + 4 * p < nblk) {
+    for (int t = 0; t < 2; ++t) {
+      if (q >= nblk) break;
       uint32_t r[4];
-      ldmatrix_x4(rbase + ((uint32_t)((half + 4 * p + 2 * (mi >> 1)) ^ ri) << 4), r);
+      ldmatrix_x4(rbase + t * 16 * 128 + ((uint32_t)((q + 4 * (mi >> 1)) ^ ri) << 4), r);
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        if (half + 4 * p + 2 * q < nblk) {
-          const int gb = gb0 + 4 * p + 2 * q;
+      for (int k = 0; k < 2; ++k) {
+        if (q + 4 * k < nblk) {
+          const int gb = gb0 + 4 * k;
           const uint4 B = *reinterpret_cast<const uint4*>(tg + 64 * gb);
-          block_mma(r[2 * q], r[2 * q + 1], B, lut[sc0[gb]], lut[sc1[gb]], acc);
+          block_mma(r[2 * k], r[2 * k + 1], B, lut[sc[16 * t * nb + gb]], lut[sc[(16 * t + 8) * nb + gb]], acc[t]);
         }
       }
     }
-  }
   }
 }
 
@@ -383,15 +391,16 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
   }
 
   // -------------------------------------------------------------- consumers
-  // Warp w owns tile w % kTiles (rows 16 tile .. 16 tile + 15 of the unit) and the
-  // blocks of parity w / kTiles of every stage: the pair of warps of one tile runs two
-  // independent chains, and the odd-block warp hands its sums over at the unit's end.
-  const int tile = warp % kTiles, half = warp / kTiles;
+  // Warp w owns tile pair tp = w % 4 (rows 32 tp .. 32 tp + 31 of the unit) and the
+  // blocks of class q = w / 4 (block index mod 4) of every box: a block's token
+  // fragments serve both tiles.  At the unit's end the four warps of a pair add their
+  // sums in shared memory, and warps q = 0, 1 finish tiles 2 tp and 2 tp + 1.
+  const int tp = warp % (kTiles / 2), q = warp / (kTiles / 2);
   const int g = lane >> 2, c = lane & 3;
   const int mi = lane >> 3, ri = lane & 7;        // this lane's ldmatrix address: matrix, row
   uint8_t* tok = smem + L.tok;
   const uint8_t* tg = tok + g * L.pitch + 16 * c; // token column g, inputs 8c.. of each block
-  float4* part = reinterpret_cast<float4*>(smem + L.part) + tile * 32 + lane;
+  float4* part = reinterpret_cast<float4*>(smem + L.part) + (tp * kClasses) * 2 * 32 + lane;
   int st = 0, its = 0, cur = -1;               // ring slot, scale loads consumed, staged item
   uint32_t ph = 0;                               // phase parity of ring slot st
   for (int u = u0; u < u1; ++u) {
@@ -422,25 +431,24 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
       cur = ai;
     }
     const int row0 = t * kRows, nrows = min(kRows, a.R - row0);
-    const bool on = 16 * tile < nrows;           // nrows is a multiple of 32
+    const bool on = 32 * tp < nrows;             // nrows is a multiple of 32
     const int sb = its & 1;
     bool ok = tc::mbar_wait(tc::smem_u32(&sfull_bar[sb]), (its >> 1) & 1, abort, status);
-    const uint8_t* sc0 = smem + L.scales + sb * L.scale_bytes + (16 * tile + g) * L.nb;
-    const uint8_t* sc1 = sc0 + 8 * L.nb;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint8_t* sc = smem + L.scales + sb * L.scale_bytes + (32 * tp + g) * L.nb;
+    float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     for (int s = 0; s < nst; ++s) {
       ok = ok && tc::mbar_wait(tc::smem_u32(&full_bar[st]), ph, abort, status);
       if (ok && on) {
-        const uint32_t rbase = tc::smem_u32(smem + st * kStageBytes) + (16 * tile + 8 * (mi & 1) + ri) * 128;
+        const uint32_t rbase = tc::smem_u32(smem + st * kStageBytes) + (32 * tp + 8 * (mi & 1) + ri) * 128;
         const int nblk = min(kBlocksPerStage, L.nb - s * kBlocksPerStage);
 #pragma unroll
         for (int j = 0; j < kBoxes; ++j) {
           const int nbj = min(kBlocksPerBox, nblk - j * kBlocksPerBox);
-          const int gb0 = s * kBlocksPerStage + j * kBlocksPerBox + half;
+          const int gb0 = s * kBlocksPerStage + j * kBlocksPerBox + q;
           if (nbj == kBlocksPerBox)
-            stage_blocks<true>(rbase + j * kBoxBytes, mi, ri, half, tg, sc0, sc1, lut, gb0, kBlocksPerBox, acc);
+            box_pair<true>(rbase + j * kBoxBytes, mi, ri, q, tg, sc, L.nb, lut, gb0, kBlocksPerBox, acc2);
           else if (nbj > 0)
-            stage_blocks<false>(rbase + j * kBoxBytes, mi, ri, half, tg, sc0, sc1, lut, gb0, nbj, acc);
+            box_pair<false>(rbase + j * kBoxBytes, mi, ri, q, tg, sc, L.nb, lut, gb0, nbj, acc2);
         }
       }
       // Each lane arrives once its own reads of the stage are done (its ldmatrix
@@ -455,18 +463,25 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
     if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sempty_bar[sb]));
     ++its;
     if (!on) continue;
-    // the odd-block warp of the tile hands its sums to the even-block warp
-    if (half) *part = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    pair_sync(tile);
-    if (!half) {
-      const float4 o = *part;
-      acc[0] += o.x;
-      acc[1] += o.y;
-      acc[2] += o.z;
-      acc[3] += o.w;
+    // the pair's four block classes add up in class order; warp q < 2 takes tile 2 tp + q
+#pragma unroll
+    for (int t2 = 0; t2 < 2; ++t2)
+      part[(q * 2 + t2) * 32] = make_float4(acc2[t2][0], acc2[t2][1], acc2[t2][2], acc2[t2][3]);
+    quad_sync(tp);
+    const int tile = 2 * tp + (q & 1);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (q < 2) {
+#pragma unroll
+      for (int qq = 0; qq < kClasses; ++qq) {
+        const float4 o = part[(qq * 2 + q) * 32];
+        acc[0] += o.x;
+        acc[1] += o.y;
+        acc[2] += o.z;
+        acc[3] += o.w;
+      }
     }
-    pair_sync(tile);                             // read before the next unit writes
-    if (half || !ok) continue;
+    quad_sync(tp);                               // read before the next unit writes
+    if (q >= 2 || !ok) continue;
 
     // ------------------------------------------------------------ epilogue
     // acc: rows g (tokens 2c, 2c+1) and g+8 of the tile, times 2^e of the token.
