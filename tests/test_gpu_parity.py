@@ -66,6 +66,12 @@ ROUTE_SPECS = [
     mi.small_spec("qwen", 64, 8, 2, 32, 32, 33, bias=None),
     mi.small_spec("qwen", 128, 40, 6, 32, 64, 17, bias=("normal", 0.5)),
     mi.small_spec("gptoss", 96, 12, 3, 64, 0, 31, bias=("normal", 0.1)),
+    # more than 256 tokens: the tensor-core logits GEMM, its k range cut into parts
+    # (4 and 3 here) that the select kernel adds; with and without the shared gate
+    mi.small_spec("qwen", 256, 32, 4, 32, 64, 300, bias=("normal", 0.5)),
+    mi.small_spec("gptoss", 192, 16, 4, 64, 0, 520, bias=("normal", 0.1)),
+    # enough m tiles for every SM: one part, still through the scratch
+    mi.small_spec("qwen", 128, 16, 2, 32, 32, 19500, bias=("normal", 0.5)),
 ]
 
 
