@@ -229,7 +229,7 @@ def moe_select_path(cfg: MoeCfg, T: int) -> int:
 
 PLAN_DECODE_WARP, PLAN_DECODE_RING, PLAN_PREFILL_BF16, PLAN_PREFILL_F16 = 1, 2, 3, 4
 PLAN_NAMES = {1: "decode: warp MMAs, register-held weight loads",
-              2: "decode: warp MMAs, TMA-fed MXFP4 weight ring",
+              2: "decode: warp MMAs, TMA-fed weight ring",
               3: "prefill: tcgen05 grouped GEMMs, bf16 operands",
               4: "prefill: tcgen05 grouped GEMMs, f16 operands (MXFP4, two m tiles per weight tile)"}
 

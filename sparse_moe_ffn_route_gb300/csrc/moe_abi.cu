@@ -203,10 +203,15 @@ int decode_chunks(const moe_cfg_t* c, int T) {
   return 4LL * T * c->top_k <= 16LL * c->n_experts ? 1 : 4;
 }
 
-// Decode path: one-chunk MXFP4 items take the TMA-fed ring kernels (which fall back to
-// the register-stream ones only if the device lacks the shared memory they need).
+// Decode path: one-chunk items take the TMA-fed ring kernels (which fall back to the
+// register-stream ones only if the device lacks the shared memory they need): MXFP4
+// weights, and bf16 weights in the separate gate / up layout with d, ff, sff
+// multiples of 64.
 bool decode_ring(const moe_cfg_t* c) {
-  return c->wfmt == MOE_WFMT_MXFP4 && c->path != MOE_PATH_DECODE_REGISTERS;
+  if (c->path == MOE_PATH_DECODE_REGISTERS) return false;
+  if (c->wfmt == MOE_WFMT_MXFP4) return true;
+  return c->wfmt == MOE_WFMT_BF16 && !c->interleaved_gate_up && c->d_model % 64 == 0 &&
+         c->expert_ff % 64 == 0 && c->shared_ff % 64 == 0;
 }
 
 // Caller-owned events recorded at phase boundaries (moe_set_phase_events).
@@ -348,19 +353,26 @@ int run_experts(const moe_cfg_t* c, const void* x_layer, int T, const moe_expert
   const int max_items = L.E1 + (L.S + tpg - 1) / tpg;
   MOE_CUDA(launch_permute(rs, L.S, L.E1, tpg, at<int>(ws, L.hist), s));
   MOE_CUDA(mark_phase(3, s));
-  // MXFP4 one-chunk items: the TMA-fed shared-memory weight stream when it applies.
+  // One-chunk items: the TMA-fed shared-memory weight stream when it applies.
   const bool ring = chunks == 1 && decode_ring(c);
+  const bool fp4 = c->wfmt == MOE_WFMT_MXFP4;
   bool done = false;
-  if (ring)
+  if (ring && fp4)
     MOE_CUDA(launch_gateup_decode_fp4(p, rs, static_cast<const uint16_t*>(x), L.K, h, L.ldh, max_items,
                                       s, &done));
+  else if (ring)
+    MOE_CUDA(launch_gateup_decode_ring(p, rs, static_cast<const uint16_t*>(x), L.K, h, L.ldh, max_items,
+                                       s, &done));
   if (!done)
     MOE_CUDA(launch_gateup_decode(p, c->wfmt, c->interleaved_gate_up, rs,
                                   static_cast<const uint16_t*>(x), L.K, h, L.ldh, max_items, chunks,
                                   s));
   MOE_CUDA(mark_phase(4, s));
   done = false;
-  if (ring) MOE_CUDA(launch_down_decode_fp4(p, rs, h, L.ldh, Y, max_items, s, &done));
+  if (ring && fp4)
+    MOE_CUDA(launch_down_decode_fp4(p, rs, h, L.ldh, Y, max_items, s, &done));
+  else if (ring)
+    MOE_CUDA(launch_down_decode_ring(p, rs, h, L.ldh, Y, max_items, s, &done));
   if (!done) MOE_CUDA(launch_down_decode(p, c->wfmt, rs, h, L.ldh, Y, max_items, chunks, s));
   MOE_CUDA(mark_phase(5, s));
   MOE_CUDA(launch_combine(Y, rs.slot_w, rs.slot_expert, T, L.K, c->d_model, L.E1, resid, y,

@@ -147,6 +147,43 @@ def test_layer_matches_oracle(spec):
     check_outputs(y32, y16, ref.y, spec.name)
 
 
+# bf16 decode with few tokens per expert: the weights stream through the TMA-fed
+# shared-memory ring (separate gate / up, d, ff, sff multiples of 64).  Cases: the
+# shared expert with as many units as the routed ones, none, and fewer (ff 192, sff
+# 128: the shared expert skips a unit); d = 192 leaves a half unit of down rows.
+RING_SPECS = [
+    mi.small_spec("qwen", 128, 32, 4, 64, 64, 8, bias=("normal", 0.5)),
+    mi.small_spec("qwen", 256, 16, 2, 128, 0, 5),
+    mi.small_spec("qwen", 192, 24, 3, 192, 128, 7, bias=("normal", 0.5)),
+    mi.small_spec("qwen", 64, 64, 8, 64, 64, 11, bias=("normal", 0.5), expert_weights_scale=2.5),
+]
+
+
+@pytest.mark.parametrize("spec", RING_SPECS, ids=lambda s: s.name)
+@pytest.mark.parametrize("path", [1, 3], ids=["ring", "registers"])
+def test_bf16_decode_ring(spec, path):
+    moe = moe_lib()
+    T, k = spec.tokens, spec.top_k
+    assert 4 * T * k <= 16 * spec.n_experts                      # one-chunk items
+    lay = mi.make_layer(spec)
+    g = oracle.gating_for(spec)
+    ref = oracle.forward(g, lay)
+    x, router, experts, shared = upload(lay)
+    c = cfg_for(spec, path=path)
+    assert moe.moe_kernel_plan(c, T) == (moe.PLAN_DECODE_RING if path == 1 else moe.PLAN_DECODE_WARP)
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    ws = moe.workspace(c, T)
+    y16 = moe.moe_ffn_forward(c, x, router, experts, shared, topk_ids=ids, ws=ws)
+    y32 = moe.moe_ffn_forward(c.replace(y_fp32=1), x, router, experts, shared, ws=ws)
+    assert moe.moe_device_status(ws)[0] == 0
+    ids_g = ids.cpu().numpy()
+    diff = np.any(ids_g != ref.ids, axis=1)
+    assert not np.any(diff & ~oracle.near_tie_tokens(ref.logits, ref.ids))
+    if np.any(diff):
+        ref = oracle.forward(g, lay, forced_ids=np.where(diff[:, None], ids_g, ref.ids))
+    check_outputs(y32, y16, ref.y, spec.name)
+
+
 def test_interleaved_bf16_clamped_layer():
     moe = moe_lib()
     spec = mi.small_spec("qwen", 96, 8, 3, 64, 0, 29, bias=("normal", 0.3))
