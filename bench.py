@@ -52,6 +52,8 @@ def parse():
                     help="CPU oracle baseline budget (0 disables)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
+    ap.add_argument("--path", choices=["auto", "decode", "prefill", "decode-registers"], default="auto",
+                    help="the expert path (cfg.path); auto picks by tokens per expert")
     return ap.parse_args()
 
 
@@ -292,6 +294,8 @@ def run_ours(args, rank, world, local_rank):
         cfg = moe.qwen_cfg(spec.d_model, spec.n_experts, spec.top_k, spec.expert_ff, spec.shared_ff)
     else:
         cfg = moe.gptoss_cfg(spec.d_model, spec.n_experts, spec.top_k, spec.expert_ff)
+    cfg = cfg.replace(path={"auto": moe.PATH_AUTO, "decode": moe.PATH_DECODE, "prefill": moe.PATH_PREFILL,
+                            "decode-registers": moe.PATH_DECODE_REGISTERS}[args.path])
     T = spec.tokens
     ws = moe.workspace(cfg, T, dev)
     y = torch.empty_like(x)
@@ -434,7 +438,7 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_of(spec),
+        "config": dict(config_of(spec), **({} if args.path == "auto" else {"path": args.path})),
         "ms_per_step_median": statistics.median(step_ms), "ms_per_step_min": min(step_ms),
         "roofline": roof,
         "cpu_baseline": cpu,

@@ -75,9 +75,10 @@ enum {
 enum {
   MOE_PATH_AUTO = 0,    /* pick by mean tokens per expert, T*k/E */
   MOE_PATH_DECODE = 1,  /* weight-streaming grouped matvec (mma.sync); when experts have
-                           at most 4 tokens on average, MXFP4 weights and bf16 weights in
-                           the separate gate / up layout (d, ff, sff multiples of 64)
-                           stream through a TMA-fed shared-memory ring */
+                           at most 4 tokens on average, MXFP4 weights, and bf16 weights
+                           in the separate gate / up layout (d, ff, sff multiples of 64)
+                           for small batches, stream through a TMA-fed shared-memory
+                           ring */
   MOE_PATH_PREFILL = 2, /* grouped GEMM on tcgen05 / TMEM fed by TMA */
   MOE_PATH_DECODE_REGISTERS = 3  /* MOE_PATH_DECODE with every weight load going straight
                                     to registers (no shared-memory ring); same results to
@@ -164,7 +165,9 @@ enum {
                                    loaded straight into registers */
   MOE_PLAN_DECODE_RING = 2,     /* the same, weights streaming through a TMA-fed
                                    shared-memory ring (items of at most 8 tokens; MXFP4,
-                                   or bf16 in the separate gate / up layout) */
+                                   or bf16 in the separate gate / up layout while the
+                                   down projection has fewer than 16 x 152 units of
+                                   128 rows) */
   MOE_PLAN_PREFILL_BF16 = 3,    /* tcgen05 grouped GEMMs with bf16 operands (bf16 weights,
                                    or MXFP4 decoded to bf16 in shared memory) */
   MOE_PLAN_PREFILL_F16 = 4      /* tcgen05 grouped GEMMs with f16 operands: MXFP4 with the

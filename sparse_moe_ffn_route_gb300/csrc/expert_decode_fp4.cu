@@ -386,7 +386,8 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
           tc::mbar_wait(tc::smem_u32(&sfull_bar[i & 1]), (i >> 1) & 1, never, status);
       }
     }
-    pdl_trigger();
+    // no early signal to the dependent launch: the consumers give it when the CTA's
+    // work is done
     return;
   }
 

@@ -3,22 +3,23 @@
 // bytes in flight per SM do not depend on registers.
 //
 // One persistent CTA per SM takes an equal contiguous share of the units (work item
-// x 128 weight rows).  Warp 16 is the producer: one elected lane streams each unit's
-// rows into a ring of stages, a stage being two 64-input k chunks of the unit's 128
-// rows (four TMA boxes of 64 rows x 128 bytes, 128-byte swizzle, 32 KB).
-//   gate_up: the 128 rows of a unit are the gate rows then the up rows of 64
+// x 128 weight rows, or 64 when the expected work would give the CTAs fewer than
+// four units each).  Warp 16 is the producer: one elected lane streams each unit's
+// rows into a ring of 32 KB stages, a stage being 64-input k chunks of the unit's
+// rows (two TMA boxes of half the unit's rows x 128 bytes each, 128-byte swizzle).
+//   gate_up: the rows of a unit are the gate rows then the up rows of the same
 //            features (separate gate and up matrices);
-//   down:    128 consecutive output rows of the down matrix.
+//   down:    consecutive output rows of the down matrix.
 // The shared expert (virtual expert E) takes its own matrices.
 //
-// Warps 0..15 consume: the pair of warps w and w + 8 owns MMA tile w % 8 and takes
-// the even / odd k16 steps.  An ldmatrix x4 of the swizzled stage gives the tile's
-// A fragment (gate_up: rows 0..7 the gate rows and rows 8..15 the up rows of
-// features 8 tile .. 8 tile + 7, so that one lane holds gate and up of the same
-// feature; down: 16 consecutive output rows); the item's token rows, staged in
-// shared memory as bf16 (h as its (hi, lo) pair), give the B fragments by
-// ldmatrix as well.  mma.sync m16n8k16 with fp32 accumulation; the odd-step warp
-// hands its sums to the even one at the unit's end, which runs the epilogue.
+// Warps 0..15 consume: each MMA tile of 16 rows has 16 / tiles warps, which take
+// the k16 steps of every chunk in turn.  An ldmatrix x4 of the swizzled stage gives
+// the tile's A fragment (gate_up: rows 0..7 the gate rows and rows 8..15 the up rows
+// of 8 features, so that one lane holds gate and up of the same feature; down: 16
+// consecutive output rows); the item's token rows, staged in shared memory as bf16
+// (h as its (hi, lo) pair), give the B fragments by ldmatrix as well.  mma.sync
+// m16n8k16 with fp32 accumulation; at the unit's end the tile's warps add their
+// sums in order and the first runs the epilogue.
 //
 // Sources: "qwen35moe - Forward-Pass Design", sections "Shared-expert MoE FFN"
 // (SwiGLU experts, shared expert) and "K80 GPU decode" (grouped MoE: all selected
@@ -32,17 +33,25 @@
 namespace moe {
 namespace {
 
-constexpr int kTiles = 8;                         // 16-row MMA tiles per unit
-constexpr int kCW = 2 * kTiles;                   // consumer warps: two per tile (even / odd k16 steps)
+constexpr int kCW = 16;                           // consumer warps
 constexpr int kThreads = (kCW + 1) * 32;          // + the producer warp
-constexpr int kRows = 16 * kTiles;                // weight rows per unit
-constexpr int kBoxRows = 64;
-constexpr int kBoxBytes = kBoxRows * 128;         // one TMA box: 64 rows x 128 bytes (64 inputs)
-constexpr int kChunkBytes = 2 * kBoxBytes;        // a 64-input k chunk of the unit's 128 rows
-constexpr int kChunks = 2;                        // k chunks per ring stage
-constexpr int kStageBytes = kChunks * kChunkBytes;
+constexpr int kStageBytes = 32 * 1024;            // one ring stage
 constexpr int kMaxRingStages = 8;
 constexpr int kTokens = 8;                        // token rows per work item
+
+// Unit geometry: TILES 16-row MMA tiles (8, or 4 when there are few units, so that
+// the CTAs' shares even out); TMA boxes of 8 TILES rows x 128 bytes (64 inputs), two
+// per 64-input k chunk; the consumer warps split into TILES tiles x 16 / TILES k16
+// step classes.
+template <int TILES>
+struct Geo {
+  static constexpr int kRows = 16 * TILES;                  // weight rows per unit
+  static constexpr int kBoxRows = 8 * TILES;
+  static constexpr int kBoxBytes = kBoxRows * 128;
+  static constexpr int kChunkBytes = 2 * kBoxBytes;         // a 64-input k chunk of the unit's rows
+  static constexpr int kChunks = kStageBytes / kChunkBytes;  // k chunks per ring stage
+  static constexpr int kClasses = kCW / TILES;              // warps per tile (k16 step classes)
+};
 
 // Shared memory, from a 1024-aligned base: ring stages | partial sums | token rows
 // (for down, the lo halves follow the hi rows).
@@ -60,7 +69,7 @@ __host__ __device__ inline RingSmem ring_smem(int kin, bool pair, int stages) {
   m.pitch = ring_pitch(kin);
   m.ring = 0;
   m.part = stages * kStageBytes;
-  m.tok = m.part + kTiles * 32 * 16;
+  m.tok = m.part + kCW * 32 * 16;                  // partial sums [tile][class][lane]
   m.total = m.tok + (pair ? 2 : 1) * kTokens * m.pitch;
   return m;
 }
@@ -77,8 +86,10 @@ __device__ __forceinline__ void consumers_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kCW * 32) : "memory");
 }
 
-__device__ __forceinline__ void pair_sync(int tile) {
-  asm volatile("bar.sync %0, 64;" ::"r"(2 + tile) : "memory");
+// Barrier among the warps of one tile (named barriers 2 .. 2 + TILES - 1).
+template <int CLASSES>
+__device__ __forceinline__ void tile_sync(int tile) {
+  asm volatile("bar.sync %0, %1;" ::"r"(2 + tile), "n"(CLASSES * 32) : "memory");
 }
 
 // volatile: they read shared memory that an mbarrier wait or a barrier made valid.
@@ -113,11 +124,14 @@ struct RingArgs {
 // GATEUP: the units' rows are 64 gate rows (map m0) then 64 up rows (map m1) of the
 // same features; routed experts from m0 / m1, the shared expert from s0 / s1.
 // Otherwise: 128 down rows from m0 (shared: s0), tokens are h (hi, lo) rows.
-template <bool GATEUP>
+template <bool GATEUP, int TILES>
 __global__ void __launch_bounds__(kThreads, 1)
 ring_stream_kernel(const __grid_constant__ CUtensorMap m0, const __grid_constant__ CUtensorMap m1,
                    const __grid_constant__ CUtensorMap s0, const __grid_constant__ CUtensorMap s1,
                    const RingArgs a) {
+  using G = Geo<TILES>;
+  constexpr int kRows = G::kRows, kBoxRows = G::kBoxRows, kBoxBytes = G::kBoxBytes;
+  constexpr int kChunkBytes = G::kChunkBytes, kChunks = G::kChunks, kClasses = G::kClasses;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = tc::smem_align1024(smem_raw);
   __shared__ __align__(8) uint64_t full_bar[kMaxRingStages], empty_bar[kMaxRingStages];
@@ -152,9 +166,9 @@ ring_stream_kernel(const __grid_constant__ CUtensorMap m0, const __grid_constant
   const int n_items = *a.rs.n_work;
   const long long U = (long long)(n_items > 0 ? n_items : 0) * a.tiles;
   const int u0 = (int)(U * blockIdx.x / gridDim.x), u1 = (int)(U * (blockIdx.x + 1) / gridDim.x);
-  // unit u: work item u / tiles, 128 weight rows (gate_up: 64 features) number u % tiles;
-  // an expert with fewer rows than the widest skips its last units
-  constexpr int kUnitRows = GATEUP ? 64 : kRows;
+  // unit u: work item u / tiles, kRows weight rows (gate_up: kRows / 2 features) number
+  // u % tiles; an expert with fewer rows than the widest skips its last units
+  constexpr int kUnitRows = GATEUP ? kRows / 2 : kRows;
   auto unit_on = [&](int v, int t) { return kUnitRows * t < (v == a.E ? a.Rs : a.R); };
 
   if (warp == kCW) {
@@ -202,12 +216,13 @@ ring_stream_kernel(const __grid_constant__ CUtensorMap m0, const __grid_constant
           tc::mbar_wait(tc::smem_u32(&full_bar[i % a.stages]), (i / a.stages) & 1, never, status);
       }
     }
-    pdl_trigger();
+    // no early signal to the dependent launch: the consumers give it when the CTA's
+    // work is done
     return;
   }
 
   // -------------------------------------------------------------- consumers
-  const int tile = warp % kTiles, par = warp / kTiles;
+  const int tile = warp % TILES, cls = warp / TILES;
   const int g = lane >> 2, c = lane & 3;
   const int mi = lane >> 3, ri = lane & 7;        // this lane's ldmatrix address: matrix, row
   // A: the box and row of MMA row 8 (mi & 1) + ri of the tile; k half mi >> 1
@@ -226,7 +241,7 @@ ring_stream_kernel(const __grid_constant__ CUtensorMap m0, const __grid_constant
   uint8_t* tok = smem + L.tok;
   const uint32_t boff = tc::smem_u32(tok) + (uint32_t)((lane & 7) * L.pitch + ((lane >> 3) & 1) * 16);
   const uint32_t lo_off = (uint32_t)(kTokens * L.pitch);
-  float4* part = reinterpret_cast<float4*>(smem + L.part) + tile * 32 + lane;
+  float4* part = reinterpret_cast<float4*>(smem + L.part) + tile * kClasses * 32 + lane;
   int st = 0, cur = -1;                          // ring slot, staged item
   uint32_t ph = 0;
   for (int u = u0; u < u1; ++u) {
@@ -279,7 +294,7 @@ ring_stream_kernel(const __grid_constant__ CUtensorMap m0, const __grid_constant
         const uint32_t sbase = tc::smem_u32(smem + st * kStageBytes) + aoff;
         for (int j = 0; j < nch; ++j) {
 #pragma unroll
-          for (int s16 = par; s16 < 4; s16 += 2) {   // this warp's k16 steps of the chunk
+          for (int s16 = cls; s16 < 4; s16 += kClasses) {   // this warp's k16 steps of the chunk
             const int kg = (kc + j) * 64 + 16 * s16;
             uint32_t A[4], b0, b1;
             ldsm_x4(sbase + j * kChunkBytes + ((uint32_t)((2 * s16 + kh) ^ ri) << 4), A);
@@ -300,23 +315,26 @@ ring_stream_kernel(const __grid_constant__ CUtensorMap m0, const __grid_constant
         ph ^= 1;
       }
     }
-    // the odd-step warp of the tile hands its sums to the even-step warp
-    if (par) *part = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    pair_sync(tile);
-    if (!par) {
-      const float4 o = *part;
-      acc[0] += o.x;
-      acc[1] += o.y;
-      acc[2] += o.z;
-      acc[3] += o.w;
+    // the tile's step classes add up in class order in the class-0 warp
+    if (cls) part[cls * 32] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    tile_sync<kClasses>(tile);
+    if (!cls) {
+#pragma unroll
+      for (int q = 1; q < kClasses; ++q) {
+        const float4 o = part[q * 32];
+        acc[0] += o.x;
+        acc[1] += o.y;
+        acc[2] += o.z;
+        acc[3] += o.w;
+      }
     }
-    pair_sync(tile);                             // read before the next unit writes
-    if (par || !ok) continue;
+    tile_sync<kClasses>(tile);                   // read before the next unit writes
+    if (cls || !ok) continue;
 
     // ------------------------------------------------------------ epilogue
     // acc: MMA rows g (tokens 2c, 2c+1) and g + 8
     if (GATEUP) {
-      const int f = 64 * t + 8 * tile + g;       // row g: its gate, row g + 8: its up
+      const int f = kUnitRows * t + 8 * tile + g;   // row g: its gate, row g + 8: its up
       float bg = 0.f, bu = 0.f;
       if (!sh && a.gu_bias) {
         const size_t row = (size_t)v * 2 * a.R + 2 * (size_t)f;
@@ -358,14 +376,14 @@ ring_stream_kernel(const __grid_constant__ CUtensorMap m0, const __grid_constant
   pdl_trigger();
 }
 
-template <bool GATEUP>
+template <bool GATEUP, int TILES>
 void set_ring_smem(int bytes) {
   static int done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || done[dev] >= bytes) return;
-  if (cudaFuncSetAttribute(ring_stream_kernel<GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) ==
-      cudaSuccess)
+  if (cudaFuncSetAttribute(ring_stream_kernel<GATEUP, TILES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           bytes) == cudaSuccess)
     done[dev] = bytes;
 }
 
@@ -380,31 +398,58 @@ int ring_stages(int kin, bool pair) {
   return st >= 2 ? st : 0;
 }
 
-template <bool GATEUP>
-cudaError_t launch_ring(const CUtensorMap& m0, const CUtensorMap& m1, const CUtensorMap& s0, const CUtensorMap& s1,
-                        RingArgs a, int max_items, cudaStream_t s, bool* launched) {
-  const int kmax = a.kin > a.kin_s ? a.kin : a.kin_s;
-  a.stages = ring_stages(kmax, !GATEUP);
-  if (!a.stages) return cudaSuccess;
-  const int bytes = ring_smem(kmax, !GATEUP, a.stages).total + 1024;
-  set_ring_smem<GATEUP>(bytes);
-  const long long units = (long long)max_items * a.tiles;
-  int grid = sm_count();
-  if (units < grid) grid = (int)(units > 0 ? units : 1);
-  *launched = true;
-  return launch_pdl(ring_stream_kernel<GATEUP>, dim3(grid), dim3(kThreads), (size_t)bytes, s, m0, m1, s0, s1, a);
-}
-
 // bf16 matrix [rows, cols], boxes of box_rows x 64 elements with the 128-byte swizzle.
 bool ring_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rows, cols, cols * 2, box_rows, 64,
                   CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// The maps (box rows 8 TILES) and the launch of one geometry.  GATEUP: gate / up
+// (m0, m1; shared s0, s1); else down (m0; shared s0).
+template <bool GATEUP, int TILES>
+cudaError_t launch_ring(const ExpertParams& p, RingArgs a, int max_items, cudaStream_t s, bool* launched) {
+  using G = Geo<TILES>;
+  const int kmax = a.kin > a.kin_s ? a.kin : a.kin_s;
+  a.stages = ring_stages(kmax, !GATEUP);
+  if (!a.stages) return cudaSuccess;
+  const int unit = GATEUP ? G::kRows / 2 : G::kRows;        // features (gate_up) or rows per unit
+  a.tiles = ((a.R > a.Rs ? a.R : a.Rs) + unit - 1) / unit;
+  CUtensorMap m0, m1, s0, s1;
+  if (GATEUP) {
+    if (!ring_map(&m0, p.gate, (uint64_t)p.E * p.ff, p.d, G::kBoxRows) ||
+        !ring_map(&m1, p.up, (uint64_t)p.E * p.ff, p.d, G::kBoxRows))
+      return cudaSuccess;
+    s0 = m0;
+    s1 = m1;
+    if (p.sff && (!ring_map(&s0, p.sh_gate, (uint64_t)p.sff, p.d, G::kBoxRows) ||
+                  !ring_map(&s1, p.sh_up, (uint64_t)p.sff, p.d, G::kBoxRows)))
+      return cudaSuccess;
+  } else {
+    if (!ring_map(&m0, p.down, (uint64_t)p.E * p.d, p.ff, G::kBoxRows)) return cudaSuccess;
+    s0 = m0;
+    if (p.sff && !ring_map(&s0, p.sh_down, (uint64_t)p.d, p.sff, G::kBoxRows)) return cudaSuccess;
+    m1 = m0;
+    s1 = s0;
+  }
+  const int bytes = ring_smem(kmax, !GATEUP, a.stages).total + 1024;
+  set_ring_smem<GATEUP, TILES>(bytes);
+  const long long units = (long long)max_items * a.tiles;
+  int grid = sm_count();
+  if (units < grid) grid = (int)(units > 0 ? units : 1);
+  *launched = true;
+  return launch_pdl(ring_stream_kernel<GATEUP, TILES>, dim3(grid), dim3(kThreads), (size_t)bytes, s, m0, m1, s0,
+                    s1, a);
+}
+
+// Units of 128 rows unless the expected work would give the CTAs fewer than four
+// each; then units of 64 rows, so that the shares even out.
+bool small_units(long long units128) { return units128 < 4LL * sm_count(); }
+
 }  // namespace
 
 cudaError_t launch_gateup_decode_ring(const ExpertParams& p, const RouteState& rs, const uint16_t* x, int K,
-                                      uint16_t* h, int ldh, int max_items, cudaStream_t s, bool* launched) {
+                                      uint16_t* h, int ldh, int max_items, int expect_items, cudaStream_t s,
+                                      bool* launched) {
   *launched = false;
   RingArgs a{};
   a.rs = rs;
@@ -413,7 +458,6 @@ cudaError_t launch_gateup_decode_ring(const ExpertParams& p, const RouteState& r
   a.Rs = p.sff;
   a.kin = p.d;
   a.kin_s = p.d;
-  a.tiles = ((p.ff > p.sff ? p.ff : p.sff) + 63) / 64;
   a.gu_bias = p.gu_bias;
   a.x = x;
   a.K = K;
@@ -422,20 +466,13 @@ cudaError_t launch_gateup_decode_ring(const ExpertParams& p, const RouteState& r
   a.act = p.act;
   a.limit = p.limit;
   a.alpha = p.alpha;
-  CUtensorMap m0, m1, s0, s1;
-  if (!ring_map(&m0, p.gate, (uint64_t)p.E * p.ff, p.d, kBoxRows) ||
-      !ring_map(&m1, p.up, (uint64_t)p.E * p.ff, p.d, kBoxRows))
-    return cudaSuccess;
-  s0 = m0;
-  s1 = m1;
-  if (p.sff && (!ring_map(&s0, p.sh_gate, (uint64_t)p.sff, p.d, kBoxRows) ||
-                !ring_map(&s1, p.sh_up, (uint64_t)p.sff, p.d, kBoxRows)))
-    return cudaSuccess;
-  return launch_ring<true>(m0, m1, s0, s1, a, max_items, s, launched);
+  const long long units128 = (long long)expect_items * (((p.ff > p.sff ? p.ff : p.sff) + 63) / 64);
+  if (small_units(units128)) return launch_ring<true, 4>(p, a, max_items, s, launched);
+  return launch_ring<true, 8>(p, a, max_items, s, launched);
 }
 
 cudaError_t launch_down_decode_ring(const ExpertParams& p, const RouteState& rs, const uint16_t* h, int ldh,
-                                    float* Y, int max_items, cudaStream_t s, bool* launched) {
+                                    float* Y, int max_items, int expect_items, cudaStream_t s, bool* launched) {
   *launched = false;
   RingArgs a{};
   a.rs = rs;
@@ -444,16 +481,13 @@ cudaError_t launch_down_decode_ring(const ExpertParams& p, const RouteState& rs,
   a.Rs = p.d;
   a.kin = p.ff;
   a.kin_s = p.sff ? p.sff : p.ff;
-  a.tiles = (p.d + kRows - 1) / kRows;
   a.dn_bias = p.dn_bias;
   a.h = const_cast<uint16_t*>(h);
   a.ldh = ldh;
   a.Y = Y;
-  CUtensorMap m0, s0;
-  if (!ring_map(&m0, p.down, (uint64_t)p.E * p.d, p.ff, kBoxRows)) return cudaSuccess;
-  s0 = m0;
-  if (p.sff && !ring_map(&s0, p.sh_down, (uint64_t)p.d, p.sff, kBoxRows)) return cudaSuccess;
-  return launch_ring<false>(m0, m0, s0, s0, a, max_items, s, launched);
+  const long long units128 = (long long)expect_items * ((p.d + 127) / 128);
+  if (small_units(units128)) return launch_ring<false, 4>(p, a, max_items, s, launched);
+  return launch_ring<false, 8>(p, a, max_items, s, launched);
 }
 
 }  // namespace moe

@@ -148,10 +148,12 @@ cudaError_t launch_down_decode(const ExpertParams& p, int wfmt, const RouteState
 // of 64), one-chunk items (at most 8 token rows): the weights stream through a
 // TMA-fed shared-memory ring (expert_decode_ring.cu).  *launched comes back false
 // when the ring does not fit the device (the caller then runs the kernels above).
+// expect_items: the expected number of work items (the unit size follows from it).
 cudaError_t launch_gateup_decode_ring(const ExpertParams& p, const RouteState& rs, const uint16_t* x, int K,
-                                      uint16_t* h, int ldh, int max_items, cudaStream_t s, bool* launched);
+                                      uint16_t* h, int ldh, int max_items, int expect_items, cudaStream_t s,
+                                      bool* launched);
 cudaError_t launch_down_decode_ring(const ExpertParams& p, const RouteState& rs, const uint16_t* h, int ldh,
-                                    float* Y, int max_items, cudaStream_t s, bool* launched);
+                                    float* Y, int max_items, int expect_items, cudaStream_t s, bool* launched);
 
 // Prefill path: grouped GEMMs on tcgen05 (see expert_prefill.cu).  The work list
 // must hold 128-row m tiles (permute with tpg = 128).

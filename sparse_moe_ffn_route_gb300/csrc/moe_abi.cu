@@ -203,15 +203,27 @@ int decode_chunks(const moe_cfg_t* c, int T) {
   return 4LL * T * c->top_k <= 16LL * c->n_experts ? 1 : 4;
 }
 
+// Decode path, expected work items for T tokens: the distinct routed experts (at most
+// T k or E), plus the shared expert's items of 8 rows.
+int expect_items(const moe_cfg_t* c, int T) {
+  const long long tk = (long long)T * c->top_k;
+  return (int)(tk < c->n_experts ? tk : c->n_experts) + (c->shared_ff > 0 ? (T + 7) / 8 : 0);
+}
+
 // Decode path: one-chunk items take the TMA-fed ring kernels (which fall back to the
 // register-stream ones only if the device lacks the shared memory they need): MXFP4
-// weights, and bf16 weights in the separate gate / up layout with d, ff, sff
-// multiples of 64.
-bool decode_ring(const moe_cfg_t* c) {
+// weights; bf16 weights in the separate gate / up layout with d, ff, sff multiples
+// of 64 while the down projection has fewer than kRingUnits units of 128 rows (16
+// per SM of a 152-SM GB300).  Past that the register-stream kernels are as fast or
+// faster (Qwen3.5-mini T=64: 0.242 against 0.244 ms a step; T=8: 0.103 against
+// 0.090 ms with the ring).
+constexpr long long kRingUnits = 16LL * 152;
+bool decode_ring(const moe_cfg_t* c, int T) {
   if (c->path == MOE_PATH_DECODE_REGISTERS) return false;
   if (c->wfmt == MOE_WFMT_MXFP4) return true;
   return c->wfmt == MOE_WFMT_BF16 && !c->interleaved_gate_up && c->d_model % 64 == 0 &&
-         c->expert_ff % 64 == 0 && c->shared_ff % 64 == 0;
+         c->expert_ff % 64 == 0 && c->shared_ff % 64 == 0 &&
+         (long long)expect_items(c, T) * ((c->d_model + 127) / 128) < kRingUnits;
 }
 
 // Caller-owned events recorded at phase boundaries (moe_set_phase_events).
@@ -354,15 +366,16 @@ int run_experts(const moe_cfg_t* c, const void* x_layer, int T, const moe_expert
   MOE_CUDA(launch_permute(rs, L.S, L.E1, tpg, at<int>(ws, L.hist), s));
   MOE_CUDA(mark_phase(3, s));
   // One-chunk items: the TMA-fed shared-memory weight stream when it applies.
-  const bool ring = chunks == 1 && decode_ring(c);
+  const bool ring = chunks == 1 && decode_ring(c, T);
   const bool fp4 = c->wfmt == MOE_WFMT_MXFP4;
+  const int items = expect_items(c, T);
   bool done = false;
   if (ring && fp4)
     MOE_CUDA(launch_gateup_decode_fp4(p, rs, static_cast<const uint16_t*>(x), L.K, h, L.ldh, max_items,
                                       s, &done));
   else if (ring)
     MOE_CUDA(launch_gateup_decode_ring(p, rs, static_cast<const uint16_t*>(x), L.K, h, L.ldh, max_items,
-                                       s, &done));
+                                       items, s, &done));
   if (!done)
     MOE_CUDA(launch_gateup_decode(p, c->wfmt, c->interleaved_gate_up, rs,
                                   static_cast<const uint16_t*>(x), L.K, h, L.ldh, max_items, chunks,
@@ -372,7 +385,7 @@ int run_experts(const moe_cfg_t* c, const void* x_layer, int T, const moe_expert
   if (ring && fp4)
     MOE_CUDA(launch_down_decode_fp4(p, rs, h, L.ldh, Y, max_items, s, &done));
   else if (ring)
-    MOE_CUDA(launch_down_decode_ring(p, rs, h, L.ldh, Y, max_items, s, &done));
+    MOE_CUDA(launch_down_decode_ring(p, rs, h, L.ldh, Y, max_items, items, s, &done));
   if (!done) MOE_CUDA(launch_down_decode(p, c->wfmt, rs, h, L.ldh, Y, max_items, chunks, s));
   MOE_CUDA(mark_phase(5, s));
   MOE_CUDA(launch_combine(Y, rs.slot_w, rs.slot_expert, T, L.K, c->d_model, L.E1, resid, y,
@@ -407,7 +420,7 @@ int moe_kernel_plan(const moe_cfg_t* cfg, int32_t T) {
   if (!make_layout(cfg, T, &L)) return MOE_ERR_UNSUPPORTED;
   if (L.prefill_fp4) return MOE_PLAN_PREFILL_F16;
   if (L.prefill) return MOE_PLAN_PREFILL_BF16;
-  return decode_chunks(cfg, T) == 1 && decode_ring(cfg) ? MOE_PLAN_DECODE_RING : MOE_PLAN_DECODE_WARP;
+  return decode_chunks(cfg, T) == 1 && decode_ring(cfg, T) ? MOE_PLAN_DECODE_RING : MOE_PLAN_DECODE_WARP;
 }
 
 int moe_route(const moe_cfg_t* cfg, const void* x, int32_t T, const moe_router_t* router,

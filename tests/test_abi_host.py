@@ -49,7 +49,7 @@ def test_kernel_plan_per_workload():
     import moe_inputs as mi
     want = {
         "qwen35_mini_moe_decode_t8": moe.PLAN_DECODE_RING,
-        "qwen35_mini_moe_decode_t64": moe.PLAN_DECODE_RING,
+        "qwen35_mini_moe_decode_t64": moe.PLAN_DECODE_WARP,
         "qwen35_mini_moe_prefill_t4096": moe.PLAN_PREFILL_BF16,
         "gptoss_20b_moe_decode_t32": moe.PLAN_DECODE_RING,
         "gptoss_20b_moe_prefill_t8192": moe.PLAN_PREFILL_F16,
@@ -79,10 +79,11 @@ def test_kernel_plan_forms():
     # multiples of 64; otherwise (or when asked) the register-stream kernels
     assert moe.moe_kernel_plan(q, 4) == moe.PLAN_DECODE_WARP                       # d = 96
     b = moe.qwen_cfg()
-    assert moe.moe_kernel_plan(b, 64) == moe.PLAN_DECODE_RING
-    assert moe.moe_kernel_plan(b.replace(path=moe.PATH_DECODE_REGISTERS), 64) == moe.PLAN_DECODE_WARP
-    assert moe.moe_kernel_plan(b.replace(interleaved_gate_up=1, shared_ff=0), 64) == moe.PLAN_DECODE_WARP
-    assert moe.moe_kernel_plan(b.replace(shared_ff=96), 64) == moe.PLAN_DECODE_WARP
+    assert moe.moe_kernel_plan(b, 8) == moe.PLAN_DECODE_RING
+    assert moe.moe_kernel_plan(b, 64) == moe.PLAN_DECODE_WARP       # many units: register stream
+    assert moe.moe_kernel_plan(b.replace(path=moe.PATH_DECODE_REGISTERS), 8) == moe.PLAN_DECODE_WARP
+    assert moe.moe_kernel_plan(b.replace(interleaved_gate_up=1, shared_ff=0), 8) == moe.PLAN_DECODE_WARP
+    assert moe.moe_kernel_plan(b.replace(shared_ff=96), 8) == moe.PLAN_DECODE_WARP
     assert moe._lib.moe_kernel_plan(ctypes.byref(moe.qwen_cfg()), -1) == -1
 
 
