@@ -10,13 +10,14 @@
 // one bulk copy.  About 128 KB of weights are in flight per SM at any time, without
 // holding registers.
 //
-// Warps 0..15 consume: the pair of warps w and w + 8 owns rows 16w..16w+15 of the
-// unit (one MMA tile), each taking every other block of a stage.  An
-// ldmatrix of the swizzled stage hands lane (g, c) the four code bytes 4c..4c+3 of
-// one 32-input block of rows g and g+8, so both k16 MMAs of that block see inputs of
-// that block only: the block's two MMAs accumulate into a fresh fp32 fragment that
-// is then scaled once by 2^(s - 127) (exact in fp32 for every scale byte, through a
-// 256-entry table that also maps 0 to 2^-127 and 255 to NaN).  Codes become exact
+// Warps 0..15 consume: warp w owns the tile pair w % 4 (rows 32 (w % 4) .. + 31 of
+// the unit, two MMA tiles) and the blocks of class w / 4 (block index mod 4) of every
+// box.  An ldmatrix of the swizzled stage hands lane (g, c) the four code bytes
+// 4c..4c+3 of one 32-input block of rows g and g+8, so both k16 MMAs of that block see
+// inputs of that block only: the block's two MMAs give a fresh fp32 product that is
+// scaled once by 2^(s - 127) (exact in fp32 for every scale byte, through a 256-entry
+// table that also maps 0 to 2^-127 and 255 to NaN) into the output fragment; a
+// block's token fragments serve both tiles of the pair.  Codes become exact
 // f16 pairs with cvt.rn.f16x2.e2m1x2.  The token operand is the item's rows staged
 // in shared memory as f16 scaled by 2^e per token (largest magnitude in
 // [2^14, 2^15)), so bf16 x is exact and h = hi + lo keeps 11 bits; the epilogue

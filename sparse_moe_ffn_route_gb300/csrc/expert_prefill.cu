@@ -17,7 +17,14 @@
 //               each stage back to the producer and each finished tile to the
 //               epilogue;
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator row that their TMEM lane
-//               quarter holds, bias + activation (gate_up) or bias (down), stores.
+//               quarter holds, bias + activation (gate_up) or bias (down), stores
+//               (down and the router logits: turned around in shared memory so that
+//               every store writes whole lines);
+//   warps 6..   MXFP4: dequant warps (B tiles into shared memory); bf16 gate_up:
+//               loader warps that copy the A rows from x by row index (cp.async)
+//               instead of a TMA load of a gathered copy.
+// The router logits run through the same kernel (dense mode), with the k range cut
+// into parts when there are few m tiles.
 // Every mbarrier wait is bounded; a wait that gives up sets the device status
 // and an abort flag, the CTA drains its copies and MMAs in flight, frees TMEM and
 // returns.
