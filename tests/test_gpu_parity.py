@@ -560,6 +560,7 @@ def test_residual_with_caller_routing():
 GRAPH_CASES = [
     mi.small_spec("qwen", 128, 16, 4, 64, 96, 33, bias=("normal", 0.5)),          # decode
     mi.small_spec("gptoss", 96, 12, 4, 96, 0, 7, bias=("normal", 0.1)),           # decode ring
+    mi.small_spec("qwen", 128, 32, 4, 64, 64, 8, bias=("normal", 0.5)),            # bf16 decode ring
     mi.small_spec("gptoss", 128, 4, 2, 128, 0, 600, bias=("normal", 0.1)),        # prefill f16
     mi.small_spec("qwen", 256, 16, 4, 128, 128, 300, bias=("normal", 0.5)),       # prefill bf16
 ]
