@@ -326,6 +326,11 @@ def test_full_workload(name, full_layers):
     yp32 = torch.full((T, spec.d_model), float("nan"), dtype=torch.float32).pin_memory()
     moe.moe_ffn_forward_host(c.replace(y_fp32=1), xh, router, experts, shared, y_host=yp32, ws=ws)
     assert torch.equal(yp32, y32.cpu())
+    # page-locked but not 16-byte aligned: the staged copy
+    buf = torch.full((T * spec.d_model + 1,), float("nan"), dtype=torch.bfloat16).pin_memory()
+    yu = buf[1:].view(T, spec.d_model)
+    moe.moe_ffn_forward_host(c, xh, router, experts, shared, y_host=yu, ws=ws)
+    assert torch.equal(yu.view(torch.int16), y.cpu().view(torch.int16))
 
 
 # ----------------------------------------------------------------------------- prefill (tcgen05) path
