@@ -11,13 +11,14 @@
 // holding registers.
 //
 // Warps 0..15 consume: warp w owns the tile pair w % 4 (rows 32 (w % 4) .. + 31 of
-// the unit, two MMA tiles) and the blocks of class w / 4 (block index mod 4) of every
-// box.  An ldmatrix of the swizzled stage hands lane (g, c) the four code bytes
-// 4c..4c+3 of one 32-input block of rows g and g+8, so both k16 MMAs of that block see
-// inputs of that block only: the block's two MMAs give a fresh fp32 product that is
-// scaled once by 2^(s - 127) (exact in fp32 for every scale byte, through a 256-entry
-// table that also maps 0 to 2^-127 and 255 to NaN) into the output fragment; a
-// block's token fragments serve both tiles of the pair.  Codes become exact
+// the unit, two MMA tiles) and two adjacent 32-input blocks of every box (the pair
+// turns with the unit).  An ldmatrix of the swizzled stage hands lane (g, c) the four
+// code bytes 4c..4c+3 of one block of rows g and g+8, so both k16 MMAs of that block
+// see inputs of that block only: the block's two MMAs give a fresh fp32 product that
+// is scaled once by 2^(s - 127) into the output fragment.  The scale is exact in fp32
+// for every byte (0 gives 2^-127, 255 NaN): a row's two scale bytes become a bf16
+// pair with one hardware conversion, or, for rows of an odd number of blocks, come
+// from a 256-entry table.  A block's token fragments serve both tiles of the pair.  Codes become exact
 // f16 pairs with cvt.rn.f16x2.e2m1x2.  The token operand is the item's rows staged
 // in shared memory as f16 scaled by 2^e per token (largest magnitude in
 // [2^14, 2^15)), so bf16 x is exact and h = hi + lo keeps 11 bits; the epilogue
@@ -36,7 +37,7 @@ namespace moe {
 namespace {
 
 constexpr int kTiles = 8;                         // 16-row MMA tiles per unit
-constexpr int kClasses = 4;                       // block classes (block index mod 4)
+constexpr int kClasses = 4;                       // block classes (adjacent block pairs of a box)
 constexpr int kCW = kTiles / 2 * kClasses;        // consumer warps: one per (tile pair, block class)
 constexpr int kThreads = (kCW + 1) * 32;          // + the producer warp
 constexpr int kRows = 16 * kTiles;                // weight rows per unit
@@ -78,12 +79,15 @@ __host__ __device__ inline F4Smem f4_smem(int kin, int stages) {
   return m;
 }
 
-__device__ __forceinline__ float act_swiglu(float g, float u) { return g / (1.f + __expf(-g)) * u; }
+// The activations divide with __fdividef (2 ulp): the IEEE division's slow path sits on
+// the critical path at every unit's end.  A denominator that overflows to infinity
+// gives 0, the limit of both functions there.
+__device__ __forceinline__ float act_swiglu(float g, float u) { return __fdividef(g, 1.f + __expf(-g)) * u; }
 
 __device__ __forceinline__ float act_clamped(float g, float u, float limit, float alpha) {
   g = fminf(g, limit);
   u = fminf(fmaxf(u, -limit), limit);
-  return (u + 1.f) * g / (1.f + __expf(-alpha * g));
+  return __fdividef((u + 1.f) * g, 1.f + __expf(-alpha * g));
 }
 
 // Barrier among the consumer warps only (the producer keeps streaming).
@@ -224,53 +228,67 @@ __device__ __forceinline__ void block_mma(const uint32_t wa, const uint32_t wb, 
   acc[3] = fmaf(s1, tt[3], acc[3]);
 }
 
-// Blocks q and q + 4 (those below nblk) of one box for the two tiles of a pair:
+// Two E8M0 scale bytes (low byte first) as fp32 2^(s - 127) each, through the
+// hardware conversion to a bf16 pair: exact for every byte, 0 giving 2^-127 and 255
+// NaN, like the table.
+__device__ __forceinline__ void e8m0x2_to_f32(uint16_t v, float& lo, float& hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.ue8m0x2 %0, %1;" : "=r"(r) : "h"(v));
+  lo = __uint_as_float(r << 16);
+  hi = __uint_as_float(r & 0xffff0000u);
+}
+
+// Blocks 2 qe and 2 qe + 1 (those below nblk) of one box for the two tiles of a pair:
 // acc[t] += 2^(s - 127) * (block's codes x token rows), per block.  rbase: the lane's
 // ldmatrix row in the box for the pair's first tile (the second's is 16 rows on);
-// sc: the scale bytes of row g of the first tile; gb0: global block index of block q.
-// One x4 ldmatrix per tile hands lane (g, c) the code bytes 4c..4c+3 of rows g and
-// g + 8 of both blocks; the token fragments of a block serve both tiles.
-template <bool FULL>
-__device__ __forceinline__ void box_pair(uint32_t rbase, int mi, int ri, int q, const uint8_t* tg, const uint8_t* sc,
+// sc: the scale bytes of row g of the first tile; gb0: global block index of block
+// 2 qe.  One x4 ldmatrix per tile hands lane (g, c) the code bytes 4c..4c+3 of rows g
+// and g + 8 of both blocks; the token fragments of a block serve both tiles.
+// PAIRED (an even number of blocks per row, so that gb0 and every row start are
+// even): each row's two scale bytes come with one 16-bit load and one conversion;
+// otherwise byte by byte through the table.
+template <bool FULL, bool PAIRED>
+__device__ __forceinline__ void box_pair(uint32_t rbase, int mi, int ri, int qe, const uint8_t* tg, const uint8_t* sc,
                                          int nb, const float* lut, int gb0, int nblk, float (&acc)[2][4]) {
   if (FULL) {
     // every operand first, so that their latencies overlap
     uint32_t r[2][4];
 #pragma unroll
-    for (int t = 0; t < 2; ++t) ldmatrix_x4(rbase + t * 16 * 128 + ((uint32_t)((q + 4 * (mi >> 1)) ^ ri) << 4), r[t]);
+    for (int t = 0; t < 2; ++t) ldmatrix_x4(rbase + t * 16 * 128 + ((uint32_t)((2 * qe + (mi >> 1)) ^ ri) << 4), r[t]);
     uint4 B[2];
-    uint32_t cb[2][2][2];                         // [tile][block][row g / g + 8]
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      B[k] = *reinterpret_cast<const uint4*>(tg + 64 * (gb0 + 4 * k));
+    for (int k = 0; k < 2; ++k) B[k] = *reinterpret_cast<const uint4*>(tg + 64 * (gb0 + k));
+    float sv[2][2][2];                            // [tile][block][row g / g + 8]
+    if (PAIRED) {
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        cb[t][k][0] = sc[16 * t * nb + gb0 + 4 * k];
-        cb[t][k][1] = sc[(16 * t + 8) * nb + gb0 + 4 * k];
-      }
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint16_t v = *reinterpret_cast<const uint16_t*>(sc + (16 * t + 8 * h) * nb + gb0);
+          e8m0x2_to_f32(v, sv[t][0][h], sv[t][1][h]);
+        }
+    } else {
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) sv[t][k][h] = lut[sc[(16 * t + 8 * h) * nb + gb0 + k]];
     }
-    float sv[2][2][2];
-#pragma unroll
-    for (int t = 0; t < 2; ++t)
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        sv[t][k][0] = lut[cb[t][k][0]];
-        sv[t][k][1] = lut[cb[t][k][1]];
-      }
 #pragma unroll
     for (int k = 0; k < 2; ++k)
 #pragma unroll
       for (int t = 0; t < 2; ++t) block_mma(r[t][2 * k], r[t][2 * k + 1], B[k], sv[t][k][0], sv[t][k][1], acc[t]);
   } else {
+    if (2 * qe >= nblk) return;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-      if (q >= nblk) break;
       uint32_t r[4];
-      ldmatrix_x4(rbase + t * 16 * 128 + ((uint32_t)((q + 4 * (mi >> 1)) ^ ri) << 4), r);
+      ldmatrix_x4(rbase + t * 16 * 128 + ((uint32_t)((2 * qe + (mi >> 1)) ^ ri) << 4), r);
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
-        if (q + 4 * k < nblk) {
-          const int gb = gb0 + 4 * k;
+        if (2 * qe + k < nblk) {
+          const int gb = gb0 + k;
           const uint4 B = *reinterpret_cast<const uint4*>(tg + 64 * gb);
           block_mma(r[2 * k], r[2 * k + 1], B, lut[sc[16 * t * nb + gb]], lut[sc[(16 * t + 8) * nb + gb]], acc[t]);
         }
@@ -300,7 +318,8 @@ struct F4Args {
 
 // GATEUP: codes are gate_up [E, 2ff, d/2] bytes, tokens are x rows, output h.
 // Otherwise: codes are down [E, d, ff/2], tokens are h rows, output Y.
-template <bool GATEUP>
+// PAIRED: kin / 32 is even (scale bytes read two at a time).
+template <bool GATEUP, bool PAIRED>
 __global__ void __launch_bounds__(kThreads, 1)
 fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
   extern __shared__ uint8_t smem_raw[];
@@ -393,9 +412,9 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
   }
 
   // -------------------------------------------------------------- consumers
-  // Warp w owns tile pair tp = w % 4 (rows 32 tp .. 32 tp + 31 of the unit) and the
-  // blocks of class q = w / 4 (block index mod 4) of every box: a block's token
-  // fragments serve both tiles.  At the unit's end the four warps of a pair add their
+  // Warp w owns tile pair tp = w % 4 (rows 32 tp .. 32 tp + 31 of the unit) and, in
+  // every box, the two adjacent blocks of class qe = (w / 4 + unit) mod 4: a block's
+  // token fragments serve both tiles.  At the unit's end the four warps of a pair add their
   // sums in shared memory, and warps q = 0, 1 finish tiles 2 tp and 2 tp + 1.
   const int tp = warp % (kTiles / 2), q = warp / (kTiles / 2);
   const int g = lane >> 2, c = lane & 3;
@@ -434,10 +453,35 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
     }
     const int row0 = t * kRows, nrows = min(kRows, a.R - row0);
     const bool on = 32 * tp < nrows;             // nrows is a multiple of 32
+    // The epilogue's global operands (biases; for down the output rows) are fetched
+    // now, so that their round trip to memory overlaps the k loop instead of
+    // stalling the end of the unit.
+    const int tile = 2 * tp + (q & 1);
+    const bool odd = g & 1;
+    // gate_up: feature f of this lane; down: output rows o and o + 8
+    const int f = row0 / 2 + 8 * tile + (odd ? 4 : 0) + (g >> 1);
+    const int o = row0 + 16 * tile + g;
+    uint16_t bias_a = 0, bias_b = 0;
+    int yslot[2] = {-1, -1};
+    if (on && q < 2) {
+      if (a.bias) {
+        const uint16_t* bp = a.bias + (size_t)v * a.R + (GATEUP ? 2 * f : o);
+        bias_a = bp[0];
+        bias_b = bp[GATEUP ? 1 : 8];
+      }
+      if (!GATEUP) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+          if (2 * c + k < n) yslot[k] = a.rs.row2slot[r0 + 2 * c + k];
+      }
+    }
     const int sb = its & 1;
     bool ok = tc::mbar_wait(tc::smem_u32(&sfull_bar[sb]), (its >> 1) & 1, abort, status);
     const uint8_t* sc = smem + L.scales + sb * L.scale_bytes + (32 * tp + g) * L.nb;
     float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // the block pair this warp takes in every box turns with the unit, so that the
+    // ragged last box of a row does not always fall to the same warps
+    const int qe = (q + u) & (kClasses - 1);
     for (int s = 0; s < nst; ++s) {
       ok = ok && tc::mbar_wait(tc::smem_u32(&full_bar[st]), ph, abort, status);
       if (ok && on) {
@@ -446,11 +490,11 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
 #pragma unroll
         for (int j = 0; j < kBoxes; ++j) {
           const int nbj = min(kBlocksPerBox, nblk - j * kBlocksPerBox);
-          const int gb0 = s * kBlocksPerStage + j * kBlocksPerBox + q;
+          const int gb0 = s * kBlocksPerStage + j * kBlocksPerBox + 2 * qe;
           if (nbj == kBlocksPerBox)
-            box_pair<true>(rbase + j * kBoxBytes, mi, ri, q, tg, sc, L.nb, lut, gb0, kBlocksPerBox, acc2);
+            box_pair<true, PAIRED>(rbase + j * kBoxBytes, mi, ri, qe, tg, sc, L.nb, lut, gb0, kBlocksPerBox, acc2);
           else if (nbj > 0)
-            box_pair<false>(rbase + j * kBoxBytes, mi, ri, q, tg, sc, L.nb, lut, gb0, nbj, acc2);
+            box_pair<false, PAIRED>(rbase + j * kBoxBytes, mi, ri, qe, tg, sc, L.nb, lut, gb0, nbj, acc2);
         }
       }
       // Each lane arrives once its own reads of the stage are done (its ldmatrix
@@ -470,7 +514,6 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
     for (int t2 = 0; t2 < 2; ++t2)
       part[(q * 2 + t2) * 32] = make_float4(acc2[t2][0], acc2[t2][1], acc2[t2][2], acc2[t2][3]);
     quad_sync(tp);
-    const int tile = 2 * tp + (q & 1);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     if (q < 2) {
 #pragma unroll
@@ -495,15 +538,9 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
       float pr[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) pr[k] = __shfl_xor_sync(0xffffffffu, acc[k], 4);
-      const bool odd = g & 1;
-      const int f = row0 / 2 + 8 * tile + (odd ? 4 : 0) + (g >> 1);
       const float gt[2] = {odd ? pr[2] : acc[0], odd ? pr[3] : acc[1]};
       const float upv[2] = {odd ? acc[2] : pr[0], odd ? acc[3] : pr[1]};
-      float bg = 0.f, bu = 0.f;
-      if (a.bias) {
-        bg = bf16_to_f32(a.bias[(size_t)v * a.R + 2 * f]);
-        bu = bf16_to_f32(a.bias[(size_t)v * a.R + 2 * f + 1]);
-      }
+      const float bg = bf16_to_f32(bias_a), bu = bf16_to_f32(bias_b);
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         const int ti = 2 * c + q;
@@ -519,17 +556,11 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
         }
       }
     } else {
-      const int o = row0 + 16 * tile + g;
-      float b0 = 0.f, b1 = 0.f;
-      if (a.bias) {
-        b0 = bf16_to_f32(a.bias[(size_t)v * a.R + o]);
-        b1 = bf16_to_f32(a.bias[(size_t)v * a.R + o + 8]);
-      }
+      const float b0 = bf16_to_f32(bias_a), b1 = bf16_to_f32(bias_b);
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
-        const int ti = 2 * c + q;
-        if (ti < n) {
-          float* yrow = a.Y + (size_t)a.rs.row2slot[r0 + ti] * a.R;
+        if (yslot[q] >= 0) {
+          float* yrow = a.Y + (size_t)yslot[q] * a.R;
           yrow[o] = acc[q] * un[q] + b0;
           yrow[o + 8] = acc[2 + q] * un[q] + b1;
         }
@@ -539,13 +570,13 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
   pdl_trigger();
 }
 
-template <bool GATEUP>
+template <bool GATEUP, bool PAIRED>
 void set_fp4_smem(int bytes) {
   static int done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || done[dev] >= bytes) return;
-  if (cudaFuncSetAttribute(fp4_stream_kernel<GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) ==
+  if (cudaFuncSetAttribute(fp4_stream_kernel<GATEUP, PAIRED>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) ==
       cudaSuccess)
     done[dev] = bytes;
 }
@@ -576,12 +607,16 @@ cudaError_t launch_fp4_stream(const uint8_t* codes, const F4Args& a0, int n_expe
     return cudaSuccess;
   a.tiles = (a.R + kRows - 1) / kRows;
   const int bytes = f4_smem(a.kin, a.stages).total + 1024;
-  set_fp4_smem<GATEUP>(bytes);
   const long long units = (long long)max_items * a.tiles;
   int grid = sm_count();
   if (units < grid) grid = (int)(units > 0 ? units : 1);
   *launched = true;
-  return launch_pdl(fp4_stream_kernel<GATEUP>, dim3(grid), dim3(kThreads), (size_t)bytes, s, m, a);
+  if ((a.kin / 32) % 2 == 0) {
+    set_fp4_smem<GATEUP, true>(bytes);
+    return launch_pdl(fp4_stream_kernel<GATEUP, true>, dim3(grid), dim3(kThreads), (size_t)bytes, s, m, a);
+  }
+  set_fp4_smem<GATEUP, false>(bytes);
+  return launch_pdl(fp4_stream_kernel<GATEUP, false>, dim3(grid), dim3(kThreads), (size_t)bytes, s, m, a);
 }
 
 }  // namespace
