@@ -18,11 +18,15 @@
 // is scaled once by 2^(s - 127) into the output fragment.  The scale is exact in fp32
 // for every byte (0 gives 2^-127, 255 NaN): a row's two scale bytes become a bf16
 // pair with one hardware conversion, or, for rows of an odd number of blocks, come
-// from a 256-entry table.  A block's token fragments serve both tiles of the pair.  Codes become exact
-// f16 pairs with cvt.rn.f16x2.e2m1x2.  The token operand is the item's rows staged
-// in shared memory as f16 scaled by 2^e per token (largest magnitude in
-// [2^14, 2^15)), so bf16 x is exact and h = hi + lo keeps 11 bits; the epilogue
-// removes 2^e.
+// from a 256-entry table.  A block's token fragments serve both tiles of the pair.
+// Codes become exact f16 pairs with cvt.rn.f16x2.e2m1x2.  The token operand is the
+// item's rows staged in shared memory as f16 scaled by 2^e per token (largest
+// magnitude in [2^14, 2^15)), so bf16 x is exact and h = hi + lo keeps 11 bits.
+//
+// At a unit's end the consumers leave their partial sums in shared memory and go on
+// to the next unit.  Warp 17 finishes the unit meanwhile: it adds the four block
+// classes of each tile, removes 2^e, adds the bias and writes h (after the
+// activation) or Y, so that this tail is off the consumers' path.
 //
 // Sources: "Phase 19: MoE - gpt-oss-20b", section 2 Experts (interleaved gate_up
 // with bias, clamped GLU, down with bias) and section 3 (MXFP4: E2M1 codes, low
@@ -39,7 +43,8 @@ namespace {
 constexpr int kTiles = 8;                         // 16-row MMA tiles per unit
 constexpr int kClasses = 4;                       // block classes (adjacent block pairs of a box)
 constexpr int kCW = kTiles / 2 * kClasses;        // consumer warps: one per (tile pair, block class)
-constexpr int kThreads = (kCW + 1) * 32;          // + the producer warp
+constexpr int kEpiWarp = kCW + 1;                  // warp kCW produces, warp kCW + 1 finishes units
+constexpr int kThreads = (kCW + 2) * 32;
 constexpr int kRows = 16 * kTiles;                // weight rows per unit
 constexpr int kBoxBytes = kRows * 128;            // one TMA box: 128 rows x 128 bytes of codes
 constexpr int kBlocksPerBox = 8;                  // 32-input blocks per box row
@@ -93,11 +98,6 @@ __device__ __forceinline__ float act_clamped(float g, float u, float limit, floa
 // Barrier among the consumer warps only (the producer keeps streaming).
 __device__ __forceinline__ void consumers_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kCW * 32) : "memory");
-}
-
-// Barrier among the four warps of one tile pair (named barriers 2 .. 2 + kTiles / 2 - 1).
-__device__ __forceinline__ void quad_sync(int tp) {
-  asm volatile("bar.sync %0, %1;" ::"r"(2 + tp), "n"(kClasses * 32) : "memory");
 }
 
 // volatile: it reads shared memory that an mbarrier wait (volatile asm) made valid,
@@ -325,9 +325,9 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = tc::smem_align1024(smem_raw);
   __shared__ __align__(8) uint64_t full_bar[kMaxRingStages], empty_bar[kMaxRingStages], sfull_bar[2],
-      sempty_bar[2];
+      sempty_bar[2], part_full, part_empty;
   __shared__ int abort_s;
-  __shared__ int esc[kTokens];
+  __shared__ int esc[2][kTokens];              // token exponents of the last two staged items
   __shared__ const uint8_t* trows[kTokens];
   __shared__ uint32_t rmax[kTokens];
 
@@ -346,6 +346,8 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
       tc::mbar_init(tc::smem_u32(&sfull_bar[i]), 1);
       tc::mbar_init(tc::smem_u32(&sempty_bar[i]), kCW);
     }
+    tc::mbar_init(tc::smem_u32(&part_full), kCW * 32);     // every consumer lane arrives
+    tc::mbar_init(tc::smem_u32(&part_empty), 32);          // every epilogue lane arrives
     abort_s = 0;
     tc::fence_barrier_init();
   }
@@ -411,11 +413,115 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
     return;
   }
 
+  if (warp == kEpiWarp) {
+    // ------------------------------------------------------------ epilogue warp
+    // Finishes every unit while the consumers stream the next one: it adds the four
+    // block classes' partial sums of each tile (in class order), removes the tokens'
+    // 2^e, adds the bias and writes h (gate_up, after the activation) or Y (down).
+    // The partial-sum buffer is single: the consumers write a unit's sums once this
+    // warp has read the previous unit's.  Lane (g, c) holds, per tile, rows g and
+    // g + 8 for tokens 2c and 2c + 1.
+    const int g = lane >> 2, c = lane & 3;
+    const bool odd = g & 1;
+    const float4* part = reinterpret_cast<const float4*>(smem + L.part) + lane;
+    int cur = -1, ns = 0, nu = 0;                // staged item, items staged, units finished
+    for (int u = u0; u < u1; ++u) {
+      const int ai = u / a.tiles, t = u - ai * a.tiles;
+      const int2 item = a.rs.work[ai];
+      const int v = item.x;
+      const int r0 = a.rs.offsets[v] + item.y;
+      const int n = min(kTokens, a.rs.offsets[v + 1] - r0);
+      if (ai != cur) {
+        cur = ai;
+        ++ns;
+      }
+      const int row0 = t * kRows, nrows = min(kRows, a.R - row0);
+      // biases and output rows first, so that their round trips overlap the wait
+      uint32_t bias[kTiles];                     // two bf16: (gate, up) of feature f, or rows o, o + 8
+#pragma unroll
+      for (int tile = 0; tile < kTiles; ++tile) {
+        bias[tile] = 0;
+        if (a.bias && 16 * tile < nrows) {
+          const uint16_t* bp = a.bias + (size_t)v * a.R +
+                               (GATEUP ? 2 * (row0 / 2 + 8 * tile + (odd ? 4 : 0) + (g >> 1)) : row0 + 16 * tile + g);
+          bias[tile] = (uint32_t)bp[0] | ((uint32_t)bp[GATEUP ? 1 : 8] << 16);
+        }
+      }
+      int yslot[2] = {-1, -1};
+      if (!GATEUP) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+          if (2 * c + k < n) yslot[k] = a.rs.row2slot[r0 + 2 * c + k];
+      }
+      if (!tc::mbar_wait(tc::smem_u32(&part_full), nu & 1, abort, status)) break;
+      float acc[kTiles][4];
+#pragma unroll
+      for (int tile = 0; tile < kTiles; ++tile) {
+        acc[tile][0] = acc[tile][1] = acc[tile][2] = acc[tile][3] = 0.f;
+        if (16 * tile < nrows) {
+#pragma unroll
+          for (int qq = 0; qq < kClasses; ++qq) {
+            const float4 o = part[(((tile >> 1) * kClasses + qq) * 2 + (tile & 1)) * 32];
+            acc[tile][0] += o.x;
+            acc[tile][1] += o.y;
+            acc[tile][2] += o.z;
+            acc[tile][3] += o.w;
+          }
+        }
+      }
+      const float un[2] = {exp2i(-esc[(ns - 1) & 1][2 * c]), exp2i(-esc[(ns - 1) & 1][2 * c + 1])};
+      tc::mbar_arrive(tc::smem_u32(&part_empty));
+      ++nu;
+      if (*abort) break;
+#pragma unroll
+      for (int tile = 0; tile < kTiles; ++tile) {
+        if (16 * tile >= nrows) break;
+        const float b0 = bf16_to_f32((uint16_t)(bias[tile] & 0xffffu)), b1 = bf16_to_f32((uint16_t)(bias[tile] >> 16));
+        if (GATEUP) {
+          // MMA row i is memory row row0 + 16 tile + i: feature (row0 + 16 tile + i) / 2,
+          // its gate when i is even.  Lanes g and g^1 (lane ^ 4) trade sums: even g
+          // finishes the feature of its row g, odd g the feature of its row g + 8.
+          float pr[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) pr[k] = __shfl_xor_sync(0xffffffffu, acc[tile][k], 4);
+          const int f = row0 / 2 + 8 * tile + (odd ? 4 : 0) + (g >> 1);
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int ti = 2 * c + k;
+            if (ti < n) {
+              const float gv = (odd ? pr[2 + k] : acc[tile][k]) * un[k] + b0;
+              const float uv = (odd ? acc[tile][2 + k] : pr[k]) * un[k] + b1;
+              const float hv =
+                  a.act == MOE_ACT_SWIGLU ? act_swiglu(gv, uv) : act_clamped(gv, uv, a.limit, a.alpha);
+              // h as a pair of bf16 (hi, lo = bf16(h - hi)), the layout both down paths read
+              const uint16_t hi = f32_to_bf16(hv);
+              uint16_t* hr = a.h + (size_t)(r0 + ti) * 2 * a.ldh + f;
+              hr[0] = hi;
+              hr[a.ldh] = f32_to_bf16(hv - bf16_to_f32(hi));
+            }
+          }
+        } else {
+          const int o = row0 + 16 * tile + g;
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            if (yslot[k] >= 0) {
+              float* yrow = a.Y + (size_t)yslot[k] * a.R;
+              yrow[o] = acc[tile][k] * un[k] + b0;
+              yrow[o + 8] = acc[tile][2 + k] * un[k] + b1;
+            }
+          }
+        }
+      }
+    }
+    pdl_trigger();
+    return;
+  }
+
   // -------------------------------------------------------------- consumers
   // Warp w owns tile pair tp = w % 4 (rows 32 tp .. 32 tp + 31 of the unit) and, in
   // every box, the two adjacent blocks of class qe = (w / 4 + unit) mod 4: a block's
-  // token fragments serve both tiles.  At the unit's end the four warps of a pair add their
-  // sums in shared memory, and warps q = 0, 1 finish tiles 2 tp and 2 tp + 1.
+  // token fragments serve both tiles.  At the unit's end every warp leaves its two
+  // tiles' partial sums in shared memory for the epilogue warp and goes on.
   const int tp = warp % (kTiles / 2), q = warp / (kTiles / 2);
   const int g = lane >> 2, c = lane & 3;
   const int mi = lane >> 3, ri = lane & 7;        // this lane's ldmatrix address: matrix, row
@@ -423,6 +529,7 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
   const uint8_t* tg = tok + g * L.pitch + 16 * c; // token column g, inputs 8c.. of each block
   float4* part = reinterpret_cast<float4*>(smem + L.part) + (tp * kClasses) * 2 * 32 + lane;
   int st = 0, its = 0, cur = -1;               // ring slot, scale loads consumed, staged item
+  int ns = 0, nu = 0;                            // items staged, units handed to the epilogue warp
   uint32_t ph = 0;                               // phase parity of ring slot st
   for (int u = u0; u < u1; ++u) {
     // On abort every wait returns at once; the loop still runs to its end so that
@@ -447,34 +554,14 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
         trows[i] = p;
       }
       consumers_sync();
-      stage_tokens<!GATEUP>(tok, L.pitch, trows, n, a.kin, (size_t)a.ldh * 2, esc, rmax, warp, lane);
+      // the epilogue warp has read the exponents of every unit of the item two back
+      stage_tokens<!GATEUP>(tok, L.pitch, trows, n, a.kin, (size_t)a.ldh * 2, esc[ns & 1], rmax, warp, lane);
       consumers_sync();
       cur = ai;
+      ++ns;
     }
     const int row0 = t * kRows, nrows = min(kRows, a.R - row0);
     const bool on = 32 * tp < nrows;             // nrows is a multiple of 32
-    // The epilogue's global operands (biases; for down the output rows) are fetched
-    // now, so that their round trip to memory overlaps the k loop instead of
-    // stalling the end of the unit.
-    const int tile = 2 * tp + (q & 1);
-    const bool odd = g & 1;
-    // gate_up: feature f of this lane; down: output rows o and o + 8
-    const int f = row0 / 2 + 8 * tile + (odd ? 4 : 0) + (g >> 1);
-    const int o = row0 + 16 * tile + g;
-    uint16_t bias_a = 0, bias_b = 0;
-    int yslot[2] = {-1, -1};
-    if (on && q < 2) {
-      if (a.bias) {
-        const uint16_t* bp = a.bias + (size_t)v * a.R + (GATEUP ? 2 * f : o);
-        bias_a = bp[0];
-        bias_b = bp[GATEUP ? 1 : 8];
-      }
-      if (!GATEUP) {
-#pragma unroll
-        for (int k = 0; k < 2; ++k)
-          if (2 * c + k < n) yslot[k] = a.rs.row2slot[r0 + 2 * c + k];
-      }
-    }
     const int sb = its & 1;
     bool ok = tc::mbar_wait(tc::smem_u32(&sfull_bar[sb]), (its >> 1) & 1, abort, status);
     const uint8_t* sc = smem + L.scales + sb * L.scale_bytes + (32 * tp + g) * L.nb;
@@ -508,64 +595,15 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sempty_bar[sb]));
     ++its;
-    if (!on) continue;
-    // the pair's four block classes add up in class order; warp q < 2 takes tile 2 tp + q
+    // hand the unit's partial sums to the epilogue warp, once it has read the last ones
+    ok = tc::mbar_wait(tc::smem_u32(&part_empty), (nu & 1) ^ 1, abort, status) && ok;
+    if (ok && on) {
 #pragma unroll
-    for (int t2 = 0; t2 < 2; ++t2)
-      part[(q * 2 + t2) * 32] = make_float4(acc2[t2][0], acc2[t2][1], acc2[t2][2], acc2[t2][3]);
-    quad_sync(tp);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (q < 2) {
-#pragma unroll
-      for (int qq = 0; qq < kClasses; ++qq) {
-        const float4 o = part[(qq * 2 + q) * 32];
-        acc[0] += o.x;
-        acc[1] += o.y;
-        acc[2] += o.z;
-        acc[3] += o.w;
-      }
+      for (int t2 = 0; t2 < 2; ++t2)
+        part[(q * 2 + t2) * 32] = make_float4(acc2[t2][0], acc2[t2][1], acc2[t2][2], acc2[t2][3]);
     }
-    quad_sync(tp);                               // read before the next unit writes
-    if (q >= 2 || !ok) continue;
-
-    // ------------------------------------------------------------ epilogue
-    // acc: rows g (tokens 2c, 2c+1) and g+8 of the tile, times 2^e of the token.
-    const float un[2] = {exp2i(-esc[2 * c]), exp2i(-esc[2 * c + 1])};
-    if (GATEUP) {
-      // MMA row i is memory row row0 + 16 tile + i: feature (row0 + 16 tile + i) / 2, its gate
-      // when i is even.  Lanes g and g^1 (lane ^ 4) trade accumulators: even g finishes
-      // the feature of its row g, odd g the feature of its row g + 8.
-      float pr[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) pr[k] = __shfl_xor_sync(0xffffffffu, acc[k], 4);
-      const float gt[2] = {odd ? pr[2] : acc[0], odd ? pr[3] : acc[1]};
-      const float upv[2] = {odd ? acc[2] : pr[0], odd ? acc[3] : pr[1]};
-      const float bg = bf16_to_f32(bias_a), bu = bf16_to_f32(bias_b);
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int ti = 2 * c + q;
-        if (ti < n) {
-          const float gv = gt[q] * un[q] + bg, uv = upv[q] * un[q] + bu;
-          const float hv =
-              a.act == MOE_ACT_SWIGLU ? act_swiglu(gv, uv) : act_clamped(gv, uv, a.limit, a.alpha);
-          // h as a pair of bf16 (hi, lo = bf16(h - hi)), the layout both down paths read
-          const uint16_t hi = f32_to_bf16(hv);
-          uint16_t* hr = a.h + (size_t)(r0 + ti) * 2 * a.ldh + f;
-          hr[0] = hi;
-          hr[a.ldh] = f32_to_bf16(hv - bf16_to_f32(hi));
-        }
-      }
-    } else {
-      const float b0 = bf16_to_f32(bias_a), b1 = bf16_to_f32(bias_b);
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        if (yslot[q] >= 0) {
-          float* yrow = a.Y + (size_t)yslot[q] * a.R;
-          yrow[o] = acc[q] * un[q] + b0;
-          yrow[o + 8] = acc[2 + q] * un[q] + b1;
-        }
-      }
-    }
+    tc::mbar_arrive(tc::smem_u32(&part_full));
+    ++nu;
   }
   pdl_trigger();
 }
