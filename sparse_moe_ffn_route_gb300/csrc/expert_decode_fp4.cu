@@ -24,9 +24,10 @@
 // magnitude in [2^14, 2^15)), so bf16 x is exact and h = hi + lo keeps 11 bits.
 //
 // At a unit's end the consumers leave their partial sums in shared memory and go on
-// to the next unit.  Warp 17 finishes the unit meanwhile: it adds the four block
-// classes of each tile, removes 2^e, adds the bias and writes h (after the
-// activation) or Y, so that this tail is off the consumers' path.
+// to the next unit.  Warps 17 and 18 (on two other schedulers, four tiles each)
+// finish the unit meanwhile: they add the four block classes of each tile, remove
+// 2^e, add the bias and write h (after the activation) or Y, so that this tail is
+// off the consumers' path and no scheduler carries all of it.
 //
 // Sources: "Phase 19: MoE - gpt-oss-20b", section 2 Experts (interleaved gate_up
 // with bias, clamped GLU, down with bias) and section 3 (MXFP4: E2M1 codes, low
@@ -43,8 +44,9 @@ namespace {
 constexpr int kTiles = 8;                         // 16-row MMA tiles per unit
 constexpr int kClasses = 4;                       // block classes (adjacent block pairs of a box)
 constexpr int kCW = kTiles / 2 * kClasses;        // consumer warps: one per (tile pair, block class)
-constexpr int kEpiWarp = kCW + 1;                  // warp kCW produces, warp kCW + 1 finishes units
-constexpr int kThreads = (kCW + 2) * 32;
+constexpr int kEpiWarps = 2;                       // warp kCW produces, warps kCW + 1.. finish units
+constexpr int kEpiTiles = kTiles / kEpiWarps;      // tiles finished by one epilogue warp
+constexpr int kThreads = (kCW + 1 + kEpiWarps) * 32;
 constexpr int kRows = 16 * kTiles;                // weight rows per unit
 constexpr int kBoxBytes = kRows * 128;            // one TMA box: 128 rows x 128 bytes of codes
 constexpr int kBlocksPerBox = 8;                  // 32-input blocks per box row
@@ -347,7 +349,7 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
       tc::mbar_init(tc::smem_u32(&sempty_bar[i]), kCW);
     }
     tc::mbar_init(tc::smem_u32(&part_full), kCW * 32);     // every consumer lane arrives
-    tc::mbar_init(tc::smem_u32(&part_empty), 32);          // every epilogue lane arrives
+    tc::mbar_init(tc::smem_u32(&part_empty), kEpiWarps * 32);   // every epilogue lane arrives
     abort_s = 0;
     tc::fence_barrier_init();
   }
@@ -413,16 +415,17 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
     return;
   }
 
-  if (warp == kEpiWarp) {
-    // ------------------------------------------------------------ epilogue warp
-    // Finishes every unit while the consumers stream the next one: it adds the four
+  if (warp > kCW) {
+    // ------------------------------------------------------------ epilogue warps
+    // Finish every unit while the consumers stream the next one: each adds the four
     // block classes' partial sums of each tile (in class order), removes the tokens'
     // 2^e, adds the bias and writes h (gate_up, after the activation) or Y (down).
-    // The partial-sum buffer is single: the consumers write a unit's sums once this
-    // warp has read the previous unit's.  Lane (g, c) holds, per tile, rows g and
+    // The partial-sum buffer is single: the consumers write a unit's sums once both
+    // warps have read the previous unit's.  Lane (g, c) holds, per tile, rows g and
     // g + 8 for tokens 2c and 2c + 1.
     const int g = lane >> 2, c = lane & 3;
     const bool odd = g & 1;
+    const int tile0 = (warp - kCW - 1) * kEpiTiles;   // this warp's tiles: tile0 .. + kEpiTiles - 1
     const float4* part = reinterpret_cast<const float4*>(smem + L.part) + lane;
     int cur = -1, ns = 0, nu = 0;                // staged item, items staged, units finished
     for (int u = u0; u < u1; ++u) {
@@ -437,14 +440,15 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
       }
       const int row0 = t * kRows, nrows = min(kRows, a.R - row0);
       // biases and output rows first, so that their round trips overlap the wait
-      uint32_t bias[kTiles];                     // two bf16: (gate, up) of feature f, or rows o, o + 8
+      uint32_t bias[kEpiTiles];                  // two bf16: (gate, up) of feature f, or rows o, o + 8
 #pragma unroll
-      for (int tile = 0; tile < kTiles; ++tile) {
-        bias[tile] = 0;
+      for (int i = 0; i < kEpiTiles; ++i) {
+        const int tile = tile0 + i;
+        bias[i] = 0;
         if (a.bias && 16 * tile < nrows) {
           const uint16_t* bp = a.bias + (size_t)v * a.R +
                                (GATEUP ? 2 * (row0 / 2 + 8 * tile + (odd ? 4 : 0) + (g >> 1)) : row0 + 16 * tile + g);
-          bias[tile] = (uint32_t)bp[0] | ((uint32_t)bp[GATEUP ? 1 : 8] << 16);
+          bias[i] = (uint32_t)bp[0] | ((uint32_t)bp[GATEUP ? 1 : 8] << 16);
         }
       }
       int yslot[2] = {-1, -1};
@@ -454,18 +458,19 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
           if (2 * c + k < n) yslot[k] = a.rs.row2slot[r0 + 2 * c + k];
       }
       if (!tc::mbar_wait(tc::smem_u32(&part_full), nu & 1, abort, status)) break;
-      float acc[kTiles][4];
+      float acc[kEpiTiles][4];
 #pragma unroll
-      for (int tile = 0; tile < kTiles; ++tile) {
-        acc[tile][0] = acc[tile][1] = acc[tile][2] = acc[tile][3] = 0.f;
+      for (int i = 0; i < kEpiTiles; ++i) {
+        const int tile = tile0 + i;
+        acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
         if (16 * tile < nrows) {
 #pragma unroll
           for (int qq = 0; qq < kClasses; ++qq) {
             const float4 o = part[(((tile >> 1) * kClasses + qq) * 2 + (tile & 1)) * 32];
-            acc[tile][0] += o.x;
-            acc[tile][1] += o.y;
-            acc[tile][2] += o.z;
-            acc[tile][3] += o.w;
+            acc[i][0] += o.x;
+            acc[i][1] += o.y;
+            acc[i][2] += o.z;
+            acc[i][3] += o.w;
           }
         }
       }
@@ -474,23 +479,24 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
       ++nu;
       if (*abort) break;
 #pragma unroll
-      for (int tile = 0; tile < kTiles; ++tile) {
+      for (int i = 0; i < kEpiTiles; ++i) {
+        const int tile = tile0 + i;
         if (16 * tile >= nrows) break;
-        const float b0 = bf16_to_f32((uint16_t)(bias[tile] & 0xffffu)), b1 = bf16_to_f32((uint16_t)(bias[tile] >> 16));
+        const float b0 = bf16_to_f32((uint16_t)(bias[i] & 0xffffu)), b1 = bf16_to_f32((uint16_t)(bias[i] >> 16));
         if (GATEUP) {
           // MMA row i is memory row row0 + 16 tile + i: feature (row0 + 16 tile + i) / 2,
           // its gate when i is even.  Lanes g and g^1 (lane ^ 4) trade sums: even g
           // finishes the feature of its row g, odd g the feature of its row g + 8.
           float pr[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) pr[k] = __shfl_xor_sync(0xffffffffu, acc[tile][k], 4);
+          for (int k = 0; k < 4; ++k) pr[k] = __shfl_xor_sync(0xffffffffu, acc[i][k], 4);
           const int f = row0 / 2 + 8 * tile + (odd ? 4 : 0) + (g >> 1);
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
             const int ti = 2 * c + k;
             if (ti < n) {
-              const float gv = (odd ? pr[2 + k] : acc[tile][k]) * un[k] + b0;
-              const float uv = (odd ? acc[tile][2 + k] : pr[k]) * un[k] + b1;
+              const float gv = (odd ? pr[2 + k] : acc[i][k]) * un[k] + b0;
+              const float uv = (odd ? acc[i][2 + k] : pr[k]) * un[k] + b1;
               const float hv =
                   a.act == MOE_ACT_SWIGLU ? act_swiglu(gv, uv) : act_clamped(gv, uv, a.limit, a.alpha);
               // h as a pair of bf16 (hi, lo = bf16(h - hi)), the layout both down paths read
@@ -506,8 +512,8 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
           for (int k = 0; k < 2; ++k) {
             if (yslot[k] >= 0) {
               float* yrow = a.Y + (size_t)yslot[k] * a.R;
-              yrow[o] = acc[tile][k] * un[k] + b0;
-              yrow[o + 8] = acc[tile][2 + k] * un[k] + b1;
+              yrow[o] = acc[i][k] * un[k] + b0;
+              yrow[o + 8] = acc[i][2 + k] * un[k] + b1;
             }
           }
         }
