@@ -55,8 +55,9 @@ constexpr int kStageBytes = kBoxes * kBoxBytes;
 constexpr int kBlocksPerStage = kBoxes * kBlocksPerBox;
 constexpr int kMaxRingStages = 8;
 constexpr int kTokens = 8;                        // token rows per work item
+constexpr int kScaleBufs = 3;                     // scale buffers: a unit's scales land a unit ahead
 
-// Shared memory, from a 1024-aligned base: ring stages | scale buffers (2) |
+// Shared memory, from a 1024-aligned base: ring stages | scale buffers (3) |
 // scale table | partial sums | token rows.
 struct F4Smem {
   int stages, nb;            // ring depth; 32-input blocks per weight row
@@ -79,7 +80,7 @@ __host__ __device__ inline F4Smem f4_smem(int kin, int stages) {
   m.pitch = token_pitch(kin);
   m.ring = 0;
   m.scales = stages * kStageBytes;
-  m.lut = m.scales + 2 * m.scale_bytes;
+  m.lut = m.scales + kScaleBufs * m.scale_bytes;
   m.part = m.lut + 256 * 4;                        // partial sums [pair][class][tile][32][4]
   m.tok = m.part + kCW * 2 * 32 * 16;
   m.total = m.tok + kTokens * m.pitch;
@@ -326,8 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = tc::smem_align1024(smem_raw);
-  __shared__ __align__(8) uint64_t full_bar[kMaxRingStages], empty_bar[kMaxRingStages], sfull_bar[2],
-      sempty_bar[2], part_full, part_empty;
+  __shared__ __align__(8) uint64_t full_bar[kMaxRingStages], empty_bar[kMaxRingStages], sfull_bar[kScaleBufs],
+      sempty_bar[kScaleBufs], part_full, part_empty;
   __shared__ int abort_s;
   __shared__ int esc[2][kTokens];              // token exponents of the last two staged items
   __shared__ const uint8_t* trows[kTokens];
@@ -344,7 +345,7 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
       tc::mbar_init(tc::smem_u32(&full_bar[i]), 1);
       tc::mbar_init(tc::smem_u32(&empty_bar[i]), kCW * 32);   // every consumer lane arrives
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kScaleBufs; ++i) {
       tc::mbar_init(tc::smem_u32(&sfull_bar[i]), 1);
       tc::mbar_init(tc::smem_u32(&sempty_bar[i]), kCW);
     }
@@ -371,18 +372,30 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
       int it = 0, its = 0;                      // ring loads, scale loads issued
       int st = 0;                               // ring slot of load `it`
       uint32_t ph = 0;                          // its phase parity
-      for (int u = u0; u < u1 && !*abort; ++u) {
+      // The scale bytes of unit u go to buffer (u - u0) % kScaleBufs and are requested
+      // a unit ahead of its codes, so that the copy has a whole unit's time to land;
+      // the buffer's previous unit (u - 3) is long done by then.
+      auto load_scales = [&](int u) -> bool {
         const int ai = u / a.tiles, t = u - ai * a.tiles;
         const int v = a.rs.work[ai].x;
         const int row0 = t * kRows, nrows = min(kRows, a.R - row0);
         const long long grow = (long long)v * a.R + row0;
-        const int sb = its & 1;
-        if (!tc::mbar_wait(tc::smem_u32(&sempty_bar[sb]), ((its >> 1) & 1) ^ 1, abort, status)) break;
+        const int sb = its % kScaleBufs;
+        if (!tc::mbar_wait(tc::smem_u32(&sempty_bar[sb]), ((its / kScaleBufs) & 1) ^ 1, abort, status))
+          return false;
         const uint32_t sbytes = (uint32_t)(nrows * L.nb);
         tc::mbar_arrive_expect_tx(tc::smem_u32(&sfull_bar[sb]), sbytes);
         bulk_load(tc::smem_u32(smem + L.scales + sb * L.scale_bytes), a.scales + grow * L.nb, sbytes,
                   tc::smem_u32(&sfull_bar[sb]));
         ++its;
+        return true;
+      };
+      bool live = u0 >= u1 || load_scales(u0);
+      for (int u = u0; u < u1 && live && !*abort; ++u) {
+        if (u + 1 < u1 && !load_scales(u + 1)) break;
+        const int ai = u / a.tiles, t = u - ai * a.tiles;
+        const int v = a.rs.work[ai].x;
+        const long long grow = (long long)v * a.R + t * kRows;
         for (int s = 0; s < nst; ++s) {
           if (!tc::mbar_wait(tc::smem_u32(&empty_bar[st]), ph ^ 1, abort, status)) break;
           // only the boxes that start inside the row (kin / 2 bytes)
@@ -406,8 +419,8 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
         volatile int* never = &zero;
         for (int i = it - a.stages > 0 ? it - a.stages : 0; i < it; ++i)
           tc::mbar_wait(tc::smem_u32(&full_bar[i % a.stages]), (i / a.stages) & 1, never, status);
-        for (int i = its - 2 > 0 ? its - 2 : 0; i < its; ++i)
-          tc::mbar_wait(tc::smem_u32(&sfull_bar[i & 1]), (i >> 1) & 1, never, status);
+        for (int i = its - kScaleBufs > 0 ? its - kScaleBufs : 0; i < its; ++i)
+          tc::mbar_wait(tc::smem_u32(&sfull_bar[i % kScaleBufs]), (i / kScaleBufs) & 1, never, status);
       }
     }
     // no early signal to the dependent launch: the consumers give it when the CTA's
@@ -568,8 +581,8 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
     }
     const int row0 = t * kRows, nrows = min(kRows, a.R - row0);
     const bool on = 32 * tp < nrows;             // nrows is a multiple of 32
-    const int sb = its & 1;
-    bool ok = tc::mbar_wait(tc::smem_u32(&sfull_bar[sb]), (its >> 1) & 1, abort, status);
+    const int sb = its % kScaleBufs;
+    bool ok = tc::mbar_wait(tc::smem_u32(&sfull_bar[sb]), (its / kScaleBufs) & 1, abort, status);
     const uint8_t* sc = smem + L.scales + sb * L.scale_bytes + (32 * tp + g) * L.nb;
     float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     // the block pair this warp takes in every box turns with the unit, so that the
