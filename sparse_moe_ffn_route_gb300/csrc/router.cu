@@ -26,13 +26,14 @@ template <int MT, int NT, int WARPS, int STEPS>
 __global__ void __launch_bounds__(WARPS * 32)
 router_logits_kernel(const uint16_t* __restrict__ x, int T, int d, const uint16_t* __restrict__ w_r,
                      const uint16_t* __restrict__ bias, const uint16_t* __restrict__ wsh, int E,
-                     float* __restrict__ logits, int ldl, uint32_t* __restrict__ status) {
+                     float* __restrict__ logits, int ldl, int nsplit, size_t nstride,
+                     uint32_t* __restrict__ status) {
   constexpr int TM = 16 * MT, TN = 8 * NT;
   __shared__ float part[WARPS][TM][TN + 1];
   pdl_wait();
   pdl_trigger();
   // the first kernel of a call: start a clean device status
-  if (status && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *status = 0u;
+  if (status && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0) *status = 0u;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, c = lane & 3;
   const int t0 = blockIdx.x * TM;
@@ -62,8 +63,11 @@ router_logits_kernel(const uint16_t* __restrict__ x, int T, int d, const uint16_
 #pragma unroll
       for (int q = 0; q < 4; ++q) acc[m][n][q] = 0.f;
   const uint4 z = make_uint4(0, 0, 0, 0);
-  const int nk = d >> 5;
-  for (int s0 = warp; s0 < nk; s0 += WARPS * STEPS) {
+  // split-K: part blockIdx.z of nsplit takes the contiguous k steps [kb, nk)
+  const int nk_all = d >> 5;
+  const int kb = (int)((long long)nk_all * blockIdx.z / nsplit);
+  const int nk = (int)((long long)nk_all * (blockIdx.z + 1) / nsplit);
+  for (int s0 = kb + warp; s0 < nk; s0 += WARPS * STEPS) {
     uint4 A[STEPS][MT][2], B[STEPS][NT];
 #pragma unroll
     for (int s = 0; s < STEPS; ++s) {
@@ -105,8 +109,8 @@ router_logits_kernel(const uint16_t* __restrict__ x, int T, int d, const uint16_
       float v = 0.f;
 #pragma unroll
       for (int w = 0; w < WARPS; ++w) v += part[w][tt][ee];
-      if (e < E && bias) v += bf16_to_f32(bias[e]);
-      logits[(size_t)t * ldl + e] = v;
+      if (e < E && bias && blockIdx.z == 0) v += bf16_to_f32(bias[e]);
+      logits[blockIdx.z * nstride + (size_t)t * ldl + e] = v;
     }
   }
 }
@@ -274,6 +278,7 @@ router_select_kernel(const float* __restrict__ logits, int ldl, int nsplit, size
     for (int off = 16; off > 0; off >>= 1) sl += __shfl_xor_sync(0xffffffffu, sl, off);
   } else if (has_shared) {
     sl = row[E];
+    for (int p = 1; p < nsplit; ++p) sl += row[(size_t)p * nstride + E];   // in part order
   }
   if (has_shared && lane == 0) {
     const float sg = 1.f / (1.f + expf(-sl));
@@ -328,14 +333,28 @@ cudaError_t launch_router_logits(const uint16_t* x, int T, int d, const uint16_t
     return launch_router_gemm(x, T, d, w_r, bias, E, logits, ldl, parts, part_floats, nsplit, ppitch, status,
                               s);
   }
-  if (T <= 256) {   // latency-bound: many small CTAs, all loads of a warp in flight at once
-    dim3 grid((T + 15) / 16, (E1 + 15) / 16);
+  if (T <= 256) {
+    // Latency-bound: many small CTAs, all loads of a warp in flight at once.  When the
+    // (token, expert) tiles are too few to fill the SMs, d is split as well (parts of
+    // at least 16 k steps of 32) and the select kernel adds the parts in order.
+    dim3 grid((T + 15) / 16, (E1 + 15) / 16, 1);
+    const int tiles = (int)(grid.x * grid.y);
+    int ns = sm_count() / tiles;
+    if (ns > (d >> 5) / 16) ns = (d >> 5) / 16;
+    if (ns > 8) ns = 8;
+    if (parts && ns > 1 && (size_t)ns * (size_t)T * (size_t)E1 <= part_floats) {
+      grid.z = ns;
+      *nsplit = ns;
+      *ppitch = E1;
+      return launch_pdl(router_logits_kernel<1, 2, 16, 6>, grid, dim3(16 * 32), 0, s, x, T, d, w_r,
+                        bias, wsh, E, parts, E1, ns, (size_t)T * E1, status);
+    }
     return launch_pdl(router_logits_kernel<1, 2, 16, 6>, grid, dim3(16 * 32), 0, s, x, T, d, w_r,
-                      bias, wsh, E, logits, ldl, status);
+                      bias, wsh, E, logits, ldl, 1, (size_t)0, status);
   } else {          // throughput-bound: larger tiles, fewer re-reads of x and W_r from L2
     dim3 grid((T + 63) / 64, (E1 + 31) / 32);
     return launch_pdl(router_logits_kernel<4, 4, 4, 2>, grid, dim3(4 * 32), 0, s, x, T, d, w_r, bias,
-                      wsh, E, logits, ldl, status);
+                      wsh, E, logits, ldl, 1, (size_t)0, status);
   }
 }
 

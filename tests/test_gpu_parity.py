@@ -72,6 +72,10 @@ ROUTE_SPECS = [
     mi.small_spec("gptoss", 192, 16, 4, 64, 0, 520, bias=("normal", 0.1)),
     # enough m tiles for every SM: one part, still through the scratch
     mi.small_spec("qwen", 128, 16, 2, 32, 32, 19500, bias=("normal", 0.5)),
+    # few tokens and experts: the warp-MMA logits kernel with d cut into parts (4 and
+    # 5 here) that the select kernel adds, the shared-gate column included
+    mi.small_spec("qwen", 2048, 64, 8, 32, 32, 8, bias=("normal", 0.5)),
+    mi.small_spec("gptoss", 2880, 32, 4, 64, 0, 32, bias=("normal", 0.1)),
 ]
 
 
