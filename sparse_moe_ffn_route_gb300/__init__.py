@@ -343,6 +343,37 @@ def moe_ffn_forward_host(cfg: MoeCfg, x_host: torch.Tensor, router: Router, expe
     return y_host
 
 
+class BoundForwardHost:
+    """moe_ffn_forward_host with its arguments marshalled once, for repeated steps.
+
+    Each call runs one synchronous step exactly as moe_ffn_forward_host does (x_host's
+    current contents are copied in, y_host receives the layer's output) but skips the
+    per-call argument checks and ctypes marshalling.  The tensors given here must stay
+    alive and keep their storage while the object is used.
+    """
+
+    def __init__(self, cfg: MoeCfg, x_host: torch.Tensor, router: Router, experts: Experts,
+                 shared: Optional[Shared] = None, y_host=None, ws=None, stream=None):
+        if x_host.is_cuda:
+            raise ValueError("x_host must be a CPU tensor")
+        T = x_host.shape[0]
+        if y_host is None:
+            y_host = torch.empty(x_host.shape, dtype=torch.float32 if cfg.y_fp32 else torch.bfloat16)
+        self.ws = workspace(cfg, T) if ws is None else ws
+        self.cfg, self.x_host, self.y_host = cfg, x_host, y_host
+        self._keep = (router, experts, shared, _router(router), _experts(experts))
+        self._args = (ctypes.byref(cfg), x_host.data_ptr(), T, ctypes.byref(self._keep[3]),
+                      ctypes.byref(self._keep[4]), _shared(shared), y_host.data_ptr(), _ptr(self.ws),
+                      self.ws.numel(), _stream(stream))
+        self._fn = _lib.moe_ffn_forward_host
+
+    def __call__(self) -> torch.Tensor:
+        st = self._fn(*self._args)
+        if st != MOE_OK:
+            raise MoeError(st, "moe_ffn_forward_host")
+        return self.y_host
+
+
 def moe_mxfp4_to_bf16(blocks: torch.Tensor, scales: torch.Tensor, out=None,
                       stream=None) -> torch.Tensor:
     """blocks u8 [..., n_in/32, 16], scales u8 [..., n_in/32] -> bf16 [..., n_in]."""

@@ -335,6 +335,16 @@ def test_full_workload(name, full_layers):
     yu = buf[1:].view(T, spec.d_model)
     moe.moe_ffn_forward_host(c, xh, router, experts, shared, y_host=yu, ws=ws)
     assert torch.equal(yu.view(torch.int16), y.cpu().view(torch.int16))
+    # the bound call: the same step, x_host's contents read at each call
+    yb = torch.full((T, spec.d_model), float("nan"), dtype=torch.bfloat16).pin_memory()
+    step = moe.BoundForwardHost(c, xh, router, experts, shared, y_host=yb, ws=ws)
+    assert step() is yb and torch.equal(yb.view(torch.int16), y.cpu().view(torch.int16))
+    x0 = xh.clone()
+    xh.zero_()
+    step()
+    assert torch.equal(yb.view(torch.int16), moe.moe_ffn_forward_host(c, xh, router, experts, shared,
+                                                                       ws=ws).view(torch.int16))
+    xh.copy_(x0)
 
 
 # ----------------------------------------------------------------------------- prefill (tcgen05) path
