@@ -233,7 +233,13 @@ int moe_ffn_forward_routed(const moe_cfg_t* cfg, const void* x, int32_t T,
  * layer and synchronises `stream` before returning, so y_host is ready on return.
  * A page-locked y_host that has a device address (cudaHostAlloc, or cudaHostRegister
  * with mapping) and is 16-byte aligned is written by the last kernel directly;
- * other memory receives y through a workspace buffer and a device-to-host copy. */
+ * other memory receives y through a workspace buffer and a device-to-host copy.
+ * When x_host and y_host are both page-locked, the call's work (copies and kernels)
+ * is captured once as a CUDA graph and replayed by later calls with the same
+ * arguments (every pointer, cfg, T, ws and stream; the buffers' contents are read
+ * when the graph runs, as in a plain call); the library keeps the last four such
+ * graphs.  A stream that is itself being captured, or phase events set with
+ * moe_set_phase_events, take the plain path. */
 int moe_ffn_forward_host(const moe_cfg_t* cfg, const void* x_host, int32_t T,
                          const moe_router_t* router, const moe_experts_t* experts,
                          const moe_shared_t* shared, void* y_host, void* ws, size_t ws_bytes,

@@ -2,6 +2,7 @@
 // stream-ordered launch sequence of each entry point (see include/moe.h).
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 #include "internal.h"
 
@@ -513,6 +514,130 @@ int moe_ffn_forward_routed(const moe_cfg_t* cfg, const void* x, int32_t T,
   return run_experts(cfg, x, T, experts, shared, y, L, ws, s);
 }
 
+namespace {
+
+// The host entry's work on one stream, without the final synchronisation: x in,
+// the layer, y out (or y written across the host link by the combine kernel).
+int host_step(const moe_cfg_t* cfg, const void* x_host, int32_t T, const moe_router_t* router,
+              const moe_experts_t* experts, const moe_shared_t* shared, void* y_host, void* ydirect,
+              void* ws, size_t ws_bytes, const Layout& L, cudaStream_t s) {
+  void* xd = at<void>(ws, L.xstage);
+  void* yd = at<void>(ws, L.ystage);
+  const size_t bytes = (size_t)T * cfg->d_model * 2;
+  const size_t ybytes = (size_t)T * cfg->d_model * (cfg->y_fp32 ? 4 : 2);
+  MOE_CUDA(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s));
+  const int st = moe_ffn_forward(cfg, xd, T, router, experts, shared, ydirect ? ydirect : yd, nullptr,
+                                 nullptr, ws, ws_bytes, s);
+  if (st != MOE_OK) return st;
+  if (!ydirect) MOE_CUDA(cudaMemcpyAsync(y_host, yd, ybytes, cudaMemcpyDeviceToHost, s));
+  return MOE_OK;
+}
+
+// Repeated host-entry calls with the same arguments replay one CUDA graph of the
+// step (captured on a private stream, launched on the caller's): one launch per step
+// instead of one per kernel and copy, and no gaps between the kernels.  The key is
+// every argument (the tensors' contents are read when the graph runs, as in a plain
+// call).  Used when both host buffers are page-locked.
+struct HostGraphKey {
+  moe_cfg_t cfg;
+  moe_router_t router;
+  moe_experts_t experts;
+  moe_shared_t shared;
+  const void* x_host;
+  void* y_host;
+  void* ws;
+  size_t ws_bytes;
+  cudaStream_t stream;
+  int32_t T, has_shared, device;
+};
+
+constexpr int kHostGraphs = 4;
+struct HostGraph {
+  bool used;
+  HostGraphKey key;
+  cudaGraphExec_t exec;
+};
+std::mutex g_host_graph_mu;
+HostGraph g_host_graphs[kHostGraphs];   // not destroyed at exit: the driver reclaims them
+int g_host_graph_next = 0;
+cudaStream_t g_capture_stream[64] = {};
+
+bool page_locked(const void* p) {
+  cudaPointerAttributes pa;
+  if (cudaPointerGetAttributes(&pa, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  return pa.type == cudaMemoryTypeHost;
+}
+
+// Launches this call's cached graph on s (captured on first use; the launch happens
+// under the cache's lock, so that no other thread can retire the graph meanwhile).
+// cudaErrorNotReady: run the call directly instead (phase events set, the caller's
+// stream capturing, pageable buffers, or any failure to build the graph, which then
+// leaves no error behind).
+cudaError_t launch_host_graph(const moe_cfg_t* cfg, const void* x_host, int32_t T, const moe_router_t* router,
+                              const moe_experts_t* experts, const moe_shared_t* shared, void* y_host,
+                              void* ydirect, void* ws, size_t ws_bytes, const Layout& L, cudaStream_t s) {
+  constexpr cudaError_t kDirect = cudaErrorNotReady;
+  if (g_phase_events) return kDirect;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+    (void)cudaGetLastError();
+    return kDirect;
+  }
+  if (!page_locked(x_host) || !page_locked(y_host)) return kDirect;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return kDirect;
+  HostGraphKey key;
+  std::memset(&key, 0, sizeof(key));
+  key.cfg = *cfg;
+  key.router = *router;
+  key.experts = *experts;
+  if (shared) key.shared = *shared;
+  key.has_shared = shared != nullptr;
+  key.x_host = x_host;
+  key.y_host = y_host;
+  key.ws = ws;
+  key.ws_bytes = ws_bytes;
+  key.stream = s;
+  key.T = T;
+  key.device = dev;
+  std::lock_guard<std::mutex> lock(g_host_graph_mu);
+  for (HostGraph& g : g_host_graphs)
+    if (g.used && std::memcmp(&g.key, &key, sizeof(key)) == 0) return cudaGraphLaunch(g.exec, s);
+  if (!g_capture_stream[dev] &&
+      cudaStreamCreateWithFlags(&g_capture_stream[dev], cudaStreamNonBlocking) != cudaSuccess) {
+    (void)cudaGetLastError();
+    g_capture_stream[dev] = nullptr;
+    return kDirect;
+  }
+  const cudaStream_t cap = g_capture_stream[dev];
+  if (cudaStreamBeginCapture(cap, cudaStreamCaptureModeRelaxed) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return kDirect;
+  }
+  const int st = host_step(cfg, x_host, T, router, experts, shared, y_host, ydirect, ws, ws_bytes, L, cap);
+  cudaGraph_t graph = nullptr;
+  const cudaError_t ec = cudaStreamEndCapture(cap, &graph);
+  cudaGraphExec_t exec = nullptr;
+  if (st == MOE_OK && ec == cudaSuccess && graph &&
+      cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess)
+    exec = nullptr;
+  if (graph) cudaGraphDestroy(graph);
+  (void)cudaGetLastError();
+  if (!exec) return kDirect;
+  HostGraph& slot = g_host_graphs[g_host_graph_next];
+  g_host_graph_next = (g_host_graph_next + 1) % kHostGraphs;
+  if (slot.used) cudaGraphExecDestroy(slot.exec);   // launches still in flight complete
+  slot.used = true;
+  slot.key = key;
+  slot.exec = exec;
+  return cudaGraphLaunch(exec, s);
+}
+
+}  // namespace
+
 int moe_ffn_forward_host(const moe_cfg_t* cfg, const void* x_host, int32_t T,
                          const moe_router_t* router, const moe_experts_t* experts,
                          const moe_shared_t* shared, void* y_host, void* ws, size_t ws_bytes,
@@ -522,13 +647,11 @@ int moe_ffn_forward_host(const moe_cfg_t* cfg, const void* x_host, int32_t T,
   if (T < 0) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!x_host || !y_host) return MOE_ERR_INVALID_ARG;
+  if ((st = check_router(cfg, router)) != MOE_OK) return st;
+  if ((st = check_experts(cfg, experts, shared)) != MOE_OK) return st;
   Layout L;
   if ((st = check_ws(cfg, T, ws, ws_bytes, &L)) != MOE_OK) return st;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  void* xd = at<void>(ws, L.xstage);
-  void* yd = at<void>(ws, L.ystage);
-  const size_t bytes = (size_t)T * cfg->d_model * 2;
-  const size_t ybytes = (size_t)T * cfg->d_model * (cfg->y_fp32 ? 4 : 2);
   // Page-locked y_host with a device address (cudaHostAlloc, or cudaHostRegister
   // with mapping) takes the layer's output directly: the combine kernel writes it
   // across the host link, in place of a device staging buffer and a second copy.
@@ -541,11 +664,14 @@ int moe_ffn_forward_host(const moe_cfg_t* cfg, const void* x_host, int32_t T,
   } else {
     (void)cudaGetLastError();
   }
-  MOE_CUDA(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s));
-  st = moe_ffn_forward(cfg, xd, T, router, experts, shared, ydirect ? ydirect : yd, nullptr, nullptr,
-                       ws, ws_bytes, stream);
-  if (st != MOE_OK) return st;
-  if (!ydirect) MOE_CUDA(cudaMemcpyAsync(y_host, yd, ybytes, cudaMemcpyDeviceToHost, s));
+  const cudaError_t eg =
+      launch_host_graph(cfg, x_host, T, router, experts, shared, y_host, ydirect, ws, ws_bytes, L, s);
+  if (eg == cudaErrorNotReady) {
+    st = host_step(cfg, x_host, T, router, experts, shared, y_host, ydirect, ws, ws_bytes, L, s);
+    if (st != MOE_OK) return st;
+  } else {
+    MOE_CUDA(eg);
+  }
   MOE_CUDA(cudaStreamSynchronize(s));
   return MOE_OK;
 }

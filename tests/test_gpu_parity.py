@@ -347,6 +347,28 @@ def test_full_workload(name, full_layers):
     xh.copy_(x0)
 
 
+def test_host_entry_graph_cache():
+    """Page-locked host buffers: the host entry replays a cached graph per argument set.
+    Six sets (more than the four graphs kept) called in turn, twice, with new x each time,
+    give what the device-resident forward gives for the same x."""
+    moe = moe_lib()
+    spec = mi.small_spec("qwen", 256, 16, 4, 64, 64, 24, bias=("normal", 0.5))
+    lay = mi.make_layer(spec)
+    x, router, experts, shared = upload(lay)
+    c = cfg_for(spec)
+    T, d = spec.tokens, spec.d_model
+    ws = moe.workspace(c, T)
+    xh = torch.empty((T, d), dtype=torch.bfloat16).pin_memory()
+    ys = [torch.empty((T, d), dtype=torch.bfloat16).pin_memory() for _ in range(6)]
+    for rep in range(2):
+        for i, yh in enumerate(ys):
+            xs = mi.make_x(dataclasses.replace(spec, seed=spec.seed + 31 * i + 7 * rep), T)
+            xh.copy_(torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16))
+            moe.moe_ffn_forward_host(c, xh, router, experts, shared, y_host=yh, ws=ws)
+            want = moe.moe_ffn_forward(c, xh.cuda(), router, experts, shared, ws=ws)
+            assert torch.equal(yh.view(torch.int16), want.cpu().view(torch.int16)), (rep, i)
+
+
 # ----------------------------------------------------------------------------- prefill (tcgen05) path
 PREFILL_SPECS = [
     mi.small_spec("qwen", 128, 8, 2, 64, 64, 200),
