@@ -159,12 +159,14 @@ def expert_bytes(spec):
     return gu, dn, 2 * sff * d * 2, d * sff * 2
 
 
-def launches_per_step(plan, mxfp4, spec_slots):
+def launches_per_step(plan, mxfp4, spec_slots, tokens=0, n_experts=0):
     """Kernels of this library one moe_ffn_forward enqueues, by kernel plan."""
     router = 2                                            # logits, select
     permute = 3 if spec_slots > 2048 else 1               # count, scan, scatter (or one CTA)
     if plan in (1, 2):                                    # decode: gate_up, down, combine
-        return router + permute + 3
+        # up to 32 tokens, 256 experts, 2048 slots: the select kernel also permutes
+        fused = tokens <= 32 and n_experts <= 256 and spec_slots <= 2048
+        return router + (0 if fused else permute) + 3
     if plan == 3:                                         # 2 GEMMs, combine (MXFP4: 2 scale transposes, gather)
         return router + permute + 3 + (3 if mxfp4 else 0)
     return router + permute + 7   # 2 scale preps, gather, gate_up, h fix-up, down, combine
@@ -446,7 +448,8 @@ def run_ours(args, rank, world, local_rank):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "graph": graph_rec,
-        "gpu_launches": launches_per_step(plan, spec.mxfp4, T * (spec.top_k + (spec.shared_ff > 0))) * args.steps,
+        "gpu_launches": launches_per_step(plan, spec.mxfp4, T * (spec.top_k + (spec.shared_ff > 0)), T,
+                                          spec.n_experts) * args.steps,
         "clocks": sampler.summary(t0, t1),
         "phases_ms": phase_ms,
         "step_hbm_gbs": step_bytes / (ms / 1e3) / 1e9,

@@ -116,13 +116,16 @@ cudaError_t launch_router_gemm(const uint16_t* x, int T, int d, const uint16_t* 
 // partial sums nstride floats apart that are added in order (lsum [T, ldsum], when
 // non-null, receives the sums).  With has_shared, the shared-gate logit is column
 // E, or, when wsh is non-null, x_t . wsh computed here (x bf16 [T, d]).  Writes any
-// non-null output.
+// non-null output.  rs non-null (S = T * K <= 2048 slots, E1 virtual experts, work
+// items of tpg rows): the same launch then groups the slots by expert, in place of
+// launch_permute.
 cudaError_t launch_router_select(const float* logits, int ldl, int nsplit, size_t nstride, float* lsum,
                                  int ldsum, int T, int E, int k, int norm_topk_prob, float scale,
                                  int has_shared,
                                  int32_t* ids_out, float* w_out, float* sgate_out,
                                  int32_t* slot_expert, float* slot_w, const uint16_t* x, int d,
-                                 const uint16_t* wsh, cudaStream_t s);
+                                 const uint16_t* wsh, const RouteState* rs, int S, int E1, int tpg,
+                                 cudaStream_t s);
 
 // Copy caller routing into the slot arrays (routed entry point).
 cudaError_t launch_ingest_routing(const int32_t* ids, const float* w, const float* sgate, int T,

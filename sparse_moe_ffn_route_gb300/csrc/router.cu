@@ -7,6 +7,7 @@
 // section 2 Router (logits + bias, top-k, softmax over the chosen k).
 #include "common.cuh"
 #include "internal.h"
+#include "permute_core.cuh"
 
 namespace moe {
 namespace {
@@ -136,19 +137,43 @@ __device__ __forceinline__ float key_logit(uint32_t k) {
 // warp max over the lanes' best keys, one warp min over the indices that reach it;
 // the lane that gave up its entry then finds its next best.  Lane j keeps the j-th
 // pick.  (NaN logits are outside the routing's contract.)
-template <int EPL>
-__global__ void __launch_bounds__(kSelectWarps * 32)
-router_select_kernel(const float* __restrict__ logits, int ldl, int nsplit, size_t nstride,
-                     float* __restrict__ lsum, int ldsum, int T, int E, int k,
-                     int norm_topk_prob, float scale, int has_shared, int32_t* __restrict__ ids_out,
-                     float* __restrict__ w_out, float* __restrict__ sgate_out,
-                     int32_t* __restrict__ slot_expert, float* __restrict__ slot_w,
-                     const uint16_t* __restrict__ x, int d, const uint16_t* __restrict__ wsh) {
-  pdl_wait();
-  pdl_trigger();
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kSelectWarps + (threadIdx.x >> 5);
-  if (t >= T) return;
+// The selection for token t by one warp (lane = its lane).
+struct SelectArgs {
+  const float* logits;
+  int ldl, nsplit;
+  size_t nstride;
+  float* lsum;
+  int ldsum, T, E, k, norm_topk_prob;
+  float scale;
+  int has_shared;
+  int32_t* ids_out;
+  float* w_out;
+  float* sgate_out;
+  int32_t* slot_expert;
+  float* slot_w;
+  const uint16_t* x;
+  int d;
+  const uint16_t* wsh;
+};
+
+// DOT: the shared-gate dot x_t . wsh may be asked for (else the gate is column E).
+template <int EPL, bool DOT>
+__device__ __forceinline__ void select_token(const SelectArgs& a, int t, int lane) {
+  const float* __restrict__ logits = a.logits;
+  const int ldl = a.ldl, nsplit = a.nsplit;
+  const size_t nstride = a.nstride;
+  float* __restrict__ lsum = a.lsum;
+  const int ldsum = a.ldsum, E = a.E, k = a.k, norm_topk_prob = a.norm_topk_prob;
+  const float scale = a.scale;
+  const int has_shared = a.has_shared;
+  int32_t* __restrict__ ids_out = a.ids_out;
+  float* __restrict__ w_out = a.w_out;
+  float* __restrict__ sgate_out = a.sgate_out;
+  int32_t* __restrict__ slot_expert = a.slot_expert;
+  float* __restrict__ slot_w = a.slot_w;
+  const uint16_t* __restrict__ x = a.x;
+  const int d = a.d;
+  const uint16_t* __restrict__ wsh = a.wsh;
   const float* row = logits + (size_t)t * ldl;
   float v[EPL];
 #pragma unroll
@@ -248,7 +273,7 @@ router_select_kernel(const float* __restrict__ logits, int ldl, int nsplit, size
     }
   }
   float sl = 0.f;   // the shared-gate logit: column E of the logits, or w_sh . x here
-  if (has_shared && wsh) {
+  if (DOT && has_shared && wsh) {
     // pieces i = lane, lane + 32, ... in order, eight pieces' loads in flight at once
     constexpr int kDotBatch = 8;
     const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * d);
@@ -288,6 +313,28 @@ router_select_kernel(const float* __restrict__ logits, int ldl, int nsplit, size
       slot_w[(size_t)t * K + k] = sg;
     }
   }
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(kSelectWarps * 32) router_select_kernel(const SelectArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.x * kSelectWarps + (threadIdx.x >> 5);
+  if (t < a.T) select_token<EPL, true>(a, t, threadIdx.x & 31);
+}
+
+// Decode sizes: the selection of every token (a warp per token, in turn) and then
+// the grouping by expert in one CTA, one launch instead of two.
+template <int EPL>
+__global__ void __launch_bounds__(kPermuteThreads) select_permute_kernel(const SelectArgs a, RouteState rs,
+                                                                         int S, int E1, int tpg) {
+  __shared__ PermuteSmem sm;
+  pdl_wait();
+  pdl_trigger();
+  for (int t = threadIdx.x >> 5; t < a.T; t += kPermuteThreads / 32)
+    select_token<EPL, false>(a, t, threadIdx.x & 31);
+  __syncthreads();   // the slots are written: the block reads them back
+  permute_block(rs, S, E1, tpg, sm);
 }
 
 __global__ void ingest_routing_kernel(const int32_t* __restrict__ ids, const float* __restrict__ w,
@@ -363,14 +410,25 @@ cudaError_t launch_router_select(const float* logits, int ldl, int nsplit, size_
                                  int has_shared,
                                  int32_t* ids_out, float* w_out, float* sgate_out,
                                  int32_t* slot_expert, float* slot_w, const uint16_t* x, int d,
-                                 const uint16_t* wsh, cudaStream_t s) {
-  dim3 grid((T + kSelectWarps - 1) / kSelectWarps);
+                                 const uint16_t* wsh, const RouteState* rs, int S, int E1, int tpg,
+                                 cudaStream_t s) {
+  const SelectArgs a{logits, ldl, nsplit, nstride, lsum, ldsum, T, E, k, norm_topk_prob, scale, has_shared,
+                     ids_out, w_out, sgate_out, slot_expert, slot_w, x, d, wsh};
   const int epl = (E + 31) / 32;
-#define MOE_SELECT(N)                                                                     \
-  return launch_pdl(router_select_kernel<N>, grid, dim3(kSelectWarps * 32), 0, s, logits, ldl, nsplit, \
-                    nstride, lsum, ldsum, T,                                                          \
-                    E, k, norm_topk_prob, scale, has_shared, ids_out, w_out, sgate_out,       \
-                    slot_expert, slot_w, x, d, wsh)
+  // rs: also group the slots by expert in the same launch (one CTA); the shared gate
+  // must then come as logit column E
+  if (rs) {
+    // at most 256 experts (the widths that fit the 64 registers of a 1024-thread CTA)
+    if (wsh || S > kPermuteOneCtaSlots || epl > 8) return cudaErrorInvalidValue;
+#define MOE_SELECT(N) \
+  return launch_pdl(select_permute_kernel<N>, dim3(1), dim3(kPermuteThreads), 0, s, a, *rs, S, E1, tpg)
+    if (epl <= 1) MOE_SELECT(1);
+    else if (epl <= 4) MOE_SELECT(4);
+    else MOE_SELECT(8);
+#undef MOE_SELECT
+  }
+  dim3 grid((T + kSelectWarps - 1) / kSelectWarps);
+#define MOE_SELECT(N) return launch_pdl(router_select_kernel<N>, grid, dim3(kSelectWarps * 32), 0, s, a)
   if (epl <= 1) MOE_SELECT(1);
   else if (epl <= 2) MOE_SELECT(2);
   else if (epl <= 4) MOE_SELECT(4);
