@@ -248,6 +248,10 @@ int moe_ffn_forward_host(const moe_cfg_t* cfg, const void* x_host, int32_t T,
 /* Size of the device array that moe_ffn_forward_noalloc uses as its workspace. */
 #define MOE_NOALLOC_WORKSPACE_BYTES ((size_t)8 << 20)
 
+/* MOE_NOALLOC_WORKSPACE_BYTES as built into the library (for bindings that cannot
+ * read the header's macro).  Pure host function. */
+size_t moe_noalloc_workspace_bytes(void);
+
 /* moe_ffn_forward for callers that cannot allocate device memory.  (The pages
  * have no counterpart: this is an interface addition.)
  *
@@ -261,19 +265,34 @@ int moe_ffn_forward_host(const moe_cfg_t* cfg, const void* x_host, int32_t T,
  * allocating routine.
  *   - Arguments and results are those of moe_ffn_forward without ws/ws_bytes.
  *   - Returns MOE_ERR_WORKSPACE when moe_workspace_bytes(cfg, T) exceeds the
- *     array (above 86 tokens of the Qwen3.5-mini layer, 96 of gpt-oss-20b).
+ *     array: the largest batches that fit are 79 tokens of the Qwen3.5-mini
+ *     layer and 76 of gpt-oss-20b (76 and 72 with cfg.rms_norm, whose
+ *     normalised copy of x also lives in the workspace).
  *   - Every GPU that loads the library holds the array until the process exits.
- *   - The first call on a device, made with that device current, looks up the
- *     array's device address (cudaGetSymbolAddress) and keeps it; make that
- *     first call before any stream capture begins.
- *   - All calls on a device share the one array and it keeps the last call's
- *     contents (the kernels rewrite all scratch they read, so nothing carries
- *     over): calls that overlap on the GPU -- on different streams or from
- *     different host threads without ordering -- race and corrupt each other. */
+ *   - The array has its own device address in every CUDA context.  The first
+ *     call in a context (the device's primary context, a driver-API context the
+ *     host program made current, or the primary context re-created after
+ *     cudaDeviceReset) looks that address up (cudaGetSymbolAddress) and keeps it
+ *     under the context's unique id; make that first call before any stream
+ *     capture begins.  Up to 16 contexts are remembered at once.
+ *   - All calls in a context share the one array and it keeps the last call's
+ *     contents (the kernels rewrite all scratch they read, and the call's first
+ *     kernel clears the status word): calls that overlap on the GPU -- on
+ *     different streams or from different host threads without ordering -- race
+ *     and corrupt each other.
+ *   - Device-side checks of the call (a bounds check, a bounded wait that gave
+ *     up) are read with moe_noalloc_device_status. */
 int moe_ffn_forward_noalloc(const moe_cfg_t* cfg, const void* x, int32_t T,
                             const moe_router_t* router, const moe_experts_t* experts,
                             const moe_shared_t* shared, void* y, int32_t* topk_ids, float* topk_w,
                             void* stream);
+
+/* moe_device_status for moe_ffn_forward_noalloc: synchronises `stream`, then
+ * returns MOE_OK, MOE_ERR_DEVICE_CHECK or MOE_ERR_TIMEOUT according to the status
+ * word in the library's array for the current context, and clears it; *detail (if
+ * not NULL) receives the raw bits.  Reports the last noalloc call in this context
+ * that the stream has completed. */
+int moe_noalloc_device_status(void* stream, uint32_t* detail);
 
 /* Decode MXFP4 weights to bf16 with the decoder the expert kernels use on their
  * weight-load path.  Defined by "Phase 19: MoE - gpt-oss-20b", section 3

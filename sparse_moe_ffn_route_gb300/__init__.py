@@ -109,6 +109,10 @@ def _load():
                                             ctypes.POINTER(_Experts), ctypes.POINTER(_Shared), P,
                                             P, P, P]
     lib.moe_ffn_forward_noalloc.restype = I
+    lib.moe_noalloc_workspace_bytes.argtypes = []
+    lib.moe_noalloc_workspace_bytes.restype = ctypes.c_size_t
+    lib.moe_noalloc_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+    lib.moe_noalloc_device_status.restype = I
     lib.moe_mxfp4_to_bf16.argtypes = [P, P, ctypes.c_int64, ctypes.c_int32, P, P]
     lib.moe_mxfp4_to_bf16.restype = I
     lib.moe_set_phase_events.argtypes = [P, ctypes.c_int32]
@@ -123,7 +127,7 @@ def _load():
 _lib = _load()
 EXPORTED = ("moe_workspace_bytes", "moe_select_path", "moe_kernel_plan", "moe_route", "moe_topk_from_logits",
             "moe_ffn_forward", "moe_ffn_forward_routed", "moe_ffn_forward_host",
-            "moe_ffn_forward_noalloc",
+            "moe_ffn_forward_noalloc", "moe_noalloc_workspace_bytes", "moe_noalloc_device_status",
             "moe_mxfp4_to_bf16", "moe_set_phase_events", "moe_device_status",
             "moe_status_string")
 PHASES = ("router_logits", "router_select", "permute", "gate_up", "down", "combine")
@@ -290,15 +294,20 @@ def moe_ffn_forward(cfg: MoeCfg, x: torch.Tensor, router: Router, experts: Exper
     return y
 
 
-NOALLOC_WORKSPACE_BYTES = 8 << 20
+def moe_noalloc_workspace_bytes() -> int:
+    """Size of the library's own device array that moe_ffn_forward_noalloc works in."""
+    return int(_lib.moe_noalloc_workspace_bytes())
+
+
+NOALLOC_WORKSPACE_BYTES = moe_noalloc_workspace_bytes()
 
 
 def moe_ffn_forward_noalloc(cfg: MoeCfg, x: torch.Tensor, router: Router, experts: Experts,
                             shared: Optional[Shared] = None, y=None, topk_ids=None, topk_w=None,
                             stream=None) -> torch.Tensor:
     """moe_ffn_forward for callers that cannot allocate device memory: the library's own
-    8 MiB device array serves as workspace (see include/moe.h).  Only `y` is allocated
-    here when it is not passed in."""
+    device array (NOALLOC_WORKSPACE_BYTES) serves as workspace (see include/moe.h).  Only
+    `y` is allocated here when it is not passed in."""
     T = x.shape[0]
     if y is None:
         y = torch.empty(x.shape, dtype=torch.float32 if cfg.y_fp32 else torch.bfloat16,
@@ -409,6 +418,14 @@ def moe_device_status(ws: torch.Tensor, stream=None):
     """(status, raw bits) of the device check word; synchronises the stream and clears it."""
     bits = ctypes.c_uint32(0)
     st = _lib.moe_device_status(_ptr(ws), _stream(stream), ctypes.byref(bits))
+    return st, bits.value
+
+
+def moe_noalloc_device_status(stream=None):
+    """(status, raw bits) of the device check word of the last moe_ffn_forward_noalloc
+    call in the current context; synchronises the stream and clears it."""
+    bits = ctypes.c_uint32(0)
+    st = _lib.moe_noalloc_device_status(_stream(stream), ctypes.byref(bits))
     return st, bits.value
 
 

@@ -1,12 +1,13 @@
-"""moe_ffn_forward_noalloc: the layer without a caller workspace (GPU only).
+"""moe_ffn_forward_noalloc: the layer without a caller workspace.
 
 Callers that are handed only input and output buffers (a plug-in inside a host
 program whose memory pool owns the device, or a loop that must not call anything
 that may synchronise the device) cannot allocate the workspace moe_ffn_forward
 needs; this entry point uses an 8 MiB device array held by the library instead.
-The test calls it through the C ABI twice in a row and compares both results
-with moe_ffn_forward's on the same inputs, within the layer tolerance.  This file
-is collected last on purpose.
+The GPU test calls it through the C ABI twice in a row, compares both results with
+moe_ffn_forward's on the same inputs within the layer tolerance, and reads the
+device status word of each call through moe_noalloc_device_status.  This file is
+collected last on purpose.
 """
 import numpy as np
 import pytest
@@ -14,7 +15,6 @@ import pytest
 import moe_inputs as mi
 from gpu_util import TOL_RMS, cfg_for, moe_lib, need_gpu, upload
 
-pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 SPECS = [
@@ -23,6 +23,20 @@ SPECS = [
 ]
 
 
+def test_noalloc_size_and_token_limits():
+    """The array's size comes from the library, and the batch limits the header states
+    (79 Qwen3.5-mini tokens, 76 gpt-oss-20b; 76 and 72 with the RMSNorm) are the last
+    T whose workspace fits it."""
+    moe = moe_lib()
+    assert moe.NOALLOC_WORKSPACE_BYTES == moe.moe_noalloc_workspace_bytes() == 8 << 20
+    for cfg, rms_norm, last in ((moe.qwen_cfg(), 0, 79), (moe.gptoss_cfg(), 0, 76),
+                                (moe.qwen_cfg(), 1, 76), (moe.gptoss_cfg(), 1, 72)):
+        c = cfg.replace(rms_norm=rms_norm, rms_eps=1e-6)
+        assert moe.moe_workspace_bytes(c, last) <= moe.NOALLOC_WORKSPACE_BYTES
+        assert moe.moe_workspace_bytes(c, last + 1) > moe.NOALLOC_WORKSPACE_BYTES
+
+
+@pytest.mark.gpu
 @pytest.mark.parametrize("spec", SPECS, ids=lambda s: s.name)
 def test_noalloc_matches_forward_twice(spec):
     need_gpu()
@@ -36,12 +50,14 @@ def test_noalloc_matches_forward_twice(spec):
         for _ in range(2):
             ids = torch.empty((spec.tokens, spec.top_k), dtype=torch.int32, device="cuda")
             y = moe.moe_ffn_forward_noalloc(c, x, router, experts, shared, topk_ids=ids)
-            torch.cuda.synchronize()
+            st, bits = moe.moe_noalloc_device_status()
+            assert st == 0 and bits == 0, (st, bits)
             got = y.float().cpu().numpy()
             assert np.max(np.abs(got - ref)) <= TOL_RMS * rms
             assert ids.min().item() >= 0 and ids.max().item() < spec.n_experts
 
 
+@pytest.mark.gpu
 def test_noalloc_rejects_too_many_tokens():
     need_gpu()
     moe = moe_lib()
