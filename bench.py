@@ -3,16 +3,21 @@
 
 One step = one whole moe_ffn_forward call (router -> grouping -> experts ->
 combine) over one batch of seeded synthetic tokens, weights resident in HBM.
-Prints ONE JSON line (rank 0).  Multi-GPU runs are independent replicas (the
-layer has no exchange step on one node): value = all ranks' tokens / the slowest
-rank's time.
+Prints ONE JSON line (rank 0).  By default every workload of moe_inputs.WORKLOADS
+is measured in turn: the headline keys describe the Qwen3.5-mini decode batch of
+64 tokens, and `per_workload` holds one record per workload (step time, tokens/s,
+roofline of each expert kernel, phase split, end-to-end rate, clocks, routing
+load, near ties and the CPU oracle baseline with its parity on the sample).
+Multi-GPU runs are independent replicas (the layer has no exchange step on one
+node): value = all ranks' tokens / the slowest rank's time.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME|all]
   python bench.py --impl reference ...   # the fp64 CPU oracle on this host's cores
 """
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -26,7 +31,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s; decode HBM GB/s and prefill TFLOP/s vs roofline (1×GB300)"
-DEFAULT_WORKLOAD = "qwen35_mini_moe_decode_t64"
+HEADLINE_WORKLOAD = "qwen35_mini_moe_decode_t64"
 FLUSH_BYTES = 256 << 20          # > 2x the 129 MB L2
 
 
@@ -41,23 +46,39 @@ def flush_l2(buf, sink):
 PHASES = ("router_logits", "router_select", "permute", "gate_up", "down", "combine")
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--workload", default="all",
+                    help="one workload name, or 'all' (headline: the Qwen3.5-mini T=64 decode batch)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
-                    help="CPU oracle baseline budget (0 disables)")
+                    help="CPU oracle baseline budget of the headline workload (0 disables); "
+                         "the other workloads take half of it each")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     ap.add_argument("--path", choices=["auto", "decode", "prefill", "decode-registers"], default="auto",
                     help="the expert path (cfg.path); auto picks by tokens per expert")
-    return ap.parse_args()
+    return ap.parse_args(argv)
+
+
+def workload_names(arg):
+    import moe_inputs as mi
+    if arg == "all":
+        return list(mi.WORKLOAD_ORDER)
+    if arg not in mi.WORKLOADS:
+        raise SystemExit(f"unknown workload {arg!r}; one of {', '.join(mi.WORKLOAD_ORDER)} or 'all'")
+    return [arg]
+
+
+def headline_of(names):
+    return HEADLINE_WORKLOAD if HEADLINE_WORKLOAD in names else names[0]
 
 
 def peaks():
+    """(HBM GB/s, bf16 TFLOP/s burst, bf16 TFLOP/s sustained, source)."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
@@ -67,6 +88,8 @@ def peaks():
 
 def kernel_hash(fname):
     path = os.path.join(ROOT, "sparse_moe_ffn_route_gb300", "csrc", fname)
+    if not os.path.exists(path):
+        return None
     return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
 
 
@@ -202,21 +225,74 @@ def work(spec, ids):
     return by, fl, distinct, per_unit
 
 
+def plan_dtype(plan, mxfp4):
+    """The arithmetic type the expert kernels of a plan multiply in."""
+    if mxfp4 and plan in (2, 4):
+        return "f16 operands (MXFP4 weights decoded exactly), fp32 accumulation"
+    if mxfp4:
+        return "bf16 operands (MXFP4 weights decoded exactly), fp32 accumulation"
+    return "bf16"
+
+
+def kernel_roofline(name, by, fl, ms, hbm, tf_burst):
+    """Roofline of one expert kernel timed between L2 flushes: HBM when its arithmetic
+    intensity is below the ridge of the measured peaks, else tensor (against the burst
+    bf16 peak; f16 operands run at the bf16 rate, a nominal ratio of 1)."""
+    secs = ms / 1e3
+    gbs = by / secs / 1e9
+    tfs = fl / secs / 1e12
+    tensor = fl / by > (tf_burst * 1e12) / (hbm * 1e9)
+    return {"bound": "tensor" if tensor else "hbm", "kernel": name,
+            "achieved": tfs if tensor else gbs, "peak": tf_burst if tensor else hbm,
+            "unit": "TFLOP/s" if tensor else "GB/s",
+            "frac": (tfs / tf_burst) if tensor else (gbs / hbm),
+            "ms": ms, "hbm_gbs": gbs, "hbm_frac": gbs / hbm,
+            "tensor_tflops": tfs, "tensor_frac": tfs / tf_burst,
+            "algorithmic_bytes_per_launch": by, "algorithmic_flops_per_launch": fl}
+
+
+def routing_load(ids, n_experts):
+    """Tokens per routed expert for this step's routing."""
+    import numpy as np
+    cnt = np.bincount(ids.ravel().astype(np.int64), minlength=n_experts)
+    srt = np.sort(cnt)[::-1]
+    rec = {"min": int(cnt.min()), "max": int(cnt.max()), "mean": float(cnt.mean()),
+           "cv": float(cnt.std() / cnt.mean()) if cnt.mean() > 0 else 0.0,
+           "idle_experts": int((cnt == 0).sum()),
+           "top4_share": float(srt[:4].sum() / max(cnt.sum(), 1))}
+    if n_experts <= 64:
+        rec["tokens_per_expert"] = [int(c) for c in cnt]
+    else:
+        rec["top8"] = [int(c) for c in srt[:8]]
+    return rec
+
+
+def near_tie_count(logits, k, eps=1e-5):
+    """Tokens whose k-th/(k+1)-th largest fp32 logit, or two adjacent selected ones,
+    lie within eps (their selection may legitimately differ from exact arithmetic)."""
+    import numpy as np
+    s = -np.sort(-logits.astype(np.float64), axis=1)
+    gap_k = s[:, k - 1] - s[:, k] if logits.shape[1] > k else np.full(len(s), np.inf)
+    gap_adj = np.min(np.diff(-s[:, :k], axis=1), axis=1) if k > 1 else np.full(len(s), np.inf)
+    return int(((gap_k < eps) | (gap_adj < eps)).sum())
+
+
 # ----------------------------------------------------------------------------- arms
 def cpu_oracle_rate(spec, lay, seconds, tokens=None):
-    """tokens/s of the fp64 oracle over repeated passes on `tokens` (default: all)."""
+    """tokens/s of the fp64 oracle over repeated passes on `tokens` (default: all);
+    also returns the last pass's result."""
     import numpy as np
     import oracle
     g = oracle.gating_for(spec)
     tok = np.arange(spec.tokens, dtype=np.int32) if tokens is None else tokens
     n, t0 = 0, time.perf_counter()
     while True:
-        oracle.forward(g, lay, tokens=tok)
+        res = oracle.forward(g, lay, tokens=tok)
         n += len(tok)
         el = time.perf_counter() - t0
         if el >= seconds:
             break
-    return n / el, n, el, oracle.num_threads()
+    return n / el, n, el, oracle.num_threads(), res
 
 
 def run_reference(args, rank, world):
@@ -226,7 +302,7 @@ def run_reference(args, rank, world):
     import numpy as np
     import moe_inputs as mi
     import oracle
-    spec = mi.WORKLOADS[args.workload]
+    spec = mi.WORKLOADS[headline_of(workload_names(args.workload))]
     lay = mi.make_layer(spec)
     g = oracle.gating_for(spec)
     n_tok = min(spec.tokens, 16)
@@ -280,18 +356,44 @@ def config_of(spec):
             "parallelism": "replicas"}
 
 
-def run_ours(args, rank, world, local_rank):
+class LayerCache:
+    """Host layers and their device copies, shared by workloads of one layer: the three
+    Qwen3.5-mini workloads differ only in x and the router bias (the weights come from
+    the same seeded streams), so their 1.6 GB of experts are generated and uploaded once."""
+
+    def __init__(self, dev):
+        self.dev = dev
+        self.key = None
+        self.host = None
+        self.device = None
+
+    def get(self, spec):
+        import moe_inputs as mi
+        from sparse_moe_ffn_route_gb300 import hostio
+        key = (spec.family, spec.d_model, spec.n_experts, spec.expert_ff, spec.shared_ff, spec.seed,
+               spec.scale_lo, spec.scale_hi)
+        if key != self.key:
+            self.key, self.host, self.device = key, None, None
+            import torch
+            torch.cuda.empty_cache()
+            self.host = mi.make_layer(spec)
+            self.device = hostio.upload(self.host, self.dev)
+            return self.host, self.device
+        lay = dataclasses.replace(self.host, spec=spec, x=mi.make_x(spec),
+                                  router_b=mi.make_router_bias(spec))
+        _, router, experts, shared = self.device
+        router = dataclasses.replace(router, bias=hostio.bf16_tensor(lay.router_b, self.dev))
+        return lay, (hostio.bf16_tensor(lay.x, self.dev), router, experts, shared)
+
+
+def measure(spec, lay, dev_layer, args, rank, world, local_rank, dev, flush, sink, cpu_seconds):
+    """Every number of one workload: timed steps, phase split, graph replay, the host
+    entry point end to end, rooflines, routing load, near ties, the CPU baseline."""
     import numpy as np
     import torch
-    import moe_inputs as mi
     import sparse_moe_ffn_route_gb300 as moe
-    from sparse_moe_ffn_route_gb300 import hostio
 
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    spec = mi.WORKLOADS[args.workload]
-    lay = mi.make_layer(spec)
-    x, router, experts, shared = hostio.upload(lay, dev)
+    x, router, experts, shared = dev_layer
     if spec.family == "qwen":
         cfg = moe.qwen_cfg(spec.d_model, spec.n_experts, spec.top_k, spec.expert_ff, spec.shared_ff)
     else:
@@ -302,18 +404,15 @@ def run_ours(args, rank, world, local_rank):
     ws = moe.workspace(cfg, T, dev)
     y = torch.empty_like(x)
     ids = torch.empty((T, spec.top_k), dtype=torch.int32, device=dev)
-    flush = (torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev),
-             torch.zeros(FLUSH_BYTES, dtype=torch.uint8, device=dev))
-    sink = torch.zeros((), dtype=torch.int64, device=dev)
-    stream = torch.cuda.current_stream()
 
     plan = moe.moe_kernel_plan(cfg, T)
     moe.moe_ffn_forward(cfg, x, router, experts, shared, y=y, topk_ids=ids, ws=ws)
     torch.cuda.synchronize()
     st, bits = moe.moe_device_status(ws)
     if st != 0:
-        raise RuntimeError(f"device status {st} bits {bits:#x}")
-    by, fl, distinct, per_unit = work(spec, ids.cpu().numpy())
+        raise RuntimeError(f"{spec.name}: device status {st} bits {bits:#x}")
+    ids_np = ids.cpu().numpy()
+    by, fl, distinct, per_unit = work(spec, ids_np)
 
     for _ in range(args.warmup):
         flush_l2(flush, sink)
@@ -382,6 +481,7 @@ def run_ours(args, rank, world, local_rank):
         g_ms = max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in g_evs), world, dev)
         graph_rec = {"ms_per_step": g_ms, "value": job_rate(T, g_ms, world), "unit": "tokens/s",
                      "note": "one captured moe_ffn_forward replayed per step, L2 flushed between"}
+        del graph
 
     # end to end through the host-buffer entry point: pinned x in, pinned y out; the
     # call bound once (arguments marshalled once), as a decode loop would use it
@@ -406,55 +506,133 @@ def run_ours(args, rank, world, local_rank):
         e2e = {"value": job_rate(T, e_ms, world), "unit": "tokens/s",
                "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": y_host.numel() * 2,
                "ms_per_step": e_ms}
+        del step
+
+    # routing statistics from the library's own router: per-expert load, near ties
+    logits = torch.empty((T, spec.n_experts), dtype=torch.float32, device=dev)
+    moe.moe_route(cfg, x, router, shared, logits=logits, ws=ws)
+    # fp32 output for the parity figure of the CPU baseline's sample
+    y32 = moe.moe_ffn_forward(cfg.replace(y_fp32=1), x, router, experts, shared, ws=ws)
+    torch.cuda.synchronize()
+    load = routing_load(ids_np, spec.n_experts)
+    ties = near_tie_count(logits.cpu().numpy(), spec.top_k)
+    n_sample = min(T, 64)
+    y32_sample = y32[:n_sample].cpu().numpy().astype(np.float64)
+    del ws, y, y32, logits
 
     if rank != 0:
-        return
+        return None
     hbm, tf, tf_sus, src = peaks()
+    kernels = {p: kernel_roofline(p, by[p], fl.get(p, 0), phase_ms[p], hbm, tf) for p in ("gate_up", "down")}
     dom = max(("gate_up", "down"), key=lambda p: phase_ms[p])
-    secs = phase_ms[dom] / 1e3
-    gbs = by[dom] / secs / 1e9
-    tfs = fl.get(dom, 0) / secs / 1e12
-    # The binding roofline: HBM when the kernel's arithmetic intensity is below the
-    # ridge of the measured peaks, tensor otherwise (the other fraction alongside).
-    # A kernel timed inside the step takes the sustained tensor peak.
-    tpeak = tf_sus or tf
-    tensor_bound = fl.get(dom, 0) / by[dom] > (tpeak * 1e12) / (hbm * 1e9)
-    roof = {"bound": "tensor" if tensor_bound else "hbm", "kernel": dom,
-            "achieved": tfs if tensor_bound else gbs, "peak": tpeak if tensor_bound else hbm,
-            "unit": "TFLOP/s" if tensor_bound else "GB/s",
-            "frac": (tfs / tpeak) if tensor_bound else (gbs / hbm),
-            "peak_source": src + (" (bf16 sustained)" if tensor_bound else " (HBM copy)"),
-            "traffic": ncu_traffic(spec.name, dom),
-            "algorithmic_bytes_per_launch": by[dom], "algorithmic_flops_per_launch": fl.get(dom, 0),
-            "per_unit_bytes": per_unit[dom], "units_per_launch": distinct,
-            "hbm_gbs": gbs, "hbm_frac": gbs / hbm,
-            "tensor_tflops": tfs, "tensor_frac": tfs / tpeak,
-            "path": moe.PLAN_NAMES[plan]}
+    roof = dict(kernels[dom])
+    roof.update({"peak_source": src + (" (bf16 burst, L2 flushed between steps)" if roof["bound"] == "tensor"
+                                       else " (HBM copy)"),
+                 "traffic": ncu_traffic(spec.name, dom),
+                 "per_unit_bytes": per_unit[dom], "units_per_launch": distinct,
+                 "path": moe.PLAN_NAMES[plan]})
     step_bytes = sum(by.values())
     cpu = None
-    if args.cpu_seconds > 0:
-        rate, n, el, cores = cpu_oracle_rate(spec, lay, args.cpu_seconds,
-                                             tokens=np.arange(min(T, 64), dtype=np.int32))
+    if cpu_seconds > 0:
+        tok = np.arange(n_sample, dtype=np.int32)
+        rate, n, el, cores, res = cpu_oracle_rate(spec, lay, cpu_seconds, tokens=tok)
+        rms = float(np.sqrt(np.mean(res.y ** 2)))
         cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-               "sample": f"{n} token-evaluations (first {min(T, 64)} tokens, repeated) "
-                         f"in {el:.1f} s"}
-    out = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(config_of(spec), **({} if args.path == "auto" else {"path": args.path})),
-        "ms_per_step_median": statistics.median(step_ms), "ms_per_step_min": min(step_ms),
-        "roofline": roof,
-        "cpu_baseline": cpu,
-        "e2e": e2e,
-        "graph": graph_rec,
+               "sample": f"{n} token-evaluations (first {n_sample} tokens, repeated) in {el:.1f} s",
+               "parity_on_sample": {"tokens": n_sample,
+                                    "max_abs_err_over_rms": float(np.max(np.abs(y32_sample - res.y))) / rms,
+                                    "ids_equal": int(np.sum(np.all(res.ids == ids_np[:n_sample], axis=1))),
+                                    "bar": 2e-2}}
+    return {
+        "spec": spec, "plan": plan, "ms": ms, "value": value, "step_ms": step_ms,
+        "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e, "graph": graph_rec,
         "gpu_launches": launches_per_step(plan, spec.mxfp4, T * (spec.top_k + (spec.shared_ff > 0)), T,
                                           spec.n_experts) * args.steps,
-        "clocks": sampler.summary(t0, t1),
-        "phases_ms": phase_ms,
-        "step_hbm_gbs": step_bytes / (ms / 1e3) / 1e9,
-        "step_algorithmic_bytes": step_bytes,
-        "distinct_experts": distinct,
+        "clocks": sampler.summary(t0, t1), "phases_ms": phase_ms,
+        "step_hbm_gbs": step_bytes / (ms / 1e3) / 1e9, "step_algorithmic_bytes": step_bytes,
+        "distinct_experts": distinct, "load": load, "near_ties": ties,
+        "dtype": plan_dtype(plan, spec.mxfp4),
+    }
+
+
+def compact(rec):
+    """The per-workload record of the JSON line (rounded, without the raw step list)."""
+    def r(v, n=4):
+        if isinstance(v, float):
+            return float(f"{v:.{n}g}")
+        if isinstance(v, dict):
+            return {k: r(w, n) for k, w in v.items()}
+        if isinstance(v, list):
+            return [r(w, n) for w in v]
+        return v
+    spec = rec["spec"]
+    kern = {p: {k: r(v) for k, v in kr.items()
+                if k in ("bound", "ms", "achieved", "unit", "frac", "hbm_frac", "tensor_frac")}
+            for p, kr in rec["kernels"].items()}
+    roof = {k: r(v) for k, v in rec["roofline"].items()
+            if k in ("bound", "kernel", "achieved", "peak", "unit", "frac", "traffic",
+                     "algorithmic_bytes_per_launch", "algorithmic_flops_per_launch",
+                     "per_unit_bytes", "units_per_launch")}
+    out = {"tokens": spec.tokens, "ms_per_step": r(rec["ms"]), "value": r(rec["value"]),
+           "unit": "tokens/s", "dtype": rec["dtype"], "plan": rec["plan"], "roofline": roof,
+           "kernels": kern, "phases_ms": r(rec["phases_ms"], 3),
+           "graph_ms_per_step": r(rec["graph"]["ms_per_step"]) if rec["graph"] else None,
+           "e2e": r(rec["e2e"]) if rec["e2e"] else None,
+           "clocks": {k: rec["clocks"].get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+           "step_algorithmic_bytes": rec["step_algorithmic_bytes"],
+           "step_hbm_gbs": r(rec["step_hbm_gbs"]), "distinct_experts": rec["distinct_experts"],
+           "load": r(rec["load"], 3), "near_ties": rec["near_ties"],
+           "gpu_launches": rec["gpu_launches"],
+           "cpu_baseline": r(rec["cpu_baseline"]) if rec["cpu_baseline"] else None}
+    return out
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    import moe_inputs as mi
+    import sparse_moe_ffn_route_gb300  # noqa: F401  (fails loudly without libmoe.so)
+
+    names = workload_names(args.workload)
+    head = headline_of(names)
+    flush = (torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev),
+             torch.zeros(FLUSH_BYTES, dtype=torch.uint8, device=dev))
+    sink = torch.zeros((), dtype=torch.int64, device=dev)
+    cache = LayerCache(dev)
+    # same-layer workloads next to each other, so each layer is generated once
+    order = sorted(names, key=lambda n: (mi.WORKLOADS[n].family != mi.WORKLOADS[head].family,
+                                         mi.WORKLOADS[n].family, names.index(n)))
+    recs = {}
+    for name in order:
+        spec = mi.WORKLOADS[name]
+        if args.path != "auto" and spec.name != head:
+            continue
+        lay, dev_layer = cache.get(spec)
+        budget = args.cpu_seconds if name == head else 0.5 * args.cpu_seconds
+        recs[name] = measure(spec, lay, dev_layer, args, rank, world, local_rank, dev, flush, sink, budget)
+        torch.cuda.synchronize()
+    if rank != 0:
+        return
+    h = recs[head]
+    spec = h["spec"]
+    out = {
+        "metric": METRIC, "value": h["value"], "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": h["ms"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": h["dtype"], "data": "synthetic",
+        "config": dict(config_of(spec), **({} if args.path == "auto" else {"path": args.path})),
+        "ms_per_step_median": statistics.median(h["step_ms"]), "ms_per_step_min": min(h["step_ms"]),
+        "roofline": h["roofline"],
+        "cpu_baseline": h["cpu_baseline"],
+        "e2e": h["e2e"],
+        "graph": h["graph"],
+        "gpu_launches": h["gpu_launches"],
+        "clocks": h["clocks"],
+        "phases_ms": h["phases_ms"],
+        "step_hbm_gbs": h["step_hbm_gbs"],
+        "step_algorithmic_bytes": h["step_algorithmic_bytes"],
+        "distinct_experts": h["distinct_experts"],
+        "per_workload": {n: compact(recs[n]) for n in names if n in recs},
     }
     print(json.dumps(out), flush=True)
 
