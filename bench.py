@@ -195,8 +195,11 @@ def launches_per_step(plan, mxfp4, spec_slots, tokens=0, n_experts=0):
     return router + permute + 7   # 2 scale preps, gather, gate_up, h fix-up, down, combine
 
 
-def work(spec, ids):
-    """Algorithmic bytes and flops per phase for one step with routing `ids` [T, k]."""
+def work(spec, ids, accumulate=False):
+    """Algorithmic bytes and flops per phase for one step with routing `ids` [T, k].
+    accumulate: the prefill down projection adds the weighted expert outputs into
+    per-token fp32 sums [T, d] (cleared by the select kernel, read once by the finish
+    kernel) instead of writing Y [T*K, d] for the combine."""
     import numpy as np
     T, d, ff, sff, E, k = (spec.tokens, spec.d_model, spec.expert_ff, spec.shared_ff,
                            spec.n_experts, spec.top_k)
@@ -208,13 +211,14 @@ def work(spec, ids):
     x_bytes = T * d * 2
     h_bytes = (rows * ff + T * sff) * 2
     Y_bytes = S * d * 4
+    acc_bytes = T * d * 4
     by = {
         "router_logits": (E + has_sh) * d * 2 + x_bytes + T * (E + has_sh) * 4,
-        "router_select": T * (E + has_sh) * 4 + S * 8,
+        "router_select": T * (E + has_sh) * 4 + S * 8 + (acc_bytes if accumulate else 0),
         "permute": S * 4 * 3,
         "gate_up": distinct * gu + (sgu if has_sh else 0) + x_bytes + h_bytes,
-        "down": distinct * dn + (sdn if has_sh else 0) + h_bytes + Y_bytes,
-        "combine": Y_bytes + S * 8 + T * d * 2,
+        "down": distinct * dn + (sdn if has_sh else 0) + h_bytes + (acc_bytes if accumulate else Y_bytes),
+        "combine": (acc_bytes if accumulate else Y_bytes + S * 8) + T * d * 2,
     }
     fl = {
         "router_logits": 2 * T * (E + has_sh) * d,
@@ -412,7 +416,8 @@ def measure(spec, lay, dev_layer, args, rank, world, local_rank, dev, flush, sin
     if st != 0:
         raise RuntimeError(f"{spec.name}: device status {st} bits {bits:#x}")
     ids_np = ids.cpu().numpy()
-    by, fl, distinct, per_unit = work(spec, ids_np)
+    accumulate = plan in (moe.PLAN_PREFILL_BF16, moe.PLAN_PREFILL_F16) and not cfg.deterministic
+    by, fl, distinct, per_unit = work(spec, ids_np, accumulate)
 
     for _ in range(args.warmup):
         flush_l2(flush, sink)
@@ -551,7 +556,7 @@ def measure(spec, lay, dev_layer, args, rank, world, local_rank, dev, flush, sin
         "clocks": sampler.summary(t0, t1), "phases_ms": phase_ms,
         "step_hbm_gbs": step_bytes / (ms / 1e3) / 1e9, "step_algorithmic_bytes": step_bytes,
         "distinct_experts": distinct, "load": load, "near_ties": ties,
-        "dtype": plan_dtype(plan, spec.mxfp4),
+        "dtype": plan_dtype(plan, spec.mxfp4), "accumulate": accumulate,
     }
 
 
@@ -582,7 +587,7 @@ def compact(rec):
            "step_algorithmic_bytes": rec["step_algorithmic_bytes"],
            "step_hbm_gbs": r(rec["step_hbm_gbs"]), "distinct_experts": rec["distinct_experts"],
            "load": r(rec["load"], 3), "near_ties": rec["near_ties"],
-           "gpu_launches": rec["gpu_launches"],
+           "gpu_launches": rec["gpu_launches"], "accumulated_prefill": rec["accumulate"],
            "cpu_baseline": r(rec["cpu_baseline"]) if rec["cpu_baseline"] else None}
     return out
 

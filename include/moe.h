@@ -109,7 +109,15 @@ typedef struct {
                                    rms_eps) * router.norm_w (fp32 statistics, rounded to bf16) */
   float rms_eps;                /* Qwen 1e-6, gpt-oss 1e-5; finite and >= 0 */
   int32_t residual;             /* 1: y = x + MoE(...) (x un-normalised), summed in fp32 */
-  int32_t reserved[3];          /* must be zero */
+  int32_t deterministic;        /* 1: a token's expert outputs are summed in a fixed order by a
+                                   gather over its slots, so y is bit-identical run to run.
+                                   0: on the prefill path the down projection adds each weighted
+                                   expert output into a per-token fp32 sum with atomic adds in its
+                                   epilogue (no round trip of the [T*k, d] expert outputs through
+                                   memory); the order of those adds varies, so the last bits of y
+                                   may differ between runs.  The decode path always takes the
+                                   fixed order. */
+  int32_t reserved[2];          /* must be zero */
 } moe_cfg_t;
 
 /* Router: w bf16 [E, d] (row e = expert e's logit weights); bias bf16 [E] or NULL;
@@ -202,6 +210,22 @@ int moe_route(const moe_cfg_t* cfg, const void* x, int32_t T, const moe_router_t
  * (device), with the same rule as moe_route.  Needs no workspace. */
 int moe_topk_from_logits(const moe_cfg_t* cfg, const float* logits, int32_t T, int32_t* topk_ids,
                          float* topk_w, void* stream);
+
+/* Group token slots by expert: the permute step of the layer, on caller routing.
+ * Defined by "qwen35moe - Forward-Pass Design", section "Batched prefill"
+ * (expert-grouped batching: tokens that share an expert stream its weights once).
+ *   topk_ids  int32 [T, k] device: slot s = t * k + j chose expert topk_ids[t, j]
+ *   counts    int32 [E] device, out: slots routed to each expert
+ *   offsets   int32 [E + 1] device, out: offsets[e] = sum of counts[0 .. e - 1]
+ *   perm      int32 [T * k] device, out: perm[offsets[e] .. offsets[e + 1] - 1] are the
+ *             slots routed to e in increasing slot order (the grouping is stable:
+ *             the order the expert kernels of moe_ffn_forward see)
+ * A slot whose id lies outside [0, E) is left out of counts, offsets and perm (its
+ * entries of perm past offsets[E] are not written) and flags the device status word
+ * in ws (moe_device_status then returns MOE_ERR_DEVICE_CHECK).  ws: at least
+ * moe_workspace_bytes(cfg, T) bytes. */
+int moe_group_by_expert(const moe_cfg_t* cfg, const int32_t* topk_ids, int32_t T, int32_t* counts,
+                        int32_t* offsets, int32_t* perm, void* ws, size_t ws_bytes, void* stream);
 
 /* The whole layer: route, group tokens by expert, run the selected experts (and
  * the shared expert), combine.  y bf16 [T, d] device, out.  topk_ids [T, k] /

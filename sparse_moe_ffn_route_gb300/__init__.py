@@ -53,7 +53,7 @@ class MoeCfg(ctypes.Structure):
                 ("glu_alpha", ctypes.c_float), ("path", ctypes.c_int32),
                 ("y_fp32", ctypes.c_int32), ("rms_norm", ctypes.c_int32),
                 ("rms_eps", ctypes.c_float), ("residual", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 3)]
+                ("deterministic", ctypes.c_int32), ("reserved", ctypes.c_int32 * 2)]
 
     def replace(self, **kw) -> "MoeCfg":
         c = MoeCfg()
@@ -93,6 +93,8 @@ def _load():
     lib.moe_route.restype = I
     lib.moe_topk_from_logits.argtypes = [C, P, ctypes.c_int32, P, P, P]
     lib.moe_topk_from_logits.restype = I
+    lib.moe_group_by_expert.argtypes = [C, P, ctypes.c_int32, P, P, P, P, ctypes.c_size_t, P]
+    lib.moe_group_by_expert.restype = I
     lib.moe_ffn_forward.argtypes = [C, P, ctypes.c_int32, ctypes.POINTER(_Router),
                                     ctypes.POINTER(_Experts), ctypes.POINTER(_Shared), P, P, P, P,
                                     ctypes.c_size_t, P]
@@ -126,7 +128,7 @@ def _load():
 
 _lib = _load()
 EXPORTED = ("moe_workspace_bytes", "moe_select_path", "moe_kernel_plan", "moe_route", "moe_topk_from_logits",
-            "moe_ffn_forward", "moe_ffn_forward_routed", "moe_ffn_forward_host",
+            "moe_group_by_expert", "moe_ffn_forward", "moe_ffn_forward_routed", "moe_ffn_forward_host",
             "moe_ffn_forward_noalloc", "moe_noalloc_workspace_bytes", "moe_noalloc_device_status",
             "moe_mxfp4_to_bf16", "moe_set_phase_events", "moe_device_status",
             "moe_status_string")
@@ -276,6 +278,22 @@ def moe_topk_from_logits(cfg: MoeCfg, logits: torch.Tensor, topk_ids=None, topk_
     _check(_lib.moe_topk_from_logits(ctypes.byref(cfg), _ptr(logits, "logits"), T, _ptr(topk_ids),
                                      _ptr(topk_w), _stream(stream)), "moe_topk_from_logits")
     return topk_ids, topk_w
+
+
+def moe_group_by_expert(cfg: MoeCfg, topk_ids: torch.Tensor, counts=None, offsets=None, perm=None,
+                        ws=None, stream=None):
+    """Stable grouping of the slots t*k + j by expert: (counts [E], offsets [E+1], perm [T*k])."""
+    T = topk_ids.shape[0]
+    dev = topk_ids.device
+    E = cfg.n_experts
+    counts = torch.empty(E, dtype=torch.int32, device=dev) if counts is None else counts
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev) if offsets is None else offsets
+    perm = torch.empty(max(T * cfg.top_k, 1), dtype=torch.int32, device=dev) if perm is None else perm
+    ws = workspace(cfg, T, dev) if ws is None else ws
+    _check(_lib.moe_group_by_expert(ctypes.byref(cfg), _ptr(topk_ids, "topk_ids"), T, _ptr(counts, "counts"),
+                                    _ptr(offsets, "offsets"), _ptr(perm, "perm"), _ptr(ws), ws.numel(),
+                                    _stream(stream)), "moe_group_by_expert")
+    return counts, offsets, perm
 
 
 def moe_ffn_forward(cfg: MoeCfg, x: torch.Tensor, router: Router, experts: Experts,

@@ -1,6 +1,9 @@
 // Combine: y[t] = (x[t] +) sum_j w[t, j] * Y[t*K + j] over a token's routed slots
 // and, last, its shared-expert slot (weight = sigmoid gate), accumulated in fp32 in
-// that fixed order (the residual first) and rounded once to bf16.
+// that fixed order (the residual first) and rounded once to bf16.  On the prefill
+// path with cfg.deterministic = 0 the down projection has already added the weighted
+// slots into a per-token fp32 sum, and the finish kernel only adds the residual and
+// rounds.
 // RMSNorm: the MoE's input RMSNorm(x) = x / sqrt(mean(x^2) + eps) * w, in bf16.
 //
 // Sources: "qwen35moe - Forward-Pass Design", section "Shared-expert MoE FFN"
@@ -74,6 +77,45 @@ combine_kernel(const float* __restrict__ Y, const float* __restrict__ slot_w,
   pdl_trigger();
 }
 
+// The accumulated prefill's last step: y[t] = (x[t] +) yacc[t], where yacc holds the
+// token's weighted expert outputs (shared expert included) summed by the down
+// projection's atomic adds.
+template <bool F32>
+__global__ void __launch_bounds__(256)
+finish_kernel(const float* __restrict__ yacc, int T, int d, const uint16_t* __restrict__ resid,
+              void* __restrict__ y) {
+  pdl_wait();
+  const int d8 = d / 8;
+  const long n = (long)T * d8;
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+    const long t = i / d8;
+    const int o = (int)(i - t * d8) * 8;
+    const float4* src = reinterpret_cast<const float4*>(yacc + (size_t)t * d + o);
+    const float4 a = src[0], b = src[1];
+    float acc[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    if (resid) {
+      const uint4 r = ldg_nc_v4(resid + (size_t)t * d + o);
+      const float rv[8] = {bf16_lo(r.x), bf16_hi(r.x), bf16_lo(r.y), bf16_hi(r.y),
+                           bf16_lo(r.z), bf16_hi(r.z), bf16_lo(r.w), bf16_hi(r.w)};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = rv[j] + acc[j];
+    }
+    if (F32) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(y) + (size_t)t * d + o);
+      dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    } else {
+      uint4 out;
+      out.x = pack_bf16x2(acc[0], acc[1]);
+      out.y = pack_bf16x2(acc[2], acc[3]);
+      out.z = pack_bf16x2(acc[4], acc[5]);
+      out.w = pack_bf16x2(acc[6], acc[7]);
+      *reinterpret_cast<uint4*>(static_cast<uint16_t*>(y) + (size_t)t * d + o) = out;
+    }
+  }
+  pdl_trigger();
+}
+
 // One warp per token row: sum of squares in fp32, r = 1 / sqrt(mean + eps), and
 // xn = bf16(x * r * w).  Also the first kernel of a call that uses it: it clears the
 // device status word.
@@ -125,6 +167,16 @@ cudaError_t launch_combine(const float* Y, const float* slot_w, const int32_t* s
                       T, K, d, E1, resid, y);
   return launch_pdl(combine_kernel<false>, dim3((int)blocks), dim3(256), 0, s, Y, slot_w, slot_expert,
                     T, K, d, E1, resid, y);
+}
+
+cudaError_t launch_finish_accumulated(const float* yacc, int T, int d, const uint16_t* resid, void* y,
+                                      bool y_fp32, cudaStream_t s) {
+  const long n = (long)T * (d / 8);
+  long blocks = (n + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks < 1) blocks = 1;
+  if (y_fp32) return launch_pdl(finish_kernel<true>, dim3((int)blocks), dim3(256), 0, s, yacc, T, d, resid, y);
+  return launch_pdl(finish_kernel<false>, dim3((int)blocks), dim3(256), 0, s, yacc, T, d, resid, y);
 }
 
 cudaError_t launch_rmsnorm(const uint16_t* x, int T, int d, const uint16_t* w, float eps, uint16_t* xn,

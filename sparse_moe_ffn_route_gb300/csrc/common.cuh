@@ -69,6 +69,13 @@ __device__ __forceinline__ void stg_v8(float* p, const float* v) {
                : "memory");
 }
 
+// Four fp32 values added to p[0..3] (p 16-byte aligned) by one vector reduction in
+// L2: the per-token sums of the prefill down projection.
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
 // Streaming load for weights read once: skip L1, and let L2 fetch 256-byte
 // granules (the following k steps of the same row are requested right after).
 __device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {

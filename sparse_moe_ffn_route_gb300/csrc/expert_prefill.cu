@@ -100,6 +100,8 @@ struct GemmArgs {
   int ldh;                // width of each half
   int dual;               // down: A = h_hi and h_lo tiles against the same B tile
   float* Y;               // down output [S, d] (slot order)
+  float* yacc;            // down, when non-null: yacc[token, :] += slot_w[slot] * (row + bias) by
+                          // atomic adds (token = slot / aK), in place of the Y row
   int scale_rows;         // MXFP4: rows of one expert in the transposed scales
   int scale_nblk;         // MXFP4: 32-input blocks per weight row
   // kModeDense (router logits): A = x [rows, d], B = W_r [E, d]; no routing state
@@ -214,6 +216,12 @@ __device__ __forceinline__ void turned_rows(int r, int lane, int (&ridx)[8]) {
   for (int i = 0; i < 8; ++i) ridx[i] = __shfl_sync(0xffffffffu, r, 4 * i + (lane >> 3));
 }
 
+// The same for a per-row value (the routing weight of the row's slot).
+__device__ __forceinline__ void turned_vals(float r, int lane, float (&rv)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) rv[i] = __shfl_sync(0xffffffffu, r, 4 * i + (lane >> 3));
+}
+
 // One 32 x 32 fp32 block of a warp's rows (lane l holds row l's 32 values in v) to
 // rows ridx[i] (negative: skipped) of `base`, `pitch` floats apart, columns col ..
 // col + min(32, ncol) - 1, plus a bf16 bias per column when `bias` is non-null.
@@ -244,6 +252,34 @@ __device__ __forceinline__ void store_turned(float* stg, const float (&v)[32], c
           val.w += b4.w;
         }
         *reinterpret_cast<float4*>(base + (size_t)ridx[i] * pitch + col + cc) = val;
+      }
+    }
+  }
+  __syncwarp();
+}
+
+// store_turned for the accumulated down projection: row i of the block (plus the
+// bias) times rw[i] is added to row ridx[i] of `base` with vector atomic adds, so
+// that lanes 8j..8j+7 reduce 128 contiguous bytes of one row.
+template <int PITCH>
+__device__ __forceinline__ void red_turned(float* stg, const float (&v)[32], const int (&ridx)[8],
+                                           const float (&rw)[8], float* base, size_t pitch, int col, int ncol,
+                                           const uint16_t* bias, int lane) {
+  float4* wr = reinterpret_cast<float4*>(stg + lane * PITCH);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) wr[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  __syncwarp();
+  const int rr = lane >> 3, cc = (lane & 7) * 4;
+  if (cc < ncol) {
+    float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (bias) b4 = make_float4(bf16_to_f32(bias[cc]), bf16_to_f32(bias[cc + 1]), bf16_to_f32(bias[cc + 2]),
+                               bf16_to_f32(bias[cc + 3]));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (ridx[i] >= 0) {
+        const float4 val = *reinterpret_cast<const float4*>(stg + (4 * i + rr) * PITCH + cc);
+        red_add_v4(base + (size_t)ridx[i] * pitch + col + cc, rw[i] * (val.x + b4.x), rw[i] * (val.y + b4.y),
+                   rw[i] * (val.z + b4.z), rw[i] * (val.w + b4.w));
       }
     }
   }
@@ -542,6 +578,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
               if (i < ncol) lrow[e0 + c0 + i] = v[i] + (rbias ? bf16_to_f32(rbias[e0 + c0 + i]) : 0.f);
           }
         }
+      } else if (L::kEpiStage && g.mode == kModeDown && g.yacc) {
+        // y[token] += w(slot) * (row + bias): the weighted expert output goes straight
+        // into the token's fp32 sum
+        const int slot = valid ? g.rs.row2slot[grow] : -1;
+        int tidx[8];
+        float tw[8];
+        turned_rows(slot >= 0 ? slot / g.aK : -1, lane, tidx);
+        turned_vals(slot >= 0 ? g.rs.slot_w[slot] : 0.f, lane, tw);
+        const int o0 = tl.n * g.N;
+        const uint16_t* bp = (!sh && g.dn_bias) ? g.dn_bias + (size_t)tl.v * g.d + o0 : nullptr;
+        float* stg = reinterpret_cast<float*>(smem + kStages * kStageBytes) + q * 32 * L::kEpiPitch;
+        for (int c0 = 0; c0 < g.N; c0 += 32) {
+          float v[32];
+          tc::tmem_ld32(taddr + (uint32_t)c0, v);
+          red_turned<L::kEpiPitch>(stg, v, tidx, tw, g.yacc, (size_t)g.d, o0 + c0, g.N - c0,
+                                   bp ? bp + c0 : nullptr, lane);
+        }
       } else if (L::kEpiStage && g.mode == kModeDown) {
         const int slot = valid ? g.rs.row2slot[grow] : -1;
         int ridx[8];
@@ -554,6 +607,29 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           tc::tmem_ld32(taddr + (uint32_t)c0, v);
           store_turned<L::kEpiPitch>(stg, v, ridx, g.Y, (size_t)g.d, o0 + c0, g.N - c0, bp ? bp + c0 : nullptr,
                                      lane);
+        }
+      } else if (g.mode == kModeDown && g.yacc) {
+        const int slot = valid ? g.rs.row2slot[grow] : -1;
+        float* yrow = slot >= 0 ? g.yacc + (size_t)(slot / g.aK) * g.d : nullptr;
+        const float wt = slot >= 0 ? g.rs.slot_w[slot] : 0.f;
+        const int o0 = tl.n * g.N;
+        for (int c0 = 0; c0 < g.N; c0 += 32) {
+          float v[32];
+          tc::tmem_ld32(taddr + (uint32_t)c0, v);
+          if (yrow) {
+            const int ncol = min(32, g.N - c0);
+            if (!sh && g.dn_bias) {
+              const uint16_t* bp = g.dn_bias + (size_t)tl.v * g.d + o0 + c0;
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i < ncol) v[i] += bf16_to_f32(bp[i]);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (4 * i < ncol)
+                red_add_v4(yrow + o0 + c0 + 4 * i, wt * v[4 * i], wt * v[4 * i + 1], wt * v[4 * i + 2],
+                           wt * v[4 * i + 3]);
+          }
         }
       } else if (g.mode == kModeDown) {
         float* yrow = valid ? g.Y + (size_t)g.rs.row2slot[grow] * g.d : nullptr;
@@ -958,11 +1034,13 @@ cudaError_t launch_router_gemm(const uint16_t* x, int T, int d, const uint16_t* 
 }
 
 cudaError_t launch_down_prefill(const ExpertParams& p, int wfmt, const RouteState& rs,
-                                const uint16_t* h, int ldh, int S, float* Y,
+                                const uint16_t* h, int ldh, int S, float* Y, float* yacc, int K,
                                 const uint8_t* scalesT, int max_mtiles, cudaStream_t s) {
   const bool fp4 = wfmt == MOE_WFMT_MXFP4;
   GemmArgs g{};
   g.rs = rs;
+  g.yacc = yacc;
+  g.aK = K;
   g.E = p.E;
   g.mode = kModeDown;
   g.N = tile_n(p.d, fp4 ? Lay<true, false>::kMaxN : Lay<false, false>::kMaxN);

@@ -98,6 +98,9 @@ struct F4Gemm {
   uint32_t* hmax;             // [S] largest |h| of each row (fp32 bits), accumulated
   float limit, alpha;
   float* Y;                   // fp32 [S, d] in slot order
+  float* yacc;                // down, when non-null: yacc[slot / K] += slot_w[slot] * row (atomic
+                              // adds) in place of the Y row
+  int K;                      // slots per token
   int d;
 };
 
@@ -360,7 +363,7 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         ecm[i] = g.colmul[(size_t)u.v * g.R + col0 + i];
         ebi[i] = g.bias ? bf16_to_f32(g.bias[(size_t)u.v * g.R + col0 + i]) : 0.f;
       }
-      float rm[kG];
+      float rm[kG], rw[kG];
       size_t dst[kG];
 #pragma unroll
       for (int gi = 0; gi < kG; ++gi) {
@@ -368,9 +371,12 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         const int grow = g.rs.offsets[u.v] + u.row0 + row;
         const bool valid = gi < gm && row < u.cnt;
         rm[gi] = (valid && g.rowmul) ? g.rowmul[grow] : 1.f;
+        const int slot = (valid && !g.gateup) ? g.rs.row2slot[grow] : 0;
+        rw[gi] = (valid && g.yacc) ? g.rs.slot_w[slot] : 1.f;
         dst[gi] = !valid ? ~size_t(0)
                   : g.gateup ? (size_t)grow * g.ldh + col0 / 2
-                             : (size_t)g.rs.row2slot[grow] * g.d + col0;
+                  : g.yacc   ? (size_t)(slot / g.K) * g.d + col0
+                             : (size_t)slot * g.d + col0;
       }
       epi_sync();
       // On give-up the abort flag is set, and the next epi_any leaves the loop.
@@ -413,6 +419,14 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
               sp[0] = make_float4(hv[0], hv[1], hv[2], hv[3]);
               sp[1] = make_float4(hv[4], hv[5], hv[6], hv[7]);
             }
+          } else if (g.yacc) {
+            // the weighted row into the token's fp32 sum (16-byte aligned: d is a
+            // multiple of 32 and 16 c + col0 of 16)
+            float* yp = g.yacc + dst[gi] + 16 * c;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              red_add_v4(yp + 4 * i, rw[gi] * v[4 * i], rw[gi] * v[4 * i + 1], rw[gi] * v[4 * i + 2],
+                         rw[gi] * v[4 * i + 3]);
           } else {
             // Y rows are d fp32 apart with d a multiple of 32, and 16 c + col0 is a
             // multiple of 16: both halves of the chunk start on 32 bytes.
@@ -626,10 +640,13 @@ cudaError_t launch_gateup_prefill_fp4(const ExpertParams& p, const RouteState& r
 }
 
 cudaError_t launch_down_prefill_fp4(const ExpertParams& p, const RouteState& rs, const uint16_t* h16, int ldh16,
-                                    int S, float* Y, uint8_t* scratch, int max_items, cudaStream_t s) {
+                                    int S, float* Y, float* yacc, int K, uint8_t* scratch, int max_items,
+                                    cudaStream_t s) {
   const Fp4Scratch sc = carve(p, scratch, S);
   F4Gemm g{};
   g.rs = rs;
+  g.yacc = yacc;
+  g.K = K;
   g.E = p.E;
   g.R = p.d;
   g.nb = p.ff / 32;

@@ -118,19 +118,21 @@ cudaError_t launch_router_gemm(const uint16_t* x, int T, int d, const uint16_t* 
 // E, or, when wsh is non-null, x_t . wsh computed here (x bf16 [T, d]).  Writes any
 // non-null output.  rs non-null (S = T * K <= 2048 slots, E1 virtual experts, work
 // items of tpg rows): the same launch then groups the slots by expert, in place of
-// launch_permute.
+// launch_permute.  yzero non-null (not with rs): rows [T, d] fp32 cleared, the
+// per-token sums that the prefill down projection accumulates into.
 cudaError_t launch_router_select(const float* logits, int ldl, int nsplit, size_t nstride, float* lsum,
                                  int ldsum, int T, int E, int k, int norm_topk_prob, float scale,
                                  int has_shared,
                                  int32_t* ids_out, float* w_out, float* sgate_out,
                                  int32_t* slot_expert, float* slot_w, const uint16_t* x, int d,
                                  const uint16_t* wsh, const RouteState* rs, int S, int E1, int tpg,
-                                 cudaStream_t s);
+                                 float* yzero, cudaStream_t s);
 
-// Copy caller routing into the slot arrays (routed entry point).
+// Copy caller routing into the slot arrays (routed entry point); yzero as for
+// launch_router_select.
 cudaError_t launch_ingest_routing(const int32_t* ids, const float* w, const float* sgate, int T,
                                   int E, int k, int has_shared, int32_t* slot_expert,
-                                  float* slot_w, uint32_t* status, cudaStream_t s);
+                                  float* slot_w, uint32_t* status, float* yzero, int d, cudaStream_t s);
 
 // Histogram, offsets, work list (items of up to tpg rows) and row -> slot map; hist is
 // scratch of permute_scratch_bytes(S, E1).
@@ -173,8 +175,10 @@ cudaError_t launch_gateup_prefill(const ExpertParams& p, int wfmt, int interleav
                                   const RouteState& rs, const uint16_t* xp, int S, const uint16_t* x, int T,
                                   int K, uint16_t* h, int ldh, const uint8_t* scalesT, int max_mtiles,
                                   cudaStream_t s);
+// yacc non-null: instead of the Y rows, yacc[t] += slot_w * (row + bias) for slot
+// t * K + j, by atomic adds (yacc [T, d] fp32, zeroed before the call's down step).
 cudaError_t launch_down_prefill(const ExpertParams& p, int wfmt, const RouteState& rs,
-                                const uint16_t* h, int ldh, int S, float* Y,
+                                const uint16_t* h, int ldh, int S, float* Y, float* yacc, int K,
                                 const uint8_t* scalesT, int max_mtiles, cudaStream_t s);
 
 // f16 token operands (stage_f16.cu).  Per grouped row: rowmul = 2^-e of the staged
@@ -208,13 +212,18 @@ cudaError_t launch_prefill_fp4_prep(const ExpertParams& p, uint8_t* scratch, int
 cudaError_t launch_gateup_prefill_fp4(const ExpertParams& p, const RouteState& rs, const uint16_t* xp16, int S,
                                       uint16_t* h16, float* hside, int ldh, int kh, uint8_t* scratch,
                                       int max_items, cudaStream_t s);
+// yacc non-null: as for launch_down_prefill.
 cudaError_t launch_down_prefill_fp4(const ExpertParams& p, const RouteState& rs, const uint16_t* h16, int ldh16,
-                                    int S, float* Y, uint8_t* scratch, int max_items, cudaStream_t s);
+                                    int S, float* Y, float* yacc, int K, uint8_t* scratch, int max_items,
+                                    cudaStream_t s);
 
 // MXFP4 [rows, n_in/32, 16] + scales -> bf16 [rows, n_in].
 cudaError_t launch_mxfp4_to_bf16(const uint8_t* blocks, const uint8_t* scales, long long rows,
                                  int n_in, uint16_t* out, cudaStream_t s);
 
+// y[t] = (resid[t] +) yacc[t] (bf16 or fp32 out): the end of the accumulated prefill.
+cudaError_t launch_finish_accumulated(const float* yacc, int T, int d, const uint16_t* resid, void* y,
+                                      bool y_fp32, cudaStream_t s);
 // y[t] = (resid[t] +) sum_j slot_w[t,j] * Y[t*K + j]  (fp32 accumulation; bf16 or fp32 out).
 cudaError_t launch_combine(const float* Y, const float* slot_w, const int32_t* slot_expert, int T,
                            int K, int d, int E1, const uint16_t* resid, void* y, bool y_fp32,

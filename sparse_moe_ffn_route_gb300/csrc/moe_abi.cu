@@ -21,8 +21,9 @@ struct Layout {
   int K, E1, S, ldl, ldh;
   bool prefill;             // the expert phase runs the tcgen05 grouped GEMMs
   bool prefill_fp4;         // ... in their f16-operand MXFP4 form (expert_prefill_fp4.cu)
+  bool accumulate;          // prefill, not deterministic: down adds w * Y into yacc with atomics
   size_t status, counts, offsets, work, n_work, slot_expert, slot_w, row2slot, hist, logits, h, Y, xn,
-      xp, scalesT, xstage, ystage, total;
+      xp, scalesT, xstage, ystage, yacc, total;
 };
 
 int path_for(const moe_cfg_t* c, int T);
@@ -38,7 +39,8 @@ int validate_cfg(const moe_cfg_t* c) {
     return MOE_ERR_INVALID_ARG;
   for (int r : c->reserved)
     if (r != 0) return MOE_ERR_INVALID_ARG;
-  if (c->rms_norm < 0 || c->rms_norm > 1 || c->residual < 0 || c->residual > 1 ||
+  if (c->rms_norm < 0 || c->rms_norm > 1 || c->residual < 0 || c->residual > 1 || c->deterministic < 0 ||
+      c->deterministic > 1 ||
       !std::isfinite(c->rms_eps) || c->rms_eps < 0.f)
     return MOE_ERR_INVALID_ARG;
   if (!std::isfinite(c->expert_weights_scale) || !std::isfinite(c->glu_limit) ||
@@ -96,6 +98,8 @@ bool make_layout(const moe_cfg_t* c, int T, Layout* L) {
                       : L->prefill_fp4 ? prefill_fp4_scratch_bytes(sp, L->S)
                                        : prefill_scales_bytes(sp, c->wfmt));
   }
+  L->accumulate = L->prefill && !c->deterministic;
+  L->yacc = take(L->accumulate ? 4 * Tz * d : 0);   // per-token fp32 sums of the weighted expert outputs
   L->xn = take(c->rms_norm ? 2 * Tz * d : 0);   // RMSNorm(x), the MoE's input
   L->xstage = take(2 * Tz * d);
   L->ystage = take(4 * Tz * d);
@@ -303,7 +307,8 @@ int run_router(const moe_cfg_t* c, const void* x, int T, const moe_router_t* r,
                                 c->expert_weights_scale, has_sh, ids_out, w_out, sgate_out, slot_e,
                                 slot_w, xr, c->d_model, gate_in_logits ? nullptr : wsh,
                                 fill_slots && select_permutes(c, L, T) ? &rs : nullptr, L.S, L.E1,
-                                8 * decode_chunks(c, T), s));
+                                8 * decode_chunks(c, T), fill_slots && L.accumulate ? at<float>(ws, L.yacc) : nullptr,
+                                s));
   if (fill_slots) MOE_CUDA(mark_phase(2, s));
   if (logits_out && has_sh)
     MOE_CUDA(cudaMemcpy2DAsync(logits_out, sizeof(float) * c->n_experts, lg, sizeof(float) * ldl,
@@ -323,6 +328,15 @@ int run_experts(const moe_cfg_t* c, const void* x_layer, int T, const moe_expert
   const ExpertParams p = expert_params(c, e, sh);
   uint16_t* h = at<uint16_t>(ws, L.h);
   float* Y = at<float>(ws, L.Y);
+  // Prefill, not deterministic: the down projection adds each weighted expert output
+  // into yacc (cleared by the select / ingest kernel) and the finish kernel adds the
+  // residual and rounds; otherwise the combine gathers the Y rows in slot order.
+  float* yacc = L.accumulate ? at<float>(ws, L.yacc) : nullptr;
+  auto finish = [&](const float* Yv, const float* ya) {
+    return ya ? launch_finish_accumulated(ya, T, c->d_model, resid, y, c->y_fp32 != 0, s)
+              : launch_combine(Yv, rs.slot_w, rs.slot_expert, T, L.K, c->d_model, L.E1, resid, y,
+                               c->y_fp32 != 0, s);
+  };
   if (L.prefill_fp4) {
     // MXFP4 with the clamped GLU: f16-operand grouped GEMMs over work items of 256 rows
     // (two m tiles per dequantised weight tile).
@@ -342,10 +356,9 @@ int run_experts(const moe_cfg_t* c, const void* x_layer, int T, const moe_expert
     MOE_CUDA(launch_gateup_prefill_fp4(p, rs, xp16, L.S, h16, hside, L.ldh, kh, scratch, max_items, s));
     MOE_CUDA(mark_phase(4, s));
     MOE_CUDA(launch_h_fix_f16(hside, rows.hmax, L.S, c->expert_ff, kh, h16, L.ldh, rows.hmul, s));
-    MOE_CUDA(launch_down_prefill_fp4(p, rs, h16, L.ldh, L.S, Y, scratch, max_items, s));
+    MOE_CUDA(launch_down_prefill_fp4(p, rs, h16, L.ldh, L.S, Y, yacc, L.K, scratch, max_items, s));
     MOE_CUDA(mark_phase(5, s));
-    MOE_CUDA(launch_combine(Y, rs.slot_w, rs.slot_expert, T, L.K, c->d_model, L.E1, resid, y,
-                            c->y_fp32 != 0, s));
+    MOE_CUDA(finish(Y, yacc));
     MOE_CUDA(mark_phase(6, s));
     return MOE_OK;
   }
@@ -367,10 +380,9 @@ int run_experts(const moe_cfg_t* c, const void* x_layer, int T, const moe_expert
                                    static_cast<const uint16_t*>(x), T, L.K, h, L.ldh, scalesT,
                                    max_mtiles, s));
     MOE_CUDA(mark_phase(4, s));
-    MOE_CUDA(launch_down_prefill(p, c->wfmt, rs, h, L.ldh, L.S, Y, scalesT, max_mtiles, s));
+    MOE_CUDA(launch_down_prefill(p, c->wfmt, rs, h, L.ldh, L.S, Y, yacc, L.K, scalesT, max_mtiles, s));
     MOE_CUDA(mark_phase(5, s));
-    MOE_CUDA(launch_combine(Y, rs.slot_w, rs.slot_expert, T, L.K, c->d_model, L.E1, resid, y,
-                            c->y_fp32 != 0, s));
+    MOE_CUDA(finish(Y, yacc));
     MOE_CUDA(mark_phase(6, s));
     return MOE_OK;
   }
@@ -471,9 +483,35 @@ int moe_topk_from_logits(const moe_cfg_t* cfg, const float* logits, int32_t T, i
   const int norm = cfg->gating == MOE_GATING_TOPK_SOFTMAX ? 1 : cfg->norm_topk_prob;
   if (launch_router_select(logits, cfg->n_experts, 1, 0, nullptr, 0, T, cfg->n_experts, cfg->top_k, norm,
                            cfg->expert_weights_scale, 0, topk_ids, topk_w, nullptr, nullptr,
-                           nullptr, nullptr, 0, nullptr, nullptr, 0, 0, 0,
+                           nullptr, nullptr, 0, nullptr, nullptr, 0, 0, 0, nullptr,
                            static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+int moe_group_by_expert(const moe_cfg_t* cfg, const int32_t* topk_ids, int32_t T, int32_t* counts,
+                        int32_t* offsets, int32_t* perm, void* ws, size_t ws_bytes, void* stream) {
+  int st = validate_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!topk_ids || !perm)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(counts) || !aligned16(offsets) || (topk_ids && !aligned16(topk_ids)) ||
+      (perm && !aligned16(perm)))
+    return MOE_ERR_ALIGNMENT;
+  Layout L;
+  if ((st = check_ws(cfg, T, ws, ws_bytes, &L)) != MOE_OK) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The routed slots only (no shared expert): S = T k slots over E experts, written
+  // straight into the caller's arrays; the work list stays in the workspace.
+  RouteState rs = route_state(ws, L);
+  rs.counts = counts;
+  rs.offsets = offsets;
+  rs.row2slot = perm;
+  const int S = T * cfg->top_k;
+  MOE_CUDA(launch_ingest_routing(topk_ids, nullptr, nullptr, T, cfg->n_experts, cfg->top_k, 0, rs.slot_expert,
+                                 nullptr, rs.status, nullptr, cfg->d_model, s));
+  MOE_CUDA(launch_permute(rs, S, cfg->n_experts, 128, at<int>(ws, L.hist), s));
   return MOE_OK;
 }
 
@@ -522,7 +560,8 @@ int moe_ffn_forward_routed(const moe_cfg_t* cfg, const void* x, int32_t T,
   MOE_CUDA(mark_phase(0, s));
   MOE_CUDA(launch_ingest_routing(topk_ids, topk_w, sgate, T, cfg->n_experts, cfg->top_k,
                                  cfg->shared_ff > 0, at<int32_t>(ws, L.slot_expert),
-                                 at<float>(ws, L.slot_w), at<uint32_t>(ws, L.status), s));
+                                 at<float>(ws, L.slot_w), at<uint32_t>(ws, L.status),
+                                 L.accumulate ? at<float>(ws, L.yacc) : nullptr, cfg->d_model, s));
   MOE_CUDA(mark_phase(1, s));
   MOE_CUDA(mark_phase(2, s));
   return run_experts(cfg, x, T, experts, shared, y, L, ws, false, s);

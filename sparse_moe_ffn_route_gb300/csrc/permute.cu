@@ -11,11 +11,9 @@
 // ("Batched prefill", remaining levers) names as the way for tokens that share
 // an expert to stream its weights once.
 //
-// Rows of one expert are written in the order the warps reach them (warp-
-// aggregated shared-memory atomics), so the order inside an expert's row range
-// may change from run to run.  Results do not depend on it: every expert row is
-// computed independently and written back to its slot, and the combine sums a
-// token's slots in a fixed order.
+// The grouping is stable: expert v's rows hold the slots routed to v in increasing
+// slot order (t k + j), so the grouped order, the work items and the tokens each
+// item holds follow from the routing alone and are the same in every run.
 #include "common.cuh"
 #include "internal.h"
 #include "permute_core.cuh"
@@ -106,34 +104,17 @@ perm_scan_kernel(RouteState rs, int E1, int tpg, int* __restrict__ hist, int nch
 }
 
 // Chunk c's slots to rows: offsets[v] + hist[c][v] + the slot's rank among chunk c's
-// slots of v (warp-aggregated shared-memory atomics).
+// slots of v, in slot order (place_slots_stable).
 __global__ void __launch_bounds__(kPermuteThreads)
 perm_scatter_kernel(RouteState rs, int S, int E1, const int* __restrict__ hist) {
   __shared__ int cursor[kMaxExperts + 1];
-  const int tid = threadIdx.x, lane = tid & 31;
+  __shared__ __align__(16) uint8_t tab[(kMaxExperts + 1) * 32];
+  const int tid = threadIdx.x;
   pdl_wait();
   const int* h = hist + (size_t)blockIdx.x * E1;
   for (int v = tid; v < E1; v += kPermuteThreads) cursor[v] = rs.offsets[v] + h[v];
-  __syncthreads();
   const int s0 = blockIdx.x * kSlotsPerCta, s1 = min(S, s0 + kSlotsPerCta);
-  for (int b = s0; b < s1; b += kPermuteThreads) {
-    const int s = b + tid;
-    int v = s < s1 ? rs.slot_expert[s] : -1;
-    if (v < 0 || v >= E1) v = -1;
-    const uint32_t peers = __match_any_sync(0xffffffffu, v);
-    const int leader = __ffs(peers) - 1;
-    const int rank = __popc(peers & ((1u << lane) - 1u));
-    int base = 0;
-    if (lane == leader && v >= 0) base = atomicAdd(&cursor[v], __popc(peers));
-    base = __shfl_sync(0xffffffffu, base, leader);
-    if (v >= 0) {
-      const int row = base + rank;
-      if (row < S)
-        rs.row2slot[row] = s;
-      else
-        flag_status(rs.status, STATUS_ROW_OVERFLOW);
-    }
-  }
+  place_slots_stable(rs, s0, s1, S, E1, cursor, tab);   // (its first barrier orders cursor)
   pdl_trigger();
 }
 

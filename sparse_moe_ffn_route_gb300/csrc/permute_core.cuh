@@ -47,12 +47,57 @@ __device__ __forceinline__ int2 block_exclusive_scan2(int2 val, int2* warp_tot, 
   return make_int2(base.x + inc.x - val.x, base.y + inc.y - val.y);
 }
 
+// Stable placement of the slots [s0, s1) (at most 2048, in a block of 1024 threads):
+// warp w takes the 64 slots s0 + 64 w .. s0 + 64 w + 63, as two groups of 32 in
+// order.  A slot's row within its expert v's range is base[v] + (v's slots of the
+// earlier warps) + (v's slots before it in its own warp), so every expert's rows hold
+// its slots in increasing slot order, whatever order the warps run in.
+// tab: [E1][32] bytes of shared memory, tab[v][w] = v's slots among warp w's 64.
+__device__ __forceinline__ void place_slots_stable(const RouteState& rs, int s0, int s1, int S, int E1,
+                                                   const int* base, uint8_t* tab) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t* tw = reinterpret_cast<uint32_t*>(tab);
+  for (int i = tid; i < E1 * 8; i += kPermuteThreads) tw[i] = 0u;
+  __syncthreads();
+  int v[2], r[2];
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int s = s0 + 64 * warp + 32 * hh + lane;
+    int e = s < s1 ? rs.slot_expert[s] : -1;
+    if (e < 0 || e >= E1) e = -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    const int before = e >= 0 ? (int)tab[e * 32 + warp] : 0;   // v's slots in this warp's first group
+    __syncwarp();
+    if (e >= 0 && rank == 0) tab[e * 32 + warp] = (uint8_t)(before + __popc(peers));
+    __syncwarp();
+    v[hh] = e;
+    r[hh] = before + rank;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    if (v[hh] < 0) continue;
+    // v's slots in warps 0 .. warp - 1: a sum of bytes, four per word
+    const uint32_t* row = tw + v[hh] * 8;
+    uint32_t pre = 0;
+    for (int q = 0; q < (warp >> 2); ++q) pre = __dp4a(row[q], 0x01010101u, pre);
+    if (warp & 3) pre = __dp4a(row[warp >> 2] & ((1u << (8 * (warp & 3))) - 1u), 0x01010101u, pre);
+    const int rrow = base[v[hh]] + (int)pre + r[hh];
+    if (rrow < S)
+      rs.row2slot[rrow] = s0 + 64 * warp + 32 * hh + lane;
+    else
+      flag_status(rs.status, STATUS_ROW_OVERFLOW);
+  }
+}
+
 // Shared memory of permute_block.
 struct PermuteSmem {
-  int cnt[2 * kPermuteThreads];
-  int cursor[2 * kPermuteThreads];
+  int cnt[kMaxExperts + 2];
+  int cursor[kMaxExperts + 2];
   int2 warp_tot[32];
   int2 total;
+  __align__(16) uint8_t tab[(kMaxExperts + 1) * 32];
 };
 
 // The whole grouping by one CTA of kPermuteThreads threads, S <= 2048 slots whose
@@ -62,7 +107,7 @@ __device__ __forceinline__ void permute_block(const RouteState& rs, int S, int E
   int* cnt = sm.cnt;
   int* cursor = sm.cursor;
   int2* warp_tot = sm.warp_tot;
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x;
   for (int v = tid; v < E1; v += kPermuteThreads) cnt[v] = 0;
   __syncthreads();
 
@@ -98,25 +143,8 @@ __device__ __forceinline__ void permute_block(const RouteState& rs, int S, int E
   }
   __syncthreads();
 
-  // Scatter: each warp ranks its 32 slots per expert and reserves a run of rows.
-  for (int s0 = 0; s0 < S; s0 += kPermuteThreads) {
-    const int s = s0 + tid;
-    int v = s < S ? rs.slot_expert[s] : -1;
-    if (v < 0 || v >= E1) v = -1;
-    const uint32_t peers = __match_any_sync(0xffffffffu, v);
-    const int leader = __ffs(peers) - 1;
-    const int rank = __popc(peers & ((1u << lane) - 1u));
-    int base = 0;
-    if (lane == leader && v >= 0) base = atomicAdd(&cursor[v], __popc(peers));
-    base = __shfl_sync(0xffffffffu, base, leader);
-    if (v >= 0) {
-      const int row = base + rank;
-      if (row < S)
-        rs.row2slot[row] = s;
-      else
-        flag_status(rs.status, STATUS_ROW_OVERFLOW);
-    }
-  }
+  // Scatter, stable: every expert's rows take its slots in slot order.
+  place_slots_stable(rs, 0, S, S, E1, cursor, sm.tab);
 }
 
 }  // namespace moe

@@ -111,7 +111,8 @@ def test_unsupported_shapes():
     assert path(moe.qwen_cfg(d_model=100)) == -2                    # d % 32
     assert path(moe.gptoss_cfg().replace(interleaved_gate_up=0)) == -2
     assert path(moe.gptoss_cfg().replace(shared_ff=32)) == -2
-    assert path(moe.qwen_cfg().replace(reserved=(ctypes.c_int32 * 3)(1, 0, 0))) == -1
+    assert path(moe.qwen_cfg().replace(reserved=(ctypes.c_int32 * 2)(1, 0))) == -1
+    assert path(moe.qwen_cfg().replace(deterministic=2)) == -1
     with pytest.raises(moe.MoeError):
         moe.moe_select_path(moe.qwen_cfg(d_model=100), 8)
 
