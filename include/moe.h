@@ -344,6 +344,19 @@ int moe_mxfp4_to_bf16(const void* blocks, const void* scales, int64_t rows, int3
  * No counterpart on the pages: measurement plumbing only. */
 int moe_set_phase_events(void* const* events, int32_t n_events);
 
+/* Test hook for the give-up path of the bounded device waits (no counterpart on the
+ * pages; not for production use).  Every mbarrier wait of the TMA-fed kernels gives
+ * up after max_polls polls (default 2^20, about a second), sets MOE_ERR_TIMEOUT in
+ * the device status word, and the CTA drains what it has in flight, frees its TMEM
+ * and returns.  withhold_first_load = 1 also makes the producer of the CTA that
+ * owns the first unit of work of the grouped GEMMs (prefill, bf16 operands and
+ * router logits) and of the MXFP4 decode ring skip its first load, so that the
+ * wait for it runs out: the call's output is
+ * then undefined and moe_device_status reports MOE_ERR_TIMEOUT.  Applies to the
+ * current device, to calls enqueued after it returns; synchronises the device.
+ * Restore with moe_test_set_wait_limit(1u << 20, 0).  max_polls > 0. */
+int moe_test_set_wait_limit(uint32_t max_polls, int32_t withhold_first_load);
+
 /* Synchronises `stream`, then returns MOE_OK, MOE_ERR_DEVICE_CHECK or
  * MOE_ERR_TIMEOUT according to the device status word kept in `ws`, and clears
  * it.  *detail (if not NULL) receives the raw status bits. */

@@ -119,6 +119,8 @@ def _load():
     lib.moe_mxfp4_to_bf16.restype = I
     lib.moe_set_phase_events.argtypes = [P, ctypes.c_int32]
     lib.moe_set_phase_events.restype = I
+    lib.moe_test_set_wait_limit.argtypes = [ctypes.c_uint32, ctypes.c_int32]
+    lib.moe_test_set_wait_limit.restype = I
     lib.moe_device_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
     lib.moe_device_status.restype = I
     lib.moe_status_string.argtypes = [I]
@@ -130,7 +132,7 @@ _lib = _load()
 EXPORTED = ("moe_workspace_bytes", "moe_select_path", "moe_kernel_plan", "moe_route", "moe_topk_from_logits",
             "moe_group_by_expert", "moe_ffn_forward", "moe_ffn_forward_routed", "moe_ffn_forward_host",
             "moe_ffn_forward_noalloc", "moe_noalloc_workspace_bytes", "moe_noalloc_device_status",
-            "moe_mxfp4_to_bf16", "moe_set_phase_events", "moe_device_status",
+            "moe_mxfp4_to_bf16", "moe_set_phase_events", "moe_test_set_wait_limit", "moe_device_status",
             "moe_status_string")
 PHASES = ("router_logits", "router_select", "permute", "gate_up", "down", "combine")
 
@@ -430,6 +432,15 @@ def moe_set_phase_events(events) -> None:
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     _check(_lib.moe_set_phase_events(arr, len(events)), "moe_set_phase_events")
     _phase_keepalive = (arr, events)
+
+
+DEFAULT_WAIT_POLLS = 1 << 20
+
+
+def moe_test_set_wait_limit(max_polls: int = DEFAULT_WAIT_POLLS, withhold_first_load: bool = False) -> None:
+    """Test hook: the poll limit of the bounded device waits, and whether CTA 0's producer
+    of the TMA-fed kernels skips its first load (see include/moe.h).  Synchronises."""
+    _check(_lib.moe_test_set_wait_limit(max_polls, int(withhold_first_load)), "moe_test_set_wait_limit")
 
 
 def moe_device_status(ws: torch.Tensor, stream=None):

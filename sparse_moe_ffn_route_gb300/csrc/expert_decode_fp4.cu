@@ -370,6 +370,7 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
     // ------------------------------------------------------------ producer
     if (tc::elect_one()) {
       int it = 0, its = 0;                      // ring loads, scale loads issued
+      int withheld = -1;                        // the load skipped by the give-up test
       int st = 0;                               // ring slot of load `it`
       uint32_t ph = 0;                          // its phase parity
       // The scale bytes of unit u go to buffer (u - u0) % kScaleBufs and are requested
@@ -398,6 +399,17 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
         const long long grow = (long long)v * a.R + t * kRows;
         for (int s = 0; s < nst; ++s) {
           if (!tc::mbar_wait(tc::smem_u32(&empty_bar[st]), ph ^ 1, abort, status)) break;
+          // A slot freed by an abort is not refilled: its last load may still be landing.
+          if (*abort) break;
+          if (tc::withheld_load(it, u0 == 0)) {     // the CTA that owns unit 0
+            // the give-up test: this load is never issued, so its stage never fills
+            withheld = it++;
+            if (++st == a.stages) {
+              st = 0;
+              ph ^= 1;
+            }
+            continue;
+          }
           // only the boxes that start inside the row (kin / 2 bytes)
           const int k0 = s * kBoxes * 128;
           const int nbox = min(kBoxes, (a.kin / 2 - k0 + 127) / 128);
@@ -418,7 +430,8 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
         int zero = 0;
         volatile int* never = &zero;
         for (int i = it - a.stages > 0 ? it - a.stages : 0; i < it; ++i)
-          tc::mbar_wait(tc::smem_u32(&full_bar[i % a.stages]), (i / a.stages) & 1, never, status);
+          if (i != withheld)
+            tc::mbar_wait(tc::smem_u32(&full_bar[i % a.stages]), (i / a.stages) & 1, never, status);
         for (int i = its - kScaleBufs > 0 ? its - kScaleBufs : 0; i < its; ++i)
           tc::mbar_wait(tc::smem_u32(&sfull_bar[i % kScaleBufs]), (i / kScaleBufs) & 1, never, status);
       }
@@ -677,6 +690,8 @@ cudaError_t launch_fp4_stream(const uint8_t* codes, const F4Args& a0, int n_expe
 }
 
 }  // namespace
+
+cudaError_t fp4_stream_set_wait_test(uint32_t polls, int withhold) { return tc::set_wait_test(polls, withhold); }
 
 cudaError_t launch_gateup_decode_fp4(const ExpertParams& p, const RouteState& rs, const uint16_t* x, int K,
                                      uint16_t* h, int ldh, int max_items, cudaStream_t s, bool* launched) {

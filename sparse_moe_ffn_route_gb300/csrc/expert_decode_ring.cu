@@ -187,6 +187,8 @@ ring_stream_kernel(const __grid_constant__ CUtensorMap m0, const __grid_constant
         const int row = (sh ? 0 : v * a.R) + kUnitRows * t;
         for (int kc = 0; kc < nkc; kc += kChunks) {
           if (!tc::mbar_wait(tc::smem_u32(&empty_bar[st]), ph ^ 1, abort, status)) break;
+          // A slot freed by an abort is not refilled: its last load may still be landing.
+          if (*abort) break;
           const int nch = min(kChunks, nkc - kc);
           tc::mbar_arrive_expect_tx(tc::smem_u32(&full_bar[st]), (uint32_t)(nch * kChunkBytes));
           for (int j = 0; j < nch; ++j) {
@@ -446,6 +448,8 @@ cudaError_t launch_ring(const ExpertParams& p, RingArgs a, int max_items, cudaSt
 bool small_units(long long units128) { return units128 < 4LL * sm_count(); }
 
 }  // namespace
+
+cudaError_t ring_set_wait_test(uint32_t polls, int withhold) { return tc::set_wait_test(polls, withhold); }
 
 cudaError_t launch_gateup_decode_ring(const ExpertParams& p, const RouteState& rs, const uint16_t* x, int K,
                                       uint16_t* h, int ldh, int max_items, int expect_items, cudaStream_t s,

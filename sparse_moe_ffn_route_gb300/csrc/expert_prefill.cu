@@ -350,7 +350,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (tc::elect_one()) {
-      int s = 0, issued = 0;
+      int s = 0, issued = 0, withheld = -1;
       uint32_t ph = 0;
       for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
         const Tile tl = tile_at(g, t, n_m);
@@ -363,6 +363,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const CUtensorMap* m1 = sh ? &tmS1 : &tmB1;
         for (int kc = 0; kc < tl.nkc; ++kc) {
           if (!tc::mbar_wait(tc::smem_u32(&empty_bar[s]), ph ^ 1, abort, status)) break;
+          // A slot freed by an abort is not refilled: its last load may still be landing.
+          if (*abort) break;
+          if (tc::withheld_load(issued, blockIdx.x == 0)) {   // CTA 0 takes tile 0
+            // the give-up test: this load is never issued, so its stage never fills
+            withheld = issued++;
+            if (++s == kStages) {
+              s = 0;
+              ph ^= 1;
+            }
+            continue;
+          }
           const uint32_t fb = tc::smem_u32(&full_bar[s]);
           const uint32_t sa = tc::smem_u32(smem + s * kStageBytes);
           const uint32_t sb = sa + kAB;
@@ -395,7 +406,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         int zero = 0;
         volatile int* never = &zero;
         for (int i = consumed_s; i < issued; ++i)
-          tc::mbar_wait(tc::smem_u32(&full_bar[i % kStages]), (i / kStages) & 1, never, status);
+          if (i != withheld)
+            tc::mbar_wait(tc::smem_u32(&full_bar[i % kStages]), (i / kStages) & 1, never, status);
       }
     }
   } else if (warp == 1) {
@@ -1032,6 +1044,8 @@ cudaError_t launch_router_gemm(const uint16_t* x, int T, int d, const uint16_t* 
   if (!make_map_bf16(&tB, w_r, (uint64_t)E, d, (uint64_t)d * 2, g.N)) return cudaErrorInvalidValue;
   return launch_gemm<false, false>(tA, tB, tB, tB, tB, g, (T + kBM - 1) / kBM, s);
 }
+
+cudaError_t prefill_set_wait_test(uint32_t polls, int withhold) { return tc::set_wait_test(polls, withhold); }
 
 cudaError_t launch_down_prefill(const ExpertParams& p, int wfmt, const RouteState& rs,
                                 const uint16_t* h, int ldh, int S, float* Y, float* yacc, int K,

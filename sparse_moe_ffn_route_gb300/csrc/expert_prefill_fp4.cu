@@ -200,6 +200,8 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         const uint32_t bytes = (uint32_t)(gm * kTileA + g.N * 32);
         for (int kc = 0; kc < g.nkc; ++kc) {
           if (!tc::mbar_wait(tc::smem_u32(&empty_bar[s]), ph ^ 1, abort, status)) break;
+          // A slot freed by an abort is not refilled: its last load may still be landing.
+          if (*abort) break;
           const uint32_t fb = tc::smem_u32(&full_bar[s]);
           const uint32_t sa = tc::smem_u32(smem + s * kLoadStage);
           tc::mbar_arrive_expect_tx(fb, bytes);
@@ -638,6 +640,8 @@ cudaError_t launch_gateup_prefill_fp4(const ExpertParams& p, const RouteState& r
     return cudaErrorInvalidValue;
   return launch_fp4_gemm(tA, tC, g, max_items, s);
 }
+
+cudaError_t prefill_fp4_set_wait_test(uint32_t polls, int withhold) { return tc::set_wait_test(polls, withhold); }
 
 cudaError_t launch_down_prefill_fp4(const ExpertParams& p, const RouteState& rs, const uint16_t* h16, int ldh16,
                                     int S, float* Y, float* yacc, int K, uint8_t* scratch, int max_items,

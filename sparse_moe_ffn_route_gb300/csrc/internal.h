@@ -217,6 +217,14 @@ cudaError_t launch_down_prefill_fp4(const ExpertParams& p, const RouteState& rs,
                                     int S, float* Y, float* yacc, int K, uint8_t* scratch, int max_items,
                                     cudaStream_t s);
 
+// The bounded-wait limits of each translation unit with TMA-fed kernels (see
+// tc::WaitTest): the poll limit, and whether CTA 0's producer withholds its first load
+// (the grouped GEMMs of expert_prefill.cu and the MXFP4 decode ring read it).
+cudaError_t prefill_set_wait_test(uint32_t polls, int withhold);
+cudaError_t prefill_fp4_set_wait_test(uint32_t polls, int withhold);
+cudaError_t ring_set_wait_test(uint32_t polls, int withhold);
+cudaError_t fp4_stream_set_wait_test(uint32_t polls, int withhold);
+
 // MXFP4 [rows, n_in/32, 16] + scales -> bf16 [rows, n_in].
 cudaError_t launch_mxfp4_to_bf16(const uint8_t* blocks, const uint8_t* scales, long long rows,
                                  int n_in, uint16_t* out, cudaStream_t s);

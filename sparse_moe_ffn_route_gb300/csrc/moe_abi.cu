@@ -752,6 +752,16 @@ int moe_set_phase_events(void* const* events, int32_t n_events) {
   return MOE_OK;
 }
 
+int moe_test_set_wait_limit(uint32_t max_polls, int32_t withhold_first_load) {
+  if (max_polls == 0 || withhold_first_load < 0 || withhold_first_load > 1) return MOE_ERR_INVALID_ARG;
+  const int w = withhold_first_load;
+  MOE_CUDA(prefill_set_wait_test(max_polls, w));
+  MOE_CUDA(prefill_fp4_set_wait_test(max_polls, w));
+  MOE_CUDA(ring_set_wait_test(max_polls, w));
+  MOE_CUDA(fp4_stream_set_wait_test(max_polls, w));
+  return MOE_OK;
+}
+
 int moe_device_status(void* ws, void* stream, uint32_t* detail) {
   if (!ws) return MOE_ERR_INVALID_ARG;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);

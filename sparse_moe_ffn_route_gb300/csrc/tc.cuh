@@ -8,6 +8,7 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_runtime.h>
 
 #include "common.cuh"
 
@@ -50,13 +51,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
+// Limits of the bounded waits, per translation unit (each one that includes this
+// header has its own copy): polls = the poll limit of mbar_wait; withhold = a test
+// of the give-up path: the producer of the CTA that owns the first unit of work of
+// the kernels that read it skips its first load (never issues it), so that the wait
+// for it runs out.  Set only through
+// moe_test_set_wait_limit (set_wait_test below); the defaults are 2^20 polls and no
+// withheld load.
+struct WaitTest {
+  uint32_t polls;
+  int withhold;
+};
+static __constant__ WaitTest c_wait_test = {1u << 20, 0};
+
+// Host: this translation unit's copy of the limits (synchronous copy to the device).
+static inline cudaError_t set_wait_test(uint32_t polls, int withhold) {
+  const WaitTest w{polls, withhold};
+  return cudaMemcpyToSymbol(c_wait_test, &w, sizeof(w));
+}
+
+// Whether the producer must skip load number `i` (the give-up test only); `first`:
+// this CTA owns the kernel's first unit of work.
+__device__ __forceinline__ bool withheld_load(int i, bool first) {
+  return c_wait_test.withhold && first && i == 0;
+}
+
 // Wait for phase `parity` of `bar`, giving up after a bounded number of polls
-// (each try_wait itself blocks for a hardware-defined time slice).  On give-up
-// it sets *abort (shared) and the STATUS_TIMEOUT bit; once *abort is set every
-// later wait returns false at once, so a stuck pipeline drains in bounded time.
+// (c_wait_test.polls, 2^20 by default; each try_wait itself blocks for a
+// hardware-defined time slice).  On give-up it sets *abort (shared) and the
+// STATUS_TIMEOUT bit; once *abort is set every later wait returns false at once, so
+// a stuck pipeline drains in bounded time.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           uint32_t* status) {
-  constexpr uint32_t kMaxPolls = 1u << 20;
+  const uint32_t kMaxPolls = c_wait_test.polls;
   for (uint32_t i = 0; i < kMaxPolls; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;

@@ -175,3 +175,9 @@ def test_rms_norm_needs_the_norm_weight_and_a_router():
     assert st == -2
     # the norm's input copy makes the workspace larger
     assert moe.moe_workspace_bytes(c, 64) > moe.moe_workspace_bytes(c.replace(rms_norm=0), 64)
+
+
+def test_wait_limit_hook_rejects_bad_arguments():
+    """The test hook for the bounded waits checks its arguments before any CUDA call."""
+    assert moe._lib.moe_test_set_wait_limit(0, 0) == -1
+    assert moe._lib.moe_test_set_wait_limit(1 << 20, 2) == -1
