@@ -102,6 +102,8 @@ struct GemmArgs {
   float* Y;               // down output [S, d] (slot order)
   float* yacc;            // down, when non-null: yacc[token, :] += slot_w[slot] * (row + bias) by
                           // atomic adds (token = slot / aK), in place of the Y row
+  float* yzero;           // gate_up, when non-null: cleared by the epilogue warps before their
+  size_t yzero_n4;        // first tile (yzero_n4 float4s): the sums the down projection adds into
   int scale_rows;         // MXFP4: rows of one expert in the transposed scales
   int scale_nblk;         // MXFP4: 32-input blocks per weight row
   // kModeDense (router logits): A = x [rows, d], B = W_r [E, d]; no routing state
@@ -552,6 +554,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const int row = 32 * q + lane;
     int b = 0;
     uint32_t aph = 0;
+    if (g.yzero) {
+      // this CTA's share of the per-token sums of the accumulated down projection,
+      // cleared while the first tile's MMAs run
+      const size_t per = (g.yzero_n4 + gridDim.x - 1) / gridDim.x;
+      const size_t z0 = per * blockIdx.x, z1 = min(g.yzero_n4, z0 + per);
+      float4* z = reinterpret_cast<float4*>(g.yzero);
+      for (size_t i = z0 + (threadIdx.x - 64); i < z1; i += 128) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
       const Tile tl = tile_at(g, t, n_m);
       if (tl.skip) continue;
@@ -924,11 +934,13 @@ cudaError_t launch_transpose_scales(const ExpertParams& p, uint8_t* scratch, cud
 cudaError_t launch_gateup_prefill(const ExpertParams& p, int wfmt, int interleaved,
                                   const RouteState& rs, const uint16_t* xp, int S, const uint16_t* x, int T,
                                   int K, uint16_t* h, int ldh, const uint8_t* scalesT, int max_mtiles,
-                                  cudaStream_t s) {
+                                  float* yzero, size_t yzero_floats, cudaStream_t s) {
   const bool fp4 = wfmt == MOE_WFMT_MXFP4;
   const int nf = gateup_nf(p.ff, p.sff, interleaved, fp4 ? Lay<true, false>::kMaxN : Lay<false, false>::kMaxN);
   GemmArgs g{};
   g.rs = rs;
+  g.yzero = yzero;
+  g.yzero_n4 = yzero_floats / 4;
   g.E = p.E;
   g.mode = interleaved ? kModeGateUpInterleaved : kModeGateUpSplit;
   g.N = 2 * nf;

@@ -100,6 +100,8 @@ struct F4Gemm {
   float* Y;                   // fp32 [S, d] in slot order
   float* yacc;                // down, when non-null: yacc[slot / K] += slot_w[slot] * row (atomic
                               // adds) in place of the Y row
+  float* yzero;               // gate_up, when non-null: cleared by the epilogue warps before their
+  size_t yzero_n4;            // first unit (yzero_n4 float4s): the sums the down projection adds into
   int K;                      // slots per token
   int d;
 };
@@ -140,6 +142,63 @@ __device__ __forceinline__ bool epi_any(bool p) {
       : "r"((uint32_t)p), "n"(32 * kEpiWarps)
       : "memory");
   return r != 0;
+}
+
+// One 16-column chunk of the accumulated down projection.  Lane l holds v = 16
+// accumulator columns of its row; the row's value is v * colmul * rm + bias, times
+// the row's routing weight rw, added into the token's sum at ybase[dst] (dst = the
+// token's row offset plus the unit's first column, ~0 for no row).  The four rows of
+// a lane quad turn around by shuffles (a 4 x 4 transpose of float4 chunks, in two
+// exchange steps) so that lane j of the quad adds chunk j of each of the four rows:
+// one vector reduction instruction then covers 64 contiguous bytes of each of 8
+// rows instead of 16 bytes of each of 32.  Every lane of the warp must call it.
+__device__ __forceinline__ void red_chunk_turned(float (&v)[16], const float* cm, const float* bi, float rm,
+                                                 size_t dst, float rw, float* ybase, int lane) {
+  const float4* cm4 = reinterpret_cast<const float4*>(cm);
+  const float4* bi4 = reinterpret_cast<const float4*>(bi);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 f = cm4[i], b = bi4[i];
+    v[4 * i] = rw * fmaf(v[4 * i], f.x * rm, b.x);
+    v[4 * i + 1] = rw * fmaf(v[4 * i + 1], f.y * rm, b.y);
+    v[4 * i + 2] = rw * fmaf(v[4 * i + 2], f.z * rm, b.z);
+    v[4 * i + 3] = rw * fmaf(v[4 * i + 3], f.w * rm, b.w);
+  }
+  const int j = lane & 3;
+  // step 1 (lanes j, j ^ 2): the off-diagonal 2 x 2 blocks of chunks trade places
+  {
+    const bool hi = j & 2;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float send = hi ? v[e] : v[8 + e];          // chunks 0, 1 or chunks 2, 3
+      const float got = __shfl_xor_sync(0xffffffffu, send, 2);
+      if (hi) v[e] = got;
+      else v[8 + e] = got;
+    }
+  }
+  // step 2 (lanes j, j ^ 1): each 2 x 2 block transposes
+  {
+    const bool odd = j & 1;
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c0 = 8 * blk + e, c1 = 8 * blk + 4 + e;   // element e of chunks 2 blk, 2 blk + 1
+        const float send = odd ? v[c0] : v[c1];
+        const float got = __shfl_xor_sync(0xffffffffu, send, 1);
+        if (odd) v[c0] = got;
+        else v[c1] = got;
+      }
+    }
+  }
+  // lane j now holds chunk j of the quad's rows 0..3 (as its chunks 0..3)
+  const int base = lane & ~3;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const unsigned long long dk = __shfl_sync(0xffffffffu, (unsigned long long)dst, base + k);
+    if (dk != ~0ull)
+      red_add_v4(ybase + dk + 4 * j, v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -353,6 +412,14 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     float* ecm = reinterpret_cast<float*>(bring + kBStages * kTileB);   // [N] 2^c_n
     float* ebi = ecm + kMaxN;                                            // [N] bias
     uint32_t aph = 0;
+    if (g.yzero) {
+      // this CTA's share of the per-token sums of the accumulated down projection,
+      // cleared while the first unit's MMAs run
+      const size_t per = (g.yzero_n4 + gridDim.x - 1) / gridDim.x;
+      const size_t z0 = per * blockIdx.x, z1 = min(g.yzero_n4, z0 + per);
+      float4* z = reinterpret_cast<float4*>(g.yzero);
+      for (size_t i = z0 + etid; i < z1; i += 32 * kEpiWarps) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       // A uniform exit (the barrier also ends every use of the previous unit's constants).
       if (epi_any(*abort != 0)) break;
@@ -391,6 +458,12 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         for (int c = c_begin; c < c_end; ++c) {
           float v[16];
           tc::tmem_ld16(taddr + (uint32_t)(16 * c), v);
+          if (g.yacc) {
+            // down, accumulated (every lane of the warp takes part: the shuffles)
+            red_chunk_turned(v, ecm + 16 * c, ebi + 16 * c, valid ? rm[gi] : 1.f, valid ? dst[gi] : ~size_t(0),
+                             rw[gi], g.yacc + 16 * c, lane);
+            continue;
+          }
           if (!valid) continue;
           const float4* cm4 = reinterpret_cast<const float4*>(ecm + 16 * c);
           const float4* bi4 = reinterpret_cast<const float4*>(ebi + 16 * c);
@@ -421,14 +494,6 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
               sp[0] = make_float4(hv[0], hv[1], hv[2], hv[3]);
               sp[1] = make_float4(hv[4], hv[5], hv[6], hv[7]);
             }
-          } else if (g.yacc) {
-            // the weighted row into the token's fp32 sum (16-byte aligned: d is a
-            // multiple of 32 and 16 c + col0 of 16)
-            float* yp = g.yacc + dst[gi] + 16 * c;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              red_add_v4(yp + 4 * i, rw[gi] * v[4 * i], rw[gi] * v[4 * i + 1], rw[gi] * v[4 * i + 2],
-                         rw[gi] * v[4 * i + 3]);
           } else {
             // Y rows are d fp32 apart with d a multiple of 32, and 16 c + col0 is a
             // multiple of 16: both halves of the chunk start on 32 bytes.
@@ -606,10 +671,12 @@ Fp4Rows prefill_fp4_rows(const ExpertParams& p, uint8_t* scratch, int S) {
 
 cudaError_t launch_gateup_prefill_fp4(const ExpertParams& p, const RouteState& rs, const uint16_t* xp16, int S,
                                       uint16_t* h16, float* hside, int ldh, int kh, uint8_t* scratch,
-                                      int max_items, cudaStream_t s) {
+                                      int max_items, float* yzero, size_t yzero_floats, cudaStream_t s) {
   const Fp4Scratch sc = carve(p, scratch, S);
   F4Gemm g{};
   g.rs = rs;
+  g.yzero = yzero;
+  g.yzero_n4 = yzero_floats / 4;
   g.E = p.E;
   g.R = 2 * p.ff;
   g.nb = p.d / 32;

@@ -118,21 +118,19 @@ cudaError_t launch_router_gemm(const uint16_t* x, int T, int d, const uint16_t* 
 // E, or, when wsh is non-null, x_t . wsh computed here (x bf16 [T, d]).  Writes any
 // non-null output.  rs non-null (S = T * K <= 2048 slots, E1 virtual experts, work
 // items of tpg rows): the same launch then groups the slots by expert, in place of
-// launch_permute.  yzero non-null (not with rs): rows [T, d] fp32 cleared, the
-// per-token sums that the prefill down projection accumulates into.
+// launch_permute.
 cudaError_t launch_router_select(const float* logits, int ldl, int nsplit, size_t nstride, float* lsum,
                                  int ldsum, int T, int E, int k, int norm_topk_prob, float scale,
                                  int has_shared,
                                  int32_t* ids_out, float* w_out, float* sgate_out,
                                  int32_t* slot_expert, float* slot_w, const uint16_t* x, int d,
                                  const uint16_t* wsh, const RouteState* rs, int S, int E1, int tpg,
-                                 float* yzero, cudaStream_t s);
+                                 cudaStream_t s);
 
-// Copy caller routing into the slot arrays (routed entry point); yzero as for
-// launch_router_select.
+// Copy caller routing into the slot arrays (routed entry point).
 cudaError_t launch_ingest_routing(const int32_t* ids, const float* w, const float* sgate, int T,
                                   int E, int k, int has_shared, int32_t* slot_expert,
-                                  float* slot_w, uint32_t* status, float* yzero, int d, cudaStream_t s);
+                                  float* slot_w, uint32_t* status, cudaStream_t s);
 
 // Histogram, offsets, work list (items of up to tpg rows) and row -> slot map; hist is
 // scratch of permute_scratch_bytes(S, E1).
@@ -171,10 +169,12 @@ cudaError_t launch_transpose_scales(const ExpertParams& p, uint8_t* scratch, cud
 // gate_up over the grouped rows: A rows come from xp (the gathered x rows, MXFP4
 // weights) or, with bf16 weights, straight from x [T, d] by row index (grouped row r
 // is token row2slot[r] / K), so that no gathered copy is needed.
+// yzero non-null: the kernel's epilogue warps also clear yzero [yzero_floats] fp32 (the
+// per-token sums the accumulated down projection adds into), before their first tile.
 cudaError_t launch_gateup_prefill(const ExpertParams& p, int wfmt, int interleaved,
                                   const RouteState& rs, const uint16_t* xp, int S, const uint16_t* x, int T,
                                   int K, uint16_t* h, int ldh, const uint8_t* scalesT, int max_mtiles,
-                                  cudaStream_t s);
+                                  float* yzero, size_t yzero_floats, cudaStream_t s);
 // yacc non-null: instead of the Y rows, yacc[t] += slot_w * (row + bias) for slot
 // t * K + j, by atomic adds (yacc [T, d] fp32, zeroed before the call's down step).
 cudaError_t launch_down_prefill(const ExpertParams& p, int wfmt, const RouteState& rs,
@@ -211,7 +211,7 @@ Fp4Rows prefill_fp4_rows(const ExpertParams& p, uint8_t* scratch, int S);
 cudaError_t launch_prefill_fp4_prep(const ExpertParams& p, uint8_t* scratch, int S, cudaStream_t s);
 cudaError_t launch_gateup_prefill_fp4(const ExpertParams& p, const RouteState& rs, const uint16_t* xp16, int S,
                                       uint16_t* h16, float* hside, int ldh, int kh, uint8_t* scratch,
-                                      int max_items, cudaStream_t s);
+                                      int max_items, float* yzero, size_t yzero_floats, cudaStream_t s);
 // yacc non-null: as for launch_down_prefill.
 cudaError_t launch_down_prefill_fp4(const ExpertParams& p, const RouteState& rs, const uint16_t* h16, int ldh16,
                                     int S, float* Y, float* yacc, int K, uint8_t* scratch, int max_items,

@@ -307,8 +307,7 @@ int run_router(const moe_cfg_t* c, const void* x, int T, const moe_router_t* r,
                                 c->expert_weights_scale, has_sh, ids_out, w_out, sgate_out, slot_e,
                                 slot_w, xr, c->d_model, gate_in_logits ? nullptr : wsh,
                                 fill_slots && select_permutes(c, L, T) ? &rs : nullptr, L.S, L.E1,
-                                8 * decode_chunks(c, T), fill_slots && L.accumulate ? at<float>(ws, L.yacc) : nullptr,
-                                s));
+                                8 * decode_chunks(c, T), s));
   if (fill_slots) MOE_CUDA(mark_phase(2, s));
   if (logits_out && has_sh)
     MOE_CUDA(cudaMemcpy2DAsync(logits_out, sizeof(float) * c->n_experts, lg, sizeof(float) * ldl,
@@ -329,9 +328,11 @@ int run_experts(const moe_cfg_t* c, const void* x_layer, int T, const moe_expert
   uint16_t* h = at<uint16_t>(ws, L.h);
   float* Y = at<float>(ws, L.Y);
   // Prefill, not deterministic: the down projection adds each weighted expert output
-  // into yacc (cleared by the select / ingest kernel) and the finish kernel adds the
-  // residual and rounds; otherwise the combine gathers the Y rows in slot order.
+  // into yacc (cleared by the gate_up kernel's epilogue warps) and the finish kernel
+  // adds the residual and rounds; otherwise the combine gathers the Y rows in slot
+  // order.
   float* yacc = L.accumulate ? at<float>(ws, L.yacc) : nullptr;
+  const size_t yacc_floats = L.accumulate ? (size_t)T * c->d_model : 0;
   auto finish = [&](const float* Yv, const float* ya) {
     return ya ? launch_finish_accumulated(ya, T, c->d_model, resid, y, c->y_fp32 != 0, s)
               : launch_combine(Yv, rs.slot_w, rs.slot_expert, T, L.K, c->d_model, L.E1, resid, y,
@@ -353,7 +354,8 @@ int run_experts(const moe_cfg_t* c, const void* x_layer, int T, const moe_expert
     MOE_CUDA(launch_gather_rows_f16(static_cast<const uint16_t*>(x), rs.row2slot, L.S, L.K, c->d_model, xp16,
                                     rows.rowmul, rows.hmax, s));
     MOE_CUDA(mark_phase(3, s));
-    MOE_CUDA(launch_gateup_prefill_fp4(p, rs, xp16, L.S, h16, hside, L.ldh, kh, scratch, max_items, s));
+    MOE_CUDA(launch_gateup_prefill_fp4(p, rs, xp16, L.S, h16, hside, L.ldh, kh, scratch, max_items, yacc,
+                                       yacc_floats, s));
     MOE_CUDA(mark_phase(4, s));
     MOE_CUDA(launch_h_fix_f16(hside, rows.hmax, L.S, c->expert_ff, kh, h16, L.ldh, rows.hmul, s));
     MOE_CUDA(launch_down_prefill_fp4(p, rs, h16, L.ldh, L.S, Y, yacc, L.K, scratch, max_items, s));
@@ -378,7 +380,7 @@ int run_experts(const moe_cfg_t* c, const void* x_layer, int T, const moe_expert
     MOE_CUDA(mark_phase(3, s));
     MOE_CUDA(launch_gateup_prefill(p, c->wfmt, c->interleaved_gate_up, rs, xp, L.S,
                                    static_cast<const uint16_t*>(x), T, L.K, h, L.ldh, scalesT,
-                                   max_mtiles, s));
+                                   max_mtiles, yacc, yacc_floats, s));
     MOE_CUDA(mark_phase(4, s));
     MOE_CUDA(launch_down_prefill(p, c->wfmt, rs, h, L.ldh, L.S, Y, yacc, L.K, scalesT, max_mtiles, s));
     MOE_CUDA(mark_phase(5, s));
@@ -483,7 +485,7 @@ int moe_topk_from_logits(const moe_cfg_t* cfg, const float* logits, int32_t T, i
   const int norm = cfg->gating == MOE_GATING_TOPK_SOFTMAX ? 1 : cfg->norm_topk_prob;
   if (launch_router_select(logits, cfg->n_experts, 1, 0, nullptr, 0, T, cfg->n_experts, cfg->top_k, norm,
                            cfg->expert_weights_scale, 0, topk_ids, topk_w, nullptr, nullptr,
-                           nullptr, nullptr, 0, nullptr, nullptr, 0, 0, 0, nullptr,
+                           nullptr, nullptr, 0, nullptr, nullptr, 0, 0, 0,
                            static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
@@ -510,7 +512,7 @@ int moe_group_by_expert(const moe_cfg_t* cfg, const int32_t* topk_ids, int32_t T
   rs.row2slot = perm;
   const int S = T * cfg->top_k;
   MOE_CUDA(launch_ingest_routing(topk_ids, nullptr, nullptr, T, cfg->n_experts, cfg->top_k, 0, rs.slot_expert,
-                                 nullptr, rs.status, nullptr, cfg->d_model, s));
+                                 nullptr, rs.status, s));
   MOE_CUDA(launch_permute(rs, S, cfg->n_experts, 128, at<int>(ws, L.hist), s));
   return MOE_OK;
 }
@@ -560,8 +562,7 @@ int moe_ffn_forward_routed(const moe_cfg_t* cfg, const void* x, int32_t T,
   MOE_CUDA(mark_phase(0, s));
   MOE_CUDA(launch_ingest_routing(topk_ids, topk_w, sgate, T, cfg->n_experts, cfg->top_k,
                                  cfg->shared_ff > 0, at<int32_t>(ws, L.slot_expert),
-                                 at<float>(ws, L.slot_w), at<uint32_t>(ws, L.status),
-                                 L.accumulate ? at<float>(ws, L.yacc) : nullptr, cfg->d_model, s));
+                                 at<float>(ws, L.slot_w), at<uint32_t>(ws, L.status), s));
   MOE_CUDA(mark_phase(1, s));
   MOE_CUDA(mark_phase(2, s));
   return run_experts(cfg, x, T, experts, shared, y, L, ws, false, s);

@@ -154,7 +154,6 @@ struct SelectArgs {
   const uint16_t* x;
   int d;
   const uint16_t* wsh;
-  float* yzero;     // prefill with accumulated expert outputs: row t (d floats) is cleared
 };
 
 // DOT: the shared-gate dot x_t . wsh may be asked for (else the gate is column E).
@@ -321,14 +320,7 @@ __global__ void __launch_bounds__(kSelectWarps * 32) router_select_kernel(const 
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.x * kSelectWarps + (threadIdx.x >> 5);
-  if (t < a.T) {
-    select_token<EPL, true>(a, t, threadIdx.x & 31);
-    // the token's row of the down projection's per-token sums starts at zero
-    if (a.yzero) {
-      float4* z = reinterpret_cast<float4*>(a.yzero + (size_t)t * a.d);
-      for (int i = threadIdx.x & 31; i < a.d / 4; i += 32) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  }
+  if (t < a.T) select_token<EPL, true>(a, t, threadIdx.x & 31);
 }
 
 // Decode sizes: the selection of every token (a warp per token, in turn) and then
@@ -348,17 +340,11 @@ __global__ void __launch_bounds__(kPermuteThreads) select_permute_kernel(const S
 __global__ void ingest_routing_kernel(const int32_t* __restrict__ ids, const float* __restrict__ w,
                                       const float* __restrict__ sgate, int T, int E, int k,
                                       int has_shared, int32_t* __restrict__ slot_expert,
-                                      float* __restrict__ slot_w, uint32_t* __restrict__ status,
-                                      float* __restrict__ yzero, int d) {
+                                      float* __restrict__ slot_w, uint32_t* __restrict__ status) {
   pdl_wait();
   pdl_trigger();
   // the first kernel of a call: start a clean device status
   if (status && blockIdx.x == 0 && threadIdx.x == 0) *status = 0u;
-  if (yzero) {   // prefill with accumulated expert outputs: the per-token sums start at zero
-    const long nz = (long)T * (d / 4);
-    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < nz; i += (long)gridDim.x * blockDim.x)
-      reinterpret_cast<float4*>(yzero)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
   const int K = k + has_shared;
   const long n = (long)T * K;
   for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
@@ -425,15 +411,15 @@ cudaError_t launch_router_select(const float* logits, int ldl, int nsplit, size_
                                  int32_t* ids_out, float* w_out, float* sgate_out,
                                  int32_t* slot_expert, float* slot_w, const uint16_t* x, int d,
                                  const uint16_t* wsh, const RouteState* rs, int S, int E1, int tpg,
-                                 float* yzero, cudaStream_t s) {
+                                 cudaStream_t s) {
   const SelectArgs a{logits, ldl, nsplit, nstride, lsum, ldsum, T, E, k, norm_topk_prob, scale, has_shared,
-                     ids_out, w_out, sgate_out, slot_expert, slot_w, x, d, wsh, yzero};
+                     ids_out, w_out, sgate_out, slot_expert, slot_w, x, d, wsh};
   const int epl = (E + 31) / 32;
   // rs: also group the slots by expert in the same launch (one CTA); the shared gate
   // must then come as logit column E
   if (rs) {
     // at most 256 experts (the widths that fit the 64 registers of a 1024-thread CTA)
-    if (wsh || yzero || S > kPermuteOneCtaSlots || epl > 8) return cudaErrorInvalidValue;
+    if (wsh || S > kPermuteOneCtaSlots || epl > 8) return cudaErrorInvalidValue;
 #define MOE_SELECT(N) \
   return launch_pdl(select_permute_kernel<N>, dim3(1), dim3(kPermuteThreads), 0, s, a, *rs, S, E1, tpg)
     if (epl <= 1) MOE_SELECT(1);
@@ -455,13 +441,12 @@ cudaError_t launch_router_select(const float* logits, int ldl, int nsplit, size_
 
 cudaError_t launch_ingest_routing(const int32_t* ids, const float* w, const float* sgate, int T,
                                   int E, int k, int has_shared, int32_t* slot_expert,
-                                  float* slot_w, uint32_t* status, float* yzero, int d, cudaStream_t s) {
-  long n = (long)T * (k + has_shared);
-  if (yzero && (long)T * (d / 4) > n) n = (long)T * (d / 4);
+                                  float* slot_w, uint32_t* status, cudaStream_t s) {
+  const long n = (long)T * (k + has_shared);
   int blocks = (int)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
   if (blocks < 1) blocks = 1;   // (T = 0 still clears the status word)
   return launch_pdl(ingest_routing_kernel, dim3(blocks), dim3(256), 0, s, ids, w, sgate, T, E, k,
-                    has_shared, slot_expert, slot_w, status, yzero, d);
+                    has_shared, slot_expert, slot_w, status);
 }
 
 }  // namespace moe
