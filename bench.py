@@ -214,9 +214,9 @@ def work(spec, ids, accumulate=False):
     acc_bytes = T * d * 4
     by = {
         "router_logits": (E + has_sh) * d * 2 + x_bytes + T * (E + has_sh) * 4,
-        "router_select": T * (E + has_sh) * 4 + S * 8 + (acc_bytes if accumulate else 0),
+        "router_select": T * (E + has_sh) * 4 + S * 8,
         "permute": S * 4 * 3,
-        "gate_up": distinct * gu + (sgu if has_sh else 0) + x_bytes + h_bytes,
+        "gate_up": distinct * gu + (sgu if has_sh else 0) + x_bytes + h_bytes + (acc_bytes if accumulate else 0),
         "down": distinct * dn + (sdn if has_sh else 0) + h_bytes + (acc_bytes if accumulate else Y_bytes),
         "combine": (acc_bytes if accumulate else Y_bytes + S * 8) + T * d * 2,
     }
