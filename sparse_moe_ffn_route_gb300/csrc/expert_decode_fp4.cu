@@ -2,8 +2,9 @@
 // stream through shared memory.
 //
 // One persistent CTA per SM takes a contiguous share of the units (work item of up
-// to 8 token rows of one expert) x (128 weight rows), so every CTA gets the same
-// number of units and re-stages its token rows only when the item changes.  Warp 16
+// to 8 token rows of one expert) x (128 weight rows; for gate_up, 64 at the ends of
+// the shares, which are cut in 64-row halves so that no CTA has more than half a unit
+// above the average), and re-stages its token rows only when the item changes.  Warp 16
 // is the producer: one elected lane streams each unit's codes into a ring of
 // shared-memory stages with TMA (two boxes of 128 rows x 128 bytes, 128-byte
 // swizzle: 512 inputs of each row per stage) and the unit's E8M0 scale bytes with
@@ -304,7 +305,8 @@ struct F4Args {
   RouteState rs;
   int R;                      // weight rows per expert: gate_up 2ff (gate, up interleaved), down d
   int kin;                    // inputs per weight row: gate_up d, down ff
-  int tiles;                  // units per work item: ceil(R / kRows)
+  int tiles;                  // positions per work item: gate_up half units (kRows / 2 weight rows),
+                              // down full units (kRows)
   int stages;                 // ring depth
   const uint8_t* scales;      // E8M0 [E, R, kin/32]
   const uint16_t* bias;       // bf16 [E, R] or null
@@ -319,12 +321,48 @@ struct F4Args {
   float* Y;
 };
 
+// The units of one CTA.  gate_up: the work is cut into half units (kRows / 2 weight rows
+// of one work item) and every CTA takes an equal contiguous share of them, so that no
+// CTA has more than half a unit above the average; within its share a CTA takes two
+// halves of the same item, the first at an even position, as one full unit (a 128-row
+// box), and a lone half at either end of the share, or the last 64 rows of an item, as
+// a half unit (a 64-row box).  down: equal shares of full units (the last unit of an
+// item may be short, and loads a 64-row box when it has at most 64 rows).  Every role
+// of the CTA walks the same sequence.
+struct UnitSeq {
+  int p, end, tiles, R, ord;   // next position, end of the share, positions per item, rows per expert, units so far
+  bool halves;                 // positions are half units (else full units of kRows rows)
+};
+
+struct F4Unit {
+  int ai, row0, nrows, ord;    // work item, first weight row, rows (<= kRows), unit ordinal in the CTA
+};
+
+__device__ __forceinline__ bool next_unit(UnitSeq& q, F4Unit& u) {
+  if (q.p >= q.end) return false;
+  const int ai = q.p / q.tiles, th = q.p - ai * q.tiles;
+  u.ai = ai;
+  u.ord = q.ord++;
+  if (!q.halves) {
+    u.row0 = th * kRows;
+    u.nrows = min(kRows, q.R - u.row0);
+    q.p += 1;
+    return true;
+  }
+  const bool full = (th & 1) == 0 && q.p + 1 < q.end && th + 1 < q.tiles;
+  u.row0 = th * (kRows / 2);
+  u.nrows = min(full ? kRows : kRows / 2, q.R - u.row0);
+  q.p += full ? 2 : 1;
+  return true;
+}
+
 // GATEUP: codes are gate_up [E, 2ff, d/2] bytes, tokens are x rows, output h.
 // Otherwise: codes are down [E, d, ff/2], tokens are h rows, output Y.
 // PAIRED: kin / 32 is even (scale bytes read two at a time).
 template <bool GATEUP, bool PAIRED>
 __global__ void __launch_bounds__(kThreads, 1)
-fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
+fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmW64,
+                  const F4Args a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = tc::smem_align1024(smem_raw);
   __shared__ __align__(8) uint64_t full_bar[kMaxRingStages], empty_bar[kMaxRingStages], sfull_bar[kScaleBufs],
@@ -357,13 +395,17 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
   // E8M0 byte -> 2^(s - 127) as fp32: 0 is 2^-127 (subnormal), 255 is NaN
   for (int i = threadIdx.x; i < 256; i += blockDim.x)
     lut[i] = i == 0 ? __uint_as_float(0x00400000u) : i == 255 ? __uint_as_float(0x7FC00000u) : exp2i(i - 127);
-  if (warp == kCW && lane == 0) tc::tma_prefetch_desc(&tmW);
+  if (warp == kCW && lane == 0) {
+    tc::tma_prefetch_desc(&tmW);
+    tc::tma_prefetch_desc(&tmW64);
+  }
   __syncthreads();
   pdl_wait();
 
   const int n_items = *a.rs.n_work;
-  const long long U = (long long)(n_items > 0 ? n_items : 0) * a.tiles;
-  const int u0 = (int)(U * blockIdx.x / gridDim.x), u1 = (int)(U * (blockIdx.x + 1) / gridDim.x);
+  const long long H = (long long)(n_items > 0 ? n_items : 0) * a.tiles;
+  const int h0 = (int)(H * blockIdx.x / gridDim.x), h1 = (int)(H * (blockIdx.x + 1) / gridDim.x);
+  const UnitSeq seq0{h0, h1, a.tiles, a.R, 0, GATEUP};
   const int nst = (L.nb + kBlocksPerStage - 1) / kBlocksPerStage;   // stages per unit
 
   if (warp == kCW) {
@@ -373,14 +415,13 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
       int withheld = -1;                        // the load skipped by the give-up test
       int st = 0;                               // ring slot of load `it`
       uint32_t ph = 0;                          // its phase parity
-      // The scale bytes of unit u go to buffer (u - u0) % kScaleBufs and are requested
-      // a unit ahead of its codes, so that the copy has a whole unit's time to land;
-      // the buffer's previous unit (u - 3) is long done by then.
-      auto load_scales = [&](int u) -> bool {
-        const int ai = u / a.tiles, t = u - ai * a.tiles;
-        const int v = a.rs.work[ai].x;
-        const int row0 = t * kRows, nrows = min(kRows, a.R - row0);
-        const long long grow = (long long)v * a.R + row0;
+      // The scale bytes of the CTA's n-th unit go to buffer n % kScaleBufs and are
+      // requested a unit ahead of its codes, so that the copy has a whole unit's time to
+      // land; the buffer's previous unit (n - 3) is long done by then.
+      auto load_scales = [&](const F4Unit& un) -> bool {
+        const int v = a.rs.work[un.ai].x;
+        const int nrows = un.nrows;
+        const long long grow = (long long)v * a.R + un.row0;
         const int sb = its % kScaleBufs;
         if (!tc::mbar_wait(tc::smem_u32(&sempty_bar[sb]), ((its / kScaleBufs) & 1) ^ 1, abort, status))
           return false;
@@ -391,17 +432,24 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
         ++its;
         return true;
       };
-      bool live = u0 >= u1 || load_scales(u0);
-      for (int u = u0; u < u1 && live && !*abort; ++u) {
-        if (u + 1 < u1 && !load_scales(u + 1)) break;
-        const int ai = u / a.tiles, t = u - ai * a.tiles;
-        const int v = a.rs.work[ai].x;
-        const long long grow = (long long)v * a.R + t * kRows;
+      UnitSeq ahead = seq0;                     // runs one unit ahead (its scales go first)
+      F4Unit un, nx;
+      bool has_next = next_unit(ahead, nx);
+      bool live = !has_next || load_scales(nx);
+      while (live && !*abort && has_next) {
+        un = nx;
+        has_next = next_unit(ahead, nx);
+        if (has_next && !load_scales(nx)) break;
+        const int v = a.rs.work[un.ai].x;
+        const long long grow = (long long)v * a.R + un.row0;
+        const bool half = un.nrows <= kRows / 2;
+        const CUtensorMap* wm = half ? &tmW64 : &tmW;
+        const uint32_t box_bytes = half ? kBoxBytes / 2 : kBoxBytes;
         for (int s = 0; s < nst; ++s) {
           if (!tc::mbar_wait(tc::smem_u32(&empty_bar[st]), ph ^ 1, abort, status)) break;
           // A slot freed by an abort is not refilled: its last load may still be landing.
           if (*abort) break;
-          if (tc::withheld_load(it, u0 == 0)) {     // the CTA that owns unit 0
+          if (tc::withheld_load(it, h0 == 0)) {     // the CTA that owns the first unit
             // the give-up test: this load is never issued, so its stage never fills
             withheld = it++;
             if (++st == a.stages) {
@@ -413,9 +461,9 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
           // only the boxes that start inside the row (kin / 2 bytes)
           const int k0 = s * kBoxes * 128;
           const int nbox = min(kBoxes, (a.kin / 2 - k0 + 127) / 128);
-          tc::mbar_arrive_expect_tx(tc::smem_u32(&full_bar[st]), (uint32_t)(nbox * kBoxBytes));
+          tc::mbar_arrive_expect_tx(tc::smem_u32(&full_bar[st]), (uint32_t)nbox * box_bytes);
           for (int j = 0; j < nbox; ++j)
-            tc::tma_load_2d(tc::smem_u32(smem + st * kStageBytes + j * kBoxBytes), &tmW, k0 + 128 * j,
+            tc::tma_load_2d(tc::smem_u32(smem + st * kStageBytes + j * kBoxBytes), wm, k0 + 128 * j,
                             (int)grow, tc::smem_u32(&full_bar[st]));
           ++it;
           if (++st == a.stages) {
@@ -454,8 +502,10 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
     const int tile0 = (warp - kCW - 1) * kEpiTiles;   // this warp's tiles: tile0 .. + kEpiTiles - 1
     const float4* part = reinterpret_cast<const float4*>(smem + L.part) + lane;
     int cur = -1, ns = 0, nu = 0;                // staged item, items staged, units finished
-    for (int u = u0; u < u1; ++u) {
-      const int ai = u / a.tiles, t = u - ai * a.tiles;
+    UnitSeq seq = seq0;
+    F4Unit un;
+    while (next_unit(seq, un)) {
+      const int ai = un.ai;
       const int2 item = a.rs.work[ai];
       const int v = item.x;
       const int r0 = a.rs.offsets[v] + item.y;
@@ -464,7 +514,7 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
         cur = ai;
         ++ns;
       }
-      const int row0 = t * kRows, nrows = min(kRows, a.R - row0);
+      const int row0 = un.row0, nrows = un.nrows;
       // biases and output rows first, so that their round trips overlap the wait
       uint32_t bias[kEpiTiles];                  // two bf16: (gate, up) of feature f, or rows o, o + 8
 #pragma unroll
@@ -563,10 +613,12 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
   int st = 0, its = 0, cur = -1;               // ring slot, scale loads consumed, staged item
   int ns = 0, nu = 0;                            // items staged, units handed to the epilogue warp
   uint32_t ph = 0;                               // phase parity of ring slot st
-  for (int u = u0; u < u1; ++u) {
+  UnitSeq seq = seq0;
+  F4Unit un;
+  while (next_unit(seq, un)) {
     // On abort every wait returns at once; the loop still runs to its end so that
     // all consumer warps take the same barriers.
-    const int ai = u / a.tiles, t = u - ai * a.tiles;
+    const int ai = un.ai;
     const int2 item = a.rs.work[ai];
     const int v = item.x;
     const int r0 = a.rs.offsets[v] + item.y;     // first permuted row of the item
@@ -592,7 +644,7 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
       cur = ai;
       ++ns;
     }
-    const int row0 = t * kRows, nrows = min(kRows, a.R - row0);
+    const int nrows = un.nrows;
     const bool on = 32 * tp < nrows;             // nrows is a multiple of 32
     const int sb = its % kScaleBufs;
     bool ok = tc::mbar_wait(tc::smem_u32(&sfull_bar[sb]), (its / kScaleBufs) & 1, abort, status);
@@ -600,7 +652,7 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const F4Args a) {
     float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     // the block pair this warp takes in every box turns with the unit, so that the
     // ragged last box of a row does not always fall to the same warps
-    const int qe = (q + u) & (kClasses - 1);
+    const int qe = (q + un.ord) & (kClasses - 1);
     for (int s = 0; s < nst; ++s) {
       ok = ok && tc::mbar_wait(tc::smem_u32(&full_bar[st]), ph, abort, status);
       if (ok && on) {
@@ -671,22 +723,28 @@ cudaError_t launch_fp4_stream(const uint8_t* codes, const F4Args& a0, int n_expe
   if (!a.stages) return cudaSuccess;
   if ((reinterpret_cast<uintptr_t>(a.scales) & 15) || (reinterpret_cast<uintptr_t>(codes) & 15))
     return cudaSuccess;
-  CUtensorMap m;
+  CUtensorMap m, m64;   // boxes of 128 rows (full units) and 64 rows (half units) x 128 bytes
   if (!make_map(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, (uint64_t)n_experts * a.R, (uint64_t)a.kin / 2,
-                (uint64_t)a.kin / 2, kRows, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+                (uint64_t)a.kin / 2, kRows, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&m64, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, (uint64_t)n_experts * a.R, (uint64_t)a.kin / 2,
+                (uint64_t)a.kin / 2, kRows / 2, 128, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaSuccess;
-  a.tiles = (a.R + kRows - 1) / kRows;
+  // gate_up shares are cut in half units (1440 full units of gpt-oss-20b over 152 SMs
+  // leave 72 CTAs a whole unit above the rest); down keeps full units, where a CTA's
+  // lone halves would cost more than its imbalance
+  const int unit_rows = GATEUP ? kRows / 2 : kRows;
+  a.tiles = (a.R + unit_rows - 1) / unit_rows;
   const int bytes = f4_smem(a.kin, a.stages).total + 1024;
-  const long long units = (long long)max_items * a.tiles;
+  const long long halves = (long long)max_items * a.tiles;
   int grid = sm_count();
-  if (units < grid) grid = (int)(units > 0 ? units : 1);
+  if (halves < grid) grid = (int)(halves > 0 ? halves : 1);
   *launched = true;
   if ((a.kin / 32) % 2 == 0) {
     set_fp4_smem<GATEUP, true>(bytes);
-    return launch_pdl(fp4_stream_kernel<GATEUP, true>, dim3(grid), dim3(kThreads), (size_t)bytes, s, m, a);
+    return launch_pdl(fp4_stream_kernel<GATEUP, true>, dim3(grid), dim3(kThreads), (size_t)bytes, s, m, m64, a);
   }
   set_fp4_smem<GATEUP, false>(bytes);
-  return launch_pdl(fp4_stream_kernel<GATEUP, false>, dim3(grid), dim3(kThreads), (size_t)bytes, s, m, a);
+  return launch_pdl(fp4_stream_kernel<GATEUP, false>, dim3(grid), dim3(kThreads), (size_t)bytes, s, m, m64, a);
 }
 
 }  // namespace
