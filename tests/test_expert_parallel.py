@@ -152,6 +152,56 @@ def test_expert_parallel_matches_single_process_oracle(world, family):
         assert d["y_equal"], d
 
 
+def _forward_rank(rank, world, port, q):
+    """ep.forward end to end on one rank, with stand-in experts: expert e maps a row r
+    to (e + 1) * r, so the result is known in closed form."""
+    import sys
+    sys.path.insert(0, ROOT)
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    torch.distributed.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        from sparse_moe_ffn_route_gb300 import expert_parallel as ep
+        E, k, d = 8, 3, 5
+        T = [4, 0, 7, 2][rank] if world == 4 else [6, 3][rank]
+        g = torch.Generator().manual_seed(100 + rank)
+        x = torch.randn(T, d, generator=g, dtype=torch.float64)
+        ids = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).to(torch.int32) \
+            if T else torch.empty((0, k), dtype=torch.int32)
+        w = torch.rand(T, k, generator=g, dtype=torch.float64)
+        epr = E // world
+
+        def local(rows, local_ids):
+            return rows * (local_ids.to(torch.float64) + rank * epr + 1.0).unsqueeze(1)
+
+        y = ep.forward(x, ids, w, E, local)
+        want = torch.zeros((T, d), dtype=torch.float64)
+        for j in range(k):
+            want = want + w[:, j:j + 1] * (x * (ids[:, j:j + 1].to(torch.float64) + 1.0))
+        q.put({"rank": rank, "ok": bool(torch.equal(y, want)), "T": T})
+    except Exception as e:
+        q.put({"rank": rank, "error": repr(e)})
+        raise
+    finally:
+        torch.distributed.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 4])
+def test_forward_end_to_end_with_stand_in_experts(world):
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_forward_rank, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = [q.get(timeout=300) for _ in procs]
+    for p in procs:
+        p.join(120)
+    for d in res:
+        assert "error" not in d and d["ok"], d
+
+
 def test_owner_blocks_and_uneven_split_rejected():
     from sparse_moe_ffn_route_gb300 import expert_parallel as ep
     ids = torch.tensor([[0, 7], [3, 4]], dtype=torch.int32)
