@@ -124,7 +124,8 @@ def int_range_u8(key: int, slot: int, shape, lo: int, hi: int,
 
 def f64_to_bf16(v) -> np.ndarray:
     """Round fp64 values to bf16 bit patterns: first to fp32 (RNE), then RNE to 16 bits."""
-    f = np.asarray(v, dtype=np.float64).astype(np.float32)
+    with np.errstate(over="ignore"):          # beyond the fp32 range: +-inf, as in bf16
+        f = np.asarray(v, dtype=np.float64).astype(np.float32)
     shape = f.shape
     u = np.ascontiguousarray(f.reshape(-1)).view(np.uint32).astype(np.uint64)
     nan = (u & 0x7FFFFFFF) > 0x7F800000
