@@ -29,10 +29,12 @@
 // Tiling.  A work item is up to 256 rows of one expert (two m tiles of 128); a
 // unit is (work item, n tile of N <= 240 weight rows).  The dequantised B tile of
 // a k step feeds the MMAs of both m tiles, which accumulate into two TMEM
-// accumulators (columns 0 and 256).  One persistent CTA per SM walks the units
-// m-major.  Warp roles:
-//   warp 0        TMA producer: per 64-input k step, the A tile of each m tile
-//                 (128 x 64 f16, 128-byte swizzle) and the codes (N x 32 bytes)
+// accumulators (columns 0 and 256).  One persistent CTA per SM; the CTAs claim units
+// from a counter (the n tiles of an item in turn, the two-m-tile items first), so
+// that they finish within about one unit of each other.  Warp roles:
+//   warp 0        TMA producer: claims the units and hands them to the other roles
+//                 through a small queue; per 64-input k step, the A tile of each m
+//                 tile (128 x 64 f16, 128-byte swizzle) and the codes (N x 32 bytes)
 //                 into a 4-stage ring;
 //   warp 1        TMEM owner and MMA issuer (M 128, N, K 16, one elected thread);
 //   warps 2..9    epilogue: two warps per TMEM lane quarter, each half of the columns;
@@ -77,6 +79,8 @@ constexpr int kEpiWarps = 8;
 constexpr int kDqWarps = 8;
 constexpr int kThreads = 32 * (2 + kEpiWarps + kDqWarps);
 constexpr uint32_t kTmemCols = 512;               // accumulators at columns 0 and 256
+constexpr int kQ = 4;                             // unit queue: claimed units on their way to the roles
+constexpr int kQTakers = 1 + kDqWarps + 1;        // MMA thread, dequant warps, epilogue thread 0
 
 static_assert(kTileB % 1024 == 0, "B tiles must stay 1024-aligned");
 
@@ -104,6 +108,8 @@ struct F4Gemm {
   size_t yzero_n4;            // first unit (yzero_n4 float4s): the sums the down projection adds into
   int K;                      // slots per token
   int d;
+  int* sched;                 // unit counter, zero at launch: CTAs claim units from it
+  const int32_t* order;       // [work items] the order in which items are claimed
 };
 
 struct Unit {
@@ -130,18 +136,6 @@ constexpr int kSegs = (2 * kMaxN + kDqThreads - 1) / kDqThreads;
 // Barrier among the epilogue warps only (named barrier 1).
 __device__ __forceinline__ void epi_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
-}
-
-// The same barrier, returning whether `p` holds for any epilogue thread: a decision
-// that every epilogue warp takes alike (so none is left waiting at a barrier).
-__device__ __forceinline__ bool epi_any(bool p) {
-  uint32_t r;
-  asm volatile(
-      "{ .reg .pred pi, po; setp.ne.u32 pi, %1, 0; bar.red.or.pred po, 1, %2, pi; selp.u32 %0, 1, 0, po; }"
-      : "=r"(r)
-      : "r"((uint32_t)p), "n"(32 * kEpiWarps)
-      : "memory");
-  return r != 0;
 }
 
 // One 16-column chunk of the accumulated down projection.  Lane l holds v = 16
@@ -212,6 +206,11 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
   __shared__ int consumed_s;     // loads the MMA thread has waited for
+  // The producer claims each unit (atomicAdd on g.sched, mapped through g.order) and
+  // hands it to the other roles through this queue; -1 ends the work.
+  __shared__ __align__(8) uint64_t q_full[kQ], q_empty[kQ];
+  __shared__ int unit_q[kQ];
+  __shared__ int epi_unit_s;     // the unit the epilogue warps work on
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint32_t* status = g.rs.status;
@@ -229,6 +228,10 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     tc::mbar_init(tc::smem_u32(&tfull_bar), 1);
     tc::mbar_init(tc::smem_u32(&tempty_bar), kEpiWarps);
     tc::mbar_init(tc::smem_u32(&drain_bar), 1);
+    for (int i = 0; i < kQ; ++i) {
+      tc::mbar_init(tc::smem_u32(&q_full[i]), 1);
+      tc::mbar_init(tc::smem_u32(&q_empty[i]), kQTakers);
+    }
     abort_s = 0;
     consumed_s = 0;
     tc::fence_barrier_init();
@@ -249,9 +252,22 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (tc::elect_one()) {
-      int s = 0, issued = 0;
-      uint32_t ph = 0;
-      for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
+      int s = 0, issued = 0, qs = 0;
+      uint32_t ph = 0, qph = 0;
+      while (!*abort) {
+        // Claim the next unit: the n tiles of each item in turn, items in g.order.  The
+        // claim is made once this CTA's loads of its current unit are issued, a few k
+        // steps before its MMAs run dry, so that the CTAs finish within about one unit.
+        const int tk = atomicAdd(g.sched, 1);
+        const int t = tk < total ? g.order[tk / g.nt] * g.nt + tk % g.nt : -1;
+        if (!tc::mbar_wait(tc::smem_u32(&q_empty[qs]), qph ^ 1, abort, status)) break;
+        unit_q[qs] = t;
+        tc::mbar_arrive(tc::smem_u32(&q_full[qs]));
+        if (++qs == kQ) {
+          qs = 0;
+          qph ^= 1;
+        }
+        if (t < 0) break;
         const Unit u = unit_at(g, t);
         const int a_row = g.rs.offsets[u.v] + u.row0;
         const int b_row = u.v * g.R + u.n * g.N;
@@ -289,7 +305,17 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       uint32_t ph = 0, bph = 0, aph = 0;
       const uint32_t idesc = tc::idesc_f16_f32(kBM, g.N);
       bool any = false;
-      for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
+      int qs = 0;
+      uint32_t qph = 0;
+      while (!*abort) {
+        if (!tc::mbar_wait(tc::smem_u32(&q_full[qs]), qph, abort, status)) break;
+        const int t = *reinterpret_cast<volatile int*>(&unit_q[qs]);
+        tc::mbar_arrive(tc::smem_u32(&q_empty[qs]));
+        if (++qs == kQ) {
+          qs = 0;
+          qph ^= 1;
+        }
+        if (t < 0) break;
         const Unit u = unit_at(g, t);
         const int gm = u.cnt > kBM ? 2 : 1;
         if (!tc::mbar_wait(tc::smem_u32(&tempty_bar), aph ^ 1, abort, status)) break;
@@ -337,9 +363,18 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   } else if (warp >= 2 + kEpiWarps) {
     // ---------------------------------------------------------------- MXFP4 dequant
     const int tid = threadIdx.x - 32 * (2 + kEpiWarps);
-    int s = 0, bs = 0;
-    uint32_t ph = 0, bph = 0;
-    for (int t = blockIdx.x; t < total && !*abort; t += gridDim.x) {
+    int s = 0, bs = 0, qs = 0;
+    uint32_t ph = 0, bph = 0, qph = 0;
+    while (!*abort) {
+      if (!tc::mbar_wait(tc::smem_u32(&q_full[qs]), qph, abort, status)) break;
+      const int t = *reinterpret_cast<volatile int*>(&unit_q[qs]);
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&q_empty[qs]));
+      if (++qs == kQ) {
+        qs = 0;
+        qph ^= 1;
+      }
+      if (t < 0) break;
       const Unit u = unit_at(g, t);
       const size_t row0 = (size_t)u.v * g.R + (size_t)u.n * g.N;
       int c[kSegs], kr[kSegs];
@@ -420,9 +455,27 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       float4* z = reinterpret_cast<float4*>(g.yzero);
       for (size_t i = z0 + etid; i < z1; i += 32 * kEpiWarps) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      // A uniform exit (the barrier also ends every use of the previous unit's constants).
-      if (epi_any(*abort != 0)) break;
+    int qs = 0;
+    uint32_t qph = 0;
+    for (;;) {
+      // Epilogue thread 0 takes the next unit from the queue (-1 at the end or on
+      // give-up) and every epilogue warp reads it after the barrier: a uniform exit.
+      // The barrier also ends every use of the previous unit's constants.
+      if (etid == 0) {
+        int t = -1;
+        if (!*abort && tc::mbar_wait(tc::smem_u32(&q_full[qs]), qph, abort, status)) {
+          t = *reinterpret_cast<volatile int*>(&unit_q[qs]);
+          tc::mbar_arrive(tc::smem_u32(&q_empty[qs]));
+          if (++qs == kQ) {
+            qs = 0;
+            qph ^= 1;
+          }
+        }
+        epi_unit_s = t;
+      }
+      epi_sync();
+      const int t = epi_unit_s;
+      if (t < 0) break;
       const Unit u = unit_at(g, t);
       const int gm = u.cnt > kBM ? 2 : 1;
       const int col0 = u.n * g.N;                          // first weight row of the unit
@@ -448,7 +501,7 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                              : (size_t)slot * g.d + col0;
       }
       epi_sync();
-      // On give-up the abort flag is set, and the next epi_any leaves the loop.
+      // On give-up the abort flag is set, and thread 0 then ends the loop.
       if (!tc::mbar_wait(tc::smem_u32(&tfull_bar), aph, abort, status)) continue;
       tc::tc_fence_after();
       for (int gi = 0; gi < gm; ++gi) {
@@ -581,6 +634,8 @@ struct Fp4Scratch {
   float* rowmul;        // [S] 2^-e of the staged x rows
   uint32_t* hmax;       // [S] largest |h| per row
   float* hmul;          // [S] 2^-e of the staged h rows
+  int32_t* order;       // [max items] the order in which the GEMMs' CTAs claim work items
+  int32_t* sched;       // [2] unit counters of gate_up and down
 };
 
 size_t carve_off(const ExpertParams& p, int S, Fp4Scratch* sc, uint8_t* base) {
@@ -599,6 +654,8 @@ size_t carve_off(const ExpertParams& p, int S, Fp4Scratch* sc, uint8_t* base) {
   uint8_t* e = take(4 * (size_t)S);
   uint8_t* f = take(4 * (size_t)S);
   uint8_t* h = take(4 * (size_t)S);
+  uint8_t* o = take(4 * ((size_t)p.E + ((size_t)S + 2 * kBM - 1) / (2 * kBM)));
+  uint8_t* q = take(8);
   if (sc) {
     sc->colmul_gu = reinterpret_cast<float*>(a);
     sc->colmul_dn = reinterpret_cast<float*>(b);
@@ -607,6 +664,8 @@ size_t carve_off(const ExpertParams& p, int S, Fp4Scratch* sc, uint8_t* base) {
     sc->rowmul = reinterpret_cast<float*>(e);
     sc->hmax = reinterpret_cast<uint32_t*>(f);
     sc->hmul = reinterpret_cast<float*>(h);
+    sc->order = reinterpret_cast<int32_t*>(o);
+    sc->sched = reinterpret_cast<int32_t*>(q);
   }
   return off;
 }
@@ -666,7 +725,7 @@ cudaError_t launch_prefill_fp4_prep(const ExpertParams& p, uint8_t* scratch, int
 
 Fp4Rows prefill_fp4_rows(const ExpertParams& p, uint8_t* scratch, int S) {
   const Fp4Scratch sc = carve(p, scratch, S);
-  return Fp4Rows{sc.rowmul, sc.hmax, sc.hmul};
+  return Fp4Rows{sc.rowmul, sc.hmax, sc.hmul, sc.order, sc.sched};
 }
 
 cudaError_t launch_gateup_prefill_fp4(const ExpertParams& p, const RouteState& rs, const uint16_t* xp16, int S,
@@ -695,6 +754,8 @@ cudaError_t launch_gateup_prefill_fp4(const ExpertParams& p, const RouteState& r
   g.hboost = ldexpf(1.f, kh);
   g.hsmall = ldexpf(1.f, -2 - kh);
   g.hmax = sc.hmax;
+  g.sched = sc.sched;
+  g.order = sc.order;
   g.limit = p.limit;
   g.alpha = p.alpha;
   g.d = p.d;
@@ -730,6 +791,8 @@ cudaError_t launch_down_prefill_fp4(const ExpertParams& p, const RouteState& rs,
   g.rowmul = sc.hmul;
   g.bias = p.dn_bias;
   g.gateup = 0;
+  g.sched = sc.sched + 1;
+  g.order = sc.order;
   g.Y = Y;
   g.d = p.d;
   CUtensorMap tA, tC;

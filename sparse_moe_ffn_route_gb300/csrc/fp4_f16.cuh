@@ -1,6 +1,6 @@
-// Device helpers of the f16-operand MXFP4 kernels (expert_prefill_fp4.cu,
-// expert_decode_tc.cu): the clamped GLU, the exact E2M1 -> f16 decode of one
-// 32-input block into a 128-byte-swizzled K-major tile, and its f16 multiplier.
+// Device helpers of the f16-operand MXFP4 prefill kernel (expert_prefill_fp4.cu):
+// the clamped GLU, the exact E2M1 -> f16 decode of one 32-input block into a
+// 128-byte-swizzled K-major tile, and its f16 multiplier.
 //
 // Source: "Phase 19: MoE - gpt-oss-20b", section 2 (clamped GLU) and section 3
 // (MXFP4: E2M1 codes, low nibble first, one E8M0 scale per 32 inputs).

@@ -184,15 +184,23 @@ cudaError_t launch_down_prefill(const ExpertParams& p, int wfmt, const RouteStat
 // f16 token operands (stage_f16.cu).  Per grouped row: rowmul = 2^-e of the staged
 // x row, hmax = largest |h| (fp32 bits, accumulated by the gate_up epilogue), hmul =
 // 2^-e of the staged h row.
+// The grouped GEMMs of expert_prefill_fp4.cu claim their units from a counter
+// (sched[0] gate_up, sched[1] down) in the item order `order` [work items].
 struct Fp4Rows {
   float* rowmul;
   uint32_t* hmax;
   float* hmul;
+  int32_t* order;
+  int32_t* sched;
 };
 // x rows of the grouped order as f16 times 2^e per row (largest magnitude in
-// [2^14, 2^15)), rowmul[r] = 2^-e; clears hmax[r] when hmax is non-null.
+// [2^14, 2^15)), rowmul[r] = 2^-e; clears hmax[r] when hmax is non-null.  When
+// order is non-null it also writes the GEMMs' item order (items of more than
+// half_rows rows first, in the work list's order, then the others) and clears the
+// two unit counters sched[0..1].
 cudaError_t launch_gather_rows_f16(const uint16_t* x, const int32_t* row2slot, int S, int K, int d, uint16_t* xp16,
-                                   float* rowmul, uint32_t* hmax, cudaStream_t s);
+                                   float* rowmul, uint32_t* hmax, const RouteState& rs, int half_rows,
+                                   int32_t* order, int32_t* sched, cudaStream_t s);
 // h rows staged by the gate_up epilogue as f16 times 2^kh: hmul[r] = 2^-kh, except
 // rows whose largest |h| (hmax) is below 2^(-2 - kh), which are re-staged from their
 // fp32 copy (hside [S, ldh]) with their own power of two.

@@ -352,7 +352,7 @@ int run_experts(const moe_cfg_t* c, const void* x_layer, int T, const moe_expert
     MOE_CUDA(launch_prefill_fp4_prep(p, scratch, L.S, s));
     MOE_CUDA(launch_permute(rs, L.S, L.E1, kItemRows, at<int>(ws, L.hist), s));
     MOE_CUDA(launch_gather_rows_f16(static_cast<const uint16_t*>(x), rs.row2slot, L.S, L.K, c->d_model, xp16,
-                                    rows.rowmul, rows.hmax, s));
+                                    rows.rowmul, rows.hmax, rs, kItemRows / 2, rows.order, rows.sched, s));
     MOE_CUDA(mark_phase(3, s));
     MOE_CUDA(launch_gateup_prefill_fp4(p, rs, xp16, L.S, h16, hside, L.ldh, kh, scratch, max_items, yacc,
                                        yacc_floats, s));

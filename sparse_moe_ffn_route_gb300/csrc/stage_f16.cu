@@ -9,7 +9,8 @@
 //   gather_rows_f16_kernel: x rows of the grouped order -> f16 (one pass, the row held
 //                           in registers), rowmul[r] = 2^-e;
 //                           also clears the per-row maxima that the gate_up
-//                           epilogue accumulates for h.
+//                           epilogue accumulates for h, and (one warp) writes the
+//                           GEMMs' item order and clears their unit counters.
 //   h_fix_f16_kernel:       h rows, written by the gate_up epilogue as f16 times a
 //                           fixed 2^kh with each row's largest |h|: rows whose
 //                           largest |h| fits that scale keep it (hmul = 2^-kh); a row
@@ -44,6 +45,29 @@ __device__ __forceinline__ uint32_t max_abs_bf16x8(const uint4& v) {
   return __vmaxu2(__vmaxu2(v.x & mk, v.y & mk), __vmaxu2(v.z & mk, v.w & mk));
 }
 
+// The item order of the MXFP4 grouped GEMMs, written by one warp: items of more than
+// half_rows rows (two m tiles) first, in the work list's order, then the one-m-tile
+// items from the end backwards.  The GEMMs' CTAs claim units in this order, so that
+// the half-cost units come last and even out the CTAs' finishing times.
+__device__ void order_items(const RouteState& rs, int half_rows, int32_t* __restrict__ order, int lane) {
+  const int n = *rs.n_work;
+  const uint32_t below = (1u << lane) - 1u;
+  int nh = 0, nl = 0;
+  for (int b = 0; b < n; b += 32) {
+    const int i = b + lane;
+    bool heavy = false;
+    if (i < n) {
+      const int2 w = rs.work[i];
+      heavy = rs.offsets[w.x + 1] - rs.offsets[w.x] - w.y > half_rows;
+    }
+    const uint32_t hb = __ballot_sync(0xffffffffu, i < n && heavy);
+    const uint32_t lb = __ballot_sync(0xffffffffu, i < n && !heavy);
+    if (i < n) order[heavy ? nh + __popc(hb & below) : n - 1 - (nl + __popc(lb & below))] = i;
+    nh += __popc(hb);
+    nl += __popc(lb);
+  }
+}
+
 // Warp per grouped row.  UNITS > 0: the row (at most 32 * UNITS 16-byte units) is
 // loaded into registers at once (one round trip), its largest magnitude found and the
 // row converted from the registers; UNITS == 0: any width, two passes over the row.
@@ -51,9 +75,14 @@ template <int UNITS>
 __global__ void __launch_bounds__(256)
 gather_rows_f16_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ row2slot, int S, int K,
                        int d, uint16_t* __restrict__ xp, float* __restrict__ rowmul,
-                       uint32_t* __restrict__ hmax) {
+                       uint32_t* __restrict__ hmax, const RouteState rs, int half_rows,
+                       int32_t* __restrict__ order, int32_t* __restrict__ sched) {
   pdl_wait();
   const int lane = threadIdx.x & 31;
+  if (order && blockIdx.x == 0 && threadIdx.x < 32) {
+    order_items(rs, half_rows, order, lane);
+    if (lane == 0) sched[0] = sched[1] = 0;
+  }
   const int nvec = d / 8;
   for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < S; r += (gridDim.x * blockDim.x) >> 5) {
     const int t = row2slot[r] / K;
@@ -128,19 +157,17 @@ int grid_rows(int S) {
 }  // namespace
 
 cudaError_t launch_gather_rows_f16(const uint16_t* x, const int32_t* row2slot, int S, int K, int d, uint16_t* xp16,
-                                   float* rowmul, uint32_t* hmax, cudaStream_t s) {
+                                   float* rowmul, uint32_t* hmax, const RouteState& rs, int half_rows,
+                                   int32_t* order, int32_t* sched, cudaStream_t s) {
   const int units = (d / 8 + 31) / 32;   // 16-byte units per lane
-  if (units <= 8)
-    return launch_pdl(gather_rows_f16_kernel<8>, dim3(grid_rows(S)), dim3(256), 0, s, x, row2slot, S, K, d,
-                      xp16, rowmul, hmax);
-  if (units <= 12)
-    return launch_pdl(gather_rows_f16_kernel<12>, dim3(grid_rows(S)), dim3(256), 0, s, x, row2slot, S, K, d,
-                      xp16, rowmul, hmax);
-  if (units <= 16)
-    return launch_pdl(gather_rows_f16_kernel<16>, dim3(grid_rows(S)), dim3(256), 0, s, x, row2slot, S, K, d,
-                      xp16, rowmul, hmax);
-  return launch_pdl(gather_rows_f16_kernel<0>, dim3(grid_rows(S)), dim3(256), 0, s, x, row2slot, S, K, d, xp16,
-                    rowmul, hmax);
+  auto go = [&](auto kernel) {
+    return launch_pdl(kernel, dim3(grid_rows(S)), dim3(256), 0, s, x, row2slot, S, K, d, xp16, rowmul, hmax, rs,
+                      half_rows, order, sched);
+  };
+  if (units <= 8) return go(gather_rows_f16_kernel<8>);
+  if (units <= 12) return go(gather_rows_f16_kernel<12>);
+  if (units <= 16) return go(gather_rows_f16_kernel<16>);
+  return go(gather_rows_f16_kernel<0>);
 }
 
 cudaError_t launch_h_fix_f16(const float* hside, const uint32_t* hmax, int S, int ff, int kh, uint16_t* h16,
