@@ -192,7 +192,7 @@ def launches_per_step(plan, mxfp4, spec_slots, tokens=0, n_experts=0):
         return router + (0 if fused else permute) + 3
     if plan == 3:                                         # 2 GEMMs, combine (MXFP4: 2 scale transposes, gather)
         return router + permute + 3 + (3 if mxfp4 else 0)
-    return router + permute + 7   # 2 scale preps, gather, gate_up, h fix-up, down, combine
+    return router + permute + 6   # scale prep, gather, gate_up, h fix-up, down, combine
 
 
 def work(spec, ids, accumulate=False):

@@ -572,18 +572,34 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
 constexpr int kPrepRows = 128;                     // weight rows per prep CTA (one per thread)
 
-// Per weight row n of one matrix [E * R rows, nb blocks]: c_n from the row's largest
+// One matrix of weight-row scales [rows, nb blocks] and its per-row outputs.
+struct PrepMat {
+  const uint8_t* scales;
+  long long rows;
+  int nb;
+  float* colmul;
+  int32_t* cinfo;
+};
+
+// Per weight row n of each matrix (gate_up, then down): c_n from the row's largest
 // finite scale byte (that block's multiplier becomes 2^13), colmul[n] = 2^c_n, and
 // cinfo[n] = c_n | general << 16, where `general` marks a row with a block whose
 // multiplier is not a normal f16 (scale byte more than 27 below the largest, or 255).
-// One CTA per 128 weight rows, one thread per row, the rows staged in shared memory.
+// One CTA per 128 weight rows (the first blocks0 CTAs take matrix 0), one thread per
+// row, the rows staged in shared memory.
 __global__ void __launch_bounds__(256)
-fp4_prep_kernel(const uint8_t* __restrict__ scales, long long rows, int nb, float* __restrict__ colmul,
-                int32_t* __restrict__ cinfo) {
+fp4_prep_kernel(const PrepMat m0, const PrepMat m1, int blocks0) {
   extern __shared__ uint8_t tile[];               // kPrepRows rows of nb scale bytes
   pdl_wait();
   pdl_trigger();
-  const long long r0 = (long long)blockIdx.x * kPrepRows;
+  const bool second = (int)blockIdx.x >= blocks0;
+  const PrepMat& m = second ? m1 : m0;
+  const uint8_t* __restrict__ scales = m.scales;
+  const long long rows = m.rows;
+  const int nb = m.nb;
+  float* __restrict__ colmul = m.colmul;
+  int32_t* __restrict__ cinfo = m.cinfo;
+  const long long r0 = (long long)(second ? blockIdx.x - blocks0 : blockIdx.x) * kPrepRows;
   const int nrows = (int)min((long long)kPrepRows, rows - r0);
   const int bytes = nrows * nb;
   // The tile's rows are contiguous: copy them with 16-byte loads (r0 * nb is a
@@ -715,12 +731,10 @@ cudaError_t launch_prefill_fp4_prep(const ExpertParams& p, uint8_t* scratch, int
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(fp4_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return cudaErrorInvalidValue;
-  cudaError_t e = launch_pdl(fp4_prep_kernel, dim3((unsigned)((rg + kPrepRows - 1) / kPrepRows)),
-                             dim3(kPrepRows), (size_t)kPrepRows * nbg, s, p.gu_scales, rg, nbg, sc.colmul_gu,
-                             sc.cinfo_gu);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(fp4_prep_kernel, dim3((unsigned)((rd + kPrepRows - 1) / kPrepRows)), dim3(kPrepRows),
-                    (size_t)kPrepRows * nbd, s, p.dn_scales, rd, nbd, sc.colmul_dn, sc.cinfo_dn);
+  const PrepMat gu{p.gu_scales, rg, nbg, sc.colmul_gu, sc.cinfo_gu};
+  const PrepMat dn{p.dn_scales, rd, nbd, sc.colmul_dn, sc.cinfo_dn};
+  const int bg = (int)((rg + kPrepRows - 1) / kPrepRows), bd = (int)((rd + kPrepRows - 1) / kPrepRows);
+  return launch_pdl(fp4_prep_kernel, dim3((unsigned)(bg + bd)), dim3(kPrepRows), (size_t)smem, s, gu, dn, bg);
 }
 
 Fp4Rows prefill_fp4_rows(const ExpertParams& p, uint8_t* scratch, int S) {
