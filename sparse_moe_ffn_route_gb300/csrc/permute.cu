@@ -26,7 +26,7 @@ __global__ void __launch_bounds__(kPermuteThreads)
 permute_one_cta_kernel(RouteState rs, int S, int E1, int tpg) {
   __shared__ PermuteSmem sm;
   pdl_wait();
-  permute_block(rs, S, E1, tpg, sm);
+  permute_block(rs, S, E1, tpg, sm, rs.slot_expert);
   pdl_trigger();
 }
 
@@ -114,7 +114,7 @@ perm_scatter_kernel(RouteState rs, int S, int E1, const int* __restrict__ hist) 
   const int* h = hist + (size_t)blockIdx.x * E1;
   for (int v = tid; v < E1; v += kPermuteThreads) cursor[v] = rs.offsets[v] + h[v];
   const int s0 = blockIdx.x * kSlotsPerCta, s1 = min(S, s0 + kSlotsPerCta);
-  place_slots_stable(rs, s0, s1, S, E1, cursor, tab);   // (its first barrier orders cursor)
+  place_slots_stable(rs, s0, s1, S, E1, cursor, tab, rs.slot_expert);   // (its first barrier orders cursor)
   pdl_trigger();
 }
 

@@ -53,8 +53,9 @@ __device__ __forceinline__ int2 block_exclusive_scan2(int2 val, int2* warp_tot, 
 // earlier warps) + (v's slots before it in its own warp), so every expert's rows hold
 // its slots in increasing slot order, whatever order the warps run in.
 // tab: [E1][32] bytes of shared memory, tab[v][w] = v's slots among warp w's 64.
+// slots: the slots' experts (rs.slot_expert, or a shared-memory copy).
 __device__ __forceinline__ void place_slots_stable(const RouteState& rs, int s0, int s1, int S, int E1,
-                                                   const int* base, uint8_t* tab) {
+                                                   const int* base, uint8_t* tab, const int* slots) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t* tw = reinterpret_cast<uint32_t*>(tab);
   for (int i = tid; i < E1 * 8; i += kPermuteThreads) tw[i] = 0u;
@@ -63,7 +64,7 @@ __device__ __forceinline__ void place_slots_stable(const RouteState& rs, int s0,
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
     const int s = s0 + 64 * warp + 32 * hh + lane;
-    int e = s < s1 ? rs.slot_expert[s] : -1;
+    int e = s < s1 ? slots[s] : -1;
     if (e < 0 || e >= E1) e = -1;
     const uint32_t peers = __match_any_sync(0xffffffffu, e);
     const int rank = __popc(peers & ((1u << lane) - 1u));
@@ -91,19 +92,23 @@ __device__ __forceinline__ void place_slots_stable(const RouteState& rs, int s0,
   }
 }
 
-// Shared memory of permute_block.
-struct PermuteSmem {
-  int cnt[kMaxExperts + 2];
-  int cursor[kMaxExperts + 2];
+// Shared memory of permute_block, for up to MAXE routed experts (plus the shared one).
+template <int MAXE>
+struct PermuteSmemT {
+  int cnt[MAXE + 2];
+  int cursor[MAXE + 2];
   int2 warp_tot[32];
   int2 total;
-  __align__(16) uint8_t tab[(kMaxExperts + 1) * 32];
+  __align__(16) uint8_t tab[(MAXE + 1) * 32];
 };
+using PermuteSmem = PermuteSmemT<kMaxExperts>;
 
 // The whole grouping by one CTA of kPermuteThreads threads, S <= 2048 slots whose
-// slot_expert the block can read (written before a block barrier, or by an earlier
-// kernel).
-__device__ __forceinline__ void permute_block(const RouteState& rs, int S, int E1, int tpg, PermuteSmem& sm) {
+// experts `slots` holds (rs.slot_expert written by an earlier kernel, or a copy in
+// shared memory written before a block barrier).
+template <class Smem>
+__device__ __forceinline__ void permute_block(const RouteState& rs, int S, int E1, int tpg, Smem& sm,
+                                              const int* slots) {
   int* cnt = sm.cnt;
   int* cursor = sm.cursor;
   int2* warp_tot = sm.warp_tot;
@@ -112,7 +117,7 @@ __device__ __forceinline__ void permute_block(const RouteState& rs, int S, int E
   __syncthreads();
 
   for (int s = tid; s < S; s += kPermuteThreads) {
-    const int v = rs.slot_expert[s];
+    const int v = slots[s];
     if (v >= 0 && v < E1)
       atomicAdd(&cnt[v], 1);
     else
@@ -144,7 +149,7 @@ __device__ __forceinline__ void permute_block(const RouteState& rs, int S, int E
   __syncthreads();
 
   // Scatter, stable: every expert's rows take its slots in slot order.
-  place_slots_stable(rs, 0, S, S, E1, cursor, sm.tab);
+  place_slots_stable(rs, 0, S, S, E1, cursor, sm.tab, slots);
 }
 
 }  // namespace moe

@@ -157,8 +157,10 @@ struct SelectArgs {
 };
 
 // DOT: the shared-gate dot x_t . wsh may be asked for (else the gate is column E).
+// sm_slots (shared memory, or null): the slots' experts also go there, for a grouping
+// in the same block.
 template <int EPL, bool DOT>
-__device__ __forceinline__ void select_token(const SelectArgs& a, int t, int lane) {
+__device__ __forceinline__ void select_token(const SelectArgs& a, int t, int lane, int* sm_slots = nullptr) {
   const float* __restrict__ logits = a.logits;
   const int ldl = a.ldl, nsplit = a.nsplit;
   const size_t nstride = a.nstride;
@@ -271,6 +273,7 @@ __device__ __forceinline__ void select_token(const SelectArgs& a, int t, int lan
       slot_expert[(size_t)t * K + lane] = my_id;
       slot_w[(size_t)t * K + lane] = w;
     }
+    if (sm_slots) sm_slots[t * K + lane] = my_id;
   }
   float sl = 0.f;   // the shared-gate logit: column E of the logits, or w_sh . x here
   if (DOT && has_shared && wsh) {
@@ -312,6 +315,7 @@ __device__ __forceinline__ void select_token(const SelectArgs& a, int t, int lan
       slot_expert[(size_t)t * K + k] = E;
       slot_w[(size_t)t * K + k] = sg;
     }
+    if (sm_slots) sm_slots[t * K + k] = E;
   }
 }
 
@@ -328,13 +332,14 @@ __global__ void __launch_bounds__(kSelectWarps * 32) router_select_kernel(const 
 template <int EPL>
 __global__ void __launch_bounds__(kPermuteThreads) select_permute_kernel(const SelectArgs a, RouteState rs,
                                                                          int S, int E1, int tpg) {
-  __shared__ PermuteSmem sm;
+  __shared__ PermuteSmemT<256> sm;               // the fused kernel takes at most 256 experts
+  __shared__ int slots[kPermuteOneCtaSlots];     // the slots' experts, for the grouping
   pdl_wait();
   pdl_trigger();
   for (int t = threadIdx.x >> 5; t < a.T; t += kPermuteThreads / 32)
-    select_token<EPL, false>(a, t, threadIdx.x & 31);
-  __syncthreads();   // the slots are written: the block reads them back
-  permute_block(rs, S, E1, tpg, sm);
+    select_token<EPL, false>(a, t, threadIdx.x & 31, slots);
+  __syncthreads();   // the slots are written: the grouping reads them from shared memory
+  permute_block(rs, S, E1, tpg, sm, slots);
 }
 
 __global__ void ingest_routing_kernel(const int32_t* __restrict__ ids, const float* __restrict__ w,
