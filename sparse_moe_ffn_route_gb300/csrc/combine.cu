@@ -35,27 +35,28 @@ combine_kernel(const float* __restrict__ Y, const float* __restrict__ slot_w,
       acc[0] = bf16_lo(r.x); acc[1] = bf16_hi(r.x); acc[2] = bf16_lo(r.y); acc[3] = bf16_hi(r.y);
       acc[4] = bf16_lo(r.z); acc[5] = bf16_hi(r.z); acc[6] = bf16_lo(r.w); acc[7] = bf16_hi(r.w);
     }
-    // Slots in groups of four: the loads of a group are all in flight together, and
-    // the sums still take the slots in order.  A slot flagged by the permute (expert
-    // out of range) contributes nothing and its Y row is not read.
+    // Slots in groups of four: every load of a group (expert, weight, Y row) is in
+    // flight together, and the sums still take the slots in order.  A slot flagged by
+    // the permute (expert out of range) contributes nothing: its Y row (in bounds, but
+    // never written) is read and dropped by the select, not multiplied by zero.
+#pragma unroll 2
     for (int j0 = 0; j0 < K; j0 += 4) {
-      uint32_t okm = 0;
+      int v[4];
       float w[4];
       float4 a[4], b[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const long s = t * K + j0 + q;
-        const int v = j0 + q < K ? slot_expert[s] : -1;
-        const bool ok = v >= 0 && v < E1;
-        okm |= ok ? 1u << q : 0u;
-        w[q] = ok ? slot_w[s] : 0.f;
+        const bool in = j0 + q < K;
+        const long s = t * K + (in ? j0 + q : 0);
+        v[q] = in ? slot_expert[s] : -1;
+        w[q] = in ? slot_w[s] : 0.f;
         const float4* src = reinterpret_cast<const float4*>(Y + (size_t)s * d + o);
-        a[q] = ok ? src[0] : make_float4(0.f, 0.f, 0.f, 0.f);
-        b[q] = ok ? src[1] : make_float4(0.f, 0.f, 0.f, 0.f);
+        a[q] = src[0];
+        b[q] = src[1];
       }
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        if (okm & (1u << q)) {
+        if (v[q] >= 0 && v[q] < E1) {
           acc[0] += w[q] * a[q].x; acc[1] += w[q] * a[q].y; acc[2] += w[q] * a[q].z; acc[3] += w[q] * a[q].w;
           acc[4] += w[q] * b[q].x; acc[5] += w[q] * b[q].y; acc[6] += w[q] * b[q].z; acc[7] += w[q] * b[q].w;
         }
