@@ -122,6 +122,19 @@ __device__ __forceinline__ void fp4_group_mma(const uint4 (&W)[4], const Fp4Scal
   }
 }
 
+// The first kDepthBf16 k steps of a bf16 weight ring: the loads a kernel issues
+// before its token rows are staged, so that the weight stream does not wait on them.
+__device__ __forceinline__ void prime_bf16(const uint8_t* const (&R)[4], int Kin, int c,
+                                           uint4 (&W)[kDepthBf16][4]) {
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  const int nk = Kin >> 5;
+#pragma unroll
+  for (int s = 0; s < kDepthBf16; ++s)
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+      W[s][r] = s < nk ? ldg_stream_v4(R[r] + (size_t)(s * 32 + 8 * c) * 2) : z;
+}
+
 // The streaming core shared by both kernels: acc[i][ch] += tile i (rows R[2i] /
 // R[2i+1] as MMA rows g / g+8) times token chunk ch, over Kin inputs.
 // R: byte pointers to the lane's 4 weight rows; Sc: their MXFP4 scale rows;
@@ -129,21 +142,17 @@ __device__ __forceinline__ void fp4_group_mma(const uint4 (&W)[4], const Fp4Scal
 // LO: the token operand is an (hi, lo) bf16 pair whose lo half sits lo_off bytes
 // after the hi half in each row; both halves are multiplied by the same weights.
 // SB: the token rows were staged in shared memory (br are generic pointers to it).
+// W: bf16 weights, the ring as prime_bf16 left it (unused for MXFP4).
 template <int WFMT, int CH, bool LO, bool SB>
 __device__ __forceinline__ void stream_rows(const uint8_t* const (&R)[4],
                                             const uint8_t* const (&Sc)[4], int Kin, int c,
                                             const uint8_t* const (&br)[CH], int nch,
-                                            float (&acc)[2][CH][4], size_t lo_off) {
+                                            float (&acc)[2][CH][4], size_t lo_off,
+                                            uint4 (&W)[kDepthBf16][4]) {
   const uint4 z = make_uint4(0, 0, 0, 0);
   if (WFMT == MOE_WFMT_BF16) {
     constexpr int P = kDepthBf16;
     const int nk = Kin >> 5;
-    uint4 W[P][4];
-#pragma unroll
-    for (int s = 0; s < P; ++s)
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-        W[s][r] = s < nk ? ldg_stream_v4(R[r] + (size_t)(s * 32 + 8 * c) * 2) : z;
     for (int k0 = 0; k0 < nk; k0 += P) {
 #pragma unroll
       for (int s = 0; s < P; ++s) {
@@ -514,12 +523,15 @@ gateup_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__
     }
   }
   const int act = shared ? MOE_ACT_SWIGLU : p.act;
+  uint4 W[kDepthBf16][4];
+  if (WFMT == MOE_WFMT_BF16) prime_bf16(R, d, c, W);
 
   // MXFP4 with staged rows: f16 token operand (see "MXFP4 x f16 tokens")
   constexpr bool H16 = WFMT == MOE_WFMT_MXFP4 && STAGE;
   extern __shared__ __align__(16) uint8_t stage[];
   __shared__ int esc[8];                           // H16: token exponents
   for (int p0 = item.y; p0 < cnt; p0 += 8 * CH) {
+    if (WFMT == MOE_WFMT_BF16 && p0 != item.y) prime_bf16(R, d, c, W);
     const int nch = min(CH, (cnt - p0 + 7) / 8);
     const uint8_t* br[CH];
     if (STAGE) {
@@ -552,7 +564,7 @@ gateup_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__
     if constexpr (H16)
       stream_rows_fp4h(R, Sc, d, c, br[0], acc);
     else
-      stream_rows<WFMT, CH, false, STAGE>(R, Sc, d, c, br, nch, acc, 0);
+      stream_rows<WFMT, CH, false, STAGE>(R, Sc, d, c, br, nch, acc, 0, W);
     pdl_trigger();
 
     // Epilogue: bias, activation, bf16 h rows (permuted order).
@@ -590,7 +602,6 @@ template <int WFMT, int CH, bool STAGE>
 __global__ void __launch_bounds__(kWarps * 32, 3)
 down_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__ h, int ldh,
                    float* __restrict__ Y) {
-  pdl_wait();
   const int a = blockIdx.y;
   if (a >= *rs.n_work) return;
   const int2 item = rs.work[a];                    // (virtual expert, first row within it)
@@ -628,10 +639,17 @@ down_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__ h
     if (!shared && p.dn_bias) bias[r] = bf16_to_f32(p.dn_bias[(size_t)v * d + o]);
   }
 
+  uint4 W[kDepthBf16][4];
+  if (WFMT == MOE_WFMT_BF16) prime_bf16(R, Kin, c, W);
+  // The weights and the work list (written by the grouping kernel, which every CTA
+  // of the preceding gate_up launch waited for) do not depend on gate_up: only h does.
+  pdl_wait();
+
   constexpr bool H16 = WFMT == MOE_WFMT_MXFP4 && STAGE;
   extern __shared__ __align__(16) uint8_t stage[];
   __shared__ int esc[8];                           // H16: token exponents
   for (int p0 = item.y; p0 < cnt; p0 += 8 * CH) {
+    if (WFMT == MOE_WFMT_BF16 && p0 != item.y) prime_bf16(R, Kin, c, W);
     const int nch = min(CH, (cnt - p0 + 7) / 8);
     const uint8_t* br[CH];
     size_t lo_off = (size_t)ldh * 2;
@@ -672,7 +690,7 @@ down_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__ h
     if constexpr (H16)
       stream_rows_fp4h(R, Sc, Kin, c, br[0], acc);
     else
-      stream_rows<WFMT, CH, true, STAGE>(R, Sc, Kin, c, br, nch, acc, lo_off);
+      stream_rows<WFMT, CH, true, STAGE>(R, Sc, Kin, c, br, nch, acc, lo_off, W);
     pdl_trigger();
 
 #pragma unroll
