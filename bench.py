@@ -186,10 +186,10 @@ def launches_per_step(plan, mxfp4, spec_slots, tokens=0, n_experts=0):
     """Kernels of this library one moe_ffn_forward enqueues, by kernel plan."""
     router = 2                                            # logits, select
     permute = 3 if spec_slots > 2048 else 1               # count, scan, scatter (or one CTA)
-    if plan in (1, 2):                                    # decode: gate_up, down, combine
+    if plan in (1, 2, 5):                                 # decode: gate_up, down (5: one launch), combine
         # up to 32 tokens, 256 experts, 2048 slots: the select kernel also permutes
         fused = tokens <= 32 and n_experts <= 256 and spec_slots <= 2048
-        return router + (0 if fused else permute) + 3
+        return router + (0 if fused else permute) + (2 if plan == 5 else 3)
     if plan == 3:                                         # 2 GEMMs, combine (MXFP4: 2 scale transposes, gather)
         return router + permute + 3 + (3 if mxfp4 else 0)
     return router + permute + 6   # scale prep, gather, gate_up, h fix-up, down, combine
@@ -528,15 +528,25 @@ def measure(spec, lay, dev_layer, args, rank, world, local_rank, dev, flush, sin
     if rank != 0:
         return None
     hbm, tf, tf_sus, src = peaks()
-    kernels = {p: kernel_roofline(p, by[p], fl.get(p, 0), phase_ms[p], hbm, tf) for p in ("gate_up", "down")}
-    dom = max(("gate_up", "down"), key=lambda p: phase_ms[p])
+    step_bytes = sum(by.values())
+    if plan == moe.PLAN_DECODE_FUSED:
+        # gate_up and down are one kernel: the phase between their marks holds all of it
+        # (the next mark follows it at once); its algorithmic bytes are both projections'
+        GD = "gate_up+down"
+        phase_ms = {(GD if p == "gate_up" else p): t for p, t in phase_ms.items() if p != "down"}
+        by[GD], fl[GD], per_unit[GD] = by["gate_up"] + by["down"], fl["gate_up"] + fl["down"], \
+            per_unit["gate_up"] + per_unit["down"]
+        expert_phases = (GD,)
+    else:
+        expert_phases = ("gate_up", "down")
+    kernels = {p: kernel_roofline(p, by[p], fl.get(p, 0), phase_ms[p], hbm, tf) for p in expert_phases}
+    dom = max(expert_phases, key=lambda p: phase_ms[p])
     roof = dict(kernels[dom])
     roof.update({"peak_source": src + (" (bf16 burst, L2 flushed between steps)" if roof["bound"] == "tensor"
                                        else " (HBM copy)"),
                  "traffic": ncu_traffic(spec.name, dom),
                  "per_unit_bytes": per_unit[dom], "units_per_launch": distinct,
                  "path": moe.PLAN_NAMES[plan]})
-    step_bytes = sum(by.values())
     cpu = None
     if cpu_seconds > 0:
         tok = np.arange(n_sample, dtype=np.int32)

@@ -178,9 +178,14 @@ enum {
                                    128 rows) */
   MOE_PLAN_PREFILL_BF16 = 3,    /* tcgen05 grouped GEMMs with bf16 operands (bf16 weights,
                                    or MXFP4 decoded to bf16 in shared memory) */
-  MOE_PLAN_PREFILL_F16 = 4      /* tcgen05 grouped GEMMs with f16 operands: MXFP4 with the
+  MOE_PLAN_PREFILL_F16 = 4,     /* tcgen05 grouped GEMMs with f16 operands: MXFP4 with the
                                    clamped GLU, each decoded weight tile shared by two
                                    128-row tiles */
+  MOE_PLAN_DECODE_FUSED = 5     /* MOE_PLAN_DECODE_WARP's kernels as one launch (bf16
+                                   weights, items of at most 8 tokens, at most 2048 slots
+                                   when not on the ring): each CTA takes a ticket, gate_up
+                                   units first, and a down unit waits for its item's
+                                   gate_up units through a counter */
 };
 /* Returns one of MOE_PLAN_* (a host-side decision from cfg and T alone; no device
  * work), or a negative MOE_ERR_* if cfg is invalid or T < 0. */
@@ -356,6 +361,12 @@ int moe_set_phase_events(void* const* events, int32_t n_events);
  * current device, to calls enqueued after it returns; synchronises the device.
  * Restore with moe_test_set_wait_limit(1u << 20, 0).  max_polls > 0. */
 int moe_test_set_wait_limit(uint32_t max_polls, int32_t withhold_first_load);
+
+/* Test hook: enable (1, the default) or disable (0) MOE_PLAN_DECODE_FUSED, so that
+ * the two-launch form of the same kernels can be checked against it.  Host-side only
+ * (no device work); applies to calls made after it returns, from any thread.
+ * MOE_ERR_INVALID_ARG for other values. */
+int moe_test_set_decode_fusion(int32_t enable);
 
 /* Synchronises `stream`, then returns MOE_OK, MOE_ERR_DEVICE_CHECK or
  * MOE_ERR_TIMEOUT according to the device status word kept in `ws`, and clears

@@ -121,6 +121,8 @@ def _load():
     lib.moe_set_phase_events.restype = I
     lib.moe_test_set_wait_limit.argtypes = [ctypes.c_uint32, ctypes.c_int32]
     lib.moe_test_set_wait_limit.restype = I
+    lib.moe_test_set_decode_fusion.argtypes = [ctypes.c_int32]
+    lib.moe_test_set_decode_fusion.restype = I
     lib.moe_device_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
     lib.moe_device_status.restype = I
     lib.moe_status_string.argtypes = [I]
@@ -132,7 +134,8 @@ _lib = _load()
 EXPORTED = ("moe_workspace_bytes", "moe_select_path", "moe_kernel_plan", "moe_route", "moe_topk_from_logits",
             "moe_group_by_expert", "moe_ffn_forward", "moe_ffn_forward_routed", "moe_ffn_forward_host",
             "moe_ffn_forward_noalloc", "moe_noalloc_workspace_bytes", "moe_noalloc_device_status",
-            "moe_mxfp4_to_bf16", "moe_set_phase_events", "moe_test_set_wait_limit", "moe_device_status",
+            "moe_mxfp4_to_bf16", "moe_set_phase_events", "moe_test_set_wait_limit", "moe_test_set_decode_fusion",
+            "moe_device_status",
             "moe_status_string")
 PHASES = ("router_logits", "router_select", "permute", "gate_up", "down", "combine")
 
@@ -235,11 +238,12 @@ def moe_select_path(cfg: MoeCfg, T: int) -> int:
     return st
 
 
-PLAN_DECODE_WARP, PLAN_DECODE_RING, PLAN_PREFILL_BF16, PLAN_PREFILL_F16 = 1, 2, 3, 4
+PLAN_DECODE_WARP, PLAN_DECODE_RING, PLAN_PREFILL_BF16, PLAN_PREFILL_F16, PLAN_DECODE_FUSED = 1, 2, 3, 4, 5
 PLAN_NAMES = {1: "decode: warp MMAs, register-held weight loads",
               2: "decode: warp MMAs, TMA-fed weight ring",
               3: "prefill: tcgen05 grouped GEMMs, bf16 operands",
-              4: "prefill: tcgen05 grouped GEMMs, f16 operands (MXFP4, two m tiles per weight tile)"}
+              4: "prefill: tcgen05 grouped GEMMs, f16 operands (MXFP4, two m tiles per weight tile)",
+              5: "decode: warp MMAs, register-held weight loads, gate_up and down in one launch"}
 
 
 def moe_kernel_plan(cfg: MoeCfg, T: int) -> int:
@@ -441,6 +445,12 @@ def moe_test_set_wait_limit(max_polls: int = DEFAULT_WAIT_POLLS, withhold_first_
     """Test hook: the poll limit of the bounded device waits, and whether CTA 0's producer
     of the TMA-fed kernels skips its first load (see include/moe.h).  Synchronises."""
     _check(_lib.moe_test_set_wait_limit(max_polls, int(withhold_first_load)), "moe_test_set_wait_limit")
+
+
+def moe_test_set_decode_fusion(enable: bool) -> None:
+    """Test hook: whether bf16 decode with one-chunk items runs gate_up and down as one
+    launch (the default) or as two (see include/moe.h).  Host-side only."""
+    _check(_lib.moe_test_set_decode_fusion(int(bool(enable))), "moe_test_set_decode_fusion")
 
 
 def moe_device_status(ws: torch.Tensor, stream=None):

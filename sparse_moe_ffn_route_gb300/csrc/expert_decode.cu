@@ -56,15 +56,51 @@ __device__ __forceinline__ uint4 ld_b16(const uint8_t* p) {
   return ldg_nc_v4(p);
 }
 
+// 16 bytes from global memory through L2 only: data that other CTAs of the same
+// launch wrote (the read-only path may not see them).
+__device__ __forceinline__ uint4 ldg_cg_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
 // Copy `n` token rows of `rb` bytes (rows[i], global) into shared memory `dst`
-// (row i at i * rb), all threads of the CTA, then synchronise.
+// (row i at i * rb), all threads of the CTA, then synchronise.  CG: the rows were
+// written during this launch.
+template <bool CG = false>
 __device__ __forceinline__ void stage_rows(uint8_t* dst, const uint8_t* const* rows, int n, int rb) {
   const int per = rb >> 4;
   for (int i = threadIdx.x; i < n * per; i += blockDim.x) {
     const int r = i / per, c = i - r * per;
-    reinterpret_cast<uint4*>(dst + r * rb)[c] = ldg_nc_v4(rows[r] + 16 * c);
+    reinterpret_cast<uint4*>(dst + r * rb)[c] = CG ? ldg_cg_v4(rows[r] + 16 * c) : ldg_nc_v4(rows[r] + 16 * c);
   }
   __syncthreads();
+}
+
+// Bounded wait of a CTA until the counter *ctr reaches `need` (thread 0 polls with
+// acquire loads; the block barrier passes the ordering on to every thread).  False,
+// with STATUS_TIMEOUT set, if it gave up.
+constexpr uint32_t kCountPolls = 1u << 22;
+__device__ __forceinline__ bool wait_count(const int32_t* ctr, int need, uint32_t* status) {
+  __shared__ int ok_s;
+  if (threadIdx.x == 0) {
+    int ok = 0;
+    for (uint32_t i = 0; i < kCountPolls; ++i) {
+      int v;
+      asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+      if (v >= need) {
+        ok = 1;
+        break;
+      }
+      if (i > 64) __nanosleep(64);
+    }
+    if (!ok) flag_status(status, STATUS_TIMEOUT);
+    ok_s = ok;
+  }
+  __syncthreads();
+  return ok_s != 0;
 }
 
 // bf16 pair of the block's inputs (4j, 4j+1) [B = 0] or (4j+2, 4j+3) [B = 1].
@@ -466,13 +502,11 @@ __device__ __forceinline__ void zero_acc(float (&acc)[2][CH][4]) {
 // rows and rows 8..15 their up rows, so the accumulator of lane (g, c) holds gate
 // (d0, d1) and up (d2, d3) of feature f for tokens 2c and 2c+1.
 // STAGE: a one-chunk item (CH == 1) copies its token rows to shared memory first.
+// One CTA's unit: work item a (below *rs.n_work), feature tile bx.
 template <int WFMT, int CH, bool STAGE>
-__global__ void __launch_bounds__(kWarps * 32, 3)
-gateup_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__ x, int K,
-                     uint16_t* __restrict__ h, int ldh, int interleaved) {
-  pdl_wait();
-  const int a = blockIdx.y;
-  if (a >= *rs.n_work) return;
+__device__ __forceinline__ void gateup_unit(const ExpertParams& p, const RouteState& rs,
+                                            const uint16_t* __restrict__ x, int K, uint16_t* __restrict__ h,
+                                            int ldh, int interleaved, int a, int bx) {
   const int2 item = rs.work[a];                    // (virtual expert, first row within it)
   const int v = item.x;
   const bool shared = (v == p.E);
@@ -480,7 +514,7 @@ gateup_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__
   const int ffv = shared ? p.sff : p.ff;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, c = lane & 3;
-  const int f0 = blockIdx.x * kGateUpFeatures + warp * 16;
+  const int f0 = bx * kGateUpFeatures + warp * 16;
   // ff % 32 == 0: a warp's 16 features are all valid or all past the end; a warp
   // past the end still takes part in the row staging and its barriers.
   const bool warp_on = f0 < ffv;
@@ -593,17 +627,31 @@ gateup_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__
   }
 }
 
+template <int WFMT, int CH, bool STAGE>
+__global__ void __launch_bounds__(kWarps * 32, 3)
+gateup_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__ x, int K,
+                     uint16_t* __restrict__ h, int ldh, int interleaved) {
+  pdl_wait();
+  const int a = blockIdx.y;
+  if (a >= *rs.n_work) return;
+  gateup_unit<WFMT, CH, STAGE>(p, rs, x, K, h, ldh, interleaved, a, blockIdx.x);
+}
+
 // ---------------------------------------------------------------- down
 //
 // Tile i of a warp covers output rows o0 + 16i + {g, g+8}; the accumulator of
 // lane (g, c) holds rows (o, o+8) for tokens 2c, 2c+1.  Results (plus the down
 // bias) go to the token's slot row of Y.
-template <int WFMT, int CH, bool STAGE>
-__global__ void __launch_bounds__(kWarps * 32, 3)
-down_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__ h, int ldh,
-                   float* __restrict__ Y) {
-  const int a = blockIdx.y;
-  if (a >= *rs.n_work) return;
+// One CTA's unit: work item a (below *rs.n_work), output row tile bx.  The unit
+// issues its first weight loads, then waits for its h rows: FUSED, until *ready
+// reaches `need` (the fused launch, whose gate_up units count each finished item);
+// otherwise for the preceding gate_up launch.
+template <int WFMT, int CH, bool STAGE, bool FUSED>
+__device__ __forceinline__ void down_unit(const ExpertParams& p, const RouteState& rs,
+                                          const uint16_t* __restrict__ h, int ldh, float* __restrict__ Y,
+                                          int a, int bx, const int32_t* ready, int need) {
+  static_assert(!FUSED || (WFMT == MOE_WFMT_BF16 && CH == 1 && STAGE),
+                "the fused launch reads h only through the coherent staging copy");
   const int2 item = rs.work[a];                    // (virtual expert, first row within it)
   const int v = item.x;
   const bool shared = (v == p.E);
@@ -612,7 +660,7 @@ down_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__ h
   const int d = p.d;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, c = lane & 3;
-  const int o0raw = blockIdx.x * kDownRows + warp * 32;
+  const int o0raw = bx * kDownRows + warp * 32;
   // d % 32 == 0: both 16-row tiles of a warp are valid or both past the end; a warp
   // past the end still takes part in the row staging and its barriers.
   const bool warp_on = o0raw < d;
@@ -643,7 +691,11 @@ down_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__ h
   if (WFMT == MOE_WFMT_BF16) prime_bf16(R, Kin, c, W);
   // The weights and the work list (written by the grouping kernel, which every CTA
   // of the preceding gate_up launch waited for) do not depend on gate_up: only h does.
-  pdl_wait();
+  if (FUSED) {
+    if (!wait_count(ready, need, rs.status)) return;
+  } else {
+    pdl_wait();
+  }
 
   constexpr bool H16 = WFMT == MOE_WFMT_MXFP4 && STAGE;
   extern __shared__ __align__(16) uint8_t stage[];
@@ -673,7 +725,7 @@ down_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__ h
                             (threadIdx.x & 1) * lo_off;
       }
       __syncthreads();
-      stage_rows(stage, rows, 2 * n, Kin * 2);
+      stage_rows<FUSED>(stage, rows, 2 * n, Kin * 2);
       br[0] = g < n ? stage + 2 * g * Kin * 2 : nullptr;
       lo_off = (size_t)Kin * 2;
     } else {
@@ -713,6 +765,47 @@ down_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__ h
   }
 }
 
+template <int WFMT, int CH, bool STAGE>
+__global__ void __launch_bounds__(kWarps * 32, 3)
+down_decode_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__ h, int ldh,
+                   float* __restrict__ Y) {
+  const int a = blockIdx.y;
+  if (a >= *rs.n_work) return;
+  down_unit<WFMT, CH, STAGE, false>(p, rs, h, ldh, Y, a, blockIdx.x, nullptr, 0);
+}
+
+// ---------------------------------------------------------------- gate_up + down, one launch
+//
+// One-chunk bf16 items: every CTA takes a ticket (rs.fuse[0]); tickets below
+// n_work * gu_tiles are gate_up units in item order, the next n_work * dn_tiles are
+// down units in item order, the rest exit.  A gate_up unit, once its h stores are
+// fenced, adds one to its item's count (rs.fuse[1 + a]); a down unit streams its first
+// weights and then waits until that count reaches gu_tiles.  Every ticket of a
+// gate_up unit was taken, by a CTA already running, before the first down ticket,
+// so the waits end whatever order the CTAs are scheduled in; the down units of the
+// first items fill the SMs that the last gate_up units leave idle.
+__global__ void __launch_bounds__(kWarps * 32, 3)
+experts_decode_fused_kernel(ExpertParams p, RouteState rs, const uint16_t* __restrict__ x, int K,
+                            uint16_t* __restrict__ h, int ldh, float* __restrict__ Y, int interleaved,
+                            int gu_tiles, int dn_tiles) {
+  pdl_wait();
+  __shared__ int ticket_s;
+  if (threadIdx.x == 0) ticket_s = atomicAdd(rs.fuse, 1);
+  __syncthreads();
+  const int t = ticket_s, nw = *rs.n_work;
+  const int ngu = nw * gu_tiles;
+  if (t < ngu) {
+    const int a = t / gu_tiles;
+    gateup_unit<MOE_WFMT_BF16, 1, true>(p, rs, x, K, h, ldh, interleaved, a, t - a * gu_tiles);
+    __threadfence();            // this thread's h stores, before the item's count
+    __syncthreads();
+    if (threadIdx.x == 0) atomicAdd(rs.fuse + 1 + a, 1);
+  } else if (t < ngu + nw * dn_tiles) {
+    const int u = t - ngu, a = u / dn_tiles;
+    down_unit<MOE_WFMT_BF16, 1, true, true>(p, rs, h, ldh, Y, a, u - a * dn_tiles, rs.fuse + 1 + a, gu_tiles);
+  }
+}
+
 }  // namespace
 
 // Dynamic shared memory of a one-chunk item: its token rows (gate_up: x rows of
@@ -749,6 +842,34 @@ cudaError_t launch_gateup_decode(const ExpertParams& p, int wfmt, int interleave
     else MOE_GU(MOE_WFMT_MXFP4, kMaxChunks, false, 0);
   }
 #undef MOE_GU
+  return cudaGetLastError();
+}
+
+// Shared memory of the fused launch: the larger staged block, x (8 rows of d bf16)
+// for gate_up or h (8 (hi, lo) pairs of the wider FF) for down; 0 if over the limit.
+static size_t fused_stage_bytes(int d, int ff, int sff) {
+  const int fmax = ff > sff ? ff : sff;
+  const size_t smx = (size_t)8 * d * 2, smh = (size_t)16 * fmax * 2;
+  const size_t sm = smx > smh ? smx : smh;
+  return sm <= kMaxStage ? sm : 0;
+}
+
+bool decode_fused_fits(int d, int ff, int sff) { return fused_stage_bytes(d, ff, sff) != 0; }
+
+cudaError_t launch_experts_decode_fused(const ExpertParams& p, const RouteState& rs, const uint16_t* x, int K,
+                                       uint16_t* h, int ldh, float* Y, int max_items, int interleaved,
+                                       cudaStream_t s, bool* launched) {
+  *launched = false;
+  const int fmax = p.ff > p.sff ? p.ff : p.sff;
+  const size_t sm = fused_stage_bytes(p.d, p.ff, p.sff);
+  if (!rs.fuse || rs.fuse_n < 1 + max_items || sm == 0) return cudaSuccess;
+  const int gu = (fmax + kGateUpFeatures - 1) / kGateUpFeatures, dn = (p.d + kDownRows - 1) / kDownRows;
+  cudaError_t e = set_smem(experts_decode_fused_kernel, sm);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(experts_decode_fused_kernel, dim3((unsigned)((gu + dn) * max_items)), dim3(kWarps * 32), sm, s, p,
+                 rs, x, K, h, ldh, Y, interleaved, gu, dn);
+  if (e != cudaSuccess) return e;
+  *launched = true;
   return cudaGetLastError();
 }
 

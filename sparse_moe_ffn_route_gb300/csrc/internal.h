@@ -74,6 +74,11 @@ struct RouteState {
   int32_t* n_work;       // [1]
   int32_t* row2slot;     // [S]       permuted row -> slot
   uint32_t* status;      // device status word
+  // [fuse_n] counters of the fused decode launch (a ticket counter, then one count of
+  // finished gate_up units per work item); the one-CTA grouping zeroes them.  Null
+  // where the layout has none.
+  int32_t* fuse = nullptr;
+  int fuse_n = 0;
 };
 
 // ---------------------------------------------------------------- host helpers
@@ -146,6 +151,14 @@ cudaError_t launch_gateup_decode(const ExpertParams& p, int wfmt, int interleave
 cudaError_t launch_down_decode(const ExpertParams& p, int wfmt, const RouteState& rs,
                                const uint16_t* h, int ldh, float* Y, int max_items, int chunks,
                                cudaStream_t s);
+// Both of the above in one launch, for bf16 weights and one-chunk items whose token
+// rows fit the staging copy, when rs carries the fused counters (zeroed by the one-CTA
+// grouping that precedes it); *launched comes back false (nothing enqueued) otherwise.
+cudaError_t launch_experts_decode_fused(const ExpertParams& p, const RouteState& rs, const uint16_t* x, int K,
+                                       uint16_t* h, int ldh, float* Y, int max_items, int interleaved,
+                                       cudaStream_t s, bool* launched);
+// Whether the fused launch's staged rows fit for these sizes (host).
+bool decode_fused_fits(int d, int ff, int sff);
 
 // Decode path, bf16 weights in the separate gate / up layout (d, ff, sff multiples
 // of 64), one-chunk items (at most 8 token rows): the weights stream through a

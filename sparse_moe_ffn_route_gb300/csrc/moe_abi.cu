@@ -23,7 +23,8 @@ struct Layout {
   bool prefill_fp4;         // ... in their f16-operand MXFP4 form (expert_prefill_fp4.cu)
   bool accumulate;          // prefill, not deterministic: down adds w * Y into yacc with atomics
   size_t status, counts, offsets, work, n_work, slot_expert, slot_w, row2slot, hist, logits, h, Y, xn,
-      xp, scalesT, xstage, ystage, yacc, total;
+      xp, scalesT, xstage, ystage, yacc, fuse, total;
+  int fuse_n;               // decode: counters of the fused expert launch (ticket + one per work item)
 };
 
 int path_for(const moe_cfg_t* c, int T);
@@ -99,6 +100,9 @@ bool make_layout(const moe_cfg_t* c, int T, Layout* L) {
                                        : prefill_scales_bytes(sp, c->wfmt));
   }
   L->accumulate = L->prefill && !c->deterministic;
+  // a ticket counter and one count per one-chunk work item (at most E1 + S / 8 items)
+  L->fuse_n = L->prefill ? 0 : 1 + L->E1 + (int)((S + 7) / 8);
+  L->fuse = take(4 * (size_t)L->fuse_n);
   L->yacc = take(L->accumulate ? 4 * Tz * d : 0);   // per-token fp32 sums of the weighted expert outputs
   L->xn = take(c->rms_norm ? 2 * Tz * d : 0);   // RMSNorm(x), the MoE's input
   L->xstage = take(2 * Tz * d);
@@ -122,6 +126,8 @@ RouteState route_state(void* ws, const Layout& L) {
   rs.n_work = at<int32_t>(ws, L.n_work);
   rs.row2slot = at<int32_t>(ws, L.row2slot);
   rs.status = at<uint32_t>(ws, L.status);
+  rs.fuse = L.fuse_n ? at<int32_t>(ws, L.fuse) : nullptr;
+  rs.fuse_n = L.fuse_n;
   return rs;
 }
 
@@ -230,6 +236,17 @@ bool decode_ring(const moe_cfg_t* c, int T) {
   return c->wfmt == MOE_WFMT_BF16 && !c->interleaved_gate_up && c->d_model % 64 == 0 &&
          c->expert_ff % 64 == 0 && c->shared_ff % 64 == 0 &&
          (long long)expect_items(c, T) * ((c->d_model + 127) / 128) < kRingUnits;
+}
+
+// Decode, bf16 weights, one-chunk items on the register-stream kernels (not the
+// ring): gate_up and down run as one launch when the one-CTA grouping, which zeroes
+// the launch's counters, precedes it and the staged rows fit.  The two-launch form
+// stays for moe_test_set_decode_fusion(0).
+bool g_decode_fusion = true;
+bool decode_fused(const moe_cfg_t* c, const Layout& L, int T) {
+  return g_decode_fusion && !L.prefill && c->wfmt == MOE_WFMT_BF16 && decode_chunks(c, T) == 1 &&
+         !decode_ring(c, T) && L.S <= kPermuteOneCtaSlots &&
+         decode_fused_fits(c->d_model, c->expert_ff, c->shared_ff);
 }
 
 // Caller-owned events recorded at phase boundaries (moe_set_phase_events).
@@ -404,15 +421,21 @@ int run_experts(const moe_cfg_t* c, const void* x_layer, int T, const moe_expert
   else if (ring)
     MOE_CUDA(launch_gateup_decode_ring(p, rs, static_cast<const uint16_t*>(x), L.K, h, L.ldh, max_items,
                                        items, s, &done));
-  if (!done)
+  // bf16 one-chunk items on the register-stream kernels: gate_up and down in one
+  // launch (the grouping that zeroes its counters is the one-CTA routine here).
+  bool fused = false;
+  if (!done && !ring && decode_fused(c, L, T))
+    MOE_CUDA(launch_experts_decode_fused(p, rs, static_cast<const uint16_t*>(x), L.K, h, L.ldh, Y, max_items,
+                                         c->interleaved_gate_up, s, &fused));
+  if (!done && !fused)
     MOE_CUDA(launch_gateup_decode(p, c->wfmt, c->interleaved_gate_up, rs,
                                   static_cast<const uint16_t*>(x), L.K, h, L.ldh, max_items, chunks,
                                   s));
   MOE_CUDA(mark_phase(4, s));
-  done = false;
-  if (ring && fp4)
+  done = fused;
+  if (!fused && ring && fp4)
     MOE_CUDA(launch_down_decode_fp4(p, rs, h, L.ldh, Y, max_items, s, &done));
-  else if (ring)
+  else if (!fused && ring)
     MOE_CUDA(launch_down_decode_ring(p, rs, h, L.ldh, Y, max_items, items, s, &done));
   if (!done) MOE_CUDA(launch_down_decode(p, c->wfmt, rs, h, L.ldh, Y, max_items, chunks, s));
   MOE_CUDA(mark_phase(5, s));
@@ -448,6 +471,7 @@ int moe_kernel_plan(const moe_cfg_t* cfg, int32_t T) {
   if (!make_layout(cfg, T, &L)) return MOE_ERR_UNSUPPORTED;
   if (L.prefill_fp4) return MOE_PLAN_PREFILL_F16;
   if (L.prefill) return MOE_PLAN_PREFILL_BF16;
+  if (decode_fused(cfg, L, T)) return MOE_PLAN_DECODE_FUSED;
   return decode_chunks(cfg, T) == 1 && decode_ring(cfg, T) ? MOE_PLAN_DECODE_RING : MOE_PLAN_DECODE_WARP;
 }
 
@@ -760,6 +784,12 @@ int moe_test_set_wait_limit(uint32_t max_polls, int32_t withhold_first_load) {
   MOE_CUDA(prefill_fp4_set_wait_test(max_polls, w));
   MOE_CUDA(ring_set_wait_test(max_polls, w));
   MOE_CUDA(fp4_stream_set_wait_test(max_polls, w));
+  return MOE_OK;
+}
+
+int moe_test_set_decode_fusion(int32_t enable) {
+  if (enable < 0 || enable > 1) return MOE_ERR_INVALID_ARG;
+  g_decode_fusion = enable != 0;
   return MOE_OK;
 }
 

@@ -114,6 +114,8 @@ __device__ __forceinline__ void permute_block(const RouteState& rs, int S, int E
   int2* warp_tot = sm.warp_tot;
   const int tid = threadIdx.x;
   for (int v = tid; v < E1; v += kPermuteThreads) cnt[v] = 0;
+  if (rs.fuse)
+    for (int i = tid; i < rs.fuse_n; i += kPermuteThreads) rs.fuse[i] = 0;
   __syncthreads();
 
   for (int s = tid; s < S; s += kPermuteThreads) {

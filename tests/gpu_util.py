@@ -41,7 +41,8 @@ def is_exact(cfg, T):
     another order and change the last bits of the fp32 sums."""
     moe = moe_lib()
     return bool(cfg.deterministic) or moe.moe_kernel_plan(cfg, T) in (moe.PLAN_DECODE_WARP,
-                                                                       moe.PLAN_DECODE_RING)
+                                                                       moe.PLAN_DECODE_RING,
+                                                                       moe.PLAN_DECODE_FUSED)
 
 
 def bf16_ulps(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:

@@ -49,7 +49,7 @@ def test_kernel_plan_per_workload():
     import moe_inputs as mi
     want = {
         "qwen35_mini_moe_decode_t8": moe.PLAN_DECODE_RING,
-        "qwen35_mini_moe_decode_t64": moe.PLAN_DECODE_WARP,
+        "qwen35_mini_moe_decode_t64": moe.PLAN_DECODE_FUSED,
         "qwen35_mini_moe_prefill_t4096": moe.PLAN_PREFILL_BF16,
         "gptoss_20b_moe_decode_t32": moe.PLAN_DECODE_RING,
         "gptoss_20b_moe_prefill_t8192": moe.PLAN_PREFILL_F16,
@@ -76,14 +76,23 @@ def test_kernel_plan_forms():
     q = moe.qwen_cfg(d_model=96, n_experts=8, top_k=2, expert_ff=32, shared_ff=0)
     assert moe.moe_kernel_plan(q, 4096) == moe.PLAN_DECODE_WARP
     # bf16 decode: the ring takes the separate gate / up layout with d, ff, sff
-    # multiples of 64; otherwise (or when asked) the register-stream kernels
-    assert moe.moe_kernel_plan(q, 4) == moe.PLAN_DECODE_WARP                       # d = 96
+    # multiples of 64; otherwise (or when asked) the register-stream kernels, which
+    # bf16 one-chunk items run as one launch
+    assert moe.moe_kernel_plan(q, 4) == moe.PLAN_DECODE_FUSED                      # d = 96
     b = moe.qwen_cfg()
     assert moe.moe_kernel_plan(b, 8) == moe.PLAN_DECODE_RING
-    assert moe.moe_kernel_plan(b, 64) == moe.PLAN_DECODE_WARP       # many units: register stream
-    assert moe.moe_kernel_plan(b.replace(path=moe.PATH_DECODE_REGISTERS), 8) == moe.PLAN_DECODE_WARP
-    assert moe.moe_kernel_plan(b.replace(interleaved_gate_up=1, shared_ff=0), 8) == moe.PLAN_DECODE_WARP
-    assert moe.moe_kernel_plan(b.replace(shared_ff=96), 8) == moe.PLAN_DECODE_WARP
+    assert moe.moe_kernel_plan(b, 64) == moe.PLAN_DECODE_FUSED      # many units: register stream
+    assert moe.moe_kernel_plan(b.replace(path=moe.PATH_DECODE_REGISTERS), 8) == moe.PLAN_DECODE_FUSED
+    assert moe.moe_kernel_plan(b.replace(interleaved_gate_up=1, shared_ff=0), 8) == moe.PLAN_DECODE_FUSED
+    assert moe.moe_kernel_plan(b.replace(shared_ff=96), 8) == moe.PLAN_DECODE_FUSED
+    # four-chunk items and MXFP4 keep two launches; so does the test hook
+    assert moe.moe_kernel_plan(b.replace(path=moe.PATH_DECODE), 4096) == moe.PLAN_DECODE_WARP
+    moe.moe_test_set_decode_fusion(False)
+    try:
+        assert moe.moe_kernel_plan(b, 64) == moe.PLAN_DECODE_WARP
+    finally:
+        moe.moe_test_set_decode_fusion(True)
+    assert moe._lib.moe_test_set_decode_fusion(2) == -1
     assert moe._lib.moe_kernel_plan(ctypes.byref(moe.qwen_cfg()), -1) == -1
 
 

@@ -165,8 +165,11 @@ RING_SPECS = [
 
 
 @pytest.mark.parametrize("spec", RING_SPECS, ids=lambda s: s.name)
-@pytest.mark.parametrize("path", [1, 3], ids=["ring", "registers"])
-def test_bf16_decode_ring(spec, path):
+@pytest.mark.parametrize("path,fused", [(1, True), (3, True), (3, False)],
+                         ids=["ring", "registers-one-launch", "registers-two-launches"])
+def test_bf16_decode_ring(spec, path, fused):
+    """The ring, and the register-stream kernels both as the fused launch (gate_up and
+    down units in one grid, down waiting on per-item counters) and as two launches."""
     moe = moe_lib()
     T, k = spec.tokens, spec.top_k
     assert 4 * T * k <= 16 * spec.n_experts                      # one-chunk items
@@ -175,11 +178,16 @@ def test_bf16_decode_ring(spec, path):
     ref = oracle.forward(g, lay)
     x, router, experts, shared = upload(lay)
     c = cfg_for(spec, path=path)
-    assert moe.moe_kernel_plan(c, T) == (moe.PLAN_DECODE_RING if path == 1 else moe.PLAN_DECODE_WARP)
     ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
     ws = moe.workspace(c, T)
-    y16 = moe.moe_ffn_forward(c, x, router, experts, shared, topk_ids=ids, ws=ws)
-    y32 = moe.moe_ffn_forward(c.replace(y_fp32=1), x, router, experts, shared, ws=ws)
+    moe.moe_test_set_decode_fusion(fused)
+    try:
+        want = moe.PLAN_DECODE_RING if path == 1 else (moe.PLAN_DECODE_FUSED if fused else moe.PLAN_DECODE_WARP)
+        assert moe.moe_kernel_plan(c, T) == want
+        y16 = moe.moe_ffn_forward(c, x, router, experts, shared, topk_ids=ids, ws=ws)
+        y32 = moe.moe_ffn_forward(c.replace(y_fp32=1), x, router, experts, shared, ws=ws)
+    finally:
+        moe.moe_test_set_decode_fusion(True)
     assert moe.moe_device_status(ws)[0] == 0
     ids_g = ids.cpu().numpy()
     diff = np.any(ids_g != ref.ids, axis=1)
@@ -317,6 +325,30 @@ def full_sample(name, spec, ids_g, c):
     tok = {int(sl[-1]) // k for sl in items.values()}
     tok |= set(sample_tokens(T, 24).tolist())
     return np.array(sorted(tok), dtype=np.int32)
+
+
+def test_headline_decode_one_launch_equals_two(full_layers):
+    """The Qwen3.5-mini T=64 decode batch (221 routed experts, the shared expert's 8
+    items): gate_up and down as one launch give the bits of the two-launch form, and
+    repeated calls (each zeroing the launch's counters in its grouping) give them again."""
+    moe = moe_lib()
+    spec, lay, (x, router, experts, shared) = full_layers("qwen35_mini_moe_decode_t64")
+    c = cfg_for(spec).replace(y_fp32=1)
+    T = spec.tokens
+    ws = moe.workspace(c, T)
+    assert moe.moe_kernel_plan(c, T) == moe.PLAN_DECODE_FUSED
+    y1 = moe.moe_ffn_forward(c, x, router, experts, shared, ws=ws)
+    moe.moe_test_set_decode_fusion(False)
+    try:
+        assert moe.moe_kernel_plan(c, T) == moe.PLAN_DECODE_WARP
+        y2 = moe.moe_ffn_forward(c, x, router, experts, shared, ws=ws)
+    finally:
+        moe.moe_test_set_decode_fusion(True)
+    assert moe.moe_device_status(ws)[0] == 0
+    assert torch.equal(y1, y2)
+    for _ in range(3):
+        assert torch.equal(moe.moe_ffn_forward(c, x, router, experts, shared, ws=ws), y1)
+    assert moe.moe_device_status(ws)[0] == 0
 
 
 @pytest.mark.parametrize("name", mi.WORKLOAD_ORDER)
