@@ -226,9 +226,9 @@ int expect_items(const moe_cfg_t* c, int T) {
 // register-stream ones only if the device lacks the shared memory they need): MXFP4
 // weights; bf16 weights in the separate gate / up layout with d, ff, sff multiples
 // of 64 while the down projection has fewer than kRingUnits units of 128 rows (16
-// per SM of a 152-SM GB300).  Past that the register-stream kernels are as fast or
-// faster (Qwen3.5-mini T=64: 0.242 against 0.244 ms a step; T=8: 0.103 against
-// 0.090 ms with the ring).
+// per SM of a 152-SM GB300).  Past that the register-stream kernels, in their
+// one-launch form, are faster (Qwen3.5-mini T=64: 0.234 against 0.244 ms a step with
+// the ring); below it the two are level (T=8: 0.0915 against 0.0909 ms).
 constexpr long long kRingUnits = 16LL * 152;
 bool decode_ring(const moe_cfg_t* c, int T) {
   if (c->path == MOE_PATH_DECODE_REGISTERS) return false;
