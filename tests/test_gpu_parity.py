@@ -636,6 +636,7 @@ def test_mxfp4_prefill_token_magnitudes(shift, det):
 # ----------------------------------------------------------------------------- RMSNorm + residual
 NORM_CASES = [
     (mi.small_spec("qwen", 128, 16, 4, 64, 96, 33, bias=("normal", 0.5)), 1, 1),       # decode, warp
+    (mi.small_spec("qwen", 96, 16, 4, 64, 64, 12, bias=("normal", 0.5)), 1, 1),        # decode, one launch
     (mi.small_spec("qwen", 256, 16, 4, 128, 128, 300, bias=("normal", 0.5)), 2, 1),    # prefill bf16
     (mi.small_spec("qwen", 256, 16, 4, 128, 128, 300, bias=("normal", 0.5)), 2, 0),    # ... accumulated
     (mi.small_spec("gptoss", 96, 12, 4, 96, 0, 7, bias=("normal", 0.1)), 1, 1),        # decode ring
