@@ -341,6 +341,8 @@ int moe_mxfp4_to_bf16(const void* blocks, const void* scales, int64_t rows, int3
  * records events[i] on its stream at the phase boundaries:
  *   [0] start  [1] router logits done  [2] top-k done  [3] grouping done
  *   [4] gate_up + activation done  [5] down done  [6] combine done
+ * (under MOE_PLAN_DECODE_FUSED gate_up and down are one launch: [4] and [5] both
+ * follow it)
  * (the routed entry point records [1] and [2] together after ingesting the
  * routing).  `events` holds n_events >= 7 cudaEvent_t handles created by the
  * caller, or exactly 2: then only the start (events[0]) and the end
@@ -350,13 +352,15 @@ int moe_mxfp4_to_bf16(const void* blocks, const void* scales, int64_t rows, int3
 int moe_set_phase_events(void* const* events, int32_t n_events);
 
 /* Test hook for the give-up path of the bounded device waits (no counterpart on the
- * pages; not for production use).  Every mbarrier wait of the TMA-fed kernels gives
- * up after max_polls polls (default 2^20, about a second), sets MOE_ERR_TIMEOUT in
- * the device status word, and the CTA drains what it has in flight, frees its TMEM
- * and returns.  withhold_first_load = 1 also makes the producer of the CTA that
- * owns the first unit of work of the grouped GEMMs (prefill, bf16 operands and
- * router logits) and of the MXFP4 decode ring skip its first load, so that the
- * wait for it runs out: the call's output is
+ * pages; not for production use).  Every mbarrier wait of the TMA-fed kernels, and
+ * the down units' wait for their item's gate_up units under MOE_PLAN_DECODE_FUSED,
+ * gives up after max_polls polls (default 2^20, about a second), sets
+ * MOE_ERR_TIMEOUT in the device status word, and the CTA drains what it has in
+ * flight, frees its TMEM and returns.  withhold_first_load = 1 also makes the
+ * producer of the CTA that owns the first unit of work of the grouped GEMMs
+ * (prefill, bf16 operands and router logits) and of the MXFP4 decode ring skip its
+ * first load, and the first gate_up unit of MOE_PLAN_DECODE_FUSED withhold its
+ * count, so that the wait for it runs out: the call's output is
  * then undefined and moe_device_status reports MOE_ERR_TIMEOUT.  Applies to the
  * current device, to calls enqueued after it returns; synchronises the device.
  * Restore with moe_test_set_wait_limit(1u << 20, 0).  max_polls > 0. */

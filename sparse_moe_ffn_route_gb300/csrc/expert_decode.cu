@@ -26,6 +26,7 @@
 // down + bias) and section 3 (MXFP4).
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace moe {
 namespace {
@@ -81,13 +82,14 @@ __device__ __forceinline__ void stage_rows(uint8_t* dst, const uint8_t* const* r
 
 // Bounded wait of a CTA until the counter *ctr reaches `need` (thread 0 polls with
 // acquire loads; the block barrier passes the ordering on to every thread).  False,
-// with STATUS_TIMEOUT set, if it gave up.
-constexpr uint32_t kCountPolls = 1u << 22;
+// with STATUS_TIMEOUT set, if it gave up after the poll limit of the bounded waits
+// (tc::c_wait_test, 2^20 polls by default).
 __device__ __forceinline__ bool wait_count(const int32_t* ctr, int need, uint32_t* status) {
   __shared__ int ok_s;
   if (threadIdx.x == 0) {
     int ok = 0;
-    for (uint32_t i = 0; i < kCountPolls; ++i) {
+    const uint32_t polls = tc::c_wait_test.polls;
+    for (uint32_t i = 0; i < polls; ++i) {
       int v;
       asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
       if (v >= need) {
@@ -799,7 +801,9 @@ experts_decode_fused_kernel(ExpertParams p, RouteState rs, const uint16_t* __res
     gateup_unit<MOE_WFMT_BF16, 1, true>(p, rs, x, K, h, ldh, interleaved, a, t - a * gu_tiles);
     __threadfence();            // this thread's h stores, before the item's count
     __syncthreads();
-    if (threadIdx.x == 0) atomicAdd(rs.fuse + 1 + a, 1);
+    // (the give-up test: the first unit withholds its count, so that item 0's down
+    // units run out of polls)
+    if (threadIdx.x == 0 && !tc::withheld_load(0, t == 0)) atomicAdd(rs.fuse + 1 + a, 1);
   } else if (t < ngu + nw * dn_tiles) {
     const int u = t - ngu, a = u / dn_tiles;
     down_unit<MOE_WFMT_BF16, 1, true, true>(p, rs, h, ldh, Y, a, u - a * dn_tiles, rs.fuse + 1 + a, gu_tiles);
@@ -855,6 +859,8 @@ static size_t fused_stage_bytes(int d, int ff, int sff) {
 }
 
 bool decode_fused_fits(int d, int ff, int sff) { return fused_stage_bytes(d, ff, sff) != 0; }
+
+cudaError_t decode_set_wait_test(uint32_t polls, int withhold) { return tc::set_wait_test(polls, withhold); }
 
 cudaError_t launch_experts_decode_fused(const ExpertParams& p, const RouteState& rs, const uint16_t* x, int K,
                                        uint16_t* h, int ldh, float* Y, int max_items, int interleaved,

@@ -242,6 +242,7 @@ cudaError_t launch_down_prefill_fp4(const ExpertParams& p, const RouteState& rs,
 // tc::WaitTest): the poll limit, and whether CTA 0's producer withholds its first load
 // (the grouped GEMMs of expert_prefill.cu and the MXFP4 decode ring read it).
 cudaError_t prefill_set_wait_test(uint32_t polls, int withhold);
+cudaError_t decode_set_wait_test(uint32_t polls, int withhold);
 cudaError_t prefill_fp4_set_wait_test(uint32_t polls, int withhold);
 cudaError_t ring_set_wait_test(uint32_t polls, int withhold);
 cudaError_t fp4_stream_set_wait_test(uint32_t polls, int withhold);

@@ -784,6 +784,7 @@ int moe_test_set_wait_limit(uint32_t max_polls, int32_t withhold_first_load) {
   MOE_CUDA(prefill_fp4_set_wait_test(max_polls, w));
   MOE_CUDA(ring_set_wait_test(max_polls, w));
   MOE_CUDA(fp4_stream_set_wait_test(max_polls, w));
+  MOE_CUDA(decode_set_wait_test(max_polls, w));
   return MOE_OK;
 }
 

@@ -4,11 +4,14 @@ Every mbarrier wait of the TMA-fed kernels polls a bounded number of times; on
 give-up the CTA sets MOE_ERR_TIMEOUT in the device status word, drains the copies
 and MMAs it has in flight, frees its TMEM and returns.  The test hook
 moe_test_set_wait_limit shortens the poll limit and makes the producer of the CTA
-that owns the first unit of work skip its first load, so that the wait for that load runs out: in the prefill grouped GEMM
-(tcgen05, TMEM accumulators) and in the MXFP4 decode ring.  The call must report
-MOE_ERR_TIMEOUT through moe_device_status, and the next, normal call on the same
-context must run and match the oracle: TMEM was freed and nothing was left waiting.
-No GPU fault is involved: the skipped load is simply never issued.
+that owns the first unit of work skip its first load, so that the wait for that load
+runs out: in the prefill grouped GEMM (tcgen05, TMEM accumulators) and in the MXFP4
+decode ring.  In the one-launch bf16 decode the first gate_up unit withholds its
+item's count instead, so that the down units of that item wait in vain.  The call
+must report MOE_ERR_TIMEOUT through moe_device_status, and the next, normal call on
+the same context must run and match the oracle: TMEM was freed, the counters were
+zeroed again and nothing was left waiting.  No GPU fault is involved: the skipped load
+or count is simply never issued.
 """
 import numpy as np
 import pytest
@@ -28,6 +31,8 @@ CASES = [
     (mi.small_spec("qwen", 256, 16, 4, 128, 128, 200, bias=("normal", 0.5)), 2, "PREFILL_BF16"),
     # gpt-oss-style MXFP4 layer on the decode ring
     (mi.small_spec("gptoss", 256, 16, 2, 128, 0, 23, bias=("normal", 0.1)), 1, "DECODE_RING"),
+    # Qwen-style bf16 layer on the one-launch decode (down units wait on item counts)
+    (mi.small_spec("qwen", 96, 16, 4, 64, 64, 12, bias=("normal", 0.5)), 1, "DECODE_FUSED"),
 ]
 
 
