@@ -156,9 +156,13 @@ __device__ __forceinline__ uint4 scaled_f16x8(const uint4& v, const uint4& l, fl
 // the hi half of an (hi, lo) pair whose lo half is lo_off bytes further, and the
 // staged value is hi + lo.  rmax[8] must be zero on entry; esc[i] receives row i's
 // exponent.  Contains the consumer barriers that separate its two phases.
+// pmax (PAIR only, or null): each row's largest |hi| (bf16 bits), already gathered by
+// the producer of h; e then comes from it, and hi and lo load in one round trip with
+// no barrier.
 template <bool PAIR>
 __device__ void stage_tokens(uint8_t* tok, int pitch, const uint8_t* const* rows, int n, int kin,
-                             size_t lo_off, int* esc, uint32_t* rmax, int warp, int lane) {
+                             size_t lo_off, int* esc, uint32_t* rmax, int warp, int lane,
+                             const uint32_t* pmax = nullptr) {
   const int r = warp % kTokens, hf = warp / kTokens;
   const int per = kin >> 3;                       // 16-byte units of bf16 input per row
   const int hu = (per + 1) >> 1;                  // units per half row
@@ -167,6 +171,28 @@ __device__ void stage_tokens(uint8_t* tok, int pitch, const uint8_t* const* rows
   uint4* drow = reinterpret_cast<uint4*>(tok + (size_t)r * pitch);
   const uint8_t* src = r < n ? rows[r] : nullptr;
   uint4 hv[kStageUnits], lv[kStageUnits];
+  if (PAIR && pmax) {
+    const int e = src ? row_exp(pmax[r]) : 0;
+    const float s = exp2i(e);
+    for (int u0 = ub; u0 < ue; u0 += 32 * kStageUnits) {
+#pragma unroll
+      for (int i = 0; i < kStageUnits; ++i) {
+        const int u = u0 + lane + 32 * i;
+        hv[i] = lv[i] = make_uint4(0, 0, 0, 0);
+        if (src && u < ue) {
+          hv[i] = ldg_nc_v4(src + 16 * u);
+          lv[i] = ldg_nc_v4(src + lo_off + 16 * u);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kStageUnits; ++i) {
+        const int u = u0 + lane + 32 * i;
+        if (u < ue) drow[u] = src ? scaled_f16x8(hv[i], lv[i], s) : make_uint4(0, 0, 0, 0);
+      }
+    }
+    if (lane == 0 && hf == 0) esc[r] = e;
+    return;
+  }
   uint32_t m2 = 0;
   if (src) {
     for (int u0 = ub; u0 < ue; u0 += 32 * kStageUnits) {
@@ -400,7 +426,12 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant
     tc::tma_prefetch_desc(&tmW64);
   }
   __syncthreads();
-  pdl_wait();
+  // gate_up: the work list comes from the grouping kernel just before.  down: the work
+  // list was there before the gate_up launch let this one start (each of its CTAs
+  // waited for the grouping); only h depends on gate_up, and the consumers wait for it
+  // before they stage it.  The producer waits too, so that its weight stream does not
+  // take bandwidth from gate_up's last units.
+  if (GATEUP || warp == kCW) pdl_wait();
 
   const int n_items = *a.rs.n_work;
   const long long H = (long long)(n_items > 0 ? n_items : 0) * a.tiles;
@@ -554,6 +585,7 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant
       tc::mbar_arrive(tc::smem_u32(&part_empty));
       ++nu;
       if (*abort) break;
+      uint32_t hm[2] = {0u, 0u};                 // gate_up: the largest |hi| of tokens 2c, 2c + 1
 #pragma unroll
       for (int i = 0; i < kEpiTiles; ++i) {
         const int tile = tile0 + i;
@@ -580,6 +612,7 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant
               uint16_t* hr = a.h + (size_t)(r0 + ti) * 2 * a.ldh + f;
               hr[0] = hi;
               hr[a.ldh] = f32_to_bf16(hv - bf16_to_f32(hi));
+              hm[k] = max(hm[k], (uint32_t)(hi & 0x7FFFu));
             }
           }
         } else {
@@ -592,6 +625,19 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant
               yrow[o + 8] = acc[i][2 + k] * un[k] + b1;
             }
           }
+        }
+      }
+      if (GATEUP && a.rs.hmax) {
+        // the unit's largest |hi| per token, over the 8 lanes (g) of each token pair,
+        // into the row's maximum for the down staging (the same bf16 bits that staging
+        // would find: NaN above inf above every finite value)
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          uint32_t m = hm[k];
+          m = max(m, __shfl_xor_sync(0xffffffffu, m, 4));
+          m = max(m, __shfl_xor_sync(0xffffffffu, m, 8));
+          m = max(m, __shfl_xor_sync(0xffffffffu, m, 16));
+          if (g == 0 && 2 * c + k < n && m) atomicMax(a.rs.hmax + r0 + 2 * c + k, m);
         }
       }
     }
@@ -638,8 +684,11 @@ fp4_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant
         trows[i] = p;
       }
       consumers_sync();
+      // down: h is gate_up's output, the first thing here that needs it
+      if (!GATEUP && ns == 0) pdl_wait();
       // the epilogue warp has read the exponents of every unit of the item two back
-      stage_tokens<!GATEUP>(tok, L.pitch, trows, n, a.kin, (size_t)a.ldh * 2, esc[ns & 1], rmax, warp, lane);
+      stage_tokens<!GATEUP>(tok, L.pitch, trows, n, a.kin, (size_t)a.ldh * 2, esc[ns & 1], rmax, warp, lane,
+                            GATEUP || !a.rs.hmax ? nullptr : a.rs.hmax + r0);
       consumers_sync();
       cur = ai;
       ++ns;

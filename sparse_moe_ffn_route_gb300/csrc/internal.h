@@ -74,11 +74,15 @@ struct RouteState {
   int32_t* n_work;       // [1]
   int32_t* row2slot;     // [S]       permuted row -> slot
   uint32_t* status;      // device status word
-  // [fuse_n] counters of the fused decode launch (a ticket counter, then one count of
-  // finished gate_up units per work item); the one-CTA grouping zeroes them.  Null
-  // where the layout has none.
+  // [fuse_n] per-call counters that the one-CTA grouping zeroes: for the fused decode
+  // launch a ticket counter and one count of finished gate_up units per work item,
+  // then hmax.  Null where the layout has none.
   int32_t* fuse = nullptr;
   int fuse_n = 0;
+  // [S], the last S entries of fuse: per permuted row, the largest |hi| of its h row
+  // (bf16 bits), gathered by the MXFP4 decode ring's gate_up epilogue for its down
+  // staging.  Null unless the one-CTA grouping zeroes it (S <= 2048).
+  uint32_t* hmax = nullptr;
 };
 
 // ---------------------------------------------------------------- host helpers

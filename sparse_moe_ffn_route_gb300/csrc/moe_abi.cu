@@ -100,8 +100,9 @@ bool make_layout(const moe_cfg_t* c, int T, Layout* L) {
                                        : prefill_scales_bytes(sp, c->wfmt));
   }
   L->accumulate = L->prefill && !c->deterministic;
-  // a ticket counter and one count per one-chunk work item (at most E1 + S / 8 items)
-  L->fuse_n = L->prefill ? 0 : 1 + L->E1 + (int)((S + 7) / 8);
+  // a ticket counter and one count per one-chunk work item (at most E1 + S / 8 items),
+  // then the largest |hi| of each permuted row's h
+  L->fuse_n = L->prefill ? 0 : 1 + L->E1 + (int)((S + 7) / 8) + (int)S;
   L->fuse = take(4 * (size_t)L->fuse_n);
   L->yacc = take(L->accumulate ? 4 * Tz * d : 0);   // per-token fp32 sums of the weighted expert outputs
   L->xn = take(c->rms_norm ? 2 * Tz * d : 0);   // RMSNorm(x), the MoE's input
@@ -128,6 +129,7 @@ RouteState route_state(void* ws, const Layout& L) {
   rs.status = at<uint32_t>(ws, L.status);
   rs.fuse = L.fuse_n ? at<int32_t>(ws, L.fuse) : nullptr;
   rs.fuse_n = L.fuse_n;
+  rs.hmax = L.fuse_n && L.S <= kPermuteOneCtaSlots ? reinterpret_cast<uint32_t*>(rs.fuse + L.fuse_n - L.S) : nullptr;
   return rs;
 }
 
@@ -421,6 +423,9 @@ int run_experts(const moe_cfg_t* c, const void* x_layer, int T, const moe_expert
   else if (ring)
     MOE_CUDA(launch_gateup_decode_ring(p, rs, static_cast<const uint16_t*>(x), L.K, h, L.ldh, max_items,
                                        items, s, &done));
+  // the per-row maxima of h exist only when the MXFP4 ring's gate_up wrote them
+  RouteState rs_dn = rs;
+  if (!(ring && fp4 && done)) rs_dn.hmax = nullptr;
   // bf16 one-chunk items on the register-stream kernels: gate_up and down in one
   // launch (the grouping that zeroes its counters is the one-CTA routine here).
   bool fused = false;
@@ -434,7 +439,7 @@ int run_experts(const moe_cfg_t* c, const void* x_layer, int T, const moe_expert
   MOE_CUDA(mark_phase(4, s));
   done = fused;
   if (!fused && ring && fp4)
-    MOE_CUDA(launch_down_decode_fp4(p, rs, h, L.ldh, Y, max_items, s, &done));
+    MOE_CUDA(launch_down_decode_fp4(p, rs_dn, h, L.ldh, Y, max_items, s, &done));
   else if (!fused && ring)
     MOE_CUDA(launch_down_decode_ring(p, rs, h, L.ldh, Y, max_items, items, s, &done));
   if (!done) MOE_CUDA(launch_down_decode(p, c->wfmt, rs, h, L.ldh, Y, max_items, chunks, s));
