@@ -29,6 +29,23 @@ CASES = [
     (mi.small_spec("qwen", 128, 16, 4, 64, 96, 200, bias=("normal", 0.5)), 1, "DECODE_WARP",
      ["router_logits_kernel", "router_select_kernel", "permute_one_cta_kernel", "gateup_decode_kernel",
       "down_decode_kernel", "combine_kernel"]),
+    # prefill (cfg.path 2): the router as a dense GEMM past 256 tokens where it applies,
+    # then the grouped GEMMs; the fixed-order combine (deterministic) or the finish of
+    # the accumulated down projection
+    (mi.small_spec("qwen", 256, 16, 4, 128, 128, 300, bias=("normal", 0.5)), 2, "PREFILL_BF16",
+     ["grouped_gemm_kernel", "router_select_kernel", "permute_one_cta_kernel", "grouped_gemm_kernel",
+      "grouped_gemm_kernel", "combine_kernel"]),
+    (mi.small_spec("gptoss", 128, 4, 2, 128, 0, 600, bias=("normal", 0.1)), 2, "PREFILL_F16",
+     ["router_logits_kernel", "router_select_kernel", "fp4_prep_kernel", "permute_one_cta_kernel",
+      "gather_rows_f16_kernel", "fp4_gemm_kernel", "h_fix_f16_kernel", "fp4_gemm_kernel", "combine_kernel"]),
+]
+ACCUMULATED = [
+    (mi.small_spec("qwen", 256, 16, 4, 128, 128, 300, bias=("normal", 0.5)), "PREFILL_BF16",
+     ["grouped_gemm_kernel", "router_select_kernel", "permute_one_cta_kernel", "grouped_gemm_kernel",
+      "grouped_gemm_kernel", "finish_kernel"]),
+    (mi.small_spec("gptoss", 128, 4, 2, 128, 0, 600, bias=("normal", 0.1)), "PREFILL_F16",
+     ["router_logits_kernel", "router_select_kernel", "fp4_prep_kernel", "permute_one_cta_kernel",
+      "gather_rows_f16_kernel", "fp4_gemm_kernel", "h_fix_f16_kernel", "fp4_gemm_kernel", "finish_kernel"]),
 ]
 
 
@@ -51,15 +68,10 @@ def _short(name):
     return m.group(1) if m else name
 
 
-@pytest.mark.parametrize("spec,path,plan,want", CASES,
-                         ids=["fused-bf16", "ring-bf16", "ring-mxfp4", "warp-four-chunks"])
-def test_kernels_launched_per_plan(spec, path, plan, want, profiler_ready):
-    moe = moe_lib()
-    c = cfg_for(spec, path=path)
-    T = spec.tokens
-    assert moe.moe_kernel_plan(c, T) == getattr(moe, "PLAN_" + plan)
+def _launched(moe, c, spec):
+    """The ordered kernel names of one moe_ffn_forward (after a first, untimed call)."""
     x, router, experts, shared = upload(mi.make_layer(spec))
-    ws = moe.workspace(c, T)
+    ws = moe.workspace(c, spec.tokens)
     y = torch.empty_like(x)
     moe.moe_ffn_forward(c, x, router, experts, shared, y=y, ws=ws)      # first call: attributes set
     torch.cuda.synchronize()
@@ -67,12 +79,33 @@ def test_kernels_launched_per_plan(spec, path, plan, want, profiler_ready):
     with profile(activities=[ProfilerActivity.CUDA]) as prof:
         moe.moe_ffn_forward(c, x, router, experts, shared, y=y, ws=ws)
         torch.cuda.synchronize()
+    assert moe.moe_device_status(ws)[0] == 0
     evs = [e for e in prof.events() if getattr(e, "device_type", None) is not None
            and str(e.device_type).endswith("CUDA")]
     if not evs:
         pytest.skip("the profiler recorded no CUDA kernels here")
     evs.sort(key=lambda e: e.time_range.start)
     got = [_short(e.name) for e in evs]
-    ours = [k for k in got if k.endswith("_kernel") and not k.startswith(("vectorized", "elementwise"))]
+    return [k for k in got if k.endswith("_kernel") and not k.startswith(("vectorized", "elementwise"))], got
+
+
+@pytest.mark.parametrize("spec,path,plan,want", CASES,
+                         ids=["fused-bf16", "ring-bf16", "ring-mxfp4", "warp-four-chunks", "prefill-bf16",
+                              "prefill-f16"])
+def test_kernels_launched_per_plan(spec, path, plan, want, profiler_ready):
+    moe = moe_lib()
+    c = cfg_for(spec, path=path)
+    assert moe.moe_kernel_plan(c, spec.tokens) == getattr(moe, "PLAN_" + plan)
+    ours, got = _launched(moe, c, spec)
     assert ours == want, (plan, got)
-    assert moe.moe_device_status(ws)[0] == 0
+
+
+@pytest.mark.parametrize("spec,plan,want", ACCUMULATED, ids=["prefill-bf16", "prefill-f16"])
+def test_kernels_launched_accumulated_prefill(spec, plan, want, profiler_ready):
+    """The library default (cfg.deterministic = 0): the down projection accumulates and
+    the finish kernel rounds, with no combine."""
+    moe = moe_lib()
+    c = cfg_for(spec, path=2, deterministic=0)
+    assert moe.moe_kernel_plan(c, spec.tokens) == getattr(moe, "PLAN_" + plan)
+    ours, got = _launched(moe, c, spec)
+    assert ours == want, (plan, got)
