@@ -234,6 +234,64 @@ def test_forced_routing_hot_expert_and_duplicates(family):
     check_outputs(y32, y16, ref.y, family)
 
 
+# The one-launch bf16 decode (gate_up and down units in one grid, down waiting on its
+# item's count) at its edges: one token; a shared expert wider than the routed ones
+# (the routed items' extra gate_up units do no work but still count); d over one
+# 128-row tile with no shared expert (the last down tile ragged).
+FUSED_EDGE = [
+    mi.small_spec("qwen", 96, 16, 4, 64, 64, 1, bias=("normal", 0.5)),
+    mi.small_spec("qwen", 96, 16, 4, 64, 160, 9, bias=("normal", 0.5)),
+    mi.small_spec("qwen", 160, 64, 4, 96, 0, 16, bias=("normal", 0.5)),
+]
+
+
+@pytest.mark.parametrize("spec", FUSED_EDGE, ids=lambda s: s.name)
+def test_one_launch_decode_edges(spec):
+    moe = moe_lib()
+    T, k = spec.tokens, spec.top_k
+    lay = mi.make_layer(spec)
+    g = oracle.gating_for(spec)
+    ref = oracle.forward(g, lay)
+    x, router, experts, shared = upload(lay)
+    c = cfg_for(spec)
+    assert moe.moe_kernel_plan(c, T) == moe.PLAN_DECODE_FUSED
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    ws = moe.workspace(c, T)
+    y16 = moe.moe_ffn_forward(c, x, router, experts, shared, topk_ids=ids, ws=ws)
+    y32 = moe.moe_ffn_forward(c.replace(y_fp32=1), x, router, experts, shared, ws=ws)
+    assert moe.moe_device_status(ws)[0] == 0
+    ids_g = ids.cpu().numpy()
+    diff = np.any(ids_g != ref.ids, axis=1)
+    assert not np.any(diff & ~oracle.near_tie_tokens(ref.logits, ref.ids))
+    if np.any(diff):
+        ref = oracle.forward(g, lay, forced_ids=np.where(diff[:, None], ids_g, ref.ids))
+    check_outputs(y32, y16, ref.y, spec.name)
+
+
+def test_one_launch_decode_hot_expert_and_duplicates():
+    """Every token sends two slots to expert 3 (32 rows: four items of one expert) and
+    one each to experts 1 and 5 or 9, through the one-launch decode."""
+    moe = moe_lib()
+    spec = mi.small_spec("qwen", 96, 64, 4, 64, 64, 16)
+    lay = mi.make_layer(spec)
+    g = oracle.gating_for(spec)
+    T = spec.tokens
+    forced = np.tile(np.array([3, 3, 1, 5], np.int32), (T, 1))
+    forced[::3, 3] = 9
+    ref = oracle.forward(g, lay, forced_ids=forced)
+    x, router, experts, shared = upload(lay)
+    c = cfg_for(spec)
+    assert moe.moe_kernel_plan(c, T) == moe.PLAN_DECODE_FUSED
+    sg = torch.from_numpy(ref.sgate.astype(np.float32)).cuda()
+    ids_d = torch.from_numpy(forced).cuda()
+    w_d = torch.from_numpy(ref.w.astype(np.float32)).cuda()
+    ws = moe.workspace(c, T)
+    y16 = moe.moe_ffn_forward_routed(c, x, ids_d, w_d, experts, shared, sgate=sg, ws=ws)
+    y32 = moe.moe_ffn_forward_routed(c.replace(y_fp32=1), x, ids_d, w_d, experts, shared, sgate=sg, ws=ws)
+    assert moe.moe_device_status(ws)[0] == 0
+    check_outputs(y32, y16, ref.y, "one launch, hot expert")
+
+
 def test_bad_ids_are_flagged_not_faulting():
     moe = moe_lib()
     spec = mi.small_spec("qwen", 64, 8, 2, 32, 32, 6)
