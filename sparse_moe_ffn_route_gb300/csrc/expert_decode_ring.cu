@@ -161,7 +161,12 @@ ring_stream_kernel(const __grid_constant__ CUtensorMap m0, const __grid_constant
     }
   }
   __syncthreads();
-  pdl_wait();
+  // gate_up: the work list comes from the grouping kernel just before.  down: it was
+  // there before the gate_up launch let this one start (each of its CTAs waited for
+  // the grouping); only h depends on gate_up, and the consumers wait for it before
+  // they first stage it.  The producer waits too, so that its weight stream does not
+  // take bandwidth from gate_up's last units.
+  if (GATEUP || warp == kCW) pdl_wait();
 
   const int n_items = *a.rs.n_work;
   const long long U = (long long)(n_items > 0 ? n_items : 0) * a.tiles;
@@ -259,6 +264,7 @@ ring_stream_kernel(const __grid_constant__ CUtensorMap m0, const __grid_constant
     const int kin = sh ? a.kin_s : a.kin;
     if (ai != cur) {
       // the item's token rows as bf16 (down: hi rows, then lo rows), rows n..7 zero
+      if (!GATEUP && cur < 0) pdl_wait();        // down: h is gate_up's output
       consumers_sync();                          // every warp is done with the old rows
       if (threadIdx.x < kTokens) {
         const int i = threadIdx.x;
@@ -276,11 +282,29 @@ ring_stream_kernel(const __grid_constant__ CUtensorMap m0, const __grid_constant
         const int r = warp % kTokens, hf = warp / kTokens;
         const int per = kin / 8;                 // 16-byte units per row
         const uint8_t* src = trows[r];
-        for (int pass = 0; pass < (GATEUP ? 1 : 2); ++pass) {
-          uint4* drow = reinterpret_cast<uint4*>(tok + pass * lo_off + (size_t)r * L.pitch);
-          const uint8_t* srow = src ? src + (size_t)pass * a.ldh * 2 : nullptr;
-          for (int i = hf * 32 + lane; i < per; i += 64)
-            drow[i] = srow ? ldg_nc_v4(srow + 16 * i) : make_uint4(0u, 0u, 0u, 0u);
+        // every load of the lane (both halves of an h row) before any store: one round trip
+        constexpr int kU = 4;                    // 16-byte units per lane and half row in flight
+        uint4* drow = reinterpret_cast<uint4*>(tok + (size_t)r * L.pitch);
+        uint4* drow_lo = reinterpret_cast<uint4*>(tok + lo_off + (size_t)r * L.pitch);
+        for (int i0 = hf * 32 + lane; i0 < per; i0 += 64 * kU) {
+          uint4 hv[kU], lv[kU];
+#pragma unroll
+          for (int j = 0; j < kU; ++j) {
+            const int i = i0 + 64 * j;
+            hv[j] = lv[j] = make_uint4(0u, 0u, 0u, 0u);
+            if (src && i < per) {
+              hv[j] = ldg_nc_v4(src + 16 * i);
+              if (!GATEUP) lv[j] = ldg_nc_v4(src + (size_t)a.ldh * 2 + 16 * i);
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < kU; ++j) {
+            const int i = i0 + 64 * j;
+            if (i < per) {
+              drow[i] = hv[j];
+              if (!GATEUP) drow_lo[i] = lv[j];
+            }
+          }
         }
       }
       consumers_sync();
