@@ -791,10 +791,13 @@ experts_decode_fused_kernel(ExpertParams p, RouteState rs, const uint16_t* __res
                             uint16_t* __restrict__ h, int ldh, float* __restrict__ Y, int interleaved,
                             int gu_tiles, int dn_tiles) {
   pdl_wait();
-  __shared__ int ticket_s;
-  if (threadIdx.x == 0) ticket_s = atomicAdd(rs.fuse, 1);
+  __shared__ int ticket_s, nw_s;
+  if (threadIdx.x == 0) {
+    ticket_s = atomicAdd(rs.fuse, 1);
+    nw_s = *rs.n_work;                           // in flight with the ticket's round trip
+  }
   __syncthreads();
-  const int t = ticket_s, nw = *rs.n_work;
+  const int t = ticket_s, nw = nw_s;
   const int ngu = nw * gu_tiles;
   if (t < ngu) {
     const int a = t / gu_tiles;
