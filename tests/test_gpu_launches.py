@@ -20,6 +20,10 @@ pytestmark = pytest.mark.gpu
 CASES = [
     (mi.small_spec("qwen", 96, 16, 4, 64, 64, 12, bias=("normal", 0.5)), 1, "DECODE_FUSED",
      ["router_logits_kernel", "select_permute_kernel", "experts_decode_fused_kernel", "combine_kernel"]),
+    # more than 32 tokens: the select kernel, then the one-CTA grouping
+    (mi.small_spec("qwen", 96, 64, 4, 64, 64, 40, bias=("normal", 0.5)), 1, "DECODE_FUSED",
+     ["router_logits_kernel", "router_select_kernel", "permute_one_cta_kernel", "experts_decode_fused_kernel",
+      "combine_kernel"]),
     (mi.small_spec("qwen", 128, 32, 4, 64, 64, 8, bias=("normal", 0.5)), 1, "DECODE_RING",
      ["router_logits_kernel", "select_permute_kernel", "ring_stream_kernel", "ring_stream_kernel",
       "combine_kernel"]),
@@ -90,8 +94,8 @@ def _launched(moe, c, spec):
 
 
 @pytest.mark.parametrize("spec,path,plan,want", CASES,
-                         ids=["fused-bf16", "ring-bf16", "ring-mxfp4", "warp-four-chunks", "prefill-bf16",
-                              "prefill-f16"])
+                         ids=["fused-bf16", "fused-bf16-40-tokens", "ring-bf16", "ring-mxfp4", "warp-four-chunks",
+                              "prefill-bf16", "prefill-f16"])
 def test_kernels_launched_per_plan(spec, path, plan, want, profiler_ready):
     moe = moe_lib()
     c = cfg_for(spec, path=path)
